@@ -1,0 +1,224 @@
+"""CPU float64 oracle for exact attention -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The product path (the CUDA library and
+its Python binding) never imports it and shares no code with it.
+
+The arithmetic lives in ``attn_oracle.c`` (plain C, OpenMP over rows, double
+precision); this module only builds that file with gcc and marshals numpy
+arrays.  Every function is pinned by ``tests/test_oracle.py`` against values
+that do not come from the oracle itself.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "attn_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile ``attn_oracle.c`` into ``liboracle.so`` (gcc, -O2, OpenMP)."""
+    if (not force and os.path.exists(_LIB)
+            and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
+        return _LIB
+    tmp = _LIB + ".tmp.%d" % os.getpid()
+    # -ffp-contract=off: no fused multiply-add, so every product and sum is
+    # rounded exactly as written.
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp",
+           "-ffp-contract=off", "-o", tmp, _SRC, "-lm"]
+    subprocess.check_call(cmd)
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    if _lib is not None:
+        return _lib
+    build()
+    lib = ctypes.CDLL(_LIB)
+    P = ctypes.c_void_p
+    L = ctypes.c_long
+    D = ctypes.c_double
+    I = ctypes.c_int
+    lib.oracle_num_threads.restype = I
+    lib.oracle_attn_fwd.argtypes = [P, P, P, L, L, L, L, L, L, I, D, P, P]
+    lib.oracle_attn_fwd.restype = I
+    lib.oracle_attn_rows.argtypes = [P, P, P, L, L, L, L, L, L, I, D, L, P, P, P]
+    lib.oracle_attn_rows.restype = I
+    lib.oracle_attn_fwd_tiled.argtypes = [P, P, P, L, L, L, L, L, L, I, D, L, L, P, P, P]
+    lib.oracle_attn_fwd_tiled.restype = I
+    lib.oracle_online_trace.argtypes = [P, L, L, P, P, P]
+    lib.oracle_online_trace.restype = None
+    lib.oracle_segment_state.argtypes = [P, P, P, L, L, L, L, L, L, I, D, L, L, L, L, L, P, P, P]
+    lib.oracle_segment_state.restype = None
+    lib.oracle_state_merge.argtypes = [D, D, P, D, D, P, L, P, P, P]
+    lib.oracle_state_merge.restype = None
+    lib.oracle_merge_lse.argtypes = [L, L, L, P, P, P, P]
+    lib.oracle_merge_lse.restype = None
+    lib.oracle_decode_split.argtypes = [P, P, P, L, L, L, L, L, D, L, P, P]
+    lib.oracle_decode_split.restype = I
+    _lib = lib
+    return lib
+
+
+def _f32(a) -> np.ndarray:
+    """Float32 C-contiguous view of a numpy array or CPU torch tensor.
+
+    bf16 and fp32 values are exact in float32, so nothing is rounded here.
+    """
+    if hasattr(a, "detach"):  # torch tensor
+        a = a.detach().to("cpu")
+        import torch
+        a = a.to(torch.float32).numpy()
+    a = np.ascontiguousarray(a, dtype=np.float32)
+    return a
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def num_threads() -> int:
+    """Threads the oracle's OpenMP loops use."""
+    return int(_load().oracle_num_threads())
+
+
+def _shapes(q, k, Nq_axis=1):
+    B, Nq, Hq, d = q.shape
+    Bk, Nk, Hkv, dk = k.shape
+    assert B == Bk and d == dk, "q/k shapes disagree"
+    return B, Hq, Hkv, Nq, Nk, d
+
+
+def attn_fwd(q, k, v, causal: bool, scale: float):
+    """Algorithm 0, every row.  Returns (o [B,Nq,Hq,d], lse [B,Hq,Nq]) float64."""
+    lib = _load()
+    q, k, v = _f32(q), _f32(k), _f32(v)
+    B, Hq, Hkv, Nq, Nk, d = _shapes(q, k)
+    o = np.zeros((B, Nq, Hq, d), np.float64)
+    lse = np.zeros((B, Hq, Nq), np.float64)
+    rc = lib.oracle_attn_fwd(_ptr(q), _ptr(k), _ptr(v), B, Hq, Hkv, Nq, Nk, d,
+                             int(causal), float(scale), _ptr(o), _ptr(lse))
+    if rc != 0:
+        raise ValueError("oracle_attn_fwd rejected the shapes (rc=%d)" % rc)
+    return o, lse
+
+
+def attn_rows(q, k, v, causal: bool, scale: float, rows):
+    """Algorithm 0 for selected rows.
+
+    ``rows`` is an int array [n, 3] of (b, hq, i).  Returns (o [n, d],
+    lse [n]) float64.
+    """
+    lib = _load()
+    q, k, v = _f32(q), _f32(k), _f32(v)
+    B, Hq, Hkv, Nq, Nk, d = _shapes(q, k)
+    sel = np.ascontiguousarray(np.asarray(rows, dtype=np.int64).reshape(-1, 3))
+    n = sel.shape[0]
+    o = np.zeros((n, d), np.float64)
+    lse = np.zeros((n,), np.float64)
+    rc = lib.oracle_attn_rows(_ptr(q), _ptr(k), _ptr(v), B, Hq, Hkv, Nq, Nk, d,
+                              int(causal), float(scale), n,
+                              sel.ctypes.data_as(ctypes.c_void_p), _ptr(o), _ptr(lse))
+    if rc != 0:
+        raise ValueError("oracle_attn_rows rejected its arguments (rc=%d)" % rc)
+    return o, lse
+
+
+def attn_fwd_tiled(q, k, v, causal: bool, scale: float, Br: int, Bc: int):
+    """Tiled online-softmax forward.  Returns (o, lse, blocks_computed)."""
+    lib = _load()
+    q, k, v = _f32(q), _f32(k), _f32(v)
+    B, Hq, Hkv, Nq, Nk, d = _shapes(q, k)
+    o = np.zeros((B, Nq, Hq, d), np.float64)
+    lse = np.zeros((B, Hq, Nq), np.float64)
+    nb = ctypes.c_long(0)
+    rc = lib.oracle_attn_fwd_tiled(_ptr(q), _ptr(k), _ptr(v), B, Hq, Hkv, Nq, Nk, d,
+                                   int(causal), float(scale), int(Br), int(Bc),
+                                   _ptr(o), _ptr(lse), ctypes.byref(nb))
+    if rc != 0:
+        raise ValueError("oracle_attn_fwd_tiled rejected its arguments (rc=%d)" % rc)
+    return o, lse, int(nb.value)
+
+
+def online_trace(x, block: int):
+    """Online softmax over a score row in blocks: (m, l, alpha) after each block."""
+    lib = _load()
+    x = np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+    nb = (x.size + block - 1) // block
+    m = np.zeros(nb)
+    l = np.zeros(nb)
+    a = np.zeros(nb)
+    lib.oracle_online_trace(_ptr(x), x.size, int(block), _ptr(m), _ptr(l), _ptr(a))
+    return m, l, a
+
+
+def segment_state(q, k, v, causal: bool, scale: float, b: int, hq: int, i: int,
+                  j0: int, j1: int):
+    """Unnormalised partial state (m, l, acc) of keys [j0, j1) for row (b, hq, i)."""
+    lib = _load()
+    q, k, v = _f32(q), _f32(k), _f32(v)
+    B, Hq, Hkv, Nq, Nk, d = _shapes(q, k)
+    m = ctypes.c_double(0)
+    l = ctypes.c_double(0)
+    acc = np.zeros(d, np.float64)
+    lib.oracle_segment_state(_ptr(q), _ptr(k), _ptr(v), B, Hq, Hkv, Nq, Nk, d,
+                             int(causal), float(scale), b, hq, i, j0, j1,
+                             ctypes.byref(m), ctypes.byref(l), _ptr(acc))
+    return m.value, l.value, acc
+
+
+def state_merge(a, b):
+    """Merge two partial states (m, l, acc) of one row."""
+    lib = _load()
+    m_a, l_a, acc_a = a
+    m_b, l_b, acc_b = b
+    acc_a = np.ascontiguousarray(acc_a, np.float64)
+    acc_b = np.ascontiguousarray(acc_b, np.float64)
+    d = acc_a.size
+    m = ctypes.c_double(0)
+    l = ctypes.c_double(0)
+    acc = np.zeros(d, np.float64)
+    lib.oracle_state_merge(float(m_a), float(l_a), _ptr(acc_a), float(m_b), float(l_b),
+                           _ptr(acc_b), d, ctypes.byref(m), ctypes.byref(l), _ptr(acc))
+    return m.value, l.value, acc
+
+
+def merge_lse(o_parts, lse_parts):
+    """LSE-form merge.  o_parts [P, rows, d], lse_parts [P, rows] -> (o, lse)."""
+    lib = _load()
+    o_parts = np.ascontiguousarray(o_parts, np.float64)
+    lse_parts = np.ascontiguousarray(lse_parts, np.float64)
+    P, rows, d = o_parts.shape
+    assert lse_parts.shape == (P, rows)
+    o = np.zeros((rows, d), np.float64)
+    lse = np.zeros((rows,), np.float64)
+    lib.oracle_merge_lse(P, rows, d, _ptr(o_parts), _ptr(lse_parts), _ptr(o), _ptr(lse))
+    return o, lse
+
+
+def decode_split(q, k, v, scale: float, nsplit: int):
+    """Per-segment partials of flash-decoding (Nq = 1).
+
+    Returns (o_parts [nsplit, B*Hq, d], lse_parts [nsplit, B*Hq]) float64.
+    """
+    lib = _load()
+    q, k, v = _f32(q), _f32(k), _f32(v)
+    B, Hq, Hkv, Nq, Nk, d = _shapes(q, k)
+    assert Nq == 1, "decode takes one query per sequence"
+    rows = B * Hq
+    o_parts = np.zeros((nsplit, rows, d), np.float64)
+    lse_parts = np.zeros((nsplit, rows), np.float64)
+    rc = lib.oracle_decode_split(_ptr(q), _ptr(k), _ptr(v), B, Hq, Hkv, Nk, d,
+                                 float(scale), int(nsplit), _ptr(o_parts), _ptr(lse_parts))
+    if rc != 0:
+        raise ValueError("oracle_decode_split rejected its arguments (rc=%d)" % rc)
+    return o_parts, lse_parts

@@ -1,0 +1,337 @@
+"""Pins for the CPU oracle (no GPU).
+
+Each test checks the oracle against something other than itself: numbers
+printed in the lecture notes (tests/golden), closed forms, invariants, and
+brute force on tiny inputs written out with Python loops.  A plausible slip in
+the oracle (a dropped term, a wrong sign or index, a transposed operand, a
+wrong causal offset or GQA mapping) fails at least one of them.
+"""
+import json
+import math
+import os
+import random
+
+import numpy as np
+import pytest
+import torch
+
+from exact_attention_62_gb300.inputs import make_qkv
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+# ---------------------------------------------------------------- worked numbers
+
+def test_online_softmax_worked_example(oracle_mod):
+    """Lecture 11, exercise 1: blocks [1,3] then [2,5]."""
+    g = _golden("online_softmax_ex1.json")
+    m, l, a = oracle_mod.online_trace(g["scores"], g["block"])
+    dec = g["decimals"]
+    for b, want in enumerate(g["after_block"]):
+        assert round(m[b], dec) == want["m"]
+        assert round(l[b], dec) == want["l"]
+        if "alpha" in want:
+            assert round(a[b], dec) == want["alpha"]
+    assert round(l[-1], dec) == g["one_shot_l_at_m5"]
+
+
+def test_state_merge_worked_example(oracle_mod):
+    """The two blocks of exercise 1 merged as partial states give the one-shot l."""
+    g = _golden("online_softmax_ex1.json")
+    x = g["scores"]
+
+    def state(seg):
+        m = max(seg)
+        return m, sum(math.exp(s - m) for s in seg), np.zeros(1)
+
+    m, l, _ = oracle_mod.state_merge(state(x[:2]), state(x[2:]))
+    assert m == 5.0
+    assert round(l, g["decimals"]) == g["one_shot_l_at_m5"]
+
+
+def test_causal_block_fraction(oracle_mod):
+    """Lecture 11 section 5.3: computed-block fraction at N=4096, blocks 64/128/256."""
+    g = _golden("causal_block_fraction.json")
+    N = g["N"]
+    q, k, v = make_qkv(1, 1, 1, N, N, 2, seed=3, dtype=torch.float32)
+    for blk, want in g["fractions"].items():
+        blk = int(blk)
+        _, _, nb = oracle_mod.attn_fwd_tiled(q, k, v, True, 1.0, blk, blk)
+        T = N // blk
+        assert nb == T * (T + 1) // 2
+        assert round(nb / (T * T), g["decimals"]) == want
+
+
+# ---------------------------------------------------------------- closed forms
+
+@pytest.mark.parametrize("causal,Nq,Nk,Hq,Hkv", [
+    (False, 5, 9, 4, 2), (True, 9, 9, 2, 2), (True, 3, 11, 6, 3), (True, 7, 4, 2, 1)])
+def test_zero_query_gives_mean_of_values(oracle_mod, causal, Nq, Nk, Hq, Hkv):
+    """Q = 0 makes every allowed score equal: O = mean of the allowed V rows,
+    LSE = ln(#allowed keys)."""
+    B, d = 2, 8
+    _, k, v = make_qkv(B, Hq, Hkv, Nq, Nk, d, seed=11, dtype=torch.float32)
+    q = torch.zeros(B, Nq, Hq, d)
+    o, lse = oracle_mod.attn_fwd(q, k, v, causal, 0.37)
+    G = Hq // Hkv
+    vv = v.double().numpy()
+    for b in range(B):
+        for h in range(Hq):
+            for i in range(Nq):
+                last = min(Nk - 1, i + Nk - Nq) if causal else Nk - 1
+                if last < 0:
+                    assert np.all(o[b, i, h] == 0) and lse[b, h, i] == -np.inf
+                    continue
+                want = vv[b, :last + 1, h // G].mean(axis=0)
+                np.testing.assert_allclose(o[b, i, h], want, atol=1e-13, rtol=0)
+                assert abs(lse[b, h, i] - math.log(last + 1)) < 1e-13
+
+
+def test_dominant_score_selects_one_value_row(oracle_mod):
+    """A score 900 above all others puts all weight on that key: O = v_j*,
+    LSE = s_j* (exp(-900) underflows to zero in double)."""
+    B, Hq, Hkv, Nq, Nk, d = 1, 2, 1, 6, 6, 8
+    k = torch.zeros(B, Nk, Hkv, d)
+    q = torch.zeros(B, Nq, Hq, d)
+    perm = [3, 0, 5, 1, 4, 2]
+    for j in range(Nk):
+        k[0, j, 0, j] = 30.0
+    for i in range(Nq):
+        for h in range(Hq):
+            q[0, i, h, perm[(i + h) % Nk]] = 30.0
+    _, _, v = make_qkv(B, Hq, Hkv, Nq, Nk, d, seed=5, dtype=torch.float32)
+    o, lse = oracle_mod.attn_fwd(q, k, v, False, 1.0)
+    for i in range(Nq):
+        for h in range(Hq):
+            j = perm[(i + h) % Nk]
+            np.testing.assert_array_equal(o[0, i, h], v[0, j, 0].double().numpy())
+            assert lse[0, h, i] == 900.0
+
+
+def test_probabilities_sum_to_one_and_convex_hull(oracle_mod):
+    """V = 1 gives O = 1 (rows of P sum to 1); for random V every output
+    coordinate lies between the min and max of the allowed V rows."""
+    B, Hq, Hkv, Nq, Nk, d = 2, 4, 2, 13, 17, 16
+    q, k, v = make_qkv(B, Hq, Hkv, Nq, Nk, d, seed=21, dtype=torch.float32)
+    for causal in (False, True):
+        o1, _ = oracle_mod.attn_fwd(q, k, torch.ones_like(v), causal, 0.25)
+        np.testing.assert_allclose(o1, 1.0, atol=1e-14, rtol=0)
+        o, _ = oracle_mod.attn_fwd(q, k, v, causal, 0.25)
+        vv = v.double().numpy()
+        for b in range(B):
+            for h in range(Hq):
+                for i in range(Nq):
+                    last = min(Nk - 1, i + Nk - Nq) if causal else Nk - 1
+                    rows = vv[b, :last + 1, h // (Hq // Hkv)]
+                    assert np.all(o[b, i, h] >= rows.min(axis=0) - 1e-14)
+                    assert np.all(o[b, i, h] <= rows.max(axis=0) + 1e-14)
+
+
+def test_shift_invariance(oracle_mod):
+    """Adding w to every key adds scale*(q_i . w) to every score of row i:
+    O is unchanged and LSE shifts by exactly that constant."""
+    B, Hq, Hkv, Nq, Nk, d = 1, 2, 2, 7, 9, 8
+    rng = np.random.default_rng(0)
+    # dyadic values so that k + w is exact in float32
+    q = torch.tensor(rng.integers(-8, 9, (B, Nq, Hq, d)) / 8.0, dtype=torch.float32)
+    k = torch.tensor(rng.integers(-8, 9, (B, Nk, Hkv, d)) / 8.0, dtype=torch.float32)
+    v = torch.tensor(rng.standard_normal((B, Nk, Hkv, d)), dtype=torch.float32)
+    w = torch.tensor(rng.integers(-4, 5, (Hkv, d)) / 4.0, dtype=torch.float32)
+    scale = 0.5
+    for causal in (False, True):
+        o0, l0 = oracle_mod.attn_fwd(q, k, v, causal, scale)
+        o1, l1 = oracle_mod.attn_fwd(q, k + w, v, causal, scale)
+        np.testing.assert_allclose(o1, o0, atol=1e-12, rtol=0)
+        G = Hq // Hkv
+        for h in range(Hq):
+            shift = scale * (q[0, :, h].double() @ w[h // G].double()).numpy()
+            np.testing.assert_allclose(l1[0, h], l0[0, h] + shift, atol=1e-11, rtol=0)
+
+
+# ---------------------------------------------------------------- brute force
+
+def _brute(q, k, v, causal, scale):
+    """Textbook attention with explicit Python loops (no max subtraction:
+    inputs are tiny and bounded, so exp cannot overflow)."""
+    B, Nq, Hq, d = q.shape
+    _, Nk, Hkv, _ = k.shape
+    G = Hq // Hkv
+    o = np.zeros((B, Nq, Hq, d))
+    lse = np.zeros((B, Hq, Nq))
+    for b in range(B):
+        for h in range(Hq):
+            g = h // G
+            for i in range(Nq):
+                allowed = [j for j in range(Nk) if (not causal or j <= i + Nk - Nq)]
+                if not allowed:
+                    lse[b, h, i] = -math.inf
+                    continue
+                e = {}
+                for j in allowed:
+                    s = 0.0
+                    for t in range(d):
+                        s += float(q[b, i, h, t]) * float(k[b, j, g, t])
+                    e[j] = math.exp(scale * s)
+                z = sum(e.values())
+                for t in range(d):
+                    o[b, i, h, t] = sum(e[j] / z * float(v[b, j, g, t]) for j in allowed)
+                lse[b, h, i] = math.log(z)
+    return o, lse
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Nq,Nk,d,causal", [
+    (1, 1, 1, 1, 1, 1, False), (1, 1, 1, 4, 4, 4, True), (2, 2, 1, 3, 4, 2, True),
+    (1, 4, 2, 4, 2, 3, True), (2, 3, 3, 2, 4, 4, False), (1, 2, 2, 4, 3, 1, False)])
+def test_brute_force_tiny(oracle_mod, B, Hq, Hkv, Nq, Nk, d, causal):
+    q, k, v = make_qkv(B, Hq, Hkv, Nq, Nk, d, seed=B * 100 + Nq * 10 + d,
+                       dtype=torch.float32)
+    scale = 0.7
+    o, lse = oracle_mod.attn_fwd(q, k, v, causal, scale)
+    ob, lb = _brute(q.numpy(), k.numpy(), v.numpy(), causal, scale)
+    np.testing.assert_allclose(o, ob, atol=1e-13, rtol=0)
+    np.testing.assert_allclose(lse, lb, atol=1e-13, rtol=0)
+
+
+# ---------------------------------------------------------------- agreements
+
+@pytest.mark.parametrize("B,Hq,Hkv,Nq,Nk,d,causal,Br,Bc", [
+    (2, 4, 2, 37, 37, 16, True, 8, 8),
+    (1, 3, 3, 50, 70, 8, False, 16, 12),
+    (1, 2, 1, 1, 1000, 8, True, 64, 128),     # decode case of the lecture demo
+    (1, 2, 2, 20, 9, 4, True, 4, 4),          # Nq > Nk: leading rows are empty
+    (2, 6, 2, 33, 65, 32, True, 16, 32)])
+def test_tiled_online_matches_plain(oracle_mod, B, Hq, Hkv, Nq, Nk, d, causal, Br, Bc):
+    """Lecture 11 section 4.1: the tiled online forward equals algorithm 0."""
+    q, k, v = make_qkv(B, Hq, Hkv, Nq, Nk, d, seed=Nq + Nk, dtype=torch.float32)
+    o, lse = oracle_mod.attn_fwd(q, k, v, causal, 1.0 / math.sqrt(d))
+    ot, lt, _ = oracle_mod.attn_fwd_tiled(q, k, v, causal, 1.0 / math.sqrt(d), Br, Bc)
+    np.testing.assert_allclose(ot, o, atol=1e-12, rtol=0)
+    fin = np.isfinite(lse)
+    assert np.array_equal(fin, np.isfinite(lt))
+    np.testing.assert_allclose(lt[fin], lse[fin], atol=1e-12, rtol=1e-12)
+
+
+def test_rows_match_full(oracle_mod):
+    q, k, v = make_qkv(2, 4, 1, 30, 40, 16, seed=9)
+    o, lse = oracle_mod.attn_fwd(q, k, v, True, 0.25)
+    rows = [(0, 0, 0), (1, 3, 29), (0, 2, 17), (1, 1, 5)]
+    os_, ls = oracle_mod.attn_rows(q, k, v, True, 0.25, rows)
+    for n, (b, h, i) in enumerate(rows):
+        np.testing.assert_array_equal(os_[n], o[b, i, h])
+        assert ls[n] == lse[b, h, i]
+
+
+def test_segment_merge_associative(oracle_mod):
+    """Lecture 11 section 3.2: a row of 3000 keys cut into 12 random segments;
+    sequential, tree and shuffled merges all equal the one-shot state."""
+    Nk, d = 3000, 16
+    q, k, v = make_qkv(1, 1, 1, 1, Nk, d, seed=12, dtype=torch.float32)
+    rnd = random.Random(4)
+    cuts = sorted(rnd.sample(range(1, Nk), 11))
+    bounds = list(zip([0] + cuts, cuts + [Nk]))
+    segs = [oracle_mod.segment_state(q, k, v, False, 0.3, 0, 0, 0, a, b) for a, b in bounds]
+    full = oracle_mod.segment_state(q, k, v, False, 0.3, 0, 0, 0, 0, Nk)
+
+    def seq(states):
+        acc = states[0]
+        for s in states[1:]:
+            acc = oracle_mod.state_merge(acc, s)
+        return acc
+
+    def tree(states):
+        while len(states) > 1:
+            nxt = [oracle_mod.state_merge(states[i], states[i + 1])
+                   for i in range(0, len(states) - 1, 2)]
+            if len(states) % 2:
+                nxt.append(states[-1])
+            states = nxt
+        return states[0]
+
+    shuffled = segs[:]
+    rnd.shuffle(shuffled)
+    o_full, lse_full = oracle_mod.attn_rows(q, k, v, False, 0.3, [(0, 0, 0)])
+    for m, l, acc in (seq(segs), tree(segs), seq(shuffled)):
+        assert abs(m - full[0]) == 0.0
+        assert abs(l - full[1]) <= 1e-12 * full[1]
+        np.testing.assert_allclose(acc, full[2], atol=1e-12 * full[1], rtol=0)
+        np.testing.assert_allclose(acc / l, o_full[0], atol=1e-12, rtol=0)
+        assert abs(m + math.log(l) - lse_full[0]) <= 1e-12
+
+
+@pytest.mark.parametrize("nsplit", [1, 7, 64, 1000])
+def test_decode_splits_merge_to_direct(oracle_mod, nsplit):
+    """Lecture 11 section 6.2: 1, 7, 64 and 1000 segments merged by log-sum-exp
+    equal the direct result."""
+    B, Hq, Hkv, Nk, d = 2, 8, 2, 1000, 32
+    q, k, v = make_qkv(B, Hq, Hkv, 1, Nk, d, seed=nsplit)
+    scale = 1.0 / math.sqrt(d)
+    o, lse = oracle_mod.attn_fwd(q, k, v, False, scale)
+    op, lp = oracle_mod.decode_split(q, k, v, scale, nsplit)
+    om, lm = oracle_mod.merge_lse(op, lp)
+    np.testing.assert_allclose(om, o.reshape(B * Hq, d), atol=1e-12, rtol=0)
+    np.testing.assert_allclose(lm, lse.reshape(B * Hq), atol=1e-12, rtol=0)
+
+
+def test_merge_lse_closed_forms(oracle_mod):
+    """Two parts with equal lse a give lse = a + ln 2 and the mean output;
+    empty parts (lse = -inf) are ignored; all-empty rows give 0 and -inf."""
+    o_parts = np.array([[[1.0, 2.0], [5.0, 5.0], [0.0, 0.0]],
+                        [[3.0, -2.0], [0.0, 0.0], [0.0, 0.0]]])
+    lse_parts = np.array([[0.5, 1.25, -np.inf], [0.5, -np.inf, -np.inf]])
+    o, lse = oracle_mod.merge_lse(o_parts, lse_parts)
+    np.testing.assert_allclose(o[0], [2.0, 0.0], atol=1e-15)
+    assert abs(lse[0] - (0.5 + math.log(2.0))) < 1e-15
+    np.testing.assert_array_equal(o[1], [5.0, 5.0])
+    assert lse[1] == 1.25
+    np.testing.assert_array_equal(o[2], [0.0, 0.0])
+    assert lse[2] == -np.inf
+
+
+# ---------------------------------------------------------------- readings
+
+def test_causal_alignment_readings(oracle_mod):
+    """Bottom-right alignment: one query over 1000 keys sees every key (the
+    decode case of the lecture's demo); with Nq == Nk, row 0 sees only key 0."""
+    q, k, v = make_qkv(1, 2, 2, 1, 1000, 16, seed=2)
+    oc, lc = oracle_mod.attn_fwd(q, k, v, True, 0.25)
+    on, ln = oracle_mod.attn_fwd(q, k, v, False, 0.25)
+    np.testing.assert_array_equal(oc, on)
+    np.testing.assert_array_equal(lc, ln)
+    q, k, v = make_qkv(1, 2, 2, 8, 8, 16, seed=2, dtype=torch.float32)
+    o, lse = oracle_mod.attn_fwd(q, k, v, True, 0.25)
+    for h in range(2):
+        np.testing.assert_array_equal(o[0, 0, h], v[0, 0, h].double().numpy())
+        s00 = 0.25 * float(q[0, 0, h].double() @ k[0, 0, h].double())
+        assert abs(lse[0, h, 0] - s00) < 1e-14
+
+
+def test_empty_rows(oracle_mod):
+    """Causal with Nq > Nk: rows i < Nq - Nk have no allowed key: O = 0, LSE = -inf."""
+    q, k, v = make_qkv(1, 2, 1, 10, 4, 8, seed=3)
+    o, lse = oracle_mod.attn_fwd(q, k, v, True, 0.5)
+    assert np.all(o[0, :6] == 0.0)
+    assert np.all(lse[:, :, :6] == -np.inf)
+    assert np.all(np.isfinite(lse[:, :, 6:]))
+
+
+def test_gqa_head_mapping(oracle_mod):
+    """Query head h reads key/value head h // (Hq/Hkv): equal to plain
+    multi-head attention with each kv head repeated G times."""
+    B, Hq, Hkv, N, d = 1, 8, 2, 12, 8
+    q, k, v = make_qkv(B, Hq, Hkv, N, N, d, seed=6)
+    o, lse = oracle_mod.attn_fwd(q, k, v, True, 0.3)
+    kr = k.repeat_interleave(Hq // Hkv, dim=2)
+    vr = v.repeat_interleave(Hq // Hkv, dim=2)
+    o2, l2 = oracle_mod.attn_fwd(q, kr, vr, True, 0.3)
+    np.testing.assert_array_equal(o, o2)
+    np.testing.assert_array_equal(lse, l2)
+    # and a different mapping (h % Hkv) would differ
+    kw = k[:, :, [h % Hkv for h in range(Hq)]]
+    vw = v[:, :, [h % Hkv for h in range(Hq)]]
+    o3, _ = oracle_mod.attn_fwd(q, kw, vw, True, 0.3)
+    assert np.abs(o3 - o).max() > 1e-3
