@@ -1,0 +1,243 @@
+"""exact_attention_62_gb300 -- fused exact attention and flash-decoding for GB300.
+
+Thin Python binding over the C ABI of ``libattn.so`` (declared in
+``include/attn.h``).  The functions below carry the same names as the C entry
+points and only marshal arguments: they take CUDA torch tensors, pass their
+device pointers and the current CUDA stream, and raise ``AttnError`` on a
+non-OK status.  Every step of the computation runs in the library's CUDA
+kernels; there is no CPU or PyTorch fallback, and a missing library is an
+error.
+
+PyTorch is used only for device memory and streams.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+__all__ = [
+    "AttnError", "ATTN_BF16", "ATTN_F32", "lib", "ensure_built", "library_path",
+    "attn_fwd", "attn_decode_num_splits", "attn_decode_workspace_bytes",
+    "attn_decode_splitkv", "attn_merge_lse", "attn_status_string",
+    "attn_check_device_status", "attn_read_tile_counter", "attn_version",
+    "EXPORTED_SYMBOLS",
+]
+
+ATTN_OK, ATTN_ERR_INVALID, ATTN_ERR_UNSUPPORTED, ATTN_ERR_CUDA, ATTN_ERR_TIMEOUT = range(5)
+ATTN_BF16, ATTN_F32 = 0, 1
+
+# Every symbol include/attn.h declares.
+EXPORTED_SYMBOLS = (
+    "attn_fwd", "attn_decode_num_splits", "attn_decode_workspace_bytes",
+    "attn_decode_splitkv", "attn_merge_lse", "attn_status_string",
+    "attn_check_device_status", "attn_read_tile_counter", "attn_version",
+)
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_PKG, "libattn.so")
+_lib = None
+
+
+class AttnError(RuntimeError):
+    """A libattn entry point returned a non-OK status."""
+
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__("%s failed: %s (status %d)" % (fn, _status_text(status), status))
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def ensure_built() -> str:
+    """Builds libattn.so if it is missing; returns its path."""
+    if not os.path.exists(_LIB_PATH):
+        from . import build as _build
+        _build.build()
+    return _LIB_PATH
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libattn.so.  Raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_LIB_PATH):
+        raise RuntimeError(
+            "libattn.so is not built (%s); run `python -m exact_attention_62_gb300.build` "
+            "or __graft_entry__.build()" % _LIB_PATH)
+    L = ctypes.CDLL(_LIB_PATH)
+    P, I, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    LL, SZ = ctypes.c_longlong, ctypes.c_size_t
+    L.attn_fwd.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, F, I, P]
+    L.attn_fwd.restype = I
+    L.attn_decode_num_splits.argtypes = [I, I, I, I, I]
+    L.attn_decode_num_splits.restype = I
+    L.attn_decode_workspace_bytes.argtypes = [I, I, I, I, I, I]
+    L.attn_decode_workspace_bytes.restype = SZ
+    L.attn_decode_splitkv.argtypes = [P, P, P, P, P, I, I, I, I, I, F, I, P, SZ, I, P]
+    L.attn_decode_splitkv.restype = I
+    L.attn_merge_lse.argtypes = [P, P, I, LL, I, P, P, I, P]
+    L.attn_merge_lse.restype = I
+    L.attn_status_string.argtypes = [I]
+    L.attn_status_string.restype = ctypes.c_char_p
+    L.attn_check_device_status.argtypes = []
+    L.attn_check_device_status.restype = I
+    L.attn_read_tile_counter.argtypes = [ctypes.POINTER(ctypes.c_ulonglong), I]
+    L.attn_read_tile_counter.restype = I
+    L.attn_version.argtypes = []
+    L.attn_version.restype = ctypes.c_char_p
+    _lib = L
+    return L
+
+
+def _status_text(status: int) -> str:
+    try:
+        return lib().attn_status_string(int(status)).decode()
+    except Exception:  # library not loadable: still report the code
+        return "status %d" % status
+
+
+def _check(fn: str, status: int):
+    if status != ATTN_OK:
+        raise AttnError(fn, status)
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.bfloat16:
+        return ATTN_BF16
+    if t.dtype == torch.float32:
+        return ATTN_F32
+    raise TypeError("unsupported dtype %s (bfloat16 or float32)" % t.dtype)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need_cuda_contig(name, t):
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+
+
+def attn_fwd(q, k, v, causal: bool = False, scale: float | None = None, o=None, lse=None,
+             stream=None):
+    """O = softmax(scale q k^T) v per head, with LSE = log-sum-exp of the scores.
+
+    q [B, Nq, Hq, d], k/v [B, Nk, Hkv, d]; bf16 (tensor cores) or fp32.
+    Returns (o [B, Nq, Hq, d], lse [B, Hq, Nq] float32).
+    """
+    import torch
+    B, Nq, Hq, d = q.shape
+    Bk, Nk, Hkv, dk = k.shape
+    if Bk != B or dk != d or tuple(v.shape) != tuple(k.shape):
+        raise ValueError("shape mismatch: q %s k %s v %s" % (tuple(q.shape), tuple(k.shape), tuple(v.shape)))
+    if not (q.dtype == k.dtype == v.dtype):
+        raise ValueError("q, k, v must share a dtype")
+    for n, t in (("q", q), ("k", k), ("v", v)):
+        _need_cuda_contig(n, t)
+    if scale is None:
+        scale = d ** -0.5
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq, Nq), dtype=torch.float32, device=q.device)
+    st = lib().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Nq, Nk, d,
+                        int(bool(causal)), float(scale), _dtype_code(q), _stream(stream))
+    _check("attn_fwd", st)
+    return o, lse
+
+
+def attn_decode_num_splits(B: int, Hq: int, Hkv: int, Nk: int, d: int) -> int:
+    return int(lib().attn_decode_num_splits(B, Hq, Hkv, Nk, d))
+
+
+def attn_decode_workspace_bytes(B: int, Hq: int, Hkv: int, Nk: int, d: int,
+                                num_splits: int = 0) -> int:
+    return int(lib().attn_decode_workspace_bytes(B, Hq, Hkv, Nk, d, num_splits))
+
+
+def attn_decode_splitkv(q, k_cache, v_cache, scale: float | None = None, num_splits: int = 0,
+                        workspace=None, o=None, lse=None, stream=None):
+    """Flash-decoding: q [B, 1, Hq, d], caches [B, Nk, Hkv, d] (bf16).
+
+    Returns (o [B, 1, Hq, d], lse [B, Hq]).  ``workspace`` is a CUDA uint8
+    tensor of at least attn_decode_workspace_bytes(...) bytes; it is
+    allocated here when not given.
+    """
+    import torch
+    B, one, Hq, d = q.shape
+    if one != 1:
+        raise ValueError("decode takes one query per sequence (q.shape[1] == 1)")
+    Bk, Nk, Hkv, dk = k_cache.shape
+    if Bk != B or dk != d or tuple(v_cache.shape) != tuple(k_cache.shape):
+        raise ValueError("shape mismatch")
+    for n, t in (("q", q), ("k_cache", k_cache), ("v_cache", v_cache)):
+        _need_cuda_contig(n, t)
+    if scale is None:
+        scale = d ** -0.5
+    if num_splits == 0 and Nk > 0 and B > 0 and Hq > 0:
+        num_splits = attn_decode_num_splits(B, Hq, Hkv, Nk, d)
+    wbytes = attn_decode_workspace_bytes(B, Hq, Hkv, Nk, d, num_splits) if Nk > 0 and B > 0 and Hq > 0 else 0
+    if workspace is None and wbytes > 0:
+        workspace = torch.empty(wbytes, dtype=torch.uint8, device=q.device)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    wsize = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib().attn_decode_splitkv(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(o), _ptr(lse),
+                                   B, Hq, Hkv, Nk, d, float(scale), int(num_splits),
+                                   _ptr(workspace), wsize, _dtype_code(q), _stream(stream))
+    _check("attn_decode_splitkv", st)
+    return o, lse
+
+
+def attn_merge_lse(o_parts, lse_parts, out_dtype=None, o=None, lse=None, stream=None):
+    """Merges partials o_parts [P, rows, d] / lse_parts [P, rows] (float32)."""
+    import torch
+    P, rows, d = o_parts.shape
+    if tuple(lse_parts.shape) != (P, rows):
+        raise ValueError("lse_parts must be [P, rows]")
+    for n, t in (("o_parts", o_parts), ("lse_parts", lse_parts)):
+        _need_cuda_contig(n, t)
+    if out_dtype is None:
+        out_dtype = torch.float32
+    if o is None:
+        o = torch.empty((rows, d), dtype=out_dtype, device=o_parts.device)
+    if lse is None:
+        lse = torch.empty((rows,), dtype=torch.float32, device=o_parts.device)
+    st = lib().attn_merge_lse(_ptr(o_parts), _ptr(lse_parts), P, rows, d, _ptr(o), _ptr(lse),
+                              _dtype_code(o), _stream(stream))
+    _check("attn_merge_lse", st)
+    return o, lse
+
+
+def attn_status_string(status: int) -> str:
+    return lib().attn_status_string(int(status)).decode()
+
+
+def attn_check_device_status() -> int:
+    """Reads and clears the kernels' device status words (synchronises)."""
+    return int(lib().attn_check_device_status())
+
+
+def attn_read_tile_counter(reset: bool = False) -> int:
+    """(query tile, key tile) pairs the bf16 forward computed since the last reset."""
+    c = ctypes.c_ulonglong(0)
+    _check("attn_read_tile_counter", lib().attn_read_tile_counter(ctypes.byref(c), int(bool(reset))))
+    return int(c.value)
+
+
+def attn_version() -> str:
+    return lib().attn_version().decode()

@@ -1,0 +1,214 @@
+// api.cu -- the extern "C" entry points of libattn.so (declared and
+// documented in include/attn.h): argument checks, TMA tensor-map encoding
+// and dispatch to the kernels.  Nothing here allocates device memory,
+// synchronises a stream (except the two explicitly synchronous status
+// readers) or keeps state between calls.
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult qres;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &qres) == cudaSuccess &&
+            qres == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    });
+    return fn;
+}
+
+bool misaligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) != 0; }
+
+bool bad_scale(float s) { return !std::isfinite(s) || !(s > 0.f); }
+
+__global__ void fill_empty_kernel(void* o, float* lse, long long o_elems, long long n_lse,
+                                  bool out_bf16) {
+    const long long stride = (long long)gridDim.x * blockDim.x;
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < o_elems; i += stride) {
+        if (out_bf16)
+            static_cast<__nv_bfloat16*>(o)[i] = __float2bfloat16_rn(0.f);
+        else
+            static_cast<float*>(o)[i] = 0.f;
+    }
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n_lse; i += stride)
+        lse[i] = -INFINITY;
+}
+
+}  // namespace
+
+namespace attn_host {
+
+bool encode_bshd_map(CUtensorMap* map, const void* base, int B, int N, int H, int d, int box_rows,
+                     int elem_bytes) {
+    EncodeTiledFn fn = encode_fn();
+    if (fn == nullptr) return false;
+    const cuuint64_t e = static_cast<cuuint64_t>(elem_bytes);
+    cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)N, (cuuint64_t)B};
+    cuuint64_t strides[3] = {(cuuint64_t)d * e, (cuuint64_t)H * d * e, (cuuint64_t)N * H * d * e};
+    cuuint32_t box[4] = {(cuuint32_t)(128 / elem_bytes), 1u, (cuuint32_t)box_rows, 1u};
+    cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+    const CUtensorMapDataType dt =
+        elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    return fn(map, dt, 4, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int device_sm_count() {
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 0;
+    if (dev < 64 && cache[dev] > 0) return cache[dev];
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    if (dev < 64) cache[dev] = n;
+    return n;
+}
+
+attn_status_t launch_fill_empty(void* o, float* lse, long long rows_o, int d, long long n_lse,
+                                bool out_bf16, cudaStream_t stream) {
+    const long long o_elems = rows_o * d;
+    const long long work = o_elems > n_lse ? o_elems : n_lse;
+    long long blocks = (work + 255) / 256;
+    if (blocks > 4096) blocks = 4096;
+    if (blocks < 1) blocks = 1;
+    fill_empty_kernel<<<(unsigned)blocks, 256, 0, stream>>>(o, lse, o_elems, n_lse, out_bf16);
+    return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+}  // namespace attn_host
+
+extern "C" {
+
+attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                       int Hq, int Hkv, int Nq, int Nk, int d, int causal, float scale,
+                       attn_dtype_t dtype, void* stream) {
+    if (B < 0 || Hq < 0 || Nq < 0 || Nk < 0 || Hkv < 1 || d < 1) return ATTN_ERR_INVALID;
+    if (causal != 0 && causal != 1) return ATTN_ERR_INVALID;
+    if (dtype != ATTN_BF16 && dtype != ATTN_F32) return ATTN_ERR_INVALID;
+    if (bad_scale(scale)) return ATTN_ERR_INVALID;
+    if (Hq % Hkv != 0) return ATTN_ERR_INVALID;
+    if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+    if (B > 65535) return ATTN_ERR_UNSUPPORTED;
+    if (B == 0 || Hq == 0 || Nq == 0) return ATTN_OK;
+    if (q == nullptr || o == nullptr || lse == nullptr) return ATTN_ERR_INVALID;
+    if (Nk > 0 && (k == nullptr || v == nullptr)) return ATTN_ERR_INVALID;
+    if (misaligned(q, 16) || misaligned(o, 16) || misaligned(lse, 4)) return ATTN_ERR_INVALID;
+    if (Nk > 0 && (misaligned(k, 16) || misaligned(v, 16))) return ATTN_ERR_INVALID;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const bool bf16 = dtype == ATTN_BF16;
+    if (Nk == 0)
+        return attn_host::launch_fill_empty(o, lse, (long long)B * Nq * Hq, d,
+                                            (long long)B * Hq * Nq, bf16, st);
+    if (bf16)
+        return attn_host::launch_fwd_tc(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, causal, scale, st);
+    return attn_host::launch_fwd_f32(static_cast<const float*>(q), static_cast<const float*>(k),
+                                     static_cast<const float*>(v), static_cast<float*>(o), lse, B,
+                                     Hq, Hkv, Nq, Nk, d, causal, scale, st);
+}
+
+int attn_decode_num_splits(int B, int Hq, int Hkv, int Nk, int d) {
+    return attn_host::decode_auto_splits(B, Hq, Hkv, Nk, d);
+}
+
+size_t attn_decode_workspace_bytes(int B, int Hq, int Hkv, int Nk, int d, int num_splits) {
+    if (B < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || Nk < 1 || (d != 64 && d != 128) ||
+        num_splits < 0 || num_splits > Nk)
+        return 0;
+    int S = num_splits;
+    if (S == 0) S = attn_host::decode_auto_splits(B, Hq, Hkv, Nk, d);
+    if (S < 1) return 0;
+    return attn_host::decode_workspace_bytes(B, Hq, d, S);
+}
+
+attn_status_t attn_decode_splitkv(const void* q, const void* k_cache, const void* v_cache, void* o,
+                                  float* lse, int B, int Hq, int Hkv, int Nk, int d, float scale,
+                                  int num_splits, void* workspace, size_t workspace_bytes,
+                                  attn_dtype_t dtype, void* stream) {
+    if (B < 0 || Hq < 0 || Hkv < 1 || Nk < 0 || d < 1 || num_splits < 0) return ATTN_ERR_INVALID;
+    if (dtype != ATTN_BF16 && dtype != ATTN_F32) return ATTN_ERR_INVALID;
+    if (bad_scale(scale)) return ATTN_ERR_INVALID;
+    if (Hq % Hkv != 0) return ATTN_ERR_INVALID;
+    if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+    if (dtype != ATTN_BF16) return ATTN_ERR_UNSUPPORTED;
+    if (B > 65535 || Hq > 65535) return ATTN_ERR_UNSUPPORTED;
+    if (B == 0 || Hq == 0) return ATTN_OK;
+    if (q == nullptr || o == nullptr || lse == nullptr) return ATTN_ERR_INVALID;
+    if (misaligned(q, 16) || misaligned(o, 16) || misaligned(lse, 4)) return ATTN_ERR_INVALID;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (Nk == 0)
+        return attn_host::launch_fill_empty(o, lse, (long long)B * Hq, d, (long long)B * Hq, true,
+                                            st);
+    if (k_cache == nullptr || v_cache == nullptr) return ATTN_ERR_INVALID;
+    if (misaligned(k_cache, 16) || misaligned(v_cache, 16)) return ATTN_ERR_INVALID;
+    if (num_splits > Nk) return ATTN_ERR_INVALID;
+    int S = num_splits;
+    if (S == 0) S = attn_host::decode_auto_splits(B, Hq, Hkv, Nk, d);
+    if (S < 1) return ATTN_ERR_CUDA;
+    if (S > 65535) return ATTN_ERR_UNSUPPORTED;
+    if (S > 1) {
+        if (workspace == nullptr || misaligned(workspace, 16)) return ATTN_ERR_INVALID;
+        if (workspace_bytes < attn_host::decode_workspace_bytes(B, Hq, d, S))
+            return ATTN_ERR_INVALID;
+    }
+    return attn_host::launch_decode(q, k_cache, v_cache, o, lse, B, Hq, Hkv, Nk, d, scale, S,
+                                    workspace, st);
+}
+
+attn_status_t attn_merge_lse(const float* o_parts, const float* lse_parts, int num_parts,
+                             long long rows, int d, void* o, float* lse, attn_dtype_t out_dtype,
+                             void* stream) {
+    if (num_parts < 1 || rows < 0 || d < 4 || d > 512 || d % 4 != 0) return ATTN_ERR_INVALID;
+    if (out_dtype != ATTN_BF16 && out_dtype != ATTN_F32) return ATTN_ERR_INVALID;
+    if (rows == 0) return ATTN_OK;
+    if (o_parts == nullptr || lse_parts == nullptr || o == nullptr) return ATTN_ERR_INVALID;
+    if (misaligned(o_parts, 16) || misaligned(lse_parts, 4) || misaligned(o, 16) ||
+        (lse != nullptr && misaligned(lse, 4)))
+        return ATTN_ERR_INVALID;
+    return attn_host::launch_merge(o_parts, lse_parts, num_parts, rows, d, o, lse,
+                                   out_dtype == ATTN_BF16, static_cast<cudaStream_t>(stream));
+}
+
+const char* attn_status_string(attn_status_t status) {
+    switch (status) {
+        case ATTN_OK: return "ok";
+        case ATTN_ERR_INVALID: return "invalid argument";
+        case ATTN_ERR_UNSUPPORTED: return "unsupported configuration";
+        case ATTN_ERR_CUDA: return "CUDA error";
+        case ATTN_ERR_TIMEOUT: return "device-side wait timed out";
+    }
+    return "unknown status";
+}
+
+attn_status_t attn_check_device_status(void) {
+    if (cudaDeviceSynchronize() != cudaSuccess) return ATTN_ERR_CUDA;
+    unsigned a = 0, b = 0;
+    if (attn_host::fwd_tc_read_status(&a, true) != cudaSuccess) return ATTN_ERR_CUDA;
+    if (attn_host::decode_read_status(&b, true) != cudaSuccess) return ATTN_ERR_CUDA;
+    return (a | b) ? ATTN_ERR_TIMEOUT : ATTN_OK;
+}
+
+attn_status_t attn_read_tile_counter(unsigned long long* count, int reset) {
+    if (count == nullptr) return ATTN_ERR_INVALID;
+    if (cudaDeviceSynchronize() != cudaSuccess) return ATTN_ERR_CUDA;
+    return attn_host::fwd_tc_read_tiles(count, reset != 0) == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+const char* attn_version(void) { return "exact_attention_gb300 0.1 sm_103a"; }
+
+}  // extern "C"

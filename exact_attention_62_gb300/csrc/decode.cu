@@ -1,0 +1,499 @@
+// decode.cu -- flash-decoding on sm_103a: split-KV kernel + log-sum-exp merge.
+//
+// What it computes (Lecture 11 - Kernel Optimization Techniques, section 6.2):
+// with one query per sequence, the key/value length is cut into S segments;
+// for each (sequence, query head, segment) the segment's normalised output
+// o_s and lse_s = log sum_{j in segment} exp(scale q.k_j) are formed
+// (steps 1-2), and a second small kernel merges them:
+// lse = log sum_s exp(lse_s), o = sum_s exp(lse_s - lse) o_s (step 3).  This
+// is the associative merge of section 3.2 written in lse form.
+//
+// How (GB300 design):
+//  * Grid (segment, query-head group, sequence).  The G = Hq/Hkv query heads
+//    that share one KV head are packed into the columns of one small matrix
+//    product, so each K/V byte of the segment is read from HBM exactly once
+//    for the whole group (section 6.2, GQA paragraph).
+//  * Warp 0 streams the segment's K and V tiles (64 keys each) with TMA into
+//    a multi-stage shared-memory ring (128-byte swizzle, mbarrier full/empty
+//    pairs); four consumer warps each take 16 keys of every tile.
+//  * The consumer work per tile is two tiny matrix products done with warp
+//    MMA (m16n8k16, bf16 in, fp32 accumulate): S^T = K Q^T with the keys as
+//    the 16 rows and up to 8 query heads as the columns, then
+//    O^T += V^T P^T.  The transposed P operand is formed in registers with
+//    movmatrix.  The online-softmax state (m, l) lives per query column in
+//    registers; the running max is kept in base-2 units (scale log2 e
+//    folded in).  The kernel is HBM-bound; the tensor-core products just keep
+//    the instruction count far below the memory time.
+//  * At the end the four warps' states are merged through shared memory
+//    (the same (m, l, acc) merge).  With a single segment the kernel writes
+//    O (bf16) and LSE directly and no merge kernel runs.
+#include <algorithm>
+#include <cmath>
+#include <mutex>
+
+#include "common.cuh"
+#include "ptx.cuh"
+
+using namespace attn_dev;
+
+namespace {
+
+__device__ unsigned g_dec_status = 0;
+
+constexpr int kTileKeys = 64;
+constexpr int kConsumerWarps = 4;
+constexpr int kDecThreads = 32 * (1 + kConsumerWarps);
+constexpr float kLn2 = 0.69314718055994530942f;
+
+struct DecParams {
+    const __nv_bfloat16* q;  // [B, 1, Hq, D]
+    __nv_bfloat16* o;        // [B, 1, Hq, D]  (single segment)
+    float* lse;              // [B, Hq]        (single segment)
+    float* o_parts;          // [S, B*Hq, D]   (several segments)
+    float* lse_parts;        // [S, B*Hq]
+    int B, Hq, Hkv, Nk, G, splits, seg_len;
+    float scale_log2;
+};
+
+template <int D, int STAGES>
+struct DecLayout {
+    static constexpr int kPanelBytes = kTileKeys * 128;  // 64 keys x 64 columns x 2 B
+    static constexpr int kTileBytes = kTileKeys * D * 2;
+    static constexpr int kStageBytes = 2 * kTileBytes;   // K tile then V tile
+    static constexpr int kOffBar = STAGES * kStageBytes;
+    static constexpr int kNumBars = 2 * STAGES;          // full[STAGES], empty[STAGES]
+    static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+    static constexpr int kSmemBytes = kOffMisc + 16 + 1024;
+    // Cross-warp merge scratch [warp][8 query columns][D + 2], reusing the
+    // stage buffers once every tile has been consumed.
+    static constexpr int kRedStride = D + 2;
+    static_assert(kConsumerWarps * 8 * kRedStride * 4 <= STAGES * kStageBytes, "merge scratch");
+};
+
+template <int D>
+constexpr int dec_stages() { return D == 128 ? 3 : 6; }
+
+__device__ __forceinline__ uint32_t ld_b32(const __nv_bfloat16* p) {
+    return *reinterpret_cast<const uint32_t*>(p);
+}
+
+template <int D, int GC>
+__global__ void __launch_bounds__(kDecThreads)
+    decode_split_kernel(const __grid_constant__ CUtensorMap tmK,
+                        const __grid_constant__ CUtensorMap tmV, const DecParams p) {
+    constexpr int STAGES = dec_stages<D>();
+    using L = DecLayout<D, STAGES>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t sbase = (raw + 1023u) & ~1023u;
+    uint8_t* sgen = smem_raw + (sbase - raw);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    auto full_bar = [&](int st) -> uint32_t { return sbase + L::kOffBar + 8u * st; };
+    auto empty_bar = [&](int st) -> uint32_t { return sbase + L::kOffBar + 8u * (STAGES + st); };
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(sgen + L::kOffMisc);
+
+    const int seg = blockIdx.x;
+    const int hq0 = blockIdx.y * GC;
+    const int b = blockIdx.z;
+    const int g = hq0 / p.G;
+    const int j0 = seg * p.seg_len;
+    const int j1 = min(j0 + p.seg_len, p.Nk);
+    const int ntiles = j1 > j0 ? (j1 - j0 + kTileKeys - 1) / kTileKeys : 0;
+    const long long R = (long long)p.B * p.Hq;
+
+    if (ntiles == 0) {  // empty segment: o_s = 0, lse_s = -inf
+        for (int e = threadIdx.x; e < GC * D; e += blockDim.x) {
+            const long long row = (long long)b * p.Hq + hq0 + e / D;
+            p.o_parts[((long long)seg * R + row) * D + (e % D)] = 0.f;
+            if (e % D == 0) p.lse_parts[(long long)seg * R + row] = -INFINITY;
+        }
+        return;
+    }
+
+    if (threadIdx.x == 0) {
+        for (int st = 0; st < STAGES; ++st) {
+            mbar_init(full_bar(st), 1);
+            mbar_init(empty_bar(st), kConsumerWarps);
+        }
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    if (warp == 0) {
+        // ================================================= TMA producer
+        if (lane == 0) {
+            prefetch_tmap(&tmK);
+            prefetch_tmap(&tmV);
+            for (int t = 0; t < ntiles; ++t) {
+                const int st = t % STAGES;
+                if (!mbar_wait(empty_bar(st), ((t / STAGES) & 1) ^ 1, abort_flag, &g_dec_status))
+                    break;
+                mbar_arrive_expect_tx(full_bar(st), L::kStageBytes);
+                const uint32_t kdst = sbase + st * L::kStageBytes;
+                const int key0 = j0 + t * kTileKeys;
+#pragma unroll
+                for (int pp = 0; pp < D / 64; ++pp) {
+                    tma_load_4d(kdst + pp * L::kPanelBytes, &tmK, full_bar(st), 64 * pp, g, key0, b);
+                    tma_load_4d(kdst + L::kTileBytes + pp * L::kPanelBytes, &tmV, full_bar(st),
+                                64 * pp, g, key0, b);
+                }
+            }
+        }
+        return;  // the producer takes no part in the consumers' named barriers
+    }
+
+    // ===================================================== consumers
+    const int cw = warp - 1;
+    const int g8 = lane >> 2;  // fragment row group
+    const int t4 = lane & 3;   // fragment column pair
+    const int mi = lane >> 3;  // ldmatrix: which 8x8 matrix this lane addresses
+    const int rr = lane & 7;   // ldmatrix: which row of it
+
+    // Q^T as the B operand of S^T = K Q^T: column n = query head hq0 + n.
+    uint32_t qb[D / 16][2];
+    {
+        const bool qv = g8 < GC;
+        const __nv_bfloat16* qrow = p.q + ((long long)b * p.Hq + hq0 + (qv ? g8 : 0)) * D;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+            qb[kk][0] = qv ? ld_b32(qrow + kk * 16 + 2 * t4) : 0u;
+            qb[kk][1] = qv ? ld_b32(qrow + kk * 16 + 8 + 2 * t4) : 0u;
+        }
+    }
+    float acc[D / 16][4];
+#pragma unroll
+    for (int mb = 0; mb < D / 16; ++mb) acc[mb][0] = acc[mb][1] = acc[mb][2] = acc[mb][3] = 0.f;
+    // online-softmax state of this lane's two query columns (2 t4, 2 t4 + 1)
+    float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.f, l_b = 0.f;
+    const float sl = p.scale_log2;
+    const int kkey = 16 * cw + rr + 8 * (mi & 1);  // K row this lane addresses
+    const int vkey = 16 * cw + rr + 8 * (mi >> 1); // V row this lane addresses
+
+    for (int t = 0; t < ntiles; ++t) {
+        const int st = t % STAGES;
+        if (!mbar_wait(full_bar(st), (t / STAGES) & 1, abort_flag, &g_dec_status)) break;
+        const uint32_t kb = sbase + st * L::kStageBytes;
+        const uint32_t vb = kb + L::kTileBytes;
+
+        // S^T (16 keys x 8 query columns) = K (16 x D) Q^T (D x 8)
+        float c[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+            const int ch = 2 * kk + (mi >> 1);
+            const uint32_t addr =
+                kb + (ch >> 3) * L::kPanelBytes + kkey * 128 + (((ch & 7) ^ (kkey & 7)) << 4);
+            uint32_t a[4];
+            ldsm_x4(addr, a);
+            mma_16816(c, a, qb[kk][0], qb[kk][1]);
+        }
+        // keys of this lane: rows g8 and g8 + 8 of the warp's 16
+        const int key = j0 + t * kTileKeys + 16 * cw + g8;
+        const bool in0 = key < j1, in1 = key + 8 < j1;
+        const float x0 = in0 ? c[0] * sl : -INFINITY;  // (key,   col 2t4)
+        const float x1 = in0 ? c[1] * sl : -INFINITY;  // (key,   col 2t4+1)
+        const float x2 = in1 ? c[2] * sl : -INFINITY;  // (key+8, col 2t4)
+        const float x3 = in1 ? c[3] * sl : -INFINITY;  // (key+8, col 2t4+1)
+        float mxa = fmaxf(x0, x2), mxb = fmaxf(x1, x3);
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+            mxa = fmaxf(mxa, __shfl_xor_sync(0xffffffffu, mxa, off));
+            mxb = fmaxf(mxb, __shfl_xor_sync(0xffffffffu, mxb, off));
+        }
+        const float mna = fmaxf(m_a, mxa), mnb = fmaxf(m_b, mxb);
+        const float mua = mna == -INFINITY ? 0.f : mna;
+        const float mub = mnb == -INFINITY ? 0.f : mnb;
+        const float aa = ex2(m_a - mua), ab = ex2(m_b - mub);
+        const float p0 = ex2(x0 - mua), p2 = ex2(x2 - mua);
+        const float p1 = ex2(x1 - mub), p3 = ex2(x3 - mub);
+        l_a = fmaf(l_a, aa, p0 + p2);
+        l_b = fmaf(l_b, ab, p1 + p3);
+        m_a = mna;
+        m_b = mnb;
+#pragma unroll
+        for (int mb = 0; mb < D / 16; ++mb) {
+            acc[mb][0] *= aa;
+            acc[mb][1] *= ab;
+            acc[mb][2] *= aa;
+            acc[mb][3] *= ab;
+        }
+        // P^T as the B operand (keys x query columns)
+        const uint32_t b01 = movmatrix_trans(pack_bf16(p0, p1));
+        const uint32_t b23 = movmatrix_trans(pack_bf16(p2, p3));
+        // O^T (D x 8) += V^T (D x 16 keys) P^T (16 keys x 8)
+#pragma unroll
+        for (int mb = 0; mb < D / 16; ++mb) {
+            const int ch = 2 * mb + (mi & 1);
+            const uint32_t addr =
+                vb + (ch >> 3) * L::kPanelBytes + vkey * 128 + (((ch & 7) ^ (vkey & 7)) << 4);
+            uint32_t a[4];
+            ldsm_x4_trans(addr, a);
+            mma_16816(acc[mb], a, b01, b23);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty_bar(st));
+    }
+
+    // per-warp partial sums of l over the warp's keys
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+        l_a += __shfl_xor_sync(0xffffffffu, l_a, off);
+        l_b += __shfl_xor_sync(0xffffffffu, l_b, off);
+    }
+    // every tile has been consumed: the stage buffers are free for the merge
+    named_bar_sync(1, 32 * kConsumerWarps);
+    float* red = reinterpret_cast<float*>(sgen);
+    {
+        float* ra = red + (cw * 8 + 2 * t4) * L::kRedStride;
+        float* rb = ra + L::kRedStride;
+#pragma unroll
+        for (int mb = 0; mb < D / 16; ++mb) {
+            ra[mb * 16 + g8] = acc[mb][0];
+            rb[mb * 16 + g8] = acc[mb][1];
+            ra[mb * 16 + g8 + 8] = acc[mb][2];
+            rb[mb * 16 + g8 + 8] = acc[mb][3];
+        }
+        if (g8 == 0) {
+            ra[D] = m_a;
+            ra[D + 1] = l_a;
+            rb[D] = m_b;
+            rb[D + 1] = l_b;
+        }
+    }
+    named_bar_sync(1, 32 * kConsumerWarps);
+    for (int e = threadIdx.x - 32; e < GC * D; e += 32 * kConsumerWarps) {
+        const int qc = e / D, dd = e % D;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, red[(w * 8 + qc) * L::kRedStride + D]);
+        float lsum = 0.f, ov = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll
+            for (int w = 0; w < kConsumerWarps; ++w) {
+                const float* rw = red + (w * 8 + qc) * L::kRedStride;
+                if (rw[D] != -INFINITY) {
+                    const float cwt = ex2(rw[D] - M);
+                    lsum = fmaf(cwt, rw[D + 1], lsum);
+                    ov = fmaf(cwt, rw[dd], ov);
+                }
+            }
+        }
+        const long long row = (long long)b * p.Hq + hq0 + qc;
+        const float outv = lsum > 0.f ? ov / lsum : 0.f;
+        const float lsev = lsum > 0.f ? (M + lg2(lsum)) * kLn2 : -INFINITY;
+        if (p.splits == 1) {
+            p.o[row * D + dd] = __float2bfloat16_rn(outv);
+            if (dd == 0) p.lse[row] = lsev;
+        } else {
+            p.o_parts[((long long)seg * R + row) * D + dd] = outv;
+            if (dd == 0) p.lse_parts[(long long)seg * R + row] = lsev;
+        }
+    }
+}
+
+// One warp per row: lse = M + log sum_s exp(lse_s - M), o = sum_s exp(lse_s - lse) o_s.
+template <bool OUT_BF16>
+__global__ void __launch_bounds__(256)
+    merge_lse_kernel(const float* __restrict__ o_parts, const float* __restrict__ lse_parts, int P,
+                     long long rows, int d, void* __restrict__ o, float* __restrict__ lse) {
+    const long long row = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= rows) return;
+    float M = -INFINITY;
+    for (int s = lane; s < P; s += 32) M = fmaxf(M, lse_parts[(long long)s * rows + row]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    float Lr = -INFINITY;
+    if (M != -INFINITY) {
+        float sum = 0.f;
+        for (int s = lane; s < P; s += 32) sum += expf(lse_parts[(long long)s * rows + row] - M);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+        Lr = M + logf(sum);
+    }
+    for (int c4 = lane; 4 * c4 < d; c4 += 32) {
+        float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (Lr != -INFINITY) {
+            for (int s = 0; s < P; ++s) {
+                const float ls = lse_parts[(long long)s * rows + row];
+                if (ls == -INFINITY) continue;
+                const float w = expf(ls - Lr);
+                const float4 x =
+                    *reinterpret_cast<const float4*>(o_parts + ((long long)s * rows + row) * d + 4 * c4);
+                a.x = fmaf(w, x.x, a.x);
+                a.y = fmaf(w, x.y, a.y);
+                a.z = fmaf(w, x.z, a.z);
+                a.w = fmaf(w, x.w, a.w);
+            }
+        }
+        if constexpr (OUT_BF16) {
+            uint2 h;
+            h.x = pack_bf16(a.x, a.y);
+            h.y = pack_bf16(a.z, a.w);
+            *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(o) + row * d + 4 * c4) = h;
+        } else {
+            *reinterpret_cast<float4*>(static_cast<float*>(o) + row * d + 4 * c4) = a;
+        }
+    }
+    if (lane == 0 && lse != nullptr) lse[row] = Lr;
+}
+
+int group_cols(int G) {
+    if (G % 8 == 0) return 8;
+    if (G % 4 == 0) return 4;
+    if (G % 2 == 0) return 2;
+    return 1;
+}
+
+template <int D, int GC>
+attn_status_t launch_split(const CUtensorMap& mk, const CUtensorMap& mv, const DecParams& prm,
+                           cudaStream_t stream) {
+    using L = DecLayout<D, dec_stages<D>()>;
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [] {
+        attr_err = cudaFuncSetAttribute(decode_split_kernel<D, GC>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
+    });
+    if (attr_err != cudaSuccess) return ATTN_ERR_CUDA;
+    dim3 grid(prm.splits, prm.Hq / GC, prm.B);
+    decode_split_kernel<D, GC><<<grid, kDecThreads, L::kSmemBytes, stream>>>(mk, mv, prm);
+    return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+template <int D>
+int ctas_per_sm() {
+    static int v = -1;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        using L = DecLayout<D, dec_stages<D>()>;
+        int n = 0;
+        cudaFuncSetAttribute(decode_split_kernel<D, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             L::kSmemBytes);
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_split_kernel<D, 4>, kDecThreads,
+                                                          L::kSmemBytes) != cudaSuccess)
+            n = 1;
+        v = std::max(1, n);
+    });
+    return v;
+}
+
+}  // namespace
+
+namespace attn_host {
+
+// Segment count from a CTA-by-wave time model (Lecture 11, sections 6.3-6.4):
+// every CTA streams its segment at min(per-CTA limit, HBM / concurrent CTAs),
+// CTAs beyond one wave wait for the next, each CTA pays a fixed start-up
+// cost, and more than one segment adds the merge kernel.  The smallest
+// modelled time wins; ties go to fewer segments.
+int decode_auto_splits(int B, int Hq, int Hkv, int Nk, int d) {
+    if (B < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || Nk < 1 || (d != 64 && d != 128)) return -1;
+    const int sms = device_sm_count();
+    if (sms <= 0) return -1;
+    const int per_sm = d == 128 ? ctas_per_sm<128>() : ctas_per_sm<64>();
+    const long long slots = (long long)sms * per_sm;
+    const long long units = (long long)B * (Hq / group_cols(Hq / Hkv));
+    const double hbm = 6.5e12;        // bytes/s the whole GPU streams
+    const double cta_bw = 6.0e10;     // bytes/s one CTA can keep in flight
+    const double cta_fixed = 1.5e-6;  // start-up of one CTA wave
+    const double merge_fixed = 3.0e-6;
+    const double row_bytes = 2.0 * d * 2.0;  // one key's K and V for one head
+    int best = 1;
+    double best_t = 1e30;
+    const int max_s = std::min(Nk, 1024);
+    for (int S = 1; S <= max_s; ++S) {
+        const long long ctas = units * S;
+        const long long waves = (ctas + slots - 1) / slots;
+        const double conc = (double)std::min(ctas, slots);
+        const double bw = std::min(cta_bw, hbm / conc);
+        const int seg = (Nk + S - 1) / S;
+        const double t = (double)waves * (seg * row_bytes / bw + cta_fixed) +
+                         (S > 1 ? merge_fixed + 2.0 * units * 8 * S * (d + 1) * 4.0 / hbm : 0.0);
+        if (t < best_t * 0.995) {
+            best_t = t;
+            best = S;
+        }
+    }
+    return best;
+}
+
+size_t decode_workspace_bytes(int B, int Hq, int d, int splits) {
+    if (splits <= 1) return 0;
+    const size_t rows = (size_t)B * Hq;
+    const size_t o_bytes = (size_t)splits * rows * d * 4;
+    const size_t o_round = (o_bytes + 255) / 256 * 256;
+    return o_round + (size_t)splits * rows * 4;
+}
+
+attn_status_t launch_decode(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                            int Hq, int Hkv, int Nk, int d, float scale, int splits,
+                            void* workspace, cudaStream_t stream) {
+    CUtensorMap mk, mv;
+    if (!encode_bshd_map(&mk, k, B, Nk, Hkv, d, kTileKeys, 2) ||
+        !encode_bshd_map(&mv, v, B, Nk, Hkv, d, kTileKeys, 2))
+        return ATTN_ERR_CUDA;
+    DecParams prm;
+    prm.q = static_cast<const __nv_bfloat16*>(q);
+    prm.o = static_cast<__nv_bfloat16*>(o);
+    prm.lse = lse;
+    prm.B = B;
+    prm.Hq = Hq;
+    prm.Hkv = Hkv;
+    prm.Nk = Nk;
+    prm.G = Hq / Hkv;
+    prm.splits = splits;
+    prm.seg_len = (Nk + splits - 1) / splits;
+    prm.scale_log2 = scale * 1.4426950408889634f;
+    const size_t rows = (size_t)B * Hq;
+    if (splits > 1) {
+        const size_t o_bytes = (size_t)splits * rows * d * 4;
+        prm.o_parts = static_cast<float*>(workspace);
+        prm.lse_parts = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                                 (o_bytes + 255) / 256 * 256);
+    } else {
+        prm.o_parts = nullptr;
+        prm.lse_parts = nullptr;
+    }
+    const int GC = group_cols(prm.G);
+    attn_status_t st;
+    if (d == 128) {
+        st = GC == 8   ? launch_split<128, 8>(mk, mv, prm, stream)
+             : GC == 4 ? launch_split<128, 4>(mk, mv, prm, stream)
+             : GC == 2 ? launch_split<128, 2>(mk, mv, prm, stream)
+                       : launch_split<128, 1>(mk, mv, prm, stream);
+    } else {
+        st = GC == 8   ? launch_split<64, 8>(mk, mv, prm, stream)
+             : GC == 4 ? launch_split<64, 4>(mk, mv, prm, stream)
+             : GC == 2 ? launch_split<64, 2>(mk, mv, prm, stream)
+                       : launch_split<64, 1>(mk, mv, prm, stream);
+    }
+    if (st != ATTN_OK || splits == 1) return st;
+    return launch_merge(prm.o_parts, prm.lse_parts, splits, (long long)rows, d, o, lse, true, stream);
+}
+
+attn_status_t launch_merge(const float* o_parts, const float* lse_parts, int parts,
+                           long long rows, int d, void* o, float* lse, bool out_bf16,
+                           cudaStream_t stream) {
+    if (rows == 0) return ATTN_OK;
+    const int rows_per_block = 8;
+    const long long blocks = (rows + rows_per_block - 1) / rows_per_block;
+    if (blocks > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
+    if (out_bf16)
+        merge_lse_kernel<true><<<(unsigned)blocks, 32 * rows_per_block, 0, stream>>>(
+            o_parts, lse_parts, parts, rows, d, o, lse);
+    else
+        merge_lse_kernel<false><<<(unsigned)blocks, 32 * rows_per_block, 0, stream>>>(
+            o_parts, lse_parts, parts, rows, d, o, lse);
+    return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+cudaError_t decode_read_status(unsigned* out, bool clear) {
+    cudaError_t e = cudaMemcpyFromSymbol(out, g_dec_status, sizeof(unsigned));
+    if (e != cudaSuccess || !clear) return e;
+    const unsigned zero = 0;
+    return cudaMemcpyToSymbol(g_dec_status, &zero, sizeof(unsigned));
+}
+
+}  // namespace attn_host

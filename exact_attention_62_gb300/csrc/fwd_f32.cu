@@ -1,0 +1,213 @@
+// fwd_f32.cu -- fp32 exact-attention forward on CUDA cores.
+//
+// Same computation as the bf16 tensor-core kernel (Lecture 11 - Kernel
+// Optimization Techniques, sections 2, 3.1 and 3.3: online softmax over key
+// tiles with deferred normalisation, causal tiles beyond the diagonal
+// skipped per section 5.3), but every operand and every product stays in
+// fp32 so that fp32 inputs meet fp32 accuracy; the tensor-core path would
+// round P and the inputs to bf16/tf32.
+//
+// One CTA of 128 threads owns 32 query rows of one (batch, head); four
+// threads share a row.  Per 32-key tile: the threads stage K and V in shared
+// memory, each computes 8 scores of its row, the row's max and sum are
+// reduced across its four threads with shuffles, P goes to shared memory,
+// and each thread accumulates D/4 output columns.
+#include <mutex>
+
+#include "common.cuh"
+
+namespace {
+
+__device__ __forceinline__ long long llmin(long long a, long long b) { return a < b ? a : b; }
+
+constexpr int kRows = 32;
+constexpr int kKeys = 32;
+constexpr int kThreadsF32 = 128;
+
+struct F32Params {
+    int B, Hq, Hkv, Nq, Nk, G, causal;
+    float scale;
+};
+
+template <int D>
+struct F32Layout {
+    static constexpr int kLd = D + 4;  // padded row stride (floats)
+    static constexpr int kQ = 0;
+    static constexpr int kK = kQ + kRows * kLd;
+    static constexpr int kV = kK + kKeys * kLd;
+    static constexpr int kP = kV + kKeys * kLd;
+    static constexpr int kFloats = kP + kRows * (kKeys + 1);
+    static constexpr int kBytes = kFloats * 4;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreadsF32)
+    fwd_f32_kernel(const float* __restrict__ q, const float* __restrict__ k,
+                   const float* __restrict__ v, float* __restrict__ o, float* __restrict__ lse,
+                   const F32Params p) {
+    using L = F32Layout<D>;
+    extern __shared__ float4 smem4[];
+    float* sm = reinterpret_cast<float*>(smem4);
+    float* Qs = sm + L::kQ;
+    float* Ks = sm + L::kK;
+    float* Vs = sm + L::kV;
+    float* Ps = sm + L::kP;
+    constexpr int C4 = D / 4;       // float4 chunks per row
+    constexpr int NCH = D / 16;     // float4 chunks each thread owns
+    const int qt = blockIdx.x, hq = blockIdx.y, b = blockIdx.z;
+    const int g = hq / p.G;
+    const int tid = threadIdx.x;
+    const int r = tid >> 2, cg = tid & 3;
+    const int row = qt * kRows + r;
+
+    for (int idx = tid; idx < kRows * C4; idx += kThreadsF32) {
+        const int rr = idx / C4, c4 = idx % C4;
+        const int qr = qt * kRows + rr;
+        float4 val = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (qr < p.Nq)
+            val = __ldg(reinterpret_cast<const float4*>(
+                q + (((long long)b * p.Nq + qr) * p.Hq + hq) * D) + c4);
+        *reinterpret_cast<float4*>(Qs + rr * L::kLd + 4 * c4) = val;
+    }
+
+    int nkv;
+    if (!p.causal) {
+        nkv = (p.Nk + kKeys - 1) / kKeys;
+    } else {
+        const int last_row = min(qt * kRows + kRows - 1, p.Nq - 1);
+        const long long last = llmin((long long)p.Nk - 1, (long long)last_row + (p.Nk - p.Nq));
+        nkv = last < 0 ? 0 : (int)(last / kKeys) + 1;
+    }
+    const long long diag = (long long)row + (p.Nk - p.Nq);
+
+    float m = -INFINITY, l = 0.f;
+    float4 acc[NCH];
+#pragma unroll
+    for (int i = 0; i < NCH; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+
+    for (int jt = 0; jt < nkv; ++jt) {
+        __syncthreads();  // previous tile fully consumed
+        for (int idx = tid; idx < kKeys * C4; idx += kThreadsF32) {
+            const int rr = idx / C4, c4 = idx % C4;
+            const int key = jt * kKeys + rr;
+            float4 kv = make_float4(0.f, 0.f, 0.f, 0.f), vv = kv;
+            if (key < p.Nk) {
+                const long long off = (((long long)b * p.Nk + key) * p.Hkv + g) * D;
+                kv = __ldg(reinterpret_cast<const float4*>(k + off) + c4);
+                vv = __ldg(reinterpret_cast<const float4*>(v + off) + c4);
+            }
+            *reinterpret_cast<float4*>(Ks + rr * L::kLd + 4 * c4) = kv;
+            *reinterpret_cast<float4*>(Vs + rr * L::kLd + 4 * c4) = vv;
+        }
+        __syncthreads();
+
+        float s[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) s[i] = 0.f;
+#pragma unroll 4
+        for (int c4 = 0; c4 < C4; ++c4) {
+            const float4 qv = *reinterpret_cast<const float4*>(Qs + r * L::kLd + 4 * c4);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float4 kv = *reinterpret_cast<const float4*>(Ks + (cg + 4 * i) * L::kLd + 4 * c4);
+                s[i] = fmaf(qv.x, kv.x, s[i]);
+                s[i] = fmaf(qv.y, kv.y, s[i]);
+                s[i] = fmaf(qv.z, kv.z, s[i]);
+                s[i] = fmaf(qv.w, kv.w, s[i]);
+            }
+        }
+        float mx = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int key = jt * kKeys + cg + 4 * i;
+            const bool keep = key < p.Nk && (!p.causal || (long long)key <= diag);
+            s[i] = keep ? s[i] * p.scale : -INFINITY;
+            mx = fmaxf(mx, s[i]);
+        }
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        const float m_new = fmaxf(m, mx);
+        const float m_use = m_new == -INFINITY ? 0.f : m_new;
+        const float alpha = expf(m - m_use);
+        float ps = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float pi = expf(s[i] - m_use);
+            ps += pi;
+            Ps[r * (kKeys + 1) + cg + 4 * i] = pi;
+        }
+        ps += __shfl_xor_sync(0xffffffffu, ps, 1);
+        ps += __shfl_xor_sync(0xffffffffu, ps, 2);
+        l = fmaf(l, alpha, ps);
+        m = m_new;
+#pragma unroll
+        for (int i = 0; i < NCH; ++i) {
+            acc[i].x *= alpha;
+            acc[i].y *= alpha;
+            acc[i].z *= alpha;
+            acc[i].w *= alpha;
+        }
+        __syncwarp();  // the four threads of a row live in one warp
+#pragma unroll 4
+        for (int jj = 0; jj < kKeys; ++jj) {
+            const float pj = Ps[r * (kKeys + 1) + jj];
+#pragma unroll
+            for (int i = 0; i < NCH; ++i) {
+                const float4 vv = *reinterpret_cast<const float4*>(Vs + jj * L::kLd + 4 * (cg + 4 * i));
+                acc[i].x = fmaf(pj, vv.x, acc[i].x);
+                acc[i].y = fmaf(pj, vv.y, acc[i].y);
+                acc[i].z = fmaf(pj, vv.z, acc[i].z);
+                acc[i].w = fmaf(pj, vv.w, acc[i].w);
+            }
+        }
+    }
+
+    if (row < p.Nq) {
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        float* orow = o + (((long long)b * p.Nq + row) * p.Hq + hq) * D;
+#pragma unroll
+        for (int i = 0; i < NCH; ++i) {
+            float4 w = acc[i];
+            w.x *= inv;
+            w.y *= inv;
+            w.z *= inv;
+            w.w *= inv;
+            reinterpret_cast<float4*>(orow)[cg + 4 * i] = w;
+        }
+        if (cg == 0)
+            lse[((long long)b * p.Hq + hq) * p.Nq + row] = l > 0.f ? m + logf(l) : -INFINITY;
+    }
+}
+
+template <int D>
+attn_status_t launch_impl(const float* q, const float* k, const float* v, float* o, float* lse,
+                          const F32Params& prm, cudaStream_t stream) {
+    using L = F32Layout<D>;
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [] {
+        attr_err = cudaFuncSetAttribute(fwd_f32_kernel<D>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
+    });
+    if (attr_err != cudaSuccess) return ATTN_ERR_CUDA;
+    const long long qtiles = (prm.Nq + kRows - 1) / kRows;
+    if (qtiles > 0x7fffffffLL || prm.Hq > 65535 || prm.B > 65535) return ATTN_ERR_UNSUPPORTED;
+    dim3 grid((unsigned)qtiles, prm.Hq, prm.B);
+    fwd_f32_kernel<D><<<grid, kThreadsF32, L::kBytes, stream>>>(q, k, v, o, lse, prm);
+    return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+}  // namespace
+
+namespace attn_host {
+
+attn_status_t launch_fwd_f32(const float* q, const float* k, const float* v, float* o,
+                             float* lse, int B, int Hq, int Hkv, int Nq, int Nk, int d,
+                             int causal, float scale, cudaStream_t stream) {
+    F32Params prm{B, Hq, Hkv, Nq, Nk, Hq / Hkv, causal, scale};
+    if (d == 128) return launch_impl<128>(q, k, v, o, lse, prm, stream);
+    if (d == 64) return launch_impl<64>(q, k, v, o, lse, prm, stream);
+    return ATTN_ERR_UNSUPPORTED;
+}
+
+}  // namespace attn_host

@@ -1,0 +1,182 @@
+/*
+ * attn.h -- C ABI of libattn.so: fused exact attention forward and
+ * split-KV flash-decoding for NVIDIA GB300 (sm_103a).
+ *
+ * Sources (page titles, sections as printed on the pages):
+ *   [L11] "Lecture 11 - Kernel Optimization Techniques: FlashAttention,
+ *         flash-decoding and megakernel" (CS349E notes).
+ *   [IDX] "CUDA Kernel course index - FlashAttention v1->v4 diagrams".
+ *
+ * General conventions (all entry points):
+ *   - Every pointer argument is a DEVICE pointer unless stated otherwise.
+ *     The caller owns every buffer, including decode workspaces.  The
+ *     library allocates and frees nothing, never synchronises the stream
+ *     and keeps no per-call state; calls are asynchronous on `stream`
+ *     (a cudaStream_t passed as void*; NULL = the legacy default stream).
+ *   - Layouts are row-major and contiguous ("BSHD"):
+ *       q, o   [B, Nq, Hq, d]      k, v   [B, Nk, Hkv, d]
+ *       lse    [B, Hq, Nq]  float32 (natural log of the scaled scores)
+ *   - GQA: query head hq reads key/value head hq / (Hq / Hkv).
+ *   - Causal masking is bottom-right aligned: query row i may attend key j
+ *     iff j <= i + (Nk - Nq).  A row with no allowed key gets O = 0 and
+ *     LSE = -inf.
+ *   - Arguments are checked before anything is launched; a rejected call
+ *     launches nothing and writes nothing.  Errors inside a kernel (a bounded
+ *     wait that ran out) are recorded in a device status word that
+ *     attn_check_device_status() reads and clears.
+ *   - Pointers to q/k/v/o and to workspaces must be 16-byte aligned (TMA
+ *     and 128-bit accesses); lse must be 4-byte aligned.
+ */
+#ifndef EXACT_ATTENTION_GB300_ATTN_H
+#define EXACT_ATTENTION_GB300_ATTN_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    ATTN_OK = 0,
+    ATTN_ERR_INVALID = 1,      /* bad pointer, size, alignment or scale     */
+    ATTN_ERR_UNSUPPORTED = 2,  /* valid but not implemented (d, dtype, G)   */
+    ATTN_ERR_CUDA = 3,         /* a CUDA runtime/driver call failed         */
+    ATTN_ERR_TIMEOUT = 4       /* a device-side bounded wait ran out        */
+} attn_status_t;
+
+typedef enum {
+    ATTN_BF16 = 0,  /* q/k/v/o bfloat16, fp32 accumulation, P rounded to bf16 */
+    ATTN_F32 = 1    /* q/k/v/o float32, fp32 arithmetic throughout            */
+} attn_dtype_t;
+
+/*
+ * attn_fwd -- exact attention forward with per-row log-sum-exp.
+ *
+ * Computes, for every (b, hq, i),
+ *     O[b,i,hq,:] = softmax_j( scale * q[b,i,hq,:] . k[b,j,g,:] ) v[b,j,g,:]
+ *     lse[b,hq,i] = log sum_j exp( scale * q[b,i,hq,:] . k[b,j,g,:] )
+ * over the allowed keys j (g = hq / (Hq/Hkv); causal rule above).  This is
+ * standard attention ("algorithm 0", [L11] section 2) evaluated tile by tile
+ * with the online softmax and deferred normalisation ([L11] 3.1, 3.3; the
+ * "FlashAttention v1" pseudocode of [IDX]); L = m + log l is the statistic of
+ * [L11] 5.1.  The result is exact up to floating-point rounding ([L11] 4.1,
+ * theorem 1).
+ *
+ *   q, k, v  inputs (dtype elements, layouts above); read only.
+ *   o        output [B, Nq, Hq, d] (dtype elements); fully overwritten.
+ *   lse      output [B, Hq, Nq] float32; fully overwritten.
+ *   B, Hq, Hkv, Nq, Nk   sizes; B, Hq, Nq may be 0 (nothing to do, ATTN_OK);
+ *            Hkv >= 1, Hq % Hkv == 0, Nk >= 0 (Nk == 0: every row empty).
+ *   d        head dimension: 64 or 128 (else ATTN_ERR_UNSUPPORTED).
+ *   causal   0 or 1.
+ *   scale    multiplies q.k; finite and > 0 (commonly 1/sqrt(d)).
+ *   dtype    ATTN_BF16: tcgen05 tensor-core kernel (TMA, TMEM accumulators).
+ *            ATTN_F32: fp32 CUDA-core kernel (for fp32 accuracy).
+ * Returns ATTN_OK once the work is enqueued on `stream`.
+ */
+attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o,
+                       float* lse, int B, int Hq, int Hkv, int Nq, int Nk,
+                       int d, int causal, float scale, attn_dtype_t dtype,
+                       void* stream);
+
+/*
+ * attn_decode_num_splits -- the number of key segments attn_decode_splitkv
+ * uses when called with num_splits = 0.  It follows the CTA-by-wave model of
+ * [L11] 6.3-6.4: too few segments leave SMs idle, too many add waves and
+ * merge overhead, so the count is picked from B, the head counts, Nk and the
+ * SM count of the current device.  Returns >= 1, or -1 on invalid sizes or if
+ * the device cannot be queried.
+ */
+int attn_decode_num_splits(int B, int Hq, int Hkv, int Nk, int d);
+
+/*
+ * attn_decode_workspace_bytes -- bytes of device workspace that
+ * attn_decode_splitkv needs for these sizes (num_splits = 0 resolves through
+ * attn_decode_num_splits).  Returns 0 on invalid sizes.
+ *
+ * Workspace layout after a call with S segments (S > 1), R = B*Hq rows,
+ * row r = b*Hq + hq, all float32:
+ *     o_parts   [S, R, d]  at byte offset 0: segment outputs, each already
+ *                          normalised within its segment ([L11] 6.2 step 2);
+ *     lse_parts [S, R]     at byte offset round_up(S*R*d*4, 256).
+ * An empty segment holds o = 0, lse = -inf.  With S == 1 the workspace is
+ * not touched and may be NULL.
+ */
+size_t attn_decode_workspace_bytes(int B, int Hq, int Hkv, int Nk, int d,
+                                   int num_splits);
+
+/*
+ * attn_decode_splitkv -- flash-decoding ([L11] 6.2): one query per sequence.
+ *
+ *   q        [B, 1, Hq, d]      query of the current step.
+ *   k_cache, v_cache  [B, Nk, Hkv, d]  dense KV cache (Nk >= 1 valid rows).
+ *   o        [B, 1, Hq, d] output (dtype elements).
+ *   lse      [B, Hq] float32 output.
+ *   num_splits  0 = automatic (attn_decode_num_splits), else 1..Nk.
+ *            Segment s covers keys [s*L, min((s+1)*L, Nk)), L = ceil(Nk/S).
+ *   workspace, workspace_bytes  scratch of at least
+ *            attn_decode_workspace_bytes(...) bytes, 16-byte aligned; its
+ *            contents on return are the partials documented above.
+ *   dtype    ATTN_BF16 only (ATTN_F32 returns ATTN_ERR_UNSUPPORTED).
+ * Head dimension d is 64 or 128; any G = Hq/Hkv is accepted (query heads of
+ * one group are packed into the rows of one tile, [L11] 6.2 GQA paragraph).
+ *
+ * Step 1-2: the split kernel, one CTA per (segment, group of up to 8 query
+ * heads of one KV head, sequence), streams its K/V segment once and writes
+ * (o_s, lse_s).  Step 3: attn_merge_lse on the same stream.  With S == 1 the
+ * split kernel writes O and LSE directly and no merge runs.
+ */
+attn_status_t attn_decode_splitkv(const void* q, const void* k_cache,
+                                  const void* v_cache, void* o, float* lse,
+                                  int B, int Hq, int Hkv, int Nk, int d,
+                                  float scale, int num_splits,
+                                  void* workspace, size_t workspace_bytes,
+                                  attn_dtype_t dtype, void* stream);
+
+/*
+ * attn_merge_lse -- exact merge of partial attention results in log-sum-exp
+ * form ([L11] 6.2 step 3; the associative merge of [L11] 3.2):
+ *     lse[r] = log sum_p exp(lse_parts[p, r])
+ *     o[r,:] = sum_p exp(lse_parts[p, r] - lse[r]) * o_parts[p, r, :]
+ * computed after subtracting max_p lse_parts[p, r].  Parts with lse = -inf
+ * are empty and ignored; a row whose parts are all empty gets o = 0,
+ * lse = -inf.
+ *
+ *   o_parts   [num_parts, rows, d] float32, each normalised within its part.
+ *   lse_parts [num_parts, rows] float32.
+ *   o         [rows, d] output in out_dtype (ATTN_BF16 or ATTN_F32).
+ *   lse       [rows] float32 output (may be NULL if not wanted).
+ *   num_parts >= 1, rows >= 0, d a multiple of 4 in [4, 512].
+ */
+attn_status_t attn_merge_lse(const float* o_parts, const float* lse_parts,
+                             int num_parts, long long rows, int d, void* o,
+                             float* lse, attn_dtype_t out_dtype, void* stream);
+
+/* Static English text for a status code. */
+const char* attn_status_string(attn_status_t status);
+
+/*
+ * attn_check_device_status -- reads and clears the device status words of
+ * every kernel family in the library (synchronises the device first).
+ * Returns ATTN_ERR_TIMEOUT if any bounded wait ran out since the last call,
+ * ATTN_ERR_CUDA if the device could not be read, else ATTN_OK.
+ */
+attn_status_t attn_check_device_status(void);
+
+/*
+ * attn_read_tile_counter -- number of (query tile, key tile) pairs the bf16
+ * forward kernel has computed since the last reset (synchronises the device;
+ * reset != 0 clears it after reading).  Tiles are 128 x 128.  A causal call
+ * with Nq = Nk = N computes T(T+1)/2 of the T^2 pairs, T = N/128, i.e. the
+ * fraction 1/2 + 1/(2T) of [L11] 5.3 (0.516 at N = 4096).
+ */
+attn_status_t attn_read_tile_counter(unsigned long long* count, int reset);
+
+/* Library version string, e.g. "exact_attention_gb300 0.1 sm_103a". */
+const char* attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EXACT_ATTENTION_GB300_ATTN_H */

@@ -1,0 +1,127 @@
+"""The C ABI without a GPU: the library loads, exports every symbol the
+header declares, and rejects bad arguments before launching anything."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import exact_attention_62_gb300 as pkg
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                      "include", "attn.h")
+
+OK, INVALID, UNSUPPORTED, CUDA, TIMEOUT = range(5)
+BF16, F32 = 0, 1
+# aligned, never dereferenced: every call below is rejected (or is a no-op)
+# before the library touches a pointer or the CUDA runtime
+FAKE = ctypes.c_void_p(0x7f0000000000)
+FAKE_LSE = ctypes.c_void_p(0x7f0000100000)
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(attn_[a-z0-9_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def L(attn):
+    return attn.lib()
+
+
+def test_header_declares_the_documented_set():
+    assert declared_functions() == sorted(pkg.EXPORTED_SYMBOLS)
+
+
+def test_every_declared_symbol_is_exported(L):
+    for name in declared_functions():
+        assert hasattr(L, name), name
+
+
+def test_status_strings_and_version(L):
+    for code in range(5):
+        assert pkg.attn_status_string(code)
+    assert pkg.attn_status_string(99) == "unknown status"
+    assert "sm_103a" in pkg.attn_version()
+
+
+def fwd(L, B=1, Hq=2, Hkv=1, Nq=8, Nk=8, d=64, causal=0, scale=0.125, dtype=BF16,
+        q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE_LSE):
+    return L.attn_fwd(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, causal, scale, dtype, None)
+
+
+def test_fwd_rejects_bad_arguments(L):
+    assert fwd(L, d=96) == UNSUPPORTED
+    assert fwd(L, d=256) == UNSUPPORTED
+    assert fwd(L, Hq=3, Hkv=2) == INVALID
+    assert fwd(L, Hkv=0) == INVALID
+    for bad in ({"B": -1}, {"Hq": -2}, {"Nq": -1}, {"Nk": -5}, {"d": 0}):
+        assert fwd(L, **bad) == INVALID, bad
+    for s in (0.0, -1.0, float("nan"), float("inf")):
+        assert fwd(L, scale=s) == INVALID, s
+    assert fwd(L, causal=2) == INVALID
+    assert fwd(L, dtype=7) == INVALID
+    assert fwd(L, q=None) == INVALID
+    assert fwd(L, k=None) == INVALID
+    assert fwd(L, lse=None) == INVALID
+    assert fwd(L, o=ctypes.c_void_p(0x7f0000000008)) == INVALID  # not 16-byte aligned
+    assert fwd(L, lse=ctypes.c_void_p(0x7f0000000002)) == INVALID
+
+
+def test_fwd_empty_is_a_noop(L):
+    assert fwd(L, B=0, q=None, k=None, v=None, o=None, lse=None) == OK
+    assert fwd(L, Nq=0, q=None, k=None, v=None, o=None, lse=None) == OK
+    assert fwd(L, Hq=0) == OK
+
+
+def dec(L, B=1, Hq=8, Hkv=2, Nk=100, d=128, scale=0.1, S=0, ws=None, wbytes=0, dtype=BF16):
+    return L.attn_decode_splitkv(FAKE, FAKE, FAKE, FAKE, FAKE_LSE, B, Hq, Hkv, Nk, d, scale, S,
+                                 ws, wbytes, dtype, None)
+
+
+def test_decode_rejects_bad_arguments(L):
+    assert dec(L, dtype=F32) == UNSUPPORTED
+    assert dec(L, d=80) == UNSUPPORTED
+    assert dec(L, Hq=6, Hkv=4) == INVALID
+    assert dec(L, S=-1) == INVALID
+    assert dec(L, S=101) == INVALID            # more segments than keys
+    assert dec(L, S=4, ws=None) == INVALID       # several segments need a workspace
+    need = pkg.attn_decode_workspace_bytes(1, 8, 2, 100, 128, 4)
+    assert dec(L, S=4, ws=FAKE, wbytes=need - 1) == INVALID
+    assert dec(L, scale=float("nan")) == INVALID
+    assert dec(L, B=0) == OK
+
+
+def test_decode_workspace_layout():
+    # o_parts [S, R, d] fp32 rounded up to 256 bytes, then lse_parts [S, R]
+    for B, Hq, d, S in ((1, 32, 128, 19), (16, 32, 128, 3), (3, 5, 64, 7)):
+        R = B * Hq
+        o_bytes = S * R * d * 4
+        want = (o_bytes + 255) // 256 * 256 + S * R * 4
+        assert pkg.attn_decode_workspace_bytes(B, Hq, 1, 1000, d, S) == want
+    assert pkg.attn_decode_workspace_bytes(1, 8, 2, 100, 128, 1) == 0  # one segment: none
+    assert pkg.attn_decode_workspace_bytes(1, 8, 3, 100, 128, 2) == 0  # invalid sizes
+
+
+def test_merge_rejects_bad_arguments(L):
+    m = lambda P=2, rows=4, d=64, dt=F32: L.attn_merge_lse(FAKE, FAKE_LSE, P, rows, d, FAKE,
+                                                          FAKE_LSE, dt, None)
+    assert m(P=0) == INVALID
+    assert m(d=6) == INVALID
+    assert m(d=516) == INVALID
+    assert m(rows=-1) == INVALID
+    assert m(dt=5) == INVALID
+    assert m(rows=0) == OK
+
+
+def test_tile_counter_needs_a_pointer(L):
+    assert L.attn_read_tile_counter(None, 0) == INVALID
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    """No silent fallback: a missing libattn.so is an error."""
+    monkeypatch.setattr(pkg, "_lib", None)
+    monkeypatch.setattr(pkg, "_LIB_PATH", str(tmp_path / "libattn.so"))
+    with pytest.raises(RuntimeError, match="not built"):
+        pkg.lib()

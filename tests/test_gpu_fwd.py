@@ -1,0 +1,155 @@
+"""Parity of attn_fwd (tcgen05 bf16 path and fp32 path) against the oracle."""
+import json
+import math
+import os
+import subprocess
+import sys
+
+import numpy as np
+import pytest
+import torch
+
+from exact_attention_62_gb300.inputs import make_qkv, sample_rows
+from parity import compare, guarded, guards_intact, to_np64
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def run_case(attn, oracle_mod, B, Hq, Hkv, Nq, Nk, d, causal, seed, dtype=torch.bfloat16,
+             q_scale=1.0, guard=True):
+    q, k, v = make_qkv(B, Hq, Hkv, Nq, Nk, d, seed, dtype=dtype, q_scale=q_scale)
+    scale = 1.0 / math.sqrt(d)
+    qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
+    o, ob, og = guarded((B, Nq, Hq, d), dtype, DEV)
+    lse, lb, lg = guarded((B, Hq, Nq), torch.float32, DEV)
+    attn.attn_fwd(qd, kd, vd, causal, scale, o=o, lse=lse)
+    torch.cuda.synchronize()
+    assert attn.attn_check_device_status() == 0
+    if guard:
+        assert guards_intact(ob, og) and guards_intact(lb, lg), "write outside O/LSE"
+    o_ref, lse_ref = oracle_mod.attn_fwd(q, k, v, causal, scale)
+    return compare(o, lse, o_ref, lse_ref, dtype,
+                   "B%d Hq%d Hkv%d Nq%d Nk%d d%d causal%d" % (B, Hq, Hkv, Nq, Nk, d, causal))
+
+
+def test_single_head_bf16(attn, oracle_mod):
+    """B=1, H=1, N=256, d=64, non-causal, bf16."""
+    run_case(attn, oracle_mod, 1, 1, 1, 256, 256, 64, False, seed=0)
+
+
+def test_single_head_fp32(attn, oracle_mod):
+    """B=1, H=1, N=256, d=64, non-causal, fp32 (tolerance 1e-5)."""
+    run_case(attn, oracle_mod, 1, 1, 1, 256, 256, 64, False, seed=0, dtype=torch.float32)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_ragged_lengths(attn, oracle_mod, causal):
+    """B=8, Hq=Hkv=12, N=1000 (not a tile multiple), d=64."""
+    run_case(attn, oracle_mod, 8, 12, 12, 1000, 1000, 64, causal, seed=1)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_ragged_outlier(attn, oracle_mod, causal):
+    """Same shapes with Q scaled by 8: near one-hot softmax rows."""
+    run_case(attn, oracle_mod, 8, 12, 12, 1000, 1000, 64, causal, seed=1, q_scale=8.0)
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Nq,Nk,d,causal", [
+    (1, 1, 1, 1, 1, 64, False),          # a single key
+    (2, 4, 2, 129, 129, 128, True),      # just past one tile, GQA
+    (1, 2, 2, 257, 300, 128, False),     # just past one tile pair
+    (1, 8, 2, 300, 1000, 128, True),     # Nq < Nk: bottom-right causal
+    (1, 4, 4, 1000, 300, 64, True),      # Nq > Nk: leading rows have no key
+    (1, 2, 1, 1, 1000, 128, True),       # one query over 1000 keys (decode case)
+    (3, 6, 3, 777, 777, 128, True),
+    (2, 8, 8, 513, 2000, 64, False),
+])
+def test_shapes(attn, oracle_mod, B, Hq, Hkv, Nq, Nk, d, causal):
+    run_case(attn, oracle_mod, B, Hq, Hkv, Nq, Nk, d, causal, seed=Nq + Nk + d)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_fp32_shapes(attn, oracle_mod, d):
+    run_case(attn, oracle_mod, 2, 4, 2, 77, 150, d, True, seed=5, dtype=torch.float32)
+    run_case(attn, oracle_mod, 1, 2, 2, 150, 77, d, True, seed=6, dtype=torch.float32)
+
+
+def test_empty_key_set(attn):
+    """Nk = 0: every row is empty, O = 0 and LSE = -inf."""
+    q = torch.randn(2, 5, 4, 64, device=DEV).to(torch.bfloat16)
+    k = torch.empty(2, 0, 2, 64, device=DEV, dtype=torch.bfloat16)
+    o, lse = attn.attn_fwd(q, k, k.clone(), False, 0.125)
+    torch.cuda.synchronize()
+    assert torch.all(o == 0) and torch.all(lse == float("-inf"))
+
+
+def _sampled_full_size(attn, oracle_mod, B, Hq, Hkv, N, d, causal, seed, n_rows):
+    """Full-size run (the benchmark's launch configuration), checked on
+    sampled rows that the oracle computes one by one."""
+    q, k, v = make_qkv(B, Hq, Hkv, N, N, d, seed)
+    scale = 1.0 / math.sqrt(d)
+    o, lse = attn.attn_fwd(q.to(DEV), k.to(DEV), v.to(DEV), causal, scale)
+    torch.cuda.synchronize()
+    assert attn.attn_check_device_status() == 0
+    rows = sample_rows(B, Hq, N, n_rows, seed)
+    # tile edges: last row of the first tile, first row of the second pair
+    rows += [(0, 0, 127), (0, Hq - 1, 128), (B - 1, 0, 255), (B - 1, Hq - 1, 256)]
+    o_ref, lse_ref = oracle_mod.attn_rows(q, k, v, causal, scale, rows)
+    o_sel = torch.stack([o[b, i, h] for b, h, i in rows])
+    l_sel = torch.stack([lse[b, h, i] for b, h, i in rows])
+    compare(o_sel, l_sel, o_ref, lse_ref, torch.bfloat16, "full-size sampled")
+    lse_all = lse.float()
+    assert torch.isfinite(lse_all).all()
+
+
+def test_training_prefill_full_size(attn, oracle_mod):
+    """B=4, Hq=Hkv=16, N=4096, d=128, causal."""
+    _sampled_full_size(attn, oracle_mod, 4, 16, 16, 4096, 128, True, seed=2, n_rows=384)
+
+
+def test_long_sequence_gqa_full_size(attn, oracle_mod):
+    """B=1, Hq=32, Hkv=8, N=16384, d=128, causal."""
+    _sampled_full_size(attn, oracle_mod, 1, 32, 8, 16384, 128, True, seed=3, n_rows=192)
+
+
+def test_causal_tile_fraction(attn):
+    """Lecture 11 section 5.3: N=4096 with 128x128 tiles computes 0.516 of
+    the tiles under a causal mask (read from the kernel's tile counter)."""
+    with open(os.path.join(os.path.dirname(__file__), "golden", "causal_block_fraction.json")) as f:
+        g = json.load(f)
+    N = g["N"]
+    q, k, v = make_qkv(1, 1, 1, N, N, 128, seed=4)
+    q, k, v = q.to(DEV), k.to(DEV), v.to(DEV)
+    attn.attn_read_tile_counter(reset=True)
+    attn.attn_fwd(q, k, v, True, 0.1)
+    n = attn.attn_read_tile_counter(reset=True)
+    T = N // 128
+    assert n == T * (T + 1) // 2
+    assert round(n / (T * T), g["decimals"]) == g["fractions"]["128"]
+    attn.attn_fwd(q, k, v, False, 0.1)
+    assert attn.attn_read_tile_counter(reset=True) == T * T
+
+
+def test_p_through_shared_memory_variant(attn):
+    """The debugging variant that stages P in shared memory gives the same
+    answer as the tensor-memory variant (same oracle tolerance)."""
+    code = r"""
+import math, torch, sys
+sys.path.insert(0, %r); sys.path.insert(0, %r)
+import exact_attention_62_gb300 as attn, oracle
+from exact_attention_62_gb300.inputs import make_qkv
+from parity import compare
+for (B, H, N, d, c) in [(2, 3, 300, 64, True), (1, 2, 520, 128, True), (1, 2, 257, 128, False)]:
+    q, k, v = make_qkv(B, H, H, N, N, d, 9)
+    o, l = attn.attn_fwd(q.cuda(), k.cuda(), v.cuda(), c, 1 / math.sqrt(d))
+    torch.cuda.synchronize()
+    ro, rl = oracle.attn_fwd(q, k, v, c, 1 / math.sqrt(d))
+    compare(o, l, ro, rl, torch.bfloat16, "smem-P")
+assert attn.attn_check_device_status() == 0
+print("ok")
+""" % (os.path.dirname(os.path.dirname(os.path.abspath(__file__))), os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, ATTN_FWD_P_SMEM="1")
+    r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
+                       timeout=600)
+    assert r.returncode == 0 and "ok" in r.stdout, r.stdout + r.stderr
