@@ -1,0 +1,461 @@
+"""Benchmark: exact-attention forward TFLOP/s and flash-decoding GB/s on GB300.
+
+One step = one pass of the whole hot path over one batch of synthetic input:
+  prefill  attn_fwd   B=4, Hq=Hkv=16, Nq=Nk=4096, d=128, causal, bf16
+  decode   attn_decode_splitkv  B=1, Hq=32, Hkv=8, Nk=65536, d=128, bf16
+Inputs are resident in HBM when the timed region starts and are larger than
+L2; L2 is also flushed (256 MiB write) before every timed step, outside the
+events.  Each call is timed with CUDA events on the launching stream.
+
+value  = prefill TFLOP/s (FLOPs counted as 4 Nq Nk d per head, halved for
+         causal, summed over ranks) / max-over-ranks time.
+decode = GB/s of the decode call (K + V + Q + O + LSE bytes, each once).
+e2e    = the same metrics through the C ABI with pinned host buffers: the
+         host->device copy of the inputs and the device->host copy of O and
+         LSE are inside the timed region.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+For N > 1 run under torchrun; every rank runs an independent replica of the
+workload (weak scaling) and rank 0 prints the line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "attn fwd TFLOP/s & % of GB300 BF16 tensor peak; decode GB/s & % of HBM BW"
+
+# name -> (B, Hq, Hkv, Nq, Nk, d, causal)
+PREFILL = {
+    "single_head": (1, 1, 1, 256, 256, 64, False),
+    "ragged": (8, 12, 12, 1000, 1000, 64, False),
+    "ragged_causal": (8, 12, 12, 1000, 1000, 64, True),
+    "training_prefill": (4, 16, 16, 4096, 4096, 128, True),
+    "long_sequence": (1, 32, 8, 16384, 16384, 128, True),
+}
+DECODE = {
+    "decode_64k": (1, 32, 8, 65536, 128),
+    "decode_b16_8k": (16, 32, 8, 8192, 128),
+}
+
+# DRAM traffic of one forward launch from an ncu capture, keyed by the hash of
+# the kernel source it was measured on (any later change to the source turns
+# the figure into null).  Filled from profiles/ summaries.
+NCU_TRAFFIC = {}
+
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def prefill_flops(cfg) -> float:
+    B, Hq, Hkv, Nq, Nk, d, causal = cfg
+    f = 4.0 * Nq * Nk * d * B * Hq
+    return f / 2 if causal else f
+
+
+def decode_bytes(cfg) -> float:
+    B, Hq, Hkv, Nk, d = cfg
+    kv = 2.0 * B * Nk * Hkv * d * 2
+    return kv + 2.0 * B * Hq * d * 2 + B * Hq * 4
+
+
+def src_hash(name: str) -> str:
+    p = os.path.join(ROOT, "exact_attention_62_gb300", "csrc", name)
+    with open(p, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """Samples nvidia-smi clocks and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            import tempfile
+            fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+            os.close(fd)
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.out.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, val in zip(names, parts[5:9]):
+                    if val.lower() == "active":
+                        reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ----------------------------------------------------------------------------- reference arm
+
+_ORACLE_INPUTS = {}
+
+
+def oracle_prefill_sample(cfg, seconds: float, seed: int = 0):
+    """Times the oracle (as it stands) on random rows of the prefill workload
+    until `seconds` of wall time are used.  Returns (TFLOP/s, rows, cores)."""
+    import oracle
+    from exact_attention_62_gb300.inputs import make_qkv, sample_rows
+    B, Hq, Hkv, Nq, Nk, d, causal = cfg
+    key = (cfg, seed)
+    if key not in _ORACLE_INPUTS:
+        q, k, v = make_qkv(B, Hq, Hkv, Nq, Nk, d, seed)
+        _ORACLE_INPUTS[key] = (tuple(oracle._f32(x) for x in (q, k, v)),
+                               sample_rows(B, Hq, Nq, 1 << 20, seed + 1))
+    (qf, kf, vf), rows = _ORACLE_INPUTS[key]
+    per_row = prefill_flops(cfg) / (B * Hq * Nq)  # same counting as the GPU metric
+    done, t_used, chunk = 0, 0.0, 256
+    while t_used < seconds and done < len(rows):
+        sel = rows[done:done + chunk]
+        t0 = time.perf_counter()
+        oracle.attn_rows(qf, kf, vf, causal, 1.0 / math.sqrt(d), sel)
+        t_used += time.perf_counter() - t0
+        done += len(sel)
+        chunk = min(chunk * 2, 8192)
+    return done * per_row / t_used / 1e12, done, oracle.num_threads()
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    oracle.build()
+    cfg = PREFILL[args.prefill]
+    per_step = max(1.0, min(8.0, 150.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        oracle_prefill_sample(cfg, per_step / 4)
+    vals, rows_total, cores = [], 0, 1
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        v, rows, cores = oracle_prefill_sample(cfg, per_step)
+        vals.append(v)
+        rows_total += rows
+    wall = time.perf_counter() - t0
+    value = statistics.mean(vals)
+    B, Hq, Hkv, Nq, Nk, d, causal = cfg
+    sample = ("%d random rows (b, hq, i) of the %s workload per step, ~%.0f s of CPU work each; "
+              "FLOPs counted as for the GPU (4 Nk d per row, halved for causal)") % (
+        rows_total // max(1, args.steps), args.prefill, per_step)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1000.0 * wall / max(1, args.steps), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "%s B=%d Hq=%d Hkv=%d Nq=%d Nk=%d d=%d causal=%d (CPU oracle sample)"
+                               % (args.prefill, B, Hq, Hkv, Nq, Nk, d, causal)},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line))
+    return 0
+
+
+# ----------------------------------------------------------------------------- our arm
+
+def run_ours(args):
+    import torch
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import exact_attention_62_gb300 as attn
+    from exact_attention_62_gb300.inputs import make_qkv
+
+    attn.ensure_built()
+    do_pre = args.only in (None, "prefill")
+    do_dec = args.only in (None, "decode")
+    pcfg = PREFILL[args.prefill]
+    dcfg = DECODE[args.decode]
+    B, Hq, Hkv, Nq, Nk, d, causal = pcfg
+    dB, dHq, dHkv, dNk, dd = dcfg
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    if do_pre:
+        scale = 1.0 / math.sqrt(d)
+        qh, kh, vh = make_qkv(B, Hq, Hkv, Nq, Nk, d, seed=10 + rank)
+        q, k, v = qh.to(dev), kh.to(dev), vh.to(dev)
+        o = torch.empty_like(q)
+        lse = torch.empty((B, Hq, Nq), dtype=torch.float32, device=dev)
+    if do_dec:
+        dq_h, dk_h, dv_h = make_qkv(dB, dHq, dHkv, 1, dNk, dd, seed=20 + rank)
+        dq, dk, dv = dq_h.to(dev), dk_h.to(dev), dv_h.to(dev)
+        splits = attn.attn_decode_num_splits(dB, dHq, dHkv, dNk, dd)
+        if args.splits:
+            splits = args.splits
+        wbytes = attn.attn_decode_workspace_bytes(dB, dHq, dHkv, dNk, dd, splits)
+        ws = torch.empty(max(16, wbytes), dtype=torch.uint8, device=dev)
+        do = torch.empty_like(dq)
+        dlse = torch.empty((dB, dHq), dtype=torch.float32, device=dev)
+
+    def prefill():
+        if do_pre:
+            attn.attn_fwd(q, k, v, causal, scale, o=o, lse=lse)
+
+    def decode():
+        if do_dec:
+            attn.attn_decode_splitkv(dq, dk, dv, 1.0 / math.sqrt(dd), splits, workspace=ws,
+                                     o=do, lse=dlse)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        prefill()
+        decode()
+    torch.cuda.synchronize()
+    if attn.attn_check_device_status() != 0:
+        raise RuntimeError("device status reports a timed-out wait during warm-up")
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter()
+    for s in range(K):
+        flush.zero_()
+        ev[s][0].record(stream)
+        prefill()
+        ev[s][1].record(stream)
+        decode()
+        ev[s][2].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    t_wall = time.perf_counter() - t_wall
+    clk = clocks.stop()
+    if attn.attn_check_device_status() != 0:
+        raise RuntimeError("device status reports a timed-out wait")
+    pre_total = max_over_ranks(sum(ev[s][0].elapsed_time(ev[s][1]) for s in range(K)), world, dev)
+    dec_total = max_over_ranks(sum(ev[s][1].elapsed_time(ev[s][2]) for s in range(K)), world, dev)
+    peaks, peak_src = load_peaks()
+
+    if args.only is not None:
+        if rank == 0:
+            print(json.dumps({"profile_only": args.only, "prefill_ms": pre_total / K,
+                              "decode_ms": dec_total / K, "clocks": clk}))
+        return 0
+
+    # ---- end to end through the C ABI with pinned host buffers
+    e_pre_ms = e_dec_ms = None
+    if not args.no_e2e:
+        qh_p, kh_p, vh_p = qh.pin_memory(), kh.pin_memory(), vh.pin_memory()
+        o_h = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+        l_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+        dq_p, dk_p, dv_p = dq_h.pin_memory(), dk_h.pin_memory(), dv_h.pin_memory()
+        do_h = torch.empty(do.shape, dtype=do.dtype).pin_memory()
+        dl_h = torch.empty(dlse.shape, dtype=dlse.dtype).pin_memory()
+        e_pre, e_dec = [], []
+        for s in range(max(3, min(K, 10)) + 1):
+            flush.zero_()
+            e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+            e0.record(stream)
+            q.copy_(qh_p, non_blocking=True)
+            k.copy_(kh_p, non_blocking=True)
+            v.copy_(vh_p, non_blocking=True)
+            prefill()
+            o_h.copy_(o, non_blocking=True)
+            l_h.copy_(lse, non_blocking=True)
+            e1.record(stream)
+            dq.copy_(dq_p, non_blocking=True)
+            dk.copy_(dk_p, non_blocking=True)
+            dv.copy_(dv_p, non_blocking=True)
+            decode()
+            do_h.copy_(do, non_blocking=True)
+            dl_h.copy_(dlse, non_blocking=True)
+            e2.record(stream)
+            torch.cuda.synchronize()
+            if s > 0:  # the first pass warms the copy path
+                e_pre.append(e0.elapsed_time(e1))
+                e_dec.append(e1.elapsed_time(e2))
+        e_pre_ms = max_over_ranks(statistics.mean(e_pre), world, dev)
+        e_dec_ms = max_over_ranks(statistics.mean(e_dec), world, dev)
+
+    # ---- roofline of the forward kernel (the step's dominant kernel) and of decode
+    flops = prefill_flops(pcfg)
+    pre_ms_avg = pre_total / K
+    achieved = flops / (pre_ms_avg * 1e-3) / 1e12
+    peak_t = float(peaks["bf16_tflops"])
+    rec = NCU_TRAFFIC.get(args.prefill)
+    traffic = rec["bytes_per_launch"] if rec and rec.get("src_hash") == src_hash("fwd_tc.cu") else None
+    dbytes = decode_bytes(dcfg)
+    dec_ms_avg = dec_total / K
+    dec_gbs = dbytes / (dec_ms_avg * 1e-3) / 1e9
+    peak_h = float(peaks["hbm_gbs"])
+    drec = NCU_TRAFFIC.get(args.decode)
+    dtraffic = drec["bytes_per_launch"] if drec and drec.get("src_hash") == src_hash("decode.cu") else None
+
+    if rank != 0:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return 0
+    cpu = None
+    if not args.no_cpu_baseline:
+        v_cpu, rows, cores = oracle_prefill_sample(pcfg, args.cpu_seconds)
+        cpu = {"value": v_cpu, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+               "sample": "%d random rows of the %s workload (~%.0f s of CPU work), FLOPs counted "
+                         "as for the GPU (4 Nk d per row, halved for causal)"
+                         % (rows, args.prefill, args.cpu_seconds)}
+    launches_per_step = 1 + (1 if splits == 1 else 2)
+    h2d = sum(t.numel() * t.element_size() for t in (q, k, v))
+    d2h = o.numel() * o.element_size() + lse.numel() * lse.element_size()
+    dh2d = sum(t.numel() * t.element_size() for t in (dq, dk, dv))
+    dd2h = do.numel() * do.element_size() + dlse.numel() * dlse.element_size()
+    e2e = None
+    de2e = None
+    if e_pre_ms is not None:
+        e2e = {"value": flops / (e_pre_ms * 1e-3) / 1e12 * world, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+        de2e = {"value": dbytes / (e_dec_ms * 1e-3) / 1e9 * world, "unit": "GB/s",
+                "h2d_bytes_per_step": dh2d, "d2h_bytes_per_step": dd2h}
+    line = {
+        "metric": METRIC,
+        "value": achieved * world,
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": (pre_total + dec_total) / K,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {
+            "workload": "prefill %s + decode %s" % (args.prefill, args.decode),
+            "prefill": {"B": B, "Hq": Hq, "Hkv": Hkv, "Nq": Nq, "Nk": Nk, "d": d,
+                        "causal": bool(causal), "ms": pre_ms_avg},
+            "decode": {"B": dB, "Hq": dHq, "Hkv": dHkv, "Nk": dNk, "d": dd, "splits": splits,
+                       "ms": dec_ms_avg},
+            "l2": "inputs larger than L2 and L2 flushed (256 MiB write) before every timed step",
+            "parallelism": "independent replicas" if world > 1 else "single GPU",
+        },
+        "decode": {
+            "value": dec_gbs * world, "unit": "GB/s",
+            "roofline": {"bound": "hbm", "achieved": dec_gbs, "peak": peak_h, "unit": "GB/s",
+                         "frac": dec_gbs / peak_h, "traffic": dtraffic,
+                         "peak_source": "%s HBM copy" % peak_src},
+            "e2e": de2e,
+        },
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_t, "unit": "TFLOP/s",
+                     "frac": achieved / peak_t, "traffic": traffic,
+                     "peak_source": "%s bf16 burst" % peak_src},
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+        "clocks": clk,
+        "gpu_launches": K * launches_per_step,
+        "wall_s": t_wall,
+    }
+    print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--prefill", choices=sorted(PREFILL), default="training_prefill")
+    ap.add_argument("--decode", choices=sorted(DECODE), default="decode_64k")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", choices=["prefill", "decode"], default=None,
+                    help="time one half of the step only (for profiling; no JSON contract)")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer measurement")
+    ap.add_argument("--splits", type=int, default=0, help="decode segments (0 = automatic)")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())
