@@ -52,7 +52,12 @@ DECODE = {
 # DRAM traffic of one forward launch from an ncu capture, keyed by the hash of
 # the kernel source it was measured on (any later change to the source turns
 # the figure into null).  Filled from profiles/ summaries.
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    "training_prefill": {"bytes_per_launch": 580.6e6, "src_hash": "98c23f5d704b2c06",
+                         "profile": "profiles/fwd_tc_training_prefill.md"},
+    "decode_64k": {"bytes_per_launch": 275.2e6, "src_hash": "31e02a38a10a64b8",
+                   "profile": "profiles/decode_split_64k.md"},
+}
 
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -108,6 +113,10 @@ class ClockSampler:
                 stdout=self.out, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
+            return
+        t0 = time.time()  # wait for the first sample so the window is covered
+        while time.time() - t0 < 5.0 and os.path.getsize(self.path) == 0:
+            time.sleep(0.02)
 
     def stop(self):
         if self.proc is None:
@@ -291,6 +300,15 @@ def run_ours(args):
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
     clocks = ClockSampler(local)
     clocks.start()
+    # The timed region lasts milliseconds, shorter than nvidia-smi's sampling
+    # period, so the same step also runs untimed for ~0.5 s right before it:
+    # the clock samples cover that soak and the timed region.
+    t_soak = time.perf_counter()
+    while time.perf_counter() - t_soak < 0.5:
+        for _ in range(8):
+            prefill()
+            decode()
+        torch.cuda.synchronize()
     barrier(world)
     torch.cuda.synchronize()
     t_wall = time.perf_counter()
@@ -411,6 +429,8 @@ def run_ours(args):
                        "ms": dec_ms_avg},
             "l2": "inputs larger than L2 and L2 flushed (256 MiB write) before every timed step",
             "parallelism": "independent replicas" if world > 1 else "single GPU",
+            "clocks_window": "nvidia-smi every 100 ms over a 0.5 s untimed soak of the same "
+                             "step followed by the timed steps",
         },
         "decode": {
             "value": dec_gbs * world, "unit": "GB/s",

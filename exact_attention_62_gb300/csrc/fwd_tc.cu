@@ -28,7 +28,9 @@
 //    masks them only on tiles that need it (ragged tail, causal diagonal),
 //    applies the online update with exp2 (scale * log2 e folded in), writes
 //    P as bf16 (into TMEM over the consumed scores, or into shared memory),
-//    rescales its O row in TMEM when the running max grew, and at the end
+//    rescales its O row in TMEM only when the running max grew by more than a
+//    threshold (the conditional rescale of the FA4 section of the course
+//    index; exact, see below), and at the end
 //    writes O = acc / l through shared memory with a TMA store and LSE =
 //    m + ln l.
 //  * Key tiles that are fully masked by causality are never loaded or
@@ -63,6 +65,7 @@ struct FwdParams {
     int causal;
     int num_pairs;
     float scale_log2;
+    float rescale_thr;  // log2 units; 0 = rescale whenever the max grows
 };
 
 template <int D, bool P_TMEM>
@@ -313,9 +316,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mx0 = fmaxf(mx0, __uint_as_float(s[c]));
                 mx1 = fmaxf(mx1, __uint_as_float(s[c + 1]));
             }
-            const float m_new = fmaxf(m, fmaxf(mx0, mx1) * sl);
+            // Conditional rescale: the reference max moves only when the tile's max
+            // exceeds it by more than rescale_thr (log2 units).  acc and l always share
+            // the reference, so O = acc / l and LSE = m + log l stay exact; a stale
+            // reference only bounds P by 2^rescale_thr.
+            const float m_tile = fmaxf(mx0, mx1) * sl;
+            float m_new = m, alpha = 1.f;
+            if (m_tile > m + p.rescale_thr) {
+                m_new = m_tile;
+                alpha = ex2(m - m_new);  // 0 on the first non-empty tile
+            }
             const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-            const float alpha = ex2(m - m_use);
             float sum0 = 0.f, sum1 = 0.f;
             uint32_t pk[kBN / 2];
 #pragma unroll
@@ -410,6 +421,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
+// Threshold of the conditional rescale in log2 units.  8 keeps every P below
+// 256 (exact in bf16's range, no fp32 overflow risk in l or acc).
+// ATTN_FWD_RESCALE_THRESHOLD overrides it (0 = rescale on every max increase).
+float rescale_threshold() {
+    static const float v = [] {
+        const char* e = std::getenv("ATTN_FWD_RESCALE_THRESHOLD");
+        if (e == nullptr) return 8.0f;
+        const float x = std::strtof(e, nullptr);
+        return (x >= 0.f && x <= 16.f) ? x : 8.0f;
+    }();
+    return v;
+}
+
 template <int D, bool P_TMEM>
 attn_status_t launch_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                           int Hq, int Hkv, int Nq, int Nk, float scale, int causal,
@@ -441,6 +465,7 @@ attn_status_t launch_impl(const void* q, const void* k, const void* v, void* o, 
     prm.causal = causal;
     prm.num_pairs = (Nq + kQT * kBM - 1) / (kQT * kBM);
     prm.scale_log2 = scale * 1.4426950408889634f;
+    prm.rescale_thr = rescale_threshold();
     const long long grid = (long long)prm.num_pairs * B * Hq;
     if (grid > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
     fwd_tc_kernel<D, P_TMEM><<<(unsigned)grid, kThreads, L::kSmemBytes, stream>>>(mq, mk, mv, mo,

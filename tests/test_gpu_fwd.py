@@ -131,25 +131,29 @@ def test_causal_tile_fraction(attn):
     assert attn.attn_read_tile_counter(reset=True) == T * T
 
 
-def test_p_through_shared_memory_variant(attn):
-    """The debugging variant that stages P in shared memory gives the same
-    answer as the tensor-memory variant (same oracle tolerance)."""
+@pytest.mark.parametrize("env", [{"ATTN_FWD_P_SMEM": "1"}, {"ATTN_FWD_RESCALE_THRESHOLD": "0"}],
+                         ids=["p_in_smem", "rescale_every_growth"])
+def test_kernel_variants(attn, env):
+    """The debugging variant that stages P in shared memory, and the forward
+    with the conditional rescale switched off (rescale whenever the running
+    max grows), give the oracle's answer within the same tolerance."""
     code = r"""
 import math, torch, sys
 sys.path.insert(0, %r); sys.path.insert(0, %r)
 import exact_attention_62_gb300 as attn, oracle
 from exact_attention_62_gb300.inputs import make_qkv
 from parity import compare
-for (B, H, N, d, c) in [(2, 3, 300, 64, True), (1, 2, 520, 128, True), (1, 2, 257, 128, False)]:
-    q, k, v = make_qkv(B, H, H, N, N, d, 9)
+cases = [(2, 3, 300, 64, True, 1.0), (1, 2, 520, 128, True, 1.0), (1, 2, 257, 128, False, 1.0),
+         (1, 2, 700, 64, True, 8.0)]
+for (B, H, N, d, c, qs) in cases:
+    q, k, v = make_qkv(B, H, H, N, N, d, 9, q_scale=qs)
     o, l = attn.attn_fwd(q.cuda(), k.cuda(), v.cuda(), c, 1 / math.sqrt(d))
     torch.cuda.synchronize()
     ro, rl = oracle.attn_fwd(q, k, v, c, 1 / math.sqrt(d))
-    compare(o, l, ro, rl, torch.bfloat16, "smem-P")
+    compare(o, l, ro, rl, torch.bfloat16, "variant")
 assert attn.attn_check_device_status() == 0
 print("ok")
 """ % (os.path.dirname(os.path.dirname(os.path.abspath(__file__))), os.path.dirname(os.path.abspath(__file__)))
-    env = dict(os.environ, ATTN_FWD_P_SMEM="1")
-    r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
-                       timeout=600)
+    r = subprocess.run([sys.executable, "-c", code], env=dict(os.environ, **env),
+                       capture_output=True, text=True, timeout=600)
     assert r.returncode == 0 and "ok" in r.stdout, r.stdout + r.stderr
