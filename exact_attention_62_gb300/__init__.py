@@ -20,7 +20,7 @@ __all__ = [
     "attn_fwd", "attn_decode_num_splits", "attn_decode_workspace_bytes",
     "attn_decode_splitkv", "attn_merge_lse", "attn_status_string",
     "attn_check_device_status", "attn_read_tile_counter", "attn_version",
-    "EXPORTED_SYMBOLS",
+    "attn_decode_splitkv_static", "DECODE_STATIC_SCRATCH_BYTES", "EXPORTED_SYMBOLS",
 ]
 
 ATTN_OK, ATTN_ERR_INVALID, ATTN_ERR_UNSUPPORTED, ATTN_ERR_CUDA, ATTN_ERR_TIMEOUT = range(5)
@@ -31,7 +31,11 @@ EXPORTED_SYMBOLS = (
     "attn_fwd", "attn_decode_num_splits", "attn_decode_workspace_bytes",
     "attn_decode_splitkv", "attn_merge_lse", "attn_status_string",
     "attn_check_device_status", "attn_read_tile_counter", "attn_version",
+    "attn_decode_splitkv_static",
 )
+
+# Size of the scratch area built into the library for attn_decode_splitkv_static.
+DECODE_STATIC_SCRATCH_BYTES = 8 << 20
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_PKG, "libattn.so")
@@ -88,6 +92,8 @@ def lib() -> ctypes.CDLL:
     L.attn_read_tile_counter.restype = I
     L.attn_version.argtypes = []
     L.attn_version.restype = ctypes.c_char_p
+    L.attn_decode_splitkv_static.argtypes = [P, P, P, P, P, I, I, I, I, I, F, I, I, P]
+    L.attn_decode_splitkv_static.restype = I
     _lib = L
     return L
 
@@ -200,6 +206,38 @@ def attn_decode_splitkv(q, k_cache, v_cache, scale: float | None = None, num_spl
                                    B, Hq, Hkv, Nk, d, float(scale), int(num_splits),
                                    _ptr(workspace), wsize, _dtype_code(q), _stream(stream))
     _check("attn_decode_splitkv", st)
+    return o, lse
+
+
+def attn_decode_splitkv_static(q, k_cache, v_cache, scale: float | None = None,
+                               num_splits: int = 0, o=None, lse=None, stream=None):
+    """Flash-decoding for callers that cannot allocate device memory.
+
+    Same arguments and results as attn_decode_splitkv without the workspace:
+    the partials go to a fixed scratch area inside the library
+    (DECODE_STATIC_SCRATCH_BYTES, shared by every call).  Calls that overlap
+    on the GPU race on that area.  The output tensors are allocated here only
+    when not given; pass o and lse to allocate nothing at all.
+    """
+    import torch
+    B, one, Hq, d = q.shape
+    if one != 1:
+        raise ValueError("decode takes one query per sequence (q.shape[1] == 1)")
+    Bk, Nk, Hkv, dk = k_cache.shape
+    if Bk != B or dk != d or tuple(v_cache.shape) != tuple(k_cache.shape):
+        raise ValueError("shape mismatch")
+    for n, t in (("q", q), ("k_cache", k_cache), ("v_cache", v_cache)):
+        _need_cuda_contig(n, t)
+    if scale is None:
+        scale = d ** -0.5
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    st = lib().attn_decode_splitkv_static(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(o),
+                                          _ptr(lse), B, Hq, Hkv, Nk, d, float(scale),
+                                          int(num_splits), _dtype_code(q), _stream(stream))
+    _check("attn_decode_splitkv_static", st)
     return o, lse
 
 

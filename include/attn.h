@@ -134,6 +134,42 @@ attn_status_t attn_decode_splitkv(const void* q, const void* k_cache,
                                   attn_dtype_t dtype, void* stream);
 
 /*
+ * attn_decode_splitkv_static -- attn_decode_splitkv for callers that cannot
+ * allocate device memory.  The pages have no counterpart; this is a library
+ * convenience.
+ *
+ * Some callers cannot provide the decode workspace: code whose device memory
+ * is owned by a host framework's allocator (raw cudaMalloc not allowed), code
+ * whose memory budget is planned ahead of time, and latency-critical paths
+ * that must not call cudaMalloc/cudaFree (those calls can block or
+ * synchronise the device).  This entry point takes the same arguments as
+ * attn_decode_splitkv minus the workspace and computes the same result with
+ * the same kernels, using a scratch area built into the library: a
+ * file-scope device array of ATTN_DECODE_STATIC_SCRATCH_BYTES that every GPU
+ * on which the library is loaded keeps until the process exits.
+ *
+ *   - It allocates and frees nothing.
+ *   - Its first call on a device looks up the scratch area's device address
+ *     (cudaGetSymbolAddress, with that device current) and caches it; make
+ *     that first call before any stream capture.
+ *   - Sizes whose partials need more than ATTN_DECODE_STATIC_SCRATCH_BYTES
+ *     (see attn_decode_workspace_bytes) return ATTN_ERR_UNSUPPORTED and
+ *     launch nothing; use attn_decode_splitkv with a larger workspace instead.
+ *   - All calls share the one scratch area, which keeps the last call's
+ *     partials (nothing in it needs to start at zero: every partial is written
+ *     before it is read).  Calls whose kernels overlap on the GPU (different
+ *     streams, or concurrent host threads) race on it; calls ordered on one
+ *     stream do not.
+ * Other arguments, results and errors: as attn_decode_splitkv.
+ */
+#define ATTN_DECODE_STATIC_SCRATCH_BYTES (8u << 20)
+attn_status_t attn_decode_splitkv_static(const void* q, const void* k_cache,
+                                         const void* v_cache, void* o, float* lse,
+                                         int B, int Hq, int Hkv, int Nk, int d,
+                                         float scale, int num_splits,
+                                         attn_dtype_t dtype, void* stream);
+
+/*
  * attn_merge_lse -- exact merge of partial attention results in log-sum-exp
  * form ([L11] 6.2 step 3; the associative merge of [L11] 3.2):
  *     lse[r] = log sum_p exp(lse_parts[p, r])
