@@ -11,28 +11,31 @@
 // query-block-outer order of FlashAttention-2 (Lecture 11, section 4.2).
 //
 // How (GB300 design; the pages' FA2/FA3 kernels are prior art, not copied):
-//  * One CTA owns two 128-row query tiles of one (batch, head) -- 256 rows.
-//    Consecutive CTAs walk the heads of one batch, so the query heads of a
+//  * Persistent: one CTA per SM walks a static list of work units.  A unit
+//    is two 128-row query tiles (256 rows) of one (batch, head).  Units are
+//    ordered longest first for causal masks and dealt to the CTAs in snake
+//    order (c, 2G-1-c, 2G+c, ...), which balances the decreasing unit costs.
+//    Consecutive units walk the heads of one batch, so the query heads of a
 //    GQA group (which read the same K/V) run side by side and share L2.
-//    For causal masks the longest row blocks are scheduled first.
-//  * Warp 0 (one thread) is the TMA producer: both Q tiles once, then K_j
-//    and V_j into separate multi-stage rings (mbarrier full/empty pairs).
+//  * Warp 0 (one thread) is the TMA producer: each unit's Q tiles (as soon
+//    as the previous unit's last S has read the buffer), then K_j and V_j
+//    into separate multi-stage rings that run on across units.
 //  * Warp 1 (one thread) issues every tcgen05.mma: S_t = Q_t K_j^T into TMEM
 //    and O_t += P_t V_j into TMEM, and signals completion with
 //    tcgen05.commit.  Issue order  PV0(j), S0(j+1), PV1(j), S1(j+1)  lets the
 //    softmax of one query tile run while the tensor core works on the other
 //    (the ping-pong of the FA3 section of the course index, rebuilt around
-//    single-thread async MMA and TMEM accumulators).
-//  * Warps 2-5 and 6-9 are the softmax warpgroups of query tiles 0 and 1.
+//    single-thread async MMA and TMEM accumulators); the next unit's first
+//    two S products follow the current unit's last PV with no gap.
+//  * Warps 4-7 and 8-11 are the softmax warpgroups of query tiles 0 and 1.
 //    Each thread owns one row (one TMEM lane): it loads its 128 scores,
 //    masks them only on tiles that need it (ragged tail, causal diagonal),
 //    applies the online update with exp2 (scale * log2 e folded in), writes
-//    P as bf16 (into TMEM over the consumed scores, or into shared memory),
-//    rescales its O row in TMEM only when the running max grew by more than a
-//    threshold (the conditional rescale of the FA4 section of the course
-//    index; exact, see below), and at the end
-//    writes O = acc / l through shared memory with a TMA store and LSE =
-//    m + ln l.
+//    P as bf16 into TMEM over the consumed scores (or into shared memory in
+//    the debugging variant), rescales its O row in TMEM when the reference
+//    max moved, and at the end of a unit loads O, hands the TMEM columns back
+//    to the MMA warp at once, and stores O = acc / l and LSE = m + ln l
+//    straight to global memory.
 //  * Key tiles that are fully masked by causality are never loaded or
 //    computed (Lecture 11, section 5.3).
 #include <cstdio>
@@ -53,17 +56,29 @@ __device__ unsigned long long g_fwd_tiles = 0;
 
 constexpr int kBM = 128;        // query rows per tile (one TMEM lane each)
 constexpr int kBN = 128;        // keys per tile
-constexpr int kQT = 2;          // query tiles per CTA
-constexpr int kThreads = 320;   // 10 warps
+constexpr int kQT = 2;          // query tiles per unit
+// 12 warps: warpgroup 0 = producer (warp 0), MMA issuer (warp 1), two idle
+// warps; warpgroups 1 and 2 = softmax of query tiles 0 and 1.
+constexpr int kThreads = 384;
+// Register split.  The kernel is compiled for kLaunchRegs per thread (the
+// most 384 threads allow: each SM sub-partition holds three warps of 32 lanes
+// and 16384 registers).  Warpgroup 0 then gives registers back and the two
+// softmax warpgroups take them: 128 * kRegsWG0 + 256 * kRegsSoftmax must not
+// exceed 384 * kLaunchRegs (63488 <= 64512; per sub-partition 112 + 2 * 192 <= 512).
+constexpr int kLaunchRegs = 168;
+constexpr int kRegsWG0 = 112;
+constexpr int kRegsSoftmax = 192;
+static_assert(128 * kRegsWG0 + 256 * kRegsSoftmax <= kThreads * kLaunchRegs, "register split");
 constexpr int kPanelBytes = 128 * 128;  // 128 rows x 128 B: one 64-column swizzled panel
 constexpr float kLn2 = 0.69314718055994530942f;
 
 struct FwdParams {
     float* lse;
-    __nv_bfloat16* o;  // only for rows that have no allowed key
+    __nv_bfloat16* o;
     int B, Hq, Hkv, Nq, Nk, G;
     int causal;
     int num_pairs;
+    int num_units;
     float scale_log2;
     float rescale_thr;  // log2 units; 0 = rescale whenever the max grows
 };
@@ -82,15 +97,16 @@ struct Layout {
     static constexpr int kOffV = kOffK + kKSt * kKVBytes;
     static constexpr int kOffBar = kOffV + kVSt * kKVBytes;
     static constexpr int kBarQFull = 0;
-    static constexpr int kBarKFull = kBarQFull + kQT;
+    static constexpr int kBarQEmpty = kBarQFull + kQT;
+    static constexpr int kBarKFull = kBarQEmpty + kQT;
     static constexpr int kBarKEmpty = kBarKFull + kKSt;
     static constexpr int kBarVFull = kBarKEmpty + kKSt;
     static constexpr int kBarVEmpty = kBarVFull + kVSt;
     static constexpr int kBarSFull = kBarVEmpty + kVSt;
     static constexpr int kBarPFull = kBarSFull + kQT;
     static constexpr int kBarOFull = kBarPFull + kQT;
-    static constexpr int kBarStaged = kBarOFull + kQT;
-    static constexpr int kNumBars = kBarStaged + kQT;
+    static constexpr int kBarOEmpty = kBarOFull + kQT;
+    static constexpr int kNumBars = kBarOEmpty + kQT;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
     static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + slack to align the base
     // TMEM columns: S_0, S_1 (128 fp32 each; P_t overwrites the first 64 of
@@ -100,6 +116,17 @@ struct Layout {
     static constexpr uint32_t kTmemCols = 512;
     static_assert(256 + 2 * D <= 512, "TMEM budget");
     static_assert(kSmemBytes <= 232448, "shared memory budget");
+    // 128 threads arrive per phase on these; one arrival (expect_tx or commit) on the rest
+    __host__ __device__ static constexpr bool per_thread_bar(int i) {
+        return (i >= kBarPFull && i < kBarPFull + kQT) || (i >= kBarOEmpty && i < kBarOEmpty + kQT);
+    }
+};
+
+// One work unit: 256 query rows of one (batch, head) and the key-tile count
+// of each of its two 128-row tiles.
+struct Unit {
+    int b, hq, g, row0;
+    int n[kQT];
 };
 
 // Number of key tiles a 128-row query tile starting at row `rs` must visit.
@@ -111,11 +138,32 @@ __device__ __forceinline__ int kv_tiles_for(int rs, const FwdParams& p) {
     return last < 0 ? 0 : (int)(last / kBN) + 1;
 }
 
+// The k-th unit of this CTA (snake order over a longest-first list), or -1.
+__device__ __forceinline__ int unit_index(int k, const FwdParams& p) {
+    const int G = gridDim.x, c = blockIdx.x;
+    const long long u = (long long)k * G + ((k & 1) ? (G - 1 - c) : c);
+    return u < p.num_units ? (int)u : -1;
+}
+
+__device__ __forceinline__ Unit unit_at(int u, const FwdParams& p) {
+    const int BH = p.B * p.Hq;
+    const int bh = u % BH;
+    const int pr = u / BH;
+    const int pair = p.causal ? (p.num_pairs - 1 - pr) : pr;
+    Unit x;
+    x.hq = bh % p.Hq;
+    x.b = bh / p.Hq;
+    x.g = x.hq / p.G;
+    x.row0 = pair * (kQT * kBM);
+#pragma unroll
+    for (int t = 0; t < kQT; ++t) x.n[t] = kv_tiles_for(x.row0 + t * kBM, p);
+    return x;
+}
+
 template <int D, bool P_TMEM>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
-                  const FwdParams p) {
+                  const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
     using L = Layout<D, P_TMEM>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -127,27 +175,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(sgen + L::kOffMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sgen + L::kOffMisc + 4);
 
-    // ---- work unit: (pair of query tiles, head, batch)
-    const int BH = p.B * p.Hq;
-    const int bh = blockIdx.x % BH;
-    const int pr = blockIdx.x / BH;
-    const int pair = p.causal ? (p.num_pairs - 1 - pr) : pr;
-    const int hq = bh % p.Hq;
-    const int b = bh / p.Hq;
-    const int g = hq / p.G;
-    const int row0 = pair * (kQT * kBM);
-    int n_t[kQT];
-#pragma unroll
-    for (int t = 0; t < kQT; ++t) n_t[t] = kv_tiles_for(row0 + t * kBM, p);
-    const int n = max(n_t[0], n_t[1]);
-
     // ---- set-up: barriers, TMEM
     if (threadIdx.x == 0) {
-        for (int i = 0; i < L::kNumBars; ++i) {
-            const bool per_thread = (i >= L::kBarPFull && i < L::kBarPFull + kQT) ||
-                                    (i >= L::kBarStaged && i < L::kBarStaged + kQT);
-            mbar_init(bar(i), per_thread ? 128u : 1u);
-        }
+        for (int i = 0; i < L::kNumBars; ++i) mbar_init(bar(i), L::per_thread_bar(i) ? 128u : 1u);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -159,256 +189,324 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-
-    if (warp == 0) {
+    if (warp < 4) {
+      warpgroup_reg_dealloc<kRegsWG0>();
+      if (warp == 0) {
         // ================================================= TMA producer
         if (lane == 0) {
             prefetch_tmap(&tmQ);
             prefetch_tmap(&tmK);
             prefetch_tmap(&tmV);
-            prefetch_tmap(&tmO);
-            for (int t = 0; t < kQT; ++t) {
-                if (n_t[t] == 0) continue;
-                mbar_arrive_expect_tx(bar(L::kBarQFull + t), L::kQBytes);
-                for (int pp = 0; pp < L::kPanels; ++pp)
-                    tma_load_4d(sbase + L::kOffQ + t * L::kQBytes + pp * kPanelBytes, &tmQ,
-                                bar(L::kBarQFull + t), 64 * pp, hq, row0 + t * kBM, b);
-            }
-            for (int j = 0; j < n; ++j) {
-                const int ks = j % L::kKSt;
-                if (!mbar_wait(bar(L::kBarKEmpty + ks), ((j / L::kKSt) & 1) ^ 1, abort_flag,
-                               &g_fwd_status))
-                    break;
-                mbar_arrive_expect_tx(bar(L::kBarKFull + ks), L::kKVBytes);
-                for (int pp = 0; pp < L::kPanels; ++pp)
-                    tma_load_4d(sbase + L::kOffK + ks * L::kKVBytes + pp * kPanelBytes, &tmK,
-                                bar(L::kBarKFull + ks), 64 * pp, g, j * kBN, b);
-                const int vs = j % L::kVSt;
-                if (!mbar_wait(bar(L::kBarVEmpty + vs), ((j / L::kVSt) & 1) ^ 1, abort_flag,
-                               &g_fwd_status))
-                    break;
-                mbar_arrive_expect_tx(bar(L::kBarVFull + vs), L::kKVBytes);
-                for (int pp = 0; pp < L::kPanels; ++pp)
-                    tma_load_4d(sbase + L::kOffV + vs * L::kKVBytes + pp * kPanelBytes, &tmV,
-                                bar(L::kBarVFull + vs), 64 * pp, g, j * kBN, b);
+            int kv = 0;                 // key tiles loaded so far (ring position)
+            int q_loads[kQT] = {0, 0};  // Q_t loads so far
+            bool ok = true;
+            for (int k = 0; ok; ++k) {
+                const int u = unit_index(k, p);
+                if (u < 0) break;
+                const Unit x = unit_at(u, p);
+                for (int t = 0; t < kQT && ok; ++t) {
+                    if (x.n[t] == 0) continue;
+                    if (q_loads[t] > 0)  // the previous unit's last S_t has read Q_t
+                        ok = mbar_wait(bar(L::kBarQEmpty + t), (q_loads[t] - 1) & 1, abort_flag,
+                                       &g_fwd_status);
+                    if (!ok) break;
+                    mbar_arrive_expect_tx(bar(L::kBarQFull + t), L::kQBytes);
+                    for (int pp = 0; pp < L::kPanels; ++pp)
+                        tma_load_4d(sbase + L::kOffQ + t * L::kQBytes + pp * kPanelBytes, &tmQ,
+                                    bar(L::kBarQFull + t), 64 * pp, x.hq, x.row0 + t * kBM, x.b);
+                    ++q_loads[t];
+                }
+                const int n = max(x.n[0], x.n[1]);
+                for (int j = 0; j < n && ok; ++j, ++kv) {
+                    const int ks = kv % L::kKSt;
+                    ok = mbar_wait(bar(L::kBarKEmpty + ks), ((kv / L::kKSt) & 1) ^ 1, abort_flag,
+                                   &g_fwd_status);
+                    if (!ok) break;
+                    mbar_arrive_expect_tx(bar(L::kBarKFull + ks), L::kKVBytes);
+                    for (int pp = 0; pp < L::kPanels; ++pp)
+                        tma_load_4d(sbase + L::kOffK + ks * L::kKVBytes + pp * kPanelBytes, &tmK,
+                                    bar(L::kBarKFull + ks), 64 * pp, x.g, j * kBN, x.b);
+                    const int vs = kv % L::kVSt;
+                    ok = mbar_wait(bar(L::kBarVEmpty + vs), ((kv / L::kVSt) & 1) ^ 1, abort_flag,
+                                   &g_fwd_status);
+                    if (!ok) break;
+                    mbar_arrive_expect_tx(bar(L::kBarVFull + vs), L::kKVBytes);
+                    for (int pp = 0; pp < L::kPanels; ++pp)
+                        tma_load_4d(sbase + L::kOffV + vs * L::kKVBytes + pp * kPanelBytes, &tmV,
+                                    bar(L::kBarVFull + vs), 64 * pp, x.g, j * kBN, x.b);
+                }
             }
         }
-    } else if (warp == 1) {
+      } else if (warp == 1) {
         // ================================================= MMA issuer
         if (lane == 0) {
             constexpr uint32_t kIdS = idesc_bf16_f32(kBM, kBN, false);
             constexpr uint32_t kIdPV = idesc_bf16_f32(kBM, D, true);
             bool ok = true;
-            for (int t = 0; t < kQT; ++t)
-                if (n_t[t] > 0 && ok)
-                    ok = mbar_wait(bar(L::kBarQFull + t), 0, abort_flag, &g_fwd_status);
-            int k_ready = -1, v_ready = -1;
-            auto wait_k = [&](int j) {
-                if (ok && j > k_ready) {
-                    ok = mbar_wait(bar(L::kBarKFull + j % L::kKSt), (j / L::kKSt) & 1, abort_flag,
+            int kv = 0;                     // ring position of the unit's first key tile
+            int q_waits[kQT] = {0, 0};      // Q_t phases consumed
+            int p_waits[kQT] = {0, 0};      // P_t phases consumed
+            int units_t[kQT] = {0, 0};      // units in which tile t was active
+            unsigned long long tiles = 0;
+            for (int k = 0; ok; ++k) {
+                const int u = unit_index(k, p);
+                if (u < 0) break;
+                const Unit x = unit_at(u, p);
+                const int n = max(x.n[0], x.n[1]);
+                for (int t = 0; t < kQT && ok; ++t) {
+                    if (x.n[t] == 0) continue;
+                    ok = mbar_wait(bar(L::kBarQFull + t), q_waits[t] & 1, abort_flag,
                                    &g_fwd_status);
-                    tc_fence_after();
-                    k_ready = j;
+                    ++q_waits[t];
                 }
-            };
-            auto wait_v = [&](int j) {
-                if (ok && j > v_ready) {
-                    ok = mbar_wait(bar(L::kBarVFull + j % L::kVSt), (j / L::kVSt) & 1, abort_flag,
-                                   &g_fwd_status);
-                    tc_fence_after();
-                    v_ready = j;
-                }
-            };
-            // S_t = Q_t K_j^T  (M=128 rows, N=128 keys, K=D in steps of 16)
-            auto issue_s = [&](int t, int j) {
-                wait_k(j);
-                if (!ok) return;
-                const uint32_t qa = sbase + L::kOffQ + t * L::kQBytes;
-                const uint32_t ka = sbase + L::kOffK + (j % L::kKSt) * L::kKVBytes;
-                const uint32_t dS = tmem + L::tm_s(t);
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * kPanelBytes + (kk & 3) * 32;
-                    mma_ss(dS, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024),
-                           kIdS, kk > 0 ? 1u : 0u);
-                }
-                tc_commit(bar(L::kBarSFull + t));
-            };
-            // O_t += P_t V_j  (M=128 rows, N=D, K=128 keys in steps of 16)
-            auto issue_pv = [&](int t, int j) {
-                wait_v(j);
-                if (!ok) return;
-                ok = mbar_wait(bar(L::kBarPFull + t), j & 1, abort_flag, &g_fwd_status);
-                if (!ok) return;
-                tc_fence_after();
-                const uint32_t va = sbase + L::kOffV + (j % L::kVSt) * L::kKVBytes;
-                const uint32_t dO = tmem + L::tm_o(t);
-#pragma unroll
-                for (int kk = 0; kk < kBN / 16; ++kk) {
-                    // V is [keys][D] with D contiguous: an N-major B operand.  Along N the
-                    // 64-column panels are kPanelBytes apart (LBO); along K every 8 keys
-                    // are 1024 B apart (SBO).
-                    const uint64_t bd = sdesc_sw128(va + kk * 16 * 128, kPanelBytes, 1024);
-                    const uint32_t acc = (j > 0 || kk > 0) ? 1u : 0u;
-                    if constexpr (P_TMEM) {
-                        // bf16 P packed two per 32-bit column: 16 keys = 8 columns
-                        mma_ts(dO, tmem + L::tm_s(t) + kk * 8, bd, kIdPV, acc);
-                    } else {
-                        const uint32_t pa = sbase + L::kOffP + t * L::kPBytes;
-                        const uint32_t off = (kk >> 2) * kPanelBytes + (kk & 3) * 32;
-                        mma_ss(dO, sdesc_sw128(pa + off, 16, 1024), bd, kIdPV, acc);
+                int k_ready = -1, v_ready = -1;
+                auto wait_k = [&](int j) {
+                    if (ok && j > k_ready) {
+                        const int r = kv + j;
+                        ok = mbar_wait(bar(L::kBarKFull + r % L::kKSt), (r / L::kKSt) & 1,
+                                       abort_flag, &g_fwd_status);
+                        tc_fence_after();
+                        k_ready = j;
                     }
+                };
+                auto wait_v = [&](int j) {
+                    if (ok && j > v_ready) {
+                        const int r = kv + j;
+                        ok = mbar_wait(bar(L::kBarVFull + r % L::kVSt), (r / L::kVSt) & 1,
+                                       abort_flag, &g_fwd_status);
+                        tc_fence_after();
+                        v_ready = j;
+                    }
+                };
+                // S_t = Q_t K_j^T  (M=128 rows, N=128 keys, K=D in steps of 16)
+                auto issue_s = [&](int t, int j) {
+                    wait_k(j);
+                    if (!ok) return;
+                    const uint32_t qa = sbase + L::kOffQ + t * L::kQBytes;
+                    const uint32_t ka = sbase + L::kOffK + ((kv + j) % L::kKSt) * L::kKVBytes;
+                    const uint32_t dS = tmem + L::tm_s(t);
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off = (kk >> 2) * kPanelBytes + (kk & 3) * 32;
+                        mma_ss(dS, sdesc_sw128(qa + off, 16, 1024),
+                               sdesc_sw128(ka + off, 16, 1024), kIdS, kk > 0 ? 1u : 0u);
+                    }
+                    tc_commit(bar(L::kBarSFull + t));
+                    if (j == x.n[t] - 1) tc_commit(bar(L::kBarQEmpty + t));  // Q_t fully read
+                };
+                // O_t += P_t V_j  (M=128 rows, N=D, K=128 keys in steps of 16)
+                auto issue_pv = [&](int t, int j) {
+                    wait_v(j);
+                    if (!ok) return;
+                    ok = mbar_wait(bar(L::kBarPFull + t), p_waits[t] & 1, abort_flag,
+                                   &g_fwd_status);
+                    ++p_waits[t];
+                    if (ok && j == 0 && units_t[t] > 0)  // previous unit's epilogue read O_t
+                        ok = mbar_wait(bar(L::kBarOEmpty + t), (units_t[t] - 1) & 1, abort_flag,
+                                       &g_fwd_status);
+                    if (!ok) return;
+                    tc_fence_after();
+                    const uint32_t va = sbase + L::kOffV + ((kv + j) % L::kVSt) * L::kKVBytes;
+                    const uint32_t dO = tmem + L::tm_o(t);
+#pragma unroll
+                    for (int kk = 0; kk < kBN / 16; ++kk) {
+                        // V is [keys][D] with D contiguous: an N-major B operand.  Along N
+                        // the 64-column panels are kPanelBytes apart (LBO; one panel when
+                        // D = 64); along K every 8 keys are 1024 B apart (SBO).
+                        const uint64_t bd =
+                            sdesc_sw128(va + kk * 16 * 128, D == 128 ? kPanelBytes : 1024, 1024);
+                        const uint32_t acc = (j > 0 || kk > 0) ? 1u : 0u;
+                        if constexpr (P_TMEM) {
+                            // bf16 P packed two per 32-bit column: 16 keys = 8 columns
+                            mma_ts(dO, tmem + L::tm_s(t) + kk * 8, bd, kIdPV, acc);
+                        } else {
+                            const uint32_t pa = sbase + L::kOffP + t * L::kPBytes;
+                            const uint32_t off = (kk >> 2) * kPanelBytes + (kk & 3) * 32;
+                            mma_ss(dO, sdesc_sw128(pa + off, 16, 1024), bd, kIdPV, acc);
+                        }
+                    }
+                    if (j == x.n[t] - 1) {
+                        tc_commit(bar(L::kBarOFull + t));
+                        ++units_t[t];
+                    }
+                };
+                if (x.n[0] > 0) issue_s(0, 0);
+                if (x.n[1] > 0) issue_s(1, 0);
+                if (n > 0 && ok) tc_commit(bar(L::kBarKEmpty + kv % L::kKSt));
+                for (int j = 0; j < n && ok; ++j) {
+                    if (j < x.n[0]) issue_pv(0, j);
+                    if (j + 1 < x.n[0]) issue_s(0, j + 1);
+                    if (j < x.n[1]) issue_pv(1, j);
+                    if (ok) tc_commit(bar(L::kBarVEmpty + (kv + j) % L::kVSt));
+                    if (j + 1 < x.n[1]) issue_s(1, j + 1);
+                    if (j + 1 < n && ok) tc_commit(bar(L::kBarKEmpty + (kv + j + 1) % L::kKSt));
                 }
-                if (j == n_t[t] - 1) tc_commit(bar(L::kBarOFull + t));
-            };
-            if (n_t[0] > 0) issue_s(0, 0);
-            if (n_t[1] > 0) issue_s(1, 0);
-            if (n > 0 && ok) tc_commit(bar(L::kBarKEmpty + 0));
-            for (int j = 0; j < n && ok; ++j) {
-                if (j < n_t[0]) issue_pv(0, j);
-                if (j + 1 < n_t[0]) issue_s(0, j + 1);
-                if (j < n_t[1]) issue_pv(1, j);
-                if (ok) tc_commit(bar(L::kBarVEmpty + j % L::kVSt));
-                if (j + 1 < n_t[1]) issue_s(1, j + 1);
-                if (j + 1 < n && ok) tc_commit(bar(L::kBarKEmpty + (j + 1) % L::kKSt));
+                kv += n;
+                tiles += (unsigned long long)(x.n[0] + x.n[1]);
             }
-            if (ok) atomicAdd(&g_fwd_tiles, (unsigned long long)(n_t[0] + n_t[1]));
+            if (ok && tiles) atomicAdd(&g_fwd_tiles, tiles);
         }
+      }
     } else {
+        warpgroup_reg_alloc<kRegsSoftmax>();
         // ================================================= softmax warpgroups
-        const int t = (warp - 2) >> 2;
+        const int t = (warp - 4) >> 2;
         const int q4 = warp & 3;  // TMEM lane quarter this warp may access
         const int r = q4 * 32 + lane;
         const uint32_t lane_base = static_cast<uint32_t>(q4 * 32) << 16;
         const uint32_t tS = tmem + lane_base + L::tm_s(t);
         const uint32_t tO = tmem + lane_base + L::tm_o(t);
-        const int rs = row0 + t * kBM;
-        const int row = rs + r;
-        const int nt = n_t[t];
-        const long long diag = (long long)row + (p.Nk - p.Nq);  // last causal key of this row
-        const long long diag_tile = (long long)rs + (p.Nk - p.Nq);
         const float sl = p.scale_log2;
-        float m = -INFINITY, l = 0.f;
+        int s_waits = 0, o_waits = 0;
         bool ok = true;
-        for (int j = 0; j < nt; ++j) {
-            if (!mbar_wait(bar(L::kBarSFull + t), j & 1, abort_flag, &g_fwd_status)) {
+        for (int k = 0; ok; ++k) {
+            const int u = unit_index(k, p);
+            if (u < 0) break;
+            const Unit x = unit_at(u, p);
+            const int rs = x.row0 + t * kBM;
+            const int row = rs + r;
+            const int nt = x.n[t];
+            __nv_bfloat16* orow = p.o + (((long long)x.b * p.Nq + row) * p.Hq + x.hq) * D;
+            float* lse_out = p.lse + ((long long)x.b * p.Hq + x.hq) * p.Nq + row;
+            if (nt == 0) {
+                // Tile beyond Nq, or rows with no allowed key at all.
+                if (row < p.Nq) {
+                    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+                    for (int c = 0; c < D / 8; ++c) reinterpret_cast<uint4*>(orow)[c] = z;
+                    *lse_out = -INFINITY;
+                }
+                continue;
+            }
+            const long long diag = (long long)row + (p.Nk - p.Nq);  // last causal key of the row
+            const long long diag_tile = (long long)rs + (p.Nk - p.Nq);
+            float m = -INFINITY, l = 0.f;
+            for (int j = 0; j < nt; ++j) {
+                if (!mbar_wait(bar(L::kBarSFull + t), s_waits & 1, abort_flag, &g_fwd_status)) {
+                    ok = false;
+                    break;
+                }
+                ++s_waits;
+                tc_fence_after();
+                uint32_t s[kBN];
+                tmem_ld128_sync(tS, s);
+                const int col0 = j * kBN;
+                const bool need_mask = (col0 + kBN > p.Nk) ||
+                                       (p.causal && (long long)(col0 + kBN - 1) > diag_tile);
+                if (need_mask) {
+#pragma unroll
+                    for (int c = 0; c < kBN; ++c) {
+                        const int col = col0 + c;
+                        const bool keep = col < p.Nk && (!p.causal || (long long)col <= diag);
+                        if (!keep) s[c] = __float_as_uint(-INFINITY);
+                    }
+                }
+                // row max: 8 independent chains of three-input maxima
+                float mx[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    mx[i] = fmax3(__uint_as_float(s[i]), __uint_as_float(s[i + 8]),
+                                  __uint_as_float(s[i + 16]));
+#pragma unroll
+                    for (int c = 24; c < 120; c += 16)
+                        mx[i] = fmax3(mx[i], __uint_as_float(s[c + i]), __uint_as_float(s[c + 8 + i]));
+                    mx[i] = fmaxf(mx[i], __uint_as_float(s[120 + i]));
+                }
+                const float m_tile = fmaxf(fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]),
+                                                 mx[6]), mx[7]) * sl;
+                // The reference max moves only when the tile's max exceeds it by more
+                // than rescale_thr (log2 units; 0 = whenever it grows).  acc and l always
+                // share the reference, so O = acc / l and LSE = m + log l are exact for
+                // any threshold; a stale reference only bounds P by 2^rescale_thr.
+                float m_new = m, alpha = 1.f;
+                if (m_tile > m + p.rescale_thr) {
+                    m_new = m_tile;
+                    alpha = ex2(m - m_new);  // 0 on the first non-empty tile
+                }
+                const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+                // P = exp2(s * scale log2 e - m): the scale-subtract and the row sum run on
+                // packed fp32 pairs, exp2 on the MUFU unit.
+                const uint64_t sl2 = f2_pack(sl, sl);
+                const uint64_t nm2 = f2_pack(-m_use, -m_use);
+                uint64_t sum2[2] = {0ull, 0ull};
+                uint32_t pk[kBN / 2];
+#pragma unroll
+                for (int c = 0; c < kBN / 2; ++c) {
+                    const uint64_t x = f2_fma(f2_pack(__uint_as_float(s[2 * c]),
+                                                      __uint_as_float(s[2 * c + 1])), sl2, nm2);
+                    const float p0 = ex2(f2_lo(x));
+                    const float p1 = ex2(f2_hi(x));
+                    sum2[c & 1] = f2_add(sum2[c & 1], f2_pack(p0, p1));
+                    pk[c] = pack_bf16(p0, p1);
+                    if constexpr (P_TMEM) {
+                        if (c == 31) tmem_st32(tS, pk);  // first half out while computing the rest
+                    }
+                }
+                const uint64_t sum = f2_add(sum2[0], sum2[1]);
+                l = fmaf(l, alpha, f2_lo(sum) + f2_hi(sum));
+                if constexpr (P_TMEM) {
+                    tmem_st32(tS + 32, pk + 32);
+                } else {
+                    const uint32_t pa = sbase + L::kOffP + t * L::kPBytes;
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) {  // 16 chunks of 8 keys
+                        const int panel = c >> 3, cc = c & 7;
+                        st_shared_v4(pa + panel * kPanelBytes + r * 128 + ((cc ^ (r & 7)) << 4),
+                                     pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+                    }
+                    fence_proxy_async_smem();
+                }
+                // O_t holds the sum through key tile j-1 (its PV completed before S_t(j)
+                // did); bring it to the new reference if some row of the warp moved.
+                // One TMEM round trip, packed multiplies.
+                if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+                    uint32_t xo[D];
+                    if constexpr (D == 128)
+                        tmem_ld128_sync(tO, xo);
+                    else
+                        tmem_ld64_sync(tO, xo);
+                    const uint64_t a2 = f2_pack(alpha, alpha);
+#pragma unroll
+                    for (int i = 0; i < D / 2; ++i) {
+                        const uint64_t y = f2_mul(f2_pack(__uint_as_float(xo[2 * i]),
+                                                          __uint_as_float(xo[2 * i + 1])), a2);
+                        xo[2 * i] = __float_as_uint(f2_lo(y));
+                        xo[2 * i + 1] = __float_as_uint(f2_hi(y));
+                    }
+#pragma unroll
+                    for (int c = 0; c < D; c += 32) tmem_st32(tO + c, xo + c);
+                }
+                tmem_st_wait();  // P and any rescaled O are in TMEM before the MMA is told
+                tc_fence_before();
+                mbar_arrive(bar(L::kBarPFull + t));
+                m = m_new;
+            }
+            if (!ok) break;
+            // ---- epilogue: O = acc / l, LSE = m + ln l
+            if (!mbar_wait(bar(L::kBarOFull + t), o_waits & 1, abort_flag, &g_fwd_status)) {
                 ok = false;
                 break;
             }
+            ++o_waits;
             tc_fence_after();
-            uint32_t s[kBN];
-            tmem_ld64_sync(tS, s);
-            tmem_ld64_sync(tS + 64, s + 64);
-            const int col0 = j * kBN;
-            const bool need_mask = (col0 + kBN > p.Nk) ||
-                                   (p.causal && (long long)(col0 + kBN - 1) > diag_tile);
-            if (need_mask) {
-#pragma unroll
-                for (int c = 0; c < kBN; ++c) {
-                    const int col = col0 + c;
-                    const bool keep = col < p.Nk && (!p.causal || (long long)col <= diag);
-                    if (!keep) s[c] = __float_as_uint(-INFINITY);
-                }
-            }
-            float mx0 = -INFINITY, mx1 = -INFINITY;
-#pragma unroll
-            for (int c = 0; c < kBN; c += 2) {
-                mx0 = fmaxf(mx0, __uint_as_float(s[c]));
-                mx1 = fmaxf(mx1, __uint_as_float(s[c + 1]));
-            }
-            // Conditional rescale: the reference max moves only when the tile's max
-            // exceeds it by more than rescale_thr (log2 units).  acc and l always share
-            // the reference, so O = acc / l and LSE = m + log l stay exact; a stale
-            // reference only bounds P by 2^rescale_thr.
-            const float m_tile = fmaxf(mx0, mx1) * sl;
-            float m_new = m, alpha = 1.f;
-            if (m_tile > m + p.rescale_thr) {
-                m_new = m_tile;
-                alpha = ex2(m - m_new);  // 0 on the first non-empty tile
-            }
-            const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-            float sum0 = 0.f, sum1 = 0.f;
-            uint32_t pk[kBN / 2];
-#pragma unroll
-            for (int c = 0; c < kBN / 2; ++c) {
-                const float p0 = ex2(fmaf(__uint_as_float(s[2 * c]), sl, -m_use));
-                const float p1 = ex2(fmaf(__uint_as_float(s[2 * c + 1]), sl, -m_use));
-                sum0 += p0;
-                sum1 += p1;
-                pk[c] = pack_bf16(p0, p1);
-            }
-            l = fmaf(l, alpha, sum0 + sum1);
-            if constexpr (P_TMEM) {
-                tmem_st32(tS, pk);
-                tmem_st32(tS + 32, pk + 32);
-                tmem_st_wait();
-            } else {
-                const uint32_t pa = sbase + L::kOffP + t * L::kPBytes;
-#pragma unroll
-                for (int c = 0; c < 16; ++c) {  // 16 chunks of 8 keys
-                    const int panel = c >> 3, cc = c & 7;
-                    st_shared_v4(pa + panel * kPanelBytes + r * 128 + ((cc ^ (r & 7)) << 4),
-                                 pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-                }
-                fence_proxy_async_smem();
-            }
-            // Deferred normalisation: O_t still holds the sum through key tile j-1 (its PV
-            // completed before S_t(j) did); rescale it only when some row's max grew.
-            if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll 1
-                for (int c = 0; c < D; c += 32) {
-                    uint32_t x[32];
-                    tmem_ld32_sync(tO + c, x);
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) x[i] = __float_as_uint(__uint_as_float(x[i]) * alpha);
-                    tmem_st32(tO + c, x);
-                }
-                tmem_st_wait();
-            }
+            uint32_t xo[D];
+            tmem_ld64_sync(tO, xo);
+            if constexpr (D == 128) tmem_ld64_sync(tO + 64, xo + 64);
             tc_fence_before();
-            mbar_arrive(bar(L::kBarPFull + t));
-            m = m_new;
-        }
-        if (nt == 0) {
-            // Tile beyond Nq, or rows with no allowed key at all.
+            mbar_arrive(bar(L::kBarOEmpty + t));  // the next unit's PV may overwrite O_t now
             if (row < p.Nq) {
-                __nv_bfloat16* orow = p.o + (((long long)b * p.Nq + row) * p.Hq + hq) * D;
-                uint4 z = make_uint4(0u, 0u, 0u, 0u);
+                const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
-                for (int c = 0; c < D / 8; ++c) reinterpret_cast<uint4*>(orow)[c] = z;
-                p.lse[((long long)b * p.Hq + hq) * p.Nq + row] = -INFINITY;
-            }
-        } else if (ok && mbar_wait(bar(L::kBarOFull + t), 0, abort_flag, &g_fwd_status)) {
-            tc_fence_after();
-            const float inv = l > 0.f ? 1.f / l : 0.f;
-            const uint32_t stage = sbase + L::kOffQ + t * L::kQBytes;  // Q_t is no longer read
-#pragma unroll 1
-            for (int c = 0; c < D; c += 32) {
-                uint32_t x[32];
-                tmem_ld32_sync(tO + c, x);
-                uint32_t h[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    h[i] = pack_bf16(__uint_as_float(x[2 * i]) * inv,
-                                     __uint_as_float(x[2 * i + 1]) * inv);
-                const int panel = c >> 6;
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int cc = ((c & 63) >> 3) + i;
-                    st_shared_v4(stage + panel * kPanelBytes + r * 128 + ((cc ^ (r & 7)) << 4),
-                                 h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]);
+                for (int c = 0; c < D / 8; ++c) {
+                    uint4 w;
+                    w.x = pack_bf16(__uint_as_float(xo[8 * c + 0]) * inv, __uint_as_float(xo[8 * c + 1]) * inv);
+                    w.y = pack_bf16(__uint_as_float(xo[8 * c + 2]) * inv, __uint_as_float(xo[8 * c + 3]) * inv);
+                    w.z = pack_bf16(__uint_as_float(xo[8 * c + 4]) * inv, __uint_as_float(xo[8 * c + 5]) * inv);
+                    w.w = pack_bf16(__uint_as_float(xo[8 * c + 6]) * inv, __uint_as_float(xo[8 * c + 7]) * inv);
+                    reinterpret_cast<uint4*>(orow)[c] = w;
                 }
+                *lse_out = l > 0.f ? (m + lg2(l)) * kLn2 : -INFINITY;
             }
-            fence_proxy_async_smem();
-            mbar_arrive(bar(L::kBarStaged + t));
-            if (r == 0 && mbar_wait(bar(L::kBarStaged + t), 0, abort_flag, &g_fwd_status)) {
-                for (int pp = 0; pp < L::kPanels; ++pp)
-                    tma_store_4d(&tmO, stage + pp * kPanelBytes, 64 * pp, hq, rs, b);
-                tma_store_commit_and_wait_all();
-            }
-            if (row < p.Nq)
-                p.lse[((long long)b * p.Hq + hq) * p.Nq + row] =
-                    l > 0.f ? (m + lg2(l)) * kLn2 : -INFINITY;
         }
     }
 
@@ -421,15 +519,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-// Threshold of the conditional rescale in log2 units.  8 keeps every P below
-// 256 (exact in bf16's range, no fp32 overflow risk in l or acc).
-// ATTN_FWD_RESCALE_THRESHOLD overrides it (0 = rescale on every max increase).
+// Threshold of the conditional rescale in log2 units.  0 (the default) moves
+// the reference max whenever it grows, which keeps the dominant P entry of a
+// near one-hot row at exactly 1 so bf16 rounding of P adds no error there;
+// up to 8 keeps every P below 256.  ATTN_FWD_RESCALE_THRESHOLD overrides it.
 float rescale_threshold() {
     static const float v = [] {
         const char* e = std::getenv("ATTN_FWD_RESCALE_THRESHOLD");
-        if (e == nullptr) return 8.0f;
+        if (e == nullptr) return 0.0f;
         const float x = std::strtof(e, nullptr);
-        return (x >= 0.f && x <= 16.f) ? x : 8.0f;
+        return (x >= 0.f && x <= 8.f) ? x : 0.0f;
     }();
     return v;
 }
@@ -439,11 +538,10 @@ attn_status_t launch_impl(const void* q, const void* k, const void* v, void* o, 
                           int Hq, int Hkv, int Nq, int Nk, float scale, int causal,
                           cudaStream_t stream) {
     using L = Layout<D, P_TMEM>;
-    CUtensorMap mq, mk, mv, mo;
+    CUtensorMap mq, mk, mv;
     if (!attn_host::encode_bshd_map(&mq, q, B, Nq, Hq, D, kBM, 2) ||
         !attn_host::encode_bshd_map(&mk, k, B, Nk, Hkv, D, kBN, 2) ||
-        !attn_host::encode_bshd_map(&mv, v, B, Nk, Hkv, D, kBN, 2) ||
-        !attn_host::encode_bshd_map(&mo, o, B, Nq, Hq, D, kBM, 2))
+        !attn_host::encode_bshd_map(&mv, v, B, Nk, Hkv, D, kBN, 2))
         return ATTN_ERR_CUDA;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
@@ -453,6 +551,15 @@ attn_status_t launch_impl(const void* q, const void* k, const void* v, void* o, 
                                         L::kSmemBytes);
     });
     if (attr_err != cudaSuccess) return ATTN_ERR_CUDA;
+    // The register split inside the kernel assumes exactly kLaunchRegs per
+    // thread at launch; refuse to launch a build that differs.
+    static int num_regs = -1;
+    if (num_regs < 0) {
+        cudaFuncAttributes fa;
+        if (cudaFuncGetAttributes(&fa, fwd_tc_kernel<D, P_TMEM>) != cudaSuccess) return ATTN_ERR_CUDA;
+        num_regs = fa.numRegs;
+    }
+    if (num_regs != kLaunchRegs) return ATTN_ERR_UNSUPPORTED;
     FwdParams prm;
     prm.lse = lse;
     prm.o = static_cast<__nv_bfloat16*>(o);
@@ -464,12 +571,15 @@ attn_status_t launch_impl(const void* q, const void* k, const void* v, void* o, 
     prm.G = Hq / Hkv;
     prm.causal = causal;
     prm.num_pairs = (Nq + kQT * kBM - 1) / (kQT * kBM);
+    const long long units = (long long)prm.num_pairs * B * Hq;
+    if (units > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
+    prm.num_units = (int)units;
     prm.scale_log2 = scale * 1.4426950408889634f;
     prm.rescale_thr = rescale_threshold();
-    const long long grid = (long long)prm.num_pairs * B * Hq;
-    if (grid > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
-    fwd_tc_kernel<D, P_TMEM><<<(unsigned)grid, kThreads, L::kSmemBytes, stream>>>(mq, mk, mv, mo,
-                                                                                  prm);
+    const int sms = attn_host::device_sm_count();
+    if (sms <= 0) return ATTN_ERR_CUDA;
+    const int grid = (int)(units < sms ? units : sms);
+    fwd_tc_kernel<D, P_TMEM><<<grid, kThreads, L::kSmemBytes, stream>>>(mq, mk, mv, prm);
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
