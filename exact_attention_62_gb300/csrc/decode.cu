@@ -15,7 +15,8 @@
 //    for the whole group (section 6.2, GQA paragraph).
 //  * Warp 0 streams the segment's K and V tiles (64 keys each) with TMA into
 //    a multi-stage shared-memory ring (128-byte swizzle, mbarrier full/empty
-//    pairs); four consumer warps each take 16 keys of every tile.
+//    pairs).  Two groups of four consumer warps take alternate tiles, and the
+//    four warps of a group each take 16 keys of the tile.
 //  * The consumer work per tile is two tiny matrix products done with warp
 //    MMA (m16n8k16, bf16 in, fp32 accumulate): S^T = K Q^T with the keys as
 //    the 16 rows and up to 8 query heads as the columns, then
@@ -24,7 +25,7 @@
 //    registers; the running max is kept in base-2 units (scale log2 e
 //    folded in).  The kernel is HBM-bound; the tensor-core products just keep
 //    the instruction count far below the memory time.
-//  * At the end the four warps' states are merged through shared memory
+//  * At the end the eight warps' states are merged through shared memory
 //    (the same (m, l, acc) merge).  With a single segment the kernel writes
 //    O (bf16) and LSE directly and no merge kernel runs.
 #include <algorithm>
@@ -41,7 +42,10 @@ namespace {
 __device__ unsigned g_dec_status = 0;
 
 constexpr int kTileKeys = 64;
-constexpr int kConsumerWarps = 4;
+// Consumer warps come in groups of four; group i takes the tiles t with
+// t % kGroups == i, so kGroups tiles are consumed at once.
+constexpr int kGroups = 2;
+constexpr int kConsumerWarps = 4 * kGroups;
 constexpr int kDecThreads = 32 * (1 + kConsumerWarps);
 constexpr float kLn2 = 0.69314718055994530942f;
 
@@ -68,10 +72,15 @@ struct DecLayout {
     // stage buffers once every tile has been consumed.
     static constexpr int kRedStride = D + 2;
     static_assert(kConsumerWarps * 8 * kRedStride * 4 <= STAGES * kStageBytes, "merge scratch");
+    // Tiles t and t + STAGES share a stage.  Only if they belong to the same
+    // consumer group does program order keep that group at most one phase
+    // ahead of the stage's barriers; otherwise a parity wait can be satisfied
+    // by the phase before the awaited one.
+    static_assert(STAGES % kGroups == 0, "each ring stage must belong to one consumer group");
 };
 
 template <int D>
-constexpr int dec_stages() { return D == 128 ? 3 : 6; }
+constexpr int dec_stages() { return D == 128 ? 6 : 8; }
 
 __device__ __forceinline__ uint32_t ld_b32(const __nv_bfloat16* p) {
     return *reinterpret_cast<const uint32_t*>(p);
@@ -114,7 +123,7 @@ __global__ void __launch_bounds__(kDecThreads)
     if (threadIdx.x == 0) {
         for (int st = 0; st < STAGES; ++st) {
             mbar_init(full_bar(st), 1);
-            mbar_init(empty_bar(st), kConsumerWarps);
+            mbar_init(empty_bar(st), 4);  // the four warps of the group that read it
         }
         *abort_flag = 0;
         fence_barrier_init();
@@ -146,6 +155,8 @@ __global__ void __launch_bounds__(kDecThreads)
 
     // ===================================================== consumers
     const int cw = warp - 1;
+    const int grp = cw >> 2;  // which tiles: t % kGroups == grp
+    const int kw = cw & 3;    // which 16 keys of those tiles
     const int g8 = lane >> 2;  // fragment row group
     const int t4 = lane & 3;   // fragment column pair
     const int mi = lane >> 3;  // ldmatrix: which 8x8 matrix this lane addresses
@@ -168,17 +179,18 @@ __global__ void __launch_bounds__(kDecThreads)
     // online-softmax state of this lane's two query columns (2 t4, 2 t4 + 1)
     float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.f, l_b = 0.f;
     const float sl = p.scale_log2;
-    const int kkey = 16 * cw + rr + 8 * (mi & 1);  // K row this lane addresses
-    const int vkey = 16 * cw + rr + 8 * (mi >> 1); // V row this lane addresses
+    const int kkey = 16 * kw + rr + 8 * (mi & 1);  // K row this lane addresses
+    const int vkey = 16 * kw + rr + 8 * (mi >> 1); // V row this lane addresses
 
-    for (int t = 0; t < ntiles; ++t) {
+    for (int t = grp; t < ntiles; t += kGroups) {
         const int st = t % STAGES;
         if (!mbar_wait(full_bar(st), (t / STAGES) & 1, abort_flag, &g_dec_status)) break;
         const uint32_t kb = sbase + st * L::kStageBytes;
         const uint32_t vb = kb + L::kTileBytes;
 
-        // S^T (16 keys x 8 query columns) = K (16 x D) Q^T (D x 8)
-        float c[4] = {0.f, 0.f, 0.f, 0.f};
+        // S^T (16 keys x 8 query columns) = K (16 x D) Q^T (D x 8); even and odd
+        // k-steps accumulate separately to halve the dependent MMA chain.
+        float ce[4] = {0.f, 0.f, 0.f, 0.f}, co[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
             const int ch = 2 * kk + (mi >> 1);
@@ -186,10 +198,14 @@ __global__ void __launch_bounds__(kDecThreads)
                 kb + (ch >> 3) * L::kPanelBytes + kkey * 128 + (((ch & 7) ^ (kkey & 7)) << 4);
             uint32_t a[4];
             ldsm_x4(addr, a);
-            mma_16816(c, a, qb[kk][0], qb[kk][1]);
+            if (kk & 1)
+                mma_16816(co, a, qb[kk][0], qb[kk][1]);
+            else
+                mma_16816(ce, a, qb[kk][0], qb[kk][1]);
         }
+        const float c[4] = {ce[0] + co[0], ce[1] + co[1], ce[2] + co[2], ce[3] + co[3]};
         // keys of this lane: rows g8 and g8 + 8 of the warp's 16
-        const int key = j0 + t * kTileKeys + 16 * cw + g8;
+        const int key = j0 + t * kTileKeys + 16 * kw + g8;
         const bool in0 = key < j1, in1 = key + 8 < j1;
         const float x0 = in0 ? c[0] * sl : -INFINITY;  // (key,   col 2t4)
         const float x1 = in0 ? c[1] * sl : -INFINITY;  // (key,   col 2t4+1)
@@ -235,6 +251,9 @@ __global__ void __launch_bounds__(kDecThreads)
         if (lane == 0) mbar_arrive(empty_bar(st));
     }
 
+    // The merge kernel (launched as a programmatic dependent) may start now;
+    // it waits for this grid's completion before reading any partial.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     // per-warp partial sums of l over the warp's keys
 #pragma unroll
     for (int off = 4; off < 32; off <<= 1) {
@@ -292,51 +311,100 @@ __global__ void __launch_bounds__(kDecThreads)
     }
 }
 
-// One warp per row: lse = M + log sum_s exp(lse_s - M), o = sum_s exp(lse_s - lse) o_s.
+// lse = M + log sum_s exp(lse_s - M), o = sum_s exp(lse_s - lse) o_s, one CTA
+// per row.  The merge sits between two HBM-bound launches and moves a few
+// hundred KB, so its cost is round trips, not bytes: every load of a pass is
+// independent.  Pass 1 reads all P lse_s at once (one per thread) and reduces
+// max and sum across the CTA; pass 2 spreads (segment, 4-column group) pairs
+// over the threads, so the P x d/4 partial loads are issued together, and the
+// per-segment sums are reduced through shared memory.
+constexpr int kMergeThreads = 256;
+constexpr int kMergeChunk = 1024;  // segment weights staged in shared memory per pass
+
+__device__ __forceinline__ float block_reduce(float x, bool is_max, float* red) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const float y = __shfl_xor_sync(0xffffffffu, x, off);
+        x = is_max ? fmaxf(x, y) : x + y;
+    }
+    __syncthreads();  // red may still be read from a previous reduction
+    if (lane == 0) red[w] = x;
+    __syncthreads();
+    x = red[0];
+#pragma unroll
+    for (int i = 1; i < kMergeThreads / 32; ++i) x = is_max ? fmaxf(x, red[i]) : x + red[i];
+    return x;
+}
+
 template <bool OUT_BF16>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(kMergeThreads)
     merge_lse_kernel(const float* __restrict__ o_parts, const float* __restrict__ lse_parts, int P,
                      long long rows, int d, void* __restrict__ o, float* __restrict__ lse) {
-    const long long row = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
-    if (row >= rows) return;
+    __shared__ float red[kMergeThreads / 32];
+    __shared__ float wts[kMergeChunk];
+    __shared__ float4 part[kMergeThreads];
+    // Launched as a programmatic dependent of the split kernel: wait until that
+    // grid has completed and its partials are visible (a no-op otherwise).
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const long long row = blockIdx.x;
+    const int tid = threadIdx.x;
     float M = -INFINITY;
-    for (int s = lane; s < P; s += 32) M = fmaxf(M, lse_parts[(long long)s * rows + row]);
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    for (int s = tid; s < P; s += kMergeThreads) M = fmaxf(M, lse_parts[(long long)s * rows + row]);
+    M = block_reduce(M, true, red);
     float Lr = -INFINITY;
-    if (M != -INFINITY) {
+    if (M != -INFINITY) {  // uniform across the CTA
         float sum = 0.f;
-        for (int s = lane; s < P; s += 32) sum += expf(lse_parts[(long long)s * rows + row] - M);
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-        Lr = M + logf(sum);
+        for (int s = tid; s < P; s += kMergeThreads) sum += expf(lse_parts[(long long)s * rows + row] - M);
+        Lr = M + logf(block_reduce(sum, false, red));
     }
-    for (int c4 = lane; 4 * c4 < d; c4 += 32) {
-        float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (Lr != -INFINITY) {
-            for (int s = 0; s < P; ++s) {
-                const float ls = lse_parts[(long long)s * rows + row];
-                if (ls == -INFINITY) continue;
-                const float w = expf(ls - Lr);
-                const float4 x =
-                    *reinterpret_cast<const float4*>(o_parts + ((long long)s * rows + row) * d + 4 * c4);
-                a.x = fmaf(w, x.x, a.x);
-                a.y = fmaf(w, x.y, a.y);
-                a.z = fmaf(w, x.z, a.z);
-                a.w = fmaf(w, x.w, a.w);
+    const int C = d >> 2;               // 4-column groups, 1..128
+    const int SL = kMergeThreads / C;   // segment lanes, >= 2
+    const int c4 = tid % C, sl = tid / C;
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (Lr != -INFINITY) {
+        for (int s0 = 0; s0 < P; s0 += kMergeChunk) {
+            const int n = min(kMergeChunk, P - s0);
+            __syncthreads();  // wts of the previous chunk fully consumed
+            for (int i = tid; i < n; i += kMergeThreads) {
+                const float ls = lse_parts[(long long)(s0 + i) * rows + row];
+                wts[i] = ls == -INFINITY ? 0.f : expf(ls - Lr);
             }
+            __syncthreads();
+            if (sl < SL) {
+#pragma unroll 4
+                for (int i = sl; i < n; i += SL) {
+                    const float w = wts[i];
+                    const float4 x = *reinterpret_cast<const float4*>(
+                        o_parts + ((long long)(s0 + i) * rows + row) * d + 4 * c4);
+                    a.x = fmaf(w, x.x, a.x);
+                    a.y = fmaf(w, x.y, a.y);
+                    a.z = fmaf(w, x.z, a.z);
+                    a.w = fmaf(w, x.w, a.w);
+                }
+            }
+        }
+    }
+    part[tid] = a;
+    __syncthreads();
+    if (tid < C) {
+        for (int j = 1; j < SL; ++j) {
+            const float4 x = part[j * C + tid];
+            a.x += x.x;
+            a.y += x.y;
+            a.z += x.z;
+            a.w += x.w;
         }
         if constexpr (OUT_BF16) {
             uint2 h;
             h.x = pack_bf16(a.x, a.y);
             h.y = pack_bf16(a.z, a.w);
-            *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(o) + row * d + 4 * c4) = h;
+            *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(o) + row * d + 4 * tid) = h;
         } else {
-            *reinterpret_cast<float4*>(static_cast<float*>(o) + row * d + 4 * c4) = a;
+            *reinterpret_cast<float4*>(static_cast<float*>(o) + row * d + 4 * tid) = a;
         }
     }
-    if (lane == 0 && lse != nullptr) lse[row] = Lr;
+    if (tid == 0 && lse != nullptr) lse[row] = Lr;
 }
 
 int group_cols(int G) {
@@ -477,16 +545,25 @@ attn_status_t launch_merge(const float* o_parts, const float* lse_parts, int par
                            long long rows, int d, void* o, float* lse, bool out_bf16,
                            cudaStream_t stream) {
     if (rows == 0) return ATTN_OK;
-    const int rows_per_block = 8;
-    const long long blocks = (rows + rows_per_block - 1) / rows_per_block;
-    if (blocks > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
-    if (out_bf16)
-        merge_lse_kernel<true><<<(unsigned)blocks, 32 * rows_per_block, 0, stream>>>(
-            o_parts, lse_parts, parts, rows, d, o, lse);
-    else
-        merge_lse_kernel<false><<<(unsigned)blocks, 32 * rows_per_block, 0, stream>>>(
-            o_parts, lse_parts, parts, rows, d, o, lse);
-    return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+    if (rows > 0x7fffffffLL || d < 4 || d > 4 * kMergeThreads / 2 || d % 4 != 0)
+        return ATTN_ERR_UNSUPPORTED;
+    const long long blocks = rows;
+    // Programmatic dependent launch: the merge grid is scheduled while the
+    // previous kernel on the stream drains, instead of after a full launch gap.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)blocks);
+    cfg.blockDim = dim3(kMergeThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e =
+        out_bf16 ? cudaLaunchKernelEx(&cfg, merge_lse_kernel<true>, o_parts, lse_parts, parts, rows, d, o, lse)
+                 : cudaLaunchKernelEx(&cfg, merge_lse_kernel<false>, o_parts, lse_parts, parts, rows, d, o, lse);
+    return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
 cudaError_t decode_read_status(unsigned* out, bool clear) {

@@ -93,7 +93,11 @@ def test_decode_empty_cache(attn):
 
 @pytest.mark.parametrize("P,rows,d,out", [(1, 5, 64, torch.float32), (12, 300, 128, torch.float32),
                                           (7, 1000, 128, torch.bfloat16), (40, 33, 4, torch.float32),
-                                          (3, 17, 512, torch.bfloat16)])
+                                          (3, 17, 512, torch.bfloat16),
+                                          # more parts than one staged chunk of weights
+                                          (2500, 3, 128, torch.float32), (1025, 4, 64, torch.bfloat16),
+                                          # 4-column groups that do not divide the thread count
+                                          (9, 6, 12, torch.float32), (33, 5, 20, torch.bfloat16)])
 def test_merge_lse(attn, oracle_mod, P, rows, d, out):
     """attn_merge_lse against the oracle's log-sum-exp merge, with some empty
     parts and some rows whose parts are all empty."""
