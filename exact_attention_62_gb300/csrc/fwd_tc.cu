@@ -20,9 +20,9 @@
 //  * Warp 0 (one thread) is the TMA producer: each unit's Q tiles (as soon
 //    as the previous unit's last S has read the buffer), then K_j and V_j
 //    into separate multi-stage rings that run on across units.
-//  * Warp 1 (one thread) issues every tcgen05.mma: S_t = Q_t K_j^T into TMEM
-//    and O_t += P_t V_j into TMEM, and signals completion with
-//    tcgen05.commit.  Issue order  PV0(j), S0(j+1), PV1(j), S1(j+1)  lets the
+//  * Warp 1 issues every tcgen05.mma (the warp runs convergent, one elected
+//    lane issues): S_t = Q_t K_j^T into TMEM and O_t += P_t V_j into TMEM,
+//    and signals completion with tcgen05.commit.  Issue order  PV0(j), S0(j+1), PV1(j), S1(j+1)  lets the
 //    softmax of one query tile run while the tensor core works on the other
 //    (the ping-pong of the FA3 section of the course index, rebuilt around
 //    single-thread async MMA and TMEM accumulators); the next unit's first
@@ -239,9 +239,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       } else if (warp == 1) {
         // ================================================= MMA issuer
-        if (lane == 0) {
+        // The whole warp runs the issue loop convergent, so addresses and
+        // descriptors stay warp-uniform, and one elected lane issues every
+        // tcgen05 instruction.  Each buffer's descriptor is built once; a
+        // k-step only adds a compile-time offset (16-byte units) to its
+        // start-address field.  Keeping the issue path this short matters: the
+        // warp shares its SM sub-partition with two busy softmax warps.
+        {
             constexpr uint32_t kIdS = idesc_bf16_f32(kBM, kBN, false);
             constexpr uint32_t kIdPV = idesc_bf16_f32(kBM, D, true);
+            constexpr uint32_t kHi = sdesc_sw128_hi(1024);  // every operand: 8-row groups 1024 B apart
+            // V is [keys][D] with D contiguous: an N-major B operand.  Along N the
+            // 64-column panels are kPanelBytes apart (LBO; one panel when D = 64);
+            // along K every 8 keys are 1024 B apart (SBO).
+            constexpr uint32_t kVLbo = D == 128 ? kPanelBytes : 1024;
+            auto wait = [&](uint32_t b, uint32_t parity) {
+                return mbar_wait_warp(b, parity, abort_flag, &g_fwd_status);
+            };
             bool ok = true;
             int kv = 0;                     // ring position of the unit's first key tile
             int q_waits[kQT] = {0, 0};      // Q_t phases consumed
@@ -255,16 +269,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int n = max(x.n[0], x.n[1]);
                 for (int t = 0; t < kQT && ok; ++t) {
                     if (x.n[t] == 0) continue;
-                    ok = mbar_wait(bar(L::kBarQFull + t), q_waits[t] & 1, abort_flag,
-                                   &g_fwd_status);
+                    ok = wait(bar(L::kBarQFull + t), q_waits[t] & 1);
                     ++q_waits[t];
                 }
                 int k_ready = -1, v_ready = -1;
                 auto wait_k = [&](int j) {
                     if (ok && j > k_ready) {
                         const int r = kv + j;
-                        ok = mbar_wait(bar(L::kBarKFull + r % L::kKSt), (r / L::kKSt) & 1,
-                                       abort_flag, &g_fwd_status);
+                        ok = wait(bar(L::kBarKFull + r % L::kKSt), (r / L::kKSt) & 1);
                         tc_fence_after();
                         k_ready = j;
                     }
@@ -272,8 +284,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 auto wait_v = [&](int j) {
                     if (ok && j > v_ready) {
                         const int r = kv + j;
-                        ok = mbar_wait(bar(L::kBarVFull + r % L::kVSt), (r / L::kVSt) & 1,
-                                       abort_flag, &g_fwd_status);
+                        ok = wait(bar(L::kBarVFull + r % L::kVSt), (r / L::kVSt) & 1);
                         tc_fence_after();
                         v_ready = j;
                     }
@@ -282,69 +293,64 @@ __global__ void __launch_bounds__(kThreads, 1)
                 auto issue_s = [&](int t, int j) {
                     wait_k(j);
                     if (!ok) return;
-                    const uint32_t qa = sbase + L::kOffQ + t * L::kQBytes;
-                    const uint32_t ka = sbase + L::kOffK + ((kv + j) % L::kKSt) * L::kKVBytes;
+                    const uint32_t q_lo = sdesc_sw128_lo(sbase + L::kOffQ + t * L::kQBytes, 16);
+                    const uint32_t k_lo =
+                        sdesc_sw128_lo(sbase + L::kOffK + ((kv + j) % L::kKSt) * L::kKVBytes, 16);
                     const uint32_t dS = tmem + L::tm_s(t);
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t off = (kk >> 2) * kPanelBytes + (kk & 3) * 32;
-                        mma_ss(dS, sdesc_sw128(qa + off, 16, 1024),
-                               sdesc_sw128(ka + off, 16, 1024), kIdS, kk > 0 ? 1u : 0u);
+                        const uint32_t off = ((kk >> 2) * kPanelBytes + (kk & 3) * 32) >> 4;
+                        mma_ss_elect(dS, q_lo + off, kHi, k_lo + off, kHi, kIdS, kk > 0 ? 1u : 0u);
                     }
-                    tc_commit(bar(L::kBarSFull + t));
-                    if (j == x.n[t] - 1) tc_commit(bar(L::kBarQEmpty + t));  // Q_t fully read
+                    tc_commit_elect(bar(L::kBarSFull + t));
+                    if (j == x.n[t] - 1) tc_commit_elect(bar(L::kBarQEmpty + t));  // Q_t fully read
                 };
                 // O_t += P_t V_j  (M=128 rows, N=D, K=128 keys in steps of 16)
                 auto issue_pv = [&](int t, int j) {
                     wait_v(j);
                     if (!ok) return;
-                    ok = mbar_wait(bar(L::kBarPFull + t), p_waits[t] & 1, abort_flag,
-                                   &g_fwd_status);
+                    ok = wait(bar(L::kBarPFull + t), p_waits[t] & 1);
                     ++p_waits[t];
                     if (ok && j == 0 && units_t[t] > 0)  // previous unit's epilogue read O_t
-                        ok = mbar_wait(bar(L::kBarOEmpty + t), (units_t[t] - 1) & 1, abort_flag,
-                                       &g_fwd_status);
+                        ok = wait(bar(L::kBarOEmpty + t), (units_t[t] - 1) & 1);
                     if (!ok) return;
                     tc_fence_after();
-                    const uint32_t va = sbase + L::kOffV + ((kv + j) % L::kVSt) * L::kKVBytes;
+                    const uint32_t v_lo =
+                        sdesc_sw128_lo(sbase + L::kOffV + ((kv + j) % L::kVSt) * L::kKVBytes, kVLbo);
                     const uint32_t dO = tmem + L::tm_o(t);
 #pragma unroll
                     for (int kk = 0; kk < kBN / 16; ++kk) {
-                        // V is [keys][D] with D contiguous: an N-major B operand.  Along N
-                        // the 64-column panels are kPanelBytes apart (LBO; one panel when
-                        // D = 64); along K every 8 keys are 1024 B apart (SBO).
-                        const uint64_t bd =
-                            sdesc_sw128(va + kk * 16 * 128, D == 128 ? kPanelBytes : 1024, 1024);
+                        const uint32_t v_off = (kk * 16 * 128) >> 4;  // 16 keys of 128 B rows
                         const uint32_t acc = (j > 0 || kk > 0) ? 1u : 0u;
                         if constexpr (P_TMEM) {
                             // bf16 P packed two per 32-bit column: 16 keys = 8 columns
-                            mma_ts(dO, tmem + L::tm_s(t) + kk * 8, bd, kIdPV, acc);
+                            mma_ts_elect(dO, tmem + L::tm_s(t) + kk * 8, v_lo + v_off, kHi, kIdPV, acc);
                         } else {
-                            const uint32_t pa = sbase + L::kOffP + t * L::kPBytes;
-                            const uint32_t off = (kk >> 2) * kPanelBytes + (kk & 3) * 32;
-                            mma_ss(dO, sdesc_sw128(pa + off, 16, 1024), bd, kIdPV, acc);
+                            const uint32_t p_lo = sdesc_sw128_lo(sbase + L::kOffP + t * L::kPBytes, 16);
+                            const uint32_t off = ((kk >> 2) * kPanelBytes + (kk & 3) * 32) >> 4;
+                            mma_ss_elect(dO, p_lo + off, kHi, v_lo + v_off, kHi, kIdPV, acc);
                         }
                     }
                     if (j == x.n[t] - 1) {
-                        tc_commit(bar(L::kBarOFull + t));
+                        tc_commit_elect(bar(L::kBarOFull + t));
                         ++units_t[t];
                     }
                 };
                 if (x.n[0] > 0) issue_s(0, 0);
                 if (x.n[1] > 0) issue_s(1, 0);
-                if (n > 0 && ok) tc_commit(bar(L::kBarKEmpty + kv % L::kKSt));
+                if (n > 0 && ok) tc_commit_elect(bar(L::kBarKEmpty + kv % L::kKSt));
                 for (int j = 0; j < n && ok; ++j) {
                     if (j < x.n[0]) issue_pv(0, j);
                     if (j + 1 < x.n[0]) issue_s(0, j + 1);
                     if (j < x.n[1]) issue_pv(1, j);
-                    if (ok) tc_commit(bar(L::kBarVEmpty + (kv + j) % L::kVSt));
+                    if (ok) tc_commit_elect(bar(L::kBarVEmpty + (kv + j) % L::kVSt));
                     if (j + 1 < x.n[1]) issue_s(1, j + 1);
-                    if (j + 1 < n && ok) tc_commit(bar(L::kBarKEmpty + (kv + j + 1) % L::kKSt));
+                    if (j + 1 < n && ok) tc_commit_elect(bar(L::kBarKEmpty + (kv + j + 1) % L::kKSt));
                 }
                 kv += n;
                 tiles += (unsigned long long)(x.n[0] + x.n[1]);
             }
-            if (ok && tiles) atomicAdd(&g_fwd_tiles, tiles);
+            if (ok && tiles && lane == 0) atomicAdd(&g_fwd_tiles, tiles);
         }
       }
     } else {

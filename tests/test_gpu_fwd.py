@@ -131,12 +131,12 @@ def test_causal_tile_fraction(attn):
     assert attn.attn_read_tile_counter(reset=True) == T * T
 
 
-@pytest.mark.parametrize("env", [{"ATTN_FWD_P_SMEM": "1"}, {"ATTN_FWD_RESCALE_THRESHOLD": "0"}],
-                         ids=["p_in_smem", "rescale_every_growth"])
+@pytest.mark.parametrize("env", [{"ATTN_FWD_P_SMEM": "1"}, {"ATTN_FWD_RESCALE_THRESHOLD": "2"}],
+                         ids=["p_in_smem", "rescale_threshold_2"])
 def test_kernel_variants(attn, env):
     """The debugging variant that stages P in shared memory, and the forward
-    with the conditional rescale switched off (rescale whenever the running
-    max grows), give the oracle's answer within the same tolerance."""
+    with a conditional-rescale threshold of 2 (a stale reference max within a
+    factor 4 of the true one), give the oracle's answer within tolerance."""
     code = r"""
 import math, torch, sys
 sys.path.insert(0, %r); sys.path.insert(0, %r)
