@@ -4,8 +4,11 @@ One step = one pass of the whole hot path over one batch of synthetic input:
   prefill  attn_fwd   B=4, Hq=Hkv=16, Nq=Nk=4096, d=128, causal, bf16
   decode   attn_decode_splitkv  B=1, Hq=32, Hkv=8, Nk=65536, d=128, bf16
 Inputs are resident in HBM when the timed region starts and are larger than
-L2; L2 is also flushed (256 MiB write) before every timed step, outside the
-events.  Each call is timed with CUDA events on the launching stream.
+L2; L2 is also flushed before every timed call, outside the events: a 256 MiB
+write and then a 256 MiB read, so that L2 holds only clean lines of another
+buffer and no write-back of the flush (or of the previous call's output)
+lands inside the timed region.  Each call is timed with CUDA events on the
+launching stream.
 
 value  = prefill TFLOP/s (FLOPs counted as 4 Nq Nk d per head, halved for
          causal, summed over ranks) / max-over-ranks time.
@@ -53,9 +56,9 @@ DECODE = {
 # the kernel source it was measured on (any later change to the source turns
 # the figure into null).  Filled from profiles/ summaries.
 NCU_TRAFFIC = {
-    "training_prefill": {"bytes_per_launch": 582.7e6, "src_hash": "657edaf41d723ea0",
+    "training_prefill": {"bytes_per_launch": 584.3e6, "src_hash": "da019fe8b4951b38",
                          "profile": "profiles/fwd_tc_training_prefill.md"},
-    "decode_64k": {"bytes_per_launch": 275.2e6, "src_hash": "31e02a38a10a64b8",
+    "decode_64k": {"bytes_per_launch": 275.1e6, "src_hash": "f4bb42235f95d8fe",
                    "profile": "profiles/decode_split_64k.md"},
 }
 
@@ -260,7 +263,14 @@ def run_ours(args):
     B, Hq, Hkv, Nq, Nk, d, causal = pcfg
     dB, dHq, dHkv, dNk, dd = dcfg
     stream = torch.cuda.current_stream()
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flush_w = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flush_r = torch.ones(64 << 20, dtype=torch.float32, device=dev)
+
+    def flush_l2():
+        # The write evicts everything; the read then replaces the dirty lines
+        # with clean ones, so their write-back happens here and not later.
+        flush_w.zero_()
+        flush_r.sum()
 
     if do_pre:
         scale = 1.0 / math.sqrt(d)
@@ -289,7 +299,7 @@ def run_ours(args):
                                      o=do, lse=dlse)
 
     for _ in range(args.warmup):
-        flush.zero_()
+        flush_l2()
         prefill()
         decode()
     torch.cuda.synchronize()
@@ -297,7 +307,7 @@ def run_ours(args):
         raise RuntimeError("device status reports a timed-out wait during warm-up")
 
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
     clocks = ClockSampler(local)
     clocks.start()
     # The timed region lasts milliseconds, shorter than nvidia-smi's sampling
@@ -313,12 +323,14 @@ def run_ours(args):
     torch.cuda.synchronize()
     t_wall = time.perf_counter()
     for s in range(K):
-        flush.zero_()
+        flush_l2()
         ev[s][0].record(stream)
         prefill()
         ev[s][1].record(stream)
-        decode()
+        flush_l2()
         ev[s][2].record(stream)
+        decode()
+        ev[s][3].record(stream)
     torch.cuda.synchronize()
     barrier(world)
     t_wall = time.perf_counter() - t_wall
@@ -326,7 +338,7 @@ def run_ours(args):
     if attn.attn_check_device_status() != 0:
         raise RuntimeError("device status reports a timed-out wait")
     pre_total = max_over_ranks(sum(ev[s][0].elapsed_time(ev[s][1]) for s in range(K)), world, dev)
-    dec_total = max_over_ranks(sum(ev[s][1].elapsed_time(ev[s][2]) for s in range(K)), world, dev)
+    dec_total = max_over_ranks(sum(ev[s][2].elapsed_time(ev[s][3]) for s in range(K)), world, dev)
     peaks, peak_src = load_peaks()
 
     if args.only is not None:
@@ -346,8 +358,8 @@ def run_ours(args):
         dl_h = torch.empty(dlse.shape, dtype=dlse.dtype).pin_memory()
         e_pre, e_dec = [], []
         for s in range(max(3, min(K, 10)) + 1):
-            flush.zero_()
-            e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+            flush_l2()
+            e0, e1, e2, e3 = (torch.cuda.Event(enable_timing=True) for _ in range(4))
             e0.record(stream)
             q.copy_(qh_p, non_blocking=True)
             k.copy_(kh_p, non_blocking=True)
@@ -356,17 +368,19 @@ def run_ours(args):
             o_h.copy_(o, non_blocking=True)
             l_h.copy_(lse, non_blocking=True)
             e1.record(stream)
+            flush_l2()
+            e2.record(stream)
             dq.copy_(dq_p, non_blocking=True)
             dk.copy_(dk_p, non_blocking=True)
             dv.copy_(dv_p, non_blocking=True)
             decode()
             do_h.copy_(do, non_blocking=True)
             dl_h.copy_(dlse, non_blocking=True)
-            e2.record(stream)
+            e3.record(stream)
             torch.cuda.synchronize()
             if s > 0:  # the first pass warms the copy path
                 e_pre.append(e0.elapsed_time(e1))
-                e_dec.append(e1.elapsed_time(e2))
+                e_dec.append(e2.elapsed_time(e3))
         e_pre_ms = max_over_ranks(statistics.mean(e_pre), world, dev)
         e_dec_ms = max_over_ranks(statistics.mean(e_dec), world, dev)
 
@@ -427,7 +441,8 @@ def run_ours(args):
                         "causal": bool(causal), "ms": pre_ms_avg},
             "decode": {"B": dB, "Hq": dHq, "Hkv": dHkv, "Nk": dNk, "d": dd, "splits": splits,
                        "ms": dec_ms_avg},
-            "l2": "inputs larger than L2 and L2 flushed (256 MiB write) before every timed step",
+            "l2": "inputs larger than L2; L2 flushed before every timed call (256 MiB write, "
+                  "then 256 MiB read so no dirty line is written back inside the timed region)",
             "parallelism": "independent replicas" if world > 1 else "single GPU",
             "clocks_window": "nvidia-smi every 100 ms over a 0.5 s untimed soak of the same "
                              "step followed by the timed steps",
