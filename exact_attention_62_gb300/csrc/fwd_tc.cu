@@ -51,6 +51,35 @@ namespace {
 
 __device__ __forceinline__ long long llmin(long long a, long long b) { return a < b ? a : b; }
 
+// 2^x for two values on the FMA and integer pipes instead of the MUFU unit
+// (software exp2, which the FA4 section of Lecture 11 describes for Blackwell;
+// this formulation and its polynomial are our own).  x is clamped to >= -125
+// (masked scores are -inf; 2^-125 is invisible next to a row sum >= 1), split
+// as x = j + f with j = round(x) by adding 1.5 * 2^23 (the sum's low mantissa
+// bits then hold j, and f = x - j lies in [-1/2, 1/2]), 2^f comes from a cubic
+// whose constant term is exactly 1 (so 2^0 = 1 exactly, as on the MUFU path),
+// and j is added into the exponent field: the sum's bit pattern shifted left by
+// 23 is exactly j << 23 because the constant's low nine bits are zero.  The
+// cubic was fitted for minimax relative error on [-1/2, 1/2] (iteratively
+// reweighted least squares): max relative error 1.0e-4 in fp32 arithmetic,
+// against the 2^-9 of the bf16 rounding that P goes through next.
+constexpr float kExp2C1 = 0.6932829022f;
+constexpr float kExp2C2 = 0.2422109842f;
+constexpr float kExp2C3 = 0.0550089292f;
+__device__ __forceinline__ uint64_t exp2_poly_x2(float x0, float x1) {
+    constexpr float kRound = 12582912.0f;  // 1.5 * 2^23
+    const uint64_t x = f2_pack(fmaxf(x0, -125.0f), fmaxf(x1, -125.0f));
+    const uint64_t t = f2_add(x, f2_pack(kRound, kRound));
+    const uint64_t j = f2_add(t, f2_pack(-kRound, -kRound));
+    const uint64_t f = f2_fma(j, f2_pack(-1.0f, -1.0f), x);
+    uint64_t q = f2_fma(f2_pack(kExp2C3, kExp2C3), f, f2_pack(kExp2C2, kExp2C2));
+    q = f2_fma(q, f, f2_pack(kExp2C1, kExp2C1));
+    q = f2_fma(q, f, f2_pack(1.0f, 1.0f));
+    const uint32_t r0 = static_cast<uint32_t>(q) + (static_cast<uint32_t>(t) << 23);
+    const uint32_t r1 = static_cast<uint32_t>(q >> 32) + (static_cast<uint32_t>(t >> 32) << 23);
+    return (static_cast<uint64_t>(r1) << 32) | r0;
+}
+
 __device__ unsigned g_fwd_status = 0;
 __device__ unsigned long long g_fwd_tiles = 0;
 
@@ -70,6 +99,12 @@ constexpr int kRegsWG0 = 112;
 constexpr int kRegsSoftmax = 192;
 static_assert(128 * kRegsWG0 + 256 * kRegsSoftmax <= kThreads * kLaunchRegs, "register split");
 constexpr int kPanelBytes = 128 * 128;  // 128 rows x 128 B: one 64-column swizzled panel
+// In the POLY variant of the kernel every kPolyEvery-th pair of probabilities
+// is computed by exp2_poly_x2 (FMA and integer pipes) instead of the MUFU unit.
+// Measured on GB300 it is slower at every fraction tried (1/8 .. all): with the
+// MUFU unit's doubled exp2 rate the exp loop is bound by instruction issue, not
+// by MUFU, so the default kernel keeps every exp2 on MUFU.
+constexpr int kPolyEvery = 4;
 constexpr float kLn2 = 0.69314718055994530942f;
 
 struct FwdParams {
@@ -160,7 +195,7 @@ __device__ __forceinline__ Unit unit_at(int u, const FwdParams& p) {
     return x;
 }
 
-template <int D, bool P_TMEM>
+template <int D, bool P_TMEM, bool POLY>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
@@ -440,8 +475,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int c = 0; c < kBN / 2; ++c) {
                     const uint64_t x = f2_fma(f2_pack(__uint_as_float(s[2 * c]),
                                                       __uint_as_float(s[2 * c + 1])), sl2, nm2);
-                    const float p0 = ex2(f2_lo(x));
-                    const float p1 = ex2(f2_hi(x));
+                    float p0, p1;
+                    if (POLY && c % kPolyEvery == kPolyEvery - 1) {
+                        const uint64_t y = exp2_poly_x2(f2_lo(x), f2_hi(x));
+                        p0 = f2_lo(y);
+                        p1 = f2_hi(y);
+                    } else {
+                        p0 = ex2(f2_lo(x));
+                        p1 = ex2(f2_hi(x));
+                    }
                     sum2[c & 1] = f2_add(sum2[c & 1], f2_pack(p0, p1));
                     pk[c] = pack_bf16(p0, p1);
                     if constexpr (P_TMEM) {
@@ -449,7 +491,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 const uint64_t sum = f2_add(sum2[0], sum2[1]);
-                l = fmaf(l, alpha, f2_lo(sum) + f2_hi(sum));
+                // While a row has no finite score its "probabilities" are the
+                // polynomial's clamped 2^-125, not 0: they must not count.  (acc
+                // gets only such values; a later finite score rescales it by
+                // alpha = 0, and with l = 0 the row's O is 0 and its LSE -inf.)
+                const float tile_sum = m_new == -INFINITY ? 0.f : f2_lo(sum) + f2_hi(sum);
+                l = fmaf(l, alpha, tile_sum);
                 if constexpr (P_TMEM) {
                     tmem_st32(tS + 32, pk + 32);
                 } else {
@@ -539,7 +586,7 @@ float rescale_threshold() {
     return v;
 }
 
-template <int D, bool P_TMEM>
+template <int D, bool P_TMEM, bool POLY>
 attn_status_t launch_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                           int Hq, int Hkv, int Nq, int Nk, float scale, int causal,
                           cudaStream_t stream) {
@@ -552,7 +599,7 @@ attn_status_t launch_impl(const void* q, const void* k, const void* v, void* o, 
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(fwd_tc_kernel<D, P_TMEM>,
+        attr_err = cudaFuncSetAttribute(fwd_tc_kernel<D, P_TMEM, POLY>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         L::kSmemBytes);
     });
@@ -562,7 +609,7 @@ attn_status_t launch_impl(const void* q, const void* k, const void* v, void* o, 
     static int num_regs = -1;
     if (num_regs < 0) {
         cudaFuncAttributes fa;
-        if (cudaFuncGetAttributes(&fa, fwd_tc_kernel<D, P_TMEM>) != cudaSuccess) return ATTN_ERR_CUDA;
+        if (cudaFuncGetAttributes(&fa, fwd_tc_kernel<D, P_TMEM, POLY>) != cudaSuccess) return ATTN_ERR_CUDA;
         num_regs = fa.numRegs;
     }
     if (num_regs != kLaunchRegs) return ATTN_ERR_UNSUPPORTED;
@@ -585,7 +632,7 @@ attn_status_t launch_impl(const void* q, const void* k, const void* v, void* o, 
     const int sms = attn_host::device_sm_count();
     if (sms <= 0) return ATTN_ERR_CUDA;
     const int grid = (int)(units < sms ? units : sms);
-    fwd_tc_kernel<D, P_TMEM><<<grid, kThreads, L::kSmemBytes, stream>>>(mq, mk, mv, prm);
+    fwd_tc_kernel<D, P_TMEM, POLY><<<grid, kThreads, L::kSmemBytes, stream>>>(mq, mk, mv, prm);
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
@@ -599,6 +646,16 @@ bool p_in_smem() {
     return v;
 }
 
+// Debug/measurement switch: ATTN_FWD_EXP2_POLY=1 computes every
+// kPolyEvery-th pair of probabilities with exp2_poly_x2.
+bool exp2_poly() {
+    static const bool v = [] {
+        const char* e = std::getenv("ATTN_FWD_EXP2_POLY");
+        return e != nullptr && e[0] == '1';
+    }();
+    return v;
+}
+
 }  // namespace
 
 namespace attn_host {
@@ -607,12 +664,15 @@ attn_status_t launch_fwd_tc(const void* q, const void* k, const void* v, void* o
                             int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal,
                             float scale, cudaStream_t stream) {
     const bool smem_p = p_in_smem();
+    const bool poly = exp2_poly();
     if (d == 128)
-        return smem_p ? launch_impl<128, false>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, stream)
-                      : launch_impl<128, true>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, stream);
+        return smem_p ? launch_impl<128, false, false>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, stream)
+               : poly ? launch_impl<128, true, true>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, stream)
+                      : launch_impl<128, true, false>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, stream);
     if (d == 64)
-        return smem_p ? launch_impl<64, false>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, stream)
-                      : launch_impl<64, true>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, stream);
+        return smem_p ? launch_impl<64, false, false>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, stream)
+               : poly ? launch_impl<64, true, true>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, stream)
+                      : launch_impl<64, true, false>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, stream);
     return ATTN_ERR_UNSUPPORTED;
 }
 

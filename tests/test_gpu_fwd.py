@@ -131,22 +131,26 @@ def test_causal_tile_fraction(attn):
     assert attn.attn_read_tile_counter(reset=True) == T * T
 
 
-@pytest.mark.parametrize("env", [{"ATTN_FWD_P_SMEM": "1"}, {"ATTN_FWD_RESCALE_THRESHOLD": "2"}],
-                         ids=["p_in_smem", "rescale_threshold_2"])
+@pytest.mark.parametrize("env", [{"ATTN_FWD_P_SMEM": "1"}, {"ATTN_FWD_RESCALE_THRESHOLD": "2"},
+                                 {"ATTN_FWD_EXP2_POLY": "1"}],
+                         ids=["p_in_smem", "rescale_threshold_2", "exp2_polynomial"])
 def test_kernel_variants(attn, env):
-    """The debugging variant that stages P in shared memory, and the forward
-    with a conditional-rescale threshold of 2 (a stale reference max within a
-    factor 4 of the true one), give the oracle's answer within tolerance."""
+    """The debugging variant that stages P in shared memory, the forward with a
+    conditional-rescale threshold of 2 (a stale reference max within a factor 4
+    of the true one), and the forward computing a quarter of its exp2 with the
+    polynomial instead of MUFU give the oracle's answer within tolerance,
+    including causal rows with no allowed key (Nq > Nk)."""
     code = r"""
 import math, torch, sys
 sys.path.insert(0, %r); sys.path.insert(0, %r)
 import exact_attention_62_gb300 as attn, oracle
 from exact_attention_62_gb300.inputs import make_qkv
 from parity import compare
-cases = [(2, 3, 300, 64, True, 1.0), (1, 2, 520, 128, True, 1.0), (1, 2, 257, 128, False, 1.0),
-         (1, 2, 700, 64, True, 8.0)]
-for (B, H, N, d, c, qs) in cases:
-    q, k, v = make_qkv(B, H, H, N, N, d, 9, q_scale=qs)
+cases = [(2, 3, 300, 300, 64, True, 1.0), (1, 2, 520, 520, 128, True, 1.0),
+         (1, 2, 257, 257, 128, False, 1.0), (1, 2, 700, 700, 64, True, 8.0),
+         (1, 2, 1000, 300, 128, True, 1.0), (1, 2, 1000, 300, 64, True, 1.0)]
+for (B, H, Nq, Nk, d, c, qs) in cases:
+    q, k, v = make_qkv(B, H, H, Nq, Nk, d, 9, q_scale=qs)
     o, l = attn.attn_fwd(q.cuda(), k.cuda(), v.cuda(), c, 1 / math.sqrt(d))
     torch.cuda.synchronize()
     ro, rl = oracle.attn_fwd(q, k, v, c, 1 / math.sqrt(d))
