@@ -222,3 +222,37 @@ def decode_split(q, k, v, scale: float, nsplit: int):
     if rc != 0:
         raise ValueError("oracle_decode_split rejected its arguments (rc=%d)" % rc)
     return o_parts, lse_parts
+
+
+def decode_paged(q, k_pages, v_pages, block_table, seq_lens, scale: float):
+    """Decode (one query per sequence) over a paged KV cache.
+
+    Paged KV is named in Lecture 11, section 9 (decode kernels on the
+    flash-decoding framework of section 6.2 read a paged cache); the pages fix
+    no layout, so this follows the plainest one: K/V pages [num_pages,
+    page_size, Hkv, d], block_table [B, max_pages] (int), seq_lens [B].  The
+    keys of sequence b are positions 0 .. seq_lens[b]-1 of the concatenation
+    of its pages block_table[b, 0], block_table[b, 1], ...  The result is
+    algorithm 0 (``attn_fwd``, non-causal) over exactly those keys; a sequence
+    with no keys has o = 0 and lse = -inf.  Pool slots beyond a sequence's
+    length are never read.  Returns (o [B, 1, Hq, d], lse [B, Hq]) float64.
+    """
+    q = _f32(q)
+    kp, vp = _f32(k_pages), _f32(v_pages)
+    table = np.asarray(block_table, np.int64)
+    lens = np.asarray(seq_lens, np.int64)
+    B, _, Hq, d = q.shape
+    ps = kp.shape[1]
+    o = np.zeros((B, 1, Hq, d), np.float64)
+    lse = np.full((B, Hq), -np.inf, np.float64)
+    for b in range(B):
+        L = int(lens[b])
+        if L <= 0:
+            continue
+        pages = table[b, :(L + ps - 1) // ps]
+        kb = kp[pages].reshape(-1, kp.shape[2], d)[:L][None]
+        vb = vp[pages].reshape(-1, vp.shape[2], d)[:L][None]
+        ob, lb = attn_fwd(q[b:b + 1], kb, vb, False, scale)
+        o[b] = ob[0]
+        lse[b] = lb[0, :, 0]
+    return o, lse

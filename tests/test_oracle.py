@@ -335,3 +335,60 @@ def test_gqa_head_mapping(oracle_mod):
     vw = v[:, :, [h % Hkv for h in range(Hq)]]
     o3, _ = oracle_mod.attn_fwd(q, kw, vw, True, 0.3)
     assert np.abs(o3 - o).max() > 1e-3
+
+
+# ---------------------------------------------------------------- paged decode
+def _paged_case(seed, B=3, Hq=4, Hkv=2, d=8, ps=4, num_pages=12, max_pages=4):
+    rng = np.random.default_rng(seed)
+    q = rng.standard_normal((B, 1, Hq, d)).astype(np.float32)
+    kp = rng.standard_normal((num_pages, ps, Hkv, d)).astype(np.float32)
+    vp = rng.standard_normal((num_pages, ps, Hkv, d)).astype(np.float32)
+    table = rng.permutation(num_pages)[:B * max_pages].reshape(B, max_pages)
+    return q, kp, vp, table
+
+
+def test_paged_decode_zero_query_is_mean_of_named_rows(oracle_mod):
+    """q = 0: every allowed key has the same score, so O is the mean of exactly
+    the V rows the table names among the first L positions, and LSE = ln L
+    (catches a wrong page, an off-by-one at the partial last page, and the
+    empty sequence)."""
+    q, kp, vp, table = _paged_case(1)
+    q[:] = 0.0
+    lens = np.array([7, 16, 0])
+    o, lse = oracle_mod.decode_paged(q, kp, vp, table, lens, 0.5)
+    ps, G = kp.shape[1], 2
+    for b, L in enumerate(lens):
+        if L == 0:
+            assert np.all(o[b] == 0.0) and np.all(np.isneginf(lse[b]))
+            continue
+        rows = [(table[b, j // ps], j % ps) for j in range(L)]
+        for hq in range(q.shape[2]):
+            want = np.mean([vp[pg, r, hq // G] for pg, r in rows], axis=0)
+            assert np.allclose(o[b, 0, hq], want, atol=1e-12)
+            assert lse[b, hq] == pytest.approx(math.log(L), abs=1e-12)
+
+
+def test_paged_decode_dominant_key_selects_its_row(oracle_mod):
+    q, kp, vp, table = _paged_case(2)
+    lens = np.array([9, 13, 5])
+    b, j = 1, 10                      # position 10 of sequence 1
+    pg, r = table[b, j // 4], j % 4
+    kp[pg, r, :, :] = 0.0
+    kp[pg, r, 0, 0] = 10.0            # KV head 0; other keys have |k0| of a few units
+    q[b, 0, 0, :] = 0.0
+    q[b, 0, 0, 0] = 200.0             # query head 0 of group 0 aims at that key
+    o, _ = oracle_mod.decode_paged(q, kp, vp, table, lens, 1.0)
+    assert np.allclose(o[b, 0, 0], vp[pg, r, 0], atol=1e-9)
+
+
+def test_paged_decode_ignores_slots_past_the_length(oracle_mod):
+    q, kp, vp, table = _paged_case(3)
+    lens = np.array([6, 11, 1])
+    o1, l1 = oracle_mod.decode_paged(q, kp, vp, table, lens, 0.7)
+    kp2, vp2 = kp.copy(), vp.copy()
+    for b, L in enumerate(lens):      # poison every slot a sequence does not own
+        for j in range(L, table.shape[1] * kp.shape[1]):
+            kp2[table[b, j // 4], j % 4] = np.nan
+            vp2[table[b, j // 4], j % 4] = np.nan
+    o2, l2 = oracle_mod.decode_paged(q, kp2, vp2, table, lens, 0.7)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
