@@ -20,7 +20,8 @@ __all__ = [
     "attn_fwd", "attn_decode_num_splits", "attn_decode_workspace_bytes",
     "attn_decode_splitkv", "attn_merge_lse", "attn_status_string",
     "attn_check_device_status", "attn_read_tile_counter", "attn_version",
-    "attn_decode_splitkv_static", "DECODE_STATIC_SCRATCH_BYTES", "EXPORTED_SYMBOLS",
+    "attn_decode_splitkv_static", "attn_decode_paged", "attn_decode_paged_num_splits",
+    "DECODE_STATIC_SCRATCH_BYTES", "EXPORTED_SYMBOLS",
 ]
 
 ATTN_OK, ATTN_ERR_INVALID, ATTN_ERR_UNSUPPORTED, ATTN_ERR_CUDA, ATTN_ERR_TIMEOUT = range(5)
@@ -31,7 +32,7 @@ EXPORTED_SYMBOLS = (
     "attn_fwd", "attn_decode_num_splits", "attn_decode_workspace_bytes",
     "attn_decode_splitkv", "attn_merge_lse", "attn_status_string",
     "attn_check_device_status", "attn_read_tile_counter", "attn_version",
-    "attn_decode_splitkv_static",
+    "attn_decode_splitkv_static", "attn_decode_paged", "attn_decode_paged_num_splits",
 )
 
 # Size of the scratch area built into the library for attn_decode_splitkv_static.
@@ -93,6 +94,10 @@ def lib() -> ctypes.CDLL:
     L.attn_version.argtypes = []
     L.attn_version.restype = ctypes.c_char_p
     L.attn_decode_splitkv_static.argtypes = [P, P, P, P, P, I, I, I, I, I, F, I, I, P]
+    L.attn_decode_paged.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, F, I, P, SZ, I, P]
+    L.attn_decode_paged.restype = I
+    L.attn_decode_paged_num_splits.argtypes = [I, I, I, I, I, I]
+    L.attn_decode_paged_num_splits.restype = I
     L.attn_decode_splitkv_static.restype = I
     _lib = L
     return L
@@ -279,3 +284,54 @@ def attn_read_tile_counter(reset: bool = False) -> int:
 
 def attn_version() -> str:
     return lib().attn_version().decode()
+
+
+def attn_decode_paged_num_splits(B: int, Hq: int, Hkv: int, d: int, page_size: int,
+                                 max_seq_len: int) -> int:
+    return int(lib().attn_decode_paged_num_splits(B, Hq, Hkv, d, page_size, max_seq_len))
+
+
+def attn_decode_paged(q, k_pages, v_pages, block_table, seq_lens, max_seq_len: int,
+                      scale: float | None = None, num_splits: int = 0, workspace=None, o=None,
+                      lse=None, stream=None):
+    """Flash-decoding over a paged KV cache.
+
+    q [B, 1, Hq, d]; k_pages, v_pages [num_pages, page_size, Hkv, d] (bf16);
+    block_table [B, max_pages] and seq_lens [B] int32 on the device;
+    max_seq_len >= every seq_lens[b].  Returns (o [B, 1, Hq, d], lse [B, Hq]).
+    """
+    import torch
+    B, one, Hq, d = q.shape
+    if one != 1:
+        raise ValueError("decode takes one query per sequence (q.shape[1] == 1)")
+    num_pages, page_size, Hkv, dk = k_pages.shape
+    if dk != d or tuple(v_pages.shape) != tuple(k_pages.shape):
+        raise ValueError("shape mismatch")
+    if block_table.dim() != 2 or block_table.shape[0] != B or tuple(seq_lens.shape) != (B,):
+        raise ValueError("block_table must be [B, max_pages] and seq_lens [B]")
+    if block_table.dtype != torch.int32 or seq_lens.dtype != torch.int32:
+        raise ValueError("block_table and seq_lens must be int32")
+    for n, t in (("q", q), ("k_pages", k_pages), ("v_pages", v_pages),
+                 ("block_table", block_table), ("seq_lens", seq_lens)):
+        _need_cuda_contig(n, t)
+    if scale is None:
+        scale = d ** -0.5
+    max_pages = block_table.shape[1]
+    if num_splits == 0 and max_seq_len > 0 and B > 0 and Hq > 0:
+        num_splits = attn_decode_paged_num_splits(B, Hq, Hkv, d, page_size, max_seq_len)
+    wbytes = (attn_decode_workspace_bytes(B, Hq, Hkv, max_seq_len, d, num_splits)
+              if max_seq_len > 0 and B > 0 and Hq > 0 and num_splits > 0 else 0)
+    if workspace is None and wbytes > 0:
+        workspace = torch.empty(wbytes, dtype=torch.uint8, device=q.device)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    wsize = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib().attn_decode_paged(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(block_table),
+                                 _ptr(seq_lens), _ptr(o), _ptr(lse), B, Hq, Hkv, d, num_pages,
+                                 page_size, max_pages, int(max_seq_len), float(scale),
+                                 int(num_splits), _ptr(workspace), wsize, _dtype_code(q),
+                                 _stream(stream))
+    _check("attn_decode_paged", st)
+    return o, lse

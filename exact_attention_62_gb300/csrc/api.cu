@@ -170,6 +170,63 @@ attn_status_t attn_decode_splitkv(const void* q, const void* k_cache, const void
                                     workspace, st);
 }
 
+static bool paged_page_size_ok(int page_size) {
+    return page_size == 16 || page_size == 32 || (page_size > 0 && page_size % 64 == 0);
+}
+
+int attn_decode_paged_num_splits(int B, int Hq, int Hkv, int d, int page_size, int max_seq_len) {
+    if (B < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || max_seq_len < 1 || (d != 64 && d != 128) ||
+        !paged_page_size_ok(page_size))
+        return -1;
+    return attn_host::decode_paged_auto_splits(B, Hq, Hkv, max_seq_len, d, page_size);
+}
+
+attn_status_t attn_decode_paged(const void* q, const void* k_pages, const void* v_pages,
+                                const int* block_table, const int* seq_lens, void* o, float* lse,
+                                int B, int Hq, int Hkv, int d, int num_pages, int page_size,
+                                int max_pages_per_seq, int max_seq_len, float scale,
+                                int num_splits, void* workspace, size_t workspace_bytes,
+                                attn_dtype_t dtype, void* stream) {
+    if (B < 0 || Hq < 0 || Hkv < 1 || d < 1 || num_pages < 0 || page_size < 1 ||
+        max_pages_per_seq < 0 || max_seq_len < 0 || num_splits < 0)
+        return ATTN_ERR_INVALID;
+    if (dtype != ATTN_BF16 && dtype != ATTN_F32) return ATTN_ERR_INVALID;
+    if (bad_scale(scale)) return ATTN_ERR_INVALID;
+    if (Hq % Hkv != 0) return ATTN_ERR_INVALID;
+    if ((long long)max_pages_per_seq * page_size < max_seq_len) return ATTN_ERR_INVALID;
+    if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+    if (dtype != ATTN_BF16) return ATTN_ERR_UNSUPPORTED;
+    if (!paged_page_size_ok(page_size)) return ATTN_ERR_UNSUPPORTED;
+    if (B > 65535 || Hq > 65535) return ATTN_ERR_UNSUPPORTED;
+    if (B == 0 || Hq == 0) return ATTN_OK;
+    if (q == nullptr || o == nullptr || lse == nullptr) return ATTN_ERR_INVALID;
+    if (misaligned(q, 16) || misaligned(o, 16) || misaligned(lse, 4)) return ATTN_ERR_INVALID;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (max_seq_len == 0)
+        return attn_host::launch_fill_empty(o, lse, (long long)B * Hq, d, (long long)B * Hq, true,
+                                            st);
+    if (num_pages < 1 || k_pages == nullptr || v_pages == nullptr || block_table == nullptr ||
+        seq_lens == nullptr)
+        return ATTN_ERR_INVALID;
+    if (misaligned(k_pages, 16) || misaligned(v_pages, 16) || misaligned(block_table, 4) ||
+        misaligned(seq_lens, 4))
+        return ATTN_ERR_INVALID;
+    if (num_splits > max_seq_len) return ATTN_ERR_INVALID;
+    int S = num_splits;
+    if (S == 0) S = attn_host::decode_paged_auto_splits(B, Hq, Hkv, max_seq_len, d, page_size);
+    if (S < 1) return ATTN_ERR_CUDA;
+    if (S > 65535 || !attn_host::paged_splits_fit(max_seq_len, page_size, S))
+        return ATTN_ERR_UNSUPPORTED;
+    if (S > 1) {
+        if (workspace == nullptr || misaligned(workspace, 16)) return ATTN_ERR_INVALID;
+        if (workspace_bytes < attn_host::decode_workspace_bytes(B, Hq, d, S))
+            return ATTN_ERR_INVALID;
+    }
+    return attn_host::launch_decode_paged(q, k_pages, v_pages, block_table, seq_lens, o, lse, B,
+                                          Hq, Hkv, d, num_pages, page_size, max_pages_per_seq,
+                                          max_seq_len, scale, S, workspace, st);
+}
+
 attn_status_t attn_merge_lse(const float* o_parts, const float* lse_parts, int num_parts,
                              long long rows, int d, void* o, float* lse, attn_dtype_t out_dtype,
                              void* stream) {

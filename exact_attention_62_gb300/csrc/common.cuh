@@ -41,6 +41,13 @@ attn_status_t launch_merge(const float* o_parts, const float* lse_parts, int par
                            long long rows, int d, void* o, float* lse, bool out_bf16,
                            cudaStream_t stream);
 cudaError_t decode_read_status(unsigned* out, bool clear);
+bool paged_splits_fit(int max_seq_len, int page_size, int splits);
+int decode_paged_auto_splits(int B, int Hq, int Hkv, int max_seq_len, int d, int page_size);
+attn_status_t launch_decode_paged(const void* q, const void* k_pages, const void* v_pages,
+                                  const int* block_table, const int* seq_lens, void* o, float* lse,
+                                  int B, int Hq, int Hkv, int d, int num_pages, int page_size,
+                                  int max_pages, int max_seq_len, float scale, int splits,
+                                  void* workspace, cudaStream_t stream);
 
 // ---- small utility kernels (api.cu)
 attn_status_t launch_fill_empty(void* o, float* lse, long long rows_o, int d, long long n_lse,

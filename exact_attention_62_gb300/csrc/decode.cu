@@ -55,11 +55,20 @@ struct DecParams {
     float* lse;              // [B, Hq]        (single segment)
     float* o_parts;          // [S, B*Hq, D]   (several segments)
     float* lse_parts;        // [S, B*Hq]
-    int B, Hq, Hkv, Nk, G, splits, seg_len;
+    int B, Hq, Hkv, Nk, G, splits, seg_len;  // Nk: cache length (paged: the maximum)
     float scale_log2;
+    // paged cache only
+    const int* table;        // [B, max_pages] page of each block of page_size keys
+    const int* seq_lens;     // [B]
+    int page_size, max_pages;
 };
 
-template <int D, int STAGES>
+// Paged cache: block-table entries one CTA may need (its segment's pages),
+// staged in shared memory by the producer warp.  The host keeps segments
+// short enough for this.
+constexpr int kTableCap = 4096;
+
+template <int D, int STAGES, bool PAGED = false>
 struct DecLayout {
     static constexpr int kPanelBytes = kTileKeys * 128;  // 64 keys x 64 columns x 2 B
     static constexpr int kTileBytes = kTileKeys * D * 2;
@@ -67,7 +76,9 @@ struct DecLayout {
     static constexpr int kOffBar = STAGES * kStageBytes;
     static constexpr int kNumBars = 2 * STAGES;          // full[STAGES], empty[STAGES]
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
-    static constexpr int kSmemBytes = kOffMisc + 16 + 1024;
+    static constexpr int kOffTable = kOffMisc + 16;
+    static constexpr int kSmemBytes = kOffTable + (PAGED ? kTableCap * 4 : 0) + 1024;
+    static_assert(kSmemBytes <= 232448, "shared memory budget");
     // Cross-warp merge scratch [warp][8 query columns][D + 2], reusing the
     // stage buffers once every tile has been consumed.
     static constexpr int kRedStride = D + 2;
@@ -86,12 +97,12 @@ __device__ __forceinline__ uint32_t ld_b32(const __nv_bfloat16* p) {
     return *reinterpret_cast<const uint32_t*>(p);
 }
 
-template <int D, int GC>
+template <int D, int GC, bool PAGED>
 __global__ void __launch_bounds__(kDecThreads)
     decode_split_kernel(const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, const DecParams p) {
     constexpr int STAGES = dec_stages<D>();
-    using L = DecLayout<D, STAGES>;
+    using L = DecLayout<D, STAGES, PAGED>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -106,16 +117,25 @@ __global__ void __launch_bounds__(kDecThreads)
     const int hq0 = blockIdx.y * GC;
     const int b = blockIdx.z;
     const int g = hq0 / p.G;
+    // Keys of this sequence: all Nk, or (paged) its own length, clamped to
+    // [0, Nk] where Nk is the caller's maximum.
+    int len = p.Nk;
+    if constexpr (PAGED) len = min(max(p.seq_lens[b], 0), p.Nk);
     const int j0 = seg * p.seg_len;
-    const int j1 = min(j0 + p.seg_len, p.Nk);
+    const int j1 = min(j0 + p.seg_len, len);
     const int ntiles = j1 > j0 ? (j1 - j0 + kTileKeys - 1) / kTileKeys : 0;
     const long long R = (long long)p.B * p.Hq;
 
     if (ntiles == 0) {  // empty segment: o_s = 0, lse_s = -inf
         for (int e = threadIdx.x; e < GC * D; e += blockDim.x) {
             const long long row = (long long)b * p.Hq + hq0 + e / D;
-            p.o_parts[((long long)seg * R + row) * D + (e % D)] = 0.f;
-            if (e % D == 0) p.lse_parts[(long long)seg * R + row] = -INFINITY;
+            if (p.splits == 1) {  // a sequence with no keys at all
+                p.o[row * D + (e % D)] = __float2bfloat16_rn(0.f);
+                if (e % D == 0) p.lse[row] = -INFINITY;
+            } else {
+                p.o_parts[((long long)seg * R + row) * D + (e % D)] = 0.f;
+                if (e % D == 0) p.lse_parts[(long long)seg * R + row] = -INFINITY;
+            }
         }
         return;
     }
@@ -132,6 +152,22 @@ __global__ void __launch_bounds__(kDecThreads)
 
     if (warp == 0) {
         // ================================================= TMA producer
+        // Paged cache: the tensor maps view the page pools as [pages,
+        // page_size, Hkv, D]; a tile's keys come from the pages the block
+        // table names.  Pages of 64 or more keys hold whole tiles (segments
+        // start at multiples of 64); smaller pages are loaded as 64/page_size
+        // boxes, skipping those past the sequence.
+        int first_page = 0;
+        const int* tab = nullptr;
+        if constexpr (PAGED) {
+            int* st_tab = reinterpret_cast<int*>(sgen + L::kOffTable);
+            first_page = j0 / p.page_size;
+            const int n_pages = (j1 - 1) / p.page_size - first_page + 1;
+            const int* src = p.table + (long long)b * p.max_pages + first_page;
+            for (int e = lane; e < n_pages; e += 32) st_tab[e] = src[e];
+            __syncwarp();
+            tab = st_tab;
+        }
         if (lane == 0) {
             prefetch_tmap(&tmK);
             prefetch_tmap(&tmV);
@@ -139,14 +175,44 @@ __global__ void __launch_bounds__(kDecThreads)
                 const int st = t % STAGES;
                 if (!mbar_wait(empty_bar(st), ((t / STAGES) & 1) ^ 1, abort_flag, &g_dec_status))
                     break;
-                mbar_arrive_expect_tx(full_bar(st), L::kStageBytes);
                 const uint32_t kdst = sbase + st * L::kStageBytes;
                 const int key0 = j0 + t * kTileKeys;
+                if constexpr (PAGED) {
+                    const int ps = p.page_size;
+                    if (ps >= kTileKeys) {
+                        mbar_arrive_expect_tx(full_bar(st), L::kStageBytes);
+                        const int page = tab[key0 / ps - first_page];
+                        const int row = key0 % ps;
 #pragma unroll
-                for (int pp = 0; pp < D / 64; ++pp) {
-                    tma_load_4d(kdst + pp * L::kPanelBytes, &tmK, full_bar(st), 64 * pp, g, key0, b);
-                    tma_load_4d(kdst + L::kTileBytes + pp * L::kPanelBytes, &tmV, full_bar(st),
-                                64 * pp, g, key0, b);
+                        for (int pp = 0; pp < D / 64; ++pp) {
+                            tma_load_4d(kdst + pp * L::kPanelBytes, &tmK, full_bar(st), 64 * pp, g, row,
+                                        page);
+                            tma_load_4d(kdst + L::kTileBytes + pp * L::kPanelBytes, &tmV, full_bar(st),
+                                        64 * pp, g, row, page);
+                        }
+                    } else {
+                        const int nsub = min(kTileKeys / ps, (j1 - key0 + ps - 1) / ps);
+                        mbar_arrive_expect_tx(full_bar(st), (uint32_t)(nsub * ps * D * 2 * 2));
+                        for (int r = 0; r < nsub; ++r) {
+                            const int page = tab[(key0 + r * ps) / ps - first_page];
+                            const uint32_t off = (uint32_t)(r * ps * 128);
+#pragma unroll
+                            for (int pp = 0; pp < D / 64; ++pp) {
+                                tma_load_4d(kdst + pp * L::kPanelBytes + off, &tmK, full_bar(st), 64 * pp,
+                                            g, 0, page);
+                                tma_load_4d(kdst + L::kTileBytes + pp * L::kPanelBytes + off, &tmV,
+                                            full_bar(st), 64 * pp, g, 0, page);
+                            }
+                        }
+                    }
+                } else {
+                    mbar_arrive_expect_tx(full_bar(st), L::kStageBytes);
+#pragma unroll
+                    for (int pp = 0; pp < D / 64; ++pp) {
+                        tma_load_4d(kdst + pp * L::kPanelBytes, &tmK, full_bar(st), 64 * pp, g, key0, b);
+                        tma_load_4d(kdst + L::kTileBytes + pp * L::kPanelBytes, &tmV, full_bar(st),
+                                    64 * pp, g, key0, b);
+                    }
                 }
             }
         }
@@ -187,6 +253,24 @@ __global__ void __launch_bounds__(kDecThreads)
         if (!mbar_wait(full_bar(st), (t / STAGES) & 1, abort_flag, &g_dec_status)) break;
         const uint32_t kb = sbase + st * L::kStageBytes;
         const uint32_t vb = kb + L::kTileBytes;
+        // Paged cache: V rows past the sequence hold whatever the pool has
+        // there (or stale stage data); P is 0 for them but 0 * NaN is not,
+        // so the warp zeroes its own such rows (K needs nothing: masked
+        // scores are replaced, not multiplied).
+        bool zeroed = false;
+        if constexpr (PAGED) {
+            const int kbase = j0 + t * kTileKeys + 16 * kw;
+            if (kbase + 16 > j1) {
+                for (int e = lane; e < 16 * (D / 8); e += 32) {
+                    const int rrow = e / (D / 8), ch = e % (D / 8);
+                    if (kbase + rrow >= j1)
+                        st_shared_v4(vb + (ch >> 3) * L::kPanelBytes + (16 * kw + rrow) * 128 + ((ch & 7) << 4),
+                                     0u, 0u, 0u, 0u);
+                }
+                __syncwarp();
+                zeroed = true;
+            }
+        }
 
         // S^T (16 keys x 8 query columns) = K (16 x D) Q^T (D x 8); even and odd
         // k-steps accumulate separately to halve the dependent MMA chain.
@@ -247,6 +331,8 @@ __global__ void __launch_bounds__(kDecThreads)
             ldsm_x4_trans(addr, a);
             mma_16816(acc[mb], a, b01, b23);
         }
+        // order the zeroing stores before the stage's next TMA write
+        if (zeroed) fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(empty_bar(st));
     }
@@ -414,20 +500,35 @@ int group_cols(int G) {
     return 1;
 }
 
-template <int D, int GC>
+template <int D, int GC, bool PAGED>
 attn_status_t launch_split(const CUtensorMap& mk, const CUtensorMap& mv, const DecParams& prm,
                            cudaStream_t stream) {
-    using L = DecLayout<D, dec_stages<D>()>;
+    using L = DecLayout<D, dec_stages<D>(), PAGED>;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(decode_split_kernel<D, GC>,
+        attr_err = cudaFuncSetAttribute(decode_split_kernel<D, GC, PAGED>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
     });
     if (attr_err != cudaSuccess) return ATTN_ERR_CUDA;
     dim3 grid(prm.splits, prm.Hq / GC, prm.B);
-    decode_split_kernel<D, GC><<<grid, kDecThreads, L::kSmemBytes, stream>>>(mk, mv, prm);
+    decode_split_kernel<D, GC, PAGED><<<grid, kDecThreads, L::kSmemBytes, stream>>>(mk, mv, prm);
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+template <bool PAGED>
+attn_status_t launch_split_any(int d, const CUtensorMap& mk, const CUtensorMap& mv,
+                               const DecParams& prm, cudaStream_t stream) {
+    const int GC = group_cols(prm.G);
+    if (d == 128)
+        return GC == 8   ? launch_split<128, 8, PAGED>(mk, mv, prm, stream)
+               : GC == 4 ? launch_split<128, 4, PAGED>(mk, mv, prm, stream)
+               : GC == 2 ? launch_split<128, 2, PAGED>(mk, mv, prm, stream)
+                         : launch_split<128, 1, PAGED>(mk, mv, prm, stream);
+    return GC == 8   ? launch_split<64, 8, PAGED>(mk, mv, prm, stream)
+           : GC == 4 ? launch_split<64, 4, PAGED>(mk, mv, prm, stream)
+           : GC == 2 ? launch_split<64, 2, PAGED>(mk, mv, prm, stream)
+                     : launch_split<64, 1, PAGED>(mk, mv, prm, stream);
 }
 
 template <int D>
@@ -437,10 +538,10 @@ int ctas_per_sm() {
     std::call_once(once, [] {
         using L = DecLayout<D, dec_stages<D>()>;
         int n = 0;
-        cudaFuncSetAttribute(decode_split_kernel<D, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             L::kSmemBytes);
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_split_kernel<D, 4>, kDecThreads,
-                                                          L::kSmemBytes) != cudaSuccess)
+        cudaFuncSetAttribute(decode_split_kernel<D, 4, false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_split_kernel<D, 4, false>,
+                                                          kDecThreads, L::kSmemBytes) != cudaSuccess)
             n = 1;
         v = std::max(1, n);
     });
@@ -524,19 +625,72 @@ attn_status_t launch_decode(const void* q, const void* k, const void* v, void* o
         prm.o_parts = nullptr;
         prm.lse_parts = nullptr;
     }
-    const int GC = group_cols(prm.G);
-    attn_status_t st;
-    if (d == 128) {
-        st = GC == 8   ? launch_split<128, 8>(mk, mv, prm, stream)
-             : GC == 4 ? launch_split<128, 4>(mk, mv, prm, stream)
-             : GC == 2 ? launch_split<128, 2>(mk, mv, prm, stream)
-                       : launch_split<128, 1>(mk, mv, prm, stream);
+    prm.table = nullptr;
+    prm.seq_lens = nullptr;
+    prm.page_size = 0;
+    prm.max_pages = 0;
+    const attn_status_t st = launch_split_any<false>(d, mk, mv, prm, stream);
+    if (st != ATTN_OK || splits == 1) return st;
+    return launch_merge(prm.o_parts, prm.lse_parts, splits, (long long)rows, d, o, lse, true, stream);
+}
+
+// Segment length of the paged kernel: whole 64-key tiles, so that a tile never
+// straddles a page of 64 or more keys.
+static int paged_seg_len(int max_seq_len, int splits) {
+    const int seg = (max_seq_len + splits - 1) / splits;
+    return (seg + kTileKeys - 1) / kTileKeys * kTileKeys;
+}
+
+bool paged_splits_fit(int max_seq_len, int page_size, int splits) {
+    // pages one segment can touch: its keys / page_size, plus one partial page at each end
+    const long long seg = paged_seg_len(max_seq_len, splits);
+    return seg / page_size + 2 <= kTableCap;
+}
+
+int decode_paged_auto_splits(int B, int Hq, int Hkv, int max_seq_len, int d, int page_size) {
+    int S = decode_auto_splits(B, Hq, Hkv, max_seq_len, d);
+    if (S < 1) return S;
+    while (!paged_splits_fit(max_seq_len, page_size, S) && S < max_seq_len) ++S;
+    return S;
+}
+
+attn_status_t launch_decode_paged(const void* q, const void* k_pages, const void* v_pages,
+                                  const int* block_table, const int* seq_lens, void* o, float* lse,
+                                  int B, int Hq, int Hkv, int d, int num_pages, int page_size,
+                                  int max_pages, int max_seq_len, float scale, int splits,
+                                  void* workspace, cudaStream_t stream) {
+    const int box = page_size < kTileKeys ? page_size : kTileKeys;
+    CUtensorMap mk, mv;
+    if (!encode_bshd_map(&mk, k_pages, num_pages, page_size, Hkv, d, box, 2) ||
+        !encode_bshd_map(&mv, v_pages, num_pages, page_size, Hkv, d, box, 2))
+        return ATTN_ERR_CUDA;
+    DecParams prm;
+    prm.q = static_cast<const __nv_bfloat16*>(q);
+    prm.o = static_cast<__nv_bfloat16*>(o);
+    prm.lse = lse;
+    prm.B = B;
+    prm.Hq = Hq;
+    prm.Hkv = Hkv;
+    prm.Nk = max_seq_len;
+    prm.G = Hq / Hkv;
+    prm.splits = splits;
+    prm.seg_len = paged_seg_len(max_seq_len, splits);
+    prm.scale_log2 = scale * 1.4426950408889634f;
+    prm.table = block_table;
+    prm.seq_lens = seq_lens;
+    prm.page_size = page_size;
+    prm.max_pages = max_pages;
+    const size_t rows = (size_t)B * Hq;
+    if (splits > 1) {
+        const size_t o_bytes = (size_t)splits * rows * d * 4;
+        prm.o_parts = static_cast<float*>(workspace);
+        prm.lse_parts = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                                 (o_bytes + 255) / 256 * 256);
     } else {
-        st = GC == 8   ? launch_split<64, 8>(mk, mv, prm, stream)
-             : GC == 4 ? launch_split<64, 4>(mk, mv, prm, stream)
-             : GC == 2 ? launch_split<64, 2>(mk, mv, prm, stream)
-                       : launch_split<64, 1>(mk, mv, prm, stream);
+        prm.o_parts = nullptr;
+        prm.lse_parts = nullptr;
     }
+    const attn_status_t st = launch_split_any<true>(d, mk, mv, prm, stream);
     if (st != ATTN_OK || splits == 1) return st;
     return launch_merge(prm.o_parts, prm.lse_parts, splits, (long long)rows, d, o, lse, true, stream);
 }

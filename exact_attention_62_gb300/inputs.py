@@ -64,3 +64,41 @@ def sample_rows(B: int, Hq: int, Nq: int, n: int, seed: int):
         i = r % Nq
         out.append((b, hq, i))
     return out
+
+
+def make_paged(B: int, Hq: int, Hkv: int, d: int, page_size: int, seq_lens, seed: int,
+               extra_pages: int = 3, poison: bool = True, dtype: torch.dtype = torch.bfloat16):
+    """A random paged KV cache on the CPU.
+
+    Sequence b owns ceil(seq_lens[b] / page_size) distinct pages, drawn in
+    random order from a shuffled pool with ``extra_pages`` pages nobody owns.
+    Table entries past a sequence's pages are -1.  With ``poison`` every pool
+    slot that no sequence's first seq_lens[b] positions use is NaN.
+    Returns (q [B,1,Hq,d], k_pages, v_pages [num_pages, page_size, Hkv, d],
+    block_table [B, max_pages] int32, seq_lens [B] int32).
+    """
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    lens = [int(x) for x in seq_lens]
+    need = [(L + page_size - 1) // page_size for L in lens]
+    max_pages = max(1, max(need))
+    num_pages = sum(need) + extra_pages
+    perm = torch.randperm(num_pages, generator=g).tolist()
+    table = torch.full((B, max_pages), -1, dtype=torch.int32)
+    owned = torch.zeros((num_pages, page_size), dtype=torch.bool)
+    pos = 0
+    for b in range(B):
+        for j in range(need[b]):
+            pg = perm[pos]
+            pos += 1
+            table[b, j] = pg
+            n_used = min(page_size, lens[b] - j * page_size)
+            owned[pg, :n_used] = True
+    q = torch.randn((B, 1, Hq, d), generator=g, dtype=torch.float32)
+    kp = torch.randn((num_pages, page_size, Hkv, d), generator=g, dtype=torch.float32)
+    vp = torch.randn((num_pages, page_size, Hkv, d), generator=g, dtype=torch.float32)
+    q, kp, vp = q.to(dtype), kp.to(dtype), vp.to(dtype)
+    if poison:
+        kp[~owned] = float("nan")
+        vp[~owned] = float("nan")
+    return q, kp, vp, table, torch.tensor(lens, dtype=torch.int32)

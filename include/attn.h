@@ -109,7 +109,8 @@ size_t attn_decode_workspace_bytes(int B, int Hq, int Hkv, int Nk, int d,
  * attn_decode_splitkv -- flash-decoding ([L11] 6.2): one query per sequence.
  *
  *   q        [B, 1, Hq, d]      query of the current step.
- *   k_cache, v_cache  [B, Nk, Hkv, d]  dense KV cache (Nk >= 1 valid rows).
+ *   k_cache, v_cache  [B, Nk, Hkv, d]  dense KV cache, Nk >= 0 valid rows
+ *            (Nk = 0: o = 0 and lse = -inf, nothing is read).
  *   o        [B, 1, Hq, d] output (dtype elements).
  *   lse      [B, Hq] float32 output.
  *   num_splits  0 = automatic (attn_decode_num_splits), else 1..Nk.
@@ -168,6 +169,54 @@ attn_status_t attn_decode_splitkv_static(const void* q, const void* k_cache,
                                          int B, int Hq, int Hkv, int Nk, int d,
                                          float scale, int num_splits,
                                          attn_dtype_t dtype, void* stream);
+
+/*
+ * attn_decode_paged -- flash-decoding over a paged KV cache.  [L11] 9 names
+ * paged KV caches as what decode kernels built on the flash-decoding split
+ * of [L11] 6.2 read; the pages fix no layout, and this one is the plainest:
+ *
+ *   q          [B, 1, Hq, d]  query of the current step.
+ *   k_pages, v_pages  [num_pages, page_size, Hkv, d]  page pools (bf16).
+ *   block_table [B, max_pages_per_seq] int32, device memory: the keys of
+ *              sequence b are positions 0 .. seq_lens[b]-1 of its pages
+ *              block_table[b, 0], block_table[b, 1], ... in that order.
+ *              Entries past a sequence's last page are never read; an entry
+ *              outside [0, num_pages) reads zeros.
+ *   seq_lens   [B] int32, device memory; values are clamped to
+ *              [0, max_seq_len].  A sequence of length 0 gets o = 0,
+ *              lse = -inf.
+ *   o          [B, 1, Hq, d] output (bf16).   lse [B, Hq] float32 output.
+ *   page_size  16, 32, or a multiple of 64.
+ *   max_seq_len  upper bound of seq_lens (host-known; it sets the segment
+ *              length and the workspace); max_seq_len <=
+ *              max_pages_per_seq * page_size.
+ *   num_splits 0 = automatic (attn_decode_paged_num_splits), else
+ *              1..max_seq_len.  Segment s covers positions [s*L, (s+1)*L)
+ *              with L = ceil(max_seq_len / S) rounded up to a multiple of
+ *              64; the pages one segment touches must fit a 4096-entry
+ *              table (else ATTN_ERR_UNSUPPORTED).
+ *   workspace  as attn_decode_splitkv, sized by
+ *              attn_decode_workspace_bytes(B, Hq, Hkv, max_seq_len, d, S).
+ * Slots of a page past a sequence's length may hold anything (NaN
+ * included); they do not affect the result.  The caller owns all buffers;
+ * nothing is allocated.  Errors: as attn_decode_splitkv, plus
+ * ATTN_ERR_UNSUPPORTED for other page sizes.
+ */
+attn_status_t attn_decode_paged(const void* q, const void* k_pages, const void* v_pages,
+                                const int* block_table, const int* seq_lens, void* o,
+                                float* lse, int B, int Hq, int Hkv, int d, int num_pages,
+                                int page_size, int max_pages_per_seq, int max_seq_len,
+                                float scale, int num_splits, void* workspace,
+                                size_t workspace_bytes, attn_dtype_t dtype, void* stream);
+
+/*
+ * attn_decode_paged_num_splits -- the segment count attn_decode_paged uses
+ * with num_splits = 0: attn_decode_num_splits(B, Hq, Hkv, max_seq_len, d),
+ * raised until one segment's pages fit the block-table staging area.
+ * Returns -1 on invalid sizes.
+ */
+int attn_decode_paged_num_splits(int B, int Hq, int Hkv, int d, int page_size,
+                                 int max_seq_len);
 
 /*
  * attn_merge_lse -- exact merge of partial attention results in log-sum-exp

@@ -125,3 +125,31 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(pkg, "_LIB_PATH", str(tmp_path / "libattn.so"))
     with pytest.raises(RuntimeError, match="not built"):
         pkg.lib()
+
+
+def paged(L, B=2, Hq=8, Hkv=2, d=128, num_pages=10, ps=64, max_pages=4, max_len=200, S=1,
+          ws=None, wbytes=0, dtype=BF16):
+    return L.attn_decode_paged(FAKE, FAKE, FAKE, FAKE_LSE, FAKE_LSE, FAKE, FAKE_LSE, B, Hq, Hkv, d,
+                               num_pages, ps, max_pages, max_len, 0.1, S, ws, wbytes, dtype, None)
+
+
+def test_paged_decode_rejects_bad_arguments(L):
+    assert paged(L, ps=48, max_pages=10) == UNSUPPORTED   # page sizes: 16, 32 or multiples of 64
+    assert paged(L, ps=8, max_pages=40) == UNSUPPORTED
+    assert paged(L, ps=0) == INVALID
+    assert paged(L, max_pages=3, max_len=200) == INVALID   # 3 pages of 64 < 200 keys
+    assert paged(L, dtype=F32) == UNSUPPORTED
+    assert paged(L, d=96) == UNSUPPORTED
+    assert paged(L, Hq=6, Hkv=4) == INVALID
+    assert paged(L, S=201) == INVALID             # more segments than keys
+    assert paged(L, S=4) == INVALID               # several segments need a workspace
+    assert paged(L, num_pages=0) == INVALID
+    # one segment of 100000 keys in pages of 16 would need > 4096 table entries
+    assert paged(L, ps=16, max_pages=7000, max_len=100000, S=1) == UNSUPPORTED
+    assert paged(L, B=0) == OK
+
+
+def test_paged_decode_declares_its_auto_split_rule():
+    # pages a segment touches must fit the 4096-entry staging area; the rule is host arithmetic
+    assert pkg.attn_decode_workspace_bytes(2, 8, 2, 200, 128, 3) == \
+        (3 * 16 * 128 * 4 + 255) // 256 * 256 + 3 * 16 * 4

@@ -1,0 +1,91 @@
+"""Parity of attn_decode_paged against the oracle's paged decode.
+
+Block tables are random permutations of a pool with unowned pages; every
+slot no sequence owns is NaN (it must not reach the output).  Cases cover
+page sizes 16, 32, 64 and 256, lengths on both sides of page and tile
+boundaries, empty sequences (with one and with several segments), GQA
+ratios 1, 4 and 8, d = 64 and 128, and fixed and automatic segment counts."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from exact_attention_62_gb300.inputs import make_paged
+from parity import compare
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+CASES = [
+    # B, Hq, Hkv, d, page_size, seq_lens, splits, max_seq_len (None = max of lens)
+    (4, 8, 2, 128, 16, [1, 15, 16, 17], 0, None),
+    (3, 32, 8, 128, 64, [0, 64, 1000], 0, None),
+    (2, 16, 4, 64, 32, [500, 33], 3, None),
+    (2, 8, 8, 128, 256, [5000, 4097], 0, None),
+    (2, 8, 2, 128, 64, [0, 100], 1, None),
+    (3, 8, 2, 64, 16, [63, 64, 65], 2, 400),          # segments past every sequence
+    (2, 16, 2, 128, 32, [2047, 1], 7, None),
+]
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,d,ps,lens,S,maxlen", CASES)
+def test_paged_decode_matches_oracle(attn, oracle_mod, B, Hq, Hkv, d, ps, lens, S, maxlen):
+    q, kp, vp, table, sl = make_paged(B, Hq, Hkv, d, ps, lens, seed=sum(lens) + ps)
+    scale = 1.0 / math.sqrt(d)
+    max_seq_len = maxlen if maxlen is not None else max(lens)
+    cols = (max_seq_len + ps - 1) // ps          # the table must cover max_seq_len
+    if table.shape[1] < cols:
+        table = torch.cat([table, torch.full((B, cols - table.shape[1]), -1, dtype=torch.int32)], 1)
+    o, lse = attn.attn_decode_paged(q.to(DEV), kp.to(DEV), vp.to(DEV), table.to(DEV), sl.to(DEV),
+                                    max_seq_len, scale, num_splits=S)
+    torch.cuda.synchronize()
+    assert attn.attn_check_device_status() == 0
+    ro, rl = oracle_mod.decode_paged(q, kp.float(), vp.float(), table.numpy(), sl.numpy(), scale)
+    compare(o, lse, ro, rl, torch.bfloat16, "paged %s" % (lens,))
+    for b, L in enumerate(lens):
+        if L == 0:
+            assert torch.all(o[b] == 0) and torch.all(torch.isneginf(lse[b]))
+
+
+def test_paged_long_context_and_many_sequences(attn, oracle_mod):
+    """The two decode workloads' shapes on a paged cache: one 64K sequence in
+    64-key pages, and 16 sequences of random length up to 8K in 16-key pages."""
+    for (B, lens, ps) in [(1, [65536], 64),
+                          (16, torch.randint(1, 8193, (16,), generator=torch.Generator().manual_seed(5)).tolist(), 16)]:
+        q, kp, vp, table, sl = make_paged(B, 32, 8, 128, ps, lens, seed=77, poison=True)
+        o, lse = attn.attn_decode_paged(q.to(DEV), kp.to(DEV), vp.to(DEV), table.to(DEV),
+                                        sl.to(DEV), max(lens), 128 ** -0.5)
+        torch.cuda.synchronize()
+        assert attn.attn_check_device_status() == 0
+        ro, rl = oracle_mod.decode_paged(q, kp.float(), vp.float(), table.numpy(), sl.numpy(),
+                                         128 ** -0.5)
+        compare(o, lse, ro, rl, torch.bfloat16, "paged B=%d" % B)
+
+
+def test_paged_equals_contiguous_decode(attn):
+    """With pages laid out in order, the paged call sees the same keys as the
+    dense decode of the same cache; both use the same kernels, so with the
+    same segment count the results agree bit for bit."""
+    B, Hq, Hkv, d, N, ps = 2, 16, 4, 128, 3000, 64
+    g = torch.Generator().manual_seed(9)
+    q = torch.randn((B, 1, Hq, d), generator=g).to(torch.bfloat16).to(DEV)
+    kc = torch.randn((B, N, Hkv, d), generator=g).to(torch.bfloat16).to(DEV)
+    vc = torch.randn((B, N, Hkv, d), generator=g).to(torch.bfloat16).to(DEV)
+    npg = (N + ps - 1) // ps
+    pad = npg * ps - N
+    kp = torch.cat([kc, torch.zeros((B, pad, Hkv, d), dtype=kc.dtype, device=DEV)], 1)
+    vp = torch.cat([vc, torch.zeros((B, pad, Hkv, d), dtype=vc.dtype, device=DEV)], 1)
+    kp = kp.reshape(B * npg, ps, Hkv, d).contiguous()
+    vp = vp.reshape(B * npg, ps, Hkv, d).contiguous()
+    table = torch.arange(B * npg, dtype=torch.int32, device=DEV).reshape(B, npg)
+    sl = torch.full((B,), N, dtype=torch.int32, device=DEV)
+    for S in (1, 5):   # segment lengths are whole tiles in both when N/S is
+        o1, l1 = attn.attn_decode_paged(q, kp, vp, table, sl, N, num_splits=S)
+        o2, l2 = attn.attn_decode_splitkv(q, kc, vc, num_splits=S)
+        torch.cuda.synchronize()
+        if S == 1:
+            assert torch.equal(o1, o2) and torch.equal(l1, l2)
+        else:
+            assert (o1.float() - o2.float()).abs().max().item() <= 1e-2
+            assert (l1 - l2).abs().max().item() <= 1e-4
