@@ -171,39 +171,50 @@ __global__ void __launch_bounds__(kDecThreads)
         if (lane == 0) {
             prefetch_tmap(&tmK);
             prefetch_tmap(&tmV);
+        }
+        if (PAGED && p.page_size < kTileKeys) {
+            // Small pages: 64 / page_size boxes per panel and tile.  The whole
+            // warp runs the loop; lane 0 posts the stage's byte count and lane
+            // r issues the boxes of the tile's r-th page.
+            const int ps = p.page_size;
+            for (int t = 0; t < ntiles; ++t) {
+                const int st = t % STAGES;
+                if (!mbar_wait_warp(empty_bar(st), ((t / STAGES) & 1) ^ 1, abort_flag, &g_dec_status))
+                    break;
+                const uint32_t kdst = sbase + st * L::kStageBytes;
+                const int key0 = j0 + t * kTileKeys;
+                const int nsub = min(kTileKeys / ps, (j1 - key0 + ps - 1) / ps);
+                if (lane == 0) mbar_arrive_expect_tx(full_bar(st), (uint32_t)(nsub * ps * D * 2 * 2));
+                __syncwarp();
+                if (lane < nsub) {
+                    const int page = tab[(key0 + lane * ps) / ps - first_page];
+                    const uint32_t off = (uint32_t)(lane * ps * 128);
+#pragma unroll
+                    for (int pp = 0; pp < D / 64; ++pp) {
+                        tma_load_4d(kdst + pp * L::kPanelBytes + off, &tmK, full_bar(st), 64 * pp, g, 0,
+                                    page);
+                        tma_load_4d(kdst + L::kTileBytes + pp * L::kPanelBytes + off, &tmV, full_bar(st),
+                                    64 * pp, g, 0, page);
+                    }
+                }
+            }
+        } else if (lane == 0) {
             for (int t = 0; t < ntiles; ++t) {
                 const int st = t % STAGES;
                 if (!mbar_wait(empty_bar(st), ((t / STAGES) & 1) ^ 1, abort_flag, &g_dec_status))
                     break;
                 const uint32_t kdst = sbase + st * L::kStageBytes;
                 const int key0 = j0 + t * kTileKeys;
-                if constexpr (PAGED) {
+                if (PAGED) {  // pages of 64 or more keys: one box per panel
                     const int ps = p.page_size;
-                    if (ps >= kTileKeys) {
-                        mbar_arrive_expect_tx(full_bar(st), L::kStageBytes);
-                        const int page = tab[key0 / ps - first_page];
-                        const int row = key0 % ps;
+                    mbar_arrive_expect_tx(full_bar(st), L::kStageBytes);
+                    const int page = tab[key0 / ps - first_page];
+                    const int row = key0 % ps;
 #pragma unroll
-                        for (int pp = 0; pp < D / 64; ++pp) {
-                            tma_load_4d(kdst + pp * L::kPanelBytes, &tmK, full_bar(st), 64 * pp, g, row,
-                                        page);
-                            tma_load_4d(kdst + L::kTileBytes + pp * L::kPanelBytes, &tmV, full_bar(st),
-                                        64 * pp, g, row, page);
-                        }
-                    } else {
-                        const int nsub = min(kTileKeys / ps, (j1 - key0 + ps - 1) / ps);
-                        mbar_arrive_expect_tx(full_bar(st), (uint32_t)(nsub * ps * D * 2 * 2));
-                        for (int r = 0; r < nsub; ++r) {
-                            const int page = tab[(key0 + r * ps) / ps - first_page];
-                            const uint32_t off = (uint32_t)(r * ps * 128);
-#pragma unroll
-                            for (int pp = 0; pp < D / 64; ++pp) {
-                                tma_load_4d(kdst + pp * L::kPanelBytes + off, &tmK, full_bar(st), 64 * pp,
-                                            g, 0, page);
-                                tma_load_4d(kdst + L::kTileBytes + pp * L::kPanelBytes + off, &tmV,
-                                            full_bar(st), 64 * pp, g, 0, page);
-                            }
-                        }
+                    for (int pp = 0; pp < D / 64; ++pp) {
+                        tma_load_4d(kdst + pp * L::kPanelBytes, &tmK, full_bar(st), 64 * pp, g, row, page);
+                        tma_load_4d(kdst + L::kTileBytes + pp * L::kPanelBytes, &tmV, full_bar(st),
+                                    64 * pp, g, row, page);
                     }
                 } else {
                     mbar_arrive_expect_tx(full_bar(st), L::kStageBytes);
