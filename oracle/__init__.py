@@ -256,3 +256,48 @@ def decode_paged(q, k_pages, v_pages, block_table, seq_lens, scale: float):
         o[b] = ob[0]
         lse[b] = lb[0, :, 0]
     return o, lse
+
+
+def attn_bwd(q, k, v, do, causal: bool, scale: float):
+    """Gradients of algorithm 0 (Lecture 11, section 5.1), float64.
+
+    With S = scale Q K^T (masked entries -inf), P = softmax(S) row-wise and
+    O = P V, given dO:  dV = P^T dO;  dP = dO V^T;  D_i = sum_j P_ij dP_ij,
+    which equals rowsum(dO_i * O_i) (the identity section 5.1 uses so that
+    D needs only a row of O and dO);  dS = P * (dP - D);  dQ = scale dS K;
+    dK = scale dS^T Q.  Query head hq uses KV head hq // (Hq / Hkv), so a KV
+    head's dK and dV sum over its query heads.  A row with no allowed key has
+    P = 0 and contributes nothing.  Inputs [B, N, H, d] (any float type);
+    returns (dq, dk, dv) float64 in the shapes of q, k, v.
+    """
+    q = np.asarray(_f32(q), np.float64)
+    k = np.asarray(_f32(k), np.float64)
+    v = np.asarray(_f32(v), np.float64)
+    do = np.asarray(_f32(do), np.float64)
+    B, Nq, Hq, d = q.shape
+    _, Nk, Hkv, _ = k.shape
+    G = Hq // Hkv
+    dq = np.zeros_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    i_idx = np.arange(Nq)[:, None]
+    j_idx = np.arange(Nk)[None, :]
+    allowed = np.ones((Nq, Nk), bool) if not causal else (j_idx <= i_idx + (Nk - Nq))
+    for b in range(B):
+        for hq in range(Hq):
+            g = hq // G
+            Q, K, V, dO = q[b, :, hq, :], k[b, :, g, :], v[b, :, g, :], do[b, :, hq, :]
+            S = np.where(allowed, scale * (Q @ K.T), -np.inf)
+            m = S.max(axis=1)
+            has = np.isfinite(m)
+            E = np.where(has[:, None], np.exp(S - np.where(has, m, 0.0)[:, None]), 0.0)
+            den = E.sum(axis=1)
+            P = np.where(has[:, None], E / np.where(has, den, 1.0)[:, None], 0.0)
+            O = P @ V
+            dv[b, :, g, :] += P.T @ dO
+            dP = dO @ V.T
+            D = (dO * O).sum(axis=1)
+            dS = P * (dP - D[:, None])
+            dq[b, :, hq, :] = scale * (dS @ K)
+            dk[b, :, g, :] += scale * (dS.T @ Q)
+    return dq, dk, dv

@@ -392,3 +392,51 @@ def test_paged_decode_ignores_slots_past_the_length(oracle_mod):
             vp2[table[b, j // 4], j % 4] = np.nan
     o2, l2 = oracle_mod.decode_paged(q, kp2, vp2, table, lens, 0.7)
     assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
+# ---------------------------------------------------------------- backward
+def _bwd_case(seed, B=1, Hq=2, Hkv=1, Nq=5, Nk=6, d=3):
+    rng = np.random.default_rng(seed)
+    q, k, v, do = (rng.standard_normal(s).astype(np.float32)
+                   for s in ((B, Nq, Hq, d), (B, Nk, Hkv, d), (B, Nk, Hkv, d), (B, Nq, Hq, d)))
+    return q, k, v, do
+
+
+@pytest.mark.parametrize("causal,Nq,Nk", [(False, 5, 6), (True, 5, 6), (True, 7, 4)])
+def test_backward_matches_finite_differences(oracle_mod, causal, Nq, Nk):
+    """Central differences of L = sum(O * dO), with O from the forward oracle,
+    against the backward's dQ, dK, dV (Lecture 11 section 5.1 reports ~1e-9
+    with double inputs; here inputs are float32, stepped by 2^-10, which is
+    exact for them, and the forward runs in double).  The Nq > Nk causal case
+    has rows with no allowed key."""
+    q, k, v, do = _bwd_case(11 + Nq, Nq=Nq, Nk=Nk)
+    scale = 0.7
+    h = 2.0 ** -10
+
+    def loss(qq, kk, vv):
+        o, _ = oracle_mod.attn_fwd(qq, kk, vv, causal, scale)
+        return float((o * do.astype(np.float64)).sum())
+
+    dq, dk, dv = oracle_mod.attn_bwd(q, k, v, do, causal, scale)
+    for name, x, grad in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+        fd = np.zeros(x.shape)
+        for idx in np.ndindex(*x.shape):
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += np.float32(h)
+            xm[idx] -= np.float32(h)
+            args_p = {"q": (xp, k, v), "k": (q, xp, v), "v": (q, k, xp)}[name]
+            args_m = {"q": (xm, k, v), "k": (q, xm, v), "v": (q, k, xm)}[name]
+            fd[idx] = (loss(*args_p) - loss(*args_m)) / (2 * h)
+        assert np.abs(fd - grad).max() <= 2e-6 * max(1.0, np.abs(grad).max()), name
+
+
+def test_backward_gqa_sums_over_the_group(oracle_mod):
+    """A KV head shared by two query heads gets the sum of the gradients it
+    would get as two separate (duplicated) KV heads."""
+    q, k, v, do = _bwd_case(21, Hq=2, Hkv=1, Nq=6, Nk=6, d=4)
+    dq1, dk1, dv1 = oracle_mod.attn_bwd(q, k, v, do, True, 0.5)
+    k2, v2 = np.repeat(k, 2, axis=2), np.repeat(v, 2, axis=2)
+    dq2, dk2, dv2 = oracle_mod.attn_bwd(q, k2, v2, do, True, 0.5)
+    assert np.allclose(dq1, dq2, atol=1e-13)
+    assert np.allclose(dk1[:, :, 0], dk2.sum(axis=2), atol=1e-13)
+    assert np.allclose(dv1[:, :, 0], dv2.sum(axis=2), atol=1e-13)
