@@ -21,7 +21,7 @@ __all__ = [
     "attn_decode_splitkv", "attn_merge_lse", "attn_status_string",
     "attn_check_device_status", "attn_read_tile_counter", "attn_version",
     "attn_decode_splitkv_static", "attn_decode_paged", "attn_decode_paged_num_splits",
-    "DECODE_STATIC_SCRATCH_BYTES", "EXPORTED_SYMBOLS",
+    "attn_bwd", "attn_bwd_workspace_bytes", "DECODE_STATIC_SCRATCH_BYTES", "EXPORTED_SYMBOLS",
 ]
 
 ATTN_OK, ATTN_ERR_INVALID, ATTN_ERR_UNSUPPORTED, ATTN_ERR_CUDA, ATTN_ERR_TIMEOUT = range(5)
@@ -33,6 +33,7 @@ EXPORTED_SYMBOLS = (
     "attn_decode_splitkv", "attn_merge_lse", "attn_status_string",
     "attn_check_device_status", "attn_read_tile_counter", "attn_version",
     "attn_decode_splitkv_static", "attn_decode_paged", "attn_decode_paged_num_splits",
+    "attn_bwd", "attn_bwd_workspace_bytes",
 )
 
 # Size of the scratch area built into the library for attn_decode_splitkv_static.
@@ -98,6 +99,10 @@ def lib() -> ctypes.CDLL:
     L.attn_decode_paged.restype = I
     L.attn_decode_paged_num_splits.argtypes = [I, I, I, I, I, I]
     L.attn_decode_paged_num_splits.restype = I
+    L.attn_bwd_workspace_bytes.argtypes = [I, I, I]
+    L.attn_bwd_workspace_bytes.restype = SZ
+    L.attn_bwd.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, P, SZ, I, P]
+    L.attn_bwd.restype = I
     L.attn_decode_splitkv_static.restype = I
     _lib = L
     return L
@@ -335,3 +340,38 @@ def attn_decode_paged(q, k_pages, v_pages, block_table, seq_lens, max_seq_len: i
                                  _stream(stream))
     _check("attn_decode_paged", st)
     return o, lse
+
+
+def attn_bwd_workspace_bytes(B: int, Hq: int, Nq: int) -> int:
+    return int(lib().attn_bwd_workspace_bytes(B, Hq, Nq))
+
+
+def attn_bwd(q, k, v, o, lse, dout, causal: bool, scale: float | None = None, dq=None, dk=None,
+             dv=None, workspace=None, stream=None):
+    """Backward of attn_fwd: q, o, dout [B, Nq, Hq, d]; k, v [B, Nk, Hkv, d] (bf16);
+    lse [B, Hq, Nq] float32 from the forward.  Returns (dq, dk, dv)."""
+    import torch
+    B, Nq, Hq, d = q.shape
+    Bk, Nk, Hkv, dk_ = k.shape
+    if Bk != B or dk_ != d or tuple(v.shape) != tuple(k.shape):
+        raise ValueError("shape mismatch between q and k/v")
+    if tuple(o.shape) != tuple(q.shape) or tuple(dout.shape) != tuple(q.shape):
+        raise ValueError("o and dout must have q's shape")
+    if tuple(lse.shape) != (B, Hq, Nq):
+        raise ValueError("lse must be [B, Hq, Nq]")
+    for n, t in (("q", q), ("k", k), ("v", v), ("o", o), ("lse", lse), ("dout", dout)):
+        _need_cuda_contig(n, t)
+    if scale is None:
+        scale = d ** -0.5
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    wbytes = attn_bwd_workspace_bytes(B, Hq, Nq)
+    if workspace is None:
+        workspace = torch.empty(max(16, wbytes), dtype=torch.uint8, device=q.device)
+    wsize = workspace.numel() * workspace.element_size()
+    st = lib().attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq),
+                        _ptr(dk), _ptr(dv), B, Hq, Hkv, Nq, Nk, d, int(bool(causal)),
+                        float(scale), _ptr(workspace), wsize, _dtype_code(q), _stream(stream))
+    _check("attn_bwd", st)
+    return dq, dk, dv

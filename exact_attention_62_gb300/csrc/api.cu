@@ -227,6 +227,35 @@ attn_status_t attn_decode_paged(const void* q, const void* k_pages, const void* 
                                           max_seq_len, scale, S, workspace, st);
 }
 
+size_t attn_bwd_workspace_bytes(int B, int Hq, int Nq) {
+    if (B < 0 || Hq < 0 || Nq < 0) return 0;
+    return attn_host::bwd_workspace_bytes(B, Hq, Nq);
+}
+
+attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                       const void* dout, void* dq, void* dk, void* dv, int B, int Hq, int Hkv,
+                       int Nq, int Nk, int d, int causal, float scale, void* workspace,
+                       size_t workspace_bytes, attn_dtype_t dtype, void* stream) {
+    if (B < 0 || Hq < 0 || Hkv < 1 || Nq < 0 || Nk < 0 || d < 1) return ATTN_ERR_INVALID;
+    if (causal != 0 && causal != 1) return ATTN_ERR_INVALID;
+    if (dtype != ATTN_BF16 && dtype != ATTN_F32) return ATTN_ERR_INVALID;
+    if (bad_scale(scale)) return ATTN_ERR_INVALID;
+    if (Hq % Hkv != 0) return ATTN_ERR_INVALID;
+    if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+    if (dtype != ATTN_BF16) return ATTN_ERR_UNSUPPORTED;
+    if (B == 0 || Hq == 0 || (Nq == 0 && Nk == 0)) return ATTN_OK;
+    if (Nq == 0 || Nk == 0) return ATTN_ERR_UNSUPPORTED;  // empty sides: nothing to differentiate
+    const void* ptrs[] = {q, k, v, o, dout, dq, dk, dv};
+    for (const void* ptr : ptrs)
+        if (ptr == nullptr || misaligned(ptr, 16)) return ATTN_ERR_INVALID;
+    if (lse == nullptr || misaligned(lse, 4)) return ATTN_ERR_INVALID;
+    if (workspace == nullptr || misaligned(workspace, 16) ||
+        workspace_bytes < attn_host::bwd_workspace_bytes(B, Hq, Nq))
+        return ATTN_ERR_INVALID;
+    return attn_host::launch_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, Nq, Nk, d, causal,
+                                 scale, workspace, static_cast<cudaStream_t>(stream));
+}
+
 attn_status_t attn_merge_lse(const float* o_parts, const float* lse_parts, int num_parts,
                              long long rows, int d, void* o, float* lse, attn_dtype_t out_dtype,
                              void* stream) {
@@ -254,10 +283,11 @@ const char* attn_status_string(attn_status_t status) {
 
 attn_status_t attn_check_device_status(void) {
     if (cudaDeviceSynchronize() != cudaSuccess) return ATTN_ERR_CUDA;
-    unsigned a = 0, b = 0;
+    unsigned a = 0, b = 0, c = 0;
     if (attn_host::fwd_tc_read_status(&a, true) != cudaSuccess) return ATTN_ERR_CUDA;
     if (attn_host::decode_read_status(&b, true) != cudaSuccess) return ATTN_ERR_CUDA;
-    return (a | b) ? ATTN_ERR_TIMEOUT : ATTN_OK;
+    if (attn_host::bwd_read_status(&c, true) != cudaSuccess) return ATTN_ERR_CUDA;
+    return (a | b | c) ? ATTN_ERR_TIMEOUT : ATTN_OK;
 }
 
 attn_status_t attn_read_tile_counter(unsigned long long* count, int reset) {

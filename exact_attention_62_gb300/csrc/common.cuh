@@ -49,6 +49,14 @@ attn_status_t launch_decode_paged(const void* q, const void* k_pages, const void
                                   int max_pages, int max_seq_len, float scale, int splits,
                                   void* workspace, cudaStream_t stream);
 
+// ---- backward pass (bwd_tc.cu)
+size_t bwd_workspace_bytes(int B, int Hq, int Nq);
+attn_status_t launch_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                         const void* dout, void* dq, void* dk, void* dv, int B, int Hq, int Hkv,
+                         int Nq, int Nk, int d, int causal, float scale, void* workspace,
+                         cudaStream_t stream);
+cudaError_t bwd_read_status(unsigned* out, bool clear);
+
 // ---- small utility kernels (api.cu)
 attn_status_t launch_fill_empty(void* o, float* lse, long long rows_o, int d, long long n_lse,
                                 bool out_bf16, cudaStream_t stream);

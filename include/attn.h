@@ -219,6 +219,31 @@ int attn_decode_paged_num_splits(int B, int Hq, int Hkv, int d, int page_size,
                                  int max_seq_len);
 
 /*
+ * attn_bwd -- backward pass of attn_fwd ([L11] 5.1): given dO, the gradients
+ *     dV = P^T dO,  dP = dO V^T,  D_i = rowsum(dO_i * O_i),
+ *     dS = P * (dP - D),  dQ = scale dS K,  dK = scale dS^T Q,
+ * with P recomputed from the forward's LSE, P_ij = exp(S_ij - LSE_i), and a
+ * KV head's dK, dV summed over the query heads that share it.
+ *
+ *   q, o, dout  [B, Nq, Hq, d] bf16 (o: the forward's output);
+ *   k, v        [B, Nk, Hkv, d] bf16;
+ *   lse         [B, Hq, Nq] float32 (the forward's LSE);
+ *   dq          [B, Nq, Hq, d] bf16 output;  dk, dv [B, Nk, Hkv, d] bf16 output.
+ *   causal, scale: as in the forward call that produced o and lse.
+ *   workspace   at least attn_bwd_workspace_bytes(B, Hq, Nq) bytes, 16-byte
+ *               aligned (holds D); d is 64 or 128; dtype ATTN_BF16 only.
+ * Every gradient is written exactly once (no atomics, no zero-fill needed);
+ * rows and keys that no allowed (row, key) pair touches get 0.  Three kernels
+ * run on `stream`: D, then dK/dV (key tile outer), then dQ (query tile outer).
+ */
+size_t attn_bwd_workspace_bytes(int B, int Hq, int Nq);
+attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o,
+                       const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                       int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal,
+                       float scale, void* workspace, size_t workspace_bytes,
+                       attn_dtype_t dtype, void* stream);
+
+/*
  * attn_merge_lse -- exact merge of partial attention results in log-sum-exp
  * form ([L11] 6.2 step 3; the associative merge of [L11] 3.2):
  *     lse[r] = log sum_p exp(lse_parts[p, r])

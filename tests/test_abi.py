@@ -153,3 +153,21 @@ def test_paged_decode_declares_its_auto_split_rule():
     # pages a segment touches must fit the 4096-entry staging area; the rule is host arithmetic
     assert pkg.attn_decode_workspace_bytes(2, 8, 2, 200, 128, 3) == \
         (3 * 16 * 128 * 4 + 255) // 256 * 256 + 3 * 16 * 4
+
+
+def bwd(L, B=1, Hq=2, Hkv=1, Nq=8, Nk=8, d=64, causal=0, scale=0.125, ws=FAKE, wbytes=1 << 20,
+        dtype=BF16):
+    return L.attn_bwd(FAKE, FAKE, FAKE, FAKE, FAKE_LSE, FAKE, FAKE, FAKE, FAKE, B, Hq, Hkv, Nq, Nk,
+                      d, causal, scale, ws, wbytes, dtype, None)
+
+
+def test_bwd_rejects_bad_arguments(L):
+    assert bwd(L, d=96) == UNSUPPORTED
+    assert bwd(L, dtype=F32) == UNSUPPORTED
+    assert bwd(L, Hq=3, Hkv=2) == INVALID
+    assert bwd(L, causal=2) == INVALID
+    assert bwd(L, scale=float("nan")) == INVALID
+    assert bwd(L, ws=None) == INVALID
+    assert bwd(L, wbytes=16) == INVALID          # D needs B*Hq*Nq floats
+    assert bwd(L, B=0) == OK
+    assert pkg.attn_bwd_workspace_bytes(2, 3, 100) == (2 * 3 * 100 * 4 + 255) // 256 * 256

@@ -1,0 +1,74 @@
+"""Parity of attn_bwd against the oracle's backward (Lecture 11, section 5.1).
+
+Tolerance, from the arithmetic: the gradients are bf16 outputs of fp32 sums
+whose terms use bf16 P and dS, so each element carries the 2^-9 relative
+rounding of its own value plus about 2^-9 of the magnitude of the sum's
+terms.  Required: max|d - ref| <= 1e-2 * max(1, max|ref|) per tensor (the
+measured ratio is at most 0.005) and RMS(d - ref) / RMS(ref) <= 5e-3
+(measured 0.0022-0.0026), which a 1% error in any scale factor would fail.
+The forward output and LSE that feed the backward come from attn_fwd."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from exact_attention_62_gb300.inputs import make_qkv
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+CASES = [
+    # B, Hq, Hkv, Nq, Nk, d, causal
+    (1, 2, 2, 256, 256, 64, False),
+    (1, 2, 1, 300, 300, 128, True),      # GQA 2, ragged
+    (2, 4, 2, 520, 520, 128, True),
+    (1, 2, 2, 257, 700, 64, False),      # Nq != Nk
+    (1, 4, 4, 1000, 300, 128, True),     # causal rows with no allowed key
+    (1, 2, 2, 300, 1000, 64, True),      # Nk > Nq, bottom-right causal
+    (1, 8, 1, 384, 384, 128, True),      # GQA 8
+    (1, 4, 4, 2048, 2048, 128, True),
+]
+
+
+def check(name, gpu, ref):
+    g = gpu.float().cpu().numpy().astype(np.float64)
+    assert np.all(np.isfinite(g)), name
+    err = np.abs(g - ref)
+    assert err.max() <= 1e-2 * max(1.0, np.abs(ref).max()), (name, err.max(), np.abs(ref).max())
+    rms = np.sqrt((ref ** 2).mean())
+    if rms > 0:
+        assert np.sqrt((err ** 2).mean()) / rms <= 5e-3, (name, np.sqrt((err ** 2).mean()) / rms)
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Nq,Nk,d,causal", CASES)
+def test_backward_matches_oracle(attn, oracle_mod, B, Hq, Hkv, Nq, Nk, d, causal):
+    q, k, v = make_qkv(B, Hq, Hkv, Nq, Nk, d, 5)
+    g = torch.Generator().manual_seed(6)
+    dout = torch.randn((B, Nq, Hq, d), generator=g).to(torch.bfloat16)
+    scale = 1.0 / math.sqrt(d)
+    qg, kg, vg, dog = q.to(DEV), k.to(DEV), v.to(DEV), dout.to(DEV)
+    o, lse = attn.attn_fwd(qg, kg, vg, causal, scale)
+    dq, dk, dv = attn.attn_bwd(qg, kg, vg, o, lse, dog, causal, scale)
+    torch.cuda.synchronize()
+    assert attn.attn_check_device_status() == 0
+    rq, rk, rv = oracle_mod.attn_bwd(q, k, v, dout, causal, scale)
+    check("dq", dq, rq)
+    check("dk", dk, rk)
+    check("dv", dv, rv)
+
+
+def test_backward_writes_zeros_where_nothing_flows(attn):
+    """Rows with no allowed key (causal, Nq > Nk) get dQ = 0; every output is
+    written even when the destination held garbage."""
+    B, H, Nq, Nk, d = 1, 2, 700, 200, 128
+    q, k, v = (x.to(DEV) for x in make_qkv(B, H, H, Nq, Nk, d, 8))
+    o, lse = attn.attn_fwd(q, k, v, True, 0.1)
+    dout = torch.randn_like(q)
+    dq = torch.full_like(q, float("nan"))
+    dk = torch.full_like(k, float("nan"))
+    dv = torch.full_like(v, float("nan"))
+    attn.attn_bwd(q, k, v, o, lse, dout, True, 0.1, dq=dq, dk=dk, dv=dv)
+    torch.cuda.synchronize()
+    assert torch.isfinite(dq).all() and torch.isfinite(dk).all() and torch.isfinite(dv).all()
+    assert torch.all(dq[:, :Nq - Nk] == 0)    # rows 0 .. Nq-Nk-1 see no key
