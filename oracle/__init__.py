@@ -301,3 +301,65 @@ def attn_bwd(q, k, v, do, causal: bool, scale: float):
             dq[b, :, hq, :] = scale * (dS @ K)
             dk[b, :, g, :] += scale * (dS.T @ Q)
     return dq, dk, dv
+
+
+# ------------------------------------------------------------------ FP8 (block quantisation)
+FP8_MAX = 448.0  # largest finite e4m3 value
+
+
+def quantize_fp8_blocks(x, block: int = 128):
+    """Block quantisation to e4m3 (Lecture 11, section 4.5, FP8 item: block
+    quantisation).  x [B, N, H, d] -> (codes uint8 [B, N, H, d], scales
+    float32 [B, H, ceil(N / block)]).  Per (b, h, block of `block` rows):
+    amax = max |x| (as float32), scale = amax / 448 and inv = 448 / amax in
+    float32 (1 and 1 for an all-zero block), code = e4m3(round to nearest
+    even, clamped to +-448)(x * inv) with x * inv in float32."""
+    import torch
+    xt = torch.as_tensor(np.asarray(_f32(x)))
+    B, N, H, d = xt.shape
+    nb = (N + block - 1) // block
+    codes = torch.zeros((B, N, H, d), dtype=torch.uint8)
+    scales = torch.ones((B, H, nb), dtype=torch.float32)
+    for bi in range(nb):
+        r0, r1 = bi * block, min(N, (bi + 1) * block)
+        blk = xt[:, r0:r1]                                    # [B, rows, H, d]
+        amax = blk.abs().amax(dim=(1, 3))                     # [B, H] float32
+        nz = amax > 0
+        one = torch.ones_like(amax)
+        inv = torch.where(nz, torch.full_like(amax, FP8_MAX) / torch.where(nz, amax, one), one)
+        sc = torch.where(nz, amax / FP8_MAX, one)
+        y = (blk * inv[:, None, :, None]).clamp(-FP8_MAX, FP8_MAX)
+        codes[:, r0:r1] = y.to(torch.float8_e4m3fn).view(torch.uint8)
+        scales[:, :, bi] = sc
+    return codes.numpy(), scales.numpy()
+
+
+def dequantize_fp8_blocks(codes, scales, block: int = 128):
+    """codes uint8 [B, N, H, d] (e4m3) and scales [B, H, nblocks] -> float64."""
+    import torch
+    c = torch.as_tensor(np.asarray(codes, np.uint8)).view(torch.float8_e4m3fn).to(torch.float64)
+    s = torch.as_tensor(np.asarray(scales, np.float32)).to(torch.float64)
+    B, N, H, d = c.shape
+    rows = torch.arange(N) // block
+    return (c * s[:, :, rows].permute(0, 2, 1)[..., None]).numpy()
+
+
+def score_perturbation(q_a, k_a, q_b, k_b, causal: bool, scale: float):
+    """Per query row, max over allowed keys of |S_a - S_b| with S = scale q k^T
+    (the two inputs e.g. dequantised and exact).  Returns [B, Hq, Nq] float64
+    (0 for rows with no allowed key)."""
+    qa, ka = np.asarray(q_a, np.float64), np.asarray(k_a, np.float64)
+    qb, kb = np.asarray(q_b, np.float64), np.asarray(k_b, np.float64)
+    B, Nq, Hq, d = qa.shape
+    Nk, Hkv = ka.shape[1], ka.shape[2]
+    G = Hq // Hkv
+    out = np.zeros((B, Hq, Nq))
+    allowed = np.ones((Nq, Nk), bool)
+    if causal:
+        allowed = np.arange(Nk)[None, :] <= np.arange(Nq)[:, None] + (Nk - Nq)
+    for b in range(B):
+        for h in range(Hq):
+            g = h // G
+            dS = scale * (qa[b, :, h] @ ka[b, :, g].T - qb[b, :, h] @ kb[b, :, g].T)
+            out[b, h] = np.where(allowed, np.abs(dS), 0.0).max(axis=1)
+    return out

@@ -440,3 +440,62 @@ def test_backward_gqa_sums_over_the_group(oracle_mod):
     assert np.allclose(dq1, dq2, atol=1e-13)
     assert np.allclose(dk1[:, :, 0], dk2.sum(axis=2), atol=1e-13)
     assert np.allclose(dv1[:, :, 0], dv2.sum(axis=2), atol=1e-13)
+
+
+# ---------------------------------------------------------------- FP8 block quantisation
+def _e4m3_value(code):
+    """The e4m3 (finite-only variant) format from its definition: sign bit,
+    4 exponent bits with bias 7, 3 mantissa bits, subnormals at exponent 0,
+    and exponent 15 with mantissa 7 reserved for NaN."""
+    s = -1.0 if code & 0x80 else 1.0
+    e = (code >> 3) & 0xF
+    m = code & 0x7
+    if e == 15 and m == 7:
+        return float("nan")
+    if e == 0:
+        return s * (m / 8.0) * 2.0 ** (1 - 7)
+    return s * (1.0 + m / 8.0) * 2.0 ** (e - 7)
+
+
+def test_fp8_codes_decode_as_the_format_defines(oracle_mod):
+    codes = np.arange(256, dtype=np.uint8).reshape(1, 1, 1, 256)
+    got = oracle_mod.dequantize_fp8_blocks(codes, np.ones((1, 1, 1), np.float32))
+    want = np.array([_e4m3_value(c) for c in range(256)])
+    both_nan = np.isnan(got.ravel()) & np.isnan(want)
+    assert np.all(both_nan | (got.ravel() == want))
+    assert np.nanmax(want) == oracle_mod.FP8_MAX
+
+
+def test_fp8_block_quantisation_properties(oracle_mod):
+    rng = np.random.default_rng(4)
+    x = rng.standard_normal((2, 300, 3, 64)).astype(np.float32)
+    x[1, 128:256, 2] = 0.0                      # an all-zero block
+    codes, scales = oracle_mod.quantize_fp8_blocks(x)
+    assert codes.dtype == np.uint8 and scales.shape == (2, 3, 3)
+    assert scales[1, 2, 1] == 1.0 and np.all(codes[1, 128:256, 2] == 0)
+    deq = oracle_mod.dequantize_fp8_blocks(codes, scales)
+    for b in range(2):
+        for h in range(3):
+            for bi in range(3):
+                blk = x[b, bi * 128:(bi + 1) * 128, h].astype(np.float64)
+                dq = deq[b, bi * 128:(bi + 1) * 128, h]
+                amax = np.abs(blk).max()
+                if amax == 0:
+                    continue
+                # the block's largest element maps to +-448 and back to ~amax
+                assert np.isclose(np.abs(dq).max(), amax, rtol=1e-6)
+                # e4m3 rounding: half a step of 2^-3 relative for normals, and
+                # half the subnormal step 2^-9 (times the scale) near zero
+                step = np.maximum(np.abs(blk) * 2.0 ** -4, 0.5 * 2.0 ** -9 * amax / 448.0)
+                assert np.all(np.abs(dq - blk) <= step * (1 + 1e-6))
+
+
+def test_score_perturbation_is_the_max_score_change(oracle_mod):
+    rng = np.random.default_rng(5)
+    q = rng.standard_normal((1, 4, 2, 8))
+    k = rng.standard_normal((1, 5, 1, 8))
+    q2 = q.copy()
+    q2[0, 1, 1, 0] += 0.5                       # row 1 of head 1 only
+    d = oracle_mod.score_perturbation(q2, k, q, k, False, 0.25)
+    assert np.all(d[0, 0] == 0) and np.all(d[0, 1, [0, 2, 3]] == 0)
+    assert d[0, 1, 1] == pytest.approx(0.25 * 0.5 * np.abs(k[0, :, 0, 0]).max())
