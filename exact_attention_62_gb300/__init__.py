@@ -21,7 +21,8 @@ __all__ = [
     "attn_decode_splitkv", "attn_merge_lse", "attn_status_string",
     "attn_check_device_status", "attn_read_tile_counter", "attn_version",
     "attn_decode_splitkv_static", "attn_decode_paged", "attn_decode_paged_num_splits",
-    "attn_bwd", "attn_bwd_workspace_bytes", "DECODE_STATIC_SCRATCH_BYTES", "EXPORTED_SYMBOLS",
+    "attn_bwd", "attn_bwd_workspace_bytes", "attn_quantize_fp8", "attn_fwd_fp8",
+    "DECODE_STATIC_SCRATCH_BYTES", "EXPORTED_SYMBOLS",
 ]
 
 ATTN_OK, ATTN_ERR_INVALID, ATTN_ERR_UNSUPPORTED, ATTN_ERR_CUDA, ATTN_ERR_TIMEOUT = range(5)
@@ -33,7 +34,7 @@ EXPORTED_SYMBOLS = (
     "attn_decode_splitkv", "attn_merge_lse", "attn_status_string",
     "attn_check_device_status", "attn_read_tile_counter", "attn_version",
     "attn_decode_splitkv_static", "attn_decode_paged", "attn_decode_paged_num_splits",
-    "attn_bwd", "attn_bwd_workspace_bytes",
+    "attn_bwd", "attn_bwd_workspace_bytes", "attn_quantize_fp8", "attn_fwd_fp8",
 )
 
 # Size of the scratch area built into the library for attn_decode_splitkv_static.
@@ -103,6 +104,10 @@ def lib() -> ctypes.CDLL:
     L.attn_bwd_workspace_bytes.restype = SZ
     L.attn_bwd.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, P, SZ, I, P]
     L.attn_bwd.restype = I
+    L.attn_quantize_fp8.argtypes = [P, P, P, I, I, I, I, P]
+    L.attn_quantize_fp8.restype = I
+    L.attn_fwd_fp8.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, P]
+    L.attn_fwd_fp8.restype = I
     L.attn_decode_splitkv_static.restype = I
     _lib = L
     return L
@@ -375,3 +380,44 @@ def attn_bwd(q, k, v, o, lse, dout, causal: bool, scale: float | None = None, dq
                         float(scale), _ptr(workspace), wsize, _dtype_code(q), _stream(stream))
     _check("attn_bwd", st)
     return dq, dk, dv
+
+
+def attn_quantize_fp8(x, codes=None, scales=None, stream=None):
+    """Block quantisation of a bf16 [B, N, H, d] tensor to e4m3 codes (uint8)
+    with one float32 scale per (batch, head, 128-row block).  Returns
+    (codes [B, N, H, d] uint8, scales [B, H, ceil(N/128)] float32)."""
+    import torch
+    B, N, H, d = x.shape
+    _need_cuda_contig("x", x)
+    if x.dtype != torch.bfloat16:
+        raise ValueError("x must be bfloat16")
+    codes = torch.empty(x.shape, dtype=torch.uint8, device=x.device) if codes is None else codes
+    nb = (N + 127) // 128
+    scales = torch.empty((B, H, nb), dtype=torch.float32, device=x.device) if scales is None else scales
+    st = lib().attn_quantize_fp8(_ptr(x), _ptr(codes), _ptr(scales), B, N, H, d, _stream(stream))
+    _check("attn_quantize_fp8", st)
+    return codes, scales
+
+
+def attn_fwd_fp8(q8, k8, v, q_scales, k_scales, causal: bool, scale: float | None = None, o=None,
+                 lse=None, stream=None):
+    """Forward with e4m3 Q and K codes and their block scales (from
+    attn_quantize_fp8), bf16 V.  Returns (o [B, Nq, Hq, d] bf16, lse [B, Hq, Nq])."""
+    import torch
+    B, Nq, Hq, d = q8.shape
+    Bk, Nk, Hkv, dk = k8.shape
+    if Bk != B or dk != d or tuple(v.shape) != tuple(k8.shape):
+        raise ValueError("shape mismatch")
+    if q8.dtype != torch.uint8 or k8.dtype != torch.uint8 or v.dtype != torch.bfloat16:
+        raise ValueError("q8 and k8 must be uint8 e4m3 codes and v bfloat16")
+    for n, t in (("q8", q8), ("k8", k8), ("v", v), ("q_scales", q_scales), ("k_scales", k_scales)):
+        _need_cuda_contig(n, t)
+    if scale is None:
+        scale = d ** -0.5
+    o = torch.empty((B, Nq, Hq, d), dtype=torch.bfloat16, device=v.device) if o is None else o
+    lse = torch.empty((B, Hq, Nq), dtype=torch.float32, device=v.device) if lse is None else lse
+    st = lib().attn_fwd_fp8(_ptr(q8), _ptr(k8), _ptr(v), _ptr(q_scales), _ptr(k_scales), _ptr(o),
+                            _ptr(lse), B, Hq, Hkv, Nq, Nk, d, int(bool(causal)), float(scale),
+                            _stream(stream))
+    _check("attn_fwd_fp8", st)
+    return o, lse

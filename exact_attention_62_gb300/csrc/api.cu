@@ -62,8 +62,9 @@ bool encode_bshd_map(CUtensorMap* map, const void* base, int B, int N, int H, in
     cuuint64_t strides[3] = {(cuuint64_t)d * e, (cuuint64_t)H * d * e, (cuuint64_t)N * H * d * e};
     cuuint32_t box[4] = {(cuuint32_t)(128 / elem_bytes), 1u, (cuuint32_t)box_rows, 1u};
     cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
-    const CUtensorMapDataType dt =
-        elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    const CUtensorMapDataType dt = elem_bytes == 2   ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                   : elem_bytes == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                                     : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
     return fn(map, dt, 4, const_cast<void*>(base), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
@@ -225,6 +226,39 @@ attn_status_t attn_decode_paged(const void* q, const void* k_pages, const void* 
     return attn_host::launch_decode_paged(q, k_pages, v_pages, block_table, seq_lens, o, lse, B,
                                           Hq, Hkv, d, num_pages, page_size, max_pages_per_seq,
                                           max_seq_len, scale, S, workspace, st);
+}
+
+attn_status_t attn_quantize_fp8(const void* x, void* codes, float* scales, int B, int N, int H,
+                                int d, void* stream) {
+    if (B < 0 || N < 0 || H < 0 || d < 2 || d % 2 != 0) return ATTN_ERR_INVALID;
+    if (B == 0 || N == 0 || H == 0) return ATTN_OK;
+    if (x == nullptr || codes == nullptr || scales == nullptr) return ATTN_ERR_INVALID;
+    if (misaligned(x, 16) || misaligned(codes, 16) || misaligned(scales, 4)) return ATTN_ERR_INVALID;
+    return attn_host::launch_quantize_fp8(x, codes, scales, B, N, H, d, static_cast<cudaStream_t>(stream));
+}
+
+attn_status_t attn_fwd_fp8(const void* q8, const void* k8, const void* v, const float* q_scales,
+                           const float* k_scales, void* o, float* lse, int B, int Hq, int Hkv, int Nq,
+                           int Nk, int d, int causal, float scale, void* stream) {
+    if (B < 0 || Hq < 0 || Hkv < 1 || Nq < 0 || Nk < 0 || d < 1) return ATTN_ERR_INVALID;
+    if (causal != 0 && causal != 1) return ATTN_ERR_INVALID;
+    if (bad_scale(scale)) return ATTN_ERR_INVALID;
+    if (Hq % Hkv != 0) return ATTN_ERR_INVALID;
+    if (d != 128) return ATTN_ERR_UNSUPPORTED;
+    if (B == 0 || Hq == 0 || Nq == 0) return ATTN_OK;
+    if (o == nullptr || lse == nullptr) return ATTN_ERR_INVALID;
+    if (misaligned(o, 16) || misaligned(lse, 4)) return ATTN_ERR_INVALID;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (Nk == 0)
+        return attn_host::launch_fill_empty(o, lse, (long long)B * Nq * Hq, d, (long long)B * Hq * Nq,
+                                            true, st);
+    if (q8 == nullptr || k8 == nullptr || v == nullptr || q_scales == nullptr || k_scales == nullptr)
+        return ATTN_ERR_INVALID;
+    if (misaligned(q8, 16) || misaligned(k8, 16) || misaligned(v, 16) || misaligned(q_scales, 4) ||
+        misaligned(k_scales, 4))
+        return ATTN_ERR_INVALID;
+    return attn_host::launch_fwd_fp8(q8, k8, v, q_scales, k_scales, o, lse, B, Hq, Hkv, Nq, Nk, d,
+                                     causal, scale, st);
 }
 
 size_t attn_bwd_workspace_bytes(int B, int Hq, int Nq) {

@@ -49,6 +49,13 @@ attn_status_t launch_decode_paged(const void* q, const void* k_pages, const void
                                   int max_pages, int max_seq_len, float scale, int splits,
                                   void* workspace, cudaStream_t stream);
 
+// ---- FP8 block quantisation (fp8.cu) and FP8 forward (fwd_tc.cu)
+attn_status_t launch_quantize_fp8(const void* x, void* codes, float* scales, int B, int N, int H, int d,
+                                  cudaStream_t stream);
+attn_status_t launch_fwd_fp8(const void* q8, const void* k8, const void* v, const float* q_scales,
+                             const float* k_scales, void* o, float* lse, int B, int Hq, int Hkv,
+                             int Nq, int Nk, int d, int causal, float scale, cudaStream_t stream);
+
 // ---- backward pass (bwd_tc.cu)
 size_t bwd_workspace_bytes(int B, int Hq, int Nq);
 attn_status_t launch_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,

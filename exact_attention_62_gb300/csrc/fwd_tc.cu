@@ -116,20 +116,29 @@ struct FwdParams {
     int num_units;
     float scale_log2;
     float rescale_thr;  // log2 units; 0 = rescale whenever the max grows
+    // FP8 inputs only: e4m3 Q and K with one scale per (batch, head, 128-row block)
+    const float* q_scales;  // [B, Hq, nqb]
+    const float* k_scales;  // [B, Hkv, nkb]
+    int nqb, nkb;
 };
 
-template <int D, bool P_TMEM>
+template <int D, bool P_TMEM, bool F8 = false>
 struct Layout {
-    static constexpr int kPanels = D / 64;
-    static constexpr int kQBytes = kBM * D * 2;
-    static constexpr int kKVBytes = kBN * D * 2;
+    // Q and K are bf16 or (F8) e4m3; V is always bf16.  A swizzled panel is
+    // 128 rows of 128 bytes: 64 bf16 or 128 e4m3 elements per row.
+    static constexpr int kQKElem = F8 ? 1 : 2;
+    static constexpr int kQKPanels = D * kQKElem / 128;
+    static constexpr int kPanels = D / 64;  // V panels
+    static constexpr int kQBytes = kBM * D * kQKElem;
+    static constexpr int kKBytes = kBN * D * kQKElem;
+    static constexpr int kKVBytes = kBN * D * 2;  // one V tile
     static constexpr int kPBytes = P_TMEM ? 0 : kBM * kBN * 2;
-    static constexpr int kKSt = P_TMEM ? (D == 128 ? 2 : 3) : (D == 128 ? 1 : 2);
+    static constexpr int kKSt = F8 ? 3 : P_TMEM ? (D == 128 ? 2 : 3) : (D == 128 ? 1 : 2);
     static constexpr int kVSt = kKSt;
     static constexpr int kOffQ = 0;
     static constexpr int kOffP = kOffQ + kQT * kQBytes;
     static constexpr int kOffK = kOffP + kQT * kPBytes;
-    static constexpr int kOffV = kOffK + kKSt * kKVBytes;
+    static constexpr int kOffV = kOffK + kKSt * kKBytes;
     static constexpr int kOffBar = kOffV + kVSt * kKVBytes;
     static constexpr int kBarQFull = 0;
     static constexpr int kBarQEmpty = kBarQFull + kQT;
@@ -195,11 +204,11 @@ __device__ __forceinline__ Unit unit_at(int u, const FwdParams& p) {
     return x;
 }
 
-template <int D, bool P_TMEM, bool POLY>
+template <int D, bool P_TMEM, bool POLY, bool F8>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
-    using L = Layout<D, P_TMEM>;
+    using L = Layout<D, P_TMEM, F8>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -246,9 +255,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                                        &g_fwd_status);
                     if (!ok) break;
                     mbar_arrive_expect_tx(bar(L::kBarQFull + t), L::kQBytes);
-                    for (int pp = 0; pp < L::kPanels; ++pp)
+                    for (int pp = 0; pp < L::kQKPanels; ++pp)
                         tma_load_4d(sbase + L::kOffQ + t * L::kQBytes + pp * kPanelBytes, &tmQ,
-                                    bar(L::kBarQFull + t), 64 * pp, x.hq, x.row0 + t * kBM, x.b);
+                                    bar(L::kBarQFull + t), (128 / L::kQKElem) * pp, x.hq,
+                                    x.row0 + t * kBM, x.b);
                     ++q_loads[t];
                 }
                 const int n = max(x.n[0], x.n[1]);
@@ -257,10 +267,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ok = mbar_wait(bar(L::kBarKEmpty + ks), ((kv / L::kKSt) & 1) ^ 1, abort_flag,
                                    &g_fwd_status);
                     if (!ok) break;
-                    mbar_arrive_expect_tx(bar(L::kBarKFull + ks), L::kKVBytes);
-                    for (int pp = 0; pp < L::kPanels; ++pp)
-                        tma_load_4d(sbase + L::kOffK + ks * L::kKVBytes + pp * kPanelBytes, &tmK,
-                                    bar(L::kBarKFull + ks), 64 * pp, x.g, j * kBN, x.b);
+                    mbar_arrive_expect_tx(bar(L::kBarKFull + ks), L::kKBytes);
+                    for (int pp = 0; pp < L::kQKPanels; ++pp)
+                        tma_load_4d(sbase + L::kOffK + ks * L::kKBytes + pp * kPanelBytes, &tmK,
+                                    bar(L::kBarKFull + ks), (128 / L::kQKElem) * pp, x.g, j * kBN, x.b);
                     const int vs = kv % L::kVSt;
                     ok = mbar_wait(bar(L::kBarVEmpty + vs), ((kv / L::kVSt) & 1) ^ 1, abort_flag,
                                    &g_fwd_status);
@@ -282,6 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // warp shares its SM sub-partition with two busy softmax warps.
         {
             constexpr uint32_t kIdS = idesc_bf16_f32(kBM, kBN, false);
+            constexpr uint32_t kIdS8 = idesc_e4m3_f32(kBM, kBN);
             constexpr uint32_t kIdPV = idesc_bf16_f32(kBM, D, true);
             constexpr uint32_t kHi = sdesc_sw128_hi(1024);  // every operand: 8-row groups 1024 B apart
             // V is [keys][D] with D contiguous: an N-major B operand.  Along N the
@@ -330,12 +341,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!ok) return;
                     const uint32_t q_lo = sdesc_sw128_lo(sbase + L::kOffQ + t * L::kQBytes, 16);
                     const uint32_t k_lo =
-                        sdesc_sw128_lo(sbase + L::kOffK + ((kv + j) % L::kKSt) * L::kKVBytes, 16);
+                        sdesc_sw128_lo(sbase + L::kOffK + ((kv + j) % L::kKSt) * L::kKBytes, 16);
                     const uint32_t dS = tmem + L::tm_s(t);
+                    // a k-step is 32 bytes of each row: 16 bf16 or 32 e4m3 elements
+                    constexpr int kSteps = F8 ? D / 32 : D / 16;
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
+                    for (int kk = 0; kk < kSteps; ++kk) {
                         const uint32_t off = ((kk >> 2) * kPanelBytes + (kk & 3) * 32) >> 4;
-                        mma_ss_elect(dS, q_lo + off, kHi, k_lo + off, kHi, kIdS, kk > 0 ? 1u : 0u);
+                        if constexpr (F8)
+                            mma_ss_elect_f8(dS, q_lo + off, kHi, k_lo + off, kHi, kIdS8, kk > 0 ? 1u : 0u);
+                        else
+                            mma_ss_elect(dS, q_lo + off, kHi, k_lo + off, kHi, kIdS, kk > 0 ? 1u : 0u);
                     }
                     tc_commit_elect(bar(L::kBarSFull + t));
                     if (j == x.n[t] - 1) tc_commit_elect(bar(L::kBarQEmpty + t));  // Q_t fully read
@@ -421,8 +437,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const long long diag = (long long)row + (p.Nk - p.Nq);  // last causal key of the row
             const long long diag_tile = (long long)rs + (p.Nk - p.Nq);
+            // FP8: S from the e4m3 codes is rescaled by the tile's q-block and k-block scales
+            float q_block_scale = 1.f;
+            const float* k_block_scale = nullptr;
+            if constexpr (F8) {
+                q_block_scale = p.q_scales[((long long)x.b * p.Hq + x.hq) * p.nqb + rs / kBM];
+                k_block_scale = p.k_scales + ((long long)x.b * p.Hkv + x.g) * p.nkb;
+            }
             float m = -INFINITY, l = 0.f;
             for (int j = 0; j < nt; ++j) {
+                float slj = sl;
+                if constexpr (F8) slj = sl * q_block_scale * k_block_scale[j];
                 if (!mbar_wait(bar(L::kBarSFull + t), s_waits & 1, abort_flag, &g_fwd_status)) {
                     ok = false;
                     break;
@@ -454,7 +479,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mx[i] = fmaxf(mx[i], __uint_as_float(s[120 + i]));
                 }
                 const float m_tile = fmaxf(fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]),
-                                                 mx[6]), mx[7]) * sl;
+                                                 mx[6]), mx[7]) * slj;
                 // The reference max moves only when the tile's max exceeds it by more
                 // than rescale_thr (log2 units; 0 = whenever it grows).  acc and l always
                 // share the reference, so O = acc / l and LSE = m + log l are exact for
@@ -467,7 +492,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
                 // P = exp2(s * scale log2 e - m): the scale-subtract and the row sum run on
                 // packed fp32 pairs, exp2 on the MUFU unit.
-                const uint64_t sl2 = f2_pack(sl, sl);
+                const uint64_t sl2 = f2_pack(slj, slj);
                 const uint64_t nm2 = f2_pack(-m_use, -m_use);
                 uint64_t sum2[2] = {0ull, 0ull};
                 uint32_t pk[kBN / 2];
@@ -586,20 +611,21 @@ float rescale_threshold() {
     return v;
 }
 
-template <int D, bool P_TMEM, bool POLY>
+template <int D, bool P_TMEM, bool POLY, bool F8 = false>
 attn_status_t launch_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                           int Hq, int Hkv, int Nq, int Nk, float scale, int causal,
-                          cudaStream_t stream) {
-    using L = Layout<D, P_TMEM>;
+                          cudaStream_t stream, const float* q_scales = nullptr,
+                          const float* k_scales = nullptr) {
+    using L = Layout<D, P_TMEM, F8>;
     CUtensorMap mq, mk, mv;
-    if (!attn_host::encode_bshd_map(&mq, q, B, Nq, Hq, D, kBM, 2) ||
-        !attn_host::encode_bshd_map(&mk, k, B, Nk, Hkv, D, kBN, 2) ||
+    if (!attn_host::encode_bshd_map(&mq, q, B, Nq, Hq, D, kBM, L::kQKElem) ||
+        !attn_host::encode_bshd_map(&mk, k, B, Nk, Hkv, D, kBN, L::kQKElem) ||
         !attn_host::encode_bshd_map(&mv, v, B, Nk, Hkv, D, kBN, 2))
         return ATTN_ERR_CUDA;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(fwd_tc_kernel<D, P_TMEM, POLY>,
+        attr_err = cudaFuncSetAttribute(fwd_tc_kernel<D, P_TMEM, POLY, F8>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         L::kSmemBytes);
     });
@@ -609,7 +635,7 @@ attn_status_t launch_impl(const void* q, const void* k, const void* v, void* o, 
     static int num_regs = -1;
     if (num_regs < 0) {
         cudaFuncAttributes fa;
-        if (cudaFuncGetAttributes(&fa, fwd_tc_kernel<D, P_TMEM, POLY>) != cudaSuccess) return ATTN_ERR_CUDA;
+        if (cudaFuncGetAttributes(&fa, fwd_tc_kernel<D, P_TMEM, POLY, F8>) != cudaSuccess) return ATTN_ERR_CUDA;
         num_regs = fa.numRegs;
     }
     if (num_regs != kLaunchRegs) return ATTN_ERR_UNSUPPORTED;
@@ -629,10 +655,14 @@ attn_status_t launch_impl(const void* q, const void* k, const void* v, void* o, 
     prm.num_units = (int)units;
     prm.scale_log2 = scale * 1.4426950408889634f;
     prm.rescale_thr = rescale_threshold();
+    prm.q_scales = q_scales;
+    prm.k_scales = k_scales;
+    prm.nqb = (Nq + kBM - 1) / kBM;
+    prm.nkb = (Nk + kBN - 1) / kBN;
     const int sms = attn_host::device_sm_count();
     if (sms <= 0) return ATTN_ERR_CUDA;
     const int grid = (int)(units < sms ? units : sms);
-    fwd_tc_kernel<D, P_TMEM, POLY><<<grid, kThreads, L::kSmemBytes, stream>>>(mq, mk, mv, prm);
+    fwd_tc_kernel<D, P_TMEM, POLY, F8><<<grid, kThreads, L::kSmemBytes, stream>>>(mq, mk, mv, prm);
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
@@ -674,6 +704,14 @@ attn_status_t launch_fwd_tc(const void* q, const void* k, const void* v, void* o
                : poly ? launch_impl<64, true, true>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, stream)
                       : launch_impl<64, true, false>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, stream);
     return ATTN_ERR_UNSUPPORTED;
+}
+
+attn_status_t launch_fwd_fp8(const void* q8, const void* k8, const void* v, const float* q_scales,
+                             const float* k_scales, void* o, float* lse, int B, int Hq, int Hkv,
+                             int Nq, int Nk, int d, int causal, float scale, cudaStream_t stream) {
+    if (d != 128) return ATTN_ERR_UNSUPPORTED;
+    return launch_impl<128, true, false, true>(q8, k8, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal,
+                                               stream, q_scales, k_scales);
 }
 
 cudaError_t fwd_tc_read_status(unsigned* out, bool clear) {

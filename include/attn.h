@@ -219,6 +219,38 @@ int attn_decode_paged_num_splits(int B, int Hq, int Hkv, int d, int page_size,
                                  int max_seq_len);
 
 /*
+ * attn_quantize_fp8 -- block quantisation to e4m3 ([L11] 4.5, FP8 item):
+ *   x      [B, N, H, d] bf16 input (d even).
+ *   codes  [B, N, H, d] uint8 output: e4m3 codes.
+ *   scales [B, H, ceil(N/128)] float32 output.
+ * Per (batch, head, block of 128 rows): amax = max |x|, scale = amax / 448
+ * and inv = 448 / amax in float32 (1 and 1 for an all-zero block); each code
+ * is e4m3(x * inv) rounded to nearest even and saturated to +-448, so that
+ * x ~= code_value * scale.  All steps are IEEE-defined: the result is
+ * reproducible bit for bit.
+ */
+attn_status_t attn_quantize_fp8(const void* x, void* codes, float* scales, int B, int N, int H,
+                                int d, void* stream);
+
+/*
+ * attn_fwd_fp8 -- attn_fwd with Q and K block-quantised to e4m3 (as produced
+ * by attn_quantize_fp8): S = scale * (q_code * q_scale) (k_code * k_scale)^T
+ * is formed on the tensor cores from the e4m3 codes (fp32 accumulation) and
+ * the block scales; softmax, P and P V are as in attn_fwd with bf16 V.
+ *   q8 [B, Nq, Hq, d], k8 [B, Nk, Hkv, d] uint8 e4m3 codes;
+ *   q_scales [B, Hq, ceil(Nq/128)], k_scales [B, Hkv, ceil(Nk/128)] float32;
+ *   v [B, Nk, Hkv, d] bf16;  o [B, Nq, Hq, d] bf16;  lse [B, Hq, Nq] float32.
+ * d = 128 only.  Relative to the exact attention of the unquantised inputs,
+ * the error of row i is bounded by the largest change delta_i that
+ * quantisation makes to one of its scaled scores: |dLSE_i| <= delta_i and
+ * |dO_i| <= (exp(2 delta_i) - 1) max_j |v_j - O_i| (plus the bf16 error of
+ * attn_fwd).  P V stays in bf16.
+ */
+attn_status_t attn_fwd_fp8(const void* q8, const void* k8, const void* v, const float* q_scales,
+                           const float* k_scales, void* o, float* lse, int B, int Hq, int Hkv, int Nq,
+                           int Nk, int d, int causal, float scale, void* stream);
+
+/*
  * attn_bwd -- backward pass of attn_fwd ([L11] 5.1): given dO, the gradients
  *     dV = P^T dO,  dP = dO V^T,  D_i = rowsum(dO_i * O_i),
  *     dS = P * (dP - D),  dQ = scale dS K,  dK = scale dS^T Q,

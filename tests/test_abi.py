@@ -171,3 +171,15 @@ def test_bwd_rejects_bad_arguments(L):
     assert bwd(L, wbytes=16) == INVALID          # D needs B*Hq*Nq floats
     assert bwd(L, B=0) == OK
     assert pkg.attn_bwd_workspace_bytes(2, 3, 100) == (2 * 3 * 100 * 4 + 255) // 256 * 256
+
+
+def test_fp8_entry_points_reject_bad_arguments(L):
+    assert L.attn_quantize_fp8(FAKE, FAKE, FAKE_LSE, 1, 8, 2, 7, None) == INVALID   # odd d
+    assert L.attn_quantize_fp8(None, FAKE, FAKE_LSE, 1, 8, 2, 64, None) == INVALID
+    assert L.attn_quantize_fp8(FAKE, FAKE, FAKE_LSE, 0, 8, 2, 64, None) == OK
+    f8 = lambda d=128, causal=0, Hq=2, Hkv=1, B=1: L.attn_fwd_fp8(
+        FAKE, FAKE, FAKE, FAKE_LSE, FAKE_LSE, FAKE, FAKE_LSE, B, Hq, Hkv, 8, 8, d, causal, 0.1, None)
+    assert f8(d=64) == UNSUPPORTED
+    assert f8(causal=3) == INVALID
+    assert f8(Hq=3, Hkv=2) == INVALID
+    assert f8(B=0) == OK

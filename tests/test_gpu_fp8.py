@@ -1,0 +1,84 @@
+"""FP8 (e4m3, block-quantised) Q and K for the forward.
+
+1. attn_quantize_fp8 matches the oracle's block quantisation bit for bit
+   (codes and scales): every step is IEEE-defined.
+2. attn_fwd_fp8 matches the oracle run on the dequantised Q and K within the
+   bf16 tolerance of attn_fwd: the kernel's arithmetic on the codes is exact
+   up to that.
+3. Against the exact attention of the unquantised inputs, each row obeys the
+   bound that follows from how far quantisation moves its scaled scores:
+   with delta_i = max_j |S'_ij - S_ij| (from the oracle),
+   |dLSE_i| <= delta_i + 1e-3 and
+   |dO_i| <= (exp(2 delta_i) - 1) * max_j |v_j - O_i| + 2e-2
+   (softmax weights change by at most exp(2 delta) - 1 in L1, and a change of
+   weights that sums to zero moves O by at most that times max |v_j - c|)."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from exact_attention_62_gb300.inputs import make_qkv
+from parity import compare
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.mark.parametrize("B,N,H,d,seed", [(2, 300, 3, 128, 1), (1, 1000, 2, 64, 2), (1, 128, 1, 128, 3)])
+def test_quantisation_is_bit_exact(attn, oracle_mod, B, N, H, d, seed):
+    g = torch.Generator().manual_seed(seed)
+    x = (torch.randn((B, N, H, d), generator=g) * 3).to(torch.bfloat16)
+    x[0, :, 0, 5] *= 40                       # outlier column
+    if N > 128:
+        x[-1, 128:256, -1] = 0                # an all-zero block
+    codes, scales = attn.attn_quantize_fp8(x.to(DEV))
+    torch.cuda.synchronize()
+    rc, rs = oracle_mod.quantize_fp8_blocks(x.float())
+    assert np.array_equal(codes.cpu().numpy(), rc)
+    assert np.array_equal(scales.cpu().numpy(), rs)
+
+
+CASES = [
+    # B, Hq, Hkv, Nq, Nk, causal, q_scale
+    (1, 2, 2, 300, 300, True, 1.0),
+    (2, 4, 1, 520, 520, False, 1.0),
+    (1, 2, 2, 1000, 300, True, 1.0),      # causal rows with no allowed key
+    (1, 2, 2, 700, 700, True, 8.0),       # near one-hot rows
+]
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Nq,Nk,causal,qs", CASES)
+def test_fp8_forward(attn, oracle_mod, B, Hq, Hkv, Nq, Nk, causal, qs):
+    d = 128
+    scale = 1.0 / math.sqrt(d)
+    q, k, v = make_qkv(B, Hq, Hkv, Nq, Nk, d, 12, q_scale=qs)
+    q8, qsc = attn.attn_quantize_fp8(q.to(DEV))
+    k8, ksc = attn.attn_quantize_fp8(k.to(DEV))
+    o, lse = attn.attn_fwd_fp8(q8, k8, v.to(DEV), qsc, ksc, causal, scale)
+    torch.cuda.synchronize()
+    assert attn.attn_check_device_status() == 0
+    qd = oracle_mod.dequantize_fp8_blocks(q8.cpu().numpy(), qsc.cpu().numpy())
+    kd = oracle_mod.dequantize_fp8_blocks(k8.cpu().numpy(), ksc.cpu().numpy())
+    # (2) the kernel's arithmetic on the quantised inputs
+    ro, rl = oracle_mod.attn_fwd(qd.astype(np.float32), kd.astype(np.float32), v, causal, scale)
+    compare(o, lse, ro, rl, torch.bfloat16, "fp8 vs dequantised oracle")
+    # (3) the quantisation error against the exact inputs, row by row
+    eo, el = oracle_mod.attn_fwd(q, k, v, causal, scale)
+    delta = oracle_mod.score_perturbation(qd, kd, q.double().numpy(), k.double().numpy(), causal, scale)
+    og = o.float().cpu().numpy().astype(np.float64)
+    lg = lse.cpu().numpy().astype(np.float64)
+    vv = v.double().numpy()
+    G = Hq // Hkv
+    for b in range(B):
+        for h in range(Hq):
+            for i in range(Nq):
+                last = Nk - 1 if not causal else min(Nk - 1, i + (Nk - Nq))
+                if last < 0:
+                    assert np.all(og[b, i, h] == 0.0) and lg[b, h, i] == -np.inf
+                    continue
+                dl = delta[b, h, i]
+                assert abs(lg[b, h, i] - el[b, h, i]) <= dl + 1e-3, (b, h, i)
+                spread = np.abs(vv[b, :last + 1, h // G, :] - eo[b, i, h][None, :]).max()
+                bound = math.expm1(2 * dl) * spread + 2e-2
+                assert np.abs(og[b, i, h] - eo[b, i, h]).max() <= bound, (b, h, i)
