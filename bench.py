@@ -477,6 +477,55 @@ def run_ours(args):
     return 0
 
 
+def run_extra(args):
+    """--only backward / fp8: attn_bwd or attn_fwd_fp8 on the prefill workload,
+    timed like the step's calls (L2 flushed clean before each, CUDA events).
+    For profiling; prints one JSON line, not the bench contract."""
+    import torch
+    import exact_attention_62_gb300 as attn
+    from exact_attention_62_gb300.inputs import make_qkv
+    attn.ensure_built()
+    dev = torch.device("cuda", 0)
+    B, Hq, Hkv, Nq, Nk, d, causal = PREFILL[args.prefill]
+    scale = 1.0 / math.sqrt(d)
+    q, k, v = (x.to(dev) for x in make_qkv(B, Hq, Hkv, Nq, Nk, d, seed=10))
+    o, lse = attn.attn_fwd(q, k, v, causal, scale)
+    flush_w = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flush_r = torch.ones(64 << 20, dtype=torch.float32, device=dev)
+    if args.only == "backward":
+        dout = torch.randn_like(q)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        ws = torch.empty(attn.attn_bwd_workspace_bytes(B, Hq, Nq), dtype=torch.uint8, device=dev)
+        call = lambda: attn.attn_bwd(q, k, v, o, lse, dout, causal, scale, dq=dq, dk=dk, dv=dv,
+                                     workspace=ws)
+        flops = 2.5 * prefill_flops(PREFILL[args.prefill])  # five products of 2 Nq Nk d per head
+    else:
+        q8, qs = attn.attn_quantize_fp8(q)
+        k8, ks = attn.attn_quantize_fp8(k)
+        call = lambda: attn.attn_fwd_fp8(q8, k8, v, qs, ks, causal, scale, o=o, lse=lse)
+        flops = prefill_flops(PREFILL[args.prefill])
+    for _ in range(args.warmup):
+        flush_w.zero_()
+        flush_r.sum()
+        call()
+    ts = []
+    for _ in range(args.steps):
+        flush_w.zero_()
+        flush_r.sum()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        call()
+        e1.record()
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    if attn.attn_check_device_status() != 0:
+        raise RuntimeError("device status reports a timed-out wait")
+    ms = statistics.mean(ts)
+    print(json.dumps({"profile_only": args.only, "workload": args.prefill, "ms": ms,
+                      "tflops": flops / (ms * 1e-3) / 1e12}))
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -487,8 +536,9 @@ def main(argv=None):
     ap.add_argument("--decode", choices=sorted(DECODE), default="decode_64k")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["prefill", "decode"], default=None,
-                    help="time one half of the step only (for profiling; no JSON contract)")
+    ap.add_argument("--only", choices=["prefill", "decode", "backward", "fp8"], default=None,
+                    help="time one part only (for profiling; no JSON contract): a half of the "
+                         "step, or the backward pass / the FP8-Q,K forward on the prefill workload")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer measurement")
     ap.add_argument("--splits", type=int, default=0, help="decode segments (0 = automatic)")
     args = ap.parse_args(argv)
@@ -496,6 +546,8 @@ def main(argv=None):
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         return run_reference(args)
+    if args.only in ("backward", "fp8"):
+        return run_extra(args)
     return run_ours(args)
 
 
