@@ -281,11 +281,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int col0 = j * kT;
             const bool need_mask = (col0 + kT > p.Nk) ||
                                    (p.causal && (long long)(col0 + kT - 1) > diag_tile);
+            // allowed keys of the row: tile columns [0, lim)
+            int lim = kT;
+            if (need_mask) {
+                long long end = p.Nk;
+                if (p.causal && diag + 1 < end) end = diag + 1;
+                end -= col0;
+                lim = end < 0 ? 0 : end > kT ? kT : (int)end;
+            }
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 uint32_t s[64], dp[64];
                 tmem_ld64_sync(tmem + lane_base + kS + 64 * h, s);
                 tmem_ld64_sync(tmem + lane_base + kDP + 64 * h, dp);
+                if (need_mask) {
+#pragma unroll
+                    for (int cc = 0; cc < 64; ++cc)
+                        if (64 * h + cc >= lim) s[cc] = __float_as_uint(-INFINITY);
+                }
                 uint32_t pk[32];
 #pragma unroll
                 for (int c = 0; c < 32; ++c) {
@@ -293,9 +306,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
                         const int cc = 2 * c + e;
-                        const int col = col0 + 64 * h + cc;
-                        float x = fmaf(__uint_as_float(s[cc]), sl, -lse2);
-                        if (need_mask && (col >= p.Nk || (p.causal && (long long)col > diag))) x = -INFINITY;
+                        const float x = fmaf(__uint_as_float(s[cc]), sl, -lse2);
                         const float pv = ex2(x);
                         pr[e] = pv * (__uint_as_float(dp[cc]) - dval);
                     }
@@ -504,11 +515,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int rq = it_tile(it) * kT;
             // causal: query row i may see this key iff key <= i + (Nk - Nq)
             const bool need_mask = key >= p.Nk || (p.causal && (long long)c0 + kT - 1 > (long long)rq + (p.Nk - p.Nq));
+            // the query rows that may see this key: tile columns [lo, kT)
+            int lo = 0;
+            if (need_mask) {
+                long long first = key >= p.Nk ? (long long)kT
+                                              : (p.causal ? (long long)key - (p.Nk - p.Nq) - rq : 0ll);
+                lo = first < 0 ? 0 : first > kT ? kT : (int)first;
+            }
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 uint32_t s[64], dp[64];
                 tmem_ld64_sync(tmem + lane_base + kS + 64 * h, s);
                 tmem_ld64_sync(tmem + lane_base + kDP + 64 * h, dp);
+                if (need_mask) {
+#pragma unroll
+                    for (int cc = 0; cc < 64; ++cc)
+                        if (64 * h + cc < lo) s[cc] = __float_as_uint(-INFINITY);
+                }
                 uint32_t pk[32], dk[32];
 #pragma unroll
                 for (int c = 0; c < 32; ++c) {
@@ -516,10 +539,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
                         const int cc = 64 * h + 2 * c + e;  // query row rq + cc
-                        float x = fmaf(__uint_as_float(s[2 * c + e]), sl, -lrow[cc]);
-                        if (need_mask && (key >= p.Nk ||
-                                          (p.causal && (long long)key > (long long)(rq + cc) + (p.Nk - p.Nq))))
-                            x = -INFINITY;
+                        const float x = fmaf(__uint_as_float(s[2 * c + e]), sl, -lrow[cc]);
                         pv[e] = ex2(x);
                         dsv[e] = pv[e] * (__uint_as_float(dp[2 * c + e]) - drow[cc]);
                     }

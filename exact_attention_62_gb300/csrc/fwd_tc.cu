@@ -460,12 +460,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool need_mask = (col0 + kBN > p.Nk) ||
                                        (p.causal && (long long)(col0 + kBN - 1) > diag_tile);
                 if (need_mask) {
+                    // The allowed keys of a row form a prefix of the tile: columns
+                    // [0, lim) with lim = min(Nk, last causal key + 1) - col0, clamped
+                    // to [0, kBN].  One compare against a constant per score.
+                    long long end = p.Nk;
+                    if (p.causal && diag + 1 < end) end = diag + 1;
+                    end -= col0;
+                    const int lim = end < 0 ? 0 : end > kBN ? kBN : (int)end;
 #pragma unroll
-                    for (int c = 0; c < kBN; ++c) {
-                        const int col = col0 + c;
-                        const bool keep = col < p.Nk && (!p.causal || (long long)col <= diag);
-                        if (!keep) s[c] = __float_as_uint(-INFINITY);
-                    }
+                    for (int c = 0; c < kBN; ++c)
+                        if (c >= lim) s[c] = __float_as_uint(-INFINITY);
                 }
                 // row max: 8 independent chains of three-input maxima
                 float mx[8];
