@@ -12,22 +12,26 @@
 //  * bwd_dot_kernel: D_i = rowsum(dO_i * O_i) into a workspace (the identity
 //    section 5.1 uses so that D needs only one row of O and dO).
 //  * bwd_dq_kernel: one CTA per 128-row query tile (query tile outer, like
-//    the forward).  Per key tile j: S = Q K_j^T and dP = dO V_j^T
-//    (tcgen05, operands in shared memory, accumulators in TMEM), then the
-//    elementwise warpgroup (one row per thread) forms dS = P * (dP - D) as
-//    bf16 over the first S columns, then dQ += dS K_j (A operand read from
-//    TMEM).  dQ is written once, scaled, at the end -- no atomics.
+//    the forward).  Per key tile j: S_j = Q K_j^T and dP_j = dO V_j^T
+//    (tcgen05, operands in shared memory, accumulators in TMEM); the
+//    elementwise warps read both into registers and say so, which lets the
+//    MMA warp issue S_{j+1} and dP_{j+1} while they form dS_j = P * (dP - D)
+//    as bf16 into one of two spare 64-column TMEM buffers; then
+//    dQ += dS_j K_j (A operand read from TMEM).  dQ is written once, scaled,
+//    at the end -- no atomics.
 //  * bwd_dkdv_kernel: one CTA per 128-key tile (key tile outer), looping over
 //    the query heads of its KV group and their query tiles.  With keys as the
 //    TMEM lanes: S^T = K Q_i^T and dP^T = V dO_i^T, then P^T and dS^T (bf16)
-//    over the first columns of each, then dV += P^T dO_i and dK += dS^T Q_i
-//    with both A operands read from TMEM.  The four accumulators fill the 512
-//    TMEM columns.  Each thread (one key) needs L and D of all 128 query rows
-//    of the tile: they are staged in shared memory, double-buffered.
+//    over the columns just read, then dV += P^T dO_i and dK += dS^T Q_i with
+//    both A operands read from TMEM.  The four accumulators fill the 512
+//    TMEM columns.  Each thread (one key) needs L and D of the query rows it
+//    handles: they are staged in shared memory, double-buffered.
 //  * Both main kernels: warp 0 issues the TMA loads, warp 1 (convergent, one
-//    elected lane) the MMAs, warps 4-7 do the elementwise work; rings of
-//    K/V (dQ kernel) or Q/dO (dK/dV kernel) tiles stream through shared
-//    memory.  Fully masked tiles (causality) are skipped.
+//    elected lane) the MMAs, and two elementwise warpgroups (warps 4-7 and
+//    8-11) split each tile's 128 columns between them, so each thread of a
+//    row (TMEM lane) handles 64 scores per tile.  Rings of K/V (dQ kernel) or
+//    Q/dO (dK/dV kernel) tiles stream through shared memory.  Fully masked
+//    tiles (causality) are skipped.
 //  * This pays 7 matrix products per (query tile, key tile) pair instead of
 //    the 5 of a kernel that owns all three accumulators, in exchange for no
 //    dQ atomics and one accumulator owner per output.
@@ -44,7 +48,15 @@ namespace {
 __device__ unsigned g_bwd_status = 0;
 
 constexpr int kT = 128;        // rows (queries or keys) per tile
-constexpr int kThreads = 256;  // 8 warps: 0 producer, 1 MMA, 2-3 idle, 4-7 elementwise
+// 12 warps: 0 producer, 1 MMA, 2-3 idle, 4-7 and 8-11 elementwise (one
+// warpgroup per half of a tile's columns).
+constexpr int kThreads = 384;
+// Register split: compiled for kLaunchRegs per thread (the most 384 threads
+// allow); warpgroup 0 gives registers back to the elementwise warpgroups.
+constexpr int kLaunchRegs = 168;
+constexpr int kRegsWG0 = 56;
+constexpr int kRegsEW = 224;
+static_assert(128 * kRegsWG0 + 256 * kRegsEW <= kThreads * kLaunchRegs, "register split");
 constexpr int kPanel = 128 * 128;
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -113,8 +125,9 @@ __global__ void __launch_bounds__(256)
     }
 }
 
-// Shared layout of both main kernels: two resident tiles (X0, X1), a ring of
-// STAGES stages of two streamed tiles each, barriers, misc.
+// Shared layout of the dK/dV kernel: two resident tiles (X0 = K, X1 = V), a
+// ring of STAGES stages of two streamed tiles each (Q_i, dO_i), the staged L
+// and D rows, barriers, misc.
 template <int D, int STAGES>
 struct BwdLay {
     static constexpr int kTile = kT * D * 2;
@@ -123,7 +136,7 @@ struct BwdLay {
     static constexpr int kOffX1 = kTile;
     static constexpr int kOffRing = 2 * kTile;
     static constexpr int kStage = 2 * kTile;
-    static constexpr int kOffLD = kOffRing + STAGES * kStage;  // L and D, 2 buffers x 2 x 128 floats
+    static constexpr int kOffLD = kOffRing + STAGES * kStage;  // L and D: 2 buffers x 2 warpgroups x 2 x 64 floats
     static constexpr int kOffBar = kOffLD + 2 * 2 * kT * 4;
     // barriers: X full, ring full[STAGES], ring empty[STAGES], S full, dS full, acc full
     static constexpr int kBarX = 0;
@@ -142,13 +155,45 @@ template <int D>
 constexpr int bwd_stages() { return D == 128 ? 2 : 4; }
 
 // ------------------------------------------------------------------ dQ
+// Shared layout of the dQ kernel: Q and dO resident, K and V in separate
+// rings.  A V tile is released as soon as dP has read it; a K tile only after
+// dQ += dS K has, and S of the next tile is issued while the current dS is
+// still being formed, so the K ring is one stage deeper.
+template <int D>
+struct DqLay {
+    static constexpr int kTile = kT * D * 2;
+    static constexpr int kPanels = D / 64;
+    static constexpr int kKSt = D == 128 ? 3 : 4;
+    static constexpr int kVSt = D == 128 ? 2 : 4;
+    static constexpr int kOffQ = 0;
+    static constexpr int kOffDO = kTile;
+    static constexpr int kOffK = 2 * kTile;
+    static constexpr int kOffV = kOffK + kKSt * kTile;
+    static constexpr int kOffBar = kOffV + kVSt * kTile;
+    static constexpr int kBarX = 0;                      // Q and dO loaded
+    static constexpr int kBarKFull = 1;
+    static constexpr int kBarKEmpty = kBarKFull + kKSt;
+    static constexpr int kBarVFull = kBarKEmpty + kKSt;
+    static constexpr int kBarVEmpty = kBarVFull + kVSt;
+    static constexpr int kBarS = kBarVEmpty + kVSt;      // S_j and dP_j in TMEM (commit)
+    static constexpr int kBarC = kBarS + 1;              // S_j, dP_j read into registers (256 threads)
+    static constexpr int kBarDS = kBarC + 1;             // dS_j in TMEM buffer j & 1 (256 threads; two barriers)
+    static constexpr int kBarAcc = kBarDS + 2;
+    static constexpr int kNumBars = kBarAcc + 1;
+    static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+    static constexpr int kSmem = kOffMisc + 16 + 1024;
+    static_assert(kSmem <= 232448, "shared memory budget");
+    __host__ __device__ static constexpr unsigned count(int i) {
+        return (i == kBarC || i == kBarDS || i == kBarDS + 1) ? 2u * kT : 1u;
+    }
+};
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
                   const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                   const BwdParams p) {
-    constexpr int STAGES = bwd_stages<D>();
-    using L = BwdLay<D, STAGES>;
+    using L = DqLay<D>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -178,7 +223,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < L::kNumBars; ++i) mbar_init(bar(i), i == L::kBarDS ? 128u : 1u);
+        for (int i = 0; i < L::kNumBars; ++i) mbar_init(bar(i), L::count(i));
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -190,74 +235,100 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    constexpr uint32_t kS = 0, kDP = 128, kDQ = 256;
+    // TMEM columns: S, dP (128 fp32 each), the dQ accumulator (D), and two
+    // 64-column buffers of bf16 dS (128 keys, two per column) from 384 on.
+    constexpr uint32_t kS = 0, kDP = 128, kDQ = 256, kDSb = 384;
 
-    if (warp == 0) {
-        if (lane == 0) {
-            prefetch_tmap(&tmQ);
-            prefetch_tmap(&tmDO);
-            prefetch_tmap(&tmK);
-            prefetch_tmap(&tmV);
-            mbar_arrive_expect_tx(bar(L::kBarX), 2 * L::kTile);
-            for (int pp = 0; pp < L::kPanels; ++pp) {
-                tma_load_4d(sbase + L::kOffX0 + pp * kPanel, &tmQ, bar(L::kBarX), 64 * pp, hq, r0, b);
-                tma_load_4d(sbase + L::kOffX1 + pp * kPanel, &tmDO, bar(L::kBarX), 64 * pp, hq, r0, b);
-            }
-            for (int j = 0; j < n; ++j) {
-                const int st = j % STAGES;
-                if (!mbar_wait(bar(L::kBarEmpty + st), ((j / STAGES) & 1) ^ 1, abort_flag, &g_bwd_status))
-                    break;
-                mbar_arrive_expect_tx(bar(L::kBarFull + st), L::kStage);
-                const uint32_t dst = sbase + L::kOffRing + st * L::kStage;
+    if (warp < 4) {
+        warpgroup_reg_dealloc<kRegsWG0>();
+        if (warp == 0) {
+            if (lane == 0) {
+                prefetch_tmap(&tmQ);
+                prefetch_tmap(&tmDO);
+                prefetch_tmap(&tmK);
+                prefetch_tmap(&tmV);
+                mbar_arrive_expect_tx(bar(L::kBarX), 2 * L::kTile);
                 for (int pp = 0; pp < L::kPanels; ++pp) {
-                    tma_load_4d(dst + pp * kPanel, &tmK, bar(L::kBarFull + st), 64 * pp, g, j * kT, b);
-                    tma_load_4d(dst + L::kTile + pp * kPanel, &tmV, bar(L::kBarFull + st), 64 * pp, g,
-                                j * kT, b);
+                    tma_load_4d(sbase + L::kOffQ + pp * kPanel, &tmQ, bar(L::kBarX), 64 * pp, hq, r0, b);
+                    tma_load_4d(sbase + L::kOffDO + pp * kPanel, &tmDO, bar(L::kBarX), 64 * pp, hq, r0, b);
+                }
+                for (int j = 0; j < n; ++j) {
+                    const int ks = j % L::kKSt, vs = j % L::kVSt;
+                    if (!mbar_wait(bar(L::kBarKEmpty + ks), ((j / L::kKSt) & 1) ^ 1, abort_flag, &g_bwd_status))
+                        break;
+                    mbar_arrive_expect_tx(bar(L::kBarKFull + ks), L::kTile);
+                    for (int pp = 0; pp < L::kPanels; ++pp)
+                        tma_load_4d(sbase + L::kOffK + ks * L::kTile + pp * kPanel, &tmK, bar(L::kBarKFull + ks),
+                                    64 * pp, g, j * kT, b);
+                    if (!mbar_wait(bar(L::kBarVEmpty + vs), ((j / L::kVSt) & 1) ^ 1, abort_flag, &g_bwd_status))
+                        break;
+                    mbar_arrive_expect_tx(bar(L::kBarVFull + vs), L::kTile);
+                    for (int pp = 0; pp < L::kPanels; ++pp)
+                        tma_load_4d(sbase + L::kOffV + vs * L::kTile + pp * kPanel, &tmV, bar(L::kBarVFull + vs),
+                                    64 * pp, g, j * kT, b);
                 }
             }
-        }
-    } else if (warp == 1) {
-        constexpr uint32_t kIdSS = idesc_bf16_f32(kT, kT, false);  // S, dP: N = 128 keys
-        constexpr uint32_t kIdDQ = idesc_bf16_f32(kT, D, true);    // dQ: N = D, B = K N-major
-        constexpr uint32_t kHi = sdesc_sw128_hi(1024);
-        constexpr uint32_t kKLbo = D == 128 ? kPanel : 1024;
-        bool ok = mbar_wait_warp(bar(L::kBarX), 0, abort_flag, &g_bwd_status);
-        tc_fence_after();
-        const uint32_t q_lo = sdesc_sw128_lo(sbase + L::kOffX0, 16);
-        const uint32_t do_lo = sdesc_sw128_lo(sbase + L::kOffX1, 16);
-        for (int j = 0; j < n && ok; ++j) {
-            const int st = j % STAGES;
-            ok = mbar_wait_warp(bar(L::kBarFull + st), (j / STAGES) & 1, abort_flag, &g_bwd_status);
-            if (!ok) break;
+        } else if (warp == 1) {
+            constexpr uint32_t kIdSS = idesc_bf16_f32(kT, kT, false);  // S, dP: N = 128 keys
+            constexpr uint32_t kIdDQ = idesc_bf16_f32(kT, D, true);    // dQ: N = D, B = K N-major
+            constexpr uint32_t kHi = sdesc_sw128_hi(1024);
+            constexpr uint32_t kKLbo = D == 128 ? kPanel : 1024;
+            bool ok = mbar_wait_warp(bar(L::kBarX), 0, abort_flag, &g_bwd_status);
             tc_fence_after();
-            const uint32_t kaddr = sbase + L::kOffRing + st * L::kStage;
-            const uint32_t k_lo = sdesc_sw128_lo(kaddr, 16);
-            const uint32_t v_lo = sdesc_sw128_lo(kaddr + L::kTile, 16);
+            const uint32_t q_lo = sdesc_sw128_lo(sbase + L::kOffQ, 16);
+            const uint32_t do_lo = sdesc_sw128_lo(sbase + L::kOffDO, 16);
+            // S_j = Q K_j^T and dP_j = dO V_j^T into TMEM; V_j is free once dP_j is done
+            auto issue_sdp = [&](int j) {
+                const int ks = j % L::kKSt, vs = j % L::kVSt;
+                if (ok) ok = mbar_wait_warp(bar(L::kBarKFull + ks), (j / L::kKSt) & 1, abort_flag, &g_bwd_status);
+                if (ok) ok = mbar_wait_warp(bar(L::kBarVFull + vs), (j / L::kVSt) & 1, abort_flag, &g_bwd_status);
+                if (!ok) return;
+                tc_fence_after();
+                const uint32_t k_lo = sdesc_sw128_lo(sbase + L::kOffK + ks * L::kTile, 16);
+                const uint32_t v_lo = sdesc_sw128_lo(sbase + L::kOffV + vs * L::kTile, 16);
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {  // S = Q K^T
-                const uint32_t off = ((kk >> 2) * kPanel + (kk & 3) * 32) >> 4;
-                mma_ss_elect(tmem + kS, q_lo + off, kHi, k_lo + off, kHi, kIdSS, kk > 0 ? 1u : 0u);
-            }
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = ((kk >> 2) * kPanel + (kk & 3) * 32) >> 4;
+                    mma_ss_elect(tmem + kS, q_lo + off, kHi, k_lo + off, kHi, kIdSS, kk > 0 ? 1u : 0u);
+                }
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {  // dP = dO V^T
-                const uint32_t off = ((kk >> 2) * kPanel + (kk & 3) * 32) >> 4;
-                mma_ss_elect(tmem + kDP, do_lo + off, kHi, v_lo + off, kHi, kIdSS, kk > 0 ? 1u : 0u);
-            }
-            tc_commit_elect(bar(L::kBarS));
-            ok = mbar_wait_warp(bar(L::kBarDS), j & 1, abort_flag, &g_bwd_status);
-            if (!ok) break;
-            tc_fence_after();
-            const uint32_t kn_lo = sdesc_sw128_lo(kaddr, kKLbo);
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = ((kk >> 2) * kPanel + (kk & 3) * 32) >> 4;
+                    mma_ss_elect(tmem + kDP, do_lo + off, kHi, v_lo + off, kHi, kIdSS, kk > 0 ? 1u : 0u);
+                }
+                tc_commit_elect(bar(L::kBarS));
+                tc_commit_elect(bar(L::kBarVEmpty + vs));
+            };
+            issue_sdp(0);
+            for (int j = 0; j < n && ok; ++j) {
+                if (j + 1 < n) {
+                    // the elementwise warps hold S_j and dP_j: the next pair may overwrite them
+                    ok = mbar_wait_warp(bar(L::kBarC), j & 1, abort_flag, &g_bwd_status);
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_sdp(j + 1);
+                    if (!ok) break;
+                }
+                ok = mbar_wait_warp(bar(L::kBarDS + (j & 1)), (j >> 1) & 1, abort_flag, &g_bwd_status);
+                if (!ok) break;
+                tc_fence_after();
+                const int ks = j % L::kKSt;
+                const uint32_t kn_lo = sdesc_sw128_lo(sbase + L::kOffK + ks * L::kTile, kKLbo);
+                const uint32_t ds = tmem + kDSb + 64u * (uint32_t)(j & 1);
 #pragma unroll
-            for (int kk = 0; kk < kT / 16; ++kk) {  // dQ += dS K  (dS bf16 in TMEM, 16 keys = 8 columns)
-                const uint32_t k_off = (kk * 16 * 128) >> 4;
-                mma_ts_elect(tmem + kDQ, tmem + kS + kk * 8, kn_lo + k_off, kHi, kIdDQ,
-                             (j > 0 || kk > 0) ? 1u : 0u);
+                for (int kk = 0; kk < kT / 16; ++kk) {  // dQ += dS K  (16 keys = 8 bf16 columns of dS)
+                    const uint32_t k_off = (kk * 16 * 128) >> 4;
+                    mma_ts_elect(tmem + kDQ, ds + kk * 8, kn_lo + k_off, kHi, kIdDQ, (j > 0 || kk > 0) ? 1u : 0u);
+                }
+                tc_commit_elect(bar(L::kBarKEmpty + ks));  // K_j fully read
+                if (j == n - 1) tc_commit_elect(bar(L::kBarAcc));
             }
-            tc_commit_elect(bar(L::kBarEmpty + st));  // K_j and V_j fully read
-            if (j == n - 1) tc_commit_elect(bar(L::kBarAcc));
         }
-    } else if (warp >= 4) {
+    } else {
+        warpgroup_reg_alloc<kRegsEW>();
+        // Two elementwise warpgroups share each row (TMEM lane): warpgroup w
+        // takes keys 64w .. 64w + 63 of every key tile.
+        const int w = (warp - 4) >> 2;
         const int q4 = warp & 3;
         const int r = q4 * 32 + lane;
         const int row = r0 + r;
@@ -278,62 +349,58 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             tc_fence_after();
+            uint32_t s[64], dp[64];
+            tmem_ld64_sync(tmem + lane_base + kS + 64 * w, s);
+            tmem_ld64_sync(tmem + lane_base + kDP + 64 * w, dp);
+            tc_fence_before();
+            mbar_arrive(bar(L::kBarC));
             const int col0 = j * kT;
             const bool need_mask = (col0 + kT > p.Nk) ||
                                    (p.causal && (long long)(col0 + kT - 1) > diag_tile);
-            // allowed keys of the row: tile columns [0, lim)
-            int lim = kT;
             if (need_mask) {
+                // allowed keys of the row: tile columns [0, lim)
                 long long end = p.Nk;
                 if (p.causal && diag + 1 < end) end = diag + 1;
                 end -= col0;
-                lim = end < 0 ? 0 : end > kT ? kT : (int)end;
+                const int lim = end < 0 ? 0 : end > kT ? kT : (int)end;
+#pragma unroll
+                for (int cc = 0; cc < 64; ++cc)
+                    if (64 * w + cc >= lim) s[cc] = __float_as_uint(-INFINITY);
             }
+            uint32_t pk[32];
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                uint32_t s[64], dp[64];
-                tmem_ld64_sync(tmem + lane_base + kS + 64 * h, s);
-                tmem_ld64_sync(tmem + lane_base + kDP + 64 * h, dp);
-                if (need_mask) {
+            for (int c = 0; c < 32; ++c) {
+                float pr[2];
 #pragma unroll
-                    for (int cc = 0; cc < 64; ++cc)
-                        if (64 * h + cc >= lim) s[cc] = __float_as_uint(-INFINITY);
+                for (int e = 0; e < 2; ++e) {
+                    const int cc = 2 * c + e;
+                    const float pv = ex2(fmaf(__uint_as_float(s[cc]), sl, -lse2));
+                    pr[e] = pv * (__uint_as_float(dp[cc]) - dval);
                 }
-                uint32_t pk[32];
-#pragma unroll
-                for (int c = 0; c < 32; ++c) {
-                    float pr[2];
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int cc = 2 * c + e;
-                        const float x = fmaf(__uint_as_float(s[cc]), sl, -lse2);
-                        const float pv = ex2(x);
-                        pr[e] = pv * (__uint_as_float(dp[cc]) - dval);
-                    }
-                    pk[c] = pack_bf16(pr[0], pr[1]);
-                }
-                tmem_st32(tmem + lane_base + kS + 32 * h, pk);  // dS (bf16) over S columns 0..63
+                pk[c] = pack_bf16(pr[0], pr[1]);
             }
+            tmem_st32(tmem + lane_base + kDSb + 64u * (uint32_t)(j & 1) + 32u * (uint32_t)w, pk);
             tmem_st_wait();
             tc_fence_before();
-            mbar_arrive(bar(L::kBarDS));
+            mbar_arrive(bar(L::kBarDS + (j & 1)));
         }
         if (ok && mbar_wait(bar(L::kBarAcc), 0, abort_flag, &g_bwd_status)) {
             tc_fence_after();
-            uint32_t xo[64];
-            __nv_bfloat16* out = p.dq + (((long long)b * p.Nq + row) * p.Hq + hq) * D;
+            // warpgroup w writes dQ columns [w D/2, (w + 1) D/2)
+            __nv_bfloat16* out = p.dq + (((long long)b * p.Nq + row) * p.Hq + hq) * D + w * (D / 2);
+            uint32_t xo[32];
 #pragma unroll
             for (int h = 0; h < D / 64; ++h) {
-                tmem_ld64_sync(tmem + lane_base + kDQ + 64 * h, xo);
+                tmem_ld32_sync(tmem + lane_base + kDQ + w * (D / 2) + 32 * h, xo);
                 if (row < p.Nq) {
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        uint4 w;
-                        w.x = pack_bf16(__uint_as_float(xo[8 * c + 0]) * p.scale, __uint_as_float(xo[8 * c + 1]) * p.scale);
-                        w.y = pack_bf16(__uint_as_float(xo[8 * c + 2]) * p.scale, __uint_as_float(xo[8 * c + 3]) * p.scale);
-                        w.z = pack_bf16(__uint_as_float(xo[8 * c + 4]) * p.scale, __uint_as_float(xo[8 * c + 5]) * p.scale);
-                        w.w = pack_bf16(__uint_as_float(xo[8 * c + 6]) * p.scale, __uint_as_float(xo[8 * c + 7]) * p.scale);
-                        reinterpret_cast<uint4*>(out + 64 * h)[c] = w;
+                    for (int c = 0; c < 4; ++c) {
+                        uint4 v;
+                        v.x = pack_bf16(__uint_as_float(xo[8 * c + 0]) * p.scale, __uint_as_float(xo[8 * c + 1]) * p.scale);
+                        v.y = pack_bf16(__uint_as_float(xo[8 * c + 2]) * p.scale, __uint_as_float(xo[8 * c + 3]) * p.scale);
+                        v.z = pack_bf16(__uint_as_float(xo[8 * c + 4]) * p.scale, __uint_as_float(xo[8 * c + 5]) * p.scale);
+                        v.w = pack_bf16(__uint_as_float(xo[8 * c + 6]) * p.scale, __uint_as_float(xo[8 * c + 7]) * p.scale);
+                        reinterpret_cast<uint4*>(out + 32 * h)[c] = v;
                     }
                 }
             }
@@ -391,7 +458,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < L::kNumBars; ++i) mbar_init(bar(i), i == L::kBarDS ? 128u : 1u);
+        for (int i = 0; i < L::kNumBars; ++i) mbar_init(bar(i), i == L::kBarDS ? 2u * kT : 1u);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -407,7 +474,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto it_head = [&](int it) { return g * p.G + it / per_head; };
     auto it_tile = [&](int it) { return i0 + it % per_head; };
 
-    if (warp == 0) {
+    if (warp < 4) {
+      warpgroup_reg_dealloc<kRegsWG0>();
+      if (warp == 0) {
         if (lane == 0) {
             prefetch_tmap(&tmQ);
             prefetch_tmap(&tmDO);
@@ -469,118 +538,123 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int kk = 0; kk < kT / 16; ++kk) {  // 16 query rows = 8 bf16 columns of P^T / dS^T
                 const uint32_t r_off = (kk * 16 * 128) >> 4;
                 const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
-                mma_ts_elect(tmem + kDV, tmem + kS + kk * 8, don_lo + r_off, kHi, kIdAcc, acc);   // dV += P^T dO
-                mma_ts_elect(tmem + kDK, tmem + kDP + kk * 8, qn_lo + r_off, kHi, kIdAcc, acc);   // dK += dS^T Q
+                // query rows 16kk..: warpgroup kk / 4 wrote them at columns 64 (kk / 4) + 8 (kk % 4)
+                const uint32_t pc = (kk >> 2) * 64 + (kk & 3) * 8;
+                mma_ts_elect(tmem + kDV, tmem + kS + pc, don_lo + r_off, kHi, kIdAcc, acc);   // dV += P^T dO
+                mma_ts_elect(tmem + kDK, tmem + kDP + pc, qn_lo + r_off, kHi, kIdAcc, acc);   // dK += dS^T Q
             }
             tc_commit_elect(bar(L::kBarEmpty + st));  // Q_i and dO_i fully read
             if (it == n - 1) tc_commit_elect(bar(L::kBarAcc));
         }
-    } else if (warp >= 4) {
+      }
+    } else {
+        warpgroup_reg_alloc<kRegsEW>();
+        // Two elementwise warpgroups share each key (TMEM lane): warpgroup w
+        // takes query rows 64w .. 64w + 63 of every query tile.
+        const int w = (warp - 4) >> 2;
         const int q4 = warp & 3;
-        const int r = q4 * 32 + lane;  // the key this thread owns
+        const int r = q4 * 32 + lane;
         const int key = c0 + r;
         const uint32_t lane_base = static_cast<uint32_t>(q4 * 32) << 16;
-        const int tid = threadIdx.x - 128;  // 0..127 within the warpgroup
-        float* ldbuf = reinterpret_cast<float*>(sgen + L::kOffLD);  // [2][2][128]: L*log2e, D
+        const int tid = threadIdx.x - 128 * (1 + w);  // 0..127 within the warpgroup
+        // [buffer][warpgroup][L*log2e | D][64 query rows]
+        float* ldbuf = reinterpret_cast<float*>(sgen + L::kOffLD);
         const float sl = p.scale_log2;
-        // L and D of query row `rq + tid` of head hh (rows past Nq: P = 0)
-        auto fetch = [&](int it, float& l2, float& dv) {
-            const int hh = it_head(it), row = it_tile(it) * kT + tid;
-            l2 = INFINITY;
-            dv = 0.f;
+        // thread tid stages L (tid < 64) or D (tid >= 64) of query row 64w + tid % 64
+        // of head hh (rows past Nq: P = 0)
+        auto fetch = [&](int it) {
+            const int hh = it_head(it), row = it_tile(it) * kT + 64 * w + (tid & 63);
+            float x = tid < 64 ? INFINITY : 0.f;
             if (row < p.Nq) {
                 const long long o = ((long long)b * p.Hq + hh) * p.Nq + row;
-                const float l = p.lse[o];
-                l2 = l == -INFINITY ? INFINITY : l * kLog2e;
-                dv = p.dvec[o];
+                if (tid < 64) {
+                    const float l = p.lse[o];
+                    x = l == -INFINITY ? INFINITY : l * kLog2e;
+                } else {
+                    x = p.dvec[o];
+                }
             }
+            return x;
         };
-        float nl2, ndv;
-        fetch(0, nl2, ndv);
+        float nx = fetch(0);
         bool ok = true;
         // Every thread of the warpgroup runs every iteration, also after a
         // bounded wait has given up (the abort flag then ends the remaining
         // waits at once): the named barrier below must never miss a thread.
         for (int it = 0; it < n; ++it) {
             const int buf = it & 1;
-            ldbuf[(buf * 2 + 0) * kT + tid] = nl2;
-            ldbuf[(buf * 2 + 1) * kT + tid] = ndv;
-            named_bar_sync(1, 128);  // this iteration's L and D are visible to the warpgroup
-            if (it + 1 < n) fetch(it + 1, nl2, ndv);  // in flight while this tile is processed
-            const float* lrow = ldbuf + (buf * 2 + 0) * kT;
-            const float* drow = ldbuf + (buf * 2 + 1) * kT;
+            float* lrow = ldbuf + ((buf * 2 + w) * 2 + 0) * 64;
+            float* drow = ldbuf + ((buf * 2 + w) * 2 + 1) * 64;
+            (tid < 64 ? lrow : drow)[tid & 63] = nx;
+            named_bar_sync(1 + w, 128);  // this iteration's L and D are visible to the warpgroup
+            if (it + 1 < n) nx = fetch(it + 1);  // in flight while this tile is processed
             if (ok) ok = mbar_wait(bar(L::kBarS), it & 1, abort_flag, &g_bwd_status);
             if (!ok) continue;
             tc_fence_after();
             const int rq = it_tile(it) * kT;
             // causal: query row i may see this key iff key <= i + (Nk - Nq)
             const bool need_mask = key >= p.Nk || (p.causal && (long long)c0 + kT - 1 > (long long)rq + (p.Nk - p.Nq));
-            // the query rows that may see this key: tile columns [lo, kT)
-            int lo = 0;
+            uint32_t s[64], dp[64];
+            tmem_ld64_sync(tmem + lane_base + kS + 64 * w, s);
+            tmem_ld64_sync(tmem + lane_base + kDP + 64 * w, dp);
             if (need_mask) {
-                long long first = key >= p.Nk ? (long long)kT
-                                              : (p.causal ? (long long)key - (p.Nk - p.Nq) - rq : 0ll);
-                lo = first < 0 ? 0 : first > kT ? kT : (int)first;
+                // the query rows that may see this key: tile columns [lo, kT)
+                const long long first = key >= p.Nk ? (long long)kT
+                                                     : (p.causal ? (long long)key - (p.Nk - p.Nq) - rq : 0ll);
+                const int lo = first < 0 ? 0 : first > kT ? kT : (int)first;
+#pragma unroll
+                for (int cc = 0; cc < 64; ++cc)
+                    if (64 * w + cc < lo) s[cc] = __float_as_uint(-INFINITY);
             }
+            uint32_t pk[32], dk[32];
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                uint32_t s[64], dp[64];
-                tmem_ld64_sync(tmem + lane_base + kS + 64 * h, s);
-                tmem_ld64_sync(tmem + lane_base + kDP + 64 * h, dp);
-                if (need_mask) {
+            for (int c = 0; c < 32; ++c) {
+                float pv[2], dsv[2];
 #pragma unroll
-                    for (int cc = 0; cc < 64; ++cc)
-                        if (64 * h + cc < lo) s[cc] = __float_as_uint(-INFINITY);
+                for (int e = 0; e < 2; ++e) {
+                    const int cc = 2 * c + e;  // query row rq + 64w + cc
+                    pv[e] = ex2(fmaf(__uint_as_float(s[cc]), sl, -lrow[cc]));
+                    dsv[e] = pv[e] * (__uint_as_float(dp[cc]) - drow[cc]);
                 }
-                uint32_t pk[32], dk[32];
-#pragma unroll
-                for (int c = 0; c < 32; ++c) {
-                    float pv[2], dsv[2];
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int cc = 64 * h + 2 * c + e;  // query row rq + cc
-                        const float x = fmaf(__uint_as_float(s[2 * c + e]), sl, -lrow[cc]);
-                        pv[e] = ex2(x);
-                        dsv[e] = pv[e] * (__uint_as_float(dp[2 * c + e]) - drow[cc]);
-                    }
-                    pk[c] = pack_bf16(pv[0], pv[1]);
-                    dk[c] = pack_bf16(dsv[0], dsv[1]);
-                }
-                tmem_st32(tmem + lane_base + kS + 32 * h, pk);   // P^T over S^T columns 0..63
-                tmem_st32(tmem + lane_base + kDP + 32 * h, dk);  // dS^T over dP^T columns 0..63
+                pk[c] = pack_bf16(pv[0], pv[1]);
+                dk[c] = pack_bf16(dsv[0], dsv[1]);
             }
+            // each warpgroup writes only columns it has read itself
+            tmem_st32(tmem + lane_base + kS + 64 * w, pk);   // P^T
+            tmem_st32(tmem + lane_base + kDP + 64 * w, dk);  // dS^T
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(bar(L::kBarDS));
         }
         if (ok && mbar_wait(bar(L::kBarAcc), 0, abort_flag, &g_bwd_status)) {
             tc_fence_after();
-            uint32_t xo[64];
-            const long long off = (((long long)b * p.Nk + key) * p.Hkv + g) * D;
+            // warpgroup w writes columns [w D/2, (w + 1) D/2) of dV and dK
+            const long long off = (((long long)b * p.Nk + key) * p.Hkv + g) * D + w * (D / 2);
+            uint32_t xo[32];
 #pragma unroll
             for (int h = 0; h < D / 64; ++h) {
-                tmem_ld64_sync(tmem + lane_base + kDV + 64 * h, xo);
+                tmem_ld32_sync(tmem + lane_base + kDV + w * (D / 2) + 32 * h, xo);
                 if (key < p.Nk) {
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        uint4 w;
-                        w.x = pack_bf16(__uint_as_float(xo[8 * c + 0]), __uint_as_float(xo[8 * c + 1]));
-                        w.y = pack_bf16(__uint_as_float(xo[8 * c + 2]), __uint_as_float(xo[8 * c + 3]));
-                        w.z = pack_bf16(__uint_as_float(xo[8 * c + 4]), __uint_as_float(xo[8 * c + 5]));
-                        w.w = pack_bf16(__uint_as_float(xo[8 * c + 6]), __uint_as_float(xo[8 * c + 7]));
-                        reinterpret_cast<uint4*>(p.dv + off + 64 * h)[c] = w;
+                    for (int c = 0; c < 4; ++c) {
+                        uint4 v;
+                        v.x = pack_bf16(__uint_as_float(xo[8 * c + 0]), __uint_as_float(xo[8 * c + 1]));
+                        v.y = pack_bf16(__uint_as_float(xo[8 * c + 2]), __uint_as_float(xo[8 * c + 3]));
+                        v.z = pack_bf16(__uint_as_float(xo[8 * c + 4]), __uint_as_float(xo[8 * c + 5]));
+                        v.w = pack_bf16(__uint_as_float(xo[8 * c + 6]), __uint_as_float(xo[8 * c + 7]));
+                        reinterpret_cast<uint4*>(p.dv + off + 32 * h)[c] = v;
                     }
                 }
-                tmem_ld64_sync(tmem + lane_base + kDK + 64 * h, xo);
+                tmem_ld32_sync(tmem + lane_base + kDK + w * (D / 2) + 32 * h, xo);
                 if (key < p.Nk) {
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        uint4 w;
-                        w.x = pack_bf16(__uint_as_float(xo[8 * c + 0]) * p.scale, __uint_as_float(xo[8 * c + 1]) * p.scale);
-                        w.y = pack_bf16(__uint_as_float(xo[8 * c + 2]) * p.scale, __uint_as_float(xo[8 * c + 3]) * p.scale);
-                        w.z = pack_bf16(__uint_as_float(xo[8 * c + 4]) * p.scale, __uint_as_float(xo[8 * c + 5]) * p.scale);
-                        w.w = pack_bf16(__uint_as_float(xo[8 * c + 6]) * p.scale, __uint_as_float(xo[8 * c + 7]) * p.scale);
-                        reinterpret_cast<uint4*>(p.dk + off + 64 * h)[c] = w;
+                    for (int c = 0; c < 4; ++c) {
+                        uint4 v;
+                        v.x = pack_bf16(__uint_as_float(xo[8 * c + 0]) * p.scale, __uint_as_float(xo[8 * c + 1]) * p.scale);
+                        v.y = pack_bf16(__uint_as_float(xo[8 * c + 2]) * p.scale, __uint_as_float(xo[8 * c + 3]) * p.scale);
+                        v.z = pack_bf16(__uint_as_float(xo[8 * c + 4]) * p.scale, __uint_as_float(xo[8 * c + 5]) * p.scale);
+                        v.w = pack_bf16(__uint_as_float(xo[8 * c + 6]) * p.scale, __uint_as_float(xo[8 * c + 7]) * p.scale);
+                        reinterpret_cast<uint4*>(p.dk + off + 32 * h)[c] = v;
                     }
                 }
             }
@@ -601,6 +675,7 @@ attn_status_t launch_bwd_impl(const void* q, const void* k, const void* v, const
                               int B, int Hq, int Hkv, int Nq, int Nk, int causal, float scale,
                               float* dvec, cudaStream_t stream) {
     using L = BwdLay<D, bwd_stages<D>()>;
+    using LQ = DqLay<D>;
     CUtensorMap mq, mdo, mk, mv;
     if (!attn_host::encode_bshd_map(&mq, q, B, Nq, Hq, D, kT, 2) ||
         !attn_host::encode_bshd_map(&mdo, dout, B, Nq, Hq, D, kT, 2) ||
@@ -610,12 +685,23 @@ attn_status_t launch_bwd_impl(const void* q, const void* k, const void* v, const
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmem);
+        attr_err = cudaFuncSetAttribute(bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, LQ::kSmem);
         if (attr_err == cudaSuccess)
             attr_err = cudaFuncSetAttribute(bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                             L::kSmem);
     });
     if (attr_err != cudaSuccess) return ATTN_ERR_CUDA;
+    // The register split inside both kernels assumes exactly kLaunchRegs per
+    // thread at launch; refuse to launch a build that differs.
+    static int regs_dq = -1, regs_dkdv = -1;
+    if (regs_dq < 0 || regs_dkdv < 0) {
+        cudaFuncAttributes fa;
+        if (cudaFuncGetAttributes(&fa, bwd_dq_kernel<D>) != cudaSuccess) return ATTN_ERR_CUDA;
+        regs_dq = fa.numRegs;
+        if (cudaFuncGetAttributes(&fa, bwd_dkdv_kernel<D>) != cudaSuccess) return ATTN_ERR_CUDA;
+        regs_dkdv = fa.numRegs;
+    }
+    if (regs_dq != kLaunchRegs || regs_dkdv != kLaunchRegs) return ATTN_ERR_UNSUPPORTED;
     BwdParams prm;
     prm.q = static_cast<const __nv_bfloat16*>(q);
     prm.k = static_cast<const __nv_bfloat16*>(k);
@@ -645,7 +731,7 @@ attn_status_t launch_bwd_impl(const void* q, const void* k, const void* v, const
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
     bwd_dkdv_kernel<D><<<(unsigned)dkv_blocks, kThreads, L::kSmem, stream>>>(mq, mdo, mk, mv, prm);
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
-    bwd_dq_kernel<D><<<(unsigned)dq_blocks, kThreads, L::kSmem, stream>>>(mq, mdo, mk, mv, prm);
+    bwd_dq_kernel<D><<<(unsigned)dq_blocks, kThreads, LQ::kSmem, stream>>>(mq, mdo, mk, mv, prm);
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
