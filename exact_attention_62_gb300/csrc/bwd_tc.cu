@@ -22,8 +22,10 @@
 //  * bwd_dkdv_kernel: one CTA per 128-key tile (key tile outer), looping over
 //    the query heads of its KV group and their query tiles.  With keys as the
 //    TMEM lanes: S^T = K Q_i^T and dP^T = V dO_i^T, then P^T and dS^T (bf16)
-//    over the columns just read, then dV += P^T dO_i and dK += dS^T Q_i with
-//    both A operands read from TMEM.  The four accumulators fill the 512
+//    over the dP^T columns just read, then dV += P^T dO_i and dK += dS^T Q_i
+//    with both A operands read from TMEM.  Once the elementwise warps hold
+//    S^T in registers, the next tile's S^T may be issued (when its Q tile
+//    is already loaded) while they work.  The four accumulators fill the 512
 //    TMEM columns.  Each thread (one key) needs L and D of the query rows it
 //    handles: they are staged in shared memory, double-buffered.
 //  * Both main kernels: warp 0 issues the TMA loads, warp 1 (convergent, one
@@ -92,36 +94,53 @@ __device__ __forceinline__ int first_q_tile(int c0, const BwdParams& p) {
 }
 
 // ------------------------------------------------------------------ D = rowsum(dO * O)
+// HBM-bound: each row is D bf16 of O and of dO.  A group of D/8 threads takes
+// a row with 16-byte loads; every thread has kDotRows rows' loads in flight
+// before it reduces any of them.
+constexpr int kDotThreads = 256;
+constexpr int kDotRows = 4;
 template <int D>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(kDotThreads)
     bwd_dot_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
                    float* __restrict__ dvec, int B, int Nq, int Hq) {
-    const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);  // (b, i, hq) row-major
-    const int lane = threadIdx.x & 31;
+    constexpr int kTpr = D / 8;                       // threads per row
+    constexpr int kRowsPerPass = kDotThreads / kTpr;  // rows a block covers per pass
     const long long rows = (long long)B * Nq * Hq;
-    if (row >= rows) return;
-    float acc = 0.f;
-    for (int c = lane * 4; c < D; c += 128) {
-        const uint2 a = *reinterpret_cast<const uint2*>(o + row * D + c);
-        const uint2 b = *reinterpret_cast<const uint2*>(dout + row * D + c);
-        const __nv_bfloat162* pa = reinterpret_cast<const __nv_bfloat162*>(&a);
-        const __nv_bfloat162* pb = reinterpret_cast<const __nv_bfloat162*>(&b);
+    const int sub = threadIdx.x % kTpr;
+    const long long base = (long long)blockIdx.x * kRowsPerPass * kDotRows + threadIdx.x / kTpr;
+    uint4 a[kDotRows], c[kDotRows];
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            const float2 fa = __bfloat1622float2(pa[e]);
-            const float2 fb = __bfloat1622float2(pb[e]);
-            acc = fmaf(fa.x, fb.x, acc);
-            acc = fmaf(fa.y, fb.y, acc);
+    for (int u = 0; u < kDotRows; ++u) {
+        const long long row = base + (long long)u * kRowsPerPass;  // (b, i, hq) row-major
+        a[u] = make_uint4(0u, 0u, 0u, 0u);
+        c[u] = a[u];
+        if (row < rows) {
+            a[u] = __ldg(reinterpret_cast<const uint4*>(o + row * D) + sub);
+            c[u] = __ldg(reinterpret_cast<const uint4*>(dout + row * D) + sub);
         }
     }
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (lane == 0) {
-        const int hq = (int)(row % Hq);
-        const long long bi = row / Hq;
-        const int i = (int)(bi % Nq);
-        const int b = (int)(bi / Nq);
-        dvec[((long long)b * Hq + hq) * Nq + i] = acc;
+    for (int u = 0; u < kDotRows; ++u) {
+        const __nv_bfloat162* pa = reinterpret_cast<const __nv_bfloat162*>(&a[u]);
+        const __nv_bfloat162* pc = reinterpret_cast<const __nv_bfloat162*>(&c[u]);
+        float acc = 0.f;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float2 fa = __bfloat1622float2(pa[e]);
+            const float2 fc = __bfloat1622float2(pc[e]);
+            acc = fmaf(fa.x, fc.x, acc);
+            acc = fmaf(fa.y, fc.y, acc);
+        }
+#pragma unroll
+        for (int off = kTpr / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        const long long row = base + (long long)u * kRowsPerPass;
+        if (sub == 0 && row < rows) {
+            const int hq = (int)(row % Hq);
+            const long long bi = row / Hq;
+            const int i = (int)(bi % Nq);
+            const int b = (int)(bi / Nq);
+            dvec[((long long)b * Hq + hq) * Nq + i] = acc;
+        }
     }
 }
 
@@ -138,12 +157,13 @@ struct BwdLay {
     static constexpr int kStage = 2 * kTile;
     static constexpr int kOffLD = kOffRing + STAGES * kStage;  // L and D: 2 buffers x 2 warpgroups x 2 x 64 floats
     static constexpr int kOffBar = kOffLD + 2 * 2 * kT * 4;
-    // barriers: X full, ring full[STAGES], ring empty[STAGES], S full, dS full, acc full
+    // barriers: X full, ring full[STAGES], ring empty[STAGES], S full, consumed, dS full, acc full
     static constexpr int kBarX = 0;
     static constexpr int kBarFull = 1;
     static constexpr int kBarEmpty = kBarFull + STAGES;
     static constexpr int kBarS = kBarEmpty + STAGES;
-    static constexpr int kBarDS = kBarS + 1;
+    static constexpr int kBarC = kBarS + 1;   // S^T, dP^T read into registers (256 threads)
+    static constexpr int kBarDS = kBarC + 1;  // P^T, dS^T in TMEM (256 threads)
     static constexpr int kBarAcc = kBarDS + 1;
     static constexpr int kNumBars = kBarAcc + 1;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
@@ -458,7 +478,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < L::kNumBars; ++i) mbar_init(bar(i), i == L::kBarDS ? 2u * kT : 1u);
+        for (int i = 0; i < L::kNumBars; ++i)
+            mbar_init(bar(i), (i == L::kBarDS || i == L::kBarC) ? 2u * kT : 1u);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -510,40 +531,73 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint32_t k_lo = sdesc_sw128_lo(sbase + L::kOffX0, 16);
         const uint32_t v_lo = sdesc_sw128_lo(sbase + L::kOffX1, 16);
-        for (int it = 0; it < n && ok; ++it) {
-            const int st = it % STAGES;
-            ok = mbar_wait_warp(bar(L::kBarFull + st), (it / STAGES) & 1, abort_flag, &g_bwd_status);
-            if (!ok) break;
-            tc_fence_after();
-            const uint32_t qaddr = sbase + L::kOffRing + st * L::kStage;
-            const uint32_t q_lo = sdesc_sw128_lo(qaddr, 16);
-            const uint32_t do_lo = sdesc_sw128_lo(qaddr + L::kTile, 16);
+        auto ring = [&](int it) { return sbase + L::kOffRing + (it % STAGES) * L::kStage; };
+        auto wait_full = [&](int it) {
+            if (ok) ok = mbar_wait_warp(bar(L::kBarFull + it % STAGES), (it / STAGES) & 1, abort_flag, &g_bwd_status);
+            if (ok) tc_fence_after();
+        };
+        auto issue_s = [&](int it) {  // S^T = K Q_it^T
+            const uint32_t q_lo = sdesc_sw128_lo(ring(it), 16);
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {  // S^T = K Q^T
+            for (int kk = 0; kk < D / 16; ++kk) {
                 const uint32_t off = ((kk >> 2) * kPanel + (kk & 3) * 32) >> 4;
                 mma_ss_elect(tmem + kS, k_lo + off, kHi, q_lo + off, kHi, kIdSS, kk > 0 ? 1u : 0u);
             }
+        };
+        auto issue_dp = [&](int it) {  // dP^T = V dO_it^T
+            const uint32_t do_lo = sdesc_sw128_lo(ring(it) + L::kTile, 16);
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {  // dP^T = V dO^T
+            for (int kk = 0; kk < D / 16; ++kk) {
                 const uint32_t off = ((kk >> 2) * kPanel + (kk & 3) * 32) >> 4;
                 mma_ss_elect(tmem + kDP, v_lo + off, kHi, do_lo + off, kHi, kIdSS, kk > 0 ? 1u : 0u);
             }
+        };
+        wait_full(0);
+        if (ok) {
+            issue_s(0);
+            issue_dp(0);
             tc_commit_elect(bar(L::kBarS));
+        }
+        for (int it = 0; it < n && ok; ++it) {
+            bool s_next = false;  // S^T of the next tile already issued
+            if (it + 1 < n) {
+                // The elementwise warps hold S^T and dP^T and write P^T, dS^T over
+                // dP^T only, so the S columns are free: if the next Q tile is
+                // already loaded, its S^T goes to the tensor core now.
+                ok = mbar_wait_warp(bar(L::kBarC), it & 1, abort_flag, &g_bwd_status);
+                if (!ok) break;
+                s_next = __all_sync(0xffffffffu,
+                                    mbar_try_wait(bar(L::kBarFull + (it + 1) % STAGES), ((it + 1) / STAGES) & 1));
+                if (s_next) {
+                    tc_fence_after();
+                    issue_s(it + 1);
+                }
+            }
             ok = mbar_wait_warp(bar(L::kBarDS), it & 1, abort_flag, &g_bwd_status);
             if (!ok) break;
             tc_fence_after();
-            const uint32_t qn_lo = sdesc_sw128_lo(qaddr, kNLbo);
-            const uint32_t don_lo = sdesc_sw128_lo(qaddr + L::kTile, kNLbo);
+            const uint32_t qn_lo = sdesc_sw128_lo(ring(it), kNLbo);
+            const uint32_t don_lo = sdesc_sw128_lo(ring(it) + L::kTile, kNLbo);
 #pragma unroll
             for (int kk = 0; kk < kT / 16; ++kk) {  // 16 query rows = 8 bf16 columns of P^T / dS^T
                 const uint32_t r_off = (kk * 16 * 128) >> 4;
                 const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
-                // query rows 16kk..: warpgroup kk / 4 wrote them at columns 64 (kk / 4) + 8 (kk % 4)
+                // query rows 16kk..: warpgroup kk / 4 wrote P^T at dP^T column 64 (kk / 4) + 8 (kk % 4)
+                // and dS^T 32 columns further
                 const uint32_t pc = (kk >> 2) * 64 + (kk & 3) * 8;
-                mma_ts_elect(tmem + kDV, tmem + kS + pc, don_lo + r_off, kHi, kIdAcc, acc);   // dV += P^T dO
-                mma_ts_elect(tmem + kDK, tmem + kDP + pc, qn_lo + r_off, kHi, kIdAcc, acc);   // dK += dS^T Q
+                mma_ts_elect(tmem + kDV, tmem + kDP + pc, don_lo + r_off, kHi, kIdAcc, acc);       // dV += P^T dO
+                mma_ts_elect(tmem + kDK, tmem + kDP + 32 + pc, qn_lo + r_off, kHi, kIdAcc, acc);  // dK += dS^T Q
             }
-            tc_commit_elect(bar(L::kBarEmpty + st));  // Q_i and dO_i fully read
+            tc_commit_elect(bar(L::kBarEmpty + it % STAGES));  // Q_i and dO_i fully read
+            if (it + 1 < n) {
+                if (!s_next) {
+                    wait_full(it + 1);
+                    if (!ok) break;
+                    issue_s(it + 1);
+                }
+                issue_dp(it + 1);  // after dV, dK have read P^T, dS^T (in-order pipe)
+                tc_commit_elect(bar(L::kBarS));
+            }
             if (it == n - 1) tc_commit_elect(bar(L::kBarAcc));
         }
       }
@@ -597,6 +651,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t s[64], dp[64];
             tmem_ld64_sync(tmem + lane_base + kS + 64 * w, s);
             tmem_ld64_sync(tmem + lane_base + kDP + 64 * w, dp);
+            tc_fence_before();
+            mbar_arrive(bar(L::kBarC));  // the S^T columns may be overwritten now
             if (need_mask) {
                 // the query rows that may see this key: tile columns [lo, kT)
                 const long long first = key >= p.Nk ? (long long)kT
@@ -619,9 +675,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 pk[c] = pack_bf16(pv[0], pv[1]);
                 dk[c] = pack_bf16(dsv[0], dsv[1]);
             }
-            // each warpgroup writes only columns it has read itself
-            tmem_st32(tmem + lane_base + kS + 64 * w, pk);   // P^T
-            tmem_st32(tmem + lane_base + kDP + 64 * w, dk);  // dS^T
+            // each warpgroup writes only dP^T columns it has read itself
+            tmem_st32(tmem + lane_base + kDP + 64 * w, pk);       // P^T
+            tmem_st32(tmem + lane_base + kDP + 64 * w + 32, dk);  // dS^T
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(bar(L::kBarDS));
@@ -721,12 +777,13 @@ attn_status_t launch_bwd_impl(const void* q, const void* k, const void* v, const
     prm.scale = scale;
     prm.scale_log2 = scale * kLog2e;
     const long long rows = (long long)B * Nq * Hq;
-    const long long dot_blocks = (rows + 7) / 8;
+    const long long dot_rows_per_block = (long long)(kDotThreads / (D / 8)) * kDotRows;
+    const long long dot_blocks = (rows + dot_rows_per_block - 1) / dot_rows_per_block;
     const long long dq_blocks = (long long)B * Hq * ((Nq + kT - 1) / kT);
     const long long dkv_blocks = (long long)B * Hkv * ((Nk + kT - 1) / kT);
     if (dot_blocks > 0x7fffffffLL || dq_blocks > 0x7fffffffLL || dkv_blocks > 0x7fffffffLL)
         return ATTN_ERR_UNSUPPORTED;
-    bwd_dot_kernel<D><<<(unsigned)dot_blocks, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(o),
+    bwd_dot_kernel<D><<<(unsigned)dot_blocks, kDotThreads, 0, stream>>>(static_cast<const __nv_bfloat16*>(o),
                                                                prm.do_, dvec, B, Nq, Hq);
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
     bwd_dkdv_kernel<D><<<(unsigned)dkv_blocks, kThreads, L::kSmem, stream>>>(mq, mdo, mk, mv, prm);
