@@ -19,6 +19,76 @@ constexpr int kBlockRows = 128;
 constexpr int kQThreads = 256;
 constexpr float kFp8Max = 448.0f;
 
+// Maximum of `v` over the CTA (every thread gets it).
+__device__ __forceinline__ float block_max(float v) {
+    __shared__ float red[kQThreads / 32];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+    __syncthreads();
+    v = red[0];
+#pragma unroll
+    for (int i = 1; i < kQThreads / 32; ++i) v = fmaxf(v, red[i]);
+    return v;
+}
+
+// d = 64 or 128: the block is read once, with 16-byte loads (D / 8 threads
+// per row), and held in registers while its amax is reduced; each thread
+// then writes 8 codes per chunk.  Same arithmetic as the general kernel.
+template <int D>
+__global__ void __launch_bounds__(kQThreads)
+    quantize_fp8_regs_kernel(const __nv_bfloat16* __restrict__ x, uint8_t* __restrict__ codes,
+                             float* __restrict__ scales, int N, int H) {
+    constexpr int kC = D / 8;                             // 16-byte chunks per row
+    constexpr int kK = kBlockRows * kC / kQThreads;       // chunks per thread
+    static_assert(kBlockRows * kC % kQThreads == 0, "chunk split");
+    const int blk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int nb = gridDim.x;
+    const int r0 = blk * kBlockRows;
+    const int rows = min(kBlockRows, N - r0);
+    uint4 v[kK];
+    float amax = 0.f;
+#pragma unroll
+    for (int k = 0; k < kK; ++k) {
+        const int i = threadIdx.x + k * kQThreads;
+        const int r = i / kC, c = i % kC;
+        v[k] = make_uint4(0u, 0u, 0u, 0u);
+        if (r < rows)
+            v[k] = __ldg(reinterpret_cast<const uint4*>(x + (((long long)b * N + r0 + r) * H + h) * D) + c);
+        const __nv_bfloat162* e = reinterpret_cast<const __nv_bfloat162*>(&v[k]);
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            const float2 f = __bfloat1622float2(e[t]);
+            amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+        }
+    }
+    amax = block_max(amax);
+    const bool nz = amax > 0.f;
+    const float inv = nz ? kFp8Max / amax : 1.f;
+    if (threadIdx.x == 0) scales[((long long)b * H + h) * nb + blk] = nz ? amax / kFp8Max : 1.f;
+#pragma unroll
+    for (int k = 0; k < kK; ++k) {
+        const int i = threadIdx.x + k * kQThreads;
+        const int r = i / kC, c = i % kC;
+        if (r >= rows) continue;
+        const __nv_bfloat162* e = reinterpret_cast<const __nv_bfloat162*>(&v[k]);
+        uint32_t w[2];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            const float2 f = __bfloat1622float2(e[t]);
+            const float2 y = make_float2(__fmul_rn(f.x, inv), __fmul_rn(f.y, inv));
+            const uint32_t q = __nv_cvt_float2_to_fp8x2(y, __NV_SATFINITE, __NV_E4M3);
+            if (t & 1)
+                w[t >> 1] |= q << 16;
+            else
+                w[t >> 1] = q;
+        }
+        *reinterpret_cast<uint2*>(codes + (((long long)b * N + r0 + r) * H + h) * D + 8 * c) =
+            make_uint2(w[0], w[1]);
+    }
+}
+
+// Any even d: pairs of elements, two passes over the block.
 __global__ void __launch_bounds__(kQThreads)
     quantize_fp8_kernel(const __nv_bfloat16* __restrict__ x, uint8_t* __restrict__ codes,
                         float* __restrict__ scales, int N, int H, int d) {
@@ -36,14 +106,7 @@ __global__ void __launch_bounds__(kQThreads)
         const float2 v = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(x + pair_offset(e)));
         amax = fmaxf(amax, fmaxf(fabsf(v.x), fabsf(v.y)));
     }
-    __shared__ float red[kQThreads / 32];
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
-    __syncthreads();
-    amax = red[0];
-#pragma unroll
-    for (int i = 1; i < kQThreads / 32; ++i) amax = fmaxf(amax, red[i]);
+    amax = block_max(amax);
     const bool nz = amax > 0.f;
     const float inv = nz ? kFp8Max / amax : 1.f;
     if (threadIdx.x == 0) scales[((long long)b * H + h) * nb + blk] = nz ? amax / kFp8Max : 1.f;
@@ -65,8 +128,14 @@ attn_status_t launch_quantize_fp8(const void* x, void* codes, float* scales, int
     const int nb = (N + kBlockRows - 1) / kBlockRows;
     if (nb > 0x7fffffff || H > 65535 || B > 65535) return ATTN_ERR_UNSUPPORTED;
     dim3 grid(nb, H, B);
-    quantize_fp8_kernel<<<grid, kQThreads, 0, stream>>>(static_cast<const __nv_bfloat16*>(x),
-                                                        static_cast<uint8_t*>(codes), scales, N, H, d);
+    const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
+    uint8_t* cb = static_cast<uint8_t*>(codes);
+    if (d == 128)
+        quantize_fp8_regs_kernel<128><<<grid, kQThreads, 0, stream>>>(xb, cb, scales, N, H);
+    else if (d == 64)
+        quantize_fp8_regs_kernel<64><<<grid, kQThreads, 0, stream>>>(xb, cb, scales, N, H);
+    else
+        quantize_fp8_kernel<<<grid, kQThreads, 0, stream>>>(xb, cb, scales, N, H, d);
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
