@@ -88,3 +88,66 @@ def test_reference_arm_under_torchrun_prints_once():
     assert line["impl"] == "reference" and line["n_gpus"] == 2
     assert line["cpu_baseline"]["kind"] == "oracle" and line["value"] > 0
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
+
+
+CP_WORKER = r"""
+import os, sys, json, math
+sys.path.insert(0, %r)
+import numpy as np
+import torch
+import torch.distributed as dist
+import bench, oracle
+from exact_attention_62_gb300.inputs import make_qkv
+dist.init_process_group("gloo", init_method="env://")
+rank, world, local = bench.dist_env()
+out = {}
+for name, (B, Hq, Hkv, Nq, Nk, d, causal) in {"prefill_causal": (1, 4, 2, 300, 300, 16, True),
+                                              "prefill": (2, 2, 1, 130, 257, 8, False),
+                                              "decode": (2, 4, 2, 1, 1000, 16, False)}.items():
+    q, k, v = make_qkv(B, Hq, Hkv, Nq, Nk, d, seed=3)
+    scale = 1.0 / math.sqrt(d)
+    # this rank's key shard, and the partial result of every query row over it
+    j0, j1 = rank * Nk // world, (rank + 1) * Nk // world
+    rows = B * Hq * Nq
+    o_p = torch.zeros(rows, d, dtype=torch.float64)
+    l_p = torch.full((rows,), float("-inf"), dtype=torch.float64)
+    r = 0
+    for b in range(B):
+        for hq in range(Hq):
+            for i in range(Nq):
+                m, l, acc = oracle.segment_state(q, k, v, causal, scale, b, hq, i, j0, j1)
+                if l > 0:
+                    o_p[r] = torch.from_numpy(acc / l)
+                    l_p[r] = m + math.log(l)
+                r += 1
+    # the one exchange step, then the lse merge of the gathered partials
+    o_all = [torch.empty_like(o_p) for _ in range(world)]
+    l_all = [torch.empty_like(l_p) for _ in range(world)]
+    dist.all_gather(o_all, o_p)
+    dist.all_gather(l_all, l_p)
+    o_m, l_m = oracle.merge_lse(torch.stack(o_all).numpy(), torch.stack(l_all).numpy())
+    o_ref, l_ref = oracle.attn_fwd(q, k, v, causal, scale)
+    o_ref = np.transpose(o_ref, (0, 2, 1, 3)).reshape(rows, d)      # [B, Hq, Nq, d] row order
+    l_ref = np.asarray(l_ref).reshape(rows)
+    fin = np.isfinite(l_ref)
+    out[name] = {"dO": float(np.abs(o_m - o_ref).max()),
+                 "dL": float(np.abs(l_m[fin] - l_ref[fin]).max()) if fin.any() else 0.0,
+                 "inf_match": bool(np.array_equal(np.isfinite(l_m), fin))}
+print(json.dumps({"rank": rank, "res": out}), flush=True)
+dist.destroy_process_group()
+""" % ROOT
+
+
+def test_context_parallel_merge_over_gloo_ranks():
+    """A context-parallel split (each rank holds half of the keys) needs one
+    exchange: every rank's partial (o, lse) of every query row, all-gathered,
+    then the lse merge of Lecture 11 section 6.2 step 3.  Two gloo ranks
+    compute their shards' partials with the oracle (global causal rule, so
+    some rows see no key of a shard: o = 0, lse = -inf), all-gather them and
+    merge; the result equals the unsharded oracle to 1e-12 on each rank."""
+    outs = run_two_ranks(CP_WORKER)
+    for o in outs:
+        res = json.loads(o.strip().splitlines()[-1])["res"]
+        for name, r in res.items():
+            assert r["inf_match"], name
+            assert r["dO"] <= 1e-12 and r["dL"] <= 1e-12, (name, r)
