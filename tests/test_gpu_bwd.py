@@ -72,3 +72,26 @@ def test_backward_writes_zeros_where_nothing_flows(attn):
     torch.cuda.synchronize()
     assert torch.isfinite(dq).all() and torch.isfinite(dk).all() and torch.isfinite(dv).all()
     assert torch.all(dq[:, :Nq - Nk] == 0)    # rows 0 .. Nq-Nk-1 see no key
+
+
+def test_backward_full_size_sampled_heads(attn, oracle_mod):
+    """The backward workload at full size (B=4, Hq=Hkv=16, N=4096, d=128,
+    causal), in the launch configuration the benchmark times.  Heads are
+    independent, so the oracle's backward of one (batch, head) sub-problem is
+    exact for that head's dQ, dK and dV; two heads are checked in full."""
+    B, H, N, d = 4, 16, 4096, 128
+    q, k, v = make_qkv(B, H, H, N, N, d, 12)
+    g = torch.Generator().manual_seed(13)
+    dout = torch.randn((B, N, H, d), generator=g).to(torch.bfloat16)
+    scale = 1.0 / math.sqrt(d)
+    qg, kg, vg, dog = q.to(DEV), k.to(DEV), v.to(DEV), dout.to(DEV)
+    o, lse = attn.attn_fwd(qg, kg, vg, True, scale)
+    dq, dk, dv = attn.attn_bwd(qg, kg, vg, o, lse, dog, True, scale)
+    torch.cuda.synchronize()
+    assert attn.attn_check_device_status() == 0
+    for b, h in ((1, 3), (3, 15)):
+        sl = (slice(b, b + 1), slice(None), slice(h, h + 1), slice(None))
+        rq, rk, rv = oracle_mod.attn_bwd(q[sl], k[sl], v[sl], dout[sl], True, scale)
+        check("dq b%d h%d" % (b, h), dq[sl], rq)
+        check("dk b%d h%d" % (b, h), dk[sl], rk)
+        check("dv b%d h%d" % (b, h), dv[sl], rv)
