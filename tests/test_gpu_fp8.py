@@ -86,14 +86,16 @@ def test_fp8_forward(attn, oracle_mod, B, Hq, Hkv, Nq, Nk, causal, qs):
                 assert np.abs(og[b, i, h] - eo[b, i, h]).max() <= bound, (b, h, i)
 
 
-def test_fp8_forward_full_size_sampled(attn, oracle_mod):
-    """The FP8 workload at full size (B=4, Hq=Hkv=16, N=4096, d=128, causal),
-    in the launch configuration the benchmark times, on sampled rows against
-    the oracle run on the dequantised Q and K (bar 2 above)."""
+@pytest.mark.parametrize("B,Hq,Hkv,N", [(4, 16, 16, 4096), (1, 32, 8, 16384)],
+                         ids=["training_prefill", "long_sequence"])
+def test_fp8_forward_full_size_sampled(attn, oracle_mod, B, Hq, Hkv, N):
+    """The FP8 workloads at full size (B=4, Hq=Hkv=16, N=4096 and B=1,
+    Hq=32, Hkv=8, N=16384; d=128, causal), on sampled rows against the
+    oracle run on the dequantised Q and K (bar 2 above)."""
     from exact_attention_62_gb300.inputs import sample_rows
-    B, H, N, d = 4, 16, 4096, 128
+    H, d = Hq, 128
     scale = 1.0 / math.sqrt(d)
-    q, k, v = make_qkv(B, H, H, N, N, d, 14)
+    q, k, v = make_qkv(B, Hq, Hkv, N, N, d, 14)
     q8, qsc = attn.attn_quantize_fp8(q.to(DEV))
     k8, ksc = attn.attn_quantize_fp8(k.to(DEV))
     o, lse = attn.attn_fwd_fp8(q8, k8, v.to(DEV), qsc, ksc, True, scale)
@@ -102,7 +104,7 @@ def test_fp8_forward_full_size_sampled(attn, oracle_mod):
     qd = oracle_mod.dequantize_fp8_blocks(q8.cpu().numpy(), qsc.cpu().numpy()).astype(np.float32)
     kd = oracle_mod.dequantize_fp8_blocks(k8.cpu().numpy(), ksc.cpu().numpy()).astype(np.float32)
     rows = sample_rows(B, H, N, 256, 15)
-    rows += [(0, 0, 127), (1, 7, 128), (B - 1, H - 1, N - 1), (2, 3, 0)]
+    rows += [(0, 0, 127), (B - 1, H // 2, 128), (B - 1, H - 1, N - 1), (0, 3, 0)]
     ro, rl = oracle_mod.attn_rows(qd, kd, v, True, scale, rows)
     o_sel = torch.stack([o[b, i, h] for b, h, i in rows])
     l_sel = torch.stack([lse[b, h, i] for b, h, i in rows])
