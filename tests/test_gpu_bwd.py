@@ -74,24 +74,31 @@ def test_backward_writes_zeros_where_nothing_flows(attn):
     assert torch.all(dq[:, :Nq - Nk] == 0)    # rows 0 .. Nq-Nk-1 see no key
 
 
-def test_backward_full_size_sampled_heads(attn, oracle_mod):
-    """The backward workload at full size (B=4, Hq=Hkv=16, N=4096, d=128,
-    causal), in the launch configuration the benchmark times.  Heads are
-    independent, so the oracle's backward of one (batch, head) sub-problem is
-    exact for that head's dQ, dK and dV; two heads are checked in full."""
-    B, H, N, d = 4, 16, 4096, 128
-    q, k, v = make_qkv(B, H, H, N, N, d, 12)
+@pytest.mark.parametrize("B,Hq,Hkv,N,groups", [(4, 16, 16, 4096, [(1, 3), (3, 15)]),
+                                               (1, 32, 8, 16384, [(0, 5)])],
+                         ids=["training_prefill", "long_sequence"])
+def test_backward_full_size_sampled_heads(attn, oracle_mod, B, Hq, Hkv, N, groups):
+    """The backward workloads at full size (B=4, Hq=Hkv=16, N=4096 and B=1,
+    Hq=32, Hkv=8, N=16384; d=128, causal), in the launch configuration the
+    benchmark times.  KV groups are independent, so the oracle's backward of
+    one (batch, KV head) sub-problem with its query heads is exact for their
+    dQ and for that KV head's dK and dV; the listed groups are checked in
+    full."""
+    d = 128
+    q, k, v = make_qkv(B, Hq, Hkv, N, N, d, 12)
     g = torch.Generator().manual_seed(13)
-    dout = torch.randn((B, N, H, d), generator=g).to(torch.bfloat16)
+    dout = torch.randn((B, N, Hq, d), generator=g).to(torch.bfloat16)
     scale = 1.0 / math.sqrt(d)
     qg, kg, vg, dog = q.to(DEV), k.to(DEV), v.to(DEV), dout.to(DEV)
     o, lse = attn.attn_fwd(qg, kg, vg, True, scale)
     dq, dk, dv = attn.attn_bwd(qg, kg, vg, o, lse, dog, True, scale)
     torch.cuda.synchronize()
     assert attn.attn_check_device_status() == 0
-    for b, h in ((1, 3), (3, 15)):
-        sl = (slice(b, b + 1), slice(None), slice(h, h + 1), slice(None))
-        rq, rk, rv = oracle_mod.attn_bwd(q[sl], k[sl], v[sl], dout[sl], True, scale)
-        check("dq b%d h%d" % (b, h), dq[sl], rq)
-        check("dk b%d h%d" % (b, h), dk[sl], rk)
-        check("dv b%d h%d" % (b, h), dv[sl], rv)
+    G = Hq // Hkv
+    for b, gk in groups:
+        sq = (slice(b, b + 1), slice(None), slice(gk * G, (gk + 1) * G), slice(None))
+        sk = (slice(b, b + 1), slice(None), slice(gk, gk + 1), slice(None))
+        rq, rk, rv = oracle_mod.attn_bwd(q[sq], k[sk], v[sk], dout[sq], True, scale)
+        check("dq b%d g%d" % (b, gk), dq[sq], rq)
+        check("dk b%d g%d" % (b, gk), dk[sk], rk)
+        check("dv b%d g%d" % (b, gk), dv[sk], rv)
