@@ -478,20 +478,30 @@ def run_ours(args):
 
 
 def run_extra(args):
-    """--only backward / fp8: attn_bwd or attn_fwd_fp8 on the prefill workload,
-    timed like the step's calls (L2 flushed clean before each, CUDA events).
-    For profiling; prints one JSON line, not the bench contract."""
+    """--only backward / fp8: attn_bwd or attn_fwd_fp8 on the prefill workload;
+    --only paged: attn_decode_paged on the decode workload with pages of
+    --page-size keys in a random order.  Timed like the step's calls (L2
+    flushed clean before each, CUDA events).  For profiling; prints one JSON
+    line, not the bench contract."""
     import torch
     import exact_attention_62_gb300 as attn
-    from exact_attention_62_gb300.inputs import make_qkv
+    from exact_attention_62_gb300.inputs import make_paged, make_qkv
     attn.ensure_built()
     dev = torch.device("cuda", 0)
+    flush_w = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flush_r = torch.ones(64 << 20, dtype=torch.float32, device=dev)
+    if args.only == "paged":
+        dB, dHq, dHkv, dNk, dd = DECODE[args.decode]
+        qh, kp, vp, table, lens = make_paged(dB, dHq, dHkv, dd, args.page_size, [dNk] * dB, seed=20,
+                                             extra_pages=0, poison=False)
+        qh, kp, vp, table, lens = (x.to(dev) for x in (qh, kp, vp, table, lens))
+        call = lambda: attn.attn_decode_paged(qh, kp, vp, table, lens, dNk, 1.0 / math.sqrt(dd))
+        return _time_extra(args, call, flush_w, flush_r, attn, "GB/s", decode_bytes(DECODE[args.decode]) / 1e9,
+                           args.decode)
     B, Hq, Hkv, Nq, Nk, d, causal = PREFILL[args.prefill]
     scale = 1.0 / math.sqrt(d)
     q, k, v = (x.to(dev) for x in make_qkv(B, Hq, Hkv, Nq, Nk, d, seed=10))
     o, lse = attn.attn_fwd(q, k, v, causal, scale)
-    flush_w = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
-    flush_r = torch.ones(64 << 20, dtype=torch.float32, device=dev)
     if args.only == "backward":
         dout = torch.randn_like(q)
         dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
@@ -504,6 +514,11 @@ def run_extra(args):
         k8, ks = attn.attn_quantize_fp8(k)
         call = lambda: attn.attn_fwd_fp8(q8, k8, v, qs, ks, causal, scale, o=o, lse=lse)
         flops = prefill_flops(PREFILL[args.prefill])
+    return _time_extra(args, call, flush_w, flush_r, attn, "tflops", flops / 1e12, args.prefill)
+
+
+def _time_extra(args, call, flush_w, flush_r, attn, unit, work, workload):
+    import torch
     for _ in range(args.warmup):
         flush_w.zero_()
         flush_r.sum()
@@ -521,8 +536,10 @@ def run_extra(args):
     if attn.attn_check_device_status() != 0:
         raise RuntimeError("device status reports a timed-out wait")
     ms = statistics.mean(ts)
-    print(json.dumps({"profile_only": args.only, "workload": args.prefill, "ms": ms,
-                      "tflops": flops / (ms * 1e-3) / 1e12}))
+    out = {"profile_only": args.only, "workload": workload, "ms": ms, unit: work / (ms * 1e-3)}
+    if args.only == "paged":
+        out["page_size"] = args.page_size
+    print(json.dumps(out))
     return 0
 
 
@@ -536,7 +553,8 @@ def main(argv=None):
     ap.add_argument("--decode", choices=sorted(DECODE), default="decode_64k")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["prefill", "decode", "backward", "fp8"], default=None,
+    ap.add_argument("--page-size", type=int, default=16, help="--only paged: keys per page")
+    ap.add_argument("--only", choices=["prefill", "decode", "backward", "fp8", "paged"], default=None,
                     help="time one part only (for profiling; no JSON contract): a half of the "
                          "step, or the backward pass / the FP8-Q,K forward on the prefill workload")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer measurement")
@@ -546,7 +564,7 @@ def main(argv=None):
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         return run_reference(args)
-    if args.only in ("backward", "fp8"):
+    if args.only in ("backward", "fp8", "paged"):
         return run_extra(args)
     return run_ours(args)
 
