@@ -138,17 +138,36 @@ def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
-def _stream(stream):
+def _stream(stream, device=None):
     import torch
-    s = torch.cuda.current_stream() if stream is None else stream
+    s = torch.cuda.current_stream(device) if stream is None else stream
     return ctypes.c_void_p(s.cuda_stream)
 
 
-def _need_cuda_contig(name, t):
+def _need_cuda_contig(name, t, device=None):
     if not t.is_cuda:
         raise ValueError("%s must be a CUDA tensor" % name)
     if not t.is_contiguous():
         raise ValueError("%s must be contiguous" % name)
+    if device is not None and t.device != device:
+        raise ValueError("%s is on %s, the call's tensors on %s" % (name, t.device, device))
+
+
+def _need_buffer(name, t, shape, dtype, device):
+    """A caller-provided output or input buffer: the kernels index it from the
+    sizes alone, so its shape, dtype and device must be exactly these."""
+    _need_cuda_contig(name, t, device)
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError("%s must have shape %s, got %s" % (name, tuple(shape), tuple(t.shape)))
+    if t.dtype != dtype:
+        raise ValueError("%s must be %s, got %s" % (name, dtype, t.dtype))
+
+
+def _need_workspace(t, device):
+    import torch
+    _need_cuda_contig("workspace", t, device)
+    if t.dtype != torch.uint8:
+        raise ValueError("workspace must be a uint8 tensor")
 
 
 def attn_fwd(q, k, v, causal: bool = False, scale: float | None = None, o=None, lse=None,
@@ -165,16 +184,20 @@ def attn_fwd(q, k, v, causal: bool = False, scale: float | None = None, o=None, 
         raise ValueError("shape mismatch: q %s k %s v %s" % (tuple(q.shape), tuple(k.shape), tuple(v.shape)))
     if not (q.dtype == k.dtype == v.dtype):
         raise ValueError("q, k, v must share a dtype")
+    dev = q.device
     for n, t in (("q", q), ("k", k), ("v", v)):
-        _need_cuda_contig(n, t)
+        _need_cuda_contig(n, t, dev)
     if scale is None:
         scale = d ** -0.5
     if o is None:
         o = torch.empty_like(q)
     if lse is None:
-        lse = torch.empty((B, Hq, Nq), dtype=torch.float32, device=q.device)
-    st = lib().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Nq, Nk, d,
-                        int(bool(causal)), float(scale), _dtype_code(q), _stream(stream))
+        lse = torch.empty((B, Hq, Nq), dtype=torch.float32, device=dev)
+    _need_buffer("o", o, q.shape, q.dtype, dev)
+    _need_buffer("lse", lse, (B, Hq, Nq), torch.float32, dev)
+    with torch.cuda.device(dev):
+        st = lib().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Nq, Nk, d,
+                            int(bool(causal)), float(scale), _dtype_code(q), _stream(stream, dev))
     _check("attn_fwd", st)
     return o, lse
 
@@ -203,23 +226,32 @@ def attn_decode_splitkv(q, k_cache, v_cache, scale: float | None = None, num_spl
     Bk, Nk, Hkv, dk = k_cache.shape
     if Bk != B or dk != d or tuple(v_cache.shape) != tuple(k_cache.shape):
         raise ValueError("shape mismatch")
+    if not (q.dtype == k_cache.dtype == v_cache.dtype):
+        raise ValueError("q and the caches must share a dtype")
+    dev = q.device
     for n, t in (("q", q), ("k_cache", k_cache), ("v_cache", v_cache)):
-        _need_cuda_contig(n, t)
+        _need_cuda_contig(n, t, dev)
     if scale is None:
         scale = d ** -0.5
     if num_splits == 0 and Nk > 0 and B > 0 and Hq > 0:
-        num_splits = attn_decode_num_splits(B, Hq, Hkv, Nk, d)
+        with torch.cuda.device(dev):
+            num_splits = attn_decode_num_splits(B, Hq, Hkv, Nk, d)
     wbytes = attn_decode_workspace_bytes(B, Hq, Hkv, Nk, d, num_splits) if Nk > 0 and B > 0 and Hq > 0 else 0
     if workspace is None and wbytes > 0:
-        workspace = torch.empty(wbytes, dtype=torch.uint8, device=q.device)
+        workspace = torch.empty(wbytes, dtype=torch.uint8, device=dev)
+    if workspace is not None:
+        _need_workspace(workspace, dev)
     if o is None:
         o = torch.empty_like(q)
     if lse is None:
-        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=dev)
+    _need_buffer("o", o, q.shape, q.dtype, dev)
+    _need_buffer("lse", lse, (B, Hq), torch.float32, dev)
     wsize = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    st = lib().attn_decode_splitkv(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(o), _ptr(lse),
-                                   B, Hq, Hkv, Nk, d, float(scale), int(num_splits),
-                                   _ptr(workspace), wsize, _dtype_code(q), _stream(stream))
+    with torch.cuda.device(dev):
+        st = lib().attn_decode_splitkv(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(o), _ptr(lse),
+                                       B, Hq, Hkv, Nk, d, float(scale), int(num_splits),
+                                       _ptr(workspace), wsize, _dtype_code(q), _stream(stream, dev))
     _check("attn_decode_splitkv", st)
     return o, lse
 
@@ -241,17 +273,23 @@ def attn_decode_splitkv_static(q, k_cache, v_cache, scale: float | None = None,
     Bk, Nk, Hkv, dk = k_cache.shape
     if Bk != B or dk != d or tuple(v_cache.shape) != tuple(k_cache.shape):
         raise ValueError("shape mismatch")
+    if not (q.dtype == k_cache.dtype == v_cache.dtype):
+        raise ValueError("q and the caches must share a dtype")
+    dev = q.device
     for n, t in (("q", q), ("k_cache", k_cache), ("v_cache", v_cache)):
-        _need_cuda_contig(n, t)
+        _need_cuda_contig(n, t, dev)
     if scale is None:
         scale = d ** -0.5
     if o is None:
         o = torch.empty_like(q)
     if lse is None:
-        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
-    st = lib().attn_decode_splitkv_static(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(o),
-                                          _ptr(lse), B, Hq, Hkv, Nk, d, float(scale),
-                                          int(num_splits), _dtype_code(q), _stream(stream))
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=dev)
+    _need_buffer("o", o, q.shape, q.dtype, dev)
+    _need_buffer("lse", lse, (B, Hq), torch.float32, dev)
+    with torch.cuda.device(dev):
+        st = lib().attn_decode_splitkv_static(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(o),
+                                              _ptr(lse), B, Hq, Hkv, Nk, d, float(scale),
+                                              int(num_splits), _dtype_code(q), _stream(stream, dev))
     _check("attn_decode_splitkv_static", st)
     return o, lse
 
@@ -262,16 +300,22 @@ def attn_merge_lse(o_parts, lse_parts, out_dtype=None, o=None, lse=None, stream=
     P, rows, d = o_parts.shape
     if tuple(lse_parts.shape) != (P, rows):
         raise ValueError("lse_parts must be [P, rows]")
+    if o_parts.dtype != torch.float32 or lse_parts.dtype != torch.float32:
+        raise ValueError("o_parts and lse_parts must be float32")
+    dev = o_parts.device
     for n, t in (("o_parts", o_parts), ("lse_parts", lse_parts)):
-        _need_cuda_contig(n, t)
+        _need_cuda_contig(n, t, dev)
     if out_dtype is None:
-        out_dtype = torch.float32
+        out_dtype = o.dtype if o is not None else torch.float32
     if o is None:
-        o = torch.empty((rows, d), dtype=out_dtype, device=o_parts.device)
+        o = torch.empty((rows, d), dtype=out_dtype, device=dev)
     if lse is None:
-        lse = torch.empty((rows,), dtype=torch.float32, device=o_parts.device)
-    st = lib().attn_merge_lse(_ptr(o_parts), _ptr(lse_parts), P, rows, d, _ptr(o), _ptr(lse),
-                              _dtype_code(o), _stream(stream))
+        lse = torch.empty((rows,), dtype=torch.float32, device=dev)
+    _need_buffer("o", o, (rows, d), out_dtype, dev)
+    _need_buffer("lse", lse, (rows,), torch.float32, dev)
+    with torch.cuda.device(dev):
+        st = lib().attn_merge_lse(_ptr(o_parts), _ptr(lse_parts), P, rows, d, _ptr(o), _ptr(lse),
+                                  _dtype_code(o), _stream(stream, dev))
     _check("attn_merge_lse", st)
     return o, lse
 
@@ -321,28 +365,37 @@ def attn_decode_paged(q, k_pages, v_pages, block_table, seq_lens, max_seq_len: i
         raise ValueError("block_table must be [B, max_pages] and seq_lens [B]")
     if block_table.dtype != torch.int32 or seq_lens.dtype != torch.int32:
         raise ValueError("block_table and seq_lens must be int32")
+    if not (q.dtype == k_pages.dtype == v_pages.dtype):
+        raise ValueError("q and the page pools must share a dtype")
+    dev = q.device
     for n, t in (("q", q), ("k_pages", k_pages), ("v_pages", v_pages),
                  ("block_table", block_table), ("seq_lens", seq_lens)):
-        _need_cuda_contig(n, t)
+        _need_cuda_contig(n, t, dev)
     if scale is None:
         scale = d ** -0.5
     max_pages = block_table.shape[1]
     if num_splits == 0 and max_seq_len > 0 and B > 0 and Hq > 0:
-        num_splits = attn_decode_paged_num_splits(B, Hq, Hkv, d, page_size, max_seq_len)
+        with torch.cuda.device(dev):
+            num_splits = attn_decode_paged_num_splits(B, Hq, Hkv, d, page_size, max_seq_len)
     wbytes = (attn_decode_workspace_bytes(B, Hq, Hkv, max_seq_len, d, num_splits)
               if max_seq_len > 0 and B > 0 and Hq > 0 and num_splits > 0 else 0)
     if workspace is None and wbytes > 0:
-        workspace = torch.empty(wbytes, dtype=torch.uint8, device=q.device)
+        workspace = torch.empty(wbytes, dtype=torch.uint8, device=dev)
+    if workspace is not None:
+        _need_workspace(workspace, dev)
     if o is None:
         o = torch.empty_like(q)
     if lse is None:
-        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=dev)
+    _need_buffer("o", o, q.shape, q.dtype, dev)
+    _need_buffer("lse", lse, (B, Hq), torch.float32, dev)
     wsize = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    st = lib().attn_decode_paged(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(block_table),
-                                 _ptr(seq_lens), _ptr(o), _ptr(lse), B, Hq, Hkv, d, num_pages,
-                                 page_size, max_pages, int(max_seq_len), float(scale),
-                                 int(num_splits), _ptr(workspace), wsize, _dtype_code(q),
-                                 _stream(stream))
+    with torch.cuda.device(dev):
+        st = lib().attn_decode_paged(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(block_table),
+                                     _ptr(seq_lens), _ptr(o), _ptr(lse), B, Hq, Hkv, d, num_pages,
+                                     page_size, max_pages, int(max_seq_len), float(scale),
+                                     int(num_splits), _ptr(workspace), wsize, _dtype_code(q),
+                                     _stream(stream, dev))
     _check("attn_decode_paged", st)
     return o, lse
 
@@ -364,20 +417,29 @@ def attn_bwd(q, k, v, o, lse, dout, causal: bool, scale: float | None = None, dq
         raise ValueError("o and dout must have q's shape")
     if tuple(lse.shape) != (B, Hq, Nq):
         raise ValueError("lse must be [B, Hq, Nq]")
-    for n, t in (("q", q), ("k", k), ("v", v), ("o", o), ("lse", lse), ("dout", dout)):
-        _need_cuda_contig(n, t)
+    if not (q.dtype == k.dtype == v.dtype == o.dtype == dout.dtype):
+        raise ValueError("q, k, v, o and dout must share a dtype")
+    dev = q.device
+    for n, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout)):
+        _need_cuda_contig(n, t, dev)
+    _need_buffer("lse", lse, (B, Hq, Nq), torch.float32, dev)
     if scale is None:
         scale = d ** -0.5
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
+    _need_buffer("dq", dq, q.shape, q.dtype, dev)
+    _need_buffer("dk", dk, k.shape, k.dtype, dev)
+    _need_buffer("dv", dv, v.shape, v.dtype, dev)
     wbytes = attn_bwd_workspace_bytes(B, Hq, Nq)
     if workspace is None:
-        workspace = torch.empty(max(16, wbytes), dtype=torch.uint8, device=q.device)
+        workspace = torch.empty(max(16, wbytes), dtype=torch.uint8, device=dev)
+    _need_workspace(workspace, dev)
     wsize = workspace.numel() * workspace.element_size()
-    st = lib().attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq),
-                        _ptr(dk), _ptr(dv), B, Hq, Hkv, Nq, Nk, d, int(bool(causal)),
-                        float(scale), _ptr(workspace), wsize, _dtype_code(q), _stream(stream))
+    with torch.cuda.device(dev):
+        st = lib().attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq),
+                            _ptr(dk), _ptr(dv), B, Hq, Hkv, Nq, Nk, d, int(bool(causal)),
+                            float(scale), _ptr(workspace), wsize, _dtype_code(q), _stream(stream, dev))
     _check("attn_bwd", st)
     return dq, dk, dv
 
@@ -388,13 +450,17 @@ def attn_quantize_fp8(x, codes=None, scales=None, stream=None):
     (codes [B, N, H, d] uint8, scales [B, H, ceil(N/128)] float32)."""
     import torch
     B, N, H, d = x.shape
-    _need_cuda_contig("x", x)
+    dev = x.device
+    _need_cuda_contig("x", x, dev)
     if x.dtype != torch.bfloat16:
         raise ValueError("x must be bfloat16")
-    codes = torch.empty(x.shape, dtype=torch.uint8, device=x.device) if codes is None else codes
+    codes = torch.empty(x.shape, dtype=torch.uint8, device=dev) if codes is None else codes
     nb = (N + 127) // 128
-    scales = torch.empty((B, H, nb), dtype=torch.float32, device=x.device) if scales is None else scales
-    st = lib().attn_quantize_fp8(_ptr(x), _ptr(codes), _ptr(scales), B, N, H, d, _stream(stream))
+    scales = torch.empty((B, H, nb), dtype=torch.float32, device=dev) if scales is None else scales
+    _need_buffer("codes", codes, x.shape, torch.uint8, dev)
+    _need_buffer("scales", scales, (B, H, nb), torch.float32, dev)
+    with torch.cuda.device(dev):
+        st = lib().attn_quantize_fp8(_ptr(x), _ptr(codes), _ptr(scales), B, N, H, d, _stream(stream, dev))
     _check("attn_quantize_fp8", st)
     return codes, scales
 
@@ -410,14 +476,20 @@ def attn_fwd_fp8(q8, k8, v, q_scales, k_scales, causal: bool, scale: float | Non
         raise ValueError("shape mismatch")
     if q8.dtype != torch.uint8 or k8.dtype != torch.uint8 or v.dtype != torch.bfloat16:
         raise ValueError("q8 and k8 must be uint8 e4m3 codes and v bfloat16")
-    for n, t in (("q8", q8), ("k8", k8), ("v", v), ("q_scales", q_scales), ("k_scales", k_scales)):
-        _need_cuda_contig(n, t)
+    dev = q8.device
+    for n, t in (("q8", q8), ("k8", k8), ("v", v)):
+        _need_cuda_contig(n, t, dev)
+    _need_buffer("q_scales", q_scales, (B, Hq, (Nq + 127) // 128), torch.float32, dev)
+    _need_buffer("k_scales", k_scales, (B, Hkv, (Nk + 127) // 128), torch.float32, dev)
     if scale is None:
         scale = d ** -0.5
-    o = torch.empty((B, Nq, Hq, d), dtype=torch.bfloat16, device=v.device) if o is None else o
-    lse = torch.empty((B, Hq, Nq), dtype=torch.float32, device=v.device) if lse is None else lse
-    st = lib().attn_fwd_fp8(_ptr(q8), _ptr(k8), _ptr(v), _ptr(q_scales), _ptr(k_scales), _ptr(o),
-                            _ptr(lse), B, Hq, Hkv, Nq, Nk, d, int(bool(causal)), float(scale),
-                            _stream(stream))
+    o = torch.empty((B, Nq, Hq, d), dtype=torch.bfloat16, device=dev) if o is None else o
+    lse = torch.empty((B, Hq, Nq), dtype=torch.float32, device=dev) if lse is None else lse
+    _need_buffer("o", o, (B, Nq, Hq, d), torch.bfloat16, dev)
+    _need_buffer("lse", lse, (B, Hq, Nq), torch.float32, dev)
+    with torch.cuda.device(dev):
+        st = lib().attn_fwd_fp8(_ptr(q8), _ptr(k8), _ptr(v), _ptr(q_scales), _ptr(k_scales), _ptr(o),
+                                _ptr(lse), B, Hq, Hkv, Nq, Nk, d, int(bool(causal)), float(scale),
+                                _stream(stream, dev))
     _check("attn_fwd_fp8", st)
     return o, lse
