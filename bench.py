@@ -58,7 +58,7 @@ DECODE = {
 NCU_TRAFFIC = {
     "training_prefill": {"bytes_per_launch": 586.9e6, "src_hash": "85de91f94a6afb87",
                          "profile": "profiles/fwd_tc_training_prefill.md"},
-    "decode_64k": {"bytes_per_launch": 275.0e6, "src_hash": "40e063a5d9c45647",
+    "decode_64k": {"bytes_per_launch": 274.4e6, "src_hash": "860ed8e79c5e0ccf",
                    "profile": "profiles/decode_split_64k.md"},
 }
 

@@ -568,7 +568,12 @@ namespace attn_host {
 // CTAs beyond one wave wait for the next, each CTA pays a fixed start-up
 // cost, and more than one segment adds the merge kernel.  The smallest
 // modelled time wins; ties go to fewer segments.
-int decode_auto_splits(int B, int Hq, int Hkv, int Nk, int d) {
+// Segment count that minimises a simple time model: waves of CTAs, each
+// streaming its segment at min(cta_bw, hbm / concurrent CTAs), plus a fixed
+// start-up per wave and the merge.  cta_bw is the rate one CTA sustains with
+// its ring full (measured: ~60 GB/s on a contiguous cache).  With
+// single_wave the count is capped so that all CTAs run in one wave.
+static int auto_splits_model(int B, int Hq, int Hkv, int Nk, int d, double cta_bw, bool single_wave) {
     if (B < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || Nk < 1 || (d != 64 && d != 128)) return -1;
     const int sms = device_sm_count();
     if (sms <= 0) return -1;
@@ -576,13 +581,17 @@ int decode_auto_splits(int B, int Hq, int Hkv, int Nk, int d) {
     const long long slots = (long long)sms * per_sm;
     const long long units = (long long)B * (Hq / group_cols(Hq / Hkv));
     const double hbm = 6.5e12;        // bytes/s the whole GPU streams
-    const double cta_bw = 6.0e10;     // bytes/s one CTA can keep in flight
     const double cta_fixed = 1.5e-6;  // start-up of one CTA wave
     const double merge_fixed = 3.0e-6;
     const double row_bytes = 2.0 * d * 2.0;  // one key's K and V for one head
     int best = 1;
     double best_t = 1e30;
-    const int max_s = std::min(Nk, 1024);
+    int max_s = std::min(Nk, 1024);
+    if (single_wave) {
+        // (paged) segments are whole 64-key tiles: more than Nk / 64 of them would be empty
+        max_s = std::min(max_s, (Nk + kTileKeys - 1) / kTileKeys);
+        max_s = (int)std::max(1LL, std::min((long long)max_s, slots / units));
+    }
     for (int S = 1; S <= max_s; ++S) {
         const long long ctas = units * S;
         const long long waves = (ctas + slots - 1) / slots;
@@ -597,6 +606,10 @@ int decode_auto_splits(int B, int Hq, int Hkv, int Nk, int d) {
         }
     }
     return best;
+}
+
+int decode_auto_splits(int B, int Hq, int Hkv, int Nk, int d) {
+    return auto_splits_model(B, Hq, Hkv, Nk, d, 6.0e10, false);
 }
 
 size_t decode_workspace_bytes(int B, int Hq, int d, int splits) {
@@ -659,7 +672,16 @@ bool paged_splits_fit(int max_seq_len, int page_size, int splits) {
 }
 
 int decode_paged_auto_splits(int B, int Hq, int Hkv, int max_seq_len, int d, int page_size) {
-    int S = decode_auto_splits(B, Hq, Hkv, max_seq_len, d);
+    // Pages of 64 or more keys stream like the contiguous cache.  Smaller
+    // pages split every tile into 64 / page_size boxes at random places, and
+    // one CTA sustains less (rates fitted to 64K and 16K keys, d = 128: ~33
+    // GB/s with 16-key pages, ~52 with 32-key pages), so more CTAs are needed
+    // to keep HBM busy; but a second
+    // wave of such CTAs costs more than it gains (B = 16 x 8K keys: one
+    // segment per sequence beats eight), so they are kept to one wave.
+    const bool small = page_size < 64;
+    const double cta_bw = !small ? 6.0e10 : page_size >= 32 ? 5.2e10 : 3.3e10;
+    int S = auto_splits_model(B, Hq, Hkv, max_seq_len, d, cta_bw, small);
     if (S < 1) return S;
     while (!paged_splits_fit(max_seq_len, page_size, S) && S < max_seq_len) ++S;
     return S;
