@@ -21,8 +21,8 @@ __all__ = [
     "attn_decode_splitkv", "attn_merge_lse", "attn_status_string",
     "attn_check_device_status", "attn_read_tile_counter", "attn_version",
     "attn_decode_splitkv_static", "attn_decode_paged", "attn_decode_paged_num_splits",
-    "attn_bwd", "attn_bwd_workspace_bytes", "attn_quantize_fp8", "attn_fwd_fp8",
-    "DECODE_STATIC_SCRATCH_BYTES", "EXPORTED_SYMBOLS",
+    "attn_bwd", "attn_bwd_workspace_bytes", "attn_quantize_fp8", "attn_quantize_fp8_rotated",
+    "attn_fwd_fp8", "DECODE_STATIC_SCRATCH_BYTES", "EXPORTED_SYMBOLS",
 ]
 
 ATTN_OK, ATTN_ERR_INVALID, ATTN_ERR_UNSUPPORTED, ATTN_ERR_CUDA, ATTN_ERR_TIMEOUT = range(5)
@@ -34,7 +34,8 @@ EXPORTED_SYMBOLS = (
     "attn_decode_splitkv", "attn_merge_lse", "attn_status_string",
     "attn_check_device_status", "attn_read_tile_counter", "attn_version",
     "attn_decode_splitkv_static", "attn_decode_paged", "attn_decode_paged_num_splits",
-    "attn_bwd", "attn_bwd_workspace_bytes", "attn_quantize_fp8", "attn_fwd_fp8",
+    "attn_bwd", "attn_bwd_workspace_bytes", "attn_quantize_fp8", "attn_quantize_fp8_rotated",
+    "attn_fwd_fp8",
 )
 
 # Size of the scratch area built into the library for attn_decode_splitkv_static.
@@ -106,6 +107,8 @@ def lib() -> ctypes.CDLL:
     L.attn_bwd.restype = I
     L.attn_quantize_fp8.argtypes = [P, P, P, I, I, I, I, P]
     L.attn_quantize_fp8.restype = I
+    L.attn_quantize_fp8_rotated.argtypes = [P, P, P, P, I, I, I, I, P]
+    L.attn_quantize_fp8_rotated.restype = I
     L.attn_fwd_fp8.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, P]
     L.attn_fwd_fp8.restype = I
     L.attn_decode_splitkv_static.restype = I
@@ -462,6 +465,32 @@ def attn_quantize_fp8(x, codes=None, scales=None, stream=None):
     with torch.cuda.device(dev):
         st = lib().attn_quantize_fp8(_ptr(x), _ptr(codes), _ptr(scales), B, N, H, d, _stream(stream, dev))
     _check("attn_quantize_fp8", st)
+    return codes, scales
+
+
+def attn_quantize_fp8_rotated(x, signs, codes=None, scales=None, stream=None):
+    """attn_quantize_fp8 of x R, R = diag(signs) H / sqrt(d) (H the Sylvester
+    Hadamard matrix): a random orthogonal transform that spreads outlier
+    features before quantisation.  signs: float32 [d] of +-1 on x's device,
+    the same for Q and K (then (qR)(kR)^T = qk^T and attn_fwd_fp8 takes the
+    result unchanged).  d is 64 or 128.  Returns (codes, scales) as
+    attn_quantize_fp8."""
+    import torch
+    B, N, H, d = x.shape
+    dev = x.device
+    _need_cuda_contig("x", x, dev)
+    if x.dtype != torch.bfloat16:
+        raise ValueError("x must be bfloat16")
+    _need_buffer("signs", signs, (d,), torch.float32, dev)
+    codes = torch.empty(x.shape, dtype=torch.uint8, device=dev) if codes is None else codes
+    nb = (N + 127) // 128
+    scales = torch.empty((B, H, nb), dtype=torch.float32, device=dev) if scales is None else scales
+    _need_buffer("codes", codes, x.shape, torch.uint8, dev)
+    _need_buffer("scales", scales, (B, H, nb), torch.float32, dev)
+    with torch.cuda.device(dev):
+        st = lib().attn_quantize_fp8_rotated(_ptr(x), _ptr(signs), _ptr(codes), _ptr(scales), B, N, H, d,
+                                             _stream(stream, dev))
+    _check("attn_quantize_fp8_rotated", st)
     return codes, scales
 
 

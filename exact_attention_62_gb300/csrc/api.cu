@@ -237,6 +237,18 @@ attn_status_t attn_quantize_fp8(const void* x, void* codes, float* scales, int B
     return attn_host::launch_quantize_fp8(x, codes, scales, B, N, H, d, static_cast<cudaStream_t>(stream));
 }
 
+attn_status_t attn_quantize_fp8_rotated(const void* x, const float* signs, void* codes, float* scales,
+                                        int B, int N, int H, int d, void* stream) {
+    if (B < 0 || N < 0 || H < 0 || d < 1) return ATTN_ERR_INVALID;
+    if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+    if (B == 0 || N == 0 || H == 0) return ATTN_OK;
+    if (x == nullptr || signs == nullptr || codes == nullptr || scales == nullptr) return ATTN_ERR_INVALID;
+    if (misaligned(x, 16) || misaligned(signs, 16) || misaligned(codes, 16) || misaligned(scales, 4))
+        return ATTN_ERR_INVALID;
+    return attn_host::launch_quantize_fp8_rotated(x, signs, codes, scales, B, N, H, d,
+                                                  static_cast<cudaStream_t>(stream));
+}
+
 attn_status_t attn_fwd_fp8(const void* q8, const void* k8, const void* v, const float* q_scales,
                            const float* k_scales, void* o, float* lse, int B, int Hq, int Hkv, int Nq,
                            int Nk, int d, int causal, float scale, void* stream) {

@@ -52,6 +52,8 @@ attn_status_t launch_decode_paged(const void* q, const void* k_pages, const void
 // ---- FP8 block quantisation (fp8.cu) and FP8 forward (fwd_tc.cu)
 attn_status_t launch_quantize_fp8(const void* x, void* codes, float* scales, int B, int N, int H, int d,
                                   cudaStream_t stream);
+attn_status_t launch_quantize_fp8_rotated(const void* x, const float* signs, void* codes, float* scales,
+                                          int B, int N, int H, int d, cudaStream_t stream);
 attn_status_t launch_fwd_fp8(const void* q8, const void* k8, const void* v, const float* q_scales,
                              const float* k_scales, void* o, float* lse, int B, int Hq, int Hkv,
                              int Nq, int Nk, int d, int causal, float scale, cudaStream_t stream);

@@ -1,6 +1,7 @@
 // fp8.cu -- block quantisation of bf16 [B, N, H, d] tensors to e4m3 for the
 // FP8 forward (the block quantisation of Lecture 11 - Kernel Optimization
-// Techniques, section 4.5, FP8 item).
+// Techniques, section 4.5, FP8 item), optionally after a random orthogonal
+// transform of each row (the same item's incoherent processing).
 //
 // One CTA per (row block of 128, head, batch): amax = max |x| over the
 // block's 128 rows x d columns; scale = amax / 448 and inv = 448 / amax in
@@ -9,6 +10,8 @@
 // is an IEEE-defined operation, so the codes are reproducible bit for bit.
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
+
+#include <cmath>
 
 #include "common.cuh"
 #include "ptx.cuh"
@@ -88,6 +91,96 @@ __global__ void __launch_bounds__(kQThreads)
     }
 }
 
+// Rotated variant ("incoherent processing"), d = 64 or 128: each row is
+// multiplied by diag(signs) and the d x d Sylvester Hadamard matrix before
+// the block quantisation.  A thread holds 8 consecutive elements of a row
+// (kC = D / 8 threads per row, consecutive lanes, so every load instruction
+// reads whole rows), the butterflies with h = 1, 2, 4 stay in registers and
+// h = 8 .. D/2 pair lane c with lane c ^ (h / 8) of the same row.  Every
+// butterfly is one fp32 add and one fp32 subtract, (a, b) -> (a + b, a - b),
+// taken stage by stage in increasing h, so the result is reproducible bit for
+// bit.  The block scale is multiplied by c_norm = 1 / sqrt(d) at the end,
+// which makes the transform orthogonal.  (Two threads per row, with only the
+// last stage across lanes, was measured slower: its loads no longer read
+// whole rows per instruction.)
+template <int D>
+__global__ void __launch_bounds__(kQThreads)
+    quantize_fp8_rot_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict__ signs,
+                            uint8_t* __restrict__ codes, float* __restrict__ scales, int N, int H,
+                            float c_norm) {
+    constexpr int kC = D / 8;                             // threads (16-byte chunks) per row
+    constexpr int kK = kBlockRows * kC / kQThreads;       // chunks per thread
+    static_assert(kBlockRows * kC % kQThreads == 0 && kQThreads % kC == 0 && 32 % kC == 0, "chunk split");
+    const int blk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int nb = gridDim.x;
+    const int r0 = blk * kBlockRows;
+    const int rows = min(kBlockRows, N - r0);
+    const int c = threadIdx.x % kC;  // the chunk of its rows this thread holds (the same for every k)
+    const float4 s0 = __ldg(reinterpret_cast<const float4*>(signs) + 2 * c);
+    const float4 s1 = __ldg(reinterpret_cast<const float4*>(signs) + 2 * c + 1);
+    const float sg[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+    float y[kK][8];
+    float amax = 0.f;
+#pragma unroll
+    for (int k = 0; k < kK; ++k) {
+        const int r = (threadIdx.x + k * kQThreads) / kC;
+        uint4 raw = make_uint4(0u, 0u, 0u, 0u);
+        if (r < rows)
+            raw = __ldg(reinterpret_cast<const uint4*>(x + (((long long)b * N + r0 + r) * H + h) * D) + c);
+        const __nv_bfloat162* e2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            const float2 f = __bfloat1622float2(e2[t]);
+            y[k][2 * t] = f.x * sg[2 * t];
+            y[k][2 * t + 1] = f.y * sg[2 * t + 1];
+        }
+#pragma unroll
+        for (int hh = 1; hh < 8; hh <<= 1) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                if ((e & hh) == 0) {
+                    const float a = y[k][e], bb = y[k][e + hh];
+                    y[k][e] = __fadd_rn(a, bb);
+                    y[k][e + hh] = __fsub_rn(a, bb);
+                }
+            }
+        }
+#pragma unroll
+        for (int m = 1; m < kC; m <<= 1) {
+            const bool upper = (c & m) != 0;  // this lane holds the b of each pair
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const float o = __shfl_xor_sync(0xffffffffu, y[k][e], m);
+                y[k][e] = upper ? __fsub_rn(o, y[k][e]) : __fadd_rn(y[k][e], o);
+            }
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(y[k][e]));
+    }
+    amax = block_max(amax);
+    const bool nz = amax > 0.f;
+    const float inv = nz ? kFp8Max / amax : 1.f;
+    if (threadIdx.x == 0)
+        scales[((long long)b * H + h) * nb + blk] = __fmul_rn(nz ? amax / kFp8Max : 1.f, c_norm);
+#pragma unroll
+    for (int k = 0; k < kK; ++k) {
+        const int r = (threadIdx.x + k * kQThreads) / kC;
+        if (r >= rows) continue;
+        uint32_t w[2];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            const float2 q2 = make_float2(__fmul_rn(y[k][2 * t], inv), __fmul_rn(y[k][2 * t + 1], inv));
+            const uint32_t q = __nv_cvt_float2_to_fp8x2(q2, __NV_SATFINITE, __NV_E4M3);
+            if (t & 1)
+                w[t >> 1] |= q << 16;
+            else
+                w[t >> 1] = q;
+        }
+        *reinterpret_cast<uint2*>(codes + (((long long)b * N + r0 + r) * H + h) * D + 8 * c) =
+            make_uint2(w[0], w[1]);
+    }
+}
+
 // Any even d: pairs of elements, two passes over the block.
 __global__ void __launch_bounds__(kQThreads)
     quantize_fp8_kernel(const __nv_bfloat16* __restrict__ x, uint8_t* __restrict__ codes,
@@ -136,6 +229,21 @@ attn_status_t launch_quantize_fp8(const void* x, void* codes, float* scales, int
         quantize_fp8_regs_kernel<64><<<grid, kQThreads, 0, stream>>>(xb, cb, scales, N, H);
     else
         quantize_fp8_kernel<<<grid, kQThreads, 0, stream>>>(xb, cb, scales, N, H, d);
+    return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+attn_status_t launch_quantize_fp8_rotated(const void* x, const float* signs, void* codes, float* scales,
+                                          int B, int N, int H, int d, cudaStream_t stream) {
+    const int nb = (N + kBlockRows - 1) / kBlockRows;
+    if (H > 65535 || B > 65535 || (d != 64 && d != 128)) return ATTN_ERR_UNSUPPORTED;
+    dim3 grid(nb, H, B);
+    const float c_norm = (float)(1.0 / std::sqrt((double)d));
+    const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
+    uint8_t* cb = static_cast<uint8_t*>(codes);
+    if (d == 128)
+        quantize_fp8_rot_kernel<128><<<grid, kQThreads, 0, stream>>>(xb, signs, cb, scales, N, H, c_norm);
+    else
+        quantize_fp8_rot_kernel<64><<<grid, kQThreads, 0, stream>>>(xb, signs, cb, scales, N, H, c_norm);
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

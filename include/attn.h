@@ -233,6 +233,30 @@ attn_status_t attn_quantize_fp8(const void* x, void* codes, float* scales, int B
                                 int d, void* stream);
 
 /*
+ * attn_quantize_fp8_rotated -- attn_quantize_fp8 after a random orthogonal
+ * transform of every row ("incoherent processing", [L11] 4.5, FP8 item, and
+ * the FP8 path of the FA3 section of the course index: multiplying by a
+ * random orthogonal matrix spreads outlier features over all d columns
+ * before quantisation).  The transform is R = diag(signs) H / sqrt(d), with H
+ * the d x d Sylvester Hadamard matrix (H H^T = d I), so R R^T = I and
+ * (q R)(k R)^T = q k^T: Q and K rotated with the same signs give the same
+ * scores, and attn_fwd_fp8 takes the codes and scales unchanged.
+ *   x      [B, N, H, d] bf16 input; d is 64 or 128.
+ *   signs  [d] float32 on the device, 16-byte aligned, each +1 or -1 (the
+ *          random draw; the caller supplies it and uses the same signs for
+ *          Q and K).
+ *   codes  [B, N, H, d] uint8 output;  scales [B, H, ceil(N/128)] float32.
+ * Arithmetic, all fp32 and reproducible bit for bit: y = signs * x, then
+ * the fast Walsh-Hadamard butterflies (a, b) -> (a + b, a - b) on index
+ * pairs (i, i + h) for h = 1, 2, 4, ..., d/2 in that order (y becomes y H);
+ * then the block quantisation of attn_quantize_fp8 on y; each block's scale
+ * is finally multiplied by c = float(1 / sqrt(d)) (rounded from double), so
+ * that code_value * scale ~= (x R).
+ */
+attn_status_t attn_quantize_fp8_rotated(const void* x, const float* signs, void* codes, float* scales,
+                                        int B, int N, int H, int d, void* stream);
+
+/*
  * attn_fwd_fp8 -- attn_fwd with Q and K block-quantised to e4m3 (as produced
  * by attn_quantize_fp8): S = scale * (q_code * q_scale) (k_code * k_scale)^T
  * is formed on the tensor cores from the e4m3 codes (fp32 accumulation) and

@@ -334,6 +334,43 @@ def quantize_fp8_blocks(x, block: int = 128):
     return codes.numpy(), scales.numpy()
 
 
+def hadamard_rotate(x, signs):
+    """x [..., d] (d a power of two) times diag(signs) and the d x d Sylvester
+    Hadamard matrix H (H_1 = [1], H_2n = [[H_n, H_n], [H_n, -H_n]]; H is
+    symmetric and H H^T = d I), in float32: y = signs * x, then for h = 1, 2,
+    4, ..., d/2 in that order every pair (i, i + h) inside a block of 2h
+    entries becomes (y_i + y_{i+h}, y_i - y_{i+h}).  This is the random
+    orthogonal transform of incoherent processing (Lecture 11, section 4.5,
+    FP8 item), unnormalised; the fixed stage order and float32 arithmetic
+    are the reading under which a quantised code is decided in the same
+    precision on both sides."""
+    y = np.asarray(_f32(x), np.float32) * np.asarray(signs, np.float32)
+    d = y.shape[-1]
+    if d & (d - 1):
+        raise ValueError("d must be a power of two")
+    lead = y.shape[:-1]
+    h = 1
+    while h < d:
+        z = y.reshape(lead + (d // (2 * h), 2, h))
+        a, b = z[..., 0, :], z[..., 1, :]
+        y = np.stack([a + b, a - b], axis=-2).reshape(lead + (d,))
+        h *= 2
+    return y
+
+
+def quantize_fp8_blocks_rotated(x, signs, block: int = 128):
+    """Incoherent processing before block quantisation (Lecture 11, section
+    4.5, FP8 item): the codes and scales of quantize_fp8_blocks applied to
+    hadamard_rotate(x, signs), each scale then multiplied in float32 by
+    c = float32(1 / sqrt(d)) so that codes * scales ~= x R with the orthogonal
+    R = diag(signs) H / sqrt(d).  Returns (codes, scales) like
+    quantize_fp8_blocks."""
+    y = hadamard_rotate(x, signs)
+    codes, scales = quantize_fp8_blocks(y, block)
+    c = np.float32(1.0 / np.sqrt(np.float64(y.shape[-1])))
+    return codes, (np.asarray(scales, np.float32) * c).astype(np.float32)
+
+
 def dequantize_fp8_blocks(codes, scales, block: int = 128):
     """codes uint8 [B, N, H, d] (e4m3) and scales [B, H, nblocks] -> float64."""
     import torch

@@ -177,6 +177,13 @@ def test_fp8_entry_points_reject_bad_arguments(L):
     assert L.attn_quantize_fp8(FAKE, FAKE, FAKE_LSE, 1, 8, 2, 7, None) == INVALID   # odd d
     assert L.attn_quantize_fp8(None, FAKE, FAKE_LSE, 1, 8, 2, 64, None) == INVALID
     assert L.attn_quantize_fp8(FAKE, FAKE, FAKE_LSE, 0, 8, 2, 64, None) == OK
+    rot = lambda x=FAKE, signs=FAKE_LSE, B=1, d=128: L.attn_quantize_fp8_rotated(
+        x, signs, FAKE, FAKE_LSE, B, 8, 2, d, None)
+    assert rot(d=96) == UNSUPPORTED          # the Hadamard transform needs d = 64 or 128
+    assert rot(d=0) == INVALID
+    assert rot(signs=None) == INVALID
+    assert rot(x=None) == INVALID
+    assert rot(B=0) == OK
     f8 = lambda d=128, causal=0, Hq=2, Hkv=1, B=1: L.attn_fwd_fp8(
         FAKE, FAKE, FAKE, FAKE_LSE, FAKE_LSE, FAKE, FAKE_LSE, B, Hq, Hkv, 8, 8, d, causal, 0.1, None)
     assert f8(d=64) == UNSUPPORTED

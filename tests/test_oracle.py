@@ -499,3 +499,79 @@ def test_score_perturbation_is_the_max_score_change(oracle_mod):
     d = oracle_mod.score_perturbation(q2, k, q, k, False, 0.25)
     assert np.all(d[0, 0] == 0) and np.all(d[0, 1, [0, 2, 3]] == 0)
     assert d[0, 1, 1] == pytest.approx(0.25 * 0.5 * np.abs(k[0, :, 0, 0]).max())
+
+
+# ---------------------------------------------------------------- incoherent processing
+def test_hadamard_rotation_worked_example(oracle_mod):
+    """d = 4 by hand: signs (1, -1, 1, 1) make y = (1, -2, 3, 4); with the
+    Sylvester matrix H_4 = [[1,1,1,1], [1,-1,1,-1], [1,1,-1,-1], [1,-1,-1,1]],
+    y H = (1-2+3+4, 1+2+3-4, 1-2-3-4, 1+2-3+4) = (6, 2, -8, 4)."""
+    got = oracle_mod.hadamard_rotate(np.array([[1.0, 2.0, 3.0, 4.0]]), np.array([1.0, -1.0, 1.0, 1.0]))
+    assert got.tolist() == [[6.0, 2.0, -8.0, 4.0]]
+
+
+@pytest.mark.parametrize("d", [2, 8, 64, 128])
+def test_hadamard_rotation_is_the_sylvester_matrix(oracle_mod, d):
+    """Rotating the identity with all signs +1 gives H itself: it matches the
+    Sylvester construction of scipy.linalg.hadamard, has entries +-1, and
+    H H^T = d I."""
+    scipy_linalg = pytest.importorskip("scipy.linalg")
+    H = oracle_mod.hadamard_rotate(np.eye(d), np.ones(d))
+    assert np.array_equal(H, scipy_linalg.hadamard(d).astype(np.float32))
+    assert np.array_equal(np.abs(H), np.ones((d, d), np.float32))
+    assert np.array_equal(H.astype(np.float64) @ H.T.astype(np.float64), d * np.eye(d))
+    # the signs multiply the rows of H (diag(s) H)
+    s = np.where(np.arange(d) % 3 == 0, -1.0, 1.0)
+    assert np.array_equal(oracle_mod.hadamard_rotate(np.eye(d), s), (s[:, None] * H).astype(np.float32))
+
+
+def test_hadamard_rotation_keeps_dot_products_and_spreads_outliers(oracle_mod):
+    rng = np.random.default_rng(6)
+    d = 128
+    s = rng.choice([-1.0, 1.0], size=d)
+    x = rng.standard_normal((5, d)).astype(np.float32)
+    y = rng.standard_normal((7, d)).astype(np.float32)
+    xr = oracle_mod.hadamard_rotate(x, s).astype(np.float64)
+    yr = oracle_mod.hadamard_rotate(y, s).astype(np.float64)
+    # (x R)(y R)^T = x y^T with R = diag(s) H / sqrt(d) orthogonal
+    exact = x.astype(np.float64) @ y.astype(np.float64).T
+    assert np.allclose(xr @ yr.T / d, exact, rtol=0, atol=1e-4)
+    # a single outlier feature is spread evenly over all d columns
+    one = np.zeros((1, d), np.float32)
+    one[0, 5] = 1000.0
+    assert np.array_equal(np.abs(oracle_mod.hadamard_rotate(one, s)), np.full((1, d), 1000.0, np.float32))
+
+
+def test_rotated_quantisation_dequantises_to_the_rotated_rows(oracle_mod):
+    """codes * scales of the rotated quantiser approximate x R (R orthogonal)
+    to e4m3 rounding, and the scale is the plain quantiser's scale of x H
+    times float32(1 / sqrt(d))."""
+    rng = np.random.default_rng(7)
+    d = 128
+    s = rng.choice([-1.0, 1.0], size=d).astype(np.float32)
+    x = rng.standard_normal((1, 200, 2, d)).astype(np.float32)
+    x[0, :, 0, 9] *= 40.0                       # an outlier feature
+    codes, scales = oracle_mod.quantize_fp8_blocks_rotated(x, s)
+    pc, ps = oracle_mod.quantize_fp8_blocks(oracle_mod.hadamard_rotate(x, s))
+    assert np.array_equal(codes, pc)
+    assert np.array_equal(scales, (ps * np.float32(1.0 / np.sqrt(128.0))).astype(np.float32))
+    xr = oracle_mod.hadamard_rotate(x, s).astype(np.float64) / np.sqrt(d)
+    deq = oracle_mod.dequantize_fp8_blocks(codes, scales)
+    for h in range(2):
+        for bi in range(2):
+            blk = xr[0, bi * 128:(bi + 1) * 128, h]
+            amax = np.abs(blk).max()
+            step = np.maximum(np.abs(blk) * 2.0 ** -4, 0.5 * 2.0 ** -9 * amax / 448.0)
+            assert np.all(np.abs(deq[0, bi * 128:(bi + 1) * 128, h] - blk) <= step * (1 + 1e-5))
+    # the outlier head: rotation lowers the largest relative error of a score
+    # q k^T against the plain quantiser (the reason for the transform)
+    k = rng.standard_normal((1, 200, 2, d)).astype(np.float32)
+    k[0, :, 0, 9] *= 40.0
+    kc, ks = oracle_mod.quantize_fp8_blocks_rotated(k, s)
+    qd = oracle_mod.dequantize_fp8_blocks(codes, scales)
+    kd = oracle_mod.dequantize_fp8_blocks(kc, ks)
+    qp, kp = (oracle_mod.dequantize_fp8_blocks(*oracle_mod.quantize_fp8_blocks(a)) for a in (x, k))
+    exact = np.einsum("nd,md->nm", x[0, :, 0].astype(np.float64), k[0, :, 0].astype(np.float64))
+    err_rot = np.abs(np.einsum("nd,md->nm", qd[0, :, 0], kd[0, :, 0]) - exact).mean()
+    err_plain = np.abs(np.einsum("nd,md->nm", qp[0, :, 0], kp[0, :, 0]) - exact).mean()
+    assert err_rot < err_plain
