@@ -17,7 +17,7 @@ import os
 
 __all__ = [
     "AttnError", "ATTN_BF16", "ATTN_F32", "lib", "ensure_built", "library_path",
-    "attn_fwd", "attn_decode_num_splits", "attn_decode_workspace_bytes",
+    "attn_fwd", "attn_fwd_host", "attn_decode_num_splits", "attn_decode_workspace_bytes",
     "attn_decode_splitkv", "attn_merge_lse", "attn_status_string",
     "attn_check_device_status", "attn_read_tile_counter", "attn_version",
     "attn_decode_splitkv_static", "attn_decode_paged", "attn_decode_paged_num_splits",
@@ -30,7 +30,7 @@ ATTN_BF16, ATTN_F32 = 0, 1
 
 # Every symbol include/attn.h declares.
 EXPORTED_SYMBOLS = (
-    "attn_fwd", "attn_decode_num_splits", "attn_decode_workspace_bytes",
+    "attn_fwd", "attn_fwd_host", "attn_decode_num_splits", "attn_decode_workspace_bytes",
     "attn_decode_splitkv", "attn_merge_lse", "attn_status_string",
     "attn_check_device_status", "attn_read_tile_counter", "attn_version",
     "attn_decode_splitkv_static", "attn_decode_paged", "attn_decode_paged_num_splits",
@@ -80,6 +80,8 @@ def lib() -> ctypes.CDLL:
     LL, SZ = ctypes.c_longlong, ctypes.c_size_t
     L.attn_fwd.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, F, I, P]
     L.attn_fwd.restype = I
+    L.attn_fwd_host.argtypes = [P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, I, I, P, P, P]
+    L.attn_fwd_host.restype = I
     L.attn_decode_num_splits.argtypes = [I, I, I, I, I]
     L.attn_decode_num_splits.restype = I
     L.attn_decode_workspace_bytes.argtypes = [I, I, I, I, I, I]
@@ -202,6 +204,59 @@ def attn_fwd(q, k, v, causal: bool = False, scale: float | None = None, o=None, 
         st = lib().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Nq, Nk, d,
                             int(bool(causal)), float(scale), _dtype_code(q), _stream(stream, dev))
     _check("attn_fwd", st)
+    return o, lse
+
+
+def attn_fwd_host(q, k, v, causal: bool = False, scale: float | None = None, o=None, lse=None,
+                  device_buffers=None, chunks: int = 0, stream=None, h2d_stream=None, d2h_stream=None):
+    """attn_fwd on CPU tensors (page-locked for asynchronous copies): the batch
+    is copied in, computed and copied back in chunks on three streams so the
+    transfers overlap the computation.  Returns (o, lse) CPU tensors (pinned
+    when allocated here); they hold the results once `stream` (default: the
+    current stream) has completed.  device_buffers = (q_d, k_d, v_d, o_d,
+    lse_d) reuses device memory across calls; h2d_stream / d2h_stream default
+    to two streams created here (pass the same stream as `stream` for no
+    overlap)."""
+    import torch
+    B, Nq, Hq, d = q.shape
+    Bk, Nk, Hkv, dk = k.shape
+    if Bk != B or dk != d or tuple(v.shape) != tuple(k.shape):
+        raise ValueError("shape mismatch: q %s k %s v %s" % (tuple(q.shape), tuple(k.shape), tuple(v.shape)))
+    if not (q.dtype == k.dtype == v.dtype):
+        raise ValueError("q, k, v must share a dtype")
+    for n, t in (("q", q), ("k", k), ("v", v)):
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError("%s must be a contiguous CPU tensor" % n)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    if scale is None:
+        scale = d ** -0.5
+    if o is None:
+        o = torch.empty(q.shape, dtype=q.dtype, pin_memory=True)
+    if lse is None:
+        lse = torch.empty((B, Hq, Nq), dtype=torch.float32, pin_memory=True)
+    for n, t, shape, dt in (("o", o, q.shape, q.dtype), ("lse", lse, (B, Hq, Nq), torch.float32)):
+        if t.is_cuda or not t.is_contiguous() or tuple(t.shape) != tuple(shape) or t.dtype != dt:
+            raise ValueError("%s must be a contiguous CPU %s tensor of shape %s" % (n, dt, tuple(shape)))
+    if device_buffers is None:
+        device_buffers = (torch.empty(q.shape, dtype=q.dtype, device=dev),
+                          torch.empty(k.shape, dtype=k.dtype, device=dev),
+                          torch.empty(v.shape, dtype=v.dtype, device=dev),
+                          torch.empty(q.shape, dtype=q.dtype, device=dev),
+                          torch.empty((B, Hq, Nq), dtype=torch.float32, device=dev))
+    q_d, k_d, v_d, o_d, lse_d = device_buffers
+    for n, t, ref in (("q_d", q_d, q), ("k_d", k_d, k), ("v_d", v_d, v), ("o_d", o_d, q)):
+        _need_buffer(n, t, ref.shape, ref.dtype, dev)
+    _need_buffer("lse_d", lse_d, (B, Hq, Nq), torch.float32, dev)
+    if h2d_stream is None:
+        h2d_stream = torch.cuda.Stream(dev)
+    if d2h_stream is None:
+        d2h_stream = torch.cuda.Stream(dev)
+    with torch.cuda.device(dev):
+        st = lib().attn_fwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(q_d), _ptr(k_d),
+                                 _ptr(v_d), _ptr(o_d), _ptr(lse_d), B, Hq, Hkv, Nq, Nk, d,
+                                 int(bool(causal)), float(scale), _dtype_code(q), int(chunks),
+                                 _stream(stream, dev), _stream(h2d_stream, dev), _stream(d2h_stream, dev))
+    _check("attn_fwd_host", st)
     return o, lse
 
 

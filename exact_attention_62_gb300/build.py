@@ -20,7 +20,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libattn.so")
 INCLUDE = os.path.join(ROOT, "include")
 SOURCES = ["api.cu", "fwd_tc.cu", "fwd_f32.cu", "decode.cu", "decode_static.cu", "bwd_tc.cu",
-           "fp8.cu"]
+           "fp8.cu", "host_pipeline.cu"]
 HEADERS = [os.path.join(CSRC, "ptx.cuh"), os.path.join(CSRC, "common.cuh"),
            os.path.join(INCLUDE, "attn.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

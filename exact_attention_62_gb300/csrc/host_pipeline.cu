@@ -1,0 +1,148 @@
+// host_pipeline.cu -- attn_fwd on host buffers, with the transfers overlapped
+// with the computation (the C entry point attn_fwd_host).
+//
+// The batch is cut into chunks of whole sequences.  Chunk c's inputs go
+// host -> device on the h2d stream, its forward runs on the compute stream
+// once they have arrived, and its outputs go device -> host on the d2h
+// stream once the forward is done; so the copy of chunk c + 1 and the read
+// back of chunk c - 1 proceed while chunk c computes.  Sequences are
+// independent in the forward, so every output element is the one a single
+// attn_fwd call over the whole batch writes, bit for bit.
+#include <cuda_runtime.h>
+
+#include <cmath>
+
+#include "attn.h"
+
+namespace {
+
+constexpr int kMaxChunks = 16;
+constexpr int kEvents = 2 * kMaxChunks + 2;
+
+// Events the pipeline records between its streams: created once per host
+// thread and device, reused by every call (a recorded event may be recorded
+// again once the waits on it have been enqueued).
+struct EventPool {
+    cudaEvent_t ev[kEvents];
+    int device = -1;
+    bool ready = false;
+    void release() {
+        if (!ready) return;
+        for (int i = 0; i < kEvents; ++i) cudaEventDestroy(ev[i]);
+        ready = false;
+    }
+    bool get(int dev) {
+        if (ready && device == dev) return true;
+        release();
+        for (int i = 0; i < kEvents; ++i) {
+            if (cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming) != cudaSuccess) {
+                for (int k = 0; k < i; ++k) cudaEventDestroy(ev[k]);
+                return false;
+            }
+        }
+        device = dev;
+        ready = true;
+        return true;
+    }
+    // (no destructor: the events live until the process ends, so nothing
+    // calls into the CUDA runtime during its own teardown)
+};
+thread_local EventPool t_events;
+
+bool misaligned16(const void* p) { return (reinterpret_cast<unsigned long long>(p) & 15ull) != 0; }
+
+}  // namespace
+
+extern "C" attn_status_t attn_fwd_host(const void* q_h, const void* k_h, const void* v_h, void* o_h,
+                                       float* lse_h, void* q_d, void* k_d, void* v_d, void* o_d,
+                                       float* lse_d, int B, int Hq, int Hkv, int Nq, int Nk, int d,
+                                       int causal, float scale, attn_dtype_t dtype, int chunks,
+                                       void* stream, void* h2d_stream, void* d2h_stream) {
+    if (B < 0 || Hq < 0 || Nq < 0 || Nk < 0 || Hkv < 1 || d < 1 || chunks < 0) return ATTN_ERR_INVALID;
+    if (causal != 0 && causal != 1) return ATTN_ERR_INVALID;
+    if (dtype != ATTN_BF16 && dtype != ATTN_F32) return ATTN_ERR_INVALID;
+    if (Hq % Hkv != 0) return ATTN_ERR_INVALID;
+    if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_ERR_INVALID;  // as attn_fwd
+    if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+    if (B > 65535) return ATTN_ERR_UNSUPPORTED;
+    if (B == 0 || Hq == 0 || Nq == 0) return ATTN_OK;
+    if (q_h == nullptr || o_h == nullptr || lse_h == nullptr || q_d == nullptr || o_d == nullptr ||
+        lse_d == nullptr)
+        return ATTN_ERR_INVALID;
+    if (Nk > 0 && (k_h == nullptr || v_h == nullptr || k_d == nullptr || v_d == nullptr))
+        return ATTN_ERR_INVALID;
+    if (misaligned16(q_d) || misaligned16(o_d) || (Nk > 0 && (misaligned16(k_d) || misaligned16(v_d))) ||
+        (reinterpret_cast<unsigned long long>(lse_d) & 3ull) != 0)
+        return ATTN_ERR_INVALID;
+    int n = chunks == 0 ? (B < 4 ? B : 4) : chunks;
+    if (n > B) n = B;
+    if (n > kMaxChunks) return ATTN_ERR_UNSUPPORTED;
+
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || !t_events.get(dev)) return ATTN_ERR_CUDA;
+    cudaEvent_t* ev = t_events.ev;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaStream_t up = h2d_stream ? static_cast<cudaStream_t>(h2d_stream) : st;
+    cudaStream_t down = d2h_stream ? static_cast<cudaStream_t>(d2h_stream) : st;
+
+    const size_t esz = dtype == ATTN_BF16 ? 2 : 4;
+    const size_t q_seq = (size_t)Nq * Hq * d * esz;    // bytes of one sequence's q (and o)
+    const size_t kv_seq = (size_t)Nk * Hkv * d * esz;  // ... of its k (and v)
+    const size_t l_seq = (size_t)Hq * Nq * sizeof(float);
+    const char* qh = static_cast<const char*>(q_h);
+    const char* kh = static_cast<const char*>(k_h);
+    const char* vh = static_cast<const char*>(v_h);
+    char* oh = static_cast<char*>(o_h);
+    char* lh = reinterpret_cast<char*>(lse_h);
+    char* qd = static_cast<char*>(q_d);
+    char* kd = static_cast<char*>(k_d);
+    char* vd = static_cast<char*>(v_d);
+    char* od = static_cast<char*>(o_d);
+    char* ld = reinterpret_cast<char*>(lse_d);
+
+    // the side streams start after the work already queued on the compute stream
+    cudaEvent_t ev_start = ev[2 * kMaxChunks], ev_done = ev[2 * kMaxChunks + 1];
+    if (cudaEventRecord(ev_start, st) != cudaSuccess) return ATTN_ERR_CUDA;
+    if (up != st && cudaStreamWaitEvent(up, ev_start, 0) != cudaSuccess) return ATTN_ERR_CUDA;
+    if (down != st && cudaStreamWaitEvent(down, ev_start, 0) != cudaSuccess) return ATTN_ERR_CUDA;
+
+    for (int c = 0; c < n; ++c) {
+        const int b0 = (int)((long long)B * c / n), b1 = (int)((long long)B * (c + 1) / n);
+        const int nb = b1 - b0;
+        if (cudaMemcpyAsync(qd + b0 * q_seq, qh + b0 * q_seq, nb * q_seq, cudaMemcpyHostToDevice, up) !=
+            cudaSuccess)
+            return ATTN_ERR_CUDA;
+        if (Nk > 0) {
+            if (cudaMemcpyAsync(kd + b0 * kv_seq, kh + b0 * kv_seq, nb * kv_seq, cudaMemcpyHostToDevice, up) !=
+                    cudaSuccess ||
+                cudaMemcpyAsync(vd + b0 * kv_seq, vh + b0 * kv_seq, nb * kv_seq, cudaMemcpyHostToDevice, up) !=
+                    cudaSuccess)
+                return ATTN_ERR_CUDA;
+        }
+        cudaEvent_t ev_in = ev[2 * c], ev_out = ev[2 * c + 1];
+        if (up != st) {
+            if (cudaEventRecord(ev_in, up) != cudaSuccess || cudaStreamWaitEvent(st, ev_in, 0) != cudaSuccess)
+                return ATTN_ERR_CUDA;
+        }
+        const attn_status_t s = attn_fwd(qd + b0 * q_seq, Nk > 0 ? kd + b0 * kv_seq : nullptr,
+                                         Nk > 0 ? vd + b0 * kv_seq : nullptr, od + b0 * q_seq,
+                                         reinterpret_cast<float*>(ld + b0 * l_seq), nb, Hq, Hkv, Nq, Nk, d,
+                                         causal, scale, dtype, st);
+        if (s != ATTN_OK) return s;
+        if (down != st) {
+            if (cudaEventRecord(ev_out, st) != cudaSuccess || cudaStreamWaitEvent(down, ev_out, 0) != cudaSuccess)
+                return ATTN_ERR_CUDA;
+        }
+        if (cudaMemcpyAsync(oh + b0 * q_seq, od + b0 * q_seq, nb * q_seq, cudaMemcpyDeviceToHost, down) !=
+                cudaSuccess ||
+            cudaMemcpyAsync(lh + b0 * l_seq, ld + b0 * l_seq, nb * l_seq, cudaMemcpyDeviceToHost, down) !=
+                cudaSuccess)
+            return ATTN_ERR_CUDA;
+    }
+    // the compute stream completes after the last read back
+    if (down != st) {
+        if (cudaEventRecord(ev_done, down) != cudaSuccess || cudaStreamWaitEvent(st, ev_done, 0) != cudaSuccess)
+            return ATTN_ERR_CUDA;
+    }
+    return ATTN_OK;
+}

@@ -80,6 +80,36 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o,
                        void* stream);
 
 /*
+ * attn_fwd_host -- attn_fwd with the inputs and outputs in host memory; the
+ * transfers overlap the computation.  The pages define no such call; it is
+ * the library's end-to-end entry point.
+ *   q_h, k_h, v_h, o_h, lse_h  host buffers with the layouts of attn_fwd
+ *            (page-locked memory lets the copies run asynchronously; any
+ *            host memory is accepted).
+ *   q_d, k_d, v_d, o_d, lse_d  device buffers of the same full sizes,
+ *            caller-owned, aligned as for attn_fwd.
+ *   chunks   0 = min(B, 4); else the number of batch chunks, 1..16 (at most
+ *            B).  Chunk c holds sequences [B c / n, B (c + 1) / n).
+ *   stream   the compute stream; h2d_stream and d2h_stream carry the two
+ *            copy directions (NULL: the compute stream, i.e. no overlap).
+ * Chunk c is copied host -> device on h2d_stream, computed by attn_fwd on
+ * `stream` once it has arrived, and copied back on d2h_stream once
+ * computed, so chunk c + 1 moves in while chunk c computes.  The side
+ * streams first wait for the work already queued on `stream`, and `stream`
+ * finally waits for the last read back: once `stream` has completed, o_h and
+ * lse_h hold the results, equal bit for bit to one attn_fwd call over the
+ * whole batch.  Errors as attn_fwd, checked before anything is queued (a
+ * CUDA failure later returns ATTN_ERR_CUDA with part of the work queued).
+ * The library keeps a few CUDA events per host thread for this call.
+ */
+attn_status_t attn_fwd_host(const void* q_h, const void* k_h, const void* v_h,
+                            void* o_h, float* lse_h, void* q_d, void* k_d,
+                            void* v_d, void* o_d, float* lse_d, int B, int Hq,
+                            int Hkv, int Nq, int Nk, int d, int causal,
+                            float scale, attn_dtype_t dtype, int chunks,
+                            void* stream, void* h2d_stream, void* d2h_stream);
+
+/*
  * attn_decode_num_splits -- the number of key segments attn_decode_splitkv
  * uses when called with num_splits = 0.  It follows the CTA-by-wave model of
  * [L11] 6.3-6.4: too few segments leave SMs idle, too many add waves and

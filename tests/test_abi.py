@@ -173,6 +173,22 @@ def test_bwd_rejects_bad_arguments(L):
     assert pkg.attn_bwd_workspace_bytes(2, 3, 100) == (2 * 3 * 100 * 4 + 255) // 256 * 256
 
 
+def test_fwd_host_rejects_bad_arguments(L):
+    H = ctypes.c_void_p(0x10000)   # host pointers are never touched either
+    def host(B=2, d=64, chunks=0, q_h=H, q_d=FAKE, scale=0.125, causal=0):
+        return L.attn_fwd_host(q_h, H, H, H, H, q_d, FAKE, FAKE, FAKE, FAKE_LSE, B, 2, 1, 8, 8, d, causal,
+                               scale, BF16, chunks, None, None, None)
+    assert host(d=96) == UNSUPPORTED
+    assert host(q_h=None) == INVALID
+    assert host(q_d=None) == INVALID
+    assert host(q_d=ctypes.c_void_p(0x7f0000000008)) == INVALID   # device buffer not 16-byte aligned
+    assert host(scale=float("inf")) == INVALID
+    assert host(causal=2) == INVALID
+    assert host(chunks=-1) == INVALID
+    assert host(B=20, chunks=17) == UNSUPPORTED   # at most 16 chunks
+    assert host(B=0) == OK
+
+
 def test_fp8_entry_points_reject_bad_arguments(L):
     assert L.attn_quantize_fp8(FAKE, FAKE, FAKE_LSE, 1, 8, 2, 7, None) == INVALID   # odd d
     assert L.attn_quantize_fp8(None, FAKE, FAKE_LSE, 1, 8, 2, 64, None) == INVALID
