@@ -504,6 +504,79 @@ __global__ void __launch_bounds__(kMergeThreads)
     if (tid == 0 && lse != nullptr) lse[row] = Lr;
 }
 
+// The same merge in one pass for few segments (at most kShortSeg per
+// thread): every thread issues the loads of its segments' LSE and partial
+// outputs at once, so the merge costs one round trip to L2 instead of two;
+// o = sum_s e^{lse_s - M} o_s / sum_s e^{lse_s - M} and lse = M + ln of that
+// sum (M = max_s lse_s), the same value as merge_lse_kernel up to rounding.
+constexpr int kShortSeg = 4;
+
+template <bool OUT_BF16>
+__global__ void __launch_bounds__(kMergeThreads)
+    merge_lse_short_kernel(const float* __restrict__ o_parts, const float* __restrict__ lse_parts, int P,
+                           long long rows, int d, void* __restrict__ o, float* __restrict__ lse) {
+    __shared__ float red[kMergeThreads / 32];
+    __shared__ float4 part[kMergeThreads];
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const long long row = blockIdx.x;
+    const int tid = threadIdx.x;
+    const int C = d >> 2;              // 4-column groups, 1..128
+    const int SL = kMergeThreads / C;  // segment lanes, >= 2
+    const int c4 = tid % C, sl = tid / C;
+    float ls[kShortSeg];
+    float4 x[kShortSeg];
+    float M = -INFINITY;
+#pragma unroll
+    for (int r = 0; r < kShortSeg; ++r) {
+        const int s = sl + r * SL;
+        const bool ok = sl < SL && s < P;
+        ls[r] = ok ? lse_parts[(long long)s * rows + row] : -INFINITY;
+        x[r] = ok ? *reinterpret_cast<const float4*>(o_parts + ((long long)s * rows + row) * d + 4 * c4)
+                  : make_float4(0.f, 0.f, 0.f, 0.f);
+        M = fmaxf(M, ls[r]);
+    }
+    M = block_reduce(M, true, red);
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+    float lsum = 0.f;
+    if (M != -INFINITY) {  // uniform across the CTA
+#pragma unroll
+        for (int r = 0; r < kShortSeg; ++r) {
+            if (ls[r] == -INFINITY) continue;
+            const float w = expf(ls[r] - M);
+            a.x = fmaf(w, x[r].x, a.x);
+            a.y = fmaf(w, x[r].y, a.y);
+            a.z = fmaf(w, x[r].z, a.z);
+            a.w = fmaf(w, x[r].w, a.w);
+            if (c4 == 0) lsum += w;  // each segment counted once
+        }
+    }
+    part[tid] = a;
+    lsum = block_reduce(lsum, false, red);  // its barriers also publish part[]
+    if (tid < C) {
+        for (int j = 1; j < SL; ++j) {
+            const float4 y = part[j * C + tid];
+            a.x += y.x;
+            a.y += y.y;
+            a.z += y.z;
+            a.w += y.w;
+        }
+        const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+        a.x *= inv;
+        a.y *= inv;
+        a.z *= inv;
+        a.w *= inv;
+        if constexpr (OUT_BF16) {
+            uint2 h;
+            h.x = pack_bf16(a.x, a.y);
+            h.y = pack_bf16(a.z, a.w);
+            *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(o) + row * d + 4 * tid) = h;
+        } else {
+            *reinterpret_cast<float4*>(static_cast<float*>(o) + row * d + 4 * tid) = a;
+        }
+    }
+    if (tid == 0 && lse != nullptr) lse[row] = lsum > 0.f ? M + logf(lsum) : -INFINITY;
+}
+
 int group_cols(int G) {
     if (G % 8 == 0) return 8;
     if (G % 4 == 0) return 4;
@@ -747,9 +820,15 @@ attn_status_t launch_merge(const float* o_parts, const float* lse_parts, int par
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    const cudaError_t e =
-        out_bf16 ? cudaLaunchKernelEx(&cfg, merge_lse_kernel<true>, o_parts, lse_parts, parts, rows, d, o, lse)
-                 : cudaLaunchKernelEx(&cfg, merge_lse_kernel<false>, o_parts, lse_parts, parts, rows, d, o, lse);
+    const bool short_merge = parts <= kShortSeg * (kMergeThreads / (d / 4));
+    cudaError_t e;
+    if (short_merge)
+        e = out_bf16 ? cudaLaunchKernelEx(&cfg, merge_lse_short_kernel<true>, o_parts, lse_parts, parts, rows, d, o, lse)
+                     : cudaLaunchKernelEx(&cfg, merge_lse_short_kernel<false>, o_parts, lse_parts, parts, rows, d, o,
+                                          lse);
+    else
+        e = out_bf16 ? cudaLaunchKernelEx(&cfg, merge_lse_kernel<true>, o_parts, lse_parts, parts, rows, d, o, lse)
+                     : cudaLaunchKernelEx(&cfg, merge_lse_kernel<false>, o_parts, lse_parts, parts, rows, d, o, lse);
     return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
