@@ -452,6 +452,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto bar = [&](int i) -> uint32_t { return sbase + L::kOffBar + 8u * (uint32_t)i; };
     volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(sgen + L::kOffMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sgen + L::kOffMisc + 4);
+    // The dQ kernel, launched next as a programmatic dependent, reads nothing
+    // this kernel writes: let its CTAs take the SMs this grid's last wave frees.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     // key tile, longest first (causal: the first key tiles are seen by the most rows)
     const int n_kt = (p.Nk + kT - 1) / kT;
@@ -788,8 +791,22 @@ attn_status_t launch_bwd_impl(const void* q, const void* k, const void* v, const
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
     bwd_dkdv_kernel<D><<<(unsigned)dkv_blocks, kThreads, L::kSmem, stream>>>(mq, mdo, mk, mv, prm);
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
-    bwd_dq_kernel<D><<<(unsigned)dq_blocks, kThreads, LQ::kSmem, stream>>>(mq, mdo, mk, mv, prm);
-    return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+    // dQ depends only on the row sums of bwd_dot_kernel, complete before the
+    // dK/dV grid started; as a programmatic dependent of that grid it fills
+    // the SMs of its last wave instead of waiting for all of it.  Work queued
+    // after this call still waits for both grids.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)dq_blocks);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = LQ::kSmem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, bwd_dq_kernel<D>, mq, mdo, mk, mv, prm) == cudaSuccess ? ATTN_OK
+                                                                                      : ATTN_ERR_CUDA;
 }
 
 }  // namespace
