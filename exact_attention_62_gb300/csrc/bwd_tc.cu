@@ -37,6 +37,9 @@
 //  * This pays 7 matrix products per (query tile, key tile) pair instead of
 //    the 5 of a kernel that owns all three accumulators, in exchange for no
 //    dQ atomics and one accumulator owner per output.
+//  * Launch order: rowsum, dK/dV, then dQ as a programmatic dependent of the
+//    dK/dV grid (dQ reads nothing that grid writes), so the dQ CTAs start on
+//    the SMs the dK/dV grid's last wave frees.
 #include <cmath>
 #include <mutex>
 

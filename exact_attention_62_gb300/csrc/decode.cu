@@ -27,7 +27,9 @@
 //    the instruction count far below the memory time.
 //  * At the end the eight warps' states are merged through shared memory
 //    (the same (m, l, acc) merge).  With a single segment the kernel writes
-//    O (bf16) and LSE directly and no merge kernel runs.
+//    O (bf16) and LSE directly and no merge kernel runs; otherwise the merge
+//    kernel is launched as a programmatic dependent (one pass over the
+//    partials for up to 4 segments per thread, two passes beyond).
 #include <algorithm>
 #include <cmath>
 #include <mutex>
