@@ -60,7 +60,7 @@ DECODE = {
 NCU_TRAFFIC = {
     "training_prefill": {"bytes_per_launch": 586.9e6, "src_hash": "85de91f94a6afb87",
                          "profile": "profiles/fwd_tc_training_prefill.md"},
-    "decode_64k": {"bytes_per_launch": 274.0e6, "src_hash": "a9673e613202f2b4",
+    "decode_64k": {"bytes_per_launch": 272.0e6, "src_hash": "b06bdc5bcf952bd3",
                    "profile": "profiles/decode_split_64k.md"},
 }
 

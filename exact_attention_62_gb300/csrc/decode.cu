@@ -645,19 +645,28 @@ namespace attn_host {
 // modelled time wins; ties go to fewer segments.
 // Segment count that minimises a simple time model: waves of CTAs, each
 // streaming its segment at min(cta_bw, hbm / concurrent CTAs), plus a fixed
-// start-up per wave and the merge.  cta_bw is the rate one CTA sustains with
-// its ring full (measured: ~60 GB/s on a contiguous cache).  With
-// single_wave the count is capped so that all CTAs run in one wave.
-static int auto_splits_model(int B, int Hq, int Hkv, int Nk, int d, double cta_bw, bool single_wave) {
+// start-up per wave and the merge.  With single_wave the count is capped so
+// that all CTAs run in one wave.
+struct SplitModel {
+    double cta_bw;       // bytes/s one CTA streams with its ring full
+    double hbm;          // bytes/s the whole GPU streams
+    double cta_fixed;    // start-up of one CTA wave
+    double merge_fixed;  // the merge launch
+};
+// Contiguous cache: fitted on GB300 to the measured best segment counts of
+// B = 1 x 2K-64K, B = 4 x 4K and 16K, B = 8 x 8K, B = 16 x 8K and B = 32 x 2K
+// keys (Hq = 32, Hkv = 8, d = 128); a CTA streams ~80-110 GB/s while few
+// compete, so batches of several sequences need few segments or none.
+constexpr SplitModel kDenseSplitModel = {8.0e10, 5.5e12, 0.5e-6, 4.0e-6};
+
+static int auto_splits_model(int B, int Hq, int Hkv, int Nk, int d, const SplitModel& m, bool single_wave) {
     if (B < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || Nk < 1 || (d != 64 && d != 128)) return -1;
     const int sms = device_sm_count();
     if (sms <= 0) return -1;
     const int per_sm = d == 128 ? ctas_per_sm<128>() : ctas_per_sm<64>();
     const long long slots = (long long)sms * per_sm;
     const long long units = (long long)B * (Hq / group_cols(Hq / Hkv));
-    const double hbm = 6.5e12;        // bytes/s the whole GPU streams
-    const double cta_fixed = 1.5e-6;  // start-up of one CTA wave
-    const double merge_fixed = 3.0e-6;
+    const double cta_bw = m.cta_bw, hbm = m.hbm, cta_fixed = m.cta_fixed, merge_fixed = m.merge_fixed;
     const double row_bytes = 2.0 * d * 2.0;  // one key's K and V for one head
     int best = 1;
     double best_t = 1e30;
@@ -684,7 +693,7 @@ static int auto_splits_model(int B, int Hq, int Hkv, int Nk, int d, double cta_b
 }
 
 int decode_auto_splits(int B, int Hq, int Hkv, int Nk, int d) {
-    return auto_splits_model(B, Hq, Hkv, Nk, d, 6.0e10, false);
+    return auto_splits_model(B, Hq, Hkv, Nk, d, kDenseSplitModel, false);
 }
 
 size_t decode_workspace_bytes(int B, int Hq, int d, int splits) {
@@ -756,7 +765,7 @@ int decode_paged_auto_splits(int B, int Hq, int Hkv, int max_seq_len, int d, int
     // segment per sequence beats eight), so they are kept to one wave.
     const bool small = page_size < 64;
     const double cta_bw = !small ? 6.0e10 : page_size >= 32 ? 5.2e10 : 3.3e10;
-    int S = auto_splits_model(B, Hq, Hkv, max_seq_len, d, cta_bw, small);
+    int S = auto_splits_model(B, Hq, Hkv, max_seq_len, d, SplitModel{cta_bw, 6.5e12, 1.5e-6, 3.0e-6}, small);
     if (S < 1) return S;
     while (!paged_splits_fit(max_seq_len, page_size, S) && S < max_seq_len) ++S;
     return S;
