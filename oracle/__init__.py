@@ -334,41 +334,55 @@ def quantize_fp8_blocks(x, block: int = 128):
     return codes.numpy(), scales.numpy()
 
 
-def hadamard_rotate(x, signs):
-    """x [..., d] (d a power of two) times diag(signs) and the d x d Sylvester
-    Hadamard matrix H (H_1 = [1], H_2n = [[H_n, H_n], [H_n, -H_n]]; H is
-    symmetric and H H^T = d I), in float32: y = signs * x, then for h = 1, 2,
-    4, ..., d/2 in that order every pair (i, i + h) inside a block of 2h
-    entries becomes (y_i + y_{i+h}, y_i - y_{i+h}).  This is the random
-    orthogonal transform of incoherent processing (Lecture 11, section 4.5,
-    FP8 item), unnormalised; the fixed stage order and float32 arithmetic
-    are the reading under which a quantised code is decided in the same
-    precision on both sides."""
-    y = np.asarray(_f32(x), np.float32) * np.asarray(signs, np.float32)
-    d = y.shape[-1]
-    if d & (d - 1):
+def sylvester_hadamard(d: int) -> np.ndarray:
+    """The d x d Sylvester Hadamard matrix (d a power of two) in float64:
+    H_1 = [1], H_2n = [[H_n, H_n], [H_n, -H_n]].  H is symmetric with
+    entries +-1 and H H^T = d I."""
+    if d < 1 or d & (d - 1):
         raise ValueError("d must be a power of two")
-    lead = y.shape[:-1]
-    h = 1
-    while h < d:
-        z = y.reshape(lead + (d // (2 * h), 2, h))
-        a, b = z[..., 0, :], z[..., 1, :]
-        y = np.stack([a + b, a - b], axis=-2).reshape(lead + (d,))
-        h *= 2
-    return y
+    H = np.ones((1, 1), np.float64)
+    while H.shape[0] < d:
+        H = np.block([[H, H], [H, -H]])
+    return H
+
+
+def hadamard_rotate(x, signs):
+    """x [..., d] times diag(signs) H, in float64: the unnormalised random
+    orthogonal transform of incoherent processing (Lecture 11, section 4.5,
+    FP8 item; R = diag(signs) H / sqrt(d) is orthogonal).  The plain
+    definition: one float64 matrix product with the Sylvester matrix, no
+    particular order of evaluation."""
+    y = np.asarray(_f32(x), np.float64) * np.asarray(signs, np.float64)
+    return y @ sylvester_hadamard(y.shape[-1])
 
 
 def quantize_fp8_blocks_rotated(x, signs, block: int = 128):
     """Incoherent processing before block quantisation (Lecture 11, section
-    4.5, FP8 item): the codes and scales of quantize_fp8_blocks applied to
-    hadamard_rotate(x, signs), each scale then multiplied in float32 by
-    c = float32(1 / sqrt(d)) so that codes * scales ~= x R with the orthogonal
-    R = diag(signs) H / sqrt(d).  Returns (codes, scales) like
-    quantize_fp8_blocks."""
+    4.5, FP8 item).  Reading: the rotated rows y = x diag(signs) H (exact, in
+    float64) are rounded once to float32, the quantiser's working type, and
+    block-quantised by quantize_fp8_blocks; each scale is then multiplied in
+    float32 by c = float32(1 / sqrt(d)), so that codes * scales ~= x R with
+    the orthogonal R = diag(signs) H / sqrt(d).  Returns (codes, scales) like
+    quantize_fp8_blocks.  An implementation that forms y in float32 differs
+    from this by the rounding of its own order of evaluation: see
+    rotation_error_bound."""
     y = hadamard_rotate(x, signs)
-    codes, scales = quantize_fp8_blocks(y, block)
+    codes, scales = quantize_fp8_blocks(y.astype(np.float32), block)
     c = np.float32(1.0 / np.sqrt(np.float64(y.shape[-1])))
     return codes, (np.asarray(scales, np.float32) * c).astype(np.float32)
+
+
+def rotation_error_bound(x):
+    """Bound on |y32 - y| for the rows of any float32 evaluation of the
+    rotation by the fast Walsh-Hadamard butterflies (log2 d stages of sums and
+    differences of pairs): every stage rounds each intermediate once, with a
+    relative error of at most u = 2^-24, and no intermediate exceeds
+    sum_j |x_j| in magnitude, so the error of an output is at most
+    log2(d) u sum_j |x_j| (first order; doubled here for the higher-order
+    terms).  Returns [..., 1] float64."""
+    xa = np.abs(np.asarray(_f32(x), np.float64))
+    d = xa.shape[-1]
+    return 2.0 * np.log2(d) * 2.0 ** -24 * xa.sum(axis=-1, keepdims=True)
 
 
 def dequantize_fp8_blocks(codes, scales, block: int = 128):

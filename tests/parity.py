@@ -43,3 +43,72 @@ def guards_intact(backing, guard, fill=7.0):
     lo = backing[:guard]
     hi = backing[-guard:]
     return bool(torch.all(lo == fill)) and bool(torch.all(hi == fill))
+
+
+def e4m3_values():
+    """All 256 e4m3 codes decoded from the format's definition (sign, 4-bit
+    exponent with bias 7, 3-bit mantissa, subnormals at exponent 0, NaN at
+    exponent 15 with mantissa 7)."""
+    out = np.empty(256)
+    for c in range(256):
+        s = -1.0 if c & 0x80 else 1.0
+        e, m = (c >> 3) & 0xF, c & 7
+        if e == 15 and m == 7:
+            out[c] = np.nan
+        elif e == 0:
+            out[c] = s * (m / 8.0) * 2.0 ** -6
+        else:
+            out[c] = s * (1.0 + m / 8.0) * 2.0 ** (e - 7)
+    return out
+
+
+def check_rotated_codes(codes_g, scales_g, x, signs, oracle_mod, block=128, max_frac=0.01):
+    """GPU codes and scales of the rotated block quantiser against the
+    oracle's: the oracle rotates exactly (float64) and rounds once to
+    float32; a float32 evaluation of the rotation (the kernel's butterflies)
+    may differ by the rounding of its order of evaluation, bounded by
+    oracle.rotation_error_bound E.  So a scale may differ by the relative
+    amount E_max / amax (+ a few ulps), and a code may differ from the
+    oracle's only by one e4m3 step, only where the exact scaled value lies
+    within that error of the midpoint between the two codes.  Returns the
+    number of differing codes (at most max_frac of all)."""
+    u = 2.0 ** -24
+    codes_g = np.asarray(codes_g, np.uint8)
+    scales_g = np.asarray(scales_g, np.float64)
+    y = oracle_mod.hadamard_rotate(x, signs)                   # [B, N, H, d] float64
+    E = oracle_mod.rotation_error_bound(x)[..., 0]            # [B, N, H]
+    rc, rs = oracle_mod.quantize_fp8_blocks_rotated(x, signs, block)
+    B, N, H, d = y.shape
+    c = float(np.float32(1.0 / np.sqrt(np.float64(d))))
+    vals = e4m3_values()
+    order = np.sort(vals[~np.isnan(vals)])
+    rank = {v: i for i, v in enumerate(np.unique(order))}
+    n_diff = 0
+    for b in range(B):
+        for h in range(H):
+            for bi in range((N + block - 1) // block):
+                r0, r1 = bi * block, min(N, (bi + 1) * block)
+                yb = y[b, r0:r1, h]                            # [rows, d]
+                amax = np.abs(yb).max()
+                sg, so = scales_g[b, h, bi], float(rs[b, h, bi])
+                if amax == 0.0:
+                    assert sg == so and np.all(codes_g[b, r0:r1, h] == 0), (b, h, bi)
+                    continue
+                emax = E[b, r0:r1, h].max()
+                rel = emax / amax + 4 * u
+                assert abs(sg - so) <= so * rel, ("scale", b, h, bi, sg, so)
+                cg, co = codes_g[b, r0:r1, h], rc[b, r0:r1, h]
+                bad = np.argwhere(cg != co)
+                n_diff += len(bad)
+                for i, j in bad:
+                    vg, vo = vals[cg[i, j]], vals[co[i, j]]
+                    if vg == vo:  # +0 and -0: a value below every code, of either sign
+                        continue
+                    assert abs(rank[abs(vg)] - rank[abs(vo)]) == 1 and np.sign(vg) * np.sign(vo) >= 0, \
+                        ("codes not adjacent", b, r0 + i, h, j, vg, vo)
+                    z = yb[i, j] * 448.0 / amax                # exact scaled value
+                    tol = E[b, r0 + i, h] * 448.0 / amax + abs(z) * rel + 1e-12
+                    assert abs(abs(z) - 0.5 * (abs(vg) + abs(vo))) <= tol, \
+                        ("code differs away from a rounding boundary", b, r0 + i, h, j, z, vg, vo)
+    assert n_diff <= max_frac * codes_g.size, n_diff
+    return n_diff

@@ -517,12 +517,12 @@ def test_hadamard_rotation_is_the_sylvester_matrix(oracle_mod, d):
     H H^T = d I."""
     scipy_linalg = pytest.importorskip("scipy.linalg")
     H = oracle_mod.hadamard_rotate(np.eye(d), np.ones(d))
-    assert np.array_equal(H, scipy_linalg.hadamard(d).astype(np.float32))
-    assert np.array_equal(np.abs(H), np.ones((d, d), np.float32))
-    assert np.array_equal(H.astype(np.float64) @ H.T.astype(np.float64), d * np.eye(d))
+    assert np.array_equal(H, scipy_linalg.hadamard(d).astype(np.float64))
+    assert np.array_equal(np.abs(H), np.ones((d, d)))
+    assert np.array_equal(H @ H.T, d * np.eye(d))
     # the signs multiply the rows of H (diag(s) H)
     s = np.where(np.arange(d) % 3 == 0, -1.0, 1.0)
-    assert np.array_equal(oracle_mod.hadamard_rotate(np.eye(d), s), (s[:, None] * H).astype(np.float32))
+    assert np.array_equal(oracle_mod.hadamard_rotate(np.eye(d), s), s[:, None] * H)
 
 
 def test_hadamard_rotation_keeps_dot_products_and_spreads_outliers(oracle_mod):
@@ -531,15 +531,88 @@ def test_hadamard_rotation_keeps_dot_products_and_spreads_outliers(oracle_mod):
     s = rng.choice([-1.0, 1.0], size=d)
     x = rng.standard_normal((5, d)).astype(np.float32)
     y = rng.standard_normal((7, d)).astype(np.float32)
-    xr = oracle_mod.hadamard_rotate(x, s).astype(np.float64)
-    yr = oracle_mod.hadamard_rotate(y, s).astype(np.float64)
-    # (x R)(y R)^T = x y^T with R = diag(s) H / sqrt(d) orthogonal
+    xr = oracle_mod.hadamard_rotate(x, s)
+    yr = oracle_mod.hadamard_rotate(y, s)
+    # (x R)(y R)^T = x y^T with R = diag(s) H / sqrt(d) orthogonal (float64 throughout)
     exact = x.astype(np.float64) @ y.astype(np.float64).T
-    assert np.allclose(xr @ yr.T / d, exact, rtol=0, atol=1e-4)
+    assert np.allclose(xr @ yr.T / d, exact, rtol=0, atol=1e-11)
+    # the rows keep their norm up to sqrt(d)
+    assert np.allclose((xr ** 2).sum(axis=1), d * (x.astype(np.float64) ** 2).sum(axis=1), rtol=1e-13)
     # a single outlier feature is spread evenly over all d columns
     one = np.zeros((1, d), np.float32)
     one[0, 5] = 1000.0
-    assert np.array_equal(np.abs(oracle_mod.hadamard_rotate(one, s)), np.full((1, d), 1000.0, np.float32))
+    assert np.array_equal(np.abs(oracle_mod.hadamard_rotate(one, s)), np.full((1, d), 1000.0))
+
+
+def _fwht_float32(x, s):
+    """A float32 fast Walsh-Hadamard evaluation (butterflies h = 1, 2, ...,
+    d/2), written here only to test the error bound of the oracle against
+    an order of evaluation other than its own."""
+    y = (np.asarray(x, np.float32) * np.asarray(s, np.float32)).astype(np.float32)
+    d = y.shape[-1]
+    h = 1
+    while h < d:
+        z = y.reshape(y.shape[:-1] + (d // (2 * h), 2, h))
+        a, b = z[..., 0, :], z[..., 1, :]
+        y = np.stack([a + b, a - b], axis=-2).reshape(y.shape).astype(np.float32)
+        h *= 2
+    return y
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_rotation_error_bound_holds_for_float32_butterflies(oracle_mod, d):
+    """rotation_error_bound covers a float32 butterfly evaluation on inputs
+    with widely spread magnitudes (where float32 partial sums must round), and
+    is not vacuous (within a few hundred ulps of the row's sum of |x|)."""
+    rng = np.random.default_rng(8)
+    x = (rng.standard_normal((400, d)) * np.exp2(rng.integers(-12, 12, (400, d)))).astype(np.float32)
+    s = rng.choice([-1.0, 1.0], size=d)
+    y = oracle_mod.hadamard_rotate(x, s)
+    y32 = _fwht_float32(x, s).astype(np.float64)
+    E = oracle_mod.rotation_error_bound(x)
+    err = np.abs(y32 - y)
+    assert np.all(err <= E)
+    assert err.max() > 0                          # float32 really did round somewhere
+    assert np.all(E <= 2 * 7 * 2.0 ** -24 * np.abs(x.astype(np.float64)).sum(axis=-1, keepdims=True) * 1.0001)
+
+
+def test_fp8_rounding_ties_go_to_even(oracle_mod):
+    """e4m3 rounding is round-to-nearest with ties to the even code, pinned
+    at exact midpoints between codes.  A block whose maximum is 448 has
+    scale = inv = 1, so the quantiser sees the values unchanged.  Expected
+    codes, derived from the format (code = sign << 7 | (e + 7) << 3 | m):
+      1.0625  between 1.0 (0x38, m=000) and 1.125 (0x39)   -> 0x38
+      1.1875  between 1.125 (0x39) and 1.25 (0x3A, m=010)  -> 0x3A
+      -1.0625                                               -> 0xB8
+      17      between 16 (0x58) and 18 (0x59)               -> 0x58
+      19      between 18 (0x59) and 20 (0x5A)               -> 0x5A
+      432     between 416 (0x7D, m=101) and 448 (0x7E)      -> 0x7E (the top code)
+      -432                                                  -> 0xFE
+      2^-10   between 0 and the smallest subnormal 2^-9     -> 0x00
+      3 2^-10 between 2^-9 (0x01) and 2^-8 (0x02)           -> 0x02
+    and just above a midpoint the value rounds up:
+      1.0703125 (1.0625 + 2^-7)  -> 0x39;  2^-10 (1 + 2^-7) -> 0x01."""
+    vals = [448.0, 1.0625, 1.1875, -1.0625, 17.0, 19.0, 432.0, -432.0, 2.0 ** -10, 3 * 2.0 ** -10,
+            1.0703125, 2.0 ** -10 * (1 + 2.0 ** -7)]
+    want = [0x7E, 0x38, 0x3A, 0xB8, 0x58, 0x5A, 0x7E, 0xFE, 0x00, 0x02, 0x39, 0x01]
+    x = np.zeros((1, 128, 1, 16), np.float32)
+    x[0, :len(vals), 0, 0] = vals
+    codes, scales = oracle_mod.quantize_fp8_blocks(x)
+    assert scales[0, 0, 0] == 1.0
+    assert [int(c) for c in codes[0, :len(vals), 0, 0]] == want
+
+
+def test_fp8_block_maximum_saturates_at_448(oracle_mod):
+    """When amax * float32(448 / amax) rounds above 448 (amax = 1.359375 in
+    float32: 448.00003), the block maximum still maps to the top code 448
+    (0x7E) and never to NaN, and the scale is amax / 448."""
+    amax = np.float32(1.359375)
+    assert np.float32(amax * (np.float32(448.0) / amax)) > 448.0
+    x = np.zeros((1, 128, 1, 8), np.float32)
+    x[0, 3, 0, 2], x[0, 9, 0, 5] = amax, -amax
+    codes, scales = oracle_mod.quantize_fp8_blocks(x)
+    assert codes[0, 3, 0, 2] == 0x7E and codes[0, 9, 0, 5] == 0xFE
+    assert scales[0, 0, 0] == np.float32(amax / np.float32(448.0))
 
 
 def test_rotated_quantisation_dequantises_to_the_rotated_rows(oracle_mod):
@@ -575,3 +648,34 @@ def test_rotated_quantisation_dequantises_to_the_rotated_rows(oracle_mod):
     err_rot = np.abs(np.einsum("nd,md->nm", qd[0, :, 0], kd[0, :, 0]) - exact).mean()
     err_plain = np.abs(np.einsum("nd,md->nm", qp[0, :, 0], kp[0, :, 0]) - exact).mean()
     assert err_rot < err_plain
+
+
+def test_rotated_code_checker_accepts_float32_rounding_and_rejects_real_errors(oracle_mod):
+    """check_rotated_codes (used by the GPU test of the rotated quantiser)
+    accepts the codes of a float32 butterfly evaluation and rejects a code
+    moved by one step where the value is far from a rounding boundary, and a
+    scale that is off by more than the rounding allows."""
+    from parity import check_rotated_codes
+    rng = np.random.default_rng(9)
+    d = 128
+    x = (rng.standard_normal((1, 300, 2, d)) * 3).astype(np.float32)
+    x[0, :, 0, 5] *= 40
+    x = torch.from_numpy(x).to(torch.bfloat16).float().numpy()   # bf16 inputs, as the kernel takes
+    s = rng.choice([-1.0, 1.0], size=d).astype(np.float32)
+    codes, scales = oracle_mod.quantize_fp8_blocks(_fwht_float32(x, s))
+    scales = (scales * np.float32(1.0 / np.sqrt(128.0))).astype(np.float32)
+    check_rotated_codes(codes, scales, x, s, oracle_mod)
+    bad = codes.copy()
+    y = oracle_mod.hadamard_rotate(x, s)
+    amax = np.abs(y[0, :128, 1]).max()
+    z = np.abs(y[0, :128, 1]) * 448.0 / amax
+    # an element of a middle binade far from any midpoint: move its code by one
+    frac = (z / 2.0 ** np.floor(np.log2(np.maximum(z, 1e-30)))) * 8 % 1
+    i, j = np.argwhere((z > 4) & (z < 200) & (np.abs(frac - 0.5) > 0.4))[0]
+    bad[0, i, 1, j] = bad[0, i, 1, j] + 1 if bad[0, i, 1, j] & 7 < 6 else bad[0, i, 1, j] - 1
+    with pytest.raises(AssertionError, match="away from a rounding boundary"):
+        check_rotated_codes(bad, scales, x, s, oracle_mod)
+    off = scales.copy()
+    off[0, 1, 0] *= np.float32(1 + 2.0 ** -10)
+    with pytest.raises(AssertionError, match="scale"):
+        check_rotated_codes(codes, off, x, s, oracle_mod)
