@@ -1,14 +1,19 @@
 """Benchmark: exact-attention forward TFLOP/s and flash-decoding GB/s on GB300.
 
-One step = one pass of the whole hot path over one batch of synthetic input:
-  prefill  attn_fwd   B=4, Hq=Hkv=16, Nq=Nk=4096, d=128, causal, bf16
-  decode   attn_decode_splitkv  B=1, Hq=32, Hkv=8, Nk=65536, d=128, bf16
-Inputs are resident in HBM when the timed region starts and are larger than
-L2; L2 is also flushed before every timed call, outside the events: a 256 MiB
-write and then a 256 MiB read, so that L2 holds only clean lines of another
-buffer and no write-back of the flush (or of the previous call's output)
-lands inside the timed region.  Each call is timed with CUDA events on the
-launching stream.
+One step = one pass of the whole hot path over one batch of synthetic input,
+on the largest single-GPU configurations of the workloads below:
+  prefill  attn_fwd   long_sequence: B=1, Hq=32, Hkv=8, Nq=Nk=16384, d=128,
+                      causal, bf16 (the sequence-parallel stress shape)
+  decode   attn_decode_splitkv  decode_b16_8k: B=16, Hq=32, Hkv=8, Nk=8192,
+                      d=128, bf16 (split-KV with the automatic segment count)
+Every other workload (single head fp32/bf16, ragged d=64 causal and
+non-causal, the q x 8 outlier variants, training-style prefill, the 64K-key
+decode) is timed the same way and reported per workload under "configs".
+Inputs are resident in HBM when a timed call starts; L2 is flushed before
+every timed call, outside the events: a 256 MiB write and then a 256 MiB
+read, so that L2 holds only clean lines of another buffer and no write-back
+of the flush (or of the previous call's output) lands inside the timed
+region.  Each call is timed with CUDA events on the launching stream.
 
 value  = prefill TFLOP/s (FLOPs counted as 4 Nq Nk d per head, halved for
          causal, summed over ranks) / max-over-ranks time.
@@ -16,8 +21,7 @@ decode = GB/s of the decode call (K + V + Q + O + LSE bytes, each once).
 e2e    = the same metrics through the C ABI with pinned host buffers: the
          host->device copy of the inputs and the device->host copy of O and
          LSE are inside the timed region (the forward through attn_fwd_host,
-         whose batch chunks overlap copies and computation; the decode
-         through attn_decode_splitkv after its copies).
+         the decode through attn_decode_splitkv after its copies).
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 For N > 1 run under torchrun; every rank runs an independent replica of the
@@ -54,14 +58,29 @@ DECODE = {
     "decode_b16_8k": (16, 32, 8, 8192, 128),
 }
 
-# DRAM traffic of one forward launch from an ncu capture, keyed by the hash of
-# the kernel source it was measured on (any later change to the source turns
-# the figure into null).  Filled from profiles/ summaries.
+# The step's workloads (the largest single-GPU configurations).
+HEADLINE_PREFILL = "long_sequence"
+HEADLINE_DECODE = "decode_b16_8k"
+
+# Every workload reported under "configs": name -> (prefill shape, dtype, q scale).
+PREFILL_CONFIGS = {
+    "single_head_fp32": ("single_head", "float32", 1.0),
+    "single_head_bf16": ("single_head", "bfloat16", 1.0),
+    "ragged": ("ragged", "bfloat16", 1.0),
+    "ragged_causal": ("ragged_causal", "bfloat16", 1.0),
+    "ragged_outlier": ("ragged", "bfloat16", 8.0),
+    "ragged_outlier_causal": ("ragged_causal", "bfloat16", 8.0),
+    "training_prefill": ("training_prefill", "bfloat16", 1.0),
+    "long_sequence": ("long_sequence", "bfloat16", 1.0),
+}
+NOMINAL_HBM_GBS = 8000.0  # the ~8 TB/s HBM3e figure the decode target is quoted against
+
+# DRAM traffic of one launch from an ncu capture (dram__bytes_read.sum +
+# dram__bytes_write.sum), keyed by the hash of the kernel source it was
+# measured on: any later change to the source turns the figure into null.
 NCU_TRAFFIC = {
-    "training_prefill": {"bytes_per_launch": 586.9e6, "src_hash": "85de91f94a6afb87",
-                         "profile": "profiles/fwd_tc_training_prefill.md"},
-    "decode_64k": {"bytes_per_launch": 272.0e6, "src_hash": "b06bdc5bcf952bd3",
-                   "profile": "profiles/decode_split_64k.md"},
+    "long_sequence": {"bytes_per_launch": None, "src": "fwd_tc.cu", "src_hash": None},
+    "decode_b16_8k": {"bytes_per_launch": None, "src": "decode.cu", "src_hash": None},
 }
 
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -183,6 +202,26 @@ def whole_job_rate(work_per_rank: float, ms_max_over_ranks: float, world: int, s
     return work_per_rank * world / (ms_max_over_ranks * 1e-3) / scale
 
 
+def prefill_desc(name: str) -> str:
+    B, Hq, Hkv, Nq, Nk, d, causal = PREFILL[name]
+    return "%s (B=%d Hq=%d Hkv=%d Nq=%d Nk=%d d=%d %s)" % (
+        name, B, Hq, Hkv, Nq, Nk, d, "causal" if causal else "non-causal")
+
+
+def decode_desc(name: str) -> str:
+    B, Hq, Hkv, Nk, d = DECODE[name]
+    return "%s (B=%d Hq=%d Hkv=%d Nk=%d d=%d)" % (name, B, Hq, Hkv, Nk, d)
+
+
+def workload_config(args) -> dict:
+    """The step's workload, the same on both arms."""
+    return {
+        "workload": "prefill %s + decode %s, bf16" % (prefill_desc(args.prefill), decode_desc(args.decode)),
+        "l2": "inputs larger than L2; L2 flushed before every timed call (256 MiB write, then "
+              "256 MiB read so no dirty line is written back inside the timed region)",
+    }
+
+
 # ----------------------------------------------------------------------------- reference arm
 
 _ORACLE_INPUTS = {}
@@ -231,16 +270,16 @@ def run_reference(args):
     wall = time.perf_counter() - t0
     value = statistics.mean(vals)
     B, Hq, Hkv, Nq, Nk, d, causal = cfg
-    sample = ("%d random rows (b, hq, i) of the %s workload per step, ~%.0f s of CPU work each; "
-              "FLOPs counted as for the GPU (4 Nk d per row, halved for causal)") % (
+    sample = ("%d random rows (b, hq, i) of the %s prefill per step, ~%.0f s of CPU work each; "
+              "FLOPs counted as for the GPU (4 Nk d per row, halved for causal); the oracle is "
+              "timed on the prefill half of the step, whose FLOPs are the metric") % (
         rows_total // max(1, args.steps), args.prefill, per_step)
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1000.0 * wall / max(1, args.steps), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": "%s B=%d Hq=%d Hkv=%d Nq=%d Nk=%d d=%d causal=%d (CPU oracle sample)"
-                               % (args.prefill, B, Hq, Hkv, Nq, Nk, d, causal)},
+        "config": workload_config(args),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
@@ -252,6 +291,71 @@ def run_reference(args):
 
 
 # ----------------------------------------------------------------------------- our arm
+
+def _timed_ms(call, reps: int, flush, warmup: int = 3) -> float:
+    """Mean CUDA-event time of `call` over `reps` calls, L2 flushed before each."""
+    import torch
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        flush()
+        call()
+    ts = []
+    for _ in range(reps):
+        flush()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        call()
+        e1.record(stream)
+        ts.append((e0, e1))
+    torch.cuda.synchronize()
+    return statistics.mean(a.elapsed_time(b) for a, b in ts)
+
+
+def measure_configs(attn, dev, flush, reps: int, peaks) -> dict:
+    """Every workload timed alone (L2 flushed before each call), with its
+    throughput and roofline fraction."""
+    import torch
+    from exact_attention_62_gb300.inputs import make_qkv
+    peak_t, peak_h = float(peaks["bf16_tflops"]), float(peaks["hbm_gbs"])
+    out = {}
+    for name, (shape, dt, q_scale) in PREFILL_CONFIGS.items():
+        B, Hq, Hkv, Nq, Nk, d, causal = PREFILL[shape]
+        dtype = getattr(torch, dt)
+        q, k, v = (x.to(dev) for x in make_qkv(B, Hq, Hkv, Nq, Nk, d, seed=30, dtype=dtype,
+                                                 q_scale=q_scale))
+        o, lse = torch.empty_like(q), torch.empty((B, Hq, Nq), dtype=torch.float32, device=dev)
+        scale = 1.0 / math.sqrt(d)
+        ms = _timed_ms(lambda: attn.attn_fwd(q, k, v, causal, scale, o=o, lse=lse), reps, flush)
+        tf = prefill_flops(PREFILL[shape]) / (ms * 1e-3) / 1e12
+        entry = {"shape": prefill_desc(shape), "dtype": dt, "ms": ms, "value": tf, "unit": "TFLOP/s"}
+        if q_scale != 1.0:
+            entry["q_scale"] = q_scale
+        if shape == "single_head":
+            entry["frac"] = None
+            entry["note"] = "latency-bound (one 256-row unit on one SM): time only"
+        elif dt == "bfloat16":
+            entry["frac"] = tf / peak_t
+            entry["peak"] = peak_t
+        out[name] = entry
+        del q, k, v, o, lse
+    for name in ("decode_64k", "decode_b16_8k"):
+        B, Hq, Hkv, Nk, d = DECODE[name]
+        q, k, v = (x.to(dev) for x in make_qkv(B, Hq, Hkv, 1, Nk, d, seed=31))
+        S = attn.attn_decode_num_splits(B, Hq, Hkv, Nk, d)
+        ws = torch.empty(max(16, attn.attn_decode_workspace_bytes(B, Hq, Hkv, Nk, d, S)),
+                         dtype=torch.uint8, device=dev)
+        o, lse = torch.empty_like(q), torch.empty((B, Hq), dtype=torch.float32, device=dev)
+        scale = 1.0 / math.sqrt(d)
+        ms = _timed_ms(lambda: attn.attn_decode_splitkv(q, k, v, scale, S, workspace=ws, o=o, lse=lse),
+                       reps, flush)
+        gbs = decode_bytes(DECODE[name]) / (ms * 1e-3) / 1e9
+        out[name] = {"shape": decode_desc(name), "dtype": "bfloat16", "splits": S, "ms": ms,
+                     "value": gbs, "unit": "GB/s", "frac": gbs / peak_h, "peak": peak_h,
+                     "frac_of_nominal_8tbs": gbs / NOMINAL_HBM_GBS}
+        del q, k, v, o, lse, ws
+    torch.cuda.empty_cache()
+    return out
+
 
 def run_ours(args):
     import torch
@@ -356,6 +460,13 @@ def run_ours(args):
                               "decode_ms": dec_total / K, "clocks": clk}))
         return 0
 
+    # ---- every workload of the method, each timed alone (rank 0's GPU)
+    configs = None
+    if not args.no_configs and rank == 0:
+        configs = measure_configs(attn, dev, flush_l2, min(K, 20), peaks)
+        if attn.attn_check_device_status() != 0:
+            raise RuntimeError("device status reports a timed-out wait")
+
     # ---- end to end through the C ABI with pinned host buffers
     e_pre_ms = e_dec_ms = None
     if not args.no_e2e:
@@ -366,7 +477,7 @@ def run_ours(args):
         do_h = torch.empty(do.shape, dtype=do.dtype).pin_memory()
         dl_h = torch.empty(dlse.shape, dtype=dlse.dtype).pin_memory()
         e_pre, e_dec = [], []
-        # the forward through attn_fwd_host: batch chunks copied in, computed and
+        # the forward through attn_fwd_host: chunks copied in, computed and
         # copied back on three streams, the transfers overlapping the computation
         up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
         for s in range(max(3, min(K, 10)) + 1):
@@ -399,14 +510,19 @@ def run_ours(args):
     pre_ms_avg = pre_total / K
     achieved = flops / (pre_ms_avg * 1e-3) / 1e12
     peak_t = float(peaks["bf16_tflops"])
-    rec = NCU_TRAFFIC.get(args.prefill)
-    traffic = rec["bytes_per_launch"] if rec and rec.get("src_hash") == src_hash("fwd_tc.cu") else None
+
+    def traffic_of(name):
+        rec = NCU_TRAFFIC.get(name)
+        if not rec or rec.get("bytes_per_launch") is None:
+            return None
+        return rec["bytes_per_launch"] if rec.get("src_hash") == src_hash(rec["src"]) else None
+
+    traffic = traffic_of(args.prefill)
     dbytes = decode_bytes(dcfg)
     dec_ms_avg = dec_total / K
     dec_gbs = dbytes / (dec_ms_avg * 1e-3) / 1e9
     peak_h = float(peaks["hbm_gbs"])
-    drec = NCU_TRAFFIC.get(args.decode)
-    dtraffic = drec["bytes_per_launch"] if drec and drec.get("src_hash") == src_hash("decode.cu") else None
+    dtraffic = traffic_of(args.decode)
 
     if rank != 0:
         if world > 1:
@@ -417,7 +533,7 @@ def run_ours(args):
     if not args.no_cpu_baseline:
         v_cpu, rows, cores = oracle_prefill_sample(pcfg, args.cpu_seconds)
         cpu = {"value": v_cpu, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-               "sample": "%d random rows of the %s workload (~%.0f s of CPU work), FLOPs counted "
+               "sample": "%d random rows of the %s prefill (~%.0f s of CPU work), FLOPs counted "
                          "as for the GPU (4 Nk d per row, halved for causal)"
                          % (rows, args.prefill, args.cpu_seconds)}
     launches_per_step = 1 + (1 if splits == 1 else 2)
@@ -430,9 +546,19 @@ def run_ours(args):
     if e_pre_ms is not None:
         e2e = {"value": whole_job_rate(flops, e_pre_ms, world, 1e12), "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "path": "attn_fwd_host: %d batch chunks, host copies overlapping the forward" % min(pcfg[0], 4)}
+               "path": "attn_fwd_host: host copies overlapping the forward"}
         de2e = {"value": whole_job_rate(dbytes, e_dec_ms, world, 1e9), "unit": "GB/s",
                 "h2d_bytes_per_step": dh2d, "d2h_bytes_per_step": dd2h}
+    config = workload_config(args)
+    config.update({
+        "prefill": {"B": B, "Hq": Hq, "Hkv": Hkv, "Nq": Nq, "Nk": Nk, "d": d,
+                    "causal": bool(causal), "ms": pre_ms_avg},
+        "decode": {"B": dB, "Hq": dHq, "Hkv": dHkv, "Nk": dNk, "d": dd, "splits": splits,
+                   "ms": dec_ms_avg},
+        "parallelism": "independent replicas" if world > 1 else "single GPU",
+        "clocks_window": "nvidia-smi every 100 ms over a 0.5 s untimed soak of the same "
+                         "step followed by the timed steps",
+    })
     line = {
         "metric": METRIC,
         "value": whole_job_rate(flops, pre_ms_avg, world, 1e12),
@@ -446,23 +572,13 @@ def run_ours(args):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic",
-        "config": {
-            "workload": "prefill %s + decode %s" % (args.prefill, args.decode),
-            "prefill": {"B": B, "Hq": Hq, "Hkv": Hkv, "Nq": Nq, "Nk": Nk, "d": d,
-                        "causal": bool(causal), "ms": pre_ms_avg},
-            "decode": {"B": dB, "Hq": dHq, "Hkv": dHkv, "Nk": dNk, "d": dd, "splits": splits,
-                       "ms": dec_ms_avg},
-            "l2": "inputs larger than L2; L2 flushed before every timed call (256 MiB write, "
-                  "then 256 MiB read so no dirty line is written back inside the timed region)",
-            "parallelism": "independent replicas" if world > 1 else "single GPU",
-            "clocks_window": "nvidia-smi every 100 ms over a 0.5 s untimed soak of the same "
-                             "step followed by the timed steps",
-        },
+        "config": config,
         "decode": {
             "value": whole_job_rate(dbytes, dec_ms_avg, world, 1e9), "unit": "GB/s",
             "roofline": {"bound": "hbm", "achieved": dec_gbs, "peak": peak_h, "unit": "GB/s",
                          "frac": dec_gbs / peak_h, "traffic": dtraffic,
-                         "peak_source": "%s HBM copy" % peak_src},
+                         "peak_source": "%s HBM copy" % peak_src,
+                         "frac_of_nominal_8tbs": dec_gbs / NOMINAL_HBM_GBS},
             "e2e": de2e,
         },
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_t, "unit": "TFLOP/s",
@@ -472,6 +588,7 @@ def run_ours(args):
         "cpu_baseline": cpu,
         "clocks": clk,
         "gpu_launches": K * launches_per_step,
+        "configs": configs,
         "wall_s": t_wall,
     }
     print(json.dumps(line))
@@ -502,10 +619,25 @@ def run_extra(args):
         call = lambda: attn.attn_decode_paged(qh, kp, vp, table, lens, dNk, 1.0 / math.sqrt(dd))
         return _time_extra(args, call, flush_w, flush_r, attn, "GB/s", decode_bytes(DECODE[args.decode]) / 1e9,
                            args.decode)
+    if args.only == "splitkv":
+        dB, dHq, dHkv, dNk, dd = DECODE[args.decode]
+        qh, kh, vh = (x.to(dev) for x in make_qkv(dB, dHq, dHkv, 1, dNk, dd, seed=20))
+        splits = args.splits or attn.attn_decode_num_splits(dB, dHq, dHkv, dNk, dd)
+        ws = torch.empty(max(16, attn.attn_decode_workspace_bytes(dB, dHq, dHkv, dNk, dd, splits)),
+                         dtype=torch.uint8, device=dev)
+        do, dl = torch.empty_like(qh), torch.empty((dB, dHq), dtype=torch.float32, device=dev)
+        call = lambda: attn.attn_decode_splitkv(qh, kh, vh, 1.0 / math.sqrt(dd), splits, workspace=ws,
+                                                o=do, lse=dl)
+        return _time_extra(args, call, flush_w, flush_r, attn, "GB/s", decode_bytes(DECODE[args.decode]) / 1e9,
+                           args.decode, {"splits": splits})
     B, Hq, Hkv, Nq, Nk, d, causal = PREFILL[args.prefill]
     scale = 1.0 / math.sqrt(d)
     q, k, v = (x.to(dev) for x in make_qkv(B, Hq, Hkv, Nq, Nk, d, seed=10))
     o, lse = attn.attn_fwd(q, k, v, causal, scale)
+    if args.only == "forward":
+        call = lambda: attn.attn_fwd(q, k, v, causal, scale, o=o, lse=lse)
+        return _time_extra(args, call, flush_w, flush_r, attn, "tflops",
+                           prefill_flops(PREFILL[args.prefill]) / 1e12, args.prefill)
     if args.only == "backward":
         dout = torch.randn_like(q)
         dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
@@ -521,7 +653,7 @@ def run_extra(args):
     return _time_extra(args, call, flush_w, flush_r, attn, "tflops", flops / 1e12, args.prefill)
 
 
-def _time_extra(args, call, flush_w, flush_r, attn, unit, work, workload):
+def _time_extra(args, call, flush_w, flush_r, attn, unit, work, workload, extra=None):
     import torch
     for _ in range(args.warmup):
         flush_w.zero_()
@@ -543,6 +675,7 @@ def _time_extra(args, call, flush_w, flush_r, attn, unit, work, workload):
     out = {"profile_only": args.only, "workload": workload, "ms": ms, unit: work / (ms * 1e-3)}
     if args.only == "paged":
         out["page_size"] = args.page_size
+    out.update(extra or {})
     print(json.dumps(out))
     return 0
 
@@ -553,22 +686,27 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--prefill", choices=sorted(PREFILL), default="training_prefill")
-    ap.add_argument("--decode", choices=sorted(DECODE), default="decode_64k")
+    ap.add_argument("--prefill", choices=sorted(PREFILL), default=HEADLINE_PREFILL)
+    ap.add_argument("--decode", choices=sorted(DECODE), default=HEADLINE_DECODE)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--page-size", type=int, default=16, help="--only paged: keys per page")
-    ap.add_argument("--only", choices=["prefill", "decode", "backward", "fp8", "paged"], default=None,
+    ap.add_argument("--only", choices=["prefill", "decode", "forward", "splitkv", "backward", "fp8",
+                                        "paged"], default=None,
                     help="time one part only (for profiling; no JSON contract): a half of the "
-                         "step, or the backward pass / the FP8-Q,K forward on the prefill workload")
+                         "step with the clock soak (prefill, decode); or, without the soak, "
+                         "attn_fwd / the backward pass / the FP8-Q,K forward on the prefill "
+                         "workload, attn_decode_splitkv / the paged decode on the decode workload")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer measurement")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the per-workload block (every workload timed alone)")
     ap.add_argument("--splits", type=int, default=0, help="decode segments (0 = automatic)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         return run_reference(args)
-    if args.only in ("backward", "fp8", "paged"):
+    if args.only in ("forward", "splitkv", "backward", "fp8", "paged"):
         return run_extra(args)
     return run_ours(args)
 

@@ -22,7 +22,8 @@ __all__ = [
     "attn_check_device_status", "attn_read_tile_counter", "attn_version",
     "attn_decode_splitkv_static", "attn_decode_paged", "attn_decode_paged_num_splits",
     "attn_bwd", "attn_bwd_workspace_bytes", "attn_quantize_fp8", "attn_quantize_fp8_rotated",
-    "attn_fwd_fp8", "DECODE_STATIC_SCRATCH_BYTES", "EXPORTED_SYMBOLS",
+    "attn_fwd_fp8", "DECODE_STATIC_SCRATCH_BYTES", "EXPORTED_SYMBOLS", "TEST_SYMBOLS",
+    "AttnTestOptions", "attn_fwd_test", "attn_decode_test",
 ]
 
 ATTN_OK, ATTN_ERR_INVALID, ATTN_ERR_UNSUPPORTED, ATTN_ERR_CUDA, ATTN_ERR_TIMEOUT = range(5)
@@ -38,12 +39,27 @@ EXPORTED_SYMBOLS = (
     "attn_fwd_fp8",
 )
 
+# The test-only entry points include/attn_test.h declares.
+TEST_SYMBOLS = ("attn_fwd_test", "attn_decode_test")
+
 # Size of the scratch area built into the library for attn_decode_splitkv_static.
 DECODE_STATIC_SCRATCH_BYTES = 8 << 20
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_PKG, "libattn.so")
 _lib = None
+
+
+class AttnTestOptions(ctypes.Structure):
+    """attn_test_options_t of include/attn_test.h (tests and measurements only)."""
+    _fields_ = [("p_in_smem", ctypes.c_int), ("exp2_poly", ctypes.c_int),
+                ("rescale_threshold", ctypes.c_float), ("wait_limit_cycles", ctypes.c_longlong),
+                ("skip_load", ctypes.c_int), ("softmax_split", ctypes.c_int)]
+
+    def __init__(self, p_in_smem=0, exp2_poly=0, rescale_threshold=0.0, wait_limit_cycles=0,
+                 skip_load=-1, softmax_split=0):
+        super().__init__(int(p_in_smem), int(exp2_poly), float(rescale_threshold),
+                         int(wait_limit_cycles), int(skip_load), int(softmax_split))
 
 
 class AttnError(RuntimeError):
@@ -114,6 +130,11 @@ def lib() -> ctypes.CDLL:
     L.attn_fwd_fp8.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, P]
     L.attn_fwd_fp8.restype = I
     L.attn_decode_splitkv_static.restype = I
+    OPT = ctypes.POINTER(AttnTestOptions)
+    L.attn_fwd_test.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, F, OPT, P]
+    L.attn_fwd_test.restype = I
+    L.attn_decode_test.argtypes = [P, P, P, P, P, I, I, I, I, I, F, I, P, SZ, OPT, P]
+    L.attn_decode_test.restype = I
     _lib = L
     return L
 
@@ -576,4 +597,64 @@ def attn_fwd_fp8(q8, k8, v, q_scales, k_scales, causal: bool, scale: float | Non
                                 _ptr(lse), B, Hq, Hkv, Nq, Nk, d, int(bool(causal)), float(scale),
                                 _stream(stream, dev))
     _check("attn_fwd_fp8", st)
+    return o, lse
+
+
+# ----------------------------------------------------------------------------- tests only
+
+def attn_fwd_test(q, k, v, causal: bool, scale: float, options: AttnTestOptions, o=None, lse=None,
+                  stream=None):
+    """attn_fwd_test of include/attn_test.h: the bf16 forward with test
+    options (kernel variants, wait bound, load injection).  Tests and
+    measurements only.  Returns (o, lse)."""
+    import torch
+    B, Nq, Hq, d = q.shape
+    Bk, Nk, Hkv, dk = k.shape
+    if Bk != B or dk != d or tuple(v.shape) != tuple(k.shape):
+        raise ValueError("shape mismatch")
+    if not (q.dtype == k.dtype == v.dtype == torch.bfloat16):
+        raise ValueError("q, k, v must be bfloat16")
+    dev = q.device
+    for n, t in (("q", q), ("k", k), ("v", v)):
+        _need_cuda_contig(n, t, dev)
+    o = torch.empty_like(q) if o is None else o
+    lse = torch.empty((B, Hq, Nq), dtype=torch.float32, device=dev) if lse is None else lse
+    _need_buffer("o", o, q.shape, q.dtype, dev)
+    _need_buffer("lse", lse, (B, Hq, Nq), torch.float32, dev)
+    with torch.cuda.device(dev):
+        st = lib().attn_fwd_test(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Nq, Nk,
+                                 d, int(bool(causal)), float(scale), ctypes.byref(options),
+                                 _stream(stream, dev))
+    _check("attn_fwd_test", st)
+    return o, lse
+
+
+def attn_decode_test(q, k_cache, v_cache, scale: float, num_splits: int, options: AttnTestOptions,
+                     workspace=None, o=None, lse=None, stream=None):
+    """attn_decode_test of include/attn_test.h: the split-KV decode with the
+    wait bound and load injection of `options`.  Tests only.  Returns (o, lse)."""
+    import torch
+    B, one, Hq, d = q.shape
+    Bk, Nk, Hkv, dk = k_cache.shape
+    if one != 1 or Bk != B or dk != d or tuple(v_cache.shape) != tuple(k_cache.shape):
+        raise ValueError("shape mismatch")
+    dev = q.device
+    for n, t in (("q", q), ("k_cache", k_cache), ("v_cache", v_cache)):
+        _need_cuda_contig(n, t, dev)
+    if num_splits == 0 and Nk > 0:
+        with torch.cuda.device(dev):
+            num_splits = attn_decode_num_splits(B, Hq, Hkv, Nk, d)
+    wbytes = attn_decode_workspace_bytes(B, Hq, Hkv, Nk, d, num_splits) if Nk > 0 else 0
+    if workspace is None and wbytes > 0:
+        workspace = torch.empty(wbytes, dtype=torch.uint8, device=dev)
+    o = torch.empty_like(q) if o is None else o
+    lse = torch.empty((B, Hq), dtype=torch.float32, device=dev) if lse is None else lse
+    _need_buffer("o", o, q.shape, q.dtype, dev)
+    _need_buffer("lse", lse, (B, Hq), torch.float32, dev)
+    wsize = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    with torch.cuda.device(dev):
+        st = lib().attn_decode_test(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(o), _ptr(lse), B, Hq,
+                                    Hkv, Nk, d, float(scale), int(num_splits), _ptr(workspace), wsize,
+                                    ctypes.byref(options), _stream(stream, dev))
+    _check("attn_decode_test", st)
     return o, lse

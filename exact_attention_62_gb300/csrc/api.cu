@@ -1,6 +1,7 @@
 // api.cu -- the extern "C" entry points of libattn.so (declared and
-// documented in include/attn.h): argument checks, TMA tensor-map encoding
-// and dispatch to the kernels.  Nothing here allocates device memory,
+// documented in include/attn.h, and the test-only ones in
+// include/attn_test.h): argument checks, TMA tensor-map encoding and
+// dispatch to the kernels.  Nothing here allocates device memory,
 // synchronises a stream (except the two explicitly synchronous status
 // readers) or keeps state between calls.
 #include <cmath>
@@ -71,14 +72,48 @@ bool encode_bshd_map(CUtensorMap* map, const void* base, int B, int N, int H, in
 }
 
 int device_sm_count() {
-    static int cache[64] = {0};
+    static int cache[kMaxDevices] = {0};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 0;
-    if (dev < 64 && cache[dev] > 0) return cache[dev];
+    if (dev < kMaxDevices && cache[dev] > 0) return cache[dev];
     int n = 0;
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-    if (dev < 64) cache[dev] = n;
+    if (dev < kMaxDevices) cache[dev] = n;
     return n;
+}
+
+attn_status_t check_decode_args(const void* q, const void* k_cache, const void* v_cache,
+                                const void* o, const float* lse, int B, int Hq, int Hkv, int Nk,
+                                int d, float scale, int num_splits, attn_dtype_t dtype, int* S,
+                                bool* empty) {
+    *S = 0;
+    *empty = false;
+    if (B < 0 || Hq < 0 || Hkv < 1 || Nk < 0 || d < 1 || num_splits < 0) return ATTN_ERR_INVALID;
+    if (dtype != ATTN_BF16 && dtype != ATTN_F32) return ATTN_ERR_INVALID;
+    if (bad_scale(scale)) return ATTN_ERR_INVALID;
+    if (Hq % Hkv != 0) return ATTN_ERR_INVALID;
+    if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+    if (dtype != ATTN_BF16) return ATTN_ERR_UNSUPPORTED;
+    if (B > 65535 || Hq > 65535) return ATTN_ERR_UNSUPPORTED;
+    if (B == 0 || Hq == 0) {
+        *empty = true;
+        return ATTN_OK;
+    }
+    if (q == nullptr || o == nullptr || lse == nullptr) return ATTN_ERR_INVALID;
+    if (misaligned(q, 16) || misaligned(o, 16) || misaligned(lse, 4)) return ATTN_ERR_INVALID;
+    if (Nk == 0) {
+        *empty = true;
+        return ATTN_OK;
+    }
+    if (k_cache == nullptr || v_cache == nullptr) return ATTN_ERR_INVALID;
+    if (misaligned(k_cache, 16) || misaligned(v_cache, 16)) return ATTN_ERR_INVALID;
+    if (num_splits > Nk) return ATTN_ERR_INVALID;
+    int s = num_splits;
+    if (s == 0) s = decode_auto_splits(B, Hq, Hkv, Nk, d);
+    if (s < 1) return ATTN_ERR_CUDA;
+    if (s > 65535) return ATTN_ERR_UNSUPPORTED;
+    *S = s;
+    return ATTN_OK;
 }
 
 attn_status_t launch_fill_empty(void* o, float* lse, long long rows_o, int d, long long n_lse,
@@ -123,6 +158,30 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
                                      Hq, Hkv, Nq, Nk, d, causal, scale, st);
 }
 
+attn_status_t attn_fwd_test(const void* q, const void* k, const void* v, void* o, float* lse,
+                            int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal, float scale,
+                            const attn_test_options_t* opt, void* stream) {
+    if (opt == nullptr || opt->wait_limit_cycles < 0 || !(opt->rescale_threshold >= 0.f) ||
+        !(opt->rescale_threshold <= 8.f) || opt->softmax_split < 0 || opt->softmax_split > 2)
+        return ATTN_ERR_INVALID;
+    if (B < 0 || Hq < 0 || Nq < 0 || Nk < 0 || Hkv < 1 || d < 1) return ATTN_ERR_INVALID;
+    if (causal != 0 && causal != 1) return ATTN_ERR_INVALID;
+    if (bad_scale(scale)) return ATTN_ERR_INVALID;
+    if (Hq % Hkv != 0) return ATTN_ERR_INVALID;
+    if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+    if (B > 65535) return ATTN_ERR_UNSUPPORTED;
+    if (B == 0 || Hq == 0 || Nq == 0) return ATTN_OK;
+    if (q == nullptr || o == nullptr || lse == nullptr) return ATTN_ERR_INVALID;
+    if (Nk > 0 && (k == nullptr || v == nullptr)) return ATTN_ERR_INVALID;
+    if (misaligned(q, 16) || misaligned(o, 16) || misaligned(lse, 4)) return ATTN_ERR_INVALID;
+    if (Nk > 0 && (misaligned(k, 16) || misaligned(v, 16))) return ATTN_ERR_INVALID;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (Nk == 0)
+        return attn_host::launch_fill_empty(o, lse, (long long)B * Nq * Hq, d,
+                                            (long long)B * Hq * Nq, true, st);
+    return attn_host::launch_fwd_tc(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, causal, scale, st, opt);
+}
+
 int attn_decode_num_splits(int B, int Hq, int Hkv, int Nk, int d) {
     return attn_host::decode_auto_splits(B, Hq, Hkv, Nk, d);
 }
@@ -137,38 +196,47 @@ size_t attn_decode_workspace_bytes(int B, int Hq, int Hkv, int Nk, int d, int nu
     return attn_host::decode_workspace_bytes(B, Hq, d, S);
 }
 
-attn_status_t attn_decode_splitkv(const void* q, const void* k_cache, const void* v_cache, void* o,
-                                  float* lse, int B, int Hq, int Hkv, int Nk, int d, float scale,
-                                  int num_splits, void* workspace, size_t workspace_bytes,
-                                  attn_dtype_t dtype, void* stream) {
-    if (B < 0 || Hq < 0 || Hkv < 1 || Nk < 0 || d < 1 || num_splits < 0) return ATTN_ERR_INVALID;
-    if (dtype != ATTN_BF16 && dtype != ATTN_F32) return ATTN_ERR_INVALID;
-    if (bad_scale(scale)) return ATTN_ERR_INVALID;
-    if (Hq % Hkv != 0) return ATTN_ERR_INVALID;
-    if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
-    if (dtype != ATTN_BF16) return ATTN_ERR_UNSUPPORTED;
-    if (B > 65535 || Hq > 65535) return ATTN_ERR_UNSUPPORTED;
-    if (B == 0 || Hq == 0) return ATTN_OK;
-    if (q == nullptr || o == nullptr || lse == nullptr) return ATTN_ERR_INVALID;
-    if (misaligned(q, 16) || misaligned(o, 16) || misaligned(lse, 4)) return ATTN_ERR_INVALID;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (Nk == 0)
-        return attn_host::launch_fill_empty(o, lse, (long long)B * Hq, d, (long long)B * Hq, true,
-                                            st);
-    if (k_cache == nullptr || v_cache == nullptr) return ATTN_ERR_INVALID;
-    if (misaligned(k_cache, 16) || misaligned(v_cache, 16)) return ATTN_ERR_INVALID;
-    if (num_splits > Nk) return ATTN_ERR_INVALID;
-    int S = num_splits;
-    if (S == 0) S = attn_host::decode_auto_splits(B, Hq, Hkv, Nk, d);
-    if (S < 1) return ATTN_ERR_CUDA;
-    if (S > 65535) return ATTN_ERR_UNSUPPORTED;
+// Runs the split-KV decode after the workspace check (shared by
+// attn_decode_splitkv and attn_decode_test).
+static attn_status_t decode_checked(const void* q, const void* k_cache, const void* v_cache,
+                                    void* o, float* lse, int B, int Hq, int Hkv, int Nk, int d,
+                                    float scale, int num_splits, void* workspace,
+                                    size_t workspace_bytes, attn_dtype_t dtype, void* stream,
+                                    const attn_test_options_t* test) {
+    int S = 0;
+    bool empty = false;
+    const attn_status_t st = attn_host::check_decode_args(q, k_cache, v_cache, o, lse, B, Hq, Hkv,
+                                                          Nk, d, scale, num_splits, dtype, &S, &empty);
+    if (st != ATTN_OK) return st;
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    if (empty)
+        return (B == 0 || Hq == 0) ? ATTN_OK
+                                   : attn_host::launch_fill_empty(o, lse, (long long)B * Hq, d,
+                                                                  (long long)B * Hq, true, cs);
     if (S > 1) {
         if (workspace == nullptr || misaligned(workspace, 16)) return ATTN_ERR_INVALID;
         if (workspace_bytes < attn_host::decode_workspace_bytes(B, Hq, d, S))
             return ATTN_ERR_INVALID;
     }
     return attn_host::launch_decode(q, k_cache, v_cache, o, lse, B, Hq, Hkv, Nk, d, scale, S,
-                                    workspace, st);
+                                    workspace, cs, test);
+}
+
+attn_status_t attn_decode_splitkv(const void* q, const void* k_cache, const void* v_cache, void* o,
+                                  float* lse, int B, int Hq, int Hkv, int Nk, int d, float scale,
+                                  int num_splits, void* workspace, size_t workspace_bytes,
+                                  attn_dtype_t dtype, void* stream) {
+    return decode_checked(q, k_cache, v_cache, o, lse, B, Hq, Hkv, Nk, d, scale, num_splits,
+                          workspace, workspace_bytes, dtype, stream, nullptr);
+}
+
+attn_status_t attn_decode_test(const void* q, const void* k_cache, const void* v_cache, void* o,
+                               float* lse, int B, int Hq, int Hkv, int Nk, int d, float scale,
+                               int num_splits, void* workspace, size_t workspace_bytes,
+                               const attn_test_options_t* opt, void* stream) {
+    if (opt == nullptr || opt->wait_limit_cycles < 0) return ATTN_ERR_INVALID;
+    return decode_checked(q, k_cache, v_cache, o, lse, B, Hq, Hkv, Nk, d, scale, num_splits,
+                          workspace, workspace_bytes, ATTN_BF16, stream, opt);
 }
 
 static bool paged_page_size_ok(int page_size) {

@@ -744,26 +744,13 @@ attn_status_t launch_bwd_impl(const void* q, const void* k, const void* v, const
         !attn_host::encode_bshd_map(&mk, k, B, Nk, Hkv, D, kT, 2) ||
         !attn_host::encode_bshd_map(&mv, v, B, Nk, Hkv, D, kT, 2))
         return ATTN_ERR_CUDA;
-    static std::once_flag once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, LQ::kSmem);
-        if (attr_err == cudaSuccess)
-            attr_err = cudaFuncSetAttribute(bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                            L::kSmem);
-    });
-    if (attr_err != cudaSuccess) return ATTN_ERR_CUDA;
     // The register split inside both kernels assumes exactly kLaunchRegs per
     // thread at launch; refuse to launch a build that differs.
-    static int regs_dq = -1, regs_dkdv = -1;
-    if (regs_dq < 0 || regs_dkdv < 0) {
-        cudaFuncAttributes fa;
-        if (cudaFuncGetAttributes(&fa, bwd_dq_kernel<D>) != cudaSuccess) return ATTN_ERR_CUDA;
-        regs_dq = fa.numRegs;
-        if (cudaFuncGetAttributes(&fa, bwd_dkdv_kernel<D>) != cudaSuccess) return ATTN_ERR_CUDA;
-        regs_dkdv = fa.numRegs;
-    }
-    if (regs_dq != kLaunchRegs || regs_dkdv != kLaunchRegs) return ATTN_ERR_UNSUPPORTED;
+    const attn_host::KernelSetup s_dq = attn_host::kernel_setup<bwd_dq_kernel<D>>(LQ::kSmem);
+    if (s_dq.err != cudaSuccess) return ATTN_ERR_CUDA;
+    const attn_host::KernelSetup s_dkdv = attn_host::kernel_setup<bwd_dkdv_kernel<D>>(L::kSmem);
+    if (s_dkdv.err != cudaSuccess) return ATTN_ERR_CUDA;
+    if (s_dq.num_regs != kLaunchRegs || s_dkdv.num_regs != kLaunchRegs) return ATTN_ERR_UNSUPPORTED;
     BwdParams prm;
     prm.q = static_cast<const __nv_bfloat16*>(q);
     prm.k = static_cast<const __nv_bfloat16*>(k);

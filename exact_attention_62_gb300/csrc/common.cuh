@@ -1,14 +1,56 @@
 // common.cuh -- host-side declarations shared by the translation units of
 // libattn.so (launchers, status words, tensor-map helper).  Not part of the
-// public ABI; the public ABI is include/attn.h.
+// public ABI; that is include/attn.h (and include/attn_test.h for tests).
 #pragma once
 
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <mutex>
+
 #include "../../include/attn.h"
+#include "../../include/attn_test.h"
 
 namespace attn_host {
+
+// Devices a process may drive; per-device caches below are this large.
+constexpr int kMaxDevices = 64;
+
+// One-time launch set-up of a kernel, per device.  The dynamic shared-memory
+// limit that cudaFuncSetAttribute sets belongs to the current device, and the
+// register count is read for the device that will run the kernel, so a
+// process that drives several GPUs (even from one thread) needs both for
+// each device.  The first call on a device does the set-up; later calls
+// return the cached result.  A failed set-up is not cached (the next call
+// retries).
+struct KernelSetup {
+    cudaError_t err;
+    int num_regs;
+};
+
+template <auto Kernel>
+KernelSetup kernel_setup(int dyn_smem_bytes) {
+    static std::mutex mu;
+    static bool done[kMaxDevices] = {};
+    static int regs[kMaxDevices] = {};
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        return {cudaErrorInvalidDevice, 0};
+    std::lock_guard<std::mutex> lock(mu);
+    if (!done[dev]) {
+        if (dyn_smem_bytes > 0) {
+            const cudaError_t e = cudaFuncSetAttribute(
+                Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn_smem_bytes);
+            if (e != cudaSuccess) return {e, 0};
+        }
+        cudaFuncAttributes fa;
+        const cudaError_t e = cudaFuncGetAttributes(&fa, Kernel);
+        if (e != cudaSuccess) return {e, 0};
+        regs[dev] = fa.numRegs;
+        done[dev] = true;
+    }
+    return {cudaSuccess, regs[dev]};
+}
 
 // Encodes a 4-D TMA tensor map over a row-major [B, N, H, d] tensor of
 // `elem_bytes`-byte elements, with a box of (64 elements, 1 head, box_rows,
@@ -19,10 +61,24 @@ bool encode_bshd_map(CUtensorMap* map, const void* base, int B, int N, int H, in
 // Number of SMs of the current device (cached per device); 0 on failure.
 int device_sm_count();
 
-// ---- bf16 tensor-core forward (fwd_tc.cu)
+// The argument checks of attn_decode_splitkv (everything but the workspace),
+// shared by the entry points that run the split-KV decode.  On success *S is
+// the segment count to use (num_splits, or the automatic count for 0) and
+// *empty is set when there is nothing to stream (B, Hq or Nk is 0).
+attn_status_t check_decode_args(const void* q, const void* k_cache, const void* v_cache,
+                                const void* o, const float* lse, int B, int Hq, int Hkv, int Nk,
+                                int d, float scale, int num_splits, attn_dtype_t dtype, int* S,
+                                bool* empty);
+
+// ---- bf16 tensor-core forward (fwd_tc.cu).  `test` is NULL on the
+// production path; attn_fwd_test passes its options.  lse_ld is the number
+// of floats between the LSE rows of consecutive heads (0: Nq, the layout of
+// a whole call; a call over a block of rows of a longer sequence passes that
+// sequence's length).
 attn_status_t launch_fwd_tc(const void* q, const void* k, const void* v, void* o, float* lse,
                             int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal,
-                            float scale, cudaStream_t stream);
+                            float scale, cudaStream_t stream,
+                            const attn_test_options_t* test = nullptr, long long lse_ld = 0);
 cudaError_t fwd_tc_read_status(unsigned* out, bool clear);
 cudaError_t fwd_tc_read_tiles(unsigned long long* out, bool reset);
 
@@ -36,7 +92,8 @@ int decode_auto_splits(int B, int Hq, int Hkv, int Nk, int d);
 size_t decode_workspace_bytes(int B, int Hq, int d, int splits);
 attn_status_t launch_decode(const void* q, const void* k, const void* v, void* o, float* lse,
                             int B, int Hq, int Hkv, int Nk, int d, float scale, int splits,
-                            void* workspace, cudaStream_t stream);
+                            void* workspace, cudaStream_t stream,
+                            const attn_test_options_t* test = nullptr);
 attn_status_t launch_merge(const float* o_parts, const float* lse_parts, int parts,
                            long long rows, int d, void* o, float* lse, bool out_bf16,
                            cudaStream_t stream);

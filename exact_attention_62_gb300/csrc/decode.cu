@@ -59,6 +59,8 @@ struct DecParams {
     float* lse_parts;        // [S, B*Hq]
     int B, Hq, Hkv, Nk, G, splits, seg_len;  // Nk: cache length (paged: the maximum)
     float scale_log2;
+    long long wait_limit;    // bound of every mbarrier wait, SM cycles
+    int skip_load;           // tests only: tile of block (0, 0, 0) that is never loaded (-1: none)
     // paged cache only
     const int* table;        // [B, max_pages] page of each block of page_size keys
     const int* seq_lens;     // [B]
@@ -181,7 +183,8 @@ __global__ void __launch_bounds__(kDecThreads)
             const int ps = p.page_size;
             for (int t = 0; t < ntiles; ++t) {
                 const int st = t % STAGES;
-                if (!mbar_wait_warp(empty_bar(st), ((t / STAGES) & 1) ^ 1, abort_flag, &g_dec_status))
+                if (!mbar_wait_warp(empty_bar(st), ((t / STAGES) & 1) ^ 1, abort_flag, &g_dec_status,
+                                    p.wait_limit))
                     break;
                 const uint32_t kdst = sbase + st * L::kStageBytes;
                 const int key0 = j0 + t * kTileKeys;
@@ -201,10 +204,15 @@ __global__ void __launch_bounds__(kDecThreads)
                 }
             }
         } else if (lane == 0) {
+            // Fault injection for tests: block (0, 0, 0) never loads tile
+            // skip_load, so the waits for it run out (production: -1).
+            const int skip = (blockIdx.x | blockIdx.y | blockIdx.z) == 0 ? p.skip_load : -1;
             for (int t = 0; t < ntiles; ++t) {
                 const int st = t % STAGES;
-                if (!mbar_wait(empty_bar(st), ((t / STAGES) & 1) ^ 1, abort_flag, &g_dec_status))
+                if (!mbar_wait(empty_bar(st), ((t / STAGES) & 1) ^ 1, abort_flag, &g_dec_status,
+                               p.wait_limit))
                     break;
+                if (t == skip) continue;
                 const uint32_t kdst = sbase + st * L::kStageBytes;
                 const int key0 = j0 + t * kTileKeys;
                 if (PAGED) {  // pages of 64 or more keys: one box per panel
@@ -263,7 +271,7 @@ __global__ void __launch_bounds__(kDecThreads)
 
     for (int t = grp; t < ntiles; t += kGroups) {
         const int st = t % STAGES;
-        if (!mbar_wait(full_bar(st), (t / STAGES) & 1, abort_flag, &g_dec_status)) break;
+        if (!mbar_wait(full_bar(st), (t / STAGES) & 1, abort_flag, &g_dec_status, p.wait_limit)) break;
         const uint32_t kb = sbase + st * L::kStageBytes;
         const uint32_t vb = kb + L::kTileBytes;
         // Paged cache: V rows past the sequence hold whatever the pool has
@@ -590,13 +598,8 @@ template <int D, int GC, bool PAGED>
 attn_status_t launch_split(const CUtensorMap& mk, const CUtensorMap& mv, const DecParams& prm,
                            cudaStream_t stream) {
     using L = DecLayout<D, dec_stages<D>(), PAGED>;
-    static std::once_flag once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(decode_split_kernel<D, GC, PAGED>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
-    });
-    if (attr_err != cudaSuccess) return ATTN_ERR_CUDA;
+    if (attn_host::kernel_setup<decode_split_kernel<D, GC, PAGED>>(L::kSmemBytes).err != cudaSuccess)
+        return ATTN_ERR_CUDA;
     dim3 grid(prm.splits, prm.Hq / GC, prm.B);
     decode_split_kernel<D, GC, PAGED><<<grid, kDecThreads, L::kSmemBytes, stream>>>(mk, mv, prm);
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
@@ -617,21 +620,24 @@ attn_status_t launch_split_any(int d, const CUtensorMap& mk, const CUtensorMap& 
                      : launch_split<64, 1, PAGED>(mk, mv, prm, stream);
 }
 
+// Resident split-kernel CTAs per SM on the current device (cached per device).
 template <int D>
 int ctas_per_sm() {
-    static int v = -1;
-    static std::once_flag once;
-    std::call_once(once, [] {
+    static std::mutex mu;
+    static int cache[attn_host::kMaxDevices] = {};
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= attn_host::kMaxDevices) return 1;
+    std::lock_guard<std::mutex> lock(mu);
+    if (cache[dev] == 0) {
         using L = DecLayout<D, dec_stages<D>()>;
         int n = 0;
-        cudaFuncSetAttribute(decode_split_kernel<D, 4, false>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_split_kernel<D, 4, false>,
+        if (attn_host::kernel_setup<decode_split_kernel<D, 4, false>>(L::kSmemBytes).err != cudaSuccess ||
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_split_kernel<D, 4, false>,
                                                           kDecThreads, L::kSmemBytes) != cudaSuccess)
-            n = 1;
-        v = std::max(1, n);
-    });
-    return v;
+            return 1;
+        cache[dev] = std::max(1, n);
+    }
+    return cache[dev];
 }
 
 }  // namespace
@@ -639,14 +645,11 @@ int ctas_per_sm() {
 namespace attn_host {
 
 // Segment count from a CTA-by-wave time model (Lecture 11, sections 6.3-6.4):
-// every CTA streams its segment at min(per-CTA limit, HBM / concurrent CTAs),
-// CTAs beyond one wave wait for the next, each CTA pays a fixed start-up
-// cost, and more than one segment adds the merge kernel.  The smallest
-// modelled time wins; ties go to fewer segments.
-// Segment count that minimises a simple time model: waves of CTAs, each
-// streaming its segment at min(cta_bw, hbm / concurrent CTAs), plus a fixed
-// start-up per wave and the merge.  With single_wave the count is capped so
-// that all CTAs run in one wave.
+// every CTA streams its segment at min(cta_bw, hbm / concurrent CTAs), CTAs
+// beyond one wave wait for the next, each wave pays a fixed start-up, and more
+// than one segment adds the merge.  The smallest modelled time wins; ties go
+// to fewer segments.  With single_wave the count is capped so that all CTAs
+// run in one wave.
 struct SplitModel {
     double cta_bw;       // bytes/s one CTA streams with its ring full
     double hbm;          // bytes/s the whole GPU streams
@@ -706,7 +709,7 @@ size_t decode_workspace_bytes(int B, int Hq, int d, int splits) {
 
 attn_status_t launch_decode(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                             int Hq, int Hkv, int Nk, int d, float scale, int splits,
-                            void* workspace, cudaStream_t stream) {
+                            void* workspace, cudaStream_t stream, const attn_test_options_t* test) {
     CUtensorMap mk, mv;
     if (!encode_bshd_map(&mk, k, B, Nk, Hkv, d, kTileKeys, 2) ||
         !encode_bshd_map(&mv, v, B, Nk, Hkv, d, kTileKeys, 2))
@@ -723,6 +726,8 @@ attn_status_t launch_decode(const void* q, const void* k, const void* v, void* o
     prm.splits = splits;
     prm.seg_len = (Nk + splits - 1) / splits;
     prm.scale_log2 = scale * 1.4426950408889634f;
+    prm.wait_limit = (test && test->wait_limit_cycles > 0) ? test->wait_limit_cycles : kWaitLimitCycles;
+    prm.skip_load = test ? test->skip_load : -1;
     const size_t rows = (size_t)B * Hq;
     if (splits > 1) {
         const size_t o_bytes = (size_t)splits * rows * d * 4;
@@ -793,6 +798,8 @@ attn_status_t launch_decode_paged(const void* q, const void* k_pages, const void
     prm.splits = splits;
     prm.seg_len = paged_seg_len(max_seq_len, splits);
     prm.scale_log2 = scale * 1.4426950408889634f;
+    prm.wait_limit = kWaitLimitCycles;
+    prm.skip_load = -1;
     prm.table = block_table;
     prm.seq_lens = seq_lens;
     prm.page_size = page_size;

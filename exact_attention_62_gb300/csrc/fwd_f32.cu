@@ -183,13 +183,7 @@ template <int D>
 attn_status_t launch_impl(const float* q, const float* k, const float* v, float* o, float* lse,
                           const F32Params& prm, cudaStream_t stream) {
     using L = F32Layout<D>;
-    static std::once_flag once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(fwd_f32_kernel<D>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
-    });
-    if (attr_err != cudaSuccess) return ATTN_ERR_CUDA;
+    if (attn_host::kernel_setup<fwd_f32_kernel<D>>(L::kBytes).err != cudaSuccess) return ATTN_ERR_CUDA;
     const long long qtiles = (prm.Nq + kRows - 1) / kRows;
     if (qtiles > 0x7fffffffLL || prm.Hq > 65535 || prm.B > 65535) return ATTN_ERR_UNSUPPORTED;
     dim3 grid((unsigned)qtiles, prm.Hq, prm.B);

@@ -8,15 +8,28 @@
 // back of chunk c - 1 proceed while chunk c computes.  Sequences are
 // independent in the forward, so every output element is the one a single
 // attn_fwd call over the whole batch writes, bit for bit.
+//
+// A single bf16 sequence (B == 1) is cut by query rows instead.  Chunk c
+// covers rows [r_c, r_c+1) (multiples of 256, the forward kernel's work
+// unit) and needs keys [0, e_c): all Nk without a mask, e_c = r_c+1 + (Nk -
+// Nq) with the bottom-right causal mask (Nq <= Nk), a prefix of the cache.
+// The keys past the previous chunk's prefix are copied with the chunk.  The
+// chunk's forward is the problem restricted to its rows: its row i (row
+// r_c + i of the sequence) sees key j iff j <= i + (e_c - (r_c+1 - r_c)) =
+// (r_c + i) + (Nk - Nq), the same keys as in one call over all rows, and
+// every row is computed by the same arithmetic, so the results are again
+// equal bit for bit.  The chunk's LSE rows are strided by Nq (one run per
+// head), so they are read back with one 2-D copy.
 #include <cuda_runtime.h>
 
 #include <cmath>
 
-#include "attn.h"
+#include "common.cuh"
 
 namespace {
 
 constexpr int kMaxChunks = 16;
+constexpr int kRowUnit = 256;  // query rows of one work unit of the forward kernel
 constexpr int kEvents = 2 * kMaxChunks + 2;
 
 // Events the pipeline records between its streams: created once per host
@@ -74,9 +87,12 @@ extern "C" attn_status_t attn_fwd_host(const void* q_h, const void* k_h, const v
     if (misaligned16(q_d) || misaligned16(o_d) || (Nk > 0 && (misaligned16(k_d) || misaligned16(v_d))) ||
         (reinterpret_cast<unsigned long long>(lse_d) & 3ull) != 0)
         return ATTN_ERR_INVALID;
-    int n = chunks == 0 ? (B < 4 ? B : 4) : chunks;
-    if (n > B) n = B;
+    // One bf16 sequence: chunks of query rows (see the top of this file).
+    const bool by_rows = B == 1 && dtype == ATTN_BF16 && Nk > 0 && (!causal || Nq <= Nk);
+    const int row_units = (Nq + kRowUnit - 1) / kRowUnit;
+    int n = chunks == 0 ? (by_rows ? 4 : (B < 4 ? B : 4)) : chunks;
     if (n > kMaxChunks) return ATTN_ERR_UNSUPPORTED;
+    if (n > (by_rows ? row_units : B)) n = by_rows ? row_units : B;
 
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || !t_events.get(dev)) return ATTN_ERR_CUDA;
@@ -106,7 +122,48 @@ extern "C" attn_status_t attn_fwd_host(const void* q_h, const void* k_h, const v
     if (up != st && cudaStreamWaitEvent(up, ev_start, 0) != cudaSuccess) return ATTN_ERR_CUDA;
     if (down != st && cudaStreamWaitEvent(down, ev_start, 0) != cudaSuccess) return ATTN_ERR_CUDA;
 
-    for (int c = 0; c < n; ++c) {
+    if (by_rows) {
+        const size_t q_row = (size_t)Hq * d * esz;    // bytes of one query row (all heads)
+        const size_t kv_row = (size_t)Hkv * d * esz;  // bytes of one key row
+        long long k_done = 0;                         // keys already sent
+        for (int c = 0; c < n; ++c) {
+            const int r0 = (int)((long long)row_units * c / n) * kRowUnit;
+            const int r1 = c + 1 == n ? Nq : (int)((long long)row_units * (c + 1) / n) * kRowUnit;
+            const long long k_end = causal ? (long long)r1 + (Nk - Nq) : Nk;
+            if (cudaMemcpyAsync(qd + r0 * q_row, qh + r0 * q_row, (size_t)(r1 - r0) * q_row,
+                                cudaMemcpyHostToDevice, up) != cudaSuccess)
+                return ATTN_ERR_CUDA;
+            if (k_end > k_done) {
+                const size_t off = (size_t)k_done * kv_row, len = (size_t)(k_end - k_done) * kv_row;
+                if (cudaMemcpyAsync(kd + off, kh + off, len, cudaMemcpyHostToDevice, up) != cudaSuccess ||
+                    cudaMemcpyAsync(vd + off, vh + off, len, cudaMemcpyHostToDevice, up) != cudaSuccess)
+                    return ATTN_ERR_CUDA;
+                k_done = k_end;
+            }
+            cudaEvent_t ev_in = ev[2 * c], ev_out = ev[2 * c + 1];
+            if (up != st) {
+                if (cudaEventRecord(ev_in, up) != cudaSuccess || cudaStreamWaitEvent(st, ev_in, 0) != cudaSuccess)
+                    return ATTN_ERR_CUDA;
+            }
+            const attn_status_t s = attn_host::launch_fwd_tc(qd + r0 * q_row, kd, vd, od + r0 * q_row,
+                                                             reinterpret_cast<float*>(ld) + r0, 1, Hq, Hkv,
+                                                             r1 - r0, (int)k_end, d, causal, scale, st,
+                                                             nullptr, Nq);
+            if (s != ATTN_OK) return s;
+            if (down != st) {
+                if (cudaEventRecord(ev_out, st) != cudaSuccess || cudaStreamWaitEvent(down, ev_out, 0) != cudaSuccess)
+                    return ATTN_ERR_CUDA;
+            }
+            if (cudaMemcpyAsync(oh + r0 * q_row, od + r0 * q_row, (size_t)(r1 - r0) * q_row,
+                                cudaMemcpyDeviceToHost, down) != cudaSuccess ||
+                cudaMemcpy2DAsync(lh + (size_t)r0 * sizeof(float), (size_t)Nq * sizeof(float),
+                                  ld + (size_t)r0 * sizeof(float), (size_t)Nq * sizeof(float),
+                                  (size_t)(r1 - r0) * sizeof(float), (size_t)Hq, cudaMemcpyDeviceToHost,
+                                  down) != cudaSuccess)
+                return ATTN_ERR_CUDA;
+        }
+    }
+    for (int c = 0; c < n && !by_rows; ++c) {
         const int b0 = (int)((long long)B * c / n), b1 = (int)((long long)B * (c + 1) / n);
         const int nb = b1 - b0;
         if (cudaMemcpyAsync(qd + b0 * q_seq, qh + b0 * q_seq, nb * q_seq, cudaMemcpyHostToDevice, up) !=

@@ -13,7 +13,8 @@
 
 namespace attn_dev {
 
-// A bounded wait gives up after this many SM clock cycles (~2 s at 2 GHz).
+// A bounded wait gives up after this many SM clock cycles (~2 s at 2 GHz)
+// unless the launch passes another bound (tests shorten it).
 constexpr long long kWaitLimitCycles = 1ll << 32;
 
 // Bits of the per-family device status word.
@@ -56,18 +57,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Waits for the phase with the given parity to complete.  Every wait is
-// bounded: after kWaitLimitCycles it sets the CTA's abort flag and the
-// family's device status word and returns false.  Once the abort flag is set,
-// every later wait in the CTA returns false at once, so all roles drain to
-// the CTA's teardown instead of hanging.
+// bounded: after `limit` cycles it sets the CTA's abort flag and the family's
+// device status word and returns false.  Once the abort flag is set, every
+// later wait in the CTA returns false at once, so all roles drain to the
+// CTA's teardown instead of hanging.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                          unsigned* status_word) {
+                                          unsigned* status_word, long long limit = kWaitLimitCycles) {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
         if (*abort_flag) return false;
-        if (clock64() - t0 > kWaitLimitCycles) {
+        if (clock64() - t0 > limit) {
             *abort_flag = 1;
             atomicOr(status_word, kStatusTimeout);
             return false;
@@ -246,13 +247,14 @@ __host__ __device__ constexpr uint32_t sdesc_sw128_hi(uint32_t sbo) {
 // ends once every lane has itself observed the completed phase (completion is
 // monotonic, so they agree within one more poll).
 __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity,
-                                               volatile int* abort_flag, unsigned* status_word) {
+                                               volatile int* abort_flag, unsigned* status_word,
+                                               long long limit = kWaitLimitCycles) {
     if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
     const long long t0 = clock64();
     while (true) {
         if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
         if (__any_sync(0xffffffffu, *abort_flag != 0)) return false;
-        if (__any_sync(0xffffffffu, clock64() - t0 > kWaitLimitCycles)) {
+        if (__any_sync(0xffffffffu, clock64() - t0 > limit)) {
             if ((threadIdx.x & 31) == 0) {
                 *abort_flag = 1;
                 atomicOr(status_word, kStatusTimeout);

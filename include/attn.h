@@ -88,13 +88,20 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o,
  *            host memory is accepted).
  *   q_d, k_d, v_d, o_d, lse_d  device buffers of the same full sizes,
  *            caller-owned, aligned as for attn_fwd.
- *   chunks   0 = min(B, 4); else the number of batch chunks, 1..16 (at most
- *            B).  Chunk c holds sequences [B c / n, B (c + 1) / n).
+ *   chunks   the number of chunks n, 1..16; 0 = min(B, 4) for a batch and
+ *            4 for one sequence.  With B > 1 (or fp32 inputs, or a causal
+ *            Nq > Nk) chunk c holds sequences [B c / n, B (c + 1) / n),
+ *            n <= B.  With one bf16 sequence chunk c holds the query rows
+ *            [256 floor(U c / n), 256 floor(U (c + 1) / n)) (U = ceil(Nq /
+ *            256), n <= U; the last chunk ends at Nq) together with the keys
+ *            those rows may see that no earlier chunk sent: all Nk keys go
+ *            with the first chunk without a mask, keys up to the chunk's last
+ *            row + (Nk - Nq) with the causal mask.
  *   stream   the compute stream; h2d_stream and d2h_stream carry the two
  *            copy directions (NULL: the compute stream, i.e. no overlap).
- * Chunk c is copied host -> device on h2d_stream, computed by attn_fwd on
- * `stream` once it has arrived, and copied back on d2h_stream once
- * computed, so chunk c + 1 moves in while chunk c computes.  The side
+ * Chunk c is copied host -> device on h2d_stream, computed on `stream` once
+ * it has arrived, and copied back on d2h_stream once computed, so chunk c + 1
+ * moves in while chunk c computes.  The side
  * streams first wait for the work already queued on `stream`, and `stream`
  * finally waits for the last read back: once `stream` has completed, o_h and
  * lse_h hold the results, equal bit for bit to one attn_fwd call over the
@@ -181,8 +188,11 @@ attn_status_t attn_decode_splitkv(const void* q, const void* k_cache,
  *
  *   - It allocates and frees nothing.
  *   - Its first call on a device looks up the scratch area's device address
- *     (cudaGetSymbolAddress, with that device current) and caches it; make
- *     that first call before any stream capture.
+ *     (cudaGetSymbolAddress, with that device current) and caches it with
+ *     the ID of the device's current context; make that first call before
+ *     any stream capture.  After a device reset (a new context, in which the
+ *     array may sit elsewhere) the next call looks the address up again, so
+ *     that call too belongs before any capture.
  *   - Sizes whose partials need more than ATTN_DECODE_STATIC_SCRATCH_BYTES
  *     (see attn_decode_workspace_bytes) return ATTN_ERR_UNSUPPORTED and
  *     launch nothing; use attn_decode_splitkv with a larger workspace instead.

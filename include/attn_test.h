@@ -1,0 +1,88 @@
+/*
+ * attn_test.h -- entry points of libattn.so for tests and measurements
+ * only.  A production caller uses include/attn.h; nothing here is needed to
+ * compute attention.
+ *
+ * They run the same kernels as attn_fwd and attn_decode_splitkv with
+ * settings the production entry points keep fixed:
+ *   - variants of the forward used to check that alternative formulations
+ *     give the same answer and to measure what they cost (P staged in
+ *     shared memory, part of the exponentials on the FMA pipe, a
+ *     conditional-rescale threshold);
+ *   - the bound of every device-side wait, and a fault injection that makes
+ *     one wait run out on purpose, so that tests can check the error path
+ *     that keeps a lost signal from hanging a GPU.
+ *
+ * The injection stops one TMA load from being issued: the producer of
+ * block 0 posts no byte count and issues no copy for that ring position.
+ * The wait for it then ends when the bound runs out; the kernel sets its
+ * abort flag, every role of that block drains to the block's teardown (TMEM
+ * freed, no copy or MMA in flight), the status word records the timeout and
+ * the launch completes normally.  attn_check_device_status() then returns
+ * ATTN_ERR_TIMEOUT and clears the word; the outputs of such a call are
+ * unspecified, and later calls are unaffected.
+ */
+#ifndef EXACT_ATTENTION_GB300_ATTN_TEST_H
+#define EXACT_ATTENTION_GB300_ATTN_TEST_H
+
+#include "attn.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct {
+    /* forward only: 1 = P goes through shared memory and the
+     * shared-memory form of the P V product (the default keeps P in
+     * tensor memory) */
+    int p_in_smem;
+    /* forward only: 1 = every fourth pair of exponentials is computed by a
+     * polynomial on the FMA pipe instead of the MUFU unit (software exp2 of
+     * the FA4 section of the course index) */
+    int exp2_poly;
+    /* forward only: conditional-rescale threshold in log2 units, 0..8 (the
+     * production value is 0: the reference max moves whenever it grows) */
+    float rescale_threshold;
+    /* bound of every device-side wait in SM clock cycles; 0 = the
+     * production bound (2^32 cycles, about 2 s) */
+    long long wait_limit_cycles;
+    /* -1 = none.  Otherwise the TMA producer of block 0 skips this load:
+     * forward, the K and V tiles at this position of the block's key ring
+     * (0 = the first key tile it loads); decode, this tile of the block's
+     * segment (0 = its first 64 keys). */
+    int skip_load;
+    /* forward only: softmax warpgroups per 128-row query tile, 1 (one
+     * thread per row and all 128 key columns of a key tile) or 2 (two
+     * threads per row, 64 key columns each); 0 = the production choice (1).
+     * p_in_smem and exp2_poly imply 1. */
+    int softmax_split;
+} attn_test_options_t;
+
+/*
+ * attn_fwd_test -- attn_fwd (ATTN_BF16 only) with the options above.  Same
+ * arguments, layouts and errors as attn_fwd, plus ATTN_ERR_INVALID for a
+ * NULL `opt`, a threshold outside [0, 8], a negative wait bound or a
+ * softmax_split other than 0, 1 or 2.
+ */
+attn_status_t attn_fwd_test(const void* q, const void* k, const void* v, void* o,
+                            float* lse, int B, int Hq, int Hkv, int Nq, int Nk, int d,
+                            int causal, float scale, const attn_test_options_t* opt,
+                            void* stream);
+
+/*
+ * attn_decode_test -- attn_decode_splitkv with the wait bound and the load
+ * injection of `opt` (the forward-only fields are ignored).  Same
+ * arguments and errors as attn_decode_splitkv, plus ATTN_ERR_INVALID for a
+ * NULL `opt` or a negative wait bound.
+ */
+attn_status_t attn_decode_test(const void* q, const void* k_cache, const void* v_cache,
+                               void* o, float* lse, int B, int Hq, int Hkv, int Nk, int d,
+                               float scale, int num_splits, void* workspace,
+                               size_t workspace_bytes, const attn_test_options_t* opt,
+                               void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EXACT_ATTENTION_GB300_ATTN_TEST_H */

@@ -8,8 +8,9 @@ import pytest
 
 import exact_attention_62_gb300 as pkg
 
-HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
-                      "include", "attn.h")
+INCLUDE = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
+HEADER = os.path.join(INCLUDE, "attn.h")
+TEST_HEADER = os.path.join(INCLUDE, "attn_test.h")
 
 OK, INVALID, UNSUPPORTED, CUDA, TIMEOUT = range(5)
 BF16, F32 = 0, 1
@@ -19,8 +20,8 @@ FAKE = ctypes.c_void_p(0x7f0000000000)
 FAKE_LSE = ctypes.c_void_p(0x7f0000100000)
 
 
-def declared_functions():
-    text = open(HEADER).read()
+def declared_functions(header=HEADER):
+    text = open(header).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     return sorted(set(re.findall(r"\b(attn_[a-z0-9_]+)\s*\(", text)))
 
@@ -34,8 +35,12 @@ def test_header_declares_the_documented_set():
     assert declared_functions() == sorted(pkg.EXPORTED_SYMBOLS)
 
 
+def test_test_header_declares_the_test_entry_points():
+    assert declared_functions(TEST_HEADER) == sorted(pkg.TEST_SYMBOLS)
+
+
 def test_every_declared_symbol_is_exported(L):
-    for name in declared_functions():
+    for name in declared_functions() + declared_functions(TEST_HEADER):
         assert hasattr(L, name), name
 
 
@@ -206,3 +211,41 @@ def test_fp8_entry_points_reject_bad_arguments(L):
     assert f8(causal=3) == INVALID
     assert f8(Hq=3, Hkv=2) == INVALID
     assert f8(B=0) == OK
+
+
+def test_test_entry_points_reject_bad_arguments(L):
+    """The test-only entry points check their options and then their
+    arguments as the production calls do, before any launch."""
+    opt = pkg.AttnTestOptions()
+    f = lambda o=ctypes.byref(opt), d=64, Hq=2, Hkv=1, scale=0.125: L.attn_fwd_test(
+        FAKE, FAKE, FAKE, FAKE, FAKE_LSE, 1, Hq, Hkv, 8, 8, d, 0, scale, o, None)
+    assert f(o=None) == INVALID
+    assert f(d=96) == UNSUPPORTED
+    assert f(Hq=3, Hkv=2) == INVALID
+    assert f(scale=0.0) == INVALID
+    for bad in (pkg.AttnTestOptions(rescale_threshold=9.0), pkg.AttnTestOptions(rescale_threshold=-1.0),
+                pkg.AttnTestOptions(rescale_threshold=float("nan")),
+                pkg.AttnTestOptions(wait_limit_cycles=-5)):
+        assert f(o=ctypes.byref(bad)) == INVALID
+    dt = lambda o=ctypes.byref(opt), S=4, ws=None: L.attn_decode_test(
+        FAKE, FAKE, FAKE, FAKE, FAKE_LSE, 1, 8, 2, 100, 128, 0.1, S, ws, 0, o, None)
+    assert dt(o=None) == INVALID
+    assert dt(o=ctypes.byref(pkg.AttnTestOptions(wait_limit_cycles=-1))) == INVALID
+    assert dt(S=101) == INVALID    # more segments than keys
+    assert dt(S=4) == INVALID      # several segments need a workspace
+
+
+def test_static_decode_reports_invalid_arguments_before_scratch_size(L):
+    """attn_decode_splitkv_static runs the argument checks of
+    attn_decode_splitkv first: a call that is invalid is reported as invalid
+    even when its partials would not fit the built-in scratch area."""
+    st = lambda B=64, Hq=32, Hkv=8, Nk=1000, S=2000, scale=0.1, q=FAKE: L.attn_decode_splitkv_static(
+        q, FAKE, FAKE, FAKE, FAKE_LSE, B, Hq, Hkv, Nk, 128, scale, S, BF16, None)
+    assert st() == INVALID                          # num_splits > Nk
+    assert st(S=64, scale=float("nan")) == INVALID  # bad scale
+    assert st(S=64, q=None) == INVALID
+    assert st(S=64, Hq=30, Hkv=8) == INVALID        # Hq % Hkv != 0
+    # a valid call whose partials exceed the scratch area is refused as unsupported
+    need = pkg.attn_decode_workspace_bytes(64, 32, 8, 100000, 128, 64)
+    assert need > pkg.DECODE_STATIC_SCRATCH_BYTES
+    assert st(Nk=100000, S=64) == UNSUPPORTED

@@ -2,8 +2,6 @@
 import json
 import math
 import os
-import subprocess
-import sys
 
 import numpy as np
 import pytest
@@ -84,9 +82,13 @@ def test_empty_key_set(attn):
     assert torch.all(o == 0) and torch.all(lse == float("-inf"))
 
 
-def _sampled_full_size(attn, oracle_mod, B, Hq, Hkv, N, d, causal, seed, n_rows):
-    """Full-size run (the benchmark's launch configuration), checked on
-    sampled rows that the oracle computes one by one."""
+def _sampled_full_size(attn, oracle_mod, B, Hq, Hkv, N, d, causal, seed, n_rows, groups):
+    """Full-size run (the benchmark's launch configuration), checked against
+    the oracle (a) on sampled rows across all heads, computed one by one,
+    and (b) on whole KV groups: every row of the query heads that share the
+    KV heads in `groups` (batch, kv head), against the oracle's forward of
+    that sub-problem, which is exact because KV groups are independent
+    (Lecture 11, section 4.1, theorem 1: the tiled result is the exact one)."""
     q, k, v = make_qkv(B, Hq, Hkv, N, N, d, seed)
     scale = 1.0 / math.sqrt(d)
     o, lse = attn.attn_fwd(q.to(DEV), k.to(DEV), v.to(DEV), causal, scale)
@@ -99,18 +101,27 @@ def _sampled_full_size(attn, oracle_mod, B, Hq, Hkv, N, d, causal, seed, n_rows)
     o_sel = torch.stack([o[b, i, h] for b, h, i in rows])
     l_sel = torch.stack([lse[b, h, i] for b, h, i in rows])
     compare(o_sel, l_sel, o_ref, lse_ref, torch.bfloat16, "full-size sampled")
-    lse_all = lse.float()
-    assert torch.isfinite(lse_all).all()
+    assert torch.isfinite(lse.float()).all()
+    G = Hq // Hkv
+    for b, g in groups:
+        hs = slice(g * G, (g + 1) * G)
+        og_ref, lg_ref = oracle_mod.attn_fwd(q[b:b + 1, :, hs], k[b:b + 1, :, g:g + 1],
+                                             v[b:b + 1, :, g:g + 1], causal, scale)
+        compare(o[b:b + 1, :, hs], lse[b:b + 1, hs], og_ref, lg_ref, torch.bfloat16,
+                "full-size whole KV group (b=%d, g=%d): %d heads x %d rows" % (b, g, G, N))
 
 
 def test_training_prefill_full_size(attn, oracle_mod):
-    """B=4, Hq=Hkv=16, N=4096, d=128, causal."""
-    _sampled_full_size(attn, oracle_mod, 4, 16, 16, 4096, 128, True, seed=2, n_rows=384)
+    """B=4, Hq=Hkv=16, N=4096, d=128, causal; two whole heads checked."""
+    _sampled_full_size(attn, oracle_mod, 4, 16, 16, 4096, 128, True, seed=2, n_rows=384,
+                       groups=[(0, 0), (3, 15)])
 
 
 def test_long_sequence_gqa_full_size(attn, oracle_mod):
-    """B=1, Hq=32, Hkv=8, N=16384, d=128, causal."""
-    _sampled_full_size(attn, oracle_mod, 1, 32, 8, 16384, 128, True, seed=3, n_rows=192)
+    """B=1, Hq=32, Hkv=8, N=16384, d=128, causal; one whole KV group (four
+    query heads of 16384 rows) checked."""
+    _sampled_full_size(attn, oracle_mod, 1, 32, 8, 16384, 128, True, seed=3, n_rows=192,
+                       groups=[(0, 5)])
 
 
 def test_causal_tile_fraction(attn):
@@ -131,33 +142,33 @@ def test_causal_tile_fraction(attn):
     assert attn.attn_read_tile_counter(reset=True) == T * T
 
 
-@pytest.mark.parametrize("env", [{"ATTN_FWD_P_SMEM": "1"}, {"ATTN_FWD_RESCALE_THRESHOLD": "2"},
-                                 {"ATTN_FWD_EXP2_POLY": "1"}],
+@pytest.mark.parametrize("opts", [{"p_in_smem": 1}, {"rescale_threshold": 2.0}, {"exp2_poly": 1}],
                          ids=["p_in_smem", "rescale_threshold_2", "exp2_polynomial"])
-def test_kernel_variants(attn, env):
-    """The debugging variant that stages P in shared memory, the forward with a
-    conditional-rescale threshold of 2 (a stale reference max within a factor 4
-    of the true one), and the forward computing a quarter of its exp2 with the
-    polynomial instead of MUFU give the oracle's answer within tolerance,
-    including causal rows with no allowed key (Nq > Nk)."""
-    code = r"""
-import math, torch, sys
-sys.path.insert(0, %r); sys.path.insert(0, %r)
-import exact_attention_62_gb300 as attn, oracle
-from exact_attention_62_gb300.inputs import make_qkv
-from parity import compare
-cases = [(2, 3, 300, 300, 64, True, 1.0), (1, 2, 520, 520, 128, True, 1.0),
-         (1, 2, 257, 257, 128, False, 1.0), (1, 2, 700, 700, 64, True, 8.0),
-         (1, 2, 1000, 300, 128, True, 1.0), (1, 2, 1000, 300, 64, True, 1.0)]
-for (B, H, Nq, Nk, d, c, qs) in cases:
-    q, k, v = make_qkv(B, H, H, Nq, Nk, d, 9, q_scale=qs)
-    o, l = attn.attn_fwd(q.cuda(), k.cuda(), v.cuda(), c, 1 / math.sqrt(d))
+def test_kernel_variants(attn, oracle_mod, opts):
+    """Through the test-only entry point attn_fwd_test: the debugging variant
+    that stages P in shared memory, the forward with a conditional-rescale
+    threshold of 2 (a stale reference max within a factor 4 of the true one),
+    and the forward computing a quarter of its exp2 with the polynomial
+    instead of MUFU give the oracle's answer within tolerance, including
+    causal rows with no allowed key (Nq > Nk)."""
+    cases = [(2, 3, 300, 300, 64, True, 1.0), (1, 2, 520, 520, 128, True, 1.0),
+             (1, 2, 257, 257, 128, False, 1.0), (1, 2, 700, 700, 64, True, 8.0),
+             (1, 2, 1000, 300, 128, True, 1.0), (1, 2, 1000, 300, 64, True, 1.0)]
+    opt = attn.AttnTestOptions(**opts)
+    for (B, H, Nq, Nk, d, c, qs) in cases:
+        q, k, v = make_qkv(B, H, H, Nq, Nk, d, 9, q_scale=qs)
+        o, l = attn.attn_fwd_test(q.to(DEV), k.to(DEV), v.to(DEV), c, 1 / math.sqrt(d), opt)
+        torch.cuda.synchronize()
+        ro, rl = oracle_mod.attn_fwd(q, k, v, c, 1 / math.sqrt(d))
+        compare(o, l, ro, rl, torch.bfloat16, "variant %s" % opts)
+    assert attn.attn_check_device_status() == 0
+
+
+def test_test_entry_point_defaults_equal_production(attn):
+    """attn_fwd_test with default options runs the production kernel: the
+    same bits as attn_fwd."""
+    q, k, v = (x.to(DEV) for x in make_qkv(2, 4, 2, 700, 700, 128, 11))
+    o1, l1 = attn.attn_fwd(q, k, v, True, 0.088)
+    o2, l2 = attn.attn_fwd_test(q, k, v, True, 0.088, attn.AttnTestOptions())
     torch.cuda.synchronize()
-    ro, rl = oracle.attn_fwd(q, k, v, c, 1 / math.sqrt(d))
-    compare(o, l, ro, rl, torch.bfloat16, "variant")
-assert attn.attn_check_device_status() == 0
-print("ok")
-""" % (os.path.dirname(os.path.dirname(os.path.abspath(__file__))), os.path.dirname(os.path.abspath(__file__)))
-    r = subprocess.run([sys.executable, "-c", code], env=dict(os.environ, **env),
-                       capture_output=True, text=True, timeout=600)
-    assert r.returncode == 0 and "ok" in r.stdout, r.stdout + r.stderr
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)

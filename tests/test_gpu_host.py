@@ -43,6 +43,25 @@ def test_fwd_host_equals_device_call(attn, B, Hq, Hkv, N, d, causal, chunks, pin
     assert torch.equal(o, ro) and torch.equal(lse, rl)
 
 
+@pytest.mark.parametrize("Hq,Hkv,Nq,Nk,d,causal,chunks", [
+    (8, 2, 1300, 1300, 128, True, 0),   # causal, 6 units of 256 rows in 4 chunks
+    (4, 4, 1300, 1300, 64, False, 3),   # no mask: every key goes with the first chunk
+    (8, 4, 700, 1500, 128, True, 0),    # Nq < Nk: bottom-right causal, keys in prefixes
+    (4, 2, 1024, 1024, 128, True, 16),  # more chunks asked than units: one per unit
+    (4, 2, 900, 300, 128, True, 0),     # Nq > Nk causal: whole-sequence path
+])
+def test_fwd_host_one_sequence_in_row_chunks(attn, Hq, Hkv, Nq, Nk, d, causal, chunks):
+    """One sequence is cut by query rows (with the key prefix each chunk's
+    rows may see); the result equals one device call bit for bit."""
+    scale = 1.0 / math.sqrt(d)
+    q, k, v = (t.pin_memory() for t in make_qkv(1, Hq, Hkv, Nq, Nk, d, 46 + Nq))
+    o, lse = attn.attn_fwd_host(q, k, v, causal, scale, chunks=chunks)
+    torch.cuda.synchronize()
+    assert attn.attn_check_device_status() == 0
+    ro, rl = _device_reference(attn, q, k, v, causal, scale)
+    assert torch.equal(o, ro) and torch.equal(lse, rl)
+
+
 def test_fwd_host_matches_oracle(attn, oracle_mod):
     B, Hq, Hkv, N, d = 3, 4, 2, 333, 128
     scale = 1.0 / math.sqrt(d)

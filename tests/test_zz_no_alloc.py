@@ -5,9 +5,11 @@ framework's allocator, a pre-planned memory budget, or a latency-critical path
 where an allocation could block or synchronise) use this entry point instead
 of attn_decode_splitkv: it keeps the per-segment partials in a scratch area
 built into the library.  These tests call it through the C ABI and check that
-it returns what the workspace-taking entry point returns, on two calls in a
-row with different inputs (the shared scratch area is reused), and that sizes
-needing more scratch than the library holds are refused before any launch.
+it returns what the workspace-taking entry point returns, bit for bit (the
+same kernels with the same segment count; a read of stale partials would
+show), on two calls in a row with different inputs (the shared scratch area
+is reused), and that sizes needing more scratch than the library holds are
+refused before any launch, after the usual argument checks.
 
 This file is collected last on purpose.
 """
@@ -22,7 +24,7 @@ from exact_attention_62_gb300.inputs import make_qkv
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
-OK, UNSUPPORTED = 0, 2
+OK, INVALID, UNSUPPORTED = 0, 1, 2
 BF16 = 0
 
 
@@ -53,9 +55,8 @@ def test_static_scratch_matches_workspace_entry_point(attn, B, Hq, Hkv, Nk, d, S
         assert _static_call(L, q, k, v, o, lse, S, scale) == OK
         torch.cuda.synchronize()
         assert attn.attn_check_device_status() == 0
-        d_o = (o.float() - o_ref.float()).abs().max().item()
-        d_l = (lse - l_ref).abs().max().item()
-        assert d_o <= 2e-2 and d_l <= 1e-3, (call, d_o, d_l)
+        assert torch.equal(o, o_ref), (call, (o.float() - o_ref.float()).abs().max().item())
+        assert torch.equal(lse, l_ref), (call, (lse - l_ref).abs().max().item())
 
 
 def test_static_scratch_refuses_oversized_requests(attn):
@@ -70,5 +71,21 @@ def test_static_scratch_refuses_oversized_requests(attn):
                                       ctypes.c_void_p(lse.data_ptr()), B, Hq, Hkv, Nk, d,
                                       0.1, S, BF16, None)
     assert st == UNSUPPORTED
+    torch.cuda.synchronize()
+    assert torch.all(o == 7.0) and torch.all(lse == 7.0)
+
+
+def test_static_scratch_checks_arguments_first(attn):
+    """An invalid call (more segments than keys) is reported as invalid, not
+    as too large for the scratch area, and writes nothing."""
+    L = attn.lib()
+    B, Hq, Hkv, Nk, d, S = 64, 32, 8, 1000, 128, 2000
+    o = torch.full((B, 1, Hq, d), 7.0, dtype=torch.bfloat16, device=DEV)
+    lse = torch.full((B, Hq), 7.0, dtype=torch.float32, device=DEV)
+    fake = ctypes.c_void_p(0x7f0000000000)  # never dereferenced: refused first
+    st = L.attn_decode_splitkv_static(fake, fake, fake, ctypes.c_void_p(o.data_ptr()),
+                                      ctypes.c_void_p(lse.data_ptr()), B, Hq, Hkv, Nk, d,
+                                      0.1, S, BF16, None)
+    assert st == INVALID
     torch.cuda.synchronize()
     assert torch.all(o == 7.0) and torch.all(lse == 7.0)
