@@ -52,6 +52,10 @@ PREFILL = {
     "ragged_causal": (8, 12, 12, 1000, 1000, 64, True),
     "training_prefill": (4, 16, 16, 4096, 4096, 128, True),
     "long_sequence": (1, 32, 8, 16384, 16384, 128, True),
+    # d = 64 versions of the two large shapes (for measuring the d = 64 kernel;
+    # not workloads of the report)
+    "training_prefill_d64": (4, 16, 16, 4096, 4096, 64, True),
+    "long_sequence_d64": (1, 32, 8, 16384, 16384, 64, True),
 }
 DECODE = {
     "decode_64k": (1, 32, 8, 65536, 128),

@@ -162,7 +162,7 @@ attn_status_t attn_fwd_test(const void* q, const void* k, const void* v, void* o
                             int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal, float scale,
                             const attn_test_options_t* opt, void* stream) {
     if (opt == nullptr || opt->wait_limit_cycles < 0 || !(opt->rescale_threshold >= 0.f) ||
-        !(opt->rescale_threshold <= 8.f) || opt->softmax_split < 0 || opt->softmax_split > 2)
+        !(opt->rescale_threshold <= 8.f))
         return ATTN_ERR_INVALID;
     if (B < 0 || Hq < 0 || Nq < 0 || Nk < 0 || Hkv < 1 || d < 1) return ATTN_ERR_INVALID;
     if (causal != 0 && causal != 1) return ATTN_ERR_INVALID;

@@ -84,25 +84,18 @@ __device__ unsigned long long g_fwd_tiles = 0;
 constexpr int kBM = 128;        // query rows per tile (one TMEM lane each)
 constexpr int kBN = 128;        // keys per tile
 constexpr int kQT = 2;          // query tiles per unit
-// Threads and register split of a kernel with SPLIT softmax warpgroups per
-// query tile.  SPLIT = 1: one thread per row of the tile, owning all 128 key
-// columns of a key tile; SPLIT = 2: two threads per row, 64 key columns each
-// (the two halves of a tile exchange their row maxima once per key tile).
-// Warpgroup 0 = TMA producer (warp 0), MMA issuer (warp 1) and two idle
-// warps; then the softmax warpgroups of query tile 0, then of tile 1.  The
-// kernel is compiled for kLaunchRegs per thread (the most its thread count
-// allows: an SM sub-partition has 16384 registers); warpgroup 0 gives
-// registers back and the softmax warpgroups take them, so 128 kRegsWG0 +
-// 256 SPLIT kRegsSoftmax must not exceed kThreads kLaunchRegs
-// (SPLIT 1: 63488 <= 64512; SPLIT 2: 61440 <= 61440).
-template <int SPLIT>
-struct Warps {
-    static constexpr int kThreads = 128 + 256 * SPLIT;
-    static constexpr int kLaunchRegs = SPLIT == 1 ? 168 : 96;
-    static constexpr int kRegsWG0 = SPLIT == 1 ? 112 : 64;
-    static constexpr int kRegsSoftmax = SPLIT == 1 ? 192 : 104;
-    static_assert(128 * kRegsWG0 + 256 * SPLIT * kRegsSoftmax <= kThreads * kLaunchRegs, "register split");
-};
+// 12 warps: warpgroup 0 = producer (warp 0), MMA issuer (warp 1), two idle
+// warps; warpgroups 1 and 2 = softmax of query tiles 0 and 1.
+constexpr int kThreads = 384;
+// Register split.  The kernel is compiled for kLaunchRegs per thread (the
+// most 384 threads allow: each SM sub-partition holds three warps of 32 lanes
+// and 16384 registers).  Warpgroup 0 then gives registers back and the two
+// softmax warpgroups take them: 128 * kRegsWG0 + 256 * kRegsSoftmax must not
+// exceed 384 * kLaunchRegs (63488 <= 64512; per sub-partition 112 + 2 * 192 <= 512).
+constexpr int kLaunchRegs = 168;
+constexpr int kRegsWG0 = 112;
+constexpr int kRegsSoftmax = 192;
+static_assert(128 * kRegsWG0 + 256 * kRegsSoftmax <= kThreads * kLaunchRegs, "register split");
 constexpr int kPanelBytes = 128 * 128;  // 128 rows x 128 B: one 64-column swizzled panel
 // In the POLY variant of the kernel every kPolyEvery-th pair of probabilities
 // is computed by exp2_poly_x2 (FMA and integer pipes) instead of the MUFU unit.
@@ -130,7 +123,7 @@ struct FwdParams {
     int nqb, nkb;
 };
 
-template <int D, bool P_TMEM, bool F8 = false, int SPLIT = 1>
+template <int D, bool P_TMEM, bool F8 = false>
 struct Layout {
     // Q and K are bf16 or (F8) e4m3; V is always bf16.  A swizzled panel is
     // 128 rows of 128 bytes: 64 bf16 or 128 e4m3 elements per row.
@@ -160,15 +153,7 @@ struct Layout {
     static constexpr int kBarOEmpty = kBarOFull + kQT;
     static constexpr int kNumBars = kBarOEmpty + kQT;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
-    // SPLIT = 2 only: what the two halves of a query tile exchange.
-    //   kOffXM  float [2 step parities][2 tiles][2 halves][128 rows]: row maxima
-    //   kOffXL  float [2 tiles][2 halves][128 rows]: row sums at the end of a unit
-    //   kOffXF  int   [3][2 tiles][2 halves][4 warps]: per-warp wait results
-    //           (two step parities, then the end of a unit)
-    static constexpr int kOffXM = kOffMisc + 16;
-    static constexpr int kOffXL = kOffXM + (SPLIT == 2 ? 2 * 2 * 2 * 128 * 4 : 0);
-    static constexpr int kOffXF = kOffXL + (SPLIT == 2 ? 2 * 2 * 128 * 4 : 0);
-    static constexpr int kSmemBytes = kOffXF + (SPLIT == 2 ? 3 * 2 * 2 * 4 * 4 : 0) + 1024;  // + slack to align the base
+    static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + slack to align the base
     // TMEM columns: S_0, S_1 (128 fp32 each; P_t overwrites the first 64 of
     // S_t when it lives in TMEM), then O_0, O_1 (D fp32 each).
     __host__ __device__ static constexpr uint32_t tm_s(int t) { return t ? 128u : 0u; }
@@ -176,7 +161,7 @@ struct Layout {
     static constexpr uint32_t kTmemCols = 512;
     static_assert(256 + 2 * D <= 512, "TMEM budget");
     static_assert(kSmemBytes <= 232448, "shared memory budget");
-    // 128 SPLIT threads arrive per phase on these; one arrival (expect_tx or commit) on the rest
+    // 128 threads arrive per phase on these; one arrival (expect_tx or commit) on the rest
     __host__ __device__ static constexpr bool per_thread_bar(int i) {
         return (i >= kBarPFull && i < kBarPFull + kQT) || (i >= kBarOEmpty && i < kBarOEmpty + kQT);
     }
@@ -220,12 +205,11 @@ __device__ __forceinline__ Unit unit_at(int u, const FwdParams& p) {
     return x;
 }
 
-template <int D, bool P_TMEM, bool POLY, bool F8, int SPLIT>
-__global__ void __launch_bounds__(Warps<SPLIT>::kThreads, 1)
+template <int D, bool P_TMEM, bool POLY, bool F8>
+__global__ void __launch_bounds__(kThreads, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
-    using L = Layout<D, P_TMEM, F8, SPLIT>;
-    using W = Warps<SPLIT>;
+    using L = Layout<D, P_TMEM, F8>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -238,7 +222,7 @@ __global__ void __launch_bounds__(Warps<SPLIT>::kThreads, 1)
 
     // ---- set-up: barriers, TMEM
     if (threadIdx.x == 0) {
-        for (int i = 0; i < L::kNumBars; ++i) mbar_init(bar(i), L::per_thread_bar(i) ? 128u * SPLIT : 1u);
+        for (int i = 0; i < L::kNumBars; ++i) mbar_init(bar(i), L::per_thread_bar(i) ? 128u : 1u);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -251,7 +235,7 @@ __global__ void __launch_bounds__(Warps<SPLIT>::kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     if (warp < 4) {
-      warpgroup_reg_dealloc<W::kRegsWG0>();
+      warpgroup_reg_dealloc<kRegsWG0>();
       if (warp == 0) {
         // ================================================= TMA producer
         if (lane == 0) {
@@ -428,8 +412,8 @@ __global__ void __launch_bounds__(Warps<SPLIT>::kThreads, 1)
             if (ok && tiles && lane == 0) atomicAdd(&g_fwd_tiles, tiles);
         }
       }
-    } else if constexpr (SPLIT == 1) {
-        warpgroup_reg_alloc<W::kRegsSoftmax>();
+    } else {
+        warpgroup_reg_alloc<kRegsSoftmax>();
         // ================================================= softmax warpgroups
         const int t = (warp - 4) >> 2;
         const int q4 = warp & 3;  // TMEM lane quarter this warp may access
@@ -614,191 +598,6 @@ __global__ void __launch_bounds__(Warps<SPLIT>::kThreads, 1)
                 *lse_out = l > 0.f ? (m + lg2(l)) * kLn2 : -INFINITY;
             }
         }
-    } else {
-        static_assert(SPLIT == 2 && P_TMEM && !POLY && !F8, "two softmax warpgroups per tile: bf16, P in TMEM");
-        warpgroup_reg_alloc<W::kRegsSoftmax>();
-        // ================================================= softmax, two warpgroups per query tile
-        // Warpgroup (t, h) owns key columns [64 h, 64 h + 64) of every key tile
-        // of query tile t, for all 128 rows (its warps' TMEM lane quarters).
-        // Per key tile the two halves exchange their row maxima through shared
-        // memory at a named barrier of the tile, so both use the same reference
-        // max and feed the one accumulator O_t: half h writes P for its 64 keys
-        // (packed columns [32 h, 32 h + 32) of S_t, which only it and half 0
-        // read, both before the barrier) and rescales O_t's columns
-        // [h D/2, (h + 1) D/2).  The halves' row sums, taken against the same
-        // reference, are added at the end of the unit.  Every warp publishes
-        // whether its barrier wait succeeded; after each named barrier the
-        // eight warps of the pair continue only if all did, so an aborted wait
-        // never leaves a warp alone at a named barrier.
-        constexpr int HC = kBN / 2;  // key columns of a half
-        constexpr int HD = D / 2;    // O columns a half rescales and stores
-        const int wg = (warp >> 2) - 1;
-        const int t = wg >> 1;
-        const int h = wg & 1;
-        const int q4 = warp & 3;  // TMEM lane quarter this warp may access
-        const int r = q4 * 32 + lane;
-        const uint32_t lane_base = static_cast<uint32_t>(q4 * 32) << 16;
-        const uint32_t tS = tmem + lane_base + L::tm_s(t);
-        const uint32_t tO = tmem + lane_base + L::tm_o(t) + h * HD;
-        float* xm = reinterpret_cast<float*>(sgen + L::kOffXM);
-        float* xl = reinterpret_cast<float*>(sgen + L::kOffXL);
-        volatile int* xf = reinterpret_cast<volatile int*>(sgen + L::kOffXF);
-        const float sl = p.scale_log2;
-        int s_waits = 0, o_waits = 0;
-        bool ok = true;
-        // Publishes this warp's wait result in flag set `set`, meets the other
-        // half at the tile's named barrier, and returns whether all eight
-        // warps of the pair succeeded (the same answer in every thread).
-        auto meet = [&](int set, bool okw) -> bool {
-            if (lane == 0) xf[(set * 2 + t) * 8 + h * 4 + q4] = okw ? 1 : 0;
-            named_bar_sync(1 + t, 256);
-            bool all = true;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) all = all && xf[(set * 2 + t) * 8 + i] != 0;
-            return all;
-        };
-        auto ld_o = [&](uint32_t* xo) {
-            if constexpr (HD == 64)
-                tmem_ld64_sync(tO, xo);
-            else
-                tmem_ld32_sync(tO, xo);
-        };
-        for (int k = 0; ok; ++k) {
-            const int u = unit_index(k, p);
-            if (u < 0) break;
-            const Unit x = unit_at(u, p);
-            const int rs = x.row0 + t * kBM;
-            const int row = rs + r;
-            const int nt = x.n[t];
-            __nv_bfloat16* orow = p.o + (((long long)x.b * p.Nq + row) * p.Hq + x.hq) * D + h * HD;
-            float* lse_out = p.lse + ((long long)x.b * p.Hq + x.hq) * p.lse_ld + row;
-            if (nt == 0) {
-                // Tile beyond Nq, or rows with no allowed key at all.
-                if (row < p.Nq) {
-                    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-                    for (int c = 0; c < HD / 8; ++c) reinterpret_cast<uint4*>(orow)[c] = z;
-                    if (h == 0) *lse_out = -INFINITY;
-                }
-                continue;
-            }
-            const long long diag = (long long)row + (p.Nk - p.Nq);  // last causal key of the row
-            const long long diag_tile = (long long)rs + (p.Nk - p.Nq);
-            float m = -INFINITY, l = 0.f;
-            for (int j = 0; j < nt; ++j) {
-                const bool okw = mbar_wait_warp(bar(L::kBarSFull + t), s_waits & 1, abort_flag,
-                                                &g_fwd_status, p.wait_limit);
-                const int par = s_waits & 1;
-                ++s_waits;
-                uint32_t s[HC];
-                float mloc = -INFINITY;
-                if (okw) {
-                    tc_fence_after();
-                    tmem_ld64_sync(tS + h * HC, s);
-                    const int col0 = j * kBN + h * HC;
-                    const bool need_mask = (col0 + HC > p.Nk) ||
-                                           (p.causal && (long long)(col0 + HC - 1) > diag_tile);
-                    if (need_mask) {
-                        // allowed keys of the row within this half: columns [0, lim)
-                        long long end = p.Nk;
-                        if (p.causal && diag + 1 < end) end = diag + 1;
-                        end -= col0;
-                        const int lim = end < 0 ? 0 : end > HC ? HC : (int)end;
-#pragma unroll
-                        for (int c = 0; c < HC; ++c)
-                            if (c >= lim) s[c] = __float_as_uint(-INFINITY);
-                    }
-                    // row max of the half: 8 independent chains of three-input maxima
-                    float mx[8];
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        mx[i] = fmax3(__uint_as_float(s[i]), __uint_as_float(s[i + 8]), __uint_as_float(s[i + 16]));
-                        mx[i] = fmax3(mx[i], __uint_as_float(s[i + 24]), __uint_as_float(s[i + 32]));
-                        mx[i] = fmax3(mx[i], __uint_as_float(s[i + 40]), __uint_as_float(s[i + 48]));
-                        mx[i] = fmaxf(mx[i], __uint_as_float(s[i + 56]));
-                    }
-                    mloc = fmaxf(fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), mx[6]), mx[7]) * sl;
-                }
-                xm[((par * 2 + t) * 2 + h) * 128 + r] = mloc;
-                if (!meet(par, okw)) {
-                    ok = false;
-                    break;
-                }
-                const float m_tile = fmaxf(mloc, xm[((par * 2 + t) * 2 + (h ^ 1)) * 128 + r]);
-                // The same reference-max rule as with one warpgroup per tile (the
-                // threshold is in log2 units; 0 = move whenever the max grows).
-                float m_new = m, alpha = 1.f;
-                if (m_tile > m + p.rescale_thr) {
-                    m_new = m_tile;
-                    alpha = ex2(m - m_new);  // 0 on the first non-empty tile
-                }
-                const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-                const uint64_t sl2 = f2_pack(sl, sl);
-                const uint64_t nm2 = f2_pack(-m_use, -m_use);
-                uint64_t sum2[2] = {0ull, 0ull};
-                uint32_t pk[HC / 2];
-#pragma unroll
-                for (int c = 0; c < HC / 2; ++c) {
-                    const uint64_t xx = f2_fma(f2_pack(__uint_as_float(s[2 * c]), __uint_as_float(s[2 * c + 1])),
-                                               sl2, nm2);
-                    const float p0 = ex2(f2_lo(xx)), p1 = ex2(f2_hi(xx));
-                    sum2[c & 1] = f2_add(sum2[c & 1], f2_pack(p0, p1));
-                    pk[c] = pack_bf16(p0, p1);
-                }
-                const uint64_t sum = f2_add(sum2[0], sum2[1]);
-                const float tile_sum = m_new == -INFINITY ? 0.f : f2_lo(sum) + f2_hi(sum);
-                l = fmaf(l, alpha, tile_sum);
-                tmem_st32(tS + h * (HC / 2), pk);
-                // O_t holds the sum through key tile j-1; this half brings its
-                // columns to the new reference (alpha is the same in both halves).
-                if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-                    uint32_t xo[HD];
-                    ld_o(xo);
-                    const uint64_t a2 = f2_pack(alpha, alpha);
-#pragma unroll
-                    for (int i = 0; i < HD / 2; ++i) {
-                        const uint64_t y = f2_mul(f2_pack(__uint_as_float(xo[2 * i]), __uint_as_float(xo[2 * i + 1])), a2);
-                        xo[2 * i] = __float_as_uint(f2_lo(y));
-                        xo[2 * i + 1] = __float_as_uint(f2_hi(y));
-                    }
-#pragma unroll
-                    for (int c = 0; c < HD; c += 32) tmem_st32(tO + c, xo + c);
-                }
-                tmem_st_wait();  // P and any rescaled O are in TMEM before the MMA is told
-                tc_fence_before();
-                mbar_arrive(bar(L::kBarPFull + t));
-                m = m_new;
-            }
-            if (!ok) break;
-            // ---- epilogue: O = acc / (l_0 + l_1), LSE = m + ln(l_0 + l_1)
-            const bool okw = mbar_wait_warp(bar(L::kBarOFull + t), o_waits & 1, abort_flag, &g_fwd_status,
-                                            p.wait_limit);
-            ++o_waits;
-            xl[(t * 2 + h) * 128 + r] = l;
-            if (!meet(2, okw)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            uint32_t xo[HD];
-            ld_o(xo);
-            tc_fence_before();
-            mbar_arrive(bar(L::kBarOEmpty + t));  // the next unit's PV may overwrite O_t now
-            const float lt = l + xl[(t * 2 + (h ^ 1)) * 128 + r];
-            if (row < p.Nq) {
-                const float inv = lt > 0.f ? 1.f / lt : 0.f;
-#pragma unroll
-                for (int c = 0; c < HD / 8; ++c) {
-                    uint4 w;
-                    w.x = pack_bf16(__uint_as_float(xo[8 * c + 0]) * inv, __uint_as_float(xo[8 * c + 1]) * inv);
-                    w.y = pack_bf16(__uint_as_float(xo[8 * c + 2]) * inv, __uint_as_float(xo[8 * c + 3]) * inv);
-                    w.z = pack_bf16(__uint_as_float(xo[8 * c + 4]) * inv, __uint_as_float(xo[8 * c + 5]) * inv);
-                    w.w = pack_bf16(__uint_as_float(xo[8 * c + 6]) * inv, __uint_as_float(xo[8 * c + 7]) * inv);
-                    reinterpret_cast<uint4*>(orow)[c] = w;
-                }
-                if (h == 0) *lse_out = lt > 0.f ? (m + lg2(lt)) * kLn2 : -INFINITY;
-            }
-        }
     }
 
     // ---- teardown
@@ -810,25 +609,24 @@ __global__ void __launch_bounds__(Warps<SPLIT>::kThreads, 1)
     }
 }
 
-template <int D, bool P_TMEM, bool POLY, bool F8 = false, int SPLIT = 1>
+template <int D, bool P_TMEM, bool POLY, bool F8 = false>
 attn_status_t launch_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                           int Hq, int Hkv, int Nq, int Nk, float scale, int causal,
                           cudaStream_t stream, const attn_test_options_t* test, long long lse_ld,
                           const float* q_scales = nullptr, const float* k_scales = nullptr) {
-    using L = Layout<D, P_TMEM, F8, SPLIT>;
-    using W = Warps<SPLIT>;
+    using L = Layout<D, P_TMEM, F8>;
     CUtensorMap mq, mk, mv;
     if (!attn_host::encode_bshd_map(&mq, q, B, Nq, Hq, D, kBM, L::kQKElem) ||
         !attn_host::encode_bshd_map(&mk, k, B, Nk, Hkv, D, kBN, L::kQKElem) ||
         !attn_host::encode_bshd_map(&mv, v, B, Nk, Hkv, D, kBN, 2))
         return ATTN_ERR_CUDA;
-    // The register split inside the kernel assumes exactly W::kLaunchRegs per
+    // The register split inside the kernel assumes exactly kLaunchRegs per
     // thread at launch; refuse to launch a build that differs (the split's
     // register increase would otherwise wait forever).
     const attn_host::KernelSetup ks =
-        attn_host::kernel_setup<fwd_tc_kernel<D, P_TMEM, POLY, F8, SPLIT>>(L::kSmemBytes);
+        attn_host::kernel_setup<fwd_tc_kernel<D, P_TMEM, POLY, F8>>(L::kSmemBytes);
     if (ks.err != cudaSuccess) return ATTN_ERR_CUDA;
-    if (ks.num_regs != W::kLaunchRegs) return ATTN_ERR_UNSUPPORTED;
+    if (ks.num_regs != kLaunchRegs) return ATTN_ERR_UNSUPPORTED;
     FwdParams prm;
     prm.lse = lse;
     prm.lse_ld = lse_ld > 0 ? lse_ld : Nq;
@@ -858,7 +656,7 @@ attn_status_t launch_impl(const void* q, const void* k, const void* v, void* o, 
     const int sms = attn_host::device_sm_count();
     if (sms <= 0) return ATTN_ERR_CUDA;
     const int grid = (int)(units < sms ? units : sms);
-    fwd_tc_kernel<D, P_TMEM, POLY, F8, SPLIT><<<grid, W::kThreads, L::kSmemBytes, stream>>>(mq, mk, mv, prm);
+    fwd_tc_kernel<D, P_TMEM, POLY, F8><<<grid, kThreads, L::kSmemBytes, stream>>>(mq, mk, mv, prm);
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
@@ -870,27 +668,18 @@ attn_status_t launch_fwd_tc(const void* q, const void* k, const void* v, void* o
                             int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal,
                             float scale, cudaStream_t stream, const attn_test_options_t* test,
                             long long lse_ld) {
-    // Production: P in tensor memory, every exponential on MUFU, one softmax
-    // warpgroup per query tile.  The other variants are reached only through
-    // attn_fwd_test.
+    // Production: P in tensor memory, every exponential on MUFU.  The other
+    // variants are reached only through attn_fwd_test.
     const bool smem_p = test && test->p_in_smem;
     const bool poly = test && test->exp2_poly;
-    int split = (test && test->softmax_split) ? test->softmax_split : 1;
-    if (smem_p || poly) split = 1;
-    if (d == 128) {
-        if (smem_p) return launch_impl<128, false, false>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, stream, test, lse_ld);
-        if (poly) return launch_impl<128, true, true>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, stream, test, lse_ld);
-        if (split == 2)
-            return launch_impl<128, true, false, false, 2>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, stream, test, lse_ld);
-        return launch_impl<128, true, false>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, stream, test, lse_ld);
-    }
-    if (d == 64) {
-        if (smem_p) return launch_impl<64, false, false>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, stream, test, lse_ld);
-        if (poly) return launch_impl<64, true, true>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, stream, test, lse_ld);
-        if (split == 2)
-            return launch_impl<64, true, false, false, 2>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, stream, test, lse_ld);
-        return launch_impl<64, true, false>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, stream, test, lse_ld);
-    }
+    if (d == 128)
+        return smem_p ? launch_impl<128, false, false>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, stream, test, lse_ld)
+               : poly ? launch_impl<128, true, true>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, stream, test, lse_ld)
+                      : launch_impl<128, true, false>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, stream, test, lse_ld);
+    if (d == 64)
+        return smem_p ? launch_impl<64, false, false>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, stream, test, lse_ld)
+               : poly ? launch_impl<64, true, true>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, stream, test, lse_ld)
+                      : launch_impl<64, true, false>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, stream, test, lse_ld);
     return ATTN_ERR_UNSUPPORTED;
 }
 

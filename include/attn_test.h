@@ -51,18 +51,12 @@ typedef struct {
      * (0 = the first key tile it loads); decode, this tile of the block's
      * segment (0 = its first 64 keys). */
     int skip_load;
-    /* forward only: softmax warpgroups per 128-row query tile, 1 (one
-     * thread per row and all 128 key columns of a key tile) or 2 (two
-     * threads per row, 64 key columns each); 0 = the production choice (1).
-     * p_in_smem and exp2_poly imply 1. */
-    int softmax_split;
 } attn_test_options_t;
 
 /*
  * attn_fwd_test -- attn_fwd (ATTN_BF16 only) with the options above.  Same
  * arguments, layouts and errors as attn_fwd, plus ATTN_ERR_INVALID for a
- * NULL `opt`, a threshold outside [0, 8], a negative wait bound or a
- * softmax_split other than 0, 1 or 2.
+ * NULL `opt`, a threshold outside [0, 8] or a negative wait bound.
  */
 attn_status_t attn_fwd_test(const void* q, const void* k, const void* v, void* o,
                             float* lse, int B, int Hq, int Hkv, int Nq, int Nk, int d,

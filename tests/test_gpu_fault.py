@@ -25,10 +25,12 @@ TIMEOUT = 4
 SHORT_WAIT = 2_000_000  # SM cycles, about 1 ms
 
 
-@pytest.mark.parametrize("d,N,skip", [(128, 256, 0), (64, 256, 1), (128, 700, 3)])
+@pytest.mark.parametrize("d,N,skip", [(128, 256, 0), (64, 256, 1), (128, 700, 3), (64, 700, 2)])
 def test_forward_lost_load_times_out_and_context_survives(attn, oracle_mod, d, N, skip):
-    """One work unit per block (B = H = 1): block 0 never receives the K/V
-    tiles at ring position `skip`; its MMA warp's wait runs out."""
+    """One work unit per block (B = H = 1 and N <= 256; three blocks at
+    N = 700, the injected one working on the longest unit): block 0 never
+    receives the K/V tiles at ring position `skip`; its MMA warp's wait runs
+    out."""
     q, k, v = make_qkv(1, 1, 1, N, N, d, seed=40 + d)
     qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
     scale = 1.0 / math.sqrt(d)
