@@ -3,10 +3,23 @@
 Tolerances: bf16 inputs with fp32 accumulation must match the float64 oracle
 to max |dO| <= 2e-2 and max |dLSE| <= 1e-3; fp32 inputs to 1e-5 for both.
 """
+import json
+import os
+
 import numpy as np
 import torch
 
 TOL = {torch.bfloat16: (2e-2, 1e-3), torch.float32: (1e-5, 1e-5)}
+
+
+def _log(what, d_o, d_l, rows):
+    """With ATTN_PARITY_LOG set, every comparison appends one JSON line
+    (what, max |dO|, max |dLSE|, rows compared) to that file."""
+    path = os.environ.get("ATTN_PARITY_LOG")
+    if path:
+        with open(path, "a") as f:
+            f.write(json.dumps({"what": what, "max_abs_dO": float(d_o), "max_abs_dLSE": float(d_l),
+                                "rows": int(rows)}) + "\n")
 
 
 def to_np64(t):
@@ -25,6 +38,7 @@ def compare(o_gpu, lse_gpu, o_ref, lse_ref, dtype, what=""):
     assert np.array_equal(np.isfinite(lse), fin), "%s: -inf pattern of LSE differs" % what
     assert np.all(lse[~fin] == lse_ref[~fin])
     d_l = np.abs(lse[fin] - lse_ref[fin]).max() if fin.any() else 0.0
+    _log(what, d_o, d_l, int(np.prod(o.shape[:-1])))
     assert d_o <= tol_o, "%s: max|dO| = %.3g > %.1g" % (what, d_o, tol_o)
     assert d_l <= tol_l, "%s: max|dLSE| = %.3g > %.1g" % (what, d_l, tol_l)
     return d_o, d_l

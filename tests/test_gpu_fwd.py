@@ -28,7 +28,8 @@ def run_case(attn, oracle_mod, B, Hq, Hkv, Nq, Nk, d, causal, seed, dtype=torch.
         assert guards_intact(ob, og) and guards_intact(lb, lg), "write outside O/LSE"
     o_ref, lse_ref = oracle_mod.attn_fwd(q, k, v, causal, scale)
     return compare(o, lse, o_ref, lse_ref, dtype,
-                   "B%d Hq%d Hkv%d Nq%d Nk%d d%d causal%d" % (B, Hq, Hkv, Nq, Nk, d, causal))
+                   "B%d Hq%d Hkv%d Nq%d Nk%d d%d causal%d q_scale%g %s" % (B, Hq, Hkv, Nq, Nk, d, causal,
+                                                                      q_scale, str(dtype)))
 
 
 def test_single_head_bf16(attn, oracle_mod):
@@ -100,7 +101,8 @@ def _sampled_full_size(attn, oracle_mod, B, Hq, Hkv, N, d, causal, seed, n_rows,
     o_ref, lse_ref = oracle_mod.attn_rows(q, k, v, causal, scale, rows)
     o_sel = torch.stack([o[b, i, h] for b, h, i in rows])
     l_sel = torch.stack([lse[b, h, i] for b, h, i in rows])
-    compare(o_sel, l_sel, o_ref, lse_ref, torch.bfloat16, "full-size sampled")
+    shape = "B%d Hq%d Hkv%d N%d d%d causal%d" % (B, Hq, Hkv, N, d, causal)
+    compare(o_sel, l_sel, o_ref, lse_ref, torch.bfloat16, "full-size sampled rows " + shape)
     assert torch.isfinite(lse.float()).all()
     G = Hq // Hkv
     for b, g in groups:
@@ -108,7 +110,7 @@ def _sampled_full_size(attn, oracle_mod, B, Hq, Hkv, N, d, causal, seed, n_rows,
         og_ref, lg_ref = oracle_mod.attn_fwd(q[b:b + 1, :, hs], k[b:b + 1, :, g:g + 1],
                                              v[b:b + 1, :, g:g + 1], causal, scale)
         compare(o[b:b + 1, :, hs], lse[b:b + 1, hs], og_ref, lg_ref, torch.bfloat16,
-                "full-size whole KV group (b=%d, g=%d): %d heads x %d rows" % (b, g, G, N))
+                "full-size whole KV group (b=%d, g=%d) %s" % (b, g, shape))
 
 
 def test_training_prefill_full_size(attn, oracle_mod):
