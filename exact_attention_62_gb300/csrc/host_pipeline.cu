@@ -90,7 +90,9 @@ extern "C" attn_status_t attn_fwd_host(const void* q_h, const void* k_h, const v
     // One bf16 sequence: chunks of query rows (see the top of this file).
     const bool by_rows = B == 1 && dtype == ATTN_BF16 && Nk > 0 && (!causal || Nq <= Nk);
     const int row_units = (Nq + kRowUnit - 1) / kRowUnit;
-    int n = chunks == 0 ? (by_rows ? 4 : (B < 4 ? B : 4)) : chunks;
+    // Default: 8 row chunks for one sequence (B = 1, N = 16384 causal: 2.10 ms
+    // end to end against 2.23 with 4 and 2.43 with 2 on GB300), else min(B, 4).
+    int n = chunks == 0 ? (by_rows ? 8 : (B < 4 ? B : 4)) : chunks;
     if (n > kMaxChunks) return ATTN_ERR_UNSUPPORTED;
     if (n > (by_rows ? row_units : B)) n = by_rows ? row_units : B;
 

@@ -89,7 +89,7 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o,
  *   q_d, k_d, v_d, o_d, lse_d  device buffers of the same full sizes,
  *            caller-owned, aligned as for attn_fwd.
  *   chunks   the number of chunks n, 1..16; 0 = min(B, 4) for a batch and
- *            4 for one sequence.  With B > 1 (or fp32 inputs, or a causal
+ *            8 for one sequence.  With B > 1 (or fp32 inputs, or a causal
  *            Nq > Nk) chunk c holds sequences [B c / n, B (c + 1) / n),
  *            n <= B.  With one bf16 sequence chunk c holds the query rows
  *            [256 floor(U c / n), 256 floor(U (c + 1) / n)) (U = ceil(Nq /
