@@ -40,7 +40,7 @@ EXPORTED_SYMBOLS = (
 )
 
 # The test-only entry points include/attn_test.h declares.
-TEST_SYMBOLS = ("attn_fwd_test", "attn_decode_test")
+TEST_SYMBOLS = ("attn_fwd_test", "attn_decode_test", "attn_decode_model_time", "attn_decode_model_best")
 
 # Size of the scratch area built into the library for attn_decode_splitkv_static.
 DECODE_STATIC_SCRATCH_BYTES = 8 << 20
@@ -135,6 +135,11 @@ def lib() -> ctypes.CDLL:
     L.attn_fwd_test.restype = I
     L.attn_decode_test.argtypes = [P, P, P, P, P, I, I, I, I, I, F, I, P, SZ, OPT, P]
     L.attn_decode_test.restype = I
+    DB = ctypes.c_double
+    L.attn_decode_model_time.argtypes = [I, I, I, I, I, DB, DB, DB, DB]
+    L.attn_decode_model_time.restype = DB
+    L.attn_decode_model_best.argtypes = [I, I, I, I, DB, DB, DB, DB, I]
+    L.attn_decode_model_best.restype = I
     _lib = L
     return L
 

@@ -182,6 +182,26 @@ attn_status_t attn_fwd_test(const void* q, const void* k, const void* v, void* o
     return attn_host::launch_fwd_tc(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, causal, scale, st, opt);
 }
 
+double attn_decode_model_time(int units, int slots, int Nk, int d, int num_splits,
+                              double cta_bytes_per_s, double hbm_bytes_per_s, double cta_fixed_s,
+                              double merge_fixed_s) {
+    if (units < 1 || slots < 1 || Nk < 1 || d < 1 || num_splits < 1 || !(cta_bytes_per_s > 0.0) ||
+        !(hbm_bytes_per_s > 0.0) || !(cta_fixed_s >= 0.0) || !(merge_fixed_s >= 0.0))
+        return -1.0;
+    const attn_host::SplitModel m = {cta_bytes_per_s, hbm_bytes_per_s, cta_fixed_s, merge_fixed_s};
+    return attn_host::split_model_time(units, slots, Nk, d, num_splits, m);
+}
+
+int attn_decode_model_best(int units, int slots, int Nk, int d, double cta_bytes_per_s,
+                           double hbm_bytes_per_s, double cta_fixed_s, double merge_fixed_s,
+                           int single_wave) {
+    if (units < 1 || slots < 1 || Nk < 1 || d < 1 || !(cta_bytes_per_s > 0.0) ||
+        !(hbm_bytes_per_s > 0.0) || !(cta_fixed_s >= 0.0) || !(merge_fixed_s >= 0.0))
+        return -1;
+    const attn_host::SplitModel m = {cta_bytes_per_s, hbm_bytes_per_s, cta_fixed_s, merge_fixed_s};
+    return attn_host::split_model_best(units, slots, Nk, d, m, single_wave != 0);
+}
+
 int attn_decode_num_splits(int B, int Hq, int Hkv, int Nk, int d) {
     return attn_host::decode_auto_splits(B, Hq, Hkv, Nk, d);
 }

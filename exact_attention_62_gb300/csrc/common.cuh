@@ -88,6 +88,16 @@ attn_status_t launch_fwd_f32(const float* q, const float* k, const float* v, flo
                              int causal, float scale, cudaStream_t stream);
 
 // ---- split-KV decode and LSE merge (decode.cu)
+// The segment-count model (Lecture 11, sections 6.3-6.4), as pure host
+// arithmetic: see decode.cu.
+struct SplitModel {
+    double cta_bw;       // bytes/s one CTA streams with its ring full
+    double hbm;          // bytes/s the whole GPU streams
+    double cta_fixed;    // start-up of one CTA wave, s
+    double merge_fixed;  // the merge launch, s
+};
+double split_model_time(long long units, long long slots, int Nk, int d, int S, const SplitModel& m);
+int split_model_best(long long units, long long slots, int Nk, int d, const SplitModel& m, bool single_wave);
 int decode_auto_splits(int B, int Hq, int Hkv, int Nk, int d);
 size_t decode_workspace_bytes(int B, int Hq, int d, int splits);
 attn_status_t launch_decode(const void* q, const void* k, const void* v, void* o, float* lse,

@@ -644,33 +644,35 @@ int ctas_per_sm() {
 
 namespace attn_host {
 
-// Segment count from a CTA-by-wave time model (Lecture 11, sections 6.3-6.4):
-// every CTA streams its segment at min(cta_bw, hbm / concurrent CTAs), CTAs
-// beyond one wave wait for the next, each wave pays a fixed start-up, and more
-// than one segment adds the merge.  The smallest modelled time wins; ties go
-// to fewer segments.  With single_wave the count is capped so that all CTAs
-// run in one wave.
-struct SplitModel {
-    double cta_bw;       // bytes/s one CTA streams with its ring full
-    double hbm;          // bytes/s the whole GPU streams
-    double cta_fixed;    // start-up of one CTA wave
-    double merge_fixed;  // the merge launch
-};
+// Segment count from a CTA-by-wave time model (Lecture 11, sections 6.3-6.4,
+// whose exercise 9 works the same model on an A100: 32 segments of 64 CTAs in
+// one wave beat 64 segments of 128 CTAs in two): split_model_time and
+// split_model_best below.
 // Contiguous cache: fitted on GB300 to the measured best segment counts of
 // B = 1 x 2K-64K, B = 4 x 4K and 16K, B = 8 x 8K, B = 16 x 8K and B = 32 x 2K
 // keys (Hq = 32, Hkv = 8, d = 128); a CTA streams ~80-110 GB/s while few
 // compete, so batches of several sequences need few segments or none.
 constexpr SplitModel kDenseSplitModel = {8.0e10, 5.5e12, 0.5e-6, 4.0e-6};
 
-static int auto_splits_model(int B, int Hq, int Hkv, int Nk, int d, const SplitModel& m, bool single_wave) {
-    if (B < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || Nk < 1 || (d != 64 && d != 128)) return -1;
-    const int sms = device_sm_count();
-    if (sms <= 0) return -1;
-    const int per_sm = d == 128 ? ctas_per_sm<128>() : ctas_per_sm<64>();
-    const long long slots = (long long)sms * per_sm;
-    const long long units = (long long)B * (Hq / group_cols(Hq / Hkv));
-    const double cta_bw = m.cta_bw, hbm = m.hbm, cta_fixed = m.cta_fixed, merge_fixed = m.merge_fixed;
+// Modelled time (seconds) of S segments when every segment has `units` CTAs
+// and `slots` CTAs fit on the GPU at once: waves of CTAs, each streaming its
+// segment's K/V rows at min(cta_bw, hbm / concurrent CTAs) after a fixed
+// start-up, then (S > 1) the merge launch and its partial traffic.
+double split_model_time(long long units, long long slots, int Nk, int d, int S, const SplitModel& m) {
+    const long long ctas = units * S;
+    const long long waves = (ctas + slots - 1) / slots;
+    const double conc = (double)std::min(ctas, slots);
+    const double bw = std::min(m.cta_bw, m.hbm / conc);
     const double row_bytes = 2.0 * d * 2.0;  // one key's K and V for one head
+    const int seg = (Nk + S - 1) / S;
+    return (double)waves * (seg * row_bytes / bw + m.cta_fixed) +
+           (S > 1 ? m.merge_fixed + 2.0 * units * 8 * S * (d + 1) * 4.0 / m.hbm : 0.0);
+}
+
+// The segment count with the smallest modelled time (ties, within 0.5%, go
+// to fewer segments).  With single_wave the count is capped so that all CTAs
+// run in one wave and segments are whole 64-key tiles.
+int split_model_best(long long units, long long slots, int Nk, int d, const SplitModel& m, bool single_wave) {
     int best = 1;
     double best_t = 1e30;
     int max_s = std::min(Nk, 1024);
@@ -680,19 +682,23 @@ static int auto_splits_model(int B, int Hq, int Hkv, int Nk, int d, const SplitM
         max_s = (int)std::max(1LL, std::min((long long)max_s, slots / units));
     }
     for (int S = 1; S <= max_s; ++S) {
-        const long long ctas = units * S;
-        const long long waves = (ctas + slots - 1) / slots;
-        const double conc = (double)std::min(ctas, slots);
-        const double bw = std::min(cta_bw, hbm / conc);
-        const int seg = (Nk + S - 1) / S;
-        const double t = (double)waves * (seg * row_bytes / bw + cta_fixed) +
-                         (S > 1 ? merge_fixed + 2.0 * units * 8 * S * (d + 1) * 4.0 / hbm : 0.0);
+        const double t = split_model_time(units, slots, Nk, d, S, m);
         if (t < best_t * 0.995) {
             best_t = t;
             best = S;
         }
     }
     return best;
+}
+
+static int auto_splits_model(int B, int Hq, int Hkv, int Nk, int d, const SplitModel& m, bool single_wave) {
+    if (B < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || Nk < 1 || (d != 64 && d != 128)) return -1;
+    const int sms = device_sm_count();
+    if (sms <= 0) return -1;
+    const int per_sm = d == 128 ? ctas_per_sm<128>() : ctas_per_sm<64>();
+    const long long slots = (long long)sms * per_sm;
+    const long long units = (long long)B * (Hq / group_cols(Hq / Hkv));
+    return split_model_best(units, slots, Nk, d, m, single_wave);
 }
 
 int decode_auto_splits(int B, int Hq, int Hkv, int Nk, int d) {

@@ -3,8 +3,8 @@
  * only.  A production caller uses include/attn.h; nothing here is needed to
  * compute attention.
  *
- * They run the same kernels as attn_fwd and attn_decode_splitkv with
- * settings the production entry points keep fixed:
+ * attn_fwd_test and attn_decode_test run the same kernels as attn_fwd and
+ * attn_decode_splitkv with settings the production entry points keep fixed:
  *   - variants of the forward used to check that alternative formulations
  *     give the same answer and to measure what they cost (P staged in
  *     shared memory, part of the exponentials on the FMA pipe, a
@@ -12,6 +12,8 @@
  *   - the bound of every device-side wait, and a fault injection that makes
  *     one wait run out on purpose, so that tests can check the error path
  *     that keeps a lost signal from hanging a GPU.
+ * attn_decode_model_time / _best expose the decode's segment-count model as
+ * host arithmetic, so that it can be checked without a GPU.
  *
  * The injection stops one TMA load from being issued: the producer of
  * block 0 posts no byte count and issues no copy for that ring position.
@@ -74,6 +76,30 @@ attn_status_t attn_decode_test(const void* q, const void* k_cache, const void* v
                                float scale, int num_splits, void* workspace,
                                size_t workspace_bytes, const attn_test_options_t* opt,
                                void* stream);
+
+/*
+ * attn_decode_model_time / attn_decode_model_best -- the segment-count model
+ * behind attn_decode_num_splits (the CTA-by-wave model of [L11] 6.3-6.4) as
+ * plain host arithmetic, with the machine described by the arguments instead
+ * of the current device; no CUDA call is made.
+ *   units      CTAs per segment (sequences x query-head groups)
+ *   slots      CTAs resident on the GPU at once (SMs x CTAs per SM)
+ *   Nk, d      keys and head dimension (bf16 K and V: 4 d bytes per key)
+ *   cta_bytes_per_s, hbm_bytes_per_s  one CTA's and the GPU's stream rate
+ *   cta_fixed_s, merge_fixed_s        start-up of a wave; the merge launch
+ * Time of S segments: ceil(units S / slots) waves, each streaming a segment
+ * of ceil(Nk / S) keys at min(cta rate, hbm / min(units S, slots)) plus the
+ * start-up, plus (S > 1) the merge launch and its partial traffic.  _best
+ * returns the S in 1..min(Nk, 1024) of least time (ties within 0.5% to fewer
+ * segments; single_wave caps S so that all CTAs fit in one wave), or -1 on
+ * invalid arguments; _time returns -1 on invalid arguments.
+ */
+double attn_decode_model_time(int units, int slots, int Nk, int d, int num_splits,
+                              double cta_bytes_per_s, double hbm_bytes_per_s,
+                              double cta_fixed_s, double merge_fixed_s);
+int attn_decode_model_best(int units, int slots, int Nk, int d, double cta_bytes_per_s,
+                           double hbm_bytes_per_s, double cta_fixed_s, double merge_fixed_s,
+                           int single_wave);
 
 #ifdef __cplusplus
 }
