@@ -679,3 +679,34 @@ def test_rotated_code_checker_accepts_float32_rounding_and_rejects_real_errors(o
     off[0, 1, 0] *= np.float32(1 + 2.0 ** -10)
     with pytest.raises(AssertionError, match="scale"):
         check_rotated_codes(codes, off, x, s, oracle_mod)
+
+
+# ---------------------------------------------------------------- precision readings
+def test_row_sum_must_not_accumulate_in_fp16():
+    """Lecture 11, section 3.4 and common pitfall 4: the running sum l is
+    kept in fp32 (the kernels) or double (the oracle) because a low-precision
+    accumulator stagnates once the partial sum is large: later small terms
+    are rounded away.  A 4096-key row accumulated in fp16 is off by ~1e-1
+    relative; in fp32 by ~1e-6."""
+    rng = np.random.default_rng(11)
+    s = rng.standard_normal(4096)
+    p = np.exp(s - s.max())
+    exact = math.fsum(p)
+    l16 = np.float16(0)
+    for x in p.astype(np.float16):
+        l16 = np.float16(l16 + x)
+    l32 = np.float32(0)
+    for x in p.astype(np.float32):
+        l32 = np.float32(l32 + x)
+    assert abs(float(l16) - exact) / exact > 0.05          # stagnated: order 1e-1
+    assert abs(float(l32) - exact) / exact < 1e-5
+
+
+def test_fp16_exponential_overflows_near_11_09():
+    """Lecture 11, section 3.4: subtracting the row maximum is not only for
+    fp32's sake: fp16's e^x overflows at x ~ 11.09 = ln(65504), the largest
+    fp16 value, so unshifted scores of that size would already be inf."""
+    assert math.log(65504.0) == pytest.approx(11.09, abs=0.005)
+    with np.errstate(over="ignore"):
+        assert np.isfinite(np.float16(np.exp(11.08)))
+        assert np.isinf(np.float16(np.exp(11.10)))
