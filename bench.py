@@ -643,9 +643,6 @@ def run_extra(args):
     o, lse = attn.attn_fwd(q, k, v, causal, scale)
     if args.only == "forward":
         call = lambda: attn.attn_fwd(q, k, v, causal, scale, o=o, lse=lse)
-        if args.fwd_tiles or args.mma_issuers:  # a variant through the test-only entry point
-            opt = attn.AttnTestOptions(fwd_tiles=args.fwd_tiles, mma_issuers=args.mma_issuers)
-            call = lambda: attn.attn_fwd_test(q, k, v, causal, scale, opt, o=o, lse=lse)
         return _time_extra(args, call, flush_w, flush_r, attn, "tflops",
                            prefill_flops(PREFILL[args.prefill]) / 1e12, args.prefill)
     if args.only == "backward":
@@ -711,10 +708,6 @@ def main(argv=None):
     ap.add_argument("--no-configs", action="store_true",
                     help="skip the per-workload block (every workload timed alone)")
     ap.add_argument("--splits", type=int, default=0, help="decode segments (0 = automatic)")
-    ap.add_argument("--fwd-tiles", type=int, default=0,
-                    help="--only forward: query tiles per work unit (2, or 3 at d = 64; 0 = production)")
-    ap.add_argument("--mma-issuers", type=int, default=0,
-                    help="--only forward: MMA-issuing warps (1, or one per query tile; 0 = production)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -54,13 +54,12 @@ class AttnTestOptions(ctypes.Structure):
     """attn_test_options_t of include/attn_test.h (tests and measurements only)."""
     _fields_ = [("p_in_smem", ctypes.c_int), ("exp2_poly", ctypes.c_int),
                 ("rescale_threshold", ctypes.c_float), ("wait_limit_cycles", ctypes.c_longlong),
-                ("skip_load", ctypes.c_int), ("fwd_tiles", ctypes.c_int),
-                ("mma_issuers", ctypes.c_int)]
+                ("skip_load", ctypes.c_int)]
 
     def __init__(self, p_in_smem=0, exp2_poly=0, rescale_threshold=0.0, wait_limit_cycles=0,
-                 skip_load=-1, fwd_tiles=0, mma_issuers=0):
+                 skip_load=-1):
         super().__init__(int(p_in_smem), int(exp2_poly), float(rescale_threshold),
-                         int(wait_limit_cycles), int(skip_load), int(fwd_tiles), int(mma_issuers))
+                         int(wait_limit_cycles), int(skip_load))
 
 
 class AttnError(RuntimeError):

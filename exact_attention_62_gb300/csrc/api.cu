@@ -162,8 +162,7 @@ attn_status_t attn_fwd_test(const void* q, const void* k, const void* v, void* o
                             int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal, float scale,
                             const attn_test_options_t* opt, void* stream) {
     if (opt == nullptr || opt->wait_limit_cycles < 0 || !(opt->rescale_threshold >= 0.f) ||
-        !(opt->rescale_threshold <= 8.f) || (opt->fwd_tiles != 0 && opt->fwd_tiles != 2 && opt->fwd_tiles != 3) ||
-        opt->mma_issuers < 0 || opt->mma_issuers > 3)
+        !(opt->rescale_threshold <= 8.f))
         return ATTN_ERR_INVALID;
     if (B < 0 || Hq < 0 || Nq < 0 || Nk < 0 || Hkv < 1 || d < 1) return ATTN_ERR_INVALID;
     if (causal != 0 && causal != 1) return ATTN_ERR_INVALID;

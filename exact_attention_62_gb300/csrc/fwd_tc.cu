@@ -82,29 +82,20 @@ __device__ unsigned g_fwd_status = 0;
 __device__ unsigned long long g_fwd_tiles = 0;
 
 constexpr int kBM = 128;        // query rows per tile (one TMEM lane each)
-// The work shape: QT query tiles of kBM rows per work unit, BN keys per key
-// tile, and the warp and register plan that follows.  Warpgroup 0 = TMA
-// producer (warp 0), MMA issuer (warp 1) and two idle warps; warpgroups 1..QT
-// = the softmax of query tiles 0..QT-1.  The kernel is compiled for
-// kLaunchRegs per thread (the most kThreads threads allow: 65536 registers
-// per SM); warpgroup 0 gives registers back and the softmax warpgroups take
-// them, so 128 kRegsWG0 + 128 QT kRegsSoftmax must not exceed kThreads
-// kLaunchRegs.
-//   QT = 2, BN = 128 (d = 128, and the d = 64 variants): 384 threads,
-//     168 -> 112 / 192 (63488 <= 64512).
-//   QT = 3, BN = 96 (d = 64): 512 threads, 128 -> 104 / 136 (65536 <= 65536).
-//     Three tiles' S (3 x 96 columns) and O (3 x 64) fill 480 of the 512
-//     TMEM columns: three softmax chains share one tensor pipe instead of two.
-template <int QT, int BN>
-struct Shape {
-    static constexpr int kThreads = 128 * (1 + QT);
-    static constexpr int kLaunchRegs = QT == 2 ? 168 : 128;
-    static constexpr int kRegsWG0 = QT == 2 ? 112 : 104;
-    static constexpr int kRegsSoftmax = QT == 2 ? 192 : 136;
-    static_assert(QT == 2 || QT == 3, "two or three query tiles per unit");
-    static_assert(BN % 32 == 0 && BN >= 64 && BN <= 128, "keys per tile");
-    static_assert(128 * kRegsWG0 + 128 * QT * kRegsSoftmax <= kThreads * kLaunchRegs, "register split");
-};
+constexpr int kBN = 128;        // keys per tile
+constexpr int kQT = 2;          // query tiles per unit
+// 12 warps: warpgroup 0 = producer (warp 0), MMA issuer (warp 1), two idle
+// warps; warpgroups 1 and 2 = softmax of query tiles 0 and 1.
+constexpr int kThreads = 384;
+// Register split.  The kernel is compiled for kLaunchRegs per thread (the
+// most 384 threads allow: each SM sub-partition holds three warps of 32 lanes
+// and 16384 registers).  Warpgroup 0 then gives registers back and the two
+// softmax warpgroups take them: 128 * kRegsWG0 + 256 * kRegsSoftmax must not
+// exceed 384 * kLaunchRegs (63488 <= 64512; per sub-partition 112 + 2 * 192 <= 512).
+constexpr int kLaunchRegs = 168;
+constexpr int kRegsWG0 = 112;
+constexpr int kRegsSoftmax = 192;
+static_assert(128 * kRegsWG0 + 256 * kRegsSoftmax <= kThreads * kLaunchRegs, "register split");
 constexpr int kPanelBytes = 128 * 128;  // 128 rows x 128 B: one 64-column swizzled panel
 // In the POLY variant of the kernel every kPolyEvery-th pair of probabilities
 // is computed by exp2_poly_x2 (FMA and integer pipes) instead of the MUFU unit.
@@ -120,7 +111,7 @@ struct FwdParams {
     __nv_bfloat16* o;
     int B, Hq, Hkv, Nq, Nk, G;
     int causal;
-    int num_row_units;  // units per (batch, head): ceil(Nq / (QT x 128))
+    int num_pairs;
     int num_units;
     float scale_log2;
     float rescale_thr;  // log2 units; 0 = rescale whenever the max grows
@@ -132,7 +123,7 @@ struct FwdParams {
     int nqb, nkb;
 };
 
-template <int D, bool P_TMEM, bool F8, int QT, int BN>
+template <int D, bool P_TMEM, bool F8 = false>
 struct Layout {
     // Q and K are bf16 or (F8) e4m3; V is always bf16.  A swizzled panel is
     // 128 rows of 128 bytes: 64 bf16 or 128 e4m3 elements per row.
@@ -140,64 +131,56 @@ struct Layout {
     static constexpr int kQKPanels = D * kQKElem / 128;
     static constexpr int kPanels = D / 64;  // V panels
     static constexpr int kQBytes = kBM * D * kQKElem;
-    static constexpr int kKBytes = BN * D * kQKElem;
-    static constexpr int kKVBytes = BN * D * 2;  // one V tile
-    static constexpr int kPBytes = P_TMEM ? 0 : kBM * BN * 2;
+    static constexpr int kKBytes = kBN * D * kQKElem;
+    static constexpr int kKVBytes = kBN * D * 2;  // one V tile
+    static constexpr int kPBytes = P_TMEM ? 0 : kBM * kBN * 2;
     static constexpr int kKSt = F8 ? 3 : P_TMEM ? (D == 128 ? 2 : 3) : (D == 128 ? 1 : 2);
     static constexpr int kVSt = kKSt;
     static constexpr int kOffQ = 0;
-    static constexpr int kOffP = kOffQ + QT * kQBytes;
-    static constexpr int kOffK = kOffP + QT * kPBytes;
+    static constexpr int kOffP = kOffQ + kQT * kQBytes;
+    static constexpr int kOffK = kOffP + kQT * kPBytes;
     static constexpr int kOffV = kOffK + kKSt * kKBytes;
     static constexpr int kOffBar = kOffV + kVSt * kKVBytes;
     static constexpr int kBarQFull = 0;
-    static constexpr int kBarQEmpty = kBarQFull + QT;
-    static constexpr int kBarKFull = kBarQEmpty + QT;
+    static constexpr int kBarQEmpty = kBarQFull + kQT;
+    static constexpr int kBarKFull = kBarQEmpty + kQT;
     static constexpr int kBarKEmpty = kBarKFull + kKSt;
     static constexpr int kBarVFull = kBarKEmpty + kKSt;
     static constexpr int kBarVEmpty = kBarVFull + kVSt;
     static constexpr int kBarSFull = kBarVEmpty + kVSt;
-    static constexpr int kBarPFull = kBarSFull + QT;
-    static constexpr int kBarOFull = kBarPFull + QT;
-    static constexpr int kBarOEmpty = kBarOFull + QT;
-    static constexpr int kNumBars = kBarOEmpty + QT;
+    static constexpr int kBarPFull = kBarSFull + kQT;
+    static constexpr int kBarOFull = kBarPFull + kQT;
+    static constexpr int kBarOEmpty = kBarOFull + kQT;
+    static constexpr int kNumBars = kBarOEmpty + kQT;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
     static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + slack to align the base
-    // TMEM columns: S_0 .. S_{QT-1} (BN fp32 each; P_t, bf16 two keys per
-    // column, overwrites the first BN/2 of S_t when it lives in TMEM), then
-    // O_0 .. O_{QT-1} (D fp32 each).
-    __host__ __device__ static constexpr uint32_t tm_s(int t) { return (uint32_t)(t * BN); }
-    __host__ __device__ static constexpr uint32_t tm_o(int t) { return (uint32_t)(QT * BN + t * D); }
+    // TMEM columns: S_0, S_1 (128 fp32 each; P_t overwrites the first 64 of
+    // S_t when it lives in TMEM), then O_0, O_1 (D fp32 each).
+    __host__ __device__ static constexpr uint32_t tm_s(int t) { return t ? 128u : 0u; }
+    __host__ __device__ static constexpr uint32_t tm_o(int t) { return 256u + (t ? (uint32_t)D : 0u); }
     static constexpr uint32_t kTmemCols = 512;
-    static_assert(QT * (BN + D) <= 512, "TMEM budget");
-    static_assert(P_TMEM || BN == 128, "P staged in shared memory: 128-key tiles");
-    static_assert(!F8 || (QT == 2 && BN == 128), "FP8 Q, K: one k-block scale per 128-key tile");
+    static_assert(256 + 2 * D <= 512, "TMEM budget");
     static_assert(kSmemBytes <= 232448, "shared memory budget");
-    // 128 threads arrive per phase on these
+    // 128 threads arrive per phase on these; one arrival (expect_tx or commit) on the rest
     __host__ __device__ static constexpr bool per_thread_bar(int i) {
-        return (i >= kBarPFull && i < kBarPFull + QT) || (i >= kBarOEmpty && i < kBarOEmpty + QT);
-    }
-    __host__ __device__ static constexpr bool ring_empty_bar(int i) {
-        return (i >= kBarKEmpty && i < kBarKEmpty + kKSt) || (i >= kBarVEmpty && i < kBarVEmpty + kVSt);
+        return (i >= kBarPFull && i < kBarPFull + kQT) || (i >= kBarOEmpty && i < kBarOEmpty + kQT);
     }
 };
 
-// One work unit: QT x 128 query rows of one (batch, head) and the key-tile
-// count of each of its 128-row tiles.
-template <int QT>
+// One work unit: 256 query rows of one (batch, head) and the key-tile count
+// of each of its two 128-row tiles.
 struct Unit {
     int b, hq, g, row0;
-    int n[QT];
+    int n[kQT];
 };
 
-// Number of BN-key tiles a 128-row query tile starting at row `rs` must visit.
-template <int BN>
+// Number of key tiles a 128-row query tile starting at row `rs` must visit.
 __device__ __forceinline__ int kv_tiles_for(int rs, const FwdParams& p) {
     if (rs >= p.Nq) return 0;
-    if (!p.causal) return (p.Nk + BN - 1) / BN;
+    if (!p.causal) return (p.Nk + kBN - 1) / kBN;
     const int re = min(rs + kBM, p.Nq) - 1;
     const long long last = llmin((long long)p.Nk - 1, (long long)re + (p.Nk - p.Nq));
-    return last < 0 ? 0 : (int)(last / BN) + 1;
+    return last < 0 ? 0 : (int)(last / kBN) + 1;
 }
 
 // The k-th unit of this CTA (snake order over a longest-first list), or -1.
@@ -207,29 +190,26 @@ __device__ __forceinline__ int unit_index(int k, const FwdParams& p) {
     return u < p.num_units ? (int)u : -1;
 }
 
-template <int QT, int BN>
-__device__ __forceinline__ Unit<QT> unit_at(int u, const FwdParams& p) {
+__device__ __forceinline__ Unit unit_at(int u, const FwdParams& p) {
     const int BH = p.B * p.Hq;
     const int bh = u % BH;
     const int pr = u / BH;
-    const int grp = p.causal ? (p.num_row_units - 1 - pr) : pr;
-    Unit<QT> x;
+    const int pair = p.causal ? (p.num_pairs - 1 - pr) : pr;
+    Unit x;
     x.hq = bh % p.Hq;
     x.b = bh / p.Hq;
     x.g = x.hq / p.G;
-    x.row0 = grp * (QT * kBM);
+    x.row0 = pair * (kQT * kBM);
 #pragma unroll
-    for (int t = 0; t < QT; ++t) x.n[t] = kv_tiles_for<BN>(x.row0 + t * kBM, p);
+    for (int t = 0; t < kQT; ++t) x.n[t] = kv_tiles_for(x.row0 + t * kBM, p);
     return x;
 }
 
-template <int D, bool P_TMEM, bool POLY, bool F8, int QT, int BN, int NI>
-__global__ void __launch_bounds__(Shape<QT, BN>::kThreads, 1)
+template <int D, bool P_TMEM, bool POLY, bool F8>
+__global__ void __launch_bounds__(kThreads, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
-    using L = Layout<D, P_TMEM, F8, QT, BN>;
-    using W = Shape<QT, BN>;
-    static_assert(NI == 1 || NI == QT, "one issuer, or one per query tile");
+    using L = Layout<D, P_TMEM, F8>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -242,11 +222,7 @@ __global__ void __launch_bounds__(Shape<QT, BN>::kThreads, 1)
 
     // ---- set-up: barriers, TMEM
     if (threadIdx.x == 0) {
-        // 128 softmax threads arrive on the P-full and O-empty barriers, one
-        // commit per issuer on the K and V ring's empty barriers, one arrival
-        // (expect_tx or commit) on the rest
-        for (int i = 0; i < L::kNumBars; ++i)
-            mbar_init(bar(i), L::per_thread_bar(i) ? 128u : L::ring_empty_bar(i) ? (uint32_t)NI : 1u);
+        for (int i = 0; i < L::kNumBars; ++i) mbar_init(bar(i), L::per_thread_bar(i) ? 128u : 1u);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -259,21 +235,21 @@ __global__ void __launch_bounds__(Shape<QT, BN>::kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     if (warp < 4) {
-      warpgroup_reg_dealloc<W::kRegsWG0>();
+      warpgroup_reg_dealloc<kRegsWG0>();
       if (warp == 0) {
         // ================================================= TMA producer
         if (lane == 0) {
             prefetch_tmap(&tmQ);
             prefetch_tmap(&tmK);
             prefetch_tmap(&tmV);
-            int kv = 0;          // key tiles loaded so far (ring position)
-            int q_loads[QT] = {};  // Q_t loads so far
+            int kv = 0;                 // key tiles loaded so far (ring position)
+            int q_loads[kQT] = {0, 0};  // Q_t loads so far
             bool ok = true;
             for (int k = 0; ok; ++k) {
                 const int u = unit_index(k, p);
                 if (u < 0) break;
-                const Unit<QT> x = unit_at<QT, BN>(u, p);
-                for (int t = 0; t < QT && ok; ++t) {
+                const Unit x = unit_at(u, p);
+                for (int t = 0; t < kQT && ok; ++t) {
                     if (x.n[t] == 0) continue;
                     if (q_loads[t] > 0)  // the previous unit's last S_t has read Q_t
                         ok = mbar_wait(bar(L::kBarQEmpty + t), (q_loads[t] - 1) & 1, abort_flag,
@@ -286,9 +262,7 @@ __global__ void __launch_bounds__(Shape<QT, BN>::kThreads, 1)
                                     x.row0 + t * kBM, x.b);
                     ++q_loads[t];
                 }
-                int n = 0;
-#pragma unroll
-                for (int t = 0; t < QT; ++t) n = max(n, x.n[t]);
+                const int n = max(x.n[0], x.n[1]);
                 for (int j = 0; j < n && ok; ++j, ++kv) {
                     // Fault injection for tests: block 0 never loads ring position
                     // skip_load, so the waits for it run out (production: -1).
@@ -301,7 +275,7 @@ __global__ void __launch_bounds__(Shape<QT, BN>::kThreads, 1)
                         mbar_arrive_expect_tx(bar(L::kBarKFull + ks), L::kKBytes);
                         for (int pp = 0; pp < L::kQKPanels; ++pp)
                             tma_load_4d(sbase + L::kOffK + ks * L::kKBytes + pp * kPanelBytes, &tmK,
-                                        bar(L::kBarKFull + ks), (128 / L::kQKElem) * pp, x.g, j * BN, x.b);
+                                        bar(L::kBarKFull + ks), (128 / L::kQKElem) * pp, x.g, j * kBN, x.b);
                     }
                     const int vs = kv % L::kVSt;
                     ok = mbar_wait(bar(L::kBarVEmpty + vs), ((kv / L::kVSt) & 1) ^ 1, abort_flag,
@@ -311,34 +285,22 @@ __global__ void __launch_bounds__(Shape<QT, BN>::kThreads, 1)
                         mbar_arrive_expect_tx(bar(L::kBarVFull + vs), L::kKVBytes);
                         for (int pp = 0; pp < L::kPanels; ++pp)
                             tma_load_4d(sbase + L::kOffV + vs * L::kKVBytes + pp * kPanelBytes, &tmV,
-                                        bar(L::kBarVFull + vs), 64 * pp, x.g, j * BN, x.b);
+                                        bar(L::kBarVFull + vs), 64 * pp, x.g, j * kBN, x.b);
                     }
                 }
             }
         }
-      } else if (warp <= NI) {
-        // ================================================= MMA issuers
-        // NI warps issue the tcgen05 MMAs: with NI = 1 warp 1 issues every
-        // tile's products; with NI = QT warp 1 + t issues those of query tile
-        // t, so the issue work is spread over as many SM sub-partitions.  An
-        // issuer warp runs its loop convergent, so addresses and descriptors
-        // stay warp-uniform, and one elected lane issues every tcgen05
-        // instruction (always the same lane: commit tracks per thread).  Each
-        // buffer's descriptor is built once; a k-step only adds a compile-time
-        // offset (16-byte units) to its start-address field.  The issue path
-        // is kept short: an issuer shares its SM sub-partition with QT busy
-        // softmax warps.
-        //
-        // Per key tile j an issuer runs, for each of its tiles in order,
-        // PV_t(j) then S_t(j+1); the K and V ring slots take one arrival per
-        // issuer (tcgen05.commit: it lands once the issuer's earlier products
-        // have read the slot).  An issuer whose tiles do not use key tile j
-        // still waits for it to arrive before releasing it, so that no
-        // arrival can run ahead into a later phase of the same slot.
+      } else if (warp == 1) {
+        // ================================================= MMA issuer
+        // The whole warp runs the issue loop convergent, so addresses and
+        // descriptors stay warp-uniform, and one elected lane issues every
+        // tcgen05 instruction.  Each buffer's descriptor is built once; a
+        // k-step only adds a compile-time offset (16-byte units) to its
+        // start-address field.  Keeping the issue path this short matters: the
+        // warp shares its SM sub-partition with two busy softmax warps.
         {
-            const int issuer = warp - 1;
-            constexpr uint32_t kIdS = idesc_bf16_f32(kBM, BN, false);
-            constexpr uint32_t kIdS8 = idesc_e4m3_f32(kBM, BN);
+            constexpr uint32_t kIdS = idesc_bf16_f32(kBM, kBN, false);
+            constexpr uint32_t kIdS8 = idesc_e4m3_f32(kBM, kBN);
             constexpr uint32_t kIdPV = idesc_bf16_f32(kBM, D, true);
             constexpr uint32_t kHi = sdesc_sw128_hi(1024);  // every operand: 8-row groups 1024 B apart
             // V is [keys][D] with D contiguous: an N-major B operand.  Along N the
@@ -348,23 +310,19 @@ __global__ void __launch_bounds__(Shape<QT, BN>::kThreads, 1)
             auto wait = [&](uint32_t b, uint32_t parity) {
                 return mbar_wait_warp(b, parity, abort_flag, &g_fwd_status, p.wait_limit);
             };
-            auto mine = [&](int t) { return NI == 1 || t == issuer; };
             bool ok = true;
             int kv = 0;                     // ring position of the unit's first key tile
-            int q_waits[QT] = {};           // Q_t phases consumed
-            int p_waits[QT] = {};           // P_t phases consumed
-            int units_t[QT] = {};           // units in which tile t was active
+            int q_waits[kQT] = {0, 0};      // Q_t phases consumed
+            int p_waits[kQT] = {0, 0};      // P_t phases consumed
+            int units_t[kQT] = {0, 0};      // units in which tile t was active
             unsigned long long tiles = 0;
             for (int k = 0; ok; ++k) {
                 const int u = unit_index(k, p);
                 if (u < 0) break;
-                const Unit<QT> x = unit_at<QT, BN>(u, p);
-                int n = 0;
-#pragma unroll
-                for (int t = 0; t < QT; ++t) n = max(n, x.n[t]);
-#pragma unroll
-                for (int t = 0; t < QT; ++t) {
-                    if (!mine(t) || x.n[t] == 0 || !ok) continue;
+                const Unit x = unit_at(u, p);
+                const int n = max(x.n[0], x.n[1]);
+                for (int t = 0; t < kQT && ok; ++t) {
+                    if (x.n[t] == 0) continue;
                     ok = wait(bar(L::kBarQFull + t), q_waits[t] & 1);
                     ++q_waits[t];
                 }
@@ -385,7 +343,7 @@ __global__ void __launch_bounds__(Shape<QT, BN>::kThreads, 1)
                         v_ready = j;
                     }
                 };
-                // S_t = Q_t K_j^T  (M=128 rows, N=BN keys, K=D in steps of 16)
+                // S_t = Q_t K_j^T  (M=128 rows, N=128 keys, K=D in steps of 16)
                 auto issue_s = [&](int t, int j) {
                     wait_k(j);
                     if (!ok) return;
@@ -406,7 +364,7 @@ __global__ void __launch_bounds__(Shape<QT, BN>::kThreads, 1)
                     tc_commit_elect(bar(L::kBarSFull + t));
                     if (j == x.n[t] - 1) tc_commit_elect(bar(L::kBarQEmpty + t));  // Q_t fully read
                 };
-                // O_t += P_t V_j  (M=128 rows, N=D, K=BN keys in steps of 16)
+                // O_t += P_t V_j  (M=128 rows, N=D, K=128 keys in steps of 16)
                 auto issue_pv = [&](int t, int j) {
                     wait_v(j);
                     if (!ok) return;
@@ -420,7 +378,7 @@ __global__ void __launch_bounds__(Shape<QT, BN>::kThreads, 1)
                         sdesc_sw128_lo(sbase + L::kOffV + ((kv + j) % L::kVSt) * L::kKVBytes, kVLbo);
                     const uint32_t dO = tmem + L::tm_o(t);
 #pragma unroll
-                    for (int kk = 0; kk < BN / 16; ++kk) {
+                    for (int kk = 0; kk < kBN / 16; ++kk) {
                         const uint32_t v_off = (kk * 16 * 128) >> 4;  // 16 keys of 128 B rows
                         const uint32_t acc = (j > 0 || kk > 0) ? 1u : 0u;
                         if constexpr (P_TMEM) {
@@ -437,44 +395,25 @@ __global__ void __launch_bounds__(Shape<QT, BN>::kThreads, 1)
                         ++units_t[t];
                     }
                 };
-                // release key tile j's K (V) slot: this issuer's arrival, after
-                // its products that read it
-                auto release_k = [&](int j) {
-                    wait_k(j);
-                    if (ok) tc_commit_elect(bar(L::kBarKEmpty + (kv + j) % L::kKSt));
-                };
-                auto release_v = [&](int j) {
-                    wait_v(j);
-                    if (ok) tc_commit_elect(bar(L::kBarVEmpty + (kv + j) % L::kVSt));
-                };
-#pragma unroll
-                for (int t = 0; t < QT; ++t)
-                    if (mine(t) && x.n[t] > 0) issue_s(t, 0);
-                if (n > 0) release_k(0);
-                // Per key tile: PV_0(j), S_0(j+1), PV_1(j), S_1(j+1), ... over this
-                // issuer's tiles; V_j is released after its last PV, K_{j+1} after
-                // its last S.
+                if (x.n[0] > 0) issue_s(0, 0);
+                if (x.n[1] > 0) issue_s(1, 0);
+                if (n > 0 && ok) tc_commit_elect(bar(L::kBarKEmpty + kv % L::kKSt));
                 for (int j = 0; j < n && ok; ++j) {
-                    constexpr int kLast = QT - 1;
-#pragma unroll
-                    for (int t = 0; t < QT; ++t) {
-                        if (!mine(t)) continue;
-                        if (j < x.n[t]) issue_pv(t, j);
-                        if (NI == 1 ? t == kLast : true) release_v(j);
-                        if (j + 1 < x.n[t]) issue_s(t, j + 1);
-                    }
-                    if (j + 1 < n) release_k(j + 1);
+                    if (j < x.n[0]) issue_pv(0, j);
+                    if (j + 1 < x.n[0]) issue_s(0, j + 1);
+                    if (j < x.n[1]) issue_pv(1, j);
+                    if (ok) tc_commit_elect(bar(L::kBarVEmpty + (kv + j) % L::kVSt));
+                    if (j + 1 < x.n[1]) issue_s(1, j + 1);
+                    if (j + 1 < n && ok) tc_commit_elect(bar(L::kBarKEmpty + (kv + j + 1) % L::kKSt));
                 }
                 kv += n;
-#pragma unroll
-                for (int t = 0; t < QT; ++t)
-                    if (mine(t)) tiles += (unsigned long long)x.n[t];
+                tiles += (unsigned long long)(x.n[0] + x.n[1]);
             }
             if (ok && tiles && lane == 0) atomicAdd(&g_fwd_tiles, tiles);
         }
       }
     } else {
-        warpgroup_reg_alloc<W::kRegsSoftmax>();
+        warpgroup_reg_alloc<kRegsSoftmax>();
         // ================================================= softmax warpgroups
         const int t = (warp - 4) >> 2;
         const int q4 = warp & 3;  // TMEM lane quarter this warp may access
@@ -488,7 +427,7 @@ __global__ void __launch_bounds__(Shape<QT, BN>::kThreads, 1)
         for (int k = 0; ok; ++k) {
             const int u = unit_index(k, p);
             if (u < 0) break;
-            const Unit<QT> x = unit_at<QT, BN>(u, p);
+            const Unit x = unit_at(u, p);
             const int rs = x.row0 + t * kBM;
             const int row = rs + r;
             const int nt = x.n[t];
@@ -523,37 +462,33 @@ __global__ void __launch_bounds__(Shape<QT, BN>::kThreads, 1)
                 }
                 ++s_waits;
                 tc_fence_after();
-                uint32_t s[BN];
-                if constexpr (BN == 128)
-                    tmem_ld128_sync(tS, s);
-                else
-                    tmem_ld96_sync(tS, s);
-                const int col0 = j * BN;
-                const bool need_mask = (col0 + BN > p.Nk) ||
-                                       (p.causal && (long long)(col0 + BN - 1) > diag_tile);
+                uint32_t s[kBN];
+                tmem_ld128_sync(tS, s);
+                const int col0 = j * kBN;
+                const bool need_mask = (col0 + kBN > p.Nk) ||
+                                       (p.causal && (long long)(col0 + kBN - 1) > diag_tile);
                 if (need_mask) {
                     // The allowed keys of a row form a prefix of the tile: columns
                     // [0, lim) with lim = min(Nk, last causal key + 1) - col0, clamped
-                    // to [0, BN].  One compare against a constant per score.
+                    // to [0, kBN].  One compare against a constant per score.
                     long long end = p.Nk;
                     if (p.causal && diag + 1 < end) end = diag + 1;
                     end -= col0;
-                    const int lim = end < 0 ? 0 : end > BN ? BN : (int)end;
+                    const int lim = end < 0 ? 0 : end > kBN ? kBN : (int)end;
 #pragma unroll
-                    for (int c = 0; c < BN; ++c)
+                    for (int c = 0; c < kBN; ++c)
                         if (c >= lim) s[c] = __float_as_uint(-INFINITY);
                 }
-                // row max: 8 independent chains of three-input maxima (chain i
-                // takes columns i, i + 8, i + 16, ...)
+                // row max: 8 independent chains of three-input maxima
                 float mx[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
                     mx[i] = fmax3(__uint_as_float(s[i]), __uint_as_float(s[i + 8]),
                                   __uint_as_float(s[i + 16]));
 #pragma unroll
-                    for (int c = 24; c + 8 < BN; c += 16)
+                    for (int c = 24; c < 120; c += 16)
                         mx[i] = fmax3(mx[i], __uint_as_float(s[c + i]), __uint_as_float(s[c + 8 + i]));
-                    if constexpr ((BN / 8 - 3) % 2 == 1) mx[i] = fmaxf(mx[i], __uint_as_float(s[BN - 8 + i]));
+                    mx[i] = fmaxf(mx[i], __uint_as_float(s[120 + i]));
                 }
                 const float m_tile = fmaxf(fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]),
                                                  mx[6]), mx[7]) * slj;
@@ -572,9 +507,9 @@ __global__ void __launch_bounds__(Shape<QT, BN>::kThreads, 1)
                 const uint64_t sl2 = f2_pack(slj, slj);
                 const uint64_t nm2 = f2_pack(-m_use, -m_use);
                 uint64_t sum2[2] = {0ull, 0ull};
-                uint32_t pk[BN / 2];
+                uint32_t pk[kBN / 2];
 #pragma unroll
-                for (int c = 0; c < BN / 2; ++c) {
+                for (int c = 0; c < kBN / 2; ++c) {
                     const uint64_t x = f2_fma(f2_pack(__uint_as_float(s[2 * c]),
                                                       __uint_as_float(s[2 * c + 1])), sl2, nm2);
                     float p0, p1;
@@ -589,7 +524,7 @@ __global__ void __launch_bounds__(Shape<QT, BN>::kThreads, 1)
                     sum2[c & 1] = f2_add(sum2[c & 1], f2_pack(p0, p1));
                     pk[c] = pack_bf16(p0, p1);
                     if constexpr (P_TMEM) {
-                        if (c == 31) tmem_st32(tS, pk);  // the first 32 columns out while computing the rest
+                        if (c == 31) tmem_st32(tS, pk);  // first half out while computing the rest
                     }
                 }
                 const uint64_t sum = f2_add(sum2[0], sum2[1]);
@@ -600,10 +535,7 @@ __global__ void __launch_bounds__(Shape<QT, BN>::kThreads, 1)
                 const float tile_sum = m_new == -INFINITY ? 0.f : f2_lo(sum) + f2_hi(sum);
                 l = fmaf(l, alpha, tile_sum);
                 if constexpr (P_TMEM) {
-                    if constexpr (BN == 128)
-                        tmem_st32(tS + 32, pk + 32);
-                    else
-                        tmem_st16(tS + 32, pk + 32);
+                    tmem_st32(tS + 32, pk + 32);
                 } else {
                     const uint32_t pa = sbase + L::kOffP + t * L::kPBytes;
 #pragma unroll
@@ -677,25 +609,24 @@ __global__ void __launch_bounds__(Shape<QT, BN>::kThreads, 1)
     }
 }
 
-template <int D, bool P_TMEM, bool POLY, bool F8 = false, int QT = 2, int BN = 128, int NI = 1>
+template <int D, bool P_TMEM, bool POLY, bool F8 = false>
 attn_status_t launch_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                           int Hq, int Hkv, int Nq, int Nk, float scale, int causal,
                           cudaStream_t stream, const attn_test_options_t* test, long long lse_ld,
                           const float* q_scales = nullptr, const float* k_scales = nullptr) {
-    using L = Layout<D, P_TMEM, F8, QT, BN>;
-    using W = Shape<QT, BN>;
+    using L = Layout<D, P_TMEM, F8>;
     CUtensorMap mq, mk, mv;
     if (!attn_host::encode_bshd_map(&mq, q, B, Nq, Hq, D, kBM, L::kQKElem) ||
-        !attn_host::encode_bshd_map(&mk, k, B, Nk, Hkv, D, BN, L::kQKElem) ||
-        !attn_host::encode_bshd_map(&mv, v, B, Nk, Hkv, D, BN, 2))
+        !attn_host::encode_bshd_map(&mk, k, B, Nk, Hkv, D, kBN, L::kQKElem) ||
+        !attn_host::encode_bshd_map(&mv, v, B, Nk, Hkv, D, kBN, 2))
         return ATTN_ERR_CUDA;
-    // The register split inside the kernel assumes exactly W::kLaunchRegs per
+    // The register split inside the kernel assumes exactly kLaunchRegs per
     // thread at launch; refuse to launch a build that differs (the split's
     // register increase would otherwise wait forever).
     const attn_host::KernelSetup ks =
-        attn_host::kernel_setup<fwd_tc_kernel<D, P_TMEM, POLY, F8, QT, BN, NI>>(L::kSmemBytes);
+        attn_host::kernel_setup<fwd_tc_kernel<D, P_TMEM, POLY, F8>>(L::kSmemBytes);
     if (ks.err != cudaSuccess) return ATTN_ERR_CUDA;
-    if (ks.num_regs != W::kLaunchRegs) return ATTN_ERR_UNSUPPORTED;
+    if (ks.num_regs != kLaunchRegs) return ATTN_ERR_UNSUPPORTED;
     FwdParams prm;
     prm.lse = lse;
     prm.lse_ld = lse_ld > 0 ? lse_ld : Nq;
@@ -707,8 +638,8 @@ attn_status_t launch_impl(const void* q, const void* k, const void* v, void* o, 
     prm.Nk = Nk;
     prm.G = Hq / Hkv;
     prm.causal = causal;
-    prm.num_row_units = (Nq + QT * kBM - 1) / (QT * kBM);
-    const long long units = (long long)prm.num_row_units * B * Hq;
+    prm.num_pairs = (Nq + kQT * kBM - 1) / (kQT * kBM);
+    const long long units = (long long)prm.num_pairs * B * Hq;
     if (units > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
     prm.num_units = (int)units;
     prm.scale_log2 = scale * 1.4426950408889634f;
@@ -721,11 +652,11 @@ attn_status_t launch_impl(const void* q, const void* k, const void* v, void* o, 
     prm.q_scales = q_scales;
     prm.k_scales = k_scales;
     prm.nqb = (Nq + kBM - 1) / kBM;
-    prm.nkb = (Nk + BN - 1) / BN;
+    prm.nkb = (Nk + kBN - 1) / kBN;
     const int sms = attn_host::device_sm_count();
     if (sms <= 0) return ATTN_ERR_CUDA;
     const int grid = (int)(units < sms ? units : sms);
-    fwd_tc_kernel<D, P_TMEM, POLY, F8, QT, BN, NI><<<grid, W::kThreads, L::kSmemBytes, stream>>>(mq, mk, mv, prm);
+    fwd_tc_kernel<D, P_TMEM, POLY, F8><<<grid, kThreads, L::kSmemBytes, stream>>>(mq, mk, mv, prm);
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
@@ -737,33 +668,18 @@ attn_status_t launch_fwd_tc(const void* q, const void* k, const void* v, void* o
                             int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal,
                             float scale, cudaStream_t stream, const attn_test_options_t* test,
                             long long lse_ld) {
-    // Production: P in tensor memory, every exponential on MUFU; work units of
-    // two 128-row tiles, 128-key tiles, one MMA-issuing warp.  The other
+    // Production: P in tensor memory, every exponential on MUFU.  The other
     // variants are reached only through attn_fwd_test.
     const bool smem_p = test && test->p_in_smem;
     const bool poly = test && test->exp2_poly;
-    const int tiles = (test && test->fwd_tiles) ? test->fwd_tiles : 2;
-    const int issuers = (test && test->mma_issuers) ? test->mma_issuers : 1;
-    if (tiles == 3 && (d != 64 || smem_p || poly)) return ATTN_ERR_UNSUPPORTED;
-    if (issuers != 1 && (issuers != tiles || smem_p || poly)) return ATTN_ERR_UNSUPPORTED;
-    const bool multi = issuers > 1;
-#define ATTN_FWD_ARGS q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, stream, test, lse_ld
-    if (d == 128) {
-        if (smem_p) return launch_impl<128, false, false>(ATTN_FWD_ARGS);
-        if (poly) return launch_impl<128, true, true>(ATTN_FWD_ARGS);
-        return multi ? launch_impl<128, true, false, false, 2, 128, 2>(ATTN_FWD_ARGS)
-                     : launch_impl<128, true, false>(ATTN_FWD_ARGS);
-    }
-    if (d == 64) {
-        if (tiles == 3)
-            return multi ? launch_impl<64, true, false, false, 3, 96, 3>(ATTN_FWD_ARGS)
-                         : launch_impl<64, true, false, false, 3, 96, 1>(ATTN_FWD_ARGS);
-        if (smem_p) return launch_impl<64, false, false>(ATTN_FWD_ARGS);
-        if (poly) return launch_impl<64, true, true>(ATTN_FWD_ARGS);
-        return multi ? launch_impl<64, true, false, false, 2, 128, 2>(ATTN_FWD_ARGS)
-                     : launch_impl<64, true, false>(ATTN_FWD_ARGS);
-    }
-#undef ATTN_FWD_ARGS
+    if (d == 128)
+        return smem_p ? launch_impl<128, false, false>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, stream, test, lse_ld)
+               : poly ? launch_impl<128, true, true>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, stream, test, lse_ld)
+                      : launch_impl<128, true, false>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, stream, test, lse_ld);
+    if (d == 64)
+        return smem_p ? launch_impl<64, false, false>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, stream, test, lse_ld)
+               : poly ? launch_impl<64, true, true>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, stream, test, lse_ld)
+                      : launch_impl<64, true, false>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, stream, test, lse_ld);
     return ATTN_ERR_UNSUPPORTED;
 }
 

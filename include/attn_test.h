@@ -53,23 +53,12 @@ typedef struct {
      * (0 = the first key tile it loads); decode, this tile of the block's
      * segment (0 = its first 64 keys). */
     int skip_load;
-    /* forward only: query tiles per work unit; 0 = the production choice
-     * (2, with 128-key tiles); 3 = three 128-row tiles with 96-key tiles
-     * (d = 64 only: three S and O accumulators fit tensor memory), else
-     * ATTN_ERR_UNSUPPORTED. */
-    int fwd_tiles;
-    /* forward only: MMA-issuing warps; 0 = the production choice (1);
-     * 1 = one warp issues every tile's products; otherwise one warp per
-     * query tile (must equal the tiles per unit; not with p_in_smem or
-     * exp2_poly), else ATTN_ERR_UNSUPPORTED. */
-    int mma_issuers;
 } attn_test_options_t;
 
 /*
  * attn_fwd_test -- attn_fwd (ATTN_BF16 only) with the options above.  Same
  * arguments, layouts and errors as attn_fwd, plus ATTN_ERR_INVALID for a
- * NULL `opt`, a threshold outside [0, 8], a negative wait bound,
- * fwd_tiles other than 0, 2 or 3, or mma_issuers outside 0..3.
+ * NULL `opt`, a threshold outside [0, 8] or a negative wait bound.
  */
 attn_status_t attn_fwd_test(const void* q, const void* k, const void* v, void* o,
                             float* lse, int B, int Hq, int Hkv, int Nq, int Nk, int d,

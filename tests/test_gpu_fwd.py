@@ -174,80 +174,3 @@ def test_test_entry_point_defaults_equal_production(attn):
     o2, l2 = attn.attn_fwd_test(q, k, v, True, 0.088, attn.AttnTestOptions())
     torch.cuda.synchronize()
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
-
-
-@pytest.mark.parametrize("B,Hq,Hkv,Nq,Nk,causal,qs", [
-    (8, 12, 12, 1000, 1000, False, 1.0),   # the ragged workload
-    (8, 12, 12, 1000, 1000, True, 1.0),
-    (8, 12, 12, 1000, 1000, True, 8.0),    # near one-hot rows
-    (2, 8, 2, 513, 2000, False, 1.0),      # GQA, Nq < Nk
-    (1, 4, 4, 1000, 300, True, 1.0),       # Nq > Nk: leading rows have no key
-    (1, 2, 1, 1, 1000, True, 1.0),         # one query over 1000 keys
-    (1, 1, 1, 1, 1, False, 1.0),           # a single key
-    (2, 4, 2, 129, 97, True, 1.0),         # just past one tile and one 96-key tile
-    (3, 6, 3, 777, 777, True, 1.0),
-    (1, 2, 2, 385, 385, False, 1.0),       # just past one unit of three tiles
-])
-def test_three_tiles_per_unit_d64(attn, oracle_mod, B, Hq, Hkv, Nq, Nk, causal, qs):
-    """d = 64 with three 128-row query tiles per work unit and 96-key tiles
-    (three softmax warpgroups sharing one tensor pipe) matches the oracle
-    within tolerance and writes nothing outside O and LSE."""
-    d = 64
-    q, k, v = make_qkv(B, Hq, Hkv, Nq, Nk, d, 60 + Nq, q_scale=qs)
-    scale = 1.0 / math.sqrt(d)
-    o, ob, og = guarded((B, Nq, Hq, d), torch.bfloat16, DEV)
-    lse, lb, lg = guarded((B, Hq, Nq), torch.float32, DEV)
-    opt = attn.AttnTestOptions(fwd_tiles=3)
-    attn.attn_fwd_test(q.to(DEV), k.to(DEV), v.to(DEV), causal, scale, opt, o=o, lse=lse)
-    torch.cuda.synchronize()
-    assert attn.attn_check_device_status() == 0
-    assert guards_intact(ob, og) and guards_intact(lb, lg), "write outside O/LSE"
-    o_ref, lse_ref = oracle_mod.attn_fwd(q, k, v, causal, scale)
-    compare(o, lse, o_ref, lse_ref, torch.bfloat16,
-            "three tiles B%d Hq%d Hkv%d Nq%d Nk%d d64 causal%d q_scale%g" % (B, Hq, Hkv, Nq, Nk, causal, qs))
-
-
-def test_three_tiles_need_d64(attn):
-    q, k, v = (x.to(DEV) for x in make_qkv(1, 2, 2, 300, 300, 128, 1))
-    with pytest.raises(attn.AttnError):
-        attn.attn_fwd_test(q, k, v, True, 0.1, attn.AttnTestOptions(fwd_tiles=3))
-
-
-@pytest.mark.parametrize("tiles,issuers", [(2, 2), (3, 3)], ids=["two_tiles_two_issuers", "three_tiles_three_issuers"])
-@pytest.mark.parametrize("B,Hq,Hkv,Nq,Nk,d,causal,qs", [
-    (8, 12, 12, 1000, 1000, 64, False, 1.0),
-    (8, 12, 12, 1000, 1000, 64, True, 8.0),
-    (2, 8, 2, 513, 2000, 64, False, 1.0),
-    (1, 4, 4, 1000, 300, 64, True, 1.0),      # Nq > Nk: leading rows have no key
-    (1, 2, 1, 1, 1000, 64, True, 1.0),
-    (3, 6, 3, 777, 777, 64, True, 1.0),
-    (2, 4, 2, 777, 777, 128, True, 1.0),      # d = 128 (two tiles only)
-    (1, 2, 2, 300, 1000, 128, True, 1.0),
-])
-def test_one_mma_issuer_per_tile(attn, oracle_mod, tiles, issuers, B, Hq, Hkv, Nq, Nk, d, causal, qs):
-    """One MMA-issuing warp per query tile (the K/V ring released by one
-    arrival per issuer) matches the oracle, with two tiles of 128 keys or
-    (d = 64) three tiles of 96 keys per unit."""
-    if d != 64 and tiles == 3:
-        pytest.skip("three tiles per unit need d = 64")
-    q, k, v = make_qkv(B, Hq, Hkv, Nq, Nk, d, 70 + Nq, q_scale=qs)
-    scale = 1.0 / math.sqrt(d)
-    o, ob, og = guarded((B, Nq, Hq, d), torch.bfloat16, DEV)
-    lse, lb, lg = guarded((B, Hq, Nq), torch.float32, DEV)
-    opt = attn.AttnTestOptions(fwd_tiles=tiles, mma_issuers=issuers)
-    attn.attn_fwd_test(q.to(DEV), k.to(DEV), v.to(DEV), causal, scale, opt, o=o, lse=lse)
-    torch.cuda.synchronize()
-    assert attn.attn_check_device_status() == 0
-    assert guards_intact(ob, og) and guards_intact(lb, lg), "write outside O/LSE"
-    o_ref, lse_ref = oracle_mod.attn_fwd(q, k, v, causal, scale)
-    compare(o, lse, o_ref, lse_ref, torch.bfloat16, "%d tiles, %d issuers B%d Hq%d Hkv%d Nq%d Nk%d d%d causal%d"
-            % (tiles, issuers, B, Hq, Hkv, Nq, Nk, d, causal))
-
-
-def test_one_issuer_per_tile_counts_every_tile(attn):
-    """The tile counter (one atomic add per issuer) still sees T(T+1)/2
-    causal tiles at N = 4096 with 128 x 128 tiles."""
-    q, k, v = (x.to(DEV) for x in make_qkv(1, 1, 1, 4096, 4096, 128, seed=4))
-    attn.attn_read_tile_counter(reset=True)
-    attn.attn_fwd_test(q, k, v, True, 0.1, attn.AttnTestOptions(mma_issuers=2))
-    assert attn.attn_read_tile_counter(reset=True) == 32 * 33 // 2
