@@ -39,7 +39,6 @@
 //  * Key tiles that are fully masked by causality are never loaded or
 //    computed (Lecture 11, section 5.3).
 #include <cstdio>
-#include <type_traits>
 
 #include "common.cuh"
 #include "ptx.cuh"
@@ -503,90 +502,70 @@ __global__ void __launch_bounds__(kThreads, 1)
                     alpha = ex2(m - m_new);  // 0 on the first non-empty tile
                 }
                 const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-                // O_t holds the sum through key tile j-1 (its PV completed before S_t(j)
-                // did).  If some row of the warp moved its reference, O_t is brought to
-                // the new one in 32-column chunks whose TMEM loads are issued eight
-                // pairs of exponentials ahead of their multiply and store, so the round
-                // trips overlap the MUFU-bound loop below instead of following it.  The
-                // first load waits until the first half of P is out of registers (pair
-                // 31); chunk i is scaled and stored, and chunk i + 1 loaded, after pair
-                // 63 - 8 (chunks - 1 - i); the last chunk after the loop.  The loop is
-                // compiled twice, with and without the rescale, so that neither copy
-                // branches inside.
-                const bool corr = j > 0 && __any_sync(0xffffffffu, alpha != 1.f);
-                constexpr int kOChunks = D / 32;
-                const uint64_t a2 = f2_pack(alpha, alpha);
-                auto rescale_chunk = [&](uint32_t* xo, int ch) {  // chunk ch was loaded into xo
-                    tmem_ld_wait32(xo);
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const uint64_t y = f2_mul(f2_pack(__uint_as_float(xo[2 * i]),
-                                                          __uint_as_float(xo[2 * i + 1])), a2);
-                        xo[2 * i] = __float_as_uint(f2_lo(y));
-                        xo[2 * i + 1] = __float_as_uint(f2_hi(y));
-                    }
-                    tmem_st32(tO + 32 * ch, xo);
-                };
                 // P = exp2(s * scale log2 e - m): the scale-subtract and the row sum run on
-                // packed fp32 pairs, exp2 on the MUFU unit.  Returns the packed row sum.
+                // packed fp32 pairs, exp2 on the MUFU unit.
                 const uint64_t sl2 = f2_pack(slj, slj);
                 const uint64_t nm2 = f2_pack(-m_use, -m_use);
-                auto exp_pass = [&](auto corr_tag) -> uint64_t {
-                    constexpr bool kCorr = decltype(corr_tag)::value;
-                    uint64_t sum2[2] = {0ull, 0ull};
-                    uint32_t pk[kBN / 2];
-                    uint32_t xo[32];
+                uint64_t sum2[2] = {0ull, 0ull};
+                uint32_t pk[kBN / 2];
 #pragma unroll
-                    for (int c = 0; c < kBN / 2; ++c) {
-                        const uint64_t x = f2_fma(f2_pack(__uint_as_float(s[2 * c]),
-                                                          __uint_as_float(s[2 * c + 1])), sl2, nm2);
-                        float p0, p1;
-                        if (POLY && c % kPolyEvery == kPolyEvery - 1) {
-                            const uint64_t y = exp2_poly_x2(f2_lo(x), f2_hi(x));
-                            p0 = f2_lo(y);
-                            p1 = f2_hi(y);
-                        } else {
-                            p0 = ex2(f2_lo(x));
-                            p1 = ex2(f2_hi(x));
-                        }
-                        sum2[c & 1] = f2_add(sum2[c & 1], f2_pack(p0, p1));
-                        pk[c] = pack_bf16(p0, p1);
-                        if constexpr (P_TMEM) {
-                            if (c == 31) tmem_st32(tS, pk);  // first half out while computing the rest
-                        }
-                        if constexpr (kCorr) {
-                            if (c == 31) tmem_ld32(tO, xo);
-                            if (c > 31 && (kBN / 2 - 1 - c) % 8 == 0) {
-                                const int i = kOChunks - 1 - (kBN / 2 - 1 - c) / 8;
-                                if (i >= 0 && i < kOChunks - 1) {
-                                    rescale_chunk(xo, i);
-                                    tmem_ld32(tO + 32 * (i + 1), xo);
-                                }
-                            }
-                        }
-                    }
-                    if constexpr (P_TMEM) {
-                        tmem_st32(tS + 32, pk + 32);
+                for (int c = 0; c < kBN / 2; ++c) {
+                    const uint64_t x = f2_fma(f2_pack(__uint_as_float(s[2 * c]),
+                                                      __uint_as_float(s[2 * c + 1])), sl2, nm2);
+                    float p0, p1;
+                    if (POLY && c % kPolyEvery == kPolyEvery - 1) {
+                        const uint64_t y = exp2_poly_x2(f2_lo(x), f2_hi(x));
+                        p0 = f2_lo(y);
+                        p1 = f2_hi(y);
                     } else {
-                        const uint32_t pa = sbase + L::kOffP + t * L::kPBytes;
-#pragma unroll
-                        for (int c = 0; c < 16; ++c) {  // 16 chunks of 8 keys
-                            const int panel = c >> 3, cc = c & 7;
-                            st_shared_v4(pa + panel * kPanelBytes + r * 128 + ((cc ^ (r & 7)) << 4),
-                                         pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-                        }
-                        fence_proxy_async_smem();
+                        p0 = ex2(f2_lo(x));
+                        p1 = ex2(f2_hi(x));
                     }
-                    if constexpr (kCorr) rescale_chunk(xo, kOChunks - 1);  // the last chunk
-                    return f2_add(sum2[0], sum2[1]);
-                };
-                const uint64_t sum = corr ? exp_pass(std::true_type{}) : exp_pass(std::false_type{});
+                    sum2[c & 1] = f2_add(sum2[c & 1], f2_pack(p0, p1));
+                    pk[c] = pack_bf16(p0, p1);
+                    if constexpr (P_TMEM) {
+                        if (c == 31) tmem_st32(tS, pk);  // first half out while computing the rest
+                    }
+                }
+                const uint64_t sum = f2_add(sum2[0], sum2[1]);
                 // While a row has no finite score its "probabilities" are the
                 // polynomial's clamped 2^-125, not 0: they must not count.  (acc
                 // gets only such values; a later finite score rescales it by
                 // alpha = 0, and with l = 0 the row's O is 0 and its LSE -inf.)
                 const float tile_sum = m_new == -INFINITY ? 0.f : f2_lo(sum) + f2_hi(sum);
                 l = fmaf(l, alpha, tile_sum);
+                if constexpr (P_TMEM) {
+                    tmem_st32(tS + 32, pk + 32);
+                } else {
+                    const uint32_t pa = sbase + L::kOffP + t * L::kPBytes;
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) {  // 16 chunks of 8 keys
+                        const int panel = c >> 3, cc = c & 7;
+                        st_shared_v4(pa + panel * kPanelBytes + r * 128 + ((cc ^ (r & 7)) << 4),
+                                     pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+                    }
+                    fence_proxy_async_smem();
+                }
+                // O_t holds the sum through key tile j-1 (its PV completed before S_t(j)
+                // did); bring it to the new reference if some row of the warp moved.
+                // One TMEM round trip, packed multiplies.
+                if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+                    uint32_t xo[D];
+                    if constexpr (D == 128)
+                        tmem_ld128_sync(tO, xo);
+                    else
+                        tmem_ld64_sync(tO, xo);
+                    const uint64_t a2 = f2_pack(alpha, alpha);
+#pragma unroll
+                    for (int i = 0; i < D / 2; ++i) {
+                        const uint64_t y = f2_mul(f2_pack(__uint_as_float(xo[2 * i]),
+                                                          __uint_as_float(xo[2 * i + 1])), a2);
+                        xo[2 * i] = __float_as_uint(f2_lo(y));
+                        xo[2 * i + 1] = __float_as_uint(f2_hi(y));
+                    }
+#pragma unroll
+                    for (int c = 0; c < D; c += 32) tmem_st32(tO + c, xo + c);
+                }
                 tmem_st_wait();  // P and any rescaled O are in TMEM before the MMA is told
                 tc_fence_before();
                 mbar_arrive(bar(L::kBarPFull + t));

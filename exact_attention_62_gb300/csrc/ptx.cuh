@@ -349,30 +349,7 @@ __device__ __forceinline__ void tmem_ld128_sync(uint32_t taddr, uint32_t* r) {
         : "r"(taddr), "r"(taddr + 32u), "r"(taddr + 64u), "r"(taddr + 96u)
         : "memory");
 }
-// The same 32-column load without the wait: the registers hold the data only
-// after tmem_ld_wait32 on the same array.
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
-        : ATTN_R8(0), ATTN_R8(8), ATTN_R8(16), ATTN_R8(24)
-        : "r"(taddr)
-        : "memory");
-}
 #undef ATTN_R8
-
-// Wait for this thread's earlier tcgen05.ld.  The 32 registers pass through
-// the statement, so no use of them can be scheduled before the wait.
-#define ATTN_RW8(i) "+r"(r[i]), "+r"(r[i + 1]), "+r"(r[i + 2]), "+r"(r[i + 3]), \
-                    "+r"(r[i + 4]), "+r"(r[i + 5]), "+r"(r[i + 6]), "+r"(r[i + 7])
-__device__ __forceinline__ void tmem_ld_wait32(uint32_t* r) {
-    asm volatile("tcgen05.wait::ld.sync.aligned;\n"
-                 : ATTN_RW8(0), ATTN_RW8(8), ATTN_RW8(16), ATTN_RW8(24)
-                 :
-                 : "memory");
-}
-#undef ATTN_RW8
 
 #define ATTN_W8(i) "r"(r[i]), "r"(r[i + 1]), "r"(r[i + 2]), "r"(r[i + 3]), \
                    "r"(r[i + 4]), "r"(r[i + 5]), "r"(r[i + 6]), "r"(r[i + 7])
