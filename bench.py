@@ -543,7 +543,7 @@ def run_ours(args):
                "sample": "%d random rows of the %s prefill (~%.0f s of CPU work), FLOPs counted "
                          "as for the GPU (4 Nk d per row, halved for causal)"
                          % (rows, args.prefill, args.cpu_seconds)}
-    launches_per_step = 1 + (2 if splits > 64 else 1)  # the merge kernel only beyond 64 segments
+    launches_per_step = 1 + (1 if splits == 1 else 2)
     h2d = sum(t.numel() * t.element_size() for t in (q, k, v))
     d2h = o.numel() * o.element_size() + lse.numel() * lse.element_size()
     dh2d = sum(t.numel() * t.element_size() for t in (dq, dk, dv))

@@ -27,14 +27,10 @@
 //    the instruction count far below the memory time.
 //  * At the end the eight warps' states are merged through shared memory
 //    (the same (m, l, acc) merge).  With a single segment the kernel writes
-//    O (bf16) and LSE directly.  With several, each CTA writes its segment's
-//    partial and then arrives on its (sequence, head group) word in the
-//    workspace; the CTA that arrives last merges the group's partials (step
-//    3) before it exits, so no merge launch follows.  No CTA waits for
-//    another: the others just exit.  Beyond kFusedMergeMax segments the
-//    merge kernel is launched instead, as a programmatic dependent.
+//    O (bf16) and LSE directly and no merge kernel runs; otherwise the merge
+//    kernel is launched as a programmatic dependent (one pass over the
+//    partials for up to 4 segments per thread, two passes beyond).
 #include <algorithm>
-#include <atomic>
 #include <cmath>
 #include <mutex>
 
@@ -65,10 +61,6 @@ struct DecParams {
     float scale_log2;
     long long wait_limit;    // bound of every mbarrier wait, SM cycles
     int skip_load;           // tests only: tile of block (0, 0, 0) that is never loaded (-1: none)
-    // several segments merged in the kernel: [B, Hq / GC] arrival words
-    // (high half: the call's tag, low half: CTAs arrived); null: merge kernel
-    unsigned long long* arrivals;
-    unsigned tag;            // this call's tag, never 0
     // paged cache only
     const int* table;        // [B, max_pages] page of each block of page_size keys
     const int* seq_lens;     // [B]
@@ -107,92 +99,6 @@ constexpr int dec_stages() { return D == 128 ? 6 : 8; }
 
 __device__ __forceinline__ uint32_t ld_b32(const __nv_bfloat16* p) {
     return *reinterpret_cast<const uint32_t*>(p);
-}
-
-// Segment counts up to this merge in the split kernel (the last CTA of a
-// group reads every segment's partial, eight at a time); more use the merge
-// kernel, which spreads a row's segments over a whole CTA.
-constexpr int kFusedMergeMax = 64;
-
-// The CTA's arrival on its (sequence, head group) word, by one thread after
-// the CTA's partials are written and fenced.  Returns true for the last of
-// the group's S CTAs, which then resets the word's count to 0 (a replay of
-// the same call, e.g. from a CUDA graph, finds it there).  A word whose tag
-// is not this call's (left by another call, or never written) counts as 0.
-// Each failed compare-and-swap means another CTA's succeeded, so S + 1
-// attempts always suffice; the bound only guards the loop.
-__device__ bool arrive_last(const DecParams& p, int b) {
-    unsigned long long* w = p.arrivals + (long long)b * gridDim.y + blockIdx.y;
-    const unsigned long long tag = (unsigned long long)p.tag << 32;
-    unsigned long long cur = *reinterpret_cast<volatile unsigned long long*>(w);
-    for (int it = 0; it <= p.splits; ++it) {
-        const unsigned long long want = (cur >> 32) == p.tag ? cur + 1 : tag | 1ull;
-        const unsigned long long prev = atomicCAS(w, cur, want);
-        if (prev == cur) {
-            if ((unsigned)want != (unsigned)p.splits) return false;
-            atomicExch(w, tag);
-            return true;
-        }
-        cur = prev;
-    }
-    atomicOr(&g_dec_status, kStatusTimeout);
-    return false;
-}
-
-// Step 3 for one (sequence, head group) by its last CTA: rows hq0 .. hq0+GC-1,
-// o = sum_s e^{lse_s - M} o_s / sum_s e^{lse_s - M}, lse = M + ln of that
-// sum, M the running maximum of the lse_s (section 3.2's merge in lse form,
-// taken over the segments eight at a time).  Thread e of n takes four
-// columns of one row.  The partials are read from L2 (other CTAs wrote them).
-template <int D, int GC>
-__device__ void merge_group(const DecParams& p, int b, int hq0, int tid, int n) {
-    const long long R = (long long)p.B * p.Hq;
-    constexpr int C = D / 4;
-    for (int e = tid; e < GC * C; e += n) {
-        const int qc = e / C, c4 = e % C;
-        const long long row = (long long)b * p.Hq + hq0 + qc;
-        float M = -INFINITY, lsum = 0.f;
-        float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int s0 = 0; s0 < p.splits; s0 += 8) {
-            float ls[8];
-            float4 x[8];
-#pragma unroll
-            for (int r = 0; r < 8; ++r) {
-                const long long s = s0 + r;
-                const bool in = s < p.splits;
-                ls[r] = in ? __ldcg(p.lse_parts + s * R + row) : -INFINITY;
-                x[r] = in ? __ldcg(reinterpret_cast<const float4*>(p.o_parts + (s * R + row) * D) + c4)
-                          : make_float4(0.f, 0.f, 0.f, 0.f);
-            }
-            float mc = M;
-#pragma unroll
-            for (int r = 0; r < 8; ++r) mc = fmaxf(mc, ls[r]);
-            if (mc == -INFINITY) continue;
-            const float sc = expf(M - mc);  // 0 while nothing was summed (M = -inf)
-            a.x *= sc;
-            a.y *= sc;
-            a.z *= sc;
-            a.w *= sc;
-            lsum *= sc;
-            M = mc;
-#pragma unroll
-            for (int r = 0; r < 8; ++r) {
-                if (ls[r] == -INFINITY) continue;
-                const float w = expf(ls[r] - M);
-                a.x = fmaf(w, x[r].x, a.x);
-                a.y = fmaf(w, x[r].y, a.y);
-                a.z = fmaf(w, x[r].z, a.z);
-                a.w = fmaf(w, x[r].w, a.w);
-                lsum += w;
-            }
-        }
-        const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
-        uint2 h;
-        h.x = pack_bf16(a.x * inv, a.y * inv);
-        h.y = pack_bf16(a.z * inv, a.w * inv);
-        *reinterpret_cast<uint2*>(p.o + row * D + 4 * c4) = h;
-        if (c4 == 0) p.lse[row] = lsum > 0.f ? M + logf(lsum) : -INFINITY;
-    }
 }
 
 template <int D, int GC, bool PAGED>
@@ -234,17 +140,6 @@ __global__ void __launch_bounds__(kDecThreads)
                 p.o_parts[((long long)seg * R + row) * D + (e % D)] = 0.f;
                 if (e % D == 0) p.lse_parts[(long long)seg * R + row] = -INFINITY;
             }
-        }
-        if (p.arrivals != nullptr) {  // an empty segment arrives too
-            volatile int* last = reinterpret_cast<volatile int*>(sgen + L::kOffMisc + 4);
-            __threadfence();
-            __syncthreads();
-            if (threadIdx.x == 0) {
-                *last = arrive_last(p, b);
-                __threadfence();
-            }
-            __syncthreads();
-            if (*last) merge_group<D, GC>(p, b, hq0, threadIdx.x, blockDim.x);
         }
         return;
     }
@@ -520,20 +415,6 @@ __global__ void __launch_bounds__(kDecThreads)
             p.o_parts[((long long)seg * R + row) * D + dd] = outv;
             if (dd == 0) p.lse_parts[(long long)seg * R + row] = lsev;
         }
-    }
-    if (p.arrivals != nullptr) {
-        // every consumer's partial stores, then one arrival for the CTA; the
-        // group's last CTA merges (its fence orders the others' partials,
-        // published by their fences and arrivals, before its reads)
-        volatile int* last = reinterpret_cast<volatile int*>(sgen + L::kOffMisc + 4);
-        __threadfence();
-        named_bar_sync(1, 32 * kConsumerWarps);
-        if (threadIdx.x == 32) {
-            *last = arrive_last(p, b);
-            __threadfence();
-        }
-        named_bar_sync(1, 32 * kConsumerWarps);
-        if (*last) merge_group<D, GC>(p, b, hq0, threadIdx.x - 32, 32 * kConsumerWarps);
     }
 }
 
@@ -824,50 +705,12 @@ int decode_auto_splits(int B, int Hq, int Hkv, int Nk, int d) {
     return auto_splits_model(B, Hq, Hkv, Nk, d, kDenseSplitModel, false);
 }
 
-// Workspace of S > 1 segments, R = B*Hq rows: o_parts [S, R, d] float32 at
-// 0, lse_parts [S, R] float32 at round_up(S R d 4, 256), then (S up to
-// kFusedMergeMax) the arrival words, one uint64 per (sequence, head group),
-// at round_up(that + S R 4, 256); R words bound the B * Hq / GC groups.
-struct DecWorkspace {
-    float* o_parts;
-    float* lse_parts;
-    unsigned long long* arrivals;
-};
-
-static size_t ws_lse_offset(size_t rows, int d, int splits) {
-    return ((size_t)splits * rows * d * 4 + 255) / 256 * 256;
-}
-static size_t ws_arrival_offset(size_t rows, int d, int splits) {
-    return (ws_lse_offset(rows, d, splits) + (size_t)splits * rows * 4 + 255) / 256 * 256;
-}
-
 size_t decode_workspace_bytes(int B, int Hq, int d, int splits) {
     if (splits <= 1) return 0;
     const size_t rows = (size_t)B * Hq;
-    if (splits > kFusedMergeMax) return ws_lse_offset(rows, d, splits) + (size_t)splits * rows * 4;
-    return ws_arrival_offset(rows, d, splits) + rows * 8;
-}
-
-static DecWorkspace carve_workspace(void* ws, size_t rows, int d, int splits) {
-    DecWorkspace w = {nullptr, nullptr, nullptr};
-    if (splits <= 1) return w;
-    char* base = static_cast<char*>(ws);
-    w.o_parts = reinterpret_cast<float*>(base);
-    w.lse_parts = reinterpret_cast<float*>(base + ws_lse_offset(rows, d, splits));
-    if (splits <= kFusedMergeMax)
-        w.arrivals = reinterpret_cast<unsigned long long*>(base + ws_arrival_offset(rows, d, splits));
-    return w;
-}
-
-// A fresh tag per launch (never 0), so that arrival words left by any other
-// call, or never written, count as empty.
-static unsigned next_arrival_tag() {
-    static std::atomic<unsigned> counter{0};
-    unsigned t;
-    do {
-        t = counter.fetch_add(1, std::memory_order_relaxed) + 1;
-    } while (t == 0);
-    return t;
+    const size_t o_bytes = (size_t)splits * rows * d * 4;
+    const size_t o_round = (o_bytes + 255) / 256 * 256;
+    return o_round + (size_t)splits * rows * 4;
 }
 
 attn_status_t launch_decode(const void* q, const void* k, const void* v, void* o, float* lse, int B,
@@ -892,17 +735,21 @@ attn_status_t launch_decode(const void* q, const void* k, const void* v, void* o
     prm.wait_limit = (test && test->wait_limit_cycles > 0) ? test->wait_limit_cycles : kWaitLimitCycles;
     prm.skip_load = test ? test->skip_load : -1;
     const size_t rows = (size_t)B * Hq;
-    const DecWorkspace w = carve_workspace(workspace, rows, d, splits);
-    prm.o_parts = w.o_parts;
-    prm.lse_parts = w.lse_parts;
-    prm.arrivals = w.arrivals;
-    prm.tag = next_arrival_tag();
+    if (splits > 1) {
+        const size_t o_bytes = (size_t)splits * rows * d * 4;
+        prm.o_parts = static_cast<float*>(workspace);
+        prm.lse_parts = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                                 (o_bytes + 255) / 256 * 256);
+    } else {
+        prm.o_parts = nullptr;
+        prm.lse_parts = nullptr;
+    }
     prm.table = nullptr;
     prm.seq_lens = nullptr;
     prm.page_size = 0;
     prm.max_pages = 0;
     const attn_status_t st = launch_split_any<false>(d, mk, mv, prm, stream);
-    if (st != ATTN_OK || splits == 1 || prm.arrivals != nullptr) return st;
+    if (st != ATTN_OK || splits == 1) return st;
     return launch_merge(prm.o_parts, prm.lse_parts, splits, (long long)rows, d, o, lse, true, stream);
 }
 
@@ -964,13 +811,17 @@ attn_status_t launch_decode_paged(const void* q, const void* k_pages, const void
     prm.page_size = page_size;
     prm.max_pages = max_pages;
     const size_t rows = (size_t)B * Hq;
-    const DecWorkspace w = carve_workspace(workspace, rows, d, splits);
-    prm.o_parts = w.o_parts;
-    prm.lse_parts = w.lse_parts;
-    prm.arrivals = w.arrivals;
-    prm.tag = next_arrival_tag();
+    if (splits > 1) {
+        const size_t o_bytes = (size_t)splits * rows * d * 4;
+        prm.o_parts = static_cast<float*>(workspace);
+        prm.lse_parts = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                                 (o_bytes + 255) / 256 * 256);
+    } else {
+        prm.o_parts = nullptr;
+        prm.lse_parts = nullptr;
+    }
     const attn_status_t st = launch_split_any<true>(d, mk, mv, prm, stream);
-    if (st != ATTN_OK || splits == 1 || prm.arrivals != nullptr) return st;
+    if (st != ATTN_OK || splits == 1) return st;
     return launch_merge(prm.o_parts, prm.lse_parts, splits, (long long)rows, d, o, lse, true, stream);
 }
 

@@ -132,17 +132,10 @@ int attn_decode_num_splits(int B, int Hq, int Hkv, int Nk, int d);
  * attn_decode_num_splits).  Returns 0 on invalid sizes.
  *
  * Workspace layout after a call with S segments (S > 1), R = B*Hq rows,
- * row r = b*Hq + hq:
- *     o_parts   [S, R, d]  float32 at byte offset 0: segment outputs, each
- *                          already normalised within its segment ([L11] 6.2
- *                          step 2);
- *     lse_parts [S, R]     float32 at byte offset A = round_up(S*R*d*4, 256);
- *     arrivals  [R]        uint64 at round_up(A + S*R*4, 256), only for
- *                          S <= 64: the split kernel's per-(sequence, head
- *                          group) arrival words (a per-call tag and a count
- *                          that every call leaves at 0).  They need no
- *                          initial value: a word without the call's tag
- *                          counts as 0.
+ * row r = b*Hq + hq, all float32:
+ *     o_parts   [S, R, d]  at byte offset 0: segment outputs, each already
+ *                          normalised within its segment ([L11] 6.2 step 2);
+ *     lse_parts [S, R]     at byte offset round_up(S*R*d*4, 256).
  * An empty segment holds o = 0, lse = -inf.  With S == 1 the workspace is
  * not touched and may be NULL.
  */
@@ -168,12 +161,8 @@ size_t attn_decode_workspace_bytes(int B, int Hq, int Hkv, int Nk, int d,
  *
  * Step 1-2: the split kernel, one CTA per (segment, group of up to 8 query
  * heads of one KV head, sequence), streams its K/V segment once and writes
- * (o_s, lse_s).  Step 3, for S <= 64: each CTA then counts itself on its
- * group's arrival word, and the group's last CTA merges the S partials
- * into O and LSE before it exits (no CTA waits for another); for S > 64:
- * the attn_merge_lse kernel on the same stream.  With S == 1 the split
- * kernel writes O and LSE directly and nothing is merged.  Calls that share
- * a workspace must not overlap on the GPU.
+ * (o_s, lse_s).  Step 3: attn_merge_lse on the same stream.  With S == 1 the
+ * split kernel writes O and LSE directly and no merge runs.
  */
 attn_status_t attn_decode_splitkv(const void* q, const void* k_cache,
                                   const void* v_cache, void* o, float* lse,
@@ -209,9 +198,9 @@ attn_status_t attn_decode_splitkv(const void* q, const void* k_cache,
  *     launch nothing; use attn_decode_splitkv with a larger workspace instead.
  *   - All calls share the one scratch area, which keeps the last call's
  *     partials (nothing in it needs to start at zero: every partial is written
- *     before it is read, and arrival words carry a per-call tag).  Calls
- *     whose kernels overlap on the GPU (different streams, or concurrent host
- *     threads) race on it; calls ordered on one stream do not.
+ *     before it is read).  Calls whose kernels overlap on the GPU (different
+ *     streams, or concurrent host threads) race on it; calls ordered on one
+ *     stream do not.
  * Other arguments, results and errors: as attn_decode_splitkv.
  */
 #define ATTN_DECODE_STATIC_SCRATCH_BYTES (8u << 20)

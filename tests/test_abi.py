@@ -98,21 +98,13 @@ def test_decode_rejects_bad_arguments(L):
     assert dec(L, B=0) == OK
 
 
-def decode_ws_bytes(B, Hq, d, S):
-    """o_parts [S, R, d] fp32 rounded up to 256 bytes, then lse_parts [S, R]
-    fp32; up to 64 segments also R uint64 arrival words after a further
-    rounding to 256 bytes."""
-    R = B * Hq
-    lse_off = (S * R * d * 4 + 255) // 256 * 256
-    if S > 64:
-        return lse_off + S * R * 4
-    return (lse_off + S * R * 4 + 255) // 256 * 256 + R * 8
-
-
 def test_decode_workspace_layout():
-    for B, Hq, d, S in ((1, 32, 128, 19), (16, 32, 128, 3), (3, 5, 64, 7), (1, 3, 64, 64),
-                        (2, 8, 128, 65), (1, 32, 128, 1000)):
-        assert pkg.attn_decode_workspace_bytes(B, Hq, 1, 1000, d, S) == decode_ws_bytes(B, Hq, d, S)
+    # o_parts [S, R, d] fp32 rounded up to 256 bytes, then lse_parts [S, R]
+    for B, Hq, d, S in ((1, 32, 128, 19), (16, 32, 128, 3), (3, 5, 64, 7)):
+        R = B * Hq
+        o_bytes = S * R * d * 4
+        want = (o_bytes + 255) // 256 * 256 + S * R * 4
+        assert pkg.attn_decode_workspace_bytes(B, Hq, 1, 1000, d, S) == want
     assert pkg.attn_decode_workspace_bytes(1, 8, 2, 100, 128, 1) == 0  # one segment: none
     assert pkg.attn_decode_workspace_bytes(1, 8, 3, 100, 128, 2) == 0  # invalid sizes
 
@@ -164,7 +156,8 @@ def test_paged_decode_rejects_bad_arguments(L):
 
 def test_paged_decode_declares_its_auto_split_rule():
     # pages a segment touches must fit the 4096-entry staging area; the rule is host arithmetic
-    assert pkg.attn_decode_workspace_bytes(2, 8, 2, 200, 128, 3) == decode_ws_bytes(2, 8, 128, 3)
+    assert pkg.attn_decode_workspace_bytes(2, 8, 2, 200, 128, 3) == \
+        (3 * 16 * 128 * 4 + 255) // 256 * 256 + 3 * 16 * 4
 
 
 def bwd(L, B=1, Hq=2, Hkv=1, Nq=8, Nk=8, d=64, causal=0, scale=0.125, ws=FAKE, wbytes=1 << 20,

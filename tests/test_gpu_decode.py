@@ -41,27 +41,7 @@ def decode_case(attn, oracle_mod, B, Hq, Hkv, Nk, d, splits, seed, check_parts=T
         op_ref, lp_ref = oracle_mod.decode_split(q, k, v, scale, S)
         # partial outputs are fp32 but built from bf16 P: same bound as O
         compare(o_parts, lse_parts, op_ref, lp_ref, torch.bfloat16, "decode partials")
-        if S <= 64:
-            check_arrival_words(flat, B, Hq, Hkv, d, S)
     return res, S
-
-
-def check_arrival_words(flat, B, Hq, Hkv, d, S):
-    """Up to 64 segments the split kernel merges in place: after the call
-    every used (sequence, head group) word holds the call's tag with a count
-    of 0, and the words past them keep the workspace's fill (0x5A bytes).
-    A group is up to 8 query heads of one KV head (8, 4, 2 or 1 of them,
-    the largest that divides Hq / Hkv)."""
-    R = B * Hq
-    off = ((S * R * d * 4 + 255) // 256 * 256 + S * R * 4 + 255) // 256 * 256
-    words = flat[off:off + R * 8].view(torch.int64).cpu().numpy().view(np.uint64)
-    G = Hq // Hkv
-    gc = next(c for c in (8, 4, 2, 1) if G % c == 0)
-    used = B * Hq // gc
-    assert np.all(words[:used] & np.uint64(0xFFFFFFFF) == 0), "arrival counts not back at 0"
-    tags = words[:used] >> np.uint64(32)
-    assert np.all(tags == tags[0]) and tags[0] != 0, "one non-zero tag per call"
-    assert np.all(words[used:] == np.uint64(0x5A5A5A5A5A5A5A5A)), "arrival words past the groups touched"
 
 
 def test_flash_decoding_long_context(attn, oracle_mod):

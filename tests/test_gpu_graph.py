@@ -81,27 +81,6 @@ def test_decode_graph(attn):
     torch.cuda.synchronize()
     assert torch.equal(o, eo) and torch.equal(lse, el)
     assert torch.equal(o_s, eo) and torch.equal(lse_s, el)
-    # Replays again: after an eager call on the same workspace (whose arrival
-    # words then carry another call's tag) and right after a replay (its own
-    # tag, count back at 0).  Both must merge every group exactly once.
-    q3, k3, v3 = make_qkv(B, Hq, Hkv, 1, Nk, d, 35)
-    q.copy_(q3)
-    k.copy_(k3)
-    v.copy_(v3)
-    eo3 = torch.empty_like(q)
-    el3 = torch.empty((B, Hq), device=DEV)
-    attn.attn_decode_splitkv(q, k, v, num_splits=S, workspace=ws, o=eo3, lse=el3)
-    for _ in range(2):
-        o.zero_()
-        lse.zero_()
-        o_s.zero_()
-        lse_s.zero_()
-        g.replay()
-        gs.replay()
-        torch.cuda.synchronize()
-        assert attn.attn_check_device_status() == 0
-        assert torch.equal(o, eo3) and torch.equal(lse, el3)
-        assert torch.equal(o_s, eo3) and torch.equal(lse_s, el3)
 
 
 def test_paged_graph_with_new_table(attn):
