@@ -652,6 +652,12 @@ def run_extra(args):
         call = lambda: attn.attn_bwd(q, k, v, o, lse, dout, causal, scale, dq=dq, dk=dk, dv=dv,
                                      workspace=ws)
         flops = 2.5 * prefill_flops(PREFILL[args.prefill])  # five products of 2 Nq Nk d per head
+    elif args.only == "fp8pv":
+        q8, qs = attn.attn_quantize_fp8(q)
+        k8, ks = attn.attn_quantize_fp8(k)
+        vt8, vs = attn.attn_quantize_fp8_v(v)
+        call = lambda: attn.attn_fwd_fp8_pv(q8, k8, vt8, qs, ks, vs, causal, scale, o=o, lse=lse)
+        flops = prefill_flops(PREFILL[args.prefill])
     else:
         q8, qs = attn.attn_quantize_fp8(q)
         k8, ks = attn.attn_quantize_fp8(k)
@@ -699,10 +705,11 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--page-size", type=int, default=16, help="--only paged: keys per page")
     ap.add_argument("--only", choices=["prefill", "decode", "forward", "splitkv", "backward", "fp8",
-                                        "paged"], default=None,
+                                        "fp8pv", "paged"], default=None,
                     help="time one part only (for profiling; no JSON contract): a half of the "
                          "step with the clock soak (prefill, decode); or, without the soak, "
-                         "attn_fwd / the backward pass / the FP8-Q,K forward on the prefill "
+                         "attn_fwd / the backward pass / the FP8-Q,K forward / the FP8-Q,K,V "
+                         "forward with e4m3 P on the prefill "
                          "workload, attn_decode_splitkv / the paged decode on the decode workload")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer measurement")
     ap.add_argument("--no-configs", action="store_true",
@@ -713,7 +720,7 @@ def main(argv=None):
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         return run_reference(args)
-    if args.only in ("forward", "splitkv", "backward", "fp8", "paged"):
+    if args.only in ("forward", "splitkv", "backward", "fp8", "fp8pv", "paged"):
         return run_extra(args)
     return run_ours(args)
 

@@ -22,7 +22,8 @@ __all__ = [
     "attn_check_device_status", "attn_read_tile_counter", "attn_version",
     "attn_decode_splitkv_static", "attn_decode_paged", "attn_decode_paged_num_splits",
     "attn_bwd", "attn_bwd_workspace_bytes", "attn_quantize_fp8", "attn_quantize_fp8_rotated",
-    "attn_fwd_fp8", "DECODE_STATIC_SCRATCH_BYTES", "EXPORTED_SYMBOLS", "TEST_SYMBOLS",
+    "attn_fwd_fp8", "attn_quantize_fp8_v", "attn_fwd_fp8_pv", "DECODE_STATIC_SCRATCH_BYTES",
+    "EXPORTED_SYMBOLS", "TEST_SYMBOLS",
     "AttnTestOptions", "attn_fwd_test", "attn_decode_test",
 ]
 
@@ -36,7 +37,7 @@ EXPORTED_SYMBOLS = (
     "attn_check_device_status", "attn_read_tile_counter", "attn_version",
     "attn_decode_splitkv_static", "attn_decode_paged", "attn_decode_paged_num_splits",
     "attn_bwd", "attn_bwd_workspace_bytes", "attn_quantize_fp8", "attn_quantize_fp8_rotated",
-    "attn_fwd_fp8",
+    "attn_fwd_fp8", "attn_quantize_fp8_v", "attn_fwd_fp8_pv",
 )
 
 # The test-only entry points include/attn_test.h declares.
@@ -129,6 +130,10 @@ def lib() -> ctypes.CDLL:
     L.attn_quantize_fp8_rotated.restype = I
     L.attn_fwd_fp8.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, P]
     L.attn_fwd_fp8.restype = I
+    L.attn_quantize_fp8_v.argtypes = [P, P, P, I, I, I, I, P]
+    L.attn_quantize_fp8_v.restype = I
+    L.attn_fwd_fp8_pv.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, P]
+    L.attn_fwd_fp8_pv.restype = I
     L.attn_decode_splitkv_static.restype = I
     OPT = ctypes.POINTER(AttnTestOptions)
     L.attn_fwd_test.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, F, OPT, P]
@@ -602,6 +607,66 @@ def attn_fwd_fp8(q8, k8, v, q_scales, k_scales, causal: bool, scale: float | Non
                                 _ptr(lse), B, Hq, Hkv, Nq, Nk, d, int(bool(causal)), float(scale),
                                 _stream(stream, dev))
     _check("attn_fwd_fp8", st)
+    return o, lse
+
+
+def fp8_v_ld(N: int) -> int:
+    """Row length (keys) of attn_quantize_fp8_v's transposed codes: N rounded
+    up to a multiple of 16."""
+    return (N + 15) // 16 * 16
+
+
+def attn_quantize_fp8_v(v, vt8=None, scales=None, stream=None):
+    """e4m3 quantisation of V for attn_fwd_fp8_pv: one float32 scale per
+    (batch, head) over the whole sequence, codes written transposed.  v: bf16
+    [B, N, H, d], d 64 or 128.  Returns (vt8 [B, H, d, fp8_v_ld(N)] uint8,
+    scales [B, H] float32); vt8[b, h, c, n] is the code of v[b, n, h, c]."""
+    import torch
+    B, N, H, d = v.shape
+    dev = v.device
+    _need_cuda_contig("v", v, dev)
+    if v.dtype != torch.bfloat16:
+        raise ValueError("v must be bfloat16")
+    shape = (B, H, d, fp8_v_ld(N))
+    vt8 = torch.empty(shape, dtype=torch.uint8, device=dev) if vt8 is None else vt8
+    scales = torch.empty((B, H), dtype=torch.float32, device=dev) if scales is None else scales
+    _need_buffer("vt8", vt8, shape, torch.uint8, dev)
+    _need_buffer("scales", scales, (B, H), torch.float32, dev)
+    with torch.cuda.device(dev):
+        st = lib().attn_quantize_fp8_v(_ptr(v), _ptr(vt8), _ptr(scales), B, N, H, d, _stream(stream, dev))
+    _check("attn_quantize_fp8_v", st)
+    return vt8, scales
+
+
+def attn_fwd_fp8_pv(q8, k8, vt8, q_scales, k_scales, v_scales, causal: bool, scale: float | None = None,
+                    o=None, lse=None, stream=None):
+    """Forward with e4m3 Q, K (attn_quantize_fp8) and V (attn_quantize_fp8_v),
+    and P rounded to e4m3 for the P V product.  Returns (o [B, Nq, Hq, d]
+    bf16, lse [B, Hq, Nq] float32)."""
+    import torch
+    B, Nq, Hq, d = q8.shape
+    Bk, Nk, Hkv, dk = k8.shape
+    if Bk != B or dk != d or tuple(vt8.shape) != (B, Hkv, d, fp8_v_ld(Nk)):
+        raise ValueError("shape mismatch")
+    if q8.dtype != torch.uint8 or k8.dtype != torch.uint8 or vt8.dtype != torch.uint8:
+        raise ValueError("q8, k8 and vt8 must be uint8 e4m3 codes")
+    dev = q8.device
+    for n, t in (("q8", q8), ("k8", k8), ("vt8", vt8)):
+        _need_cuda_contig(n, t, dev)
+    _need_buffer("q_scales", q_scales, (B, Hq, (Nq + 127) // 128), torch.float32, dev)
+    _need_buffer("k_scales", k_scales, (B, Hkv, (Nk + 127) // 128), torch.float32, dev)
+    _need_buffer("v_scales", v_scales, (B, Hkv), torch.float32, dev)
+    if scale is None:
+        scale = d ** -0.5
+    o = torch.empty((B, Nq, Hq, d), dtype=torch.bfloat16, device=dev) if o is None else o
+    lse = torch.empty((B, Hq, Nq), dtype=torch.float32, device=dev) if lse is None else lse
+    _need_buffer("o", o, (B, Nq, Hq, d), torch.bfloat16, dev)
+    _need_buffer("lse", lse, (B, Hq, Nq), torch.float32, dev)
+    with torch.cuda.device(dev):
+        st = lib().attn_fwd_fp8_pv(_ptr(q8), _ptr(k8), _ptr(vt8), _ptr(q_scales), _ptr(k_scales),
+                                   _ptr(v_scales), _ptr(o), _ptr(lse), B, Hq, Hkv, Nq, Nk, d,
+                                   int(bool(causal)), float(scale), _stream(stream, dev))
+    _check("attn_fwd_fp8_pv", st)
     return o, lse
 
 

@@ -71,6 +71,18 @@ bool encode_bshd_map(CUtensorMap* map, const void* base, int B, int N, int H, in
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool encode_vt_map(CUtensorMap* map, const void* base, int B, int H, int d, long long ld, int box_keys) {
+    EncodeTiledFn fn = encode_fn();
+    if (fn == nullptr) return false;
+    cuuint64_t dims[4] = {(cuuint64_t)ld, (cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)B};
+    cuuint64_t strides[3] = {(cuuint64_t)ld, (cuuint64_t)d * ld, (cuuint64_t)H * d * ld};
+    cuuint32_t box[4] = {(cuuint32_t)box_keys, (cuuint32_t)d, 1u, 1u};
+    cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int device_sm_count() {
     static int cache[kMaxDevices] = {0};
     int dev = 0;
@@ -359,6 +371,43 @@ attn_status_t attn_fwd_fp8(const void* q8, const void* k8, const void* v, const 
         return ATTN_ERR_INVALID;
     return attn_host::launch_fwd_fp8(q8, k8, v, q_scales, k_scales, o, lse, B, Hq, Hkv, Nq, Nk, d,
                                      causal, scale, st);
+}
+
+attn_status_t attn_quantize_fp8_v(const void* v, void* vt8, float* scales, int B, int N, int H, int d,
+                                  void* stream) {
+    if (B < 0 || N < 0 || H < 0 || d < 1) return ATTN_ERR_INVALID;
+    if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+    if (B > 65535 || H > 65535) return ATTN_ERR_UNSUPPORTED;
+    if (B == 0 || N == 0 || H == 0) return ATTN_OK;
+    if (v == nullptr || vt8 == nullptr || scales == nullptr) return ATTN_ERR_INVALID;
+    if (misaligned(v, 16) || misaligned(vt8, 16) || misaligned(scales, 4)) return ATTN_ERR_INVALID;
+    return attn_host::launch_quantize_fp8_v(v, vt8, scales, B, N, H, d, static_cast<cudaStream_t>(stream));
+}
+
+attn_status_t attn_fwd_fp8_pv(const void* q8, const void* k8, const void* vt8, const float* q_scales,
+                              const float* k_scales, const float* v_scales, void* o, float* lse, int B,
+                              int Hq, int Hkv, int Nq, int Nk, int d, int causal, float scale,
+                              void* stream) {
+    if (B < 0 || Hq < 0 || Hkv < 1 || Nq < 0 || Nk < 0 || d < 1) return ATTN_ERR_INVALID;
+    if (causal != 0 && causal != 1) return ATTN_ERR_INVALID;
+    if (bad_scale(scale)) return ATTN_ERR_INVALID;
+    if (Hq % Hkv != 0) return ATTN_ERR_INVALID;
+    if (d != 128) return ATTN_ERR_UNSUPPORTED;
+    if (B == 0 || Hq == 0 || Nq == 0) return ATTN_OK;
+    if (o == nullptr || lse == nullptr) return ATTN_ERR_INVALID;
+    if (misaligned(o, 16) || misaligned(lse, 4)) return ATTN_ERR_INVALID;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (Nk == 0)
+        return attn_host::launch_fill_empty(o, lse, (long long)B * Nq * Hq, d, (long long)B * Hq * Nq,
+                                            true, st);
+    if (q8 == nullptr || k8 == nullptr || vt8 == nullptr || q_scales == nullptr || k_scales == nullptr ||
+        v_scales == nullptr)
+        return ATTN_ERR_INVALID;
+    if (misaligned(q8, 16) || misaligned(k8, 16) || misaligned(vt8, 16) || misaligned(q_scales, 4) ||
+        misaligned(k_scales, 4) || misaligned(v_scales, 4))
+        return ATTN_ERR_INVALID;
+    return attn_host::launch_fwd_fp8_pv(q8, k8, vt8, q_scales, k_scales, v_scales, o, lse, B, Hq, Hkv, Nq,
+                                        Nk, d, causal, scale, st);
 }
 
 size_t attn_bwd_workspace_bytes(int B, int Hq, int Nq) {

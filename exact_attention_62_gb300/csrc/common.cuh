@@ -58,6 +58,15 @@ KernelSetup kernel_setup(int dyn_smem_bytes) {
 bool encode_bshd_map(CUtensorMap* map, const void* base, int B, int N, int H, int d,
                      int box_rows, int elem_bytes);
 
+// Row length (keys, padded) of the transposed e4m3 V, [B, H, d, ld]: a
+// multiple of 16 so that every row starts on a 16-byte boundary.
+inline long long fp8_v_ld(int N) { return ((long long)N + 15) / 16 * 16; }
+
+// Encodes a 4-D TMA tensor map over the transposed e4m3 V [B, H, d, ld]
+// (keys innermost), with a box of (box_keys keys, all d rows, 1 head, 1
+// batch) and 128-byte swizzle: a K-major operand tile of d rows.
+bool encode_vt_map(CUtensorMap* map, const void* base, int B, int H, int d, long long ld, int box_keys);
+
 // Number of SMs of the current device (cached per device); 0 on failure.
 int device_sm_count();
 
@@ -124,6 +133,12 @@ attn_status_t launch_quantize_fp8_rotated(const void* x, const float* signs, voi
 attn_status_t launch_fwd_fp8(const void* q8, const void* k8, const void* v, const float* q_scales,
                              const float* k_scales, void* o, float* lse, int B, int Hq, int Hkv,
                              int Nq, int Nk, int d, int causal, float scale, cudaStream_t stream);
+attn_status_t launch_quantize_fp8_v(const void* v, void* vt8, float* scales, int B, int N, int H, int d,
+                                    cudaStream_t stream);
+attn_status_t launch_fwd_fp8_pv(const void* q8, const void* k8, const void* vt8, const float* q_scales,
+                                const float* k_scales, const float* v_scales, void* o, float* lse, int B,
+                                int Hq, int Hkv, int Nq, int Nk, int d, int causal, float scale,
+                                cudaStream_t stream);
 
 // ---- backward pass (bwd_tc.cu)
 size_t bwd_workspace_bytes(int B, int Hq, int Nq);

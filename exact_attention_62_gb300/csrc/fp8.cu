@@ -181,6 +181,89 @@ __global__ void __launch_bounds__(kQThreads)
     }
 }
 
+// ---- V for the e4m3 P V product.  One scale per (batch, head) over the
+// whole sequence (a per-key-block scale would vary along the product's
+// contraction); the codes are written transposed, [B, H, d, ld] with the
+// keys innermost, so that V^T is a K-major operand tile like K.  Three
+// passes: the head's amax, the codes, the scales.
+
+// Pass 1: each CTA reduces the amax of 128 rows x D of one (batch, head)
+// and folds it into amax_bits[b, h] with an integer atomicMax on the float's
+// bits (both are non-negative, where the integer order is the float order).
+// amax_bits starts at 0.
+template <int D>
+__global__ void __launch_bounds__(kQThreads)
+    fp8_v_amax_kernel(const __nv_bfloat16* __restrict__ v, unsigned* __restrict__ amax_bits, int N, int H) {
+    constexpr int kC = D / 8;  // 16-byte chunks per row
+    const int r0 = blockIdx.x * kBlockRows, h = blockIdx.y, b = blockIdx.z;
+    const int rows = min(kBlockRows, N - r0);
+    float amax = 0.f;
+    for (int i = threadIdx.x; i < rows * kC; i += kQThreads) {
+        const int r = i / kC, c = i % kC;
+        const uint4 raw = __ldg(reinterpret_cast<const uint4*>(v + (((long long)b * N + r0 + r) * H + h) * D) + c);
+        const __nv_bfloat162* e = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            const float2 f = __bfloat1622float2(e[t]);
+            amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+        }
+    }
+    amax = block_max(amax);
+    if (threadIdx.x == 0) atomicMax(amax_bits + (long long)b * H + h, __float_as_uint(amax));
+}
+
+// Pass 2: each CTA quantises 128 keys x D of one (batch, head) with
+// inv = 448 / amax (1 for an all-zero head), the arithmetic of the block
+// quantiser, and writes them transposed through shared memory.  Loads:
+// consecutive threads take consecutive keys of one 8-column chunk, so the
+// byte stores into the [D][128] tile hit consecutive bytes; stores: eight
+// threads write one 128-byte row of codes.  Keys from N to ld get code 0.
+template <int D>
+__global__ void __launch_bounds__(kQThreads)
+    fp8_v_quant_kernel(const __nv_bfloat16* __restrict__ v, const unsigned* __restrict__ amax_bits,
+                       uint8_t* __restrict__ vt, int N, int H, long long ld) {
+    constexpr int kC = D / 8;
+    constexpr int kRow = kBlockRows + 16;  // tile row stride: 16-byte aligned, rows 4 banks apart
+    __shared__ __align__(16) uint8_t tile[D * kRow];
+    const int r0 = blockIdx.x * kBlockRows, h = blockIdx.y, b = blockIdx.z;
+    const float amax = __uint_as_float(amax_bits[(long long)b * H + h]);
+    const bool nz = amax > 0.f;
+    const float inv = nz ? kFp8Max / amax : 1.f;
+    for (int i = threadIdx.x; i < kBlockRows * kC; i += kQThreads) {
+        const int r = i % kBlockRows, c = i / kBlockRows;
+        uint4 raw = make_uint4(0u, 0u, 0u, 0u);
+        if (r0 + r < N)
+            raw = __ldg(reinterpret_cast<const uint4*>(v + (((long long)b * N + r0 + r) * H + h) * D) + c);
+        const __nv_bfloat162* e = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            const float2 f = __bfloat1622float2(e[t]);
+            const float2 y = make_float2(__fmul_rn(f.x, inv), __fmul_rn(f.y, inv));
+            const uint32_t q = __nv_cvt_float2_to_fp8x2(y, __NV_SATFINITE, __NV_E4M3);
+            tile[(8 * c + 2 * t) * kRow + r] = (uint8_t)(q & 0xFFu);
+            tile[(8 * c + 2 * t + 1) * kRow + r] = (uint8_t)(q >> 8);
+        }
+    }
+    __syncthreads();
+    const long long base = ((long long)b * H + h) * D * ld;
+    for (int i = threadIdx.x; i < D * (kBlockRows / 16); i += kQThreads) {
+        const int row = i / (kBlockRows / 16), ch = i % (kBlockRows / 16);
+        const long long key = (long long)r0 + 16 * ch;
+        if (key >= ld) continue;
+        *reinterpret_cast<uint4*>(vt + base + row * ld + key) =
+            *reinterpret_cast<const uint4*>(tile + row * kRow + 16 * ch);
+    }
+}
+
+// Pass 3: scales[i] = amax / 448 (1 for an all-zero head), over the bits
+// pass 1 left in the same words.
+__global__ void fp8_v_scale_kernel(float* __restrict__ scales, int n) {
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n) return;
+    const float amax = __uint_as_float(reinterpret_cast<const unsigned*>(scales)[i]);
+    scales[i] = amax > 0.f ? amax / kFp8Max : 1.f;
+}
+
 // Any even d: pairs of elements, two passes over the block.
 __global__ void __launch_bounds__(kQThreads)
     quantize_fp8_kernel(const __nv_bfloat16* __restrict__ x, uint8_t* __restrict__ codes,
@@ -229,6 +312,28 @@ attn_status_t launch_quantize_fp8(const void* x, void* codes, float* scales, int
         quantize_fp8_regs_kernel<64><<<grid, kQThreads, 0, stream>>>(xb, cb, scales, N, H);
     else
         quantize_fp8_kernel<<<grid, kQThreads, 0, stream>>>(xb, cb, scales, N, H, d);
+    return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+attn_status_t launch_quantize_fp8_v(const void* v, void* vt8, float* scales, int B, int N, int H, int d,
+                                    cudaStream_t stream) {
+    const int nb = (N + kBlockRows - 1) / kBlockRows;
+    if (H > 65535 || B > 65535 || (d != 64 && d != 128)) return ATTN_ERR_UNSUPPORTED;
+    const int n = B * H;
+    if (cudaMemsetAsync(scales, 0, (size_t)n * sizeof(float), stream) != cudaSuccess) return ATTN_ERR_CUDA;
+    dim3 grid(nb, H, B);
+    const __nv_bfloat16* vb = static_cast<const __nv_bfloat16*>(v);
+    unsigned* bits = reinterpret_cast<unsigned*>(scales);
+    uint8_t* out = static_cast<uint8_t*>(vt8);
+    const long long ld = fp8_v_ld(N);
+    if (d == 128) {
+        fp8_v_amax_kernel<128><<<grid, kQThreads, 0, stream>>>(vb, bits, N, H);
+        fp8_v_quant_kernel<128><<<grid, kQThreads, 0, stream>>>(vb, bits, out, N, H, ld);
+    } else {
+        fp8_v_amax_kernel<64><<<grid, kQThreads, 0, stream>>>(vb, bits, N, H);
+        fp8_v_quant_kernel<64><<<grid, kQThreads, 0, stream>>>(vb, bits, out, N, H, ld);
+    }
+    fp8_v_scale_kernel<<<(n + 255) / 256, 256, 0, stream>>>(scales, n);
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

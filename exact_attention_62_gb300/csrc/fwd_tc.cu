@@ -38,6 +38,8 @@
 //    straight to global memory.
 //  * Key tiles that are fully masked by causality are never loaded or
 //    computed (Lecture 11, section 5.3).
+#include <cuda_fp8.h>
+
 #include <cstdio>
 
 #include "common.cuh"
@@ -120,19 +122,25 @@ struct FwdParams {
     // FP8 inputs only: e4m3 Q and K with one scale per (batch, head, 128-row block)
     const float* q_scales;  // [B, Hq, nqb]
     const float* k_scales;  // [B, Hkv, nkb]
+    // FP8 V only: one scale per (batch, KV head)
+    const float* v_scales;  // [B, Hkv]
     int nqb, nkb;
 };
 
-template <int D, bool P_TMEM, bool F8 = false>
+template <int D, bool P_TMEM, bool F8 = false, bool F8V = false>
 struct Layout {
-    // Q and K are bf16 or (F8) e4m3; V is always bf16.  A swizzled panel is
-    // 128 rows of 128 bytes: 64 bf16 or 128 e4m3 elements per row.
+    // Q and K are bf16 or (F8) e4m3.  A swizzled panel is 128 rows of 128
+    // bytes: 64 bf16 or 128 e4m3 elements per row.  V is bf16, [keys][D]
+    // in D/64 panels, or (F8V) e4m3 and transposed, [D][128 keys]: one panel
+    // of D rows, K-major like K.
     static constexpr int kQKElem = F8 ? 1 : 2;
     static constexpr int kQKPanels = D * kQKElem / 128;
-    static constexpr int kPanels = D / 64;  // V panels
+    static constexpr int kPanels = D / 64;  // V panels (bf16 V: 64 columns each)
+    static_assert(F8V || kPanels * 64 == D, "bf16 V in whole 64-column panels");
     static constexpr int kQBytes = kBM * D * kQKElem;
     static constexpr int kKBytes = kBN * D * kQKElem;
-    static constexpr int kKVBytes = kBN * D * 2;  // one V tile
+    static constexpr int kKVBytes = kBN * D * (F8V ? 1 : 2);  // one V tile
+    static_assert(!F8V || (F8 && P_TMEM), "e4m3 V goes with e4m3 Q, K and P in tensor memory");
     static constexpr int kPBytes = P_TMEM ? 0 : kBM * kBN * 2;
     static constexpr int kKSt = F8 ? 3 : P_TMEM ? (D == 128 ? 2 : 3) : (D == 128 ? 1 : 2);
     static constexpr int kVSt = kKSt;
@@ -205,11 +213,11 @@ __device__ __forceinline__ Unit unit_at(int u, const FwdParams& p) {
     return x;
 }
 
-template <int D, bool P_TMEM, bool POLY, bool F8>
+template <int D, bool P_TMEM, bool POLY, bool F8, bool F8V>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
-    using L = Layout<D, P_TMEM, F8>;
+    using L = Layout<D, P_TMEM, F8, F8V>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -283,9 +291,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!ok) break;
                     if (!skip) {
                         mbar_arrive_expect_tx(bar(L::kBarVFull + vs), L::kKVBytes);
-                        for (int pp = 0; pp < L::kPanels; ++pp)
-                            tma_load_4d(sbase + L::kOffV + vs * L::kKVBytes + pp * kPanelBytes, &tmV,
-                                        bar(L::kBarVFull + vs), 64 * pp, x.g, j * kBN, x.b);
+                        if constexpr (F8V)  // V^T [b][g][D rows][keys]: 128 keys x D rows
+                            tma_load_4d(sbase + L::kOffV + vs * L::kKVBytes, &tmV, bar(L::kBarVFull + vs),
+                                        j * kBN, 0, x.g, x.b);
+                        else
+                            for (int pp = 0; pp < L::kPanels; ++pp)
+                                tma_load_4d(sbase + L::kOffV + vs * L::kKVBytes + pp * kPanelBytes, &tmV,
+                                            bar(L::kBarVFull + vs), 64 * pp, x.g, j * kBN, x.b);
                     }
                 }
             }
@@ -302,6 +314,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint32_t kIdS = idesc_bf16_f32(kBM, kBN, false);
             constexpr uint32_t kIdS8 = idesc_e4m3_f32(kBM, kBN);
             constexpr uint32_t kIdPV = idesc_bf16_f32(kBM, D, true);
+            constexpr uint32_t kIdPV8 = idesc_e4m3_f32(kBM, D);  // e4m3 P (TMEM) times e4m3 V^T
             constexpr uint32_t kHi = sdesc_sw128_hi(1024);  // every operand: 8-row groups 1024 B apart
             // V is [keys][D] with D contiguous: an N-major B operand.  Along N the
             // 64-column panels are kPanelBytes apart (LBO; one panel when D = 64);
@@ -374,9 +387,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ok = wait(bar(L::kBarOEmpty + t), (units_t[t] - 1) & 1);
                     if (!ok) return;
                     tc_fence_after();
+                    const uint32_t dO = tmem + L::tm_o(t);
+                    if constexpr (F8V) {
+                        // V^T is K-major like K: a k-step is 32 keys, 32 bytes of each of
+                        // its D rows; P packs four e4m3 keys per 32-bit column, 8 columns
+                        const uint32_t v_lo =
+                            sdesc_sw128_lo(sbase + L::kOffV + ((kv + j) % L::kVSt) * L::kKVBytes, 16);
+#pragma unroll
+                        for (int kk = 0; kk < kBN / 32; ++kk)
+                            mma_ts_elect_f8(dO, tmem + L::tm_s(t) + kk * 8, v_lo + ((kk * 32) >> 4), kHi,
+                                            kIdPV8, (j > 0 || kk > 0) ? 1u : 0u);
+                        if (j == x.n[t] - 1) {
+                            tc_commit_elect(bar(L::kBarOFull + t));
+                            ++units_t[t];
+                        }
+                        return;
+                    }
                     const uint32_t v_lo =
                         sdesc_sw128_lo(sbase + L::kOffV + ((kv + j) % L::kVSt) * L::kKVBytes, kVLbo);
-                    const uint32_t dO = tmem + L::tm_o(t);
 #pragma unroll
                     for (int kk = 0; kk < kBN / 16; ++kk) {
                         const uint32_t v_off = (kk * 16 * 128) >> 4;  // 16 keys of 128 B rows
@@ -452,6 +480,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 q_block_scale = p.q_scales[((long long)x.b * p.Hq + x.hq) * p.nqb + rs / kBM];
                 k_block_scale = p.k_scales + ((long long)x.b * p.Hkv + x.g) * p.nkb;
             }
+            // FP8 V: P is formed as 2^kPExp P and O = acc * v_scale / l
+            constexpr float kPExp = F8V ? 8.f : 0.f;
+            float v_scale = 1.f;
+            if constexpr (F8V) v_scale = p.v_scales[(long long)x.b * p.Hkv + x.g];
             float m = -INFINITY, l = 0.f;
             for (int j = 0; j < nt; ++j) {
                 float slj = sl;
@@ -504,8 +536,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
                 // P = exp2(s * scale log2 e - m): the scale-subtract and the row sum run on
                 // packed fp32 pairs, exp2 on the MUFU unit.
+                // FP8 V: P is formed as 256 P (2^8 folded into the subtrahend), so
+                // that its e4m3 codes keep three mantissa bits down to P = 2^-14; l
+                // then sums 256 P and the epilogue takes the 8 back out of the LSE.
                 const uint64_t sl2 = f2_pack(slj, slj);
-                const uint64_t nm2 = f2_pack(-m_use, -m_use);
+                const float nm = F8V ? kPExp - m_use : -m_use;
+                const uint64_t nm2 = f2_pack(nm, nm);
                 uint64_t sum2[2] = {0ull, 0ull};
                 uint32_t pk[kBN / 2];
 #pragma unroll
@@ -522,9 +558,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                         p1 = ex2(f2_hi(x));
                     }
                     sum2[c & 1] = f2_add(sum2[c & 1], f2_pack(p0, p1));
-                    pk[c] = pack_bf16(p0, p1);
-                    if constexpr (P_TMEM) {
-                        if (c == 31) tmem_st32(tS, pk);  // first half out while computing the rest
+                    if constexpr (F8V) {
+                        // e4m3, round to nearest even, saturating: four keys per word
+                        const uint32_t q2 = __nv_cvt_float2_to_fp8x2(make_float2(p0, p1), __NV_SATFINITE,
+                                                                     __NV_E4M3);
+                        if (c & 1)
+                            pk[c >> 1] |= q2 << 16;
+                        else
+                            pk[c >> 1] = q2;
+                        if (c == 31) tmem_st16(tS, pk);  // keys 0-63 out while computing the rest
+                    } else {
+                        pk[c] = pack_bf16(p0, p1);
+                        if constexpr (P_TMEM) {
+                            if (c == 31) tmem_st32(tS, pk);  // first half out while computing the rest
+                        }
                     }
                 }
                 const uint64_t sum = f2_add(sum2[0], sum2[1]);
@@ -534,7 +581,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // alpha = 0, and with l = 0 the row's O is 0 and its LSE -inf.)
                 const float tile_sum = m_new == -INFINITY ? 0.f : f2_lo(sum) + f2_hi(sum);
                 l = fmaf(l, alpha, tile_sum);
-                if constexpr (P_TMEM) {
+                if constexpr (F8V) {
+                    tmem_st16(tS + 16, pk + 16);
+                } else if constexpr (P_TMEM) {
                     tmem_st32(tS + 32, pk + 32);
                 } else {
                     const uint32_t pa = sbase + L::kOffP + t * L::kPBytes;
@@ -585,7 +634,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             mbar_arrive(bar(L::kBarOEmpty + t));  // the next unit's PV may overwrite O_t now
             if (row < p.Nq) {
-                const float inv = l > 0.f ? 1.f / l : 0.f;
+                const float inv = l > 0.f ? v_scale / l : 0.f;
 #pragma unroll
                 for (int c = 0; c < D / 8; ++c) {
                     uint4 w;
@@ -595,7 +644,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     w.w = pack_bf16(__uint_as_float(xo[8 * c + 6]) * inv, __uint_as_float(xo[8 * c + 7]) * inv);
                     reinterpret_cast<uint4*>(orow)[c] = w;
                 }
-                *lse_out = l > 0.f ? (m + lg2(l)) * kLn2 : -INFINITY;
+                *lse_out = l > 0.f ? (m + lg2(l) - kPExp) * kLn2 : -INFINITY;
             }
         }
     }
@@ -609,22 +658,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int D, bool P_TMEM, bool POLY, bool F8 = false>
+template <int D, bool P_TMEM, bool POLY, bool F8 = false, bool F8V = false>
 attn_status_t launch_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                           int Hq, int Hkv, int Nq, int Nk, float scale, int causal,
                           cudaStream_t stream, const attn_test_options_t* test, long long lse_ld,
-                          const float* q_scales = nullptr, const float* k_scales = nullptr) {
-    using L = Layout<D, P_TMEM, F8>;
+                          const float* q_scales = nullptr, const float* k_scales = nullptr,
+                          const float* v_scales = nullptr) {
+    using L = Layout<D, P_TMEM, F8, F8V>;
     CUtensorMap mq, mk, mv;
+    const bool v_ok = F8V ? attn_host::encode_vt_map(&mv, v, B, Hkv, D, attn_host::fp8_v_ld(Nk), kBN)
+                          : attn_host::encode_bshd_map(&mv, v, B, Nk, Hkv, D, kBN, 2);
     if (!attn_host::encode_bshd_map(&mq, q, B, Nq, Hq, D, kBM, L::kQKElem) ||
-        !attn_host::encode_bshd_map(&mk, k, B, Nk, Hkv, D, kBN, L::kQKElem) ||
-        !attn_host::encode_bshd_map(&mv, v, B, Nk, Hkv, D, kBN, 2))
+        !attn_host::encode_bshd_map(&mk, k, B, Nk, Hkv, D, kBN, L::kQKElem) || !v_ok)
         return ATTN_ERR_CUDA;
     // The register split inside the kernel assumes exactly kLaunchRegs per
     // thread at launch; refuse to launch a build that differs (the split's
     // register increase would otherwise wait forever).
     const attn_host::KernelSetup ks =
-        attn_host::kernel_setup<fwd_tc_kernel<D, P_TMEM, POLY, F8>>(L::kSmemBytes);
+        attn_host::kernel_setup<fwd_tc_kernel<D, P_TMEM, POLY, F8, F8V>>(L::kSmemBytes);
     if (ks.err != cudaSuccess) return ATTN_ERR_CUDA;
     if (ks.num_regs != kLaunchRegs) return ATTN_ERR_UNSUPPORTED;
     FwdParams prm;
@@ -651,12 +702,13 @@ attn_status_t launch_impl(const void* q, const void* k, const void* v, void* o, 
     prm.skip_load = test ? test->skip_load : -1;
     prm.q_scales = q_scales;
     prm.k_scales = k_scales;
+    prm.v_scales = v_scales;
     prm.nqb = (Nq + kBM - 1) / kBM;
     prm.nkb = (Nk + kBN - 1) / kBN;
     const int sms = attn_host::device_sm_count();
     if (sms <= 0) return ATTN_ERR_CUDA;
     const int grid = (int)(units < sms ? units : sms);
-    fwd_tc_kernel<D, P_TMEM, POLY, F8><<<grid, kThreads, L::kSmemBytes, stream>>>(mq, mk, mv, prm);
+    fwd_tc_kernel<D, P_TMEM, POLY, F8, F8V><<<grid, kThreads, L::kSmemBytes, stream>>>(mq, mk, mv, prm);
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
@@ -689,6 +741,15 @@ attn_status_t launch_fwd_fp8(const void* q8, const void* k8, const void* v, cons
     if (d != 128) return ATTN_ERR_UNSUPPORTED;
     return launch_impl<128, true, false, true>(q8, k8, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal,
                                                stream, nullptr, 0, q_scales, k_scales);
+}
+
+attn_status_t launch_fwd_fp8_pv(const void* q8, const void* k8, const void* vt8, const float* q_scales,
+                                const float* k_scales, const float* v_scales, void* o, float* lse, int B,
+                                int Hq, int Hkv, int Nq, int Nk, int d, int causal, float scale,
+                                cudaStream_t stream) {
+    if (d != 128) return ATTN_ERR_UNSUPPORTED;
+    return launch_impl<128, true, false, true, true>(q8, k8, vt8, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal,
+                                                     stream, nullptr, 0, q_scales, k_scales, v_scales);
 }
 
 cudaError_t fwd_tc_read_status(unsigned* out, bool clear) {

@@ -315,6 +315,53 @@ attn_status_t attn_fwd_fp8(const void* q8, const void* k8, const void* v, const 
                            int Nk, int d, int causal, float scale, void* stream);
 
 /*
+ * attn_quantize_fp8_v -- e4m3 quantisation of V for attn_fwd_fp8_pv ([L11]
+ * 4.5, FP8 item: FA3's FP8 path quantises both products' operands).  One
+ * block per (batch, head): the whole sequence shares one scale, because a
+ * scale that changed along the keys would change along the P V product's
+ * contraction.  The codes are written transposed, keys innermost, so that
+ * V^T is read as a K-major operand like K.
+ *   v      [B, N, H, d] bf16 input; d is 64 or 128.
+ *   vt8    [B, H, d, ld] uint8 output, ld = round_up(N, 16) (each row of
+ *          keys starts on a 16-byte boundary): vt8[b, h, c, n] is the code of
+ *          v[b, n, h, c]; the ld - N padding keys hold 0.
+ *   scales [B, H] float32 output.
+ * amax = max |v| over the head's N x d values; scale = amax / 448 and
+ * inv = 448 / amax in float32 (1 and 1 for an all-zero head); each code is
+ * e4m3(v * inv), rounded to nearest even and saturated: attn_quantize_fp8's
+ * arithmetic with blocks of N rows, reproducible bit for bit.  `scales` is
+ * also the working buffer of the amax pass (cleared with cudaMemsetAsync on
+ * `stream` first).  Errors: ATTN_ERR_INVALID for negative sizes, NULL or
+ * misaligned pointers (v, vt8: 16 bytes; scales: 4); ATTN_ERR_UNSUPPORTED for
+ * other d or B, H above 65535.
+ */
+attn_status_t attn_quantize_fp8_v(const void* v, void* vt8, float* scales, int B, int N, int H, int d,
+                                  void* stream);
+
+/*
+ * attn_fwd_fp8_pv -- attn_fwd_fp8 with P V in e4m3 as well: V quantised by
+ * attn_quantize_fp8_v, P formed per key tile as 256 P (the factor 2^8
+ * folded into the exponent, so P keeps e4m3's three mantissa bits down to
+ * P = 2^-14), rounded to e4m3 (nearest even) and multiplied with the V codes
+ * on the tensor cores (fp32 accumulation).  The row sum l is taken over the
+ * unrounded fp32 P, so LSE is as in attn_fwd_fp8; O = acc * v_scale / l.
+ *   q8, k8, q_scales, k_scales, o, lse: as attn_fwd_fp8;
+ *   vt8 [B, Hkv, d, round_up(Nk, 16)] uint8, v_scales [B, Hkv] float32:
+ *          attn_quantize_fp8_v's output for V [B, Nk, Hkv, d].
+ * d = 128 only.  Against the attention of the dequantised inputs (q8, k8 and
+ * vt8 times their scales) the error of row i, column c is bounded by the
+ * rounding of P: |dO_ic| <= 2^-4 sum_j w_ij |v_jc| + 2^-18 sum_j |v_jc| (w
+ * the softmax weights; 2^-4 is half an e4m3 step relative, 2^-18 the largest
+ * error of a P below e4m3's normal range) plus attn_fwd's bf16 error.
+ * Errors: as attn_fwd_fp8, and ATTN_ERR_INVALID for a NULL or misaligned
+ * vt8 (16 bytes) or v_scales (4 bytes).
+ */
+attn_status_t attn_fwd_fp8_pv(const void* q8, const void* k8, const void* vt8, const float* q_scales,
+                              const float* k_scales, const float* v_scales, void* o, float* lse, int B,
+                              int Hq, int Hkv, int Nq, int Nk, int d, int causal, float scale,
+                              void* stream);
+
+/*
  * attn_bwd -- backward pass of attn_fwd ([L11] 5.1): given dO, the gradients
  *     dV = P^T dO,  dP = dO V^T,  D_i = rowsum(dO_i * O_i),
  *     dS = P * (dP - D),  dQ = scale dS K,  dK = scale dS^T Q,

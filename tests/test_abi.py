@@ -211,6 +211,21 @@ def test_fp8_entry_points_reject_bad_arguments(L):
     assert f8(causal=3) == INVALID
     assert f8(Hq=3, Hkv=2) == INVALID
     assert f8(B=0) == OK
+    qv = lambda v=FAKE, vt=FAKE, sc=FAKE_LSE, B=1, d=128: L.attn_quantize_fp8_v(v, vt, sc, B, 8, 2, d, None)
+    assert qv(d=96) == UNSUPPORTED           # transposed tiles of 64 or 128 rows
+    assert qv(d=0) == INVALID
+    assert qv(v=None) == INVALID
+    assert qv(sc=None) == INVALID
+    assert qv(B=0) == OK
+    pv = lambda d=128, causal=0, Hq=2, Hkv=1, B=1, vt=FAKE, vs=FAKE_LSE, Nq=8: L.attn_fwd_fp8_pv(
+        FAKE, FAKE, vt, FAKE_LSE, FAKE_LSE, vs, FAKE, FAKE_LSE, B, Hq, Hkv, Nq, 8, d, causal, 0.1, None)
+    assert pv(d=64) == UNSUPPORTED
+    assert pv(causal=2) == INVALID
+    assert pv(Hq=3, Hkv=2) == INVALID
+    assert pv(vt=None) == INVALID
+    assert pv(vs=None) == INVALID
+    assert pv(B=0) == OK
+    assert pv(Nq=0) == OK
 
 
 def test_test_entry_points_reject_bad_arguments(L):

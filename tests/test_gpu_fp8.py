@@ -8,7 +8,10 @@
    derives (tests/parity.check_rotated_codes).
 2. attn_fwd_fp8 matches the oracle run on the dequantised Q and K within the
    bf16 tolerance of attn_fwd: the kernel's arithmetic on the codes is exact
-   up to that.
+   up to that.  attn_quantize_fp8_v (one block per head, transposed) is bit
+   exact as in 1, and attn_fwd_fp8_pv (e4m3 P and V) matches the oracle on
+   the dequantised Q, K and V within the bound that follows from rounding
+   256 P to e4m3 (_pv_bound_check).
 3. Against the exact attention of the unquantised inputs, each row obeys the
    bound that follows from how far quantisation moves its scaled scores:
    with delta_i = max_j |S'_ij - S_ij| (from the oracle),
@@ -23,7 +26,7 @@ import pytest
 import torch
 
 from exact_attention_62_gb300.inputs import make_qkv
-from parity import check_rotated_codes, compare
+from parity import _log, check_rotated_codes, compare
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -204,3 +207,125 @@ def test_fp8_forward_rotated(attn, oracle_mod, outlier):
         err_rot = np.abs(lg - el).mean()
         err_plain = np.abs(plse.cpu().numpy().astype(np.float64) - el).mean()
         assert err_rot < err_plain, (err_rot, err_plain)
+
+
+# ---------------------------------------------------------------- e4m3 V and P V
+def _v_codes_bnhd(vt8, N):
+    """attn_quantize_fp8_v's transposed codes [B, H, d, ld] back to [B, N, H, d]."""
+    return vt8[..., :N].permute(0, 3, 1, 2).contiguous()
+
+
+@pytest.mark.parametrize("B,N,H,d,seed", [(2, 300, 3, 128, 31), (1, 1000, 2, 64, 32), (1, 128, 1, 128, 33),
+                                         (3, 17, 2, 128, 34), (1, 4100, 1, 64, 35)])
+def test_v_quantisation_is_bit_exact(attn, oracle_mod, B, N, H, d, seed):
+    """attn_quantize_fp8_v is the block quantisation with one block per
+    (batch, head), the whole sequence (the oracle's quantize_fp8_blocks with
+    block = N), written transposed; the padding keys up to a multiple of 16
+    hold code 0 and an all-zero head gets scale 1."""
+    g = torch.Generator().manual_seed(seed)
+    v = (torch.randn((B, N, H, d), generator=g) * 2).to(torch.bfloat16)
+    v[0, :, 0, 3] *= 40                        # outlier column
+    if B > 1:
+        v[1, :, -1] = 0                        # an all-zero head
+    vt8, vsc = attn.attn_quantize_fp8_v(v.to(DEV))
+    torch.cuda.synchronize()
+    ld = (N + 15) // 16 * 16
+    assert tuple(vt8.shape) == (B, H, d, ld) and tuple(vsc.shape) == (B, H)
+    rc, rs = oracle_mod.quantize_fp8_blocks(v.float(), block=N)
+    assert np.array_equal(_v_codes_bnhd(vt8, N).cpu().numpy(), rc)
+    assert np.array_equal(vsc.cpu().numpy(), rs[:, :, 0])
+    assert torch.all(vt8[..., N:] == 0)
+    if B > 1:
+        assert vsc[1, -1].item() == 1.0 and torch.all(vt8[1, -1] == 0)
+
+
+def _pv_bound_check(o, lse, ro, rl, rabs, vabs_sum, what):
+    """The e4m3 P V bar against the oracle on the dequantised inputs: LSE
+    within attn_fwd's 1e-3 (l sums the unrounded P), and per element
+    |dO_ic| <= 2^-4 sum_j w_ij |v_jc| + 2^-18 sum_j |v_jc| + 2e-2: rounding
+    256 P to e4m3 (nearest even) moves each weight by at most half a step,
+    2^-4 of it, or by 2^-18 below the normal range (2^-14); the sums over
+    keys are bounded by all keys of the head; 2e-2 is attn_fwd's bf16 bar."""
+    og = o.float().cpu().numpy().astype(np.float64)
+    lg = lse.float().cpu().numpy().astype(np.float64)
+    fin = np.isfinite(rl)
+    assert np.array_equal(np.isfinite(lg), fin), what
+    assert np.all(lg[~fin] == rl[~fin]), what
+    d_l = np.abs(lg[fin] - rl[fin]).max() if fin.any() else 0.0
+    assert d_l <= 1e-3, what
+    bound = 2.0 ** -4 * (1 + 1e-3) * rabs + 2.0 ** -18 * vabs_sum + 2e-2
+    err = np.abs(og - ro)
+    assert np.all(np.isfinite(og)), what
+    _log(what, err.max(), d_l, int(np.prod(og.shape[:-1])))
+    assert np.all(err <= bound), "%s: worst excess %.3g" % (what, (err - bound).max())
+    return err.max()
+
+
+PV_CASES = [
+    # B, Hq, Hkv, Nq, Nk, causal, q_scale
+    (1, 2, 2, 300, 300, True, 1.0),
+    (2, 4, 1, 520, 520, False, 1.0),
+    (1, 2, 2, 1000, 300, True, 1.0),      # causal rows with no allowed key
+    (1, 2, 2, 700, 700, True, 8.0),       # near one-hot rows
+    (1, 8, 2, 257, 1000, False, 1.0),     # GQA, Nk not a multiple of 16
+]
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Nq,Nk,causal,qs", PV_CASES)
+def test_fp8_pv_forward(attn, oracle_mod, B, Hq, Hkv, Nq, Nk, causal, qs):
+    d = 128
+    scale = 1.0 / math.sqrt(d)
+    q, k, v = make_qkv(B, Hq, Hkv, Nq, Nk, d, 41, q_scale=qs)
+    v[:, :, 0, 7] *= 20                    # an outlier feature in V
+    q8, qsc = attn.attn_quantize_fp8(q.to(DEV))
+    k8, ksc = attn.attn_quantize_fp8(k.to(DEV))
+    vt8, vsc = attn.attn_quantize_fp8_v(v.to(DEV))
+    o, lse = attn.attn_fwd_fp8_pv(q8, k8, vt8, qsc, ksc, vsc, causal, scale)
+    torch.cuda.synchronize()
+    assert attn.attn_check_device_status() == 0
+    qd = oracle_mod.dequantize_fp8_blocks(q8.cpu().numpy(), qsc.cpu().numpy()).astype(np.float32)
+    kd = oracle_mod.dequantize_fp8_blocks(k8.cpu().numpy(), ksc.cpu().numpy()).astype(np.float32)
+    vd = oracle_mod.dequantize_fp8_blocks(_v_codes_bnhd(vt8, Nk).cpu().numpy(),
+                                          vsc.cpu().numpy()[:, :, None], block=Nk).astype(np.float32)
+    ro, rl = oracle_mod.attn_fwd(qd, kd, vd, causal, scale)
+    rabs, _ = oracle_mod.attn_fwd(qd, kd, np.abs(vd), causal, scale)
+    G = Hq // Hkv
+    vsum = np.abs(vd.astype(np.float64)).sum(axis=1)                        # [B, Hkv, d]
+    vabs_sum = np.repeat(vsum, G, axis=1)[:, None, :, :]                   # [B, 1, Hq, d]
+    err = _pv_bound_check(o, lse, ro, rl, rabs, vabs_sum, "fp8 P V vs dequantised oracle")
+    # and the rounding of P is visible: the result is not the bf16-P result
+    ob, _ = attn.attn_fwd_fp8(q8, k8, torch.from_numpy(vd).to(torch.bfloat16).to(DEV), qsc, ksc, causal, scale)
+    torch.cuda.synchronize()
+    assert not torch.equal(ob, o) and err > 0
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,N", [(4, 16, 16, 4096), (1, 32, 8, 16384)],
+                         ids=["training_prefill", "long_sequence"])
+def test_fp8_pv_forward_full_size_sampled(attn, oracle_mod, B, Hq, Hkv, N):
+    """The e4m3 P V forward at the two full FP8 sizes (d = 128, causal), on
+    sampled rows against the oracle run on the dequantised Q, K and V,
+    within the P-rounding bound above."""
+    from exact_attention_62_gb300.inputs import sample_rows
+    d = 128
+    scale = 1.0 / math.sqrt(d)
+    q, k, v = make_qkv(B, Hq, Hkv, N, N, d, 42)
+    q8, qsc = attn.attn_quantize_fp8(q.to(DEV))
+    k8, ksc = attn.attn_quantize_fp8(k.to(DEV))
+    vt8, vsc = attn.attn_quantize_fp8_v(v.to(DEV))
+    o, lse = attn.attn_fwd_fp8_pv(q8, k8, vt8, qsc, ksc, vsc, True, scale)
+    torch.cuda.synchronize()
+    assert attn.attn_check_device_status() == 0
+    qd = oracle_mod.dequantize_fp8_blocks(q8.cpu().numpy(), qsc.cpu().numpy()).astype(np.float32)
+    kd = oracle_mod.dequantize_fp8_blocks(k8.cpu().numpy(), ksc.cpu().numpy()).astype(np.float32)
+    vd = oracle_mod.dequantize_fp8_blocks(_v_codes_bnhd(vt8, N).cpu().numpy(),
+                                          vsc.cpu().numpy()[:, :, None], block=N).astype(np.float32)
+    rows = sample_rows(B, Hq, N, 192, 43)
+    rows += [(0, 0, 127), (B - 1, Hq // 2, 128), (B - 1, Hq - 1, N - 1), (0, 3, 0)]
+    ro, rl = oracle_mod.attn_rows(qd, kd, vd, True, scale, rows)
+    rabs, _ = oracle_mod.attn_rows(qd, kd, np.abs(vd), True, scale, rows)
+    G = Hq // Hkv
+    vsum = np.abs(vd.astype(np.float64)).sum(axis=1)                        # [B, Hkv, d]
+    vabs_sum = np.stack([vsum[b, h // G] for b, h, _ in rows])
+    o_sel = torch.stack([o[b, i, h] for b, h, i in rows])
+    l_sel = torch.stack([lse[b, h, i] for b, h, i in rows])
+    _pv_bound_check(o_sel, l_sel, ro, rl, rabs, vabs_sum, "fp8 P V full size vs dequantised oracle")
