@@ -83,10 +83,10 @@ NOMINAL_HBM_GBS = 8000.0  # the ~8 TB/s HBM3e figure the decode target is quoted
 # dram__bytes_write.sum), keyed by the hash of the kernel source it was
 # measured on: any later change to the source turns the figure into null.
 NCU_TRAFFIC = {
-    "long_sequence": {"bytes_per_launch": 344.92e6 + 101.91e6, "src": "fwd_tc.cu",
-                      "src_hash": "32ad561434cea808"},
-    "decode_b16_8k": {"bytes_per_launch": 537.03e6 + 3.98e6, "src": "decode.cu",
-                      "src_hash": "1c96db32004178d3"},
+    "long_sequence": {"bytes_per_launch": 348.34e6 + 101.28e6, "src": "fwd_tc.cu",
+                      "src_hash": "2c96717052fcb170"},
+    "decode_b16_8k": {"bytes_per_launch": 537.03e6 + 4.01e6, "src": "decode.cu",
+                      "src_hash": "e3a41edb273c7aa5"},
 }
 
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
