@@ -126,3 +126,25 @@ def check_rotated_codes(codes_g, scales_g, x, signs, oracle_mod, block=128, max_
                         ("code differs away from a rounding boundary", b, r0 + i, h, j, z, vg, vo)
     assert n_diff <= max_frac * codes_g.size, n_diff
     return n_diff
+
+
+def check_fp8_pv(o, lse, ro, rl, rabs, vabs_sum, what):
+    """The e4m3 P V bar against the oracle on the dequantised inputs: LSE
+    within attn_fwd's 1e-3 (l sums the unrounded P), and per element
+    |dO_ic| <= 2^-4 sum_j w_ij |v_jc| + 2^-18 sum_j |v_jc| + 2e-2: rounding
+    256 P to e4m3 (nearest even) moves each weight by at most half a step,
+    2^-4 of it, or by 2^-18 below the normal range (2^-14); the sums over
+    keys are bounded by all keys of the head; 2e-2 is attn_fwd's bf16 bar."""
+    og = o.float().cpu().numpy().astype(np.float64)
+    lg = lse.float().cpu().numpy().astype(np.float64)
+    fin = np.isfinite(rl)
+    assert np.array_equal(np.isfinite(lg), fin), what
+    assert np.all(lg[~fin] == rl[~fin]), what
+    d_l = np.abs(lg[fin] - rl[fin]).max() if fin.any() else 0.0
+    assert d_l <= 1e-3, what
+    bound = 2.0 ** -4 * (1 + 1e-3) * rabs + 2.0 ** -18 * vabs_sum + 2e-2
+    err = np.abs(og - ro)
+    assert np.all(np.isfinite(og)), what
+    _log(what, err.max(), d_l, int(np.prod(og.shape[:-1])))
+    assert np.all(err <= bound), "%s: worst excess %.3g" % (what, (err - bound).max())
+    return err.max()

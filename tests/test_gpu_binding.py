@@ -128,3 +128,26 @@ def test_fp8_buffers(attn):
     o, lse = attn.attn_fwd_fp8(q8, k8, v, qs, ks, True)
     torch.cuda.synchronize()
     assert torch.isfinite(lse).all() and attn.attn_check_device_status() == 0
+
+
+def test_fp8_pv_buffers(attn):
+    B, N, Hq, Hkv, d = 1, 300, 4, 2, 128
+    q, k, v = _bf((B, N, Hq, d), 17), _bf((B, N, Hkv, d), 18), _bf((B, N, Hkv, d), 19)
+    ld = (N + 15) // 16 * 16
+    _rejects(attn.attn_quantize_fp8_v, v, vt8=torch.empty((B, Hkv, d, N), device=DEV, dtype=torch.uint8))
+    _rejects(attn.attn_quantize_fp8_v, v, scales=torch.empty((B, Hkv, 1), device=DEV))
+    _rejects(attn.attn_quantize_fp8_v, v.float())
+    q8, qs = attn.attn_quantize_fp8(q)
+    k8, ks = attn.attn_quantize_fp8(k)
+    vt8, vs = attn.attn_quantize_fp8_v(v)
+    assert tuple(vt8.shape) == (B, Hkv, d, ld)
+    _rejects(attn.attn_fwd_fp8_pv, q8, k8, vt8[..., :N].contiguous(), qs, ks, vs, True)   # unpadded rows
+    _rejects(attn.attn_fwd_fp8_pv, q8, k8, vt8, qs, ks, vs[:, :1].contiguous(), True)
+    _rejects(attn.attn_fwd_fp8_pv, q8, k8, vt8, qs, ks, vs.double(), True)
+    _rejects(attn.attn_fwd_fp8_pv, q8, k8, vt8.view(torch.int8), qs, ks, vs, True)
+    _rejects(attn.attn_fwd_fp8_pv, q8, k8, vt8, qs, ks, vs, True, o=torch.empty((B, N, Hq, d), device=DEV))
+    torch.cuda.synchronize()
+    assert attn.attn_check_device_status() == 0
+    o, lse = attn.attn_fwd_fp8_pv(q8, k8, vt8, qs, ks, vs, True)
+    torch.cuda.synchronize()
+    assert torch.isfinite(lse).all() and attn.attn_check_device_status() == 0

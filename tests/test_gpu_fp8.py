@@ -11,7 +11,7 @@
    up to that.  attn_quantize_fp8_v (one block per head, transposed) is bit
    exact as in 1, and attn_fwd_fp8_pv (e4m3 P and V) matches the oracle on
    the dequantised Q, K and V within the bound that follows from rounding
-   256 P to e4m3 (_pv_bound_check).
+   256 P to e4m3 (parity.check_fp8_pv).
 3. Against the exact attention of the unquantised inputs, each row obeys the
    bound that follows from how far quantisation moves its scaled scores:
    with delta_i = max_j |S'_ij - S_ij| (from the oracle),
@@ -26,7 +26,7 @@ import pytest
 import torch
 
 from exact_attention_62_gb300.inputs import make_qkv
-from parity import _log, check_rotated_codes, compare
+from parity import check_fp8_pv, check_rotated_codes, compare
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -239,26 +239,19 @@ def test_v_quantisation_is_bit_exact(attn, oracle_mod, B, N, H, d, seed):
         assert vsc[1, -1].item() == 1.0 and torch.all(vt8[1, -1] == 0)
 
 
-def _pv_bound_check(o, lse, ro, rl, rabs, vabs_sum, what):
-    """The e4m3 P V bar against the oracle on the dequantised inputs: LSE
-    within attn_fwd's 1e-3 (l sums the unrounded P), and per element
-    |dO_ic| <= 2^-4 sum_j w_ij |v_jc| + 2^-18 sum_j |v_jc| + 2e-2: rounding
-    256 P to e4m3 (nearest even) moves each weight by at most half a step,
-    2^-4 of it, or by 2^-18 below the normal range (2^-14); the sums over
-    keys are bounded by all keys of the head; 2e-2 is attn_fwd's bf16 bar."""
-    og = o.float().cpu().numpy().astype(np.float64)
-    lg = lse.float().cpu().numpy().astype(np.float64)
-    fin = np.isfinite(rl)
-    assert np.array_equal(np.isfinite(lg), fin), what
-    assert np.all(lg[~fin] == rl[~fin]), what
-    d_l = np.abs(lg[fin] - rl[fin]).max() if fin.any() else 0.0
-    assert d_l <= 1e-3, what
-    bound = 2.0 ** -4 * (1 + 1e-3) * rabs + 2.0 ** -18 * vabs_sum + 2e-2
-    err = np.abs(og - ro)
-    assert np.all(np.isfinite(og)), what
-    _log(what, err.max(), d_l, int(np.prod(og.shape[:-1])))
-    assert np.all(err <= bound), "%s: worst excess %.3g" % (what, (err - bound).max())
-    return err.max()
+def fp8_pv_reference(oracle_mod, q8, qsc, k8, ksc, vt8, vsc, Nk, causal, scale, Hq, Hkv):
+    """The oracle on the dequantised Q, K and V of an attn_fwd_fp8_pv call,
+    with the terms of its error bound: (o, lse, sum_j w_ij |v_jc| from the
+    oracle on |V|, sum_j |v_jc| over the KV head's keys, as [B, 1, Hq, d])."""
+    qd = oracle_mod.dequantize_fp8_blocks(q8.cpu().numpy(), qsc.cpu().numpy()).astype(np.float32)
+    kd = oracle_mod.dequantize_fp8_blocks(k8.cpu().numpy(), ksc.cpu().numpy()).astype(np.float32)
+    vd = oracle_mod.dequantize_fp8_blocks(_v_codes_bnhd(vt8, Nk).cpu().numpy(),
+                                          vsc.cpu().numpy()[:, :, None], block=Nk).astype(np.float32)
+    ro, rl = oracle_mod.attn_fwd(qd, kd, vd, causal, scale)
+    rabs, _ = oracle_mod.attn_fwd(qd, kd, np.abs(vd), causal, scale)
+    vsum = np.abs(vd.astype(np.float64)).sum(axis=1)                        # [B, Hkv, d]
+    vabs_sum = np.repeat(vsum, Hq // Hkv, axis=1)[:, None, :, :]           # [B, 1, Hq, d]
+    return ro, rl, rabs, vabs_sum, vd
 
 
 PV_CASES = [
@@ -283,16 +276,9 @@ def test_fp8_pv_forward(attn, oracle_mod, B, Hq, Hkv, Nq, Nk, causal, qs):
     o, lse = attn.attn_fwd_fp8_pv(q8, k8, vt8, qsc, ksc, vsc, causal, scale)
     torch.cuda.synchronize()
     assert attn.attn_check_device_status() == 0
-    qd = oracle_mod.dequantize_fp8_blocks(q8.cpu().numpy(), qsc.cpu().numpy()).astype(np.float32)
-    kd = oracle_mod.dequantize_fp8_blocks(k8.cpu().numpy(), ksc.cpu().numpy()).astype(np.float32)
-    vd = oracle_mod.dequantize_fp8_blocks(_v_codes_bnhd(vt8, Nk).cpu().numpy(),
-                                          vsc.cpu().numpy()[:, :, None], block=Nk).astype(np.float32)
-    ro, rl = oracle_mod.attn_fwd(qd, kd, vd, causal, scale)
-    rabs, _ = oracle_mod.attn_fwd(qd, kd, np.abs(vd), causal, scale)
-    G = Hq // Hkv
-    vsum = np.abs(vd.astype(np.float64)).sum(axis=1)                        # [B, Hkv, d]
-    vabs_sum = np.repeat(vsum, G, axis=1)[:, None, :, :]                   # [B, 1, Hq, d]
-    err = _pv_bound_check(o, lse, ro, rl, rabs, vabs_sum, "fp8 P V vs dequantised oracle")
+    ro, rl, rabs, vabs_sum, vd = fp8_pv_reference(oracle_mod, q8, qsc, k8, ksc, vt8, vsc, Nk, causal, scale,
+                                                  Hq, Hkv)
+    err = check_fp8_pv(o, lse, ro, rl, rabs, vabs_sum, "fp8 P V vs dequantised oracle")
     # and the rounding of P is visible: the result is not the bf16-P result
     ob, _ = attn.attn_fwd_fp8(q8, k8, torch.from_numpy(vd).to(torch.bfloat16).to(DEV), qsc, ksc, causal, scale)
     torch.cuda.synchronize()
@@ -328,4 +314,4 @@ def test_fp8_pv_forward_full_size_sampled(attn, oracle_mod, B, Hq, Hkv, N):
     vabs_sum = np.stack([vsum[b, h // G] for b, h, _ in rows])
     o_sel = torch.stack([o[b, i, h] for b, h, i in rows])
     l_sel = torch.stack([lse[b, h, i] for b, h, i in rows])
-    _pv_bound_check(o_sel, l_sel, ro, rl, rabs, vabs_sum, "fp8 P V full size vs dequantised oracle")
+    check_fp8_pv(o_sel, l_sel, ro, rl, rabs, vabs_sum, "fp8 P V full size vs dequantised oracle")

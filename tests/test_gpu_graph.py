@@ -167,3 +167,40 @@ def test_fp8_graph(attn):
     torch.cuda.synchronize()
     assert torch.equal(q8, eq8) and torch.equal(qs, eqs) and torch.equal(k8, ek8) and torch.equal(ks, eks)
     assert torch.equal(o, eo) and torch.equal(lse, el)
+
+
+def test_fp8_pv_graph(attn):
+    """Quantise Q, K, V and run the e4m3 P V forward from one graph: the
+    V quantiser's memset, amax, codes and scale passes replay too."""
+    B, Hq, Hkv, N, d = 1, 4, 2, 500, 128
+    q, k, v = (x.to(DEV) for x in make_qkv(B, Hq, Hkv, N, N, d, 45))
+    nb = (N + 127) // 128
+    ld = (N + 15) // 16 * 16
+    q8, k8 = torch.empty(q.shape, dtype=torch.uint8, device=DEV), torch.empty(k.shape, dtype=torch.uint8, device=DEV)
+    qs, ks = torch.empty((B, Hq, nb), device=DEV), torch.empty((B, Hkv, nb), device=DEV)
+    vt8 = torch.empty((B, Hkv, d, ld), dtype=torch.uint8, device=DEV)
+    vs = torch.empty((B, Hkv), device=DEV)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, Hq, N), device=DEV)
+
+    def step():
+        attn.attn_quantize_fp8(q, codes=q8, scales=qs)
+        attn.attn_quantize_fp8(k, codes=k8, scales=ks)
+        attn.attn_quantize_fp8_v(v, vt8=vt8, scales=vs)
+        attn.attn_fwd_fp8_pv(q8, k8, vt8, qs, ks, vs, True, o=o, lse=lse)
+
+    g = _capture(step)
+    q2, k2, v2 = make_qkv(B, Hq, Hkv, N, N, d, 46)
+    q.copy_(q2)
+    k.copy_(k2)
+    v.copy_(v2 * 3)
+    g.replay()
+    torch.cuda.synchronize()
+    assert attn.attn_check_device_status() == 0
+    eq8, eqs = attn.attn_quantize_fp8(q)
+    ek8, eks = attn.attn_quantize_fp8(k)
+    evt, evs = attn.attn_quantize_fp8_v(v)
+    eo, el = attn.attn_fwd_fp8_pv(eq8, ek8, evt, eqs, eks, evs, True)
+    torch.cuda.synchronize()
+    assert torch.equal(vt8, evt) and torch.equal(vs, evs)
+    assert torch.equal(o, eo) and torch.equal(lse, el)

@@ -1,5 +1,6 @@
 """Seeded random shapes against the oracle: the forward (bf16 and fp32),
-split-KV decode, paged decode and the backward on combinations of batch,
+split-KV decode, paged decode, the backward and the two FP8 forwards on
+combinations of batch,
 GQA ratio, lengths (tile multiples or not, Nq != Nk), head dimension, mask
 and segment count that the hand-picked cases do not spell out.  The shapes
 are drawn once from a fixed seed, so every run checks the same list."""
@@ -63,10 +64,21 @@ def _bwd_shapes(n):
     return out
 
 
+def _fp8_shapes(n):
+    out = []
+    for _ in range(n):
+        Hkv = _R.choice([1, 2, 4])
+        Nq = _R.randint(1, 700)
+        Nk = Nq if _R.random() < 0.5 else _R.randint(1, 700)
+        out.append((_R.randint(1, 2), Hkv * _R.choice([1, 2, 4, 8]), Hkv, Nq, Nk, _R.random() < 0.5))
+    return out
+
+
 FWD = _fwd_shapes(40)
 DEC = _decode_shapes(20)
 PAGED = _paged_shapes(16)
 BWD = _bwd_shapes(16)
+FP8 = _fp8_shapes(12)  # drawn last, so the lists above stay as they were
 
 
 @pytest.mark.parametrize("B,Hq,Hkv,Nq,Nk,d,causal,dt", FWD)
@@ -120,3 +132,31 @@ def test_backward_random_shapes(attn, oracle_mod, B, Hq, Hkv, Nq, Nk, d, causal)
     check("dq", dq, rq)
     check("dk", dk, rk)
     check("dv", dv, rv)
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Nq,Nk,causal", FP8)
+def test_fp8_random_shapes(attn, oracle_mod, B, Hq, Hkv, Nq, Nk, causal):
+    """attn_fwd_fp8 within the bf16 bar of the oracle on the dequantised Q,
+    K, and attn_fwd_fp8_pv within the e4m3 P-rounding bound of the oracle on
+    the dequantised Q, K, V (d = 128)."""
+    import numpy as np
+    from parity import check_fp8_pv
+    from test_gpu_fp8 import fp8_pv_reference
+    d = 128
+    q, k, v = make_qkv(B, Hq, Hkv, Nq, Nk, d, 5 * Nq + Nk)
+    scale = 1.0 / math.sqrt(d)
+    q8, qsc = attn.attn_quantize_fp8(q.to(DEV))
+    k8, ksc = attn.attn_quantize_fp8(k.to(DEV))
+    vt8, vsc = attn.attn_quantize_fp8_v(v.to(DEV))
+    o8, l8 = attn.attn_fwd_fp8(q8, k8, v.to(DEV), qsc, ksc, causal, scale)
+    opv, lpv = attn.attn_fwd_fp8_pv(q8, k8, vt8, qsc, ksc, vsc, causal, scale)
+    torch.cuda.synchronize()
+    assert attn.attn_check_device_status() == 0
+    what = "B%d Hq%d Hkv%d Nq%d Nk%d c%d" % (B, Hq, Hkv, Nq, Nk, causal)
+    ro, rl, rabs, vabs_sum, _ = fp8_pv_reference(oracle_mod, q8, qsc, k8, ksc, vt8, vsc, Nk, causal, scale,
+                                                 Hq, Hkv)
+    check_fp8_pv(opv, lpv, ro, rl, rabs, vabs_sum, "fp8 P V " + what)
+    qd = oracle_mod.dequantize_fp8_blocks(q8.cpu().numpy(), qsc.cpu().numpy()).astype(np.float32)
+    kd = oracle_mod.dequantize_fp8_blocks(k8.cpu().numpy(), ksc.cpu().numpy()).astype(np.float32)
+    r8o, r8l = oracle_mod.attn_fwd(qd, kd, v, causal, scale)
+    compare(o8, l8, r8o, r8l, torch.bfloat16, "fp8 " + what)
