@@ -16,7 +16,8 @@ import ctypes
 import os
 
 __all__ = [
-    "AttnError", "ATTN_BF16", "ATTN_F32", "lib", "ensure_built", "library_path",
+    "AttnError", "ATTN_BF16", "ATTN_F32", "lib", "ensure_built", "library_path", "load_library",
+    "use_library",
     "attn_fwd", "attn_fwd_host", "attn_decode_num_splits", "attn_decode_workspace_bytes",
     "attn_decode_splitkv", "attn_merge_lse", "attn_status_string",
     "attn_check_device_status", "attn_read_tile_counter", "attn_version",
@@ -27,7 +28,7 @@ __all__ = [
     "AttnTestOptions", "attn_fwd_test", "attn_decode_test",
 ]
 
-ATTN_OK, ATTN_ERR_INVALID, ATTN_ERR_UNSUPPORTED, ATTN_ERR_CUDA, ATTN_ERR_TIMEOUT = range(5)
+ATTN_OK, ATTN_ERR_INVALID, ATTN_ERR_UNSUPPORTED, ATTN_ERR_CUDA, ATTN_ERR_TIMEOUT, ATTN_ERR_BOUNDS = range(6)
 ATTN_BF16, ATTN_F32 = 0, 1
 
 # Every symbol include/attn.h declares.
@@ -55,12 +56,12 @@ class AttnTestOptions(ctypes.Structure):
     """attn_test_options_t of include/attn_test.h (tests and measurements only)."""
     _fields_ = [("p_in_smem", ctypes.c_int), ("exp2_poly", ctypes.c_int),
                 ("rescale_threshold", ctypes.c_float), ("wait_limit_cycles", ctypes.c_longlong),
-                ("skip_load", ctypes.c_int)]
+                ("skip_load", ctypes.c_int), ("o_extent_slack", ctypes.c_longlong)]
 
     def __init__(self, p_in_smem=0, exp2_poly=0, rescale_threshold=0.0, wait_limit_cycles=0,
-                 skip_load=-1):
+                 skip_load=-1, o_extent_slack=0):
         super().__init__(int(p_in_smem), int(exp2_poly), float(rescale_threshold),
-                         int(wait_limit_cycles), int(skip_load))
+                         int(wait_limit_cycles), int(skip_load), int(o_extent_slack))
 
 
 class AttnError(RuntimeError):
@@ -92,7 +93,24 @@ def lib() -> ctypes.CDLL:
         raise RuntimeError(
             "libattn.so is not built (%s); run `python -m exact_attention_62_gb300.build` "
             "or __graft_entry__.build()" % _LIB_PATH)
-    L = ctypes.CDLL(_LIB_PATH)
+    _lib = load_library(_LIB_PATH)
+    return _lib
+
+
+def use_library(L):
+    """Makes every entry point of this module call the library L (a handle
+    from load_library) and returns the one in use before.  For tests that run
+    the same calls on the bounds-checked debug build, libattn_bounds.so."""
+    global _lib
+    old = _lib
+    _lib = L
+    return old
+
+
+def load_library(path: str) -> ctypes.CDLL:
+    """Loads a build of the library (libattn.so or the bounds-checked
+    libattn_bounds.so) with the argument types of every entry point."""
+    L = ctypes.CDLL(path)
     P, I, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
     LL, SZ = ctypes.c_longlong, ctypes.c_size_t
     L.attn_fwd.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, F, I, P]
@@ -145,7 +163,6 @@ def lib() -> ctypes.CDLL:
     L.attn_decode_model_time.restype = DB
     L.attn_decode_model_best.argtypes = [I, I, I, I, DB, DB, DB, DB, I]
     L.attn_decode_model_best.restype = I
-    _lib = L
     return L
 
 

@@ -4,6 +4,11 @@ Each translation unit under ``csrc/`` is compiled in parallel to an object in
 ``_build/`` and the objects are linked into ``libattn.so`` next to this file
 (the CUDA runtime is linked statically).  A unit is rebuilt only when it or a
 header is newer than its object.
+
+``build(bounds_check=True)`` builds the debug variant ``libattn_bounds.so``
+(objects in ``_build_bounds/``) with ATTN_BOUNDS_CHECK defined: its kernels
+check every global access that is not a TMA copy against its buffer's extent
+and report a refused access through attn_check_device_status.
 """
 from __future__ import annotations
 
@@ -18,11 +23,13 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libattn.so")
+BUILD_BOUNDS = os.path.join(PKG, "_build_bounds")
+LIB_BOUNDS = os.path.join(PKG, "libattn_bounds.so")
 INCLUDE = os.path.join(ROOT, "include")
 SOURCES = ["api.cu", "fwd_tc.cu", "fwd_f32.cu", "decode.cu", "decode_static.cu", "bwd_tc.cu",
            "fp8.cu", "host_pipeline.cu"]
 HEADERS = [os.path.join(CSRC, "ptx.cuh"), os.path.join(CSRC, "common.cuh"),
-           os.path.join(INCLUDE, "attn.h")]
+           os.path.join(INCLUDE, "attn.h"), os.path.join(INCLUDE, "attn_test.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -33,11 +40,13 @@ def nvcc() -> str:
     raise RuntimeError("nvcc not found (set NVCC or install the CUDA toolkit)")
 
 
-def _flags(verbose_ptxas: bool):
+def _flags(verbose_ptxas: bool, bounds_check: bool = False):
     f = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
                 "--expt-relaxed-constexpr", "-I", INCLUDE]
     if verbose_ptxas:
         f += ["-Xptxas", "-v"]
+    if bounds_check:
+        f += ["-DATTN_BOUNDS_CHECK"]
     return f
 
 
@@ -48,20 +57,22 @@ def _stale(src: str, obj: str) -> bool:
     return any(os.path.getmtime(p) > t for p in [src] + HEADERS)
 
 
-def build(force: bool = False, verbose_ptxas: bool = False, jobs: int = 4) -> str:
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose_ptxas: bool = False, jobs: int = 4,
+          bounds_check: bool = False) -> str:
+    build_dir, lib = (BUILD_BOUNDS, LIB_BOUNDS) if bounds_check else (BUILD, LIB)
+    os.makedirs(build_dir, exist_ok=True)
     cc = nvcc()
     objs, todo = [], []
     for s in SOURCES:
         src = os.path.join(CSRC, s)
-        obj = os.path.join(BUILD, s.replace(".cu", ".o"))
+        obj = os.path.join(build_dir, s.replace(".cu", ".o"))
         objs.append(obj)
         if force or verbose_ptxas or _stale(src, obj):
             todo.append((src, obj))
 
     def compile_one(item):
         src, obj = item
-        cmd = [cc] + _flags(verbose_ptxas) + ["-c", src, "-o", obj]
+        cmd = [cc] + _flags(verbose_ptxas, bounds_check) + ["-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         return src, r
 
@@ -74,14 +85,14 @@ def build(force: bool = False, verbose_ptxas: bool = False, jobs: int = 4) -> st
                 failed.append(src)
     if failed:
         raise RuntimeError("nvcc failed for: " + ", ".join(failed))
-    if todo or not os.path.exists(LIB) or any(os.path.getmtime(o) > os.path.getmtime(LIB) for o in objs):
-        tmp = LIB + ".tmp.%d" % os.getpid()
+    if todo or not os.path.exists(lib) or any(os.path.getmtime(o) > os.path.getmtime(lib) for o in objs):
+        tmp = lib + ".tmp.%d" % os.getpid()
         cmd = [cc] + ARCH + ["-shared", "-o", tmp] + objs
         subprocess.check_call(cmd)
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    build(force="--force" in sys.argv, verbose_ptxas="--ptxas-v" in sys.argv)
-    print(LIB)
+    print(build(force="--force" in sys.argv, verbose_ptxas="--ptxas-v" in sys.argv,
+                bounds_check="--bounds-check" in sys.argv))

@@ -11,6 +11,7 @@
 #include <cuda_bf16.h>
 
 #include "common.cuh"
+#include "ptx.cuh"
 
 namespace {
 
@@ -173,8 +174,8 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
 attn_status_t attn_fwd_test(const void* q, const void* k, const void* v, void* o, float* lse,
                             int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal, float scale,
                             const attn_test_options_t* opt, void* stream) {
-    if (opt == nullptr || opt->wait_limit_cycles < 0 || !(opt->rescale_threshold >= 0.f) ||
-        !(opt->rescale_threshold <= 8.f))
+    if (opt == nullptr || opt->wait_limit_cycles < 0 || opt->o_extent_slack < 0 ||
+        !(opt->rescale_threshold >= 0.f) || !(opt->rescale_threshold <= 8.f))
         return ATTN_ERR_INVALID;
     if (B < 0 || Hq < 0 || Nq < 0 || Nk < 0 || Hkv < 1 || d < 1) return ATTN_ERR_INVALID;
     if (causal != 0 && causal != 1) return ATTN_ERR_INVALID;
@@ -266,7 +267,7 @@ attn_status_t attn_decode_test(const void* q, const void* k_cache, const void* v
                                float* lse, int B, int Hq, int Hkv, int Nk, int d, float scale,
                                int num_splits, void* workspace, size_t workspace_bytes,
                                const attn_test_options_t* opt, void* stream) {
-    if (opt == nullptr || opt->wait_limit_cycles < 0) return ATTN_ERR_INVALID;
+    if (opt == nullptr || opt->wait_limit_cycles < 0 || opt->o_extent_slack < 0) return ATTN_ERR_INVALID;
     return decode_checked(q, k_cache, v_cache, o, lse, B, Hq, Hkv, Nk, d, scale, num_splits,
                           workspace, workspace_bytes, ATTN_BF16, stream, opt);
 }
@@ -460,17 +461,21 @@ const char* attn_status_string(attn_status_t status) {
         case ATTN_ERR_UNSUPPORTED: return "unsupported configuration";
         case ATTN_ERR_CUDA: return "CUDA error";
         case ATTN_ERR_TIMEOUT: return "device-side wait timed out";
+        case ATTN_ERR_BOUNDS: return "in-kernel bounds check refused an access";
     }
     return "unknown status";
 }
 
 attn_status_t attn_check_device_status(void) {
     if (cudaDeviceSynchronize() != cudaSuccess) return ATTN_ERR_CUDA;
-    unsigned a = 0, b = 0, c = 0;
+    unsigned a = 0, b = 0, c = 0, f = 0;
     if (attn_host::fwd_tc_read_status(&a, true) != cudaSuccess) return ATTN_ERR_CUDA;
     if (attn_host::decode_read_status(&b, true) != cudaSuccess) return ATTN_ERR_CUDA;
     if (attn_host::bwd_read_status(&c, true) != cudaSuccess) return ATTN_ERR_CUDA;
-    return (a | b | c) ? ATTN_ERR_TIMEOUT : ATTN_OK;
+    if (attn_host::fwd_f32_read_status(&f, true) != cudaSuccess) return ATTN_ERR_CUDA;
+    const unsigned all = a | b | c | f;
+    if (all & attn_dev::kStatusBounds) return ATTN_ERR_BOUNDS;
+    return all ? ATTN_ERR_TIMEOUT : ATTN_OK;
 }
 
 attn_status_t attn_read_tile_counter(unsigned long long* count, int reset) {

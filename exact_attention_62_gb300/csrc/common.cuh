@@ -89,6 +89,7 @@ attn_status_t launch_fwd_tc(const void* q, const void* k, const void* v, void* o
                             float scale, cudaStream_t stream,
                             const attn_test_options_t* test = nullptr, long long lse_ld = 0);
 cudaError_t fwd_tc_read_status(unsigned* out, bool clear);
+cudaError_t fwd_f32_read_status(unsigned* out, bool clear);
 cudaError_t fwd_tc_read_tiles(unsigned long long* out, bool reset);
 
 // ---- fp32 CUDA-core forward (fwd_f32.cu)
@@ -115,7 +116,7 @@ attn_status_t launch_decode(const void* q, const void* k, const void* v, void* o
                             const attn_test_options_t* test = nullptr);
 attn_status_t launch_merge(const float* o_parts, const float* lse_parts, int parts,
                            long long rows, int d, void* o, float* lse, bool out_bf16,
-                           cudaStream_t stream);
+                           cudaStream_t stream, long long o_slack = 0);
 cudaError_t decode_read_status(unsigned* out, bool clear);
 bool paged_splits_fit(int max_seq_len, int page_size, int splits);
 int decode_paged_auto_splits(int B, int Hq, int Hkv, int max_seq_len, int d, int page_size);

@@ -61,6 +61,7 @@ struct DecParams {
     float scale_log2;
     long long wait_limit;    // bound of every mbarrier wait, SM cycles
     int skip_load;           // tests only: tile of block (0, 0, 0) that is never loaded (-1: none)
+    long long o_slack;       // bounds-checked build, tests only: O's extent taken as this much smaller
     // paged cache only
     const int* table;        // [B, max_pages] page of each block of page_size keys
     const int* seq_lens;     // [B]
@@ -124,7 +125,13 @@ __global__ void __launch_bounds__(kDecThreads)
     // Keys of this sequence: all Nk, or (paged) its own length, clamped to
     // [0, Nk] where Nk is the caller's maximum.
     int len = p.Nk;
-    if constexpr (PAGED) len = min(max(p.seq_lens[b], 0), p.Nk);
+    if constexpr (PAGED) {
+        len = 0;
+        if (in_bounds(b, 1, p.B, &g_dec_status)) len = min(max(p.seq_lens[b], 0), p.Nk);
+    }
+    // (bounds-checked build) extents of the outputs and of the partials
+    const long long o_extent = (long long)p.B * p.Hq * D - p.o_slack;
+    const long long parts_rows = (long long)p.splits * p.B * p.Hq;
     const int j0 = seg * p.seg_len;
     const int j1 = min(j0 + p.seg_len, len);
     const int ntiles = j1 > j0 ? (j1 - j0 + kTileKeys - 1) / kTileKeys : 0;
@@ -134,11 +141,14 @@ __global__ void __launch_bounds__(kDecThreads)
         for (int e = threadIdx.x; e < GC * D; e += blockDim.x) {
             const long long row = (long long)b * p.Hq + hq0 + e / D;
             if (p.splits == 1) {  // a sequence with no keys at all
-                p.o[row * D + (e % D)] = __float2bfloat16_rn(0.f);
-                if (e % D == 0) p.lse[row] = -INFINITY;
+                if (in_bounds(row * D + (e % D), 1, o_extent, &g_dec_status))
+                    p.o[row * D + (e % D)] = __float2bfloat16_rn(0.f);
+                if (e % D == 0 && in_bounds(row, 1, (long long)p.B * p.Hq, &g_dec_status)) p.lse[row] = -INFINITY;
             } else {
-                p.o_parts[((long long)seg * R + row) * D + (e % D)] = 0.f;
-                if (e % D == 0) p.lse_parts[(long long)seg * R + row] = -INFINITY;
+                const long long po = ((long long)seg * R + row) * D + (e % D);
+                if (in_bounds(po, 1, parts_rows * D, &g_dec_status)) p.o_parts[po] = 0.f;
+                if (e % D == 0 && in_bounds((long long)seg * R + row, 1, parts_rows, &g_dec_status))
+                    p.lse_parts[(long long)seg * R + row] = -INFINITY;
             }
         }
         return;
@@ -167,8 +177,9 @@ __global__ void __launch_bounds__(kDecThreads)
             int* st_tab = reinterpret_cast<int*>(sgen + L::kOffTable);
             first_page = j0 / p.page_size;
             const int n_pages = (j1 - 1) / p.page_size - first_page + 1;
-            const int* src = p.table + (long long)b * p.max_pages + first_page;
-            for (int e = lane; e < n_pages; e += 32) st_tab[e] = src[e];
+            const long long t0 = (long long)b * p.max_pages + first_page;
+            for (int e = lane; e < n_pages; e += 32)
+                st_tab[e] = in_bounds(t0 + e, 1, (long long)p.B * p.max_pages, &g_dec_status) ? p.table[t0 + e] : 0;
             __syncwarp();
             tab = st_tab;
         }
@@ -252,8 +263,9 @@ __global__ void __launch_bounds__(kDecThreads)
     // Q^T as the B operand of S^T = K Q^T: column n = query head hq0 + n.
     uint32_t qb[D / 16][2];
     {
-        const bool qv = g8 < GC;
-        const __nv_bfloat16* qrow = p.q + ((long long)b * p.Hq + hq0 + (qv ? g8 : 0)) * D;
+        const long long qoff = ((long long)b * p.Hq + hq0 + (g8 < GC ? g8 : 0)) * D;
+        const bool qv = g8 < GC && in_bounds(qoff, D, (long long)p.B * p.Hq * D, &g_dec_status);
+        const __nv_bfloat16* qrow = p.q + qoff;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
             qb[kk][0] = qv ? ld_b32(qrow + kk * 16 + 2 * t4) : 0u;
@@ -409,11 +421,13 @@ __global__ void __launch_bounds__(kDecThreads)
         const float outv = lsum > 0.f ? ov / lsum : 0.f;
         const float lsev = lsum > 0.f ? (M + lg2(lsum)) * kLn2 : -INFINITY;
         if (p.splits == 1) {
-            p.o[row * D + dd] = __float2bfloat16_rn(outv);
-            if (dd == 0) p.lse[row] = lsev;
+            if (in_bounds(row * D + dd, 1, o_extent, &g_dec_status)) p.o[row * D + dd] = __float2bfloat16_rn(outv);
+            if (dd == 0 && in_bounds(row, 1, (long long)p.B * p.Hq, &g_dec_status)) p.lse[row] = lsev;
         } else {
-            p.o_parts[((long long)seg * R + row) * D + dd] = outv;
-            if (dd == 0) p.lse_parts[(long long)seg * R + row] = lsev;
+            const long long po = ((long long)seg * R + row) * D + dd;
+            if (in_bounds(po, 1, parts_rows * D, &g_dec_status)) p.o_parts[po] = outv;
+            if (dd == 0 && in_bounds((long long)seg * R + row, 1, parts_rows, &g_dec_status))
+                p.lse_parts[(long long)seg * R + row] = lsev;
         }
     }
 }
@@ -447,7 +461,7 @@ __device__ __forceinline__ float block_reduce(float x, bool is_max, float* red) 
 template <bool OUT_BF16>
 __global__ void __launch_bounds__(kMergeThreads)
     merge_lse_kernel(const float* __restrict__ o_parts, const float* __restrict__ lse_parts, int P,
-                     long long rows, int d, void* __restrict__ o, float* __restrict__ lse) {
+                     long long rows, int d, void* __restrict__ o, float* __restrict__ lse, long long o_slack) {
     __shared__ float red[kMergeThreads / 32];
     __shared__ float wts[kMergeChunk];
     __shared__ float4 part[kMergeThreads];
@@ -456,13 +470,18 @@ __global__ void __launch_bounds__(kMergeThreads)
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const long long row = blockIdx.x;
     const int tid = threadIdx.x;
+    // (bounds-checked build) a partial's LSE, or -inf if it lies outside lse_parts
+    auto lse_part = [&](int s) {
+        const long long off = (long long)s * rows + row;
+        return in_bounds(off, 1, (long long)P * rows, &g_dec_status) ? lse_parts[off] : -INFINITY;
+    };
     float M = -INFINITY;
-    for (int s = tid; s < P; s += kMergeThreads) M = fmaxf(M, lse_parts[(long long)s * rows + row]);
+    for (int s = tid; s < P; s += kMergeThreads) M = fmaxf(M, lse_part(s));
     M = block_reduce(M, true, red);
     float Lr = -INFINITY;
     if (M != -INFINITY) {  // uniform across the CTA
         float sum = 0.f;
-        for (int s = tid; s < P; s += kMergeThreads) sum += expf(lse_parts[(long long)s * rows + row] - M);
+        for (int s = tid; s < P; s += kMergeThreads) sum += expf(lse_part(s) - M);
         Lr = M + logf(block_reduce(sum, false, red));
     }
     const int C = d >> 2;               // 4-column groups, 1..128
@@ -474,7 +493,7 @@ __global__ void __launch_bounds__(kMergeThreads)
             const int n = min(kMergeChunk, P - s0);
             __syncthreads();  // wts of the previous chunk fully consumed
             for (int i = tid; i < n; i += kMergeThreads) {
-                const float ls = lse_parts[(long long)(s0 + i) * rows + row];
+                const float ls = lse_part(s0 + i);
                 wts[i] = ls == -INFINITY ? 0.f : expf(ls - Lr);
             }
             __syncthreads();
@@ -482,8 +501,9 @@ __global__ void __launch_bounds__(kMergeThreads)
 #pragma unroll 4
                 for (int i = sl; i < n; i += SL) {
                     const float w = wts[i];
-                    const float4 x = *reinterpret_cast<const float4*>(
-                        o_parts + ((long long)(s0 + i) * rows + row) * d + 4 * c4);
+                    const long long off = ((long long)(s0 + i) * rows + row) * d + 4 * c4;
+                    if (!in_bounds(off, 4, (long long)P * rows * d, &g_dec_status)) continue;
+                    const float4 x = *reinterpret_cast<const float4*>(o_parts + off);
                     a.x = fmaf(w, x.x, a.x);
                     a.y = fmaf(w, x.y, a.y);
                     a.z = fmaf(w, x.z, a.z);
@@ -494,7 +514,7 @@ __global__ void __launch_bounds__(kMergeThreads)
     }
     part[tid] = a;
     __syncthreads();
-    if (tid < C) {
+    if (tid < C && in_bounds(row * d + 4 * tid, 4, rows * d - o_slack, &g_dec_status)) {
         for (int j = 1; j < SL; ++j) {
             const float4 x = part[j * C + tid];
             a.x += x.x;
@@ -511,7 +531,7 @@ __global__ void __launch_bounds__(kMergeThreads)
             *reinterpret_cast<float4*>(static_cast<float*>(o) + row * d + 4 * tid) = a;
         }
     }
-    if (tid == 0 && lse != nullptr) lse[row] = Lr;
+    if (tid == 0 && lse != nullptr && in_bounds(row, 1, rows, &g_dec_status)) lse[row] = Lr;
 }
 
 // The same merge in one pass for few segments (at most kShortSeg per
@@ -524,7 +544,8 @@ constexpr int kShortSeg = 4;
 template <bool OUT_BF16>
 __global__ void __launch_bounds__(kMergeThreads)
     merge_lse_short_kernel(const float* __restrict__ o_parts, const float* __restrict__ lse_parts, int P,
-                           long long rows, int d, void* __restrict__ o, float* __restrict__ lse) {
+                           long long rows, int d, void* __restrict__ o, float* __restrict__ lse,
+                           long long o_slack) {
     __shared__ float red[kMergeThreads / 32];
     __shared__ float4 part[kMergeThreads];
     asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -539,10 +560,11 @@ __global__ void __launch_bounds__(kMergeThreads)
 #pragma unroll
     for (int r = 0; r < kShortSeg; ++r) {
         const int s = sl + r * SL;
-        const bool ok = sl < SL && s < P;
-        ls[r] = ok ? lse_parts[(long long)s * rows + row] : -INFINITY;
-        x[r] = ok ? *reinterpret_cast<const float4*>(o_parts + ((long long)s * rows + row) * d + 4 * c4)
-                  : make_float4(0.f, 0.f, 0.f, 0.f);
+        const long long lo = (long long)s * rows + row, oo = lo * d + 4 * c4;
+        const bool ok = sl < SL && s < P && in_bounds(lo, 1, (long long)P * rows, &g_dec_status) &&
+                        in_bounds(oo, 4, (long long)P * rows * d, &g_dec_status);
+        ls[r] = ok ? lse_parts[lo] : -INFINITY;
+        x[r] = ok ? *reinterpret_cast<const float4*>(o_parts + oo) : make_float4(0.f, 0.f, 0.f, 0.f);
         M = fmaxf(M, ls[r]);
     }
     M = block_reduce(M, true, red);
@@ -562,7 +584,7 @@ __global__ void __launch_bounds__(kMergeThreads)
     }
     part[tid] = a;
     lsum = block_reduce(lsum, false, red);  // its barriers also publish part[]
-    if (tid < C) {
+    if (tid < C && in_bounds(row * d + 4 * tid, 4, rows * d - o_slack, &g_dec_status)) {
         for (int j = 1; j < SL; ++j) {
             const float4 y = part[j * C + tid];
             a.x += y.x;
@@ -584,7 +606,8 @@ __global__ void __launch_bounds__(kMergeThreads)
             *reinterpret_cast<float4*>(static_cast<float*>(o) + row * d + 4 * tid) = a;
         }
     }
-    if (tid == 0 && lse != nullptr) lse[row] = lsum > 0.f ? M + logf(lsum) : -INFINITY;
+    if (tid == 0 && lse != nullptr && in_bounds(row, 1, rows, &g_dec_status))
+        lse[row] = lsum > 0.f ? M + logf(lsum) : -INFINITY;
 }
 
 int group_cols(int G) {
@@ -734,6 +757,7 @@ attn_status_t launch_decode(const void* q, const void* k, const void* v, void* o
     prm.scale_log2 = scale * 1.4426950408889634f;
     prm.wait_limit = (test && test->wait_limit_cycles > 0) ? test->wait_limit_cycles : kWaitLimitCycles;
     prm.skip_load = test ? test->skip_load : -1;
+    prm.o_slack = test ? test->o_extent_slack : 0;
     const size_t rows = (size_t)B * Hq;
     if (splits > 1) {
         const size_t o_bytes = (size_t)splits * rows * d * 4;
@@ -750,7 +774,8 @@ attn_status_t launch_decode(const void* q, const void* k, const void* v, void* o
     prm.max_pages = 0;
     const attn_status_t st = launch_split_any<false>(d, mk, mv, prm, stream);
     if (st != ATTN_OK || splits == 1) return st;
-    return launch_merge(prm.o_parts, prm.lse_parts, splits, (long long)rows, d, o, lse, true, stream);
+    return launch_merge(prm.o_parts, prm.lse_parts, splits, (long long)rows, d, o, lse, true, stream,
+                        prm.o_slack);
 }
 
 // Segment length of the paged kernel: whole 64-key tiles, so that a tile never
@@ -806,6 +831,7 @@ attn_status_t launch_decode_paged(const void* q, const void* k_pages, const void
     prm.scale_log2 = scale * 1.4426950408889634f;
     prm.wait_limit = kWaitLimitCycles;
     prm.skip_load = -1;
+    prm.o_slack = 0;
     prm.table = block_table;
     prm.seq_lens = seq_lens;
     prm.page_size = page_size;
@@ -827,7 +853,7 @@ attn_status_t launch_decode_paged(const void* q, const void* k_pages, const void
 
 attn_status_t launch_merge(const float* o_parts, const float* lse_parts, int parts,
                            long long rows, int d, void* o, float* lse, bool out_bf16,
-                           cudaStream_t stream) {
+                           cudaStream_t stream, long long o_slack) {
     if (rows == 0) return ATTN_OK;
     if (rows > 0x7fffffffLL || d < 4 || d > 4 * kMergeThreads / 2 || d % 4 != 0)
         return ATTN_ERR_UNSUPPORTED;
@@ -847,12 +873,12 @@ attn_status_t launch_merge(const float* o_parts, const float* lse_parts, int par
     const bool short_merge = parts <= kShortSeg * (kMergeThreads / (d / 4));
     cudaError_t e;
     if (short_merge)
-        e = out_bf16 ? cudaLaunchKernelEx(&cfg, merge_lse_short_kernel<true>, o_parts, lse_parts, parts, rows, d, o, lse)
+        e = out_bf16 ? cudaLaunchKernelEx(&cfg, merge_lse_short_kernel<true>, o_parts, lse_parts, parts, rows, d, o, lse, o_slack)
                      : cudaLaunchKernelEx(&cfg, merge_lse_short_kernel<false>, o_parts, lse_parts, parts, rows, d, o,
-                                          lse);
+                                          lse, o_slack);
     else
-        e = out_bf16 ? cudaLaunchKernelEx(&cfg, merge_lse_kernel<true>, o_parts, lse_parts, parts, rows, d, o, lse)
-                     : cudaLaunchKernelEx(&cfg, merge_lse_kernel<false>, o_parts, lse_parts, parts, rows, d, o, lse);
+        e = out_bf16 ? cudaLaunchKernelEx(&cfg, merge_lse_kernel<true>, o_parts, lse_parts, parts, rows, d, o, lse, o_slack)
+                     : cudaLaunchKernelEx(&cfg, merge_lse_kernel<false>, o_parts, lse_parts, parts, rows, d, o, lse, o_slack);
     return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

@@ -15,8 +15,14 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "ptx.cuh"
+
+using namespace attn_dev;
 
 namespace {
+
+// Status word of this kernel family: only the bounds-checked build sets it.
+__device__ unsigned g_f32_status = 0;
 
 __device__ __forceinline__ long long llmin(long long a, long long b) { return a < b ? a : b; }
 
@@ -64,9 +70,11 @@ __global__ void __launch_bounds__(kThreadsF32)
         const int rr = idx / C4, c4 = idx % C4;
         const int qr = qt * kRows + rr;
         float4 val = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (qr < p.Nq)
-            val = __ldg(reinterpret_cast<const float4*>(
-                q + (((long long)b * p.Nq + qr) * p.Hq + hq) * D) + c4);
+        if (qr < p.Nq) {
+            const long long qoff = (((long long)b * p.Nq + qr) * p.Hq + hq) * D;
+            if (in_bounds(qoff + 4 * c4, 4, (long long)p.B * p.Nq * p.Hq * D, &g_f32_status))
+                val = __ldg(reinterpret_cast<const float4*>(q + qoff) + c4);
+        }
         *reinterpret_cast<float4*>(Qs + rr * L::kLd + 4 * c4) = val;
     }
 
@@ -93,8 +101,10 @@ __global__ void __launch_bounds__(kThreadsF32)
             float4 kv = make_float4(0.f, 0.f, 0.f, 0.f), vv = kv;
             if (key < p.Nk) {
                 const long long off = (((long long)b * p.Nk + key) * p.Hkv + g) * D;
-                kv = __ldg(reinterpret_cast<const float4*>(k + off) + c4);
-                vv = __ldg(reinterpret_cast<const float4*>(v + off) + c4);
+                if (in_bounds(off + 4 * c4, 4, (long long)p.B * p.Nk * p.Hkv * D, &g_f32_status)) {
+                    kv = __ldg(reinterpret_cast<const float4*>(k + off) + c4);
+                    vv = __ldg(reinterpret_cast<const float4*>(v + off) + c4);
+                }
             }
             *reinterpret_cast<float4*>(Ks + rr * L::kLd + 4 * c4) = kv;
             *reinterpret_cast<float4*>(Vs + rr * L::kLd + 4 * c4) = vv;
@@ -165,16 +175,19 @@ __global__ void __launch_bounds__(kThreadsF32)
     if (row < p.Nq) {
         const float inv = l > 0.f ? 1.f / l : 0.f;
         float* orow = o + (((long long)b * p.Nq + row) * p.Hq + hq) * D;
+        if (in_bounds(orow - o, D, (long long)p.B * p.Nq * p.Hq * D, &g_f32_status)) {
 #pragma unroll
-        for (int i = 0; i < NCH; ++i) {
-            float4 w = acc[i];
-            w.x *= inv;
-            w.y *= inv;
-            w.z *= inv;
-            w.w *= inv;
-            reinterpret_cast<float4*>(orow)[cg + 4 * i] = w;
+            for (int i = 0; i < NCH; ++i) {
+                float4 w = acc[i];
+                w.x *= inv;
+                w.y *= inv;
+                w.z *= inv;
+                w.w *= inv;
+                reinterpret_cast<float4*>(orow)[cg + 4 * i] = w;
+            }
         }
-        if (cg == 0)
+        if (cg == 0 &&
+            in_bounds(((long long)b * p.Hq + hq) * p.Nq + row, 1, (long long)p.B * p.Hq * p.Nq, &g_f32_status))
             lse[((long long)b * p.Hq + hq) * p.Nq + row] = l > 0.f ? m + logf(l) : -INFINITY;
     }
 }
@@ -202,6 +215,13 @@ attn_status_t launch_fwd_f32(const float* q, const float* k, const float* v, flo
     if (d == 128) return launch_impl<128>(q, k, v, o, lse, prm, stream);
     if (d == 64) return launch_impl<64>(q, k, v, o, lse, prm, stream);
     return ATTN_ERR_UNSUPPORTED;
+}
+
+cudaError_t fwd_f32_read_status(unsigned* out, bool clear) {
+    cudaError_t e = cudaMemcpyFromSymbol(out, g_f32_status, sizeof(unsigned));
+    if (e != cudaSuccess || !clear) return e;
+    const unsigned zero = 0;
+    return cudaMemcpyToSymbol(g_f32_status, &zero, sizeof(unsigned));
 }
 
 }  // namespace attn_host

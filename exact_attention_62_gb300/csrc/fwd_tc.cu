@@ -119,6 +119,7 @@ struct FwdParams {
     float rescale_thr;  // log2 units; 0 = rescale whenever the max grows
     long long wait_limit;  // bound of every mbarrier wait, SM cycles
     int skip_load;         // tests only: ring position whose K/V block 0 never loads (-1: none)
+    long long o_slack;     // bounds-checked build, tests only: O's extent taken as this much smaller
     // FP8 inputs only: e4m3 Q and K with one scale per (batch, head, 128-row block)
     const float* q_scales;  // [B, Hq, nqb]
     const float* k_scales;  // [B, Hkv, nkb]
@@ -461,13 +462,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int nt = x.n[t];
             __nv_bfloat16* orow = p.o + (((long long)x.b * p.Nq + row) * p.Hq + x.hq) * D;
             float* lse_out = p.lse + ((long long)x.b * p.Hq + x.hq) * p.lse_ld + row;
+            // (bounds-checked build) the row's D outputs and its LSE, inside O and LSE
+            auto o_row_ok = [&]() {
+                return in_bounds(orow - p.o, D, (long long)p.B * p.Nq * p.Hq * D - p.o_slack, &g_fwd_status);
+            };
+            auto lse_ok = [&]() {
+                return in_bounds(lse_out - p.lse, 1, ((long long)p.B * p.Hq - 1) * p.lse_ld + p.Nq,
+                                 &g_fwd_status);
+            };
             if (nt == 0) {
                 // Tile beyond Nq, or rows with no allowed key at all.
                 if (row < p.Nq) {
                     const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+                    if (o_row_ok()) {
 #pragma unroll
-                    for (int c = 0; c < D / 8; ++c) reinterpret_cast<uint4*>(orow)[c] = z;
-                    *lse_out = -INFINITY;
+                        for (int c = 0; c < D / 8; ++c) reinterpret_cast<uint4*>(orow)[c] = z;
+                    }
+                    if (lse_ok()) *lse_out = -INFINITY;
                 }
                 continue;
             }
@@ -633,7 +644,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if constexpr (D == 128) tmem_ld64_sync(tO + 64, xo + 64);
             tc_fence_before();
             mbar_arrive(bar(L::kBarOEmpty + t));  // the next unit's PV may overwrite O_t now
-            if (row < p.Nq) {
+            if (row < p.Nq && o_row_ok()) {
                 const float inv = l > 0.f ? v_scale / l : 0.f;
 #pragma unroll
                 for (int c = 0; c < D / 8; ++c) {
@@ -644,8 +655,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     w.w = pack_bf16(__uint_as_float(xo[8 * c + 6]) * inv, __uint_as_float(xo[8 * c + 7]) * inv);
                     reinterpret_cast<uint4*>(orow)[c] = w;
                 }
-                *lse_out = l > 0.f ? (m + lg2(l) - kPExp) * kLn2 : -INFINITY;
             }
+            if (row < p.Nq && lse_ok()) *lse_out = l > 0.f ? (m + lg2(l) - kPExp) * kLn2 : -INFINITY;
         }
     }
 
@@ -700,6 +711,7 @@ attn_status_t launch_impl(const void* q, const void* k, const void* v, void* o, 
     prm.rescale_thr = test ? test->rescale_threshold : 0.0f;
     prm.wait_limit = (test && test->wait_limit_cycles > 0) ? test->wait_limit_cycles : kWaitLimitCycles;
     prm.skip_load = test ? test->skip_load : -1;
+    prm.o_slack = test ? test->o_extent_slack : 0;
     prm.q_scales = q_scales;
     prm.k_scales = k_scales;
     prm.v_scales = v_scales;

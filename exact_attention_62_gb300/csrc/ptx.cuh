@@ -19,6 +19,30 @@ constexpr long long kWaitLimitCycles = 1ll << 32;
 
 // Bits of the per-family device status word.
 constexpr unsigned kStatusTimeout = 1u;
+constexpr unsigned kStatusBounds = 2u;
+
+// The bounds-checked debug build (compiled with ATTN_BOUNDS_CHECK, the
+// library libattn_bounds.so) checks every global access that is not a TMA
+// copy against the extent of its buffer.
+#ifdef ATTN_BOUNDS_CHECK
+constexpr bool kBoundsCheck = true;
+#else
+constexpr bool kBoundsCheck = false;
+#endif
+
+// True iff the n elements at element offset `off` lie inside a buffer of
+// `extent` elements.  Otherwise kStatusBounds is set in the family's status
+// word and the caller skips the access: nothing traps.  In the production
+// build this is the constant true and adds no code.
+__device__ __forceinline__ bool in_bounds(long long off, long long n, long long extent, unsigned* status) {
+    if constexpr (!kBoundsCheck) {
+        return true;
+    } else {
+        if (off >= 0 && n >= 0 && off + n <= extent) return true;
+        atomicOr(status, kStatusBounds);
+        return false;
+    }
+}
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));

@@ -41,7 +41,9 @@ typedef enum {
     ATTN_ERR_INVALID = 1,      /* bad pointer, size, alignment or scale     */
     ATTN_ERR_UNSUPPORTED = 2,  /* valid but not implemented (d, dtype, G)   */
     ATTN_ERR_CUDA = 3,         /* a CUDA runtime/driver call failed         */
-    ATTN_ERR_TIMEOUT = 4       /* a device-side bounded wait ran out        */
+    ATTN_ERR_TIMEOUT = 4,      /* a device-side bounded wait ran out        */
+    ATTN_ERR_BOUNDS = 5        /* debug build only: an in-kernel index check
+                                  refused an access outside its buffer      */
 } attn_status_t;
 
 typedef enum {
@@ -411,8 +413,13 @@ const char* attn_status_string(attn_status_t status);
 /*
  * attn_check_device_status -- reads and clears the device status words of
  * every kernel family in the library (synchronises the device first).
- * Returns ATTN_ERR_TIMEOUT if any bounded wait ran out since the last call,
- * ATTN_ERR_CUDA if the device could not be read, else ATTN_OK.
+ * Returns ATTN_ERR_BOUNDS if an in-kernel index check refused an access since
+ * the last call (only the bounds-checked debug build, libattn_bounds.so, built
+ * with ATTN_BOUNDS_CHECK, makes these checks: on every global load and store
+ * that is not a TMA copy in the forward kernels, the decode split kernel and
+ * the merge kernels; a refused access is skipped, nothing traps), else
+ * ATTN_ERR_TIMEOUT if any bounded wait ran out, ATTN_ERR_CUDA if the device
+ * could not be read, else ATTN_OK.
  */
 attn_status_t attn_check_device_status(void);
 

@@ -53,12 +53,21 @@ typedef struct {
      * (0 = the first key tile it loads); decode, this tile of the block's
      * segment (0 = its first 64 keys). */
     int skip_load;
+    /* Only the bounds-checked debug build (libattn_bounds.so) reads this:
+     * the kernels take O's extent as this many elements less than B*Nq*Hq*d
+     * (decode: B*Hq*d, for the split kernel's and the merge's stores), so
+     * that the index check refuses the stores of the last rows, skips them
+     * and reports ATTN_ERR_BOUNDS (a test of the check itself; the buffer is
+     * whole, so nothing is ever written outside it).  0 = the true extent;
+     * negative = ATTN_ERR_INVALID.  Production builds ignore it. */
+    long long o_extent_slack;
 } attn_test_options_t;
 
 /*
  * attn_fwd_test -- attn_fwd (ATTN_BF16 only) with the options above.  Same
  * arguments, layouts and errors as attn_fwd, plus ATTN_ERR_INVALID for a
- * NULL `opt`, a threshold outside [0, 8] or a negative wait bound.
+ * NULL `opt`, a threshold outside [0, 8], a negative wait bound or a
+ * negative extent slack.
  */
 attn_status_t attn_fwd_test(const void* q, const void* k, const void* v, void* o,
                             float* lse, int B, int Hq, int Hkv, int Nq, int Nk, int d,
@@ -69,7 +78,7 @@ attn_status_t attn_fwd_test(const void* q, const void* k, const void* v, void* o
  * attn_decode_test -- attn_decode_splitkv with the wait bound and the load
  * injection of `opt` (the forward-only fields are ignored).  Same
  * arguments and errors as attn_decode_splitkv, plus ATTN_ERR_INVALID for a
- * NULL `opt` or a negative wait bound.
+ * NULL `opt`, a negative wait bound or a negative extent slack.
  */
 attn_status_t attn_decode_test(const void* q, const void* k_cache, const void* v_cache,
                                void* o, float* lse, int B, int Hq, int Hkv, int Nk, int d,

@@ -45,8 +45,9 @@ def test_every_declared_symbol_is_exported(L):
 
 
 def test_status_strings_and_version(L):
-    for code in range(5):
-        assert pkg.attn_status_string(code)
+    for code in range(6):
+        assert pkg.attn_status_string(code) and pkg.attn_status_string(code) != "unknown status"
+    assert "bounds" in pkg.attn_status_string(pkg.ATTN_ERR_BOUNDS)
     assert pkg.attn_status_string(99) == "unknown status"
     assert "sm_103a" in pkg.attn_version()
 
