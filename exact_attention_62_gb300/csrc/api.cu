@@ -468,12 +468,13 @@ const char* attn_status_string(attn_status_t status) {
 
 attn_status_t attn_check_device_status(void) {
     if (cudaDeviceSynchronize() != cudaSuccess) return ATTN_ERR_CUDA;
-    unsigned a = 0, b = 0, c = 0, f = 0;
+    unsigned a = 0, b = 0, c = 0, f = 0, e = 0;
     if (attn_host::fwd_tc_read_status(&a, true) != cudaSuccess) return ATTN_ERR_CUDA;
     if (attn_host::decode_read_status(&b, true) != cudaSuccess) return ATTN_ERR_CUDA;
     if (attn_host::bwd_read_status(&c, true) != cudaSuccess) return ATTN_ERR_CUDA;
     if (attn_host::fwd_f32_read_status(&f, true) != cudaSuccess) return ATTN_ERR_CUDA;
-    const unsigned all = a | b | c | f;
+    if (attn_host::fp8_read_status(&e, true) != cudaSuccess) return ATTN_ERR_CUDA;
+    const unsigned all = a | b | c | f | e;
     if (all & attn_dev::kStatusBounds) return ATTN_ERR_BOUNDS;
     return all ? ATTN_ERR_TIMEOUT : ATTN_OK;
 }

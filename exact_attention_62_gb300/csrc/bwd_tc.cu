@@ -117,7 +117,7 @@ __global__ void __launch_bounds__(kDotThreads)
         const long long row = base + (long long)u * kRowsPerPass;  // (b, i, hq) row-major
         a[u] = make_uint4(0u, 0u, 0u, 0u);
         c[u] = a[u];
-        if (row < rows) {
+        if (row < rows && in_bounds(row * D + 8 * sub, 8, rows * D, &g_bwd_status)) {
             a[u] = __ldg(reinterpret_cast<const uint4*>(o + row * D) + sub);
             c[u] = __ldg(reinterpret_cast<const uint4*>(dout + row * D) + sub);
         }
@@ -142,7 +142,8 @@ __global__ void __launch_bounds__(kDotThreads)
             const long long bi = row / Hq;
             const int i = (int)(bi % Nq);
             const int b = (int)(bi / Nq);
-            dvec[((long long)b * Hq + hq) * Nq + i] = acc;
+            if (in_bounds(((long long)b * Hq + hq) * Nq + i, 1, rows, &g_bwd_status))
+                dvec[((long long)b * Hq + hq) * Nq + i] = acc;
         }
     }
 }
@@ -238,7 +239,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (n == 0) {  // rows with no allowed key: dQ = 0
         for (int e = threadIdx.x; e < kT * (D / 8); e += kThreads) {
             const int rr = e / (D / 8), c = e % (D / 8);
-            if (r0 + rr < p.Nq)
+            if (r0 + rr < p.Nq &&
+                in_bounds((((long long)b * p.Nq + r0 + rr) * p.Hq + hq) * D + 8 * c, 8,
+                          (long long)p.B * p.Nq * p.Hq * D, &g_bwd_status))
                 reinterpret_cast<uint4*>(p.dq + (((long long)b * p.Nq + r0 + rr) * p.Hq + hq) * D)[c] =
                     make_uint4(0u, 0u, 0u, 0u);
         }
@@ -357,7 +360,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int row = r0 + r;
         const uint32_t lane_base = static_cast<uint32_t>(q4 * 32) << 16;
         float lse2 = INFINITY, dval = 0.f;  // rows past Nq: P = 0
-        if (row < p.Nq) {
+        if (row < p.Nq && in_bounds(((long long)b * p.Hq + hq) * p.Nq + row, 1,
+                                    (long long)p.B * p.Hq * p.Nq, &g_bwd_status)) {
             const float l = p.lse[((long long)b * p.Hq + hq) * p.Nq + row];
             lse2 = l == -INFINITY ? INFINITY : l * kLog2e;  // a row with no allowed key: P = 0
             dval = p.dvec[((long long)b * p.Hq + hq) * p.Nq + row];
@@ -411,11 +415,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             // warpgroup w writes dQ columns [w D/2, (w + 1) D/2)
             __nv_bfloat16* out = p.dq + (((long long)b * p.Nq + row) * p.Hq + hq) * D + w * (D / 2);
+            const bool out_ok =
+                row >= p.Nq || in_bounds(out - p.dq, D / 2, (long long)p.B * p.Nq * p.Hq * D, &g_bwd_status);
             uint32_t xo[32];
 #pragma unroll
             for (int h = 0; h < D / 64; ++h) {
                 tmem_ld32_sync(tmem + lane_base + kDQ + w * (D / 2) + 32 * h, xo);
-                if (row < p.Nq) {
+                if (row < p.Nq && out_ok) {
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
                         uint4 v;
@@ -476,8 +482,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int rr = e / (D / 8), c = e % (D / 8);
             if (c0 + rr < p.Nk) {
                 const long long off = (((long long)b * p.Nk + c0 + rr) * p.Hkv + g) * D;
-                reinterpret_cast<uint4*>(p.dk + off)[c] = make_uint4(0u, 0u, 0u, 0u);
-                reinterpret_cast<uint4*>(p.dv + off)[c] = make_uint4(0u, 0u, 0u, 0u);
+                if (in_bounds(off + 8 * c, 8, (long long)p.B * p.Nk * p.Hkv * D, &g_bwd_status)) {
+                    reinterpret_cast<uint4*>(p.dk + off)[c] = make_uint4(0u, 0u, 0u, 0u);
+                    reinterpret_cast<uint4*>(p.dv + off)[c] = make_uint4(0u, 0u, 0u, 0u);
+                }
             }
         }
         return;
@@ -625,7 +633,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         auto fetch = [&](int it) {
             const int hh = it_head(it), row = it_tile(it) * kT + 64 * w + (tid & 63);
             float x = tid < 64 ? INFINITY : 0.f;
-            if (row < p.Nq) {
+            if (row < p.Nq && in_bounds(((long long)b * p.Hq + hh) * p.Nq + row, 1,
+                                        (long long)p.B * p.Hq * p.Nq, &g_bwd_status)) {
                 const long long o = ((long long)b * p.Hq + hh) * p.Nq + row;
                 if (tid < 64) {
                     const float l = p.lse[o];
@@ -692,11 +701,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             // warpgroup w writes columns [w D/2, (w + 1) D/2) of dV and dK
             const long long off = (((long long)b * p.Nk + key) * p.Hkv + g) * D + w * (D / 2);
+            const bool out_ok =
+                key >= p.Nk || in_bounds(off, D / 2, (long long)p.B * p.Nk * p.Hkv * D, &g_bwd_status);
             uint32_t xo[32];
 #pragma unroll
             for (int h = 0; h < D / 64; ++h) {
                 tmem_ld32_sync(tmem + lane_base + kDV + w * (D / 2) + 32 * h, xo);
-                if (key < p.Nk) {
+                if (key < p.Nk && out_ok) {
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
                         uint4 v;
@@ -708,7 +719,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 tmem_ld32_sync(tmem + lane_base + kDK + w * (D / 2) + 32 * h, xo);
-                if (key < p.Nk) {
+                if (key < p.Nk && out_ok) {
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
                         uint4 v;

@@ -90,6 +90,7 @@ attn_status_t launch_fwd_tc(const void* q, const void* k, const void* v, void* o
                             const attn_test_options_t* test = nullptr, long long lse_ld = 0);
 cudaError_t fwd_tc_read_status(unsigned* out, bool clear);
 cudaError_t fwd_f32_read_status(unsigned* out, bool clear);
+cudaError_t fp8_read_status(unsigned* out, bool clear);
 cudaError_t fwd_tc_read_tiles(unsigned long long* out, bool reset);
 
 // ---- fp32 CUDA-core forward (fwd_f32.cu)

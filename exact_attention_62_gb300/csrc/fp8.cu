@@ -16,7 +16,12 @@
 #include "common.cuh"
 #include "ptx.cuh"
 
+using namespace attn_dev;
+
 namespace {
+
+// Status word of the quantisers: only the bounds-checked build sets it.
+__device__ unsigned g_fp8_status = 0;
 
 constexpr int kBlockRows = 128;
 constexpr int kQThreads = 256;
@@ -56,7 +61,8 @@ __global__ void __launch_bounds__(kQThreads)
         const int i = threadIdx.x + k * kQThreads;
         const int r = i / kC, c = i % kC;
         v[k] = make_uint4(0u, 0u, 0u, 0u);
-        if (r < rows)
+        if (r < rows && in_bounds((((long long)b * N + r0 + r) * H + h) * D + 8 * c, 8, (long long)gridDim.z * N * H * D,
+                                  &g_fp8_status))
             v[k] = __ldg(reinterpret_cast<const uint4*>(x + (((long long)b * N + r0 + r) * H + h) * D) + c);
         const __nv_bfloat162* e = reinterpret_cast<const __nv_bfloat162*>(&v[k]);
 #pragma unroll
@@ -68,12 +74,16 @@ __global__ void __launch_bounds__(kQThreads)
     amax = block_max(amax);
     const bool nz = amax > 0.f;
     const float inv = nz ? kFp8Max / amax : 1.f;
-    if (threadIdx.x == 0) scales[((long long)b * H + h) * nb + blk] = nz ? amax / kFp8Max : 1.f;
+    if (threadIdx.x == 0 && in_bounds(((long long)b * H + h) * nb + blk, 1, (long long)gridDim.z * H * nb, &g_fp8_status))
+        scales[((long long)b * H + h) * nb + blk] = nz ? amax / kFp8Max : 1.f;
 #pragma unroll
     for (int k = 0; k < kK; ++k) {
         const int i = threadIdx.x + k * kQThreads;
         const int r = i / kC, c = i % kC;
         if (r >= rows) continue;
+        if (!in_bounds((((long long)b * N + r0 + r) * H + h) * D + 8 * c, 8, (long long)gridDim.z * N * H * D,
+                       &g_fp8_status))
+            continue;
         const __nv_bfloat162* e = reinterpret_cast<const __nv_bfloat162*>(&v[k]);
         uint32_t w[2];
 #pragma unroll
@@ -125,7 +135,8 @@ __global__ void __launch_bounds__(kQThreads)
     for (int k = 0; k < kK; ++k) {
         const int r = (threadIdx.x + k * kQThreads) / kC;
         uint4 raw = make_uint4(0u, 0u, 0u, 0u);
-        if (r < rows)
+        if (r < rows && in_bounds((((long long)b * N + r0 + r) * H + h) * D + 8 * c, 8, (long long)gridDim.z * N * H * D,
+                                  &g_fp8_status))
             raw = __ldg(reinterpret_cast<const uint4*>(x + (((long long)b * N + r0 + r) * H + h) * D) + c);
         const __nv_bfloat162* e2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
 #pragma unroll
@@ -160,12 +171,15 @@ __global__ void __launch_bounds__(kQThreads)
     amax = block_max(amax);
     const bool nz = amax > 0.f;
     const float inv = nz ? kFp8Max / amax : 1.f;
-    if (threadIdx.x == 0)
+    if (threadIdx.x == 0 && in_bounds(((long long)b * H + h) * nb + blk, 1, (long long)gridDim.z * H * nb, &g_fp8_status))
         scales[((long long)b * H + h) * nb + blk] = __fmul_rn(nz ? amax / kFp8Max : 1.f, c_norm);
 #pragma unroll
     for (int k = 0; k < kK; ++k) {
         const int r = (threadIdx.x + k * kQThreads) / kC;
         if (r >= rows) continue;
+        if (!in_bounds((((long long)b * N + r0 + r) * H + h) * D + 8 * c, 8, (long long)gridDim.z * N * H * D,
+                       &g_fp8_status))
+            continue;
         uint32_t w[2];
 #pragma unroll
         for (int t = 0; t < 4; ++t) {
@@ -200,6 +214,9 @@ __global__ void __launch_bounds__(kQThreads)
     float amax = 0.f;
     for (int i = threadIdx.x; i < rows * kC; i += kQThreads) {
         const int r = i / kC, c = i % kC;
+        if (!in_bounds((((long long)b * N + r0 + r) * H + h) * D + 8 * c, 8, (long long)gridDim.z * N * H * D,
+                       &g_fp8_status))
+            continue;
         const uint4 raw = __ldg(reinterpret_cast<const uint4*>(v + (((long long)b * N + r0 + r) * H + h) * D) + c);
         const __nv_bfloat162* e = reinterpret_cast<const __nv_bfloat162*>(&raw);
 #pragma unroll
@@ -209,7 +226,8 @@ __global__ void __launch_bounds__(kQThreads)
         }
     }
     amax = block_max(amax);
-    if (threadIdx.x == 0) atomicMax(amax_bits + (long long)b * H + h, __float_as_uint(amax));
+    if (threadIdx.x == 0 && in_bounds((long long)b * H + h, 1, (long long)gridDim.z * H, &g_fp8_status))
+        atomicMax(amax_bits + (long long)b * H + h, __float_as_uint(amax));
 }
 
 // Pass 2: each CTA quantises 128 keys x D of one (batch, head) with
@@ -226,13 +244,15 @@ __global__ void __launch_bounds__(kQThreads)
     constexpr int kRow = kBlockRows + 16;  // tile row stride: 16-byte aligned, rows 4 banks apart
     __shared__ __align__(16) uint8_t tile[D * kRow];
     const int r0 = blockIdx.x * kBlockRows, h = blockIdx.y, b = blockIdx.z;
-    const float amax = __uint_as_float(amax_bits[(long long)b * H + h]);
+    const float amax = in_bounds((long long)b * H + h, 1, (long long)gridDim.z * H, &g_fp8_status)
+                           ? __uint_as_float(amax_bits[(long long)b * H + h]) : 0.f;
     const bool nz = amax > 0.f;
     const float inv = nz ? kFp8Max / amax : 1.f;
     for (int i = threadIdx.x; i < kBlockRows * kC; i += kQThreads) {
         const int r = i % kBlockRows, c = i / kBlockRows;
         uint4 raw = make_uint4(0u, 0u, 0u, 0u);
-        if (r0 + r < N)
+        if (r0 + r < N && in_bounds((((long long)b * N + r0 + r) * H + h) * D + 8 * c, 8,
+                                    (long long)gridDim.z * N * H * D, &g_fp8_status))
             raw = __ldg(reinterpret_cast<const uint4*>(v + (((long long)b * N + r0 + r) * H + h) * D) + c);
         const __nv_bfloat162* e = reinterpret_cast<const __nv_bfloat162*>(&raw);
 #pragma unroll
@@ -249,7 +269,8 @@ __global__ void __launch_bounds__(kQThreads)
     for (int i = threadIdx.x; i < D * (kBlockRows / 16); i += kQThreads) {
         const int row = i / (kBlockRows / 16), ch = i % (kBlockRows / 16);
         const long long key = (long long)r0 + 16 * ch;
-        if (key >= ld) continue;
+        if (key >= ld || !in_bounds(base + row * ld + key, 16, (long long)gridDim.z * H * D * ld, &g_fp8_status))
+            continue;
         *reinterpret_cast<uint4*>(vt + base + row * ld + key) =
             *reinterpret_cast<const uint4*>(tile + row * kRow + 16 * ch);
     }
@@ -277,17 +298,21 @@ __global__ void __launch_bounds__(kQThreads)
         const int r = e / (d / 2), c = 2 * (e % (d / 2));
         return (((long long)b * N + r0 + r) * H + h) * d + c;
     };
+    const long long extent = (long long)gridDim.z * N * H * d;
     float amax = 0.f;
     for (int e = threadIdx.x; e < pairs; e += kQThreads) {
+        if (!in_bounds(pair_offset(e), 2, extent, &g_fp8_status)) continue;
         const float2 v = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(x + pair_offset(e)));
         amax = fmaxf(amax, fmaxf(fabsf(v.x), fabsf(v.y)));
     }
     amax = block_max(amax);
     const bool nz = amax > 0.f;
     const float inv = nz ? kFp8Max / amax : 1.f;
-    if (threadIdx.x == 0) scales[((long long)b * H + h) * nb + blk] = nz ? amax / kFp8Max : 1.f;
+    if (threadIdx.x == 0 && in_bounds(((long long)b * H + h) * nb + blk, 1, (long long)gridDim.z * H * nb, &g_fp8_status))
+        scales[((long long)b * H + h) * nb + blk] = nz ? amax / kFp8Max : 1.f;
     for (int e = threadIdx.x; e < pairs; e += kQThreads) {
         const long long o = pair_offset(e);
+        if (!in_bounds(o, 2, extent, &g_fp8_status)) continue;
         const float2 v = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(x + o));
         const float2 y = make_float2(__fmul_rn(v.x, inv), __fmul_rn(v.y, inv));
         const __nv_fp8x2_storage_t q = __nv_cvt_float2_to_fp8x2(y, __NV_SATFINITE, __NV_E4M3);
@@ -350,6 +375,13 @@ attn_status_t launch_quantize_fp8_rotated(const void* x, const float* signs, voi
     else
         quantize_fp8_rot_kernel<64><<<grid, kQThreads, 0, stream>>>(xb, signs, cb, scales, N, H, c_norm);
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+cudaError_t fp8_read_status(unsigned* out, bool clear) {
+    cudaError_t e = cudaMemcpyFromSymbol(out, g_fp8_status, sizeof(unsigned));
+    if (e != cudaSuccess || !clear) return e;
+    const unsigned zero = 0;
+    return cudaMemcpyToSymbol(g_fp8_status, &zero, sizeof(unsigned));
 }
 
 }  // namespace attn_host

@@ -416,8 +416,8 @@ const char* attn_status_string(attn_status_t status);
  * Returns ATTN_ERR_BOUNDS if an in-kernel index check refused an access since
  * the last call (only the bounds-checked debug build, libattn_bounds.so, built
  * with ATTN_BOUNDS_CHECK, makes these checks: on every global load and store
- * that is not a TMA copy in the forward kernels, the decode split kernel and
- * the merge kernels; a refused access is skipped, nothing traps), else
+ * that is not a TMA copy, in every kernel family; a refused access is
+ * skipped, nothing traps), else
  * ATTN_ERR_TIMEOUT if any bounded wait ran out, ATTN_ERR_CUDA if the device
  * could not be read, else ATTN_OK.
  */

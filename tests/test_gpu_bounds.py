@@ -1,9 +1,8 @@
 """The bounds-checked debug build, libattn_bounds.so (compiled with
-ATTN_BOUNDS_CHECK).  In it, every global load and store of the forward
-kernels (tcgen05 and fp32), the decode split kernel and the merge kernels
-that is not a TMA copy is checked against its buffer's extent.  A refused
-access is skipped and reported by attn_check_device_status as
-ATTN_ERR_BOUNDS; nothing traps.
+ATTN_BOUNDS_CHECK).  In it, every global load and store that is not a TMA
+copy (forward, decode, merge, backward and FP8 kernels) is checked against
+its buffer's extent.  A refused access is skipped and reported by
+attn_check_device_status as ATTN_ERR_BOUNDS; nothing traps.
 
 1. On correct calls the checks never fire and change nothing: every result
    equals the production library's bit for bit, and the status stays OK.
@@ -130,3 +129,36 @@ def test_decode_check_refuses_past_the_extent(attn, bounds_lib, S):
     assert torch.all(rows[-1] == 7.0)                     # the last row: refused
     assert torch.equal(rows[:-1], rrows[:-1])
     assert torch.equal(lse_got, ref[1])
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Nq,Nk,d,causal", [
+    (2, 4, 2, 300, 300, 64, True),
+    (1, 8, 2, 257, 400, 128, False),
+])
+def test_backward_unchanged(attn, bounds_lib, B, Hq, Hkv, Nq, Nk, d, causal):
+    q, k, v = (x.to(DEV) for x in make_qkv(B, Hq, Hkv, Nq, Nk, d, Nq + 2 * Nk))
+    dout = torch.randn((B, Nq, Hq, d), generator=torch.Generator().manual_seed(5)).to(torch.bfloat16).to(DEV)
+    scale = 1.0 / math.sqrt(d)
+
+    def run():
+        o, lse = attn.attn_fwd(q, k, v, causal, scale)
+        return (o, lse) + tuple(attn.attn_bwd(q, k, v, o, lse, dout, causal, scale))
+
+    _both(attn, bounds_lib, run)
+
+
+def test_fp8_unchanged(attn, bounds_lib):
+    B, Hq, Hkv, N, d = 1, 4, 2, 300, 128
+    q, k, v = (x.to(DEV) for x in make_qkv(B, Hq, Hkv, N, N, d, 9))
+    signs = (torch.randint(0, 2, (d,), generator=torch.Generator().manual_seed(2)) * 2 - 1).float().to(DEV)
+
+    def run():
+        q8, qs = attn.attn_quantize_fp8(q)
+        k8, ks = attn.attn_quantize_fp8(k)
+        r8, rs = attn.attn_quantize_fp8_rotated(q, signs)
+        vt8, vs = attn.attn_quantize_fp8_v(v)
+        o8, l8 = attn.attn_fwd_fp8(q8, k8, v, qs, ks, True)
+        opv, lpv = attn.attn_fwd_fp8_pv(q8, k8, vt8, qs, ks, vs, True)
+        return q8, qs, r8, rs, vt8, vs, o8, l8, opv, lpv
+
+    _both(attn, bounds_lib, run)
