@@ -710,3 +710,44 @@ def test_fp16_exponential_overflows_near_11_09():
     with np.errstate(over="ignore"):
         assert np.isfinite(np.float16(np.exp(11.08)))
         assert np.isinf(np.float16(np.exp(11.10)))
+
+
+def test_fp8_pv_checker_accepts_e4m3_p_and_rejects_real_errors(oracle_mod):
+    """check_fp8_pv (used by the GPU tests of the e4m3 P V forward) accepts
+    an evaluation that rounds 256 P to e4m3 (nearest even) before P V, with
+    l over the unrounded P, as the bound it states allows; and rejects
+    results with a plausible mistake: a V row off by one key, a key left
+    out, or the 2^8 factor of P not taken back out."""
+    from parity import check_fp8_pv
+    rng = np.random.default_rng(11)
+    B, Hq, Hkv, Nq, Nk, d = 1, 2, 1, 40, 70, 16
+    scale = 0.5
+    q = torch.from_numpy(rng.standard_normal((B, Nq, Hq, d)).astype(np.float32)).to(torch.bfloat16)
+    k = torch.from_numpy(rng.standard_normal((B, Nk, Hkv, d)).astype(np.float32)).to(torch.bfloat16)
+    v = torch.from_numpy((rng.standard_normal((B, Nk, Hkv, d)) * 3).astype(np.float32)).to(torch.bfloat16)
+    ro, rl = oracle_mod.attn_fwd(q, k, v, True, scale)
+    rabs, _ = oracle_mod.attn_fwd(q, k, v.abs(), True, scale)
+    vabs_sum = np.abs(v.double().numpy()).sum(axis=1)[:, None, :, :].repeat(Hq, axis=2)
+
+    def emulate(v_shift=0, drop=None, undo=256.0):
+        qd, kd, vd = q.double().numpy(), k.double().numpy(), v.double().numpy()
+        o = np.zeros((B, Nq, Hq, d))
+        for h in range(Hq):
+            for i in range(Nq):
+                last = i + (Nk - Nq)
+                s = scale * kd[0, :last + 1, 0] @ qd[0, i, h]
+                pr = np.exp(s - s.max())
+                p8 = torch.from_numpy(256.0 * pr).to(torch.float8_e4m3fn).double().numpy()
+                if drop is not None and drop <= last:
+                    p8[drop] = 0.0
+                rows = np.clip(np.arange(last + 1) + v_shift, 0, Nk - 1)
+                o[0, i, h] = p8 @ vd[0, rows, 0] / (undo * pr.sum())
+        return torch.from_numpy(o).to(torch.bfloat16), torch.from_numpy(rl.astype(np.float32))
+
+    o, lse = emulate()
+    err = check_fp8_pv(o, lse, ro, rl, rabs, vabs_sum, "emulated e4m3 P")
+    assert err > 1e-3                          # the rounding of P is visible
+    for bad in (dict(v_shift=1), dict(drop=35), dict(undo=1.0)):
+        o_bad, _ = emulate(**bad)
+        with pytest.raises(AssertionError):
+            check_fp8_pv(o_bad, lse, ro, rl, rabs, vabs_sum, "planted %s" % bad)
