@@ -83,10 +83,10 @@ NOMINAL_HBM_GBS = 8000.0  # the ~8 TB/s HBM3e figure the decode target is quoted
 # dram__bytes_write.sum), keyed by the hash of the kernel source it was
 # measured on: any later change to the source turns the figure into null.
 NCU_TRAFFIC = {
-    "long_sequence": {"bytes_per_launch": 348.34e6 + 101.28e6, "src": "fwd_tc.cu",
-                      "src_hash": "2c96717052fcb170"},
-    "decode_b16_8k": {"bytes_per_launch": 537.03e6 + 4.01e6, "src": "decode.cu",
-                      "src_hash": "e3a41edb273c7aa5"},
+    "long_sequence": {"bytes_per_launch": 350.80e6 + 101.38e6, "src": "fwd_tc.cu",
+                      "src_hash": "f289683a689bd204"},
+    "decode_b16_8k": {"bytes_per_launch": 537.04e6 + 3.35e6, "src": "decode.cu",
+                      "src_hash": "b1a4a625e04ba019"},
 }
 
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
