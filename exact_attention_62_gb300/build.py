@@ -28,7 +28,7 @@ LIB_BOUNDS = os.path.join(PKG, "libattn_bounds.so")
 INCLUDE = os.path.join(ROOT, "include")
 SOURCES = ["api.cu", "fwd_tc.cu", "fwd_f32.cu", "decode.cu", "decode_static.cu", "bwd_tc.cu",
            "fp8.cu", "host_pipeline.cu"]
-HEADERS = [os.path.join(CSRC, "ptx.cuh"), os.path.join(CSRC, "common.cuh"),
+HEADERS = [os.path.join(CSRC, "ptx.cuh"), os.path.join(CSRC, "common.cuh"), os.path.join(CSRC, "per_device.h"),
            os.path.join(INCLUDE, "attn.h"), os.path.join(INCLUDE, "attn_test.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -85,14 +85,14 @@ bool encode_vt_map(CUtensorMap* map, const void* base, int B, int H, int d, long
 }
 
 int device_sm_count() {
-    static int cache[kMaxDevices] = {0};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 0;
-    if (dev < kMaxDevices && cache[dev] > 0) return cache[dev];
+    static PerDevice<int> cache;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
     int n = 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-    if (dev < kMaxDevices) cache[dev] = n;
-    return n;
+    const bool ok = cache.get(dev, &n, [&](int* out) {
+        return cudaDeviceGetAttribute(out, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && *out > 0;
+    });
+    return ok ? n : 0;
 }
 
 attn_status_t check_decode_args(const void* q, const void* k_cache, const void* v_cache,

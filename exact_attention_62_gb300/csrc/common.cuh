@@ -9,20 +9,17 @@
 #include <mutex>
 
 #include "../../include/attn.h"
+#include "per_device.h"
 #include "../../include/attn_test.h"
 
 namespace attn_host {
-
-// Devices a process may drive; per-device caches below are this large.
-constexpr int kMaxDevices = 64;
 
 // One-time launch set-up of a kernel, per device.  The dynamic shared-memory
 // limit that cudaFuncSetAttribute sets belongs to the current device, and the
 // register count is read for the device that will run the kernel, so a
 // process that drives several GPUs (even from one thread) needs both for
-// each device.  The first call on a device does the set-up; later calls
-// return the cached result.  A failed set-up is not cached (the next call
-// retries).
+// each device: a PerDevice cache (per_device.h), in which a failed set-up is
+// not kept (the next call retries).
 struct KernelSetup {
     cudaError_t err;
     int num_regs;
@@ -30,26 +27,24 @@ struct KernelSetup {
 
 template <auto Kernel>
 KernelSetup kernel_setup(int dyn_smem_bytes) {
-    static std::mutex mu;
-    static bool done[kMaxDevices] = {};
-    static int regs[kMaxDevices] = {};
+    static PerDevice<int> regs;
     int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
-        return {cudaErrorInvalidDevice, 0};
-    std::lock_guard<std::mutex> lock(mu);
-    if (!done[dev]) {
+    if (cudaGetDevice(&dev) != cudaSuccess) return {cudaErrorInvalidDevice, 0};
+    cudaError_t err = cudaSuccess;
+    int n = 0;
+    const bool ok = regs.get(dev, &n, [&](int* out) {
         if (dyn_smem_bytes > 0) {
-            const cudaError_t e = cudaFuncSetAttribute(
-                Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn_smem_bytes);
-            if (e != cudaSuccess) return {e, 0};
+            err = cudaFuncSetAttribute(Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn_smem_bytes);
+            if (err != cudaSuccess) return false;
         }
         cudaFuncAttributes fa;
-        const cudaError_t e = cudaFuncGetAttributes(&fa, Kernel);
-        if (e != cudaSuccess) return {e, 0};
-        regs[dev] = fa.numRegs;
-        done[dev] = true;
-    }
-    return {cudaSuccess, regs[dev]};
+        err = cudaFuncGetAttributes(&fa, Kernel);
+        if (err != cudaSuccess) return false;
+        *out = fa.numRegs;
+        return true;
+    });
+    if (!ok) return {err != cudaSuccess ? err : cudaErrorInvalidDevice, 0};
+    return {cudaSuccess, n};
 }
 
 // Encodes a 4-D TMA tensor map over a row-major [B, N, H, d] tensor of

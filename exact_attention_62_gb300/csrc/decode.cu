@@ -646,21 +646,21 @@ attn_status_t launch_split_any(int d, const CUtensorMap& mk, const CUtensorMap& 
 // Resident split-kernel CTAs per SM on the current device (cached per device).
 template <int D>
 int ctas_per_sm() {
-    static std::mutex mu;
-    static int cache[attn_host::kMaxDevices] = {};
+    static attn_host::PerDevice<int> cache;
     int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= attn_host::kMaxDevices) return 1;
-    std::lock_guard<std::mutex> lock(mu);
-    if (cache[dev] == 0) {
+    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    int n = 1;
+    const bool ok = cache.get(dev, &n, [&](int* out) {
         using L = DecLayout<D, dec_stages<D>()>;
-        int n = 0;
+        int k = 0;
         if (attn_host::kernel_setup<decode_split_kernel<D, 4, false>>(L::kSmemBytes).err != cudaSuccess ||
-            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_split_kernel<D, 4, false>,
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&k, decode_split_kernel<D, 4, false>,
                                                           kDecThreads, L::kSmemBytes) != cudaSuccess)
-            return 1;
-        cache[dev] = std::max(1, n);
-    }
-    return cache[dev];
+            return false;
+        *out = std::max(1, k);
+        return true;
+    });
+    return ok ? n : 1;
 }
 
 }  // namespace
