@@ -76,7 +76,6 @@ struct BwdParams {
     __nv_bfloat16* dv;
     int B, Hq, Hkv, Nq, Nk, G, causal;
     float scale, scale_log2;
-    int num_kv_units;  // dK/dV kernel: B * Hkv * key tiles
 };
 
 __device__ __forceinline__ long long llmin(long long a, long long b) { return a < b ? a : b; }
@@ -169,10 +168,8 @@ struct BwdLay {
     static constexpr int kBarS = kBarEmpty + STAGES;
     static constexpr int kBarC = kBarS + 1;   // S^T, dP^T read into registers (256 threads)
     static constexpr int kBarDS = kBarC + 1;  // P^T, dS^T in TMEM (256 threads)
-    static constexpr int kBarAcc = kBarDS + 1;   // dV, dK complete (dK/dV kernel: per unit)
-    static constexpr int kBarXE = kBarAcc + 1;   // dK/dV kernel: the unit's K, V fully read
-    static constexpr int kBarAccE = kBarXE + 1;  // dK/dV kernel: dV, dK read out of TMEM (256 threads)
-    static constexpr int kNumBars = kBarAccE + 1;
+    static constexpr int kBarAcc = kBarDS + 1;
+    static constexpr int kNumBars = kBarAcc + 1;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
     static constexpr int kSmem = kOffMisc + 16 + 1024;
     static_assert(kSmem <= 232448, "shared memory budget");
@@ -448,41 +445,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ------------------------------------------------------------------ dK, dV
-// A work unit is one 128-key tile of one KV head, (b, g, key tile), with the
-// (query head of the group, query tile) pairs whose rows may see its keys.
-// Units are numbered longest first (causal: the first key tiles are seen by
-// the most rows) and dealt to the persistent CTAs in snake order.
-struct KvUnit {
-    int b, g, c0, i0, per_head, n;  // n = (query head, query tile) iterations
-};
-
-__device__ __forceinline__ KvUnit kv_unit_at(int u, const BwdParams& p) {
-    KvUnit x;
-    const int bg = u % (p.B * p.Hkv);
-    x.b = bg / p.Hkv;
-    x.g = bg % p.Hkv;
-    x.c0 = (u / (p.B * p.Hkv)) * kT;
-    const int n_qt = (p.Nq + kT - 1) / kT;
-    x.i0 = min(first_q_tile(x.c0, p), n_qt);
-    x.per_head = n_qt - x.i0;
-    x.n = x.per_head * p.G;
-    return x;
-}
-
-// The k-th unit of this CTA, or -1.
-__device__ __forceinline__ int kv_unit_index(int k, const BwdParams& p) {
-    const int G = gridDim.x, c = blockIdx.x;
-    const long long u = (long long)k * G + ((k & 1) ? (G - 1 - c) : c);
-    return u < p.num_kv_units ? (int)u : -1;
-}
-
-// Persistent: each CTA walks its units, and a unit's edges overlap its
-// neighbours'.  The Q/dO ring runs on across units; the next unit's K and V
-// are loaded as soon as this unit's last S^T and dP^T have read them (X
-// empty, committed by the MMA warp), while the last elementwise pass, dV/dK
-// and the epilogue still run; and the epilogue reads dV, dK out of TMEM and
-// releases them (accumulators empty) before it stores, so the next unit's
-// products proceed meanwhile.
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
@@ -500,12 +462,38 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(sgen + L::kOffMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sgen + L::kOffMisc + 4);
     // The dQ kernel, launched next as a programmatic dependent, reads nothing
-    // this kernel writes: let its CTAs take the SMs this grid frees.
+    // this kernel writes: let its CTAs take the SMs this grid's last wave frees.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
+    // key tile, longest first (causal: the first key tiles are seen by the most rows)
+    const int n_kt = (p.Nk + kT - 1) / kT;
+    const int bg = blockIdx.x % (p.B * p.Hkv);
+    const int kt = (int)(blockIdx.x / (p.B * p.Hkv));
+    const int b = bg / p.Hkv, g = bg % p.Hkv;
+    const int c0 = kt * kT;
+    const int n_qt = (p.Nq + kT - 1) / kT;
+    const int i0 = min(first_q_tile(c0, p), n_qt);
+    const int per_head = n_qt - i0;
+    const int n = per_head * p.G;  // (query head, query tile) iterations
+    (void)n_kt;
+
+    if (n == 0) {  // no query row sees these keys: dK = dV = 0
+        for (int e = threadIdx.x; e < kT * (D / 8); e += kThreads) {
+            const int rr = e / (D / 8), c = e % (D / 8);
+            if (c0 + rr < p.Nk) {
+                const long long off = (((long long)b * p.Nk + c0 + rr) * p.Hkv + g) * D;
+                if (in_bounds(off + 8 * c, 8, (long long)p.B * p.Nk * p.Hkv * D, &g_bwd_status)) {
+                    reinterpret_cast<uint4*>(p.dk + off)[c] = make_uint4(0u, 0u, 0u, 0u);
+                    reinterpret_cast<uint4*>(p.dv + off)[c] = make_uint4(0u, 0u, 0u, 0u);
+                }
+            }
+        }
+        return;
+    }
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < L::kNumBars; ++i)
-            mbar_init(bar(i), (i == L::kBarDS || i == L::kBarC || i == L::kBarAccE) ? 2u * kT : 1u);
+            mbar_init(bar(i), (i == L::kBarDS || i == L::kBarC) ? 2u * kT : 1u);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -518,6 +506,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     constexpr uint32_t kS = 0, kDP = 128, kDV = 256, kDK = 384;
+    auto it_head = [&](int it) { return g * p.G + it / per_head; };
+    auto it_tile = [&](int it) { return i0 + it % per_head; };
 
     if (warp < 4) {
       warpgroup_reg_dealloc<kRegsWG0>();
@@ -527,35 +517,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             prefetch_tmap(&tmDO);
             prefetch_tmap(&tmK);
             prefetch_tmap(&tmV);
-            int gi = 0;  // Q/dO tiles loaded (ring position)
-            int ux = 0;  // units whose K and V were loaded
-            bool ok = true;
-            for (int k = 0; ok; ++k) {
-                const int u = kv_unit_index(k, p);
-                if (u < 0) break;
-                const KvUnit x = kv_unit_at(u, p);
-                if (x.n == 0) continue;
-                if (ux > 0)  // the previous unit's last S^T and dP^T have read K and V
-                    ok = mbar_wait(bar(L::kBarXE), (ux - 1) & 1, abort_flag, &g_bwd_status);
-                if (!ok) break;
-                mbar_arrive_expect_tx(bar(L::kBarX), 2 * L::kTile);
+            mbar_arrive_expect_tx(bar(L::kBarX), 2 * L::kTile);
+            for (int pp = 0; pp < L::kPanels; ++pp) {
+                tma_load_4d(sbase + L::kOffX0 + pp * kPanel, &tmK, bar(L::kBarX), 64 * pp, g, c0, b);
+                tma_load_4d(sbase + L::kOffX1 + pp * kPanel, &tmV, bar(L::kBarX), 64 * pp, g, c0, b);
+            }
+            for (int it = 0; it < n; ++it) {
+                const int st = it % STAGES;
+                if (!mbar_wait(bar(L::kBarEmpty + st), ((it / STAGES) & 1) ^ 1, abort_flag, &g_bwd_status))
+                    break;
+                mbar_arrive_expect_tx(bar(L::kBarFull + st), L::kStage);
+                const uint32_t dst = sbase + L::kOffRing + st * L::kStage;
+                const int hh = it_head(it), rq = it_tile(it) * kT;
                 for (int pp = 0; pp < L::kPanels; ++pp) {
-                    tma_load_4d(sbase + L::kOffX0 + pp * kPanel, &tmK, bar(L::kBarX), 64 * pp, x.g, x.c0, x.b);
-                    tma_load_4d(sbase + L::kOffX1 + pp * kPanel, &tmV, bar(L::kBarX), 64 * pp, x.g, x.c0, x.b);
-                }
-                ++ux;
-                for (int it = 0; it < x.n; ++it, ++gi) {
-                    const int st = gi % STAGES;
-                    ok = mbar_wait(bar(L::kBarEmpty + st), ((gi / STAGES) & 1) ^ 1, abort_flag, &g_bwd_status);
-                    if (!ok) break;
-                    mbar_arrive_expect_tx(bar(L::kBarFull + st), L::kStage);
-                    const uint32_t dst = sbase + L::kOffRing + st * L::kStage;
-                    const int hh = x.g * p.G + it / x.per_head, rq = (x.i0 + it % x.per_head) * kT;
-                    for (int pp = 0; pp < L::kPanels; ++pp) {
-                        tma_load_4d(dst + pp * kPanel, &tmQ, bar(L::kBarFull + st), 64 * pp, hh, rq, x.b);
-                        tma_load_4d(dst + L::kTile + pp * kPanel, &tmDO, bar(L::kBarFull + st), 64 * pp, hh, rq,
-                                    x.b);
-                    }
+                    tma_load_4d(dst + pp * kPanel, &tmQ, bar(L::kBarFull + st), 64 * pp, hh, rq, b);
+                    tma_load_4d(dst + L::kTile + pp * kPanel, &tmDO, bar(L::kBarFull + st), 64 * pp, hh, rq,
+                                b);
                 }
             }
         }
@@ -564,95 +541,78 @@ __global__ void __launch_bounds__(kThreads, 1)
         constexpr uint32_t kIdAcc = idesc_bf16_f32(kT, D, true);   // dV, dK: N = D, B N-major
         constexpr uint32_t kHi = sdesc_sw128_hi(1024);
         constexpr uint32_t kNLbo = D == 128 ? kPanel : 1024;
+        bool ok = mbar_wait_warp(bar(L::kBarX), 0, abort_flag, &g_bwd_status);
+        tc_fence_after();
         const uint32_t k_lo = sdesc_sw128_lo(sbase + L::kOffX0, 16);
         const uint32_t v_lo = sdesc_sw128_lo(sbase + L::kOffX1, 16);
-        bool ok = true;
-        auto ring = [&](int gi) { return sbase + L::kOffRing + (gi % STAGES) * L::kStage; };
-        auto wait_full = [&](int gi) {
-            if (ok) ok = mbar_wait_warp(bar(L::kBarFull + gi % STAGES), (gi / STAGES) & 1, abort_flag, &g_bwd_status);
+        auto ring = [&](int it) { return sbase + L::kOffRing + (it % STAGES) * L::kStage; };
+        auto wait_full = [&](int it) {
+            if (ok) ok = mbar_wait_warp(bar(L::kBarFull + it % STAGES), (it / STAGES) & 1, abort_flag, &g_bwd_status);
             if (ok) tc_fence_after();
         };
-        auto issue_s = [&](int gi) {  // S^T = K Q^T
-            const uint32_t q_lo = sdesc_sw128_lo(ring(gi), 16);
+        auto issue_s = [&](int it) {  // S^T = K Q_it^T
+            const uint32_t q_lo = sdesc_sw128_lo(ring(it), 16);
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
                 const uint32_t off = ((kk >> 2) * kPanel + (kk & 3) * 32) >> 4;
                 mma_ss_elect(tmem + kS, k_lo + off, kHi, q_lo + off, kHi, kIdSS, kk > 0 ? 1u : 0u);
             }
         };
-        auto issue_dp = [&](int gi) {  // dP^T = V dO^T
-            const uint32_t do_lo = sdesc_sw128_lo(ring(gi) + L::kTile, 16);
+        auto issue_dp = [&](int it) {  // dP^T = V dO_it^T
+            const uint32_t do_lo = sdesc_sw128_lo(ring(it) + L::kTile, 16);
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
                 const uint32_t off = ((kk >> 2) * kPanel + (kk & 3) * 32) >> 4;
                 mma_ss_elect(tmem + kDP, v_lo + off, kHi, do_lo + off, kHi, kIdSS, kk > 0 ? 1u : 0u);
             }
         };
-        int g0 = 0;  // ring position of the unit's first Q/dO tile
-        int ux = 0;  // units started
-        for (int k = 0; ok; ++k) {
-            const int u = kv_unit_index(k, p);
-            if (u < 0) break;
-            const KvUnit x = kv_unit_at(u, p);
-            if (x.n == 0) continue;
-            ok = mbar_wait_warp(bar(L::kBarX), ux & 1, abort_flag, &g_bwd_status);  // this unit's K, V
+        wait_full(0);
+        if (ok) {
+            issue_s(0);
+            issue_dp(0);
+            tc_commit_elect(bar(L::kBarS));
+        }
+        for (int it = 0; it < n && ok; ++it) {
+            bool s_next = false;  // S^T of the next tile already issued
+            if (it + 1 < n) {
+                // The elementwise warps hold S^T and dP^T and write P^T, dS^T over
+                // dP^T only, so the S columns are free: if the next Q tile is
+                // already loaded, its S^T goes to the tensor core now.
+                ok = mbar_wait_warp(bar(L::kBarC), it & 1, abort_flag, &g_bwd_status);
+                if (!ok) break;
+                s_next = __all_sync(0xffffffffu,
+                                    mbar_try_wait(bar(L::kBarFull + (it + 1) % STAGES), ((it + 1) / STAGES) & 1));
+                if (s_next) {
+                    tc_fence_after();
+                    issue_s(it + 1);
+                }
+            }
+            ok = mbar_wait_warp(bar(L::kBarDS), it & 1, abort_flag, &g_bwd_status);
             if (!ok) break;
             tc_fence_after();
-            wait_full(g0);
-            if (!ok) break;
-            issue_s(g0);
-            issue_dp(g0);
-            if (x.n == 1) tc_commit_elect(bar(L::kBarXE));  // the unit's last S^T, dP^T
-            tc_commit_elect(bar(L::kBarS));
-            for (int it = 0; it < x.n && ok; ++it) {
-                const int gi = g0 + it;
-                bool s_next = false;  // S^T of the next tile already issued
-                if (it + 1 < x.n) {
-                    // The elementwise warps hold S^T and dP^T and write P^T, dS^T over
-                    // dP^T only, so the S columns are free: if the next Q tile is
-                    // already loaded, its S^T goes to the tensor core now.
-                    ok = mbar_wait_warp(bar(L::kBarC), gi & 1, abort_flag, &g_bwd_status);
-                    if (!ok) break;
-                    s_next = __all_sync(0xffffffffu,
-                                        mbar_try_wait(bar(L::kBarFull + (gi + 1) % STAGES), ((gi + 1) / STAGES) & 1));
-                    if (s_next) {
-                        tc_fence_after();
-                        issue_s(gi + 1);
-                    }
-                }
-                ok = mbar_wait_warp(bar(L::kBarDS), gi & 1, abort_flag, &g_bwd_status);
-                if (!ok) break;
-                if (it == 0 && ux > 0)  // the previous unit's dV, dK have been read out of TMEM
-                    ok = mbar_wait_warp(bar(L::kBarAccE), (ux - 1) & 1, abort_flag, &g_bwd_status);
-                if (!ok) break;
-                tc_fence_after();
-                const uint32_t qn_lo = sdesc_sw128_lo(ring(gi), kNLbo);
-                const uint32_t don_lo = sdesc_sw128_lo(ring(gi) + L::kTile, kNLbo);
+            const uint32_t qn_lo = sdesc_sw128_lo(ring(it), kNLbo);
+            const uint32_t don_lo = sdesc_sw128_lo(ring(it) + L::kTile, kNLbo);
 #pragma unroll
-                for (int kk = 0; kk < kT / 16; ++kk) {  // 16 query rows = 8 bf16 columns of P^T / dS^T
-                    const uint32_t r_off = (kk * 16 * 128) >> 4;
-                    const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
-                    // query rows 16kk..: warpgroup kk / 4 wrote P^T at dP^T column 64 (kk / 4) + 8 (kk % 4)
-                    // and dS^T 32 columns further
-                    const uint32_t pc = (kk >> 2) * 64 + (kk & 3) * 8;
-                    mma_ts_elect(tmem + kDV, tmem + kDP + pc, don_lo + r_off, kHi, kIdAcc, acc);       // dV += P^T dO
-                    mma_ts_elect(tmem + kDK, tmem + kDP + 32 + pc, qn_lo + r_off, kHi, kIdAcc, acc);  // dK += dS^T Q
-                }
-                tc_commit_elect(bar(L::kBarEmpty + gi % STAGES));  // Q and dO of this tile fully read
-                if (it + 1 < x.n) {
-                    if (!s_next) {
-                        wait_full(gi + 1);
-                        if (!ok) break;
-                        issue_s(gi + 1);
-                    }
-                    issue_dp(gi + 1);  // after dV, dK have read P^T, dS^T (in-order pipe)
-                    if (it + 2 == x.n) tc_commit_elect(bar(L::kBarXE));  // the unit's last S^T, dP^T
-                    tc_commit_elect(bar(L::kBarS));
-                }
-                if (it == x.n - 1) tc_commit_elect(bar(L::kBarAcc));
+            for (int kk = 0; kk < kT / 16; ++kk) {  // 16 query rows = 8 bf16 columns of P^T / dS^T
+                const uint32_t r_off = (kk * 16 * 128) >> 4;
+                const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
+                // query rows 16kk..: warpgroup kk / 4 wrote P^T at dP^T column 64 (kk / 4) + 8 (kk % 4)
+                // and dS^T 32 columns further
+                const uint32_t pc = (kk >> 2) * 64 + (kk & 3) * 8;
+                mma_ts_elect(tmem + kDV, tmem + kDP + pc, don_lo + r_off, kHi, kIdAcc, acc);       // dV += P^T dO
+                mma_ts_elect(tmem + kDK, tmem + kDP + 32 + pc, qn_lo + r_off, kHi, kIdAcc, acc);  // dK += dS^T Q
             }
-            g0 += x.n;
-            ++ux;
+            tc_commit_elect(bar(L::kBarEmpty + it % STAGES));  // Q_i and dO_i fully read
+            if (it + 1 < n) {
+                if (!s_next) {
+                    wait_full(it + 1);
+                    if (!ok) break;
+                    issue_s(it + 1);
+                }
+                issue_dp(it + 1);  // after dV, dK have read P^T, dS^T (in-order pipe)
+                tc_commit_elect(bar(L::kBarS));
+            }
+            if (it == n - 1) tc_commit_elect(bar(L::kBarAcc));
         }
       }
     } else {
@@ -662,155 +622,115 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int w = (warp - 4) >> 2;
         const int q4 = warp & 3;
         const int r = q4 * 32 + lane;
+        const int key = c0 + r;
         const uint32_t lane_base = static_cast<uint32_t>(q4 * 32) << 16;
         const int tid = threadIdx.x - 128 * (1 + w);  // 0..127 within the warpgroup
         // [buffer][warpgroup][L*log2e | D][64 query rows]
         float* ldbuf = reinterpret_cast<float*>(sgen + L::kOffLD);
         const float sl = p.scale_log2;
         // thread tid stages L (tid < 64) or D (tid >= 64) of query row 64w + tid % 64
-        // of iteration `it` of unit x (rows past Nq: P = 0)
-        auto fetch = [&](const KvUnit& x, int it) {
-            const int hh = x.g * p.G + it / x.per_head;
-            const int row = (x.i0 + it % x.per_head) * kT + 64 * w + (tid & 63);
-            float v = tid < 64 ? INFINITY : 0.f;
-            if (row < p.Nq && in_bounds(((long long)x.b * p.Hq + hh) * p.Nq + row, 1,
+        // of head hh (rows past Nq: P = 0)
+        auto fetch = [&](int it) {
+            const int hh = it_head(it), row = it_tile(it) * kT + 64 * w + (tid & 63);
+            float x = tid < 64 ? INFINITY : 0.f;
+            if (row < p.Nq && in_bounds(((long long)b * p.Hq + hh) * p.Nq + row, 1,
                                         (long long)p.B * p.Hq * p.Nq, &g_bwd_status)) {
-                const long long o = ((long long)x.b * p.Hq + hh) * p.Nq + row;
+                const long long o = ((long long)b * p.Hq + hh) * p.Nq + row;
                 if (tid < 64) {
                     const float l = p.lse[o];
-                    v = l == -INFINITY ? INFINITY : l * kLog2e;
+                    x = l == -INFINITY ? INFINITY : l * kLog2e;
                 } else {
-                    v = p.dvec[o];
+                    x = p.dvec[o];
                 }
             }
-            return v;
+            return x;
         };
-        // the next unit after the k-th that has iterations (n = 0 when there is none)
-        auto next_active = [&](int k) {
-            KvUnit y{};
-            for (int kk = k + 1;; ++kk) {
-                const int u = kv_unit_index(kk, p);
-                if (u < 0) break;
-                y = kv_unit_at(u, p);
-                if (y.n > 0) return y;
-            }
-            y.n = 0;
-            return y;
-        };
+        float nx = fetch(0);
         bool ok = true;
-        int gi = 0;  // iterations processed (barrier phases, L/D buffer)
-        int ua = 0;  // units whose accumulators were read
-        bool have_nx = false;
-        float nx = 0.f;
-        // Every thread of the warpgroup runs every iteration of every unit, also
-        // after a bounded wait has given up (the abort flag then ends the
-        // remaining waits at once): the named barrier below must never miss a thread.
-        for (int k = 0;; ++k) {
-            const int u = kv_unit_index(k, p);
-            if (u < 0) break;
-            const KvUnit x = kv_unit_at(u, p);
-            const int key = x.c0 + r;
-            if (x.n == 0) {  // no query row sees these keys: dK = dV = 0 (this thread's half row)
-                if (key < p.Nk) {
-                    const long long off = (((long long)x.b * p.Nk + key) * p.Hkv + x.g) * D + w * (D / 2);
-                    if (in_bounds(off, D / 2, (long long)p.B * p.Nk * p.Hkv * D, &g_bwd_status)) {
+        // Every thread of the warpgroup runs every iteration, also after a
+        // bounded wait has given up (the abort flag then ends the remaining
+        // waits at once): the named barrier below must never miss a thread.
+        for (int it = 0; it < n; ++it) {
+            const int buf = it & 1;
+            float* lrow = ldbuf + ((buf * 2 + w) * 2 + 0) * 64;
+            float* drow = ldbuf + ((buf * 2 + w) * 2 + 1) * 64;
+            (tid < 64 ? lrow : drow)[tid & 63] = nx;
+            named_bar_sync(1 + w, 128);  // this iteration's L and D are visible to the warpgroup
+            if (it + 1 < n) nx = fetch(it + 1);  // in flight while this tile is processed
+            if (ok) ok = mbar_wait(bar(L::kBarS), it & 1, abort_flag, &g_bwd_status);
+            if (!ok) continue;
+            tc_fence_after();
+            const int rq = it_tile(it) * kT;
+            // causal: query row i may see this key iff key <= i + (Nk - Nq)
+            const bool need_mask = key >= p.Nk || (p.causal && (long long)c0 + kT - 1 > (long long)rq + (p.Nk - p.Nq));
+            uint32_t s[64], dp[64];
+            tmem_ld64_sync(tmem + lane_base + kS + 64 * w, s);
+            tmem_ld64_sync(tmem + lane_base + kDP + 64 * w, dp);
+            tc_fence_before();
+            mbar_arrive(bar(L::kBarC));  // the S^T columns may be overwritten now
+            if (need_mask) {
+                // the query rows that may see this key: tile columns [lo, kT)
+                const long long first = key >= p.Nk ? (long long)kT
+                                                     : (p.causal ? (long long)key - (p.Nk - p.Nq) - rq : 0ll);
+                const int lo = first < 0 ? 0 : first > kT ? kT : (int)first;
 #pragma unroll
-                        for (int c = 0; c < D / 16; ++c) {
-                            reinterpret_cast<uint4*>(p.dk + off)[c] = make_uint4(0u, 0u, 0u, 0u);
-                            reinterpret_cast<uint4*>(p.dv + off)[c] = make_uint4(0u, 0u, 0u, 0u);
-                        }
-                    }
-                }
-                continue;
+                for (int cc = 0; cc < 64; ++cc)
+                    if (64 * w + cc < lo) s[cc] = __float_as_uint(-INFINITY);
             }
-            if (!have_nx) nx = fetch(x, 0);  // (later units: prefetched during the previous one)
-            const KvUnit xn = next_active(k);
-            for (int it = 0; it < x.n; ++it, ++gi) {
-                const int buf = gi & 1;
-                float* lrow = ldbuf + ((buf * 2 + w) * 2 + 0) * 64;
-                float* drow = ldbuf + ((buf * 2 + w) * 2 + 1) * 64;
-                (tid < 64 ? lrow : drow)[tid & 63] = nx;
-                named_bar_sync(1 + w, 128);  // this iteration's L and D are visible to the warpgroup
-                // the next iteration's L and D in flight while this tile is processed
-                have_nx = it + 1 < x.n || xn.n > 0;
-                if (it + 1 < x.n)
-                    nx = fetch(x, it + 1);
-                else if (xn.n > 0)
-                    nx = fetch(xn, 0);
-                if (ok) ok = mbar_wait(bar(L::kBarS), gi & 1, abort_flag, &g_bwd_status);
-                if (!ok) continue;
-                tc_fence_after();
-                const int rq = (x.i0 + it % x.per_head) * kT;
-                // causal: query row i may see this key iff key <= i + (Nk - Nq)
-                const bool need_mask =
-                    key >= p.Nk || (p.causal && (long long)x.c0 + kT - 1 > (long long)rq + (p.Nk - p.Nq));
-                uint32_t s[64], dp[64];
-                tmem_ld64_sync(tmem + lane_base + kS + 64 * w, s);
-                tmem_ld64_sync(tmem + lane_base + kDP + 64 * w, dp);
-                tc_fence_before();
-                mbar_arrive(bar(L::kBarC));  // the S^T columns may be overwritten now
-                if (need_mask) {
-                    // the query rows that may see this key: tile columns [lo, kT)
-                    const long long first = key >= p.Nk ? (long long)kT
-                                                         : (p.causal ? (long long)key - (p.Nk - p.Nq) - rq : 0ll);
-                    const int lo = first < 0 ? 0 : first > kT ? kT : (int)first;
+            uint32_t pk[32], dk[32];
 #pragma unroll
-                    for (int cc = 0; cc < 64; ++cc)
-                        if (64 * w + cc < lo) s[cc] = __float_as_uint(-INFINITY);
+            for (int c = 0; c < 32; ++c) {
+                float pv[2], dsv[2];
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int cc = 2 * c + e;  // query row rq + 64w + cc
+                    pv[e] = ex2(fmaf(__uint_as_float(s[cc]), sl, -lrow[cc]));
+                    dsv[e] = pv[e] * (__uint_as_float(dp[cc]) - drow[cc]);
                 }
-                uint32_t pk[32], dk[32];
-#pragma unroll
-                for (int c = 0; c < 32; ++c) {
-                    float pv[2], dsv[2];
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int cc = 2 * c + e;  // query row rq + 64w + cc
-                        pv[e] = ex2(fmaf(__uint_as_float(s[cc]), sl, -lrow[cc]));
-                        dsv[e] = pv[e] * (__uint_as_float(dp[cc]) - drow[cc]);
-                    }
-                    pk[c] = pack_bf16(pv[0], pv[1]);
-                    dk[c] = pack_bf16(dsv[0], dsv[1]);
-                }
-                // each warpgroup writes only dP^T columns it has read itself
-                tmem_st32(tmem + lane_base + kDP + 64 * w, pk);       // P^T
-                tmem_st32(tmem + lane_base + kDP + 64 * w + 32, dk);  // dS^T
-                tmem_st_wait();
-                tc_fence_before();
-                mbar_arrive(bar(L::kBarDS));
+                pk[c] = pack_bf16(pv[0], pv[1]);
+                dk[c] = pack_bf16(dsv[0], dsv[1]);
             }
-            // epilogue: dV and dK of this warpgroup's half of the columns into
-            // registers, the accumulators released, then the stores
-            if (ok && mbar_wait(bar(L::kBarAcc), ua & 1, abort_flag, &g_bwd_status)) {
-                tc_fence_after();
-                uint32_t xv[D / 2], xk[D / 2];
+            // each warpgroup writes only dP^T columns it has read itself
+            tmem_st32(tmem + lane_base + kDP + 64 * w, pk);       // P^T
+            tmem_st32(tmem + lane_base + kDP + 64 * w + 32, dk);  // dS^T
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(bar(L::kBarDS));
+        }
+        if (ok && mbar_wait(bar(L::kBarAcc), 0, abort_flag, &g_bwd_status)) {
+            tc_fence_after();
+            // warpgroup w writes columns [w D/2, (w + 1) D/2) of dV and dK
+            const long long off = (((long long)b * p.Nk + key) * p.Hkv + g) * D + w * (D / 2);
+            const bool out_ok =
+                key >= p.Nk || in_bounds(off, D / 2, (long long)p.B * p.Nk * p.Hkv * D, &g_bwd_status);
+            uint32_t xo[32];
 #pragma unroll
-                for (int h = 0; h < D / 64; ++h) {
-                    tmem_ld32_sync(tmem + lane_base + kDV + w * (D / 2) + 32 * h, xv + 32 * h);
-                    tmem_ld32_sync(tmem + lane_base + kDK + w * (D / 2) + 32 * h, xk + 32 * h);
-                }
-                tc_fence_before();
-                mbar_arrive(bar(L::kBarAccE));  // the next unit's dV, dK may overwrite them
-                const long long off = (((long long)x.b * p.Nk + key) * p.Hkv + x.g) * D + w * (D / 2);
-                if (key < p.Nk && in_bounds(off, D / 2, (long long)p.B * p.Nk * p.Hkv * D, &g_bwd_status)) {
+            for (int h = 0; h < D / 64; ++h) {
+                tmem_ld32_sync(tmem + lane_base + kDV + w * (D / 2) + 32 * h, xo);
+                if (key < p.Nk && out_ok) {
 #pragma unroll
-                    for (int c = 0; c < D / 16; ++c) {
+                    for (int c = 0; c < 4; ++c) {
                         uint4 v;
-                        v.x = pack_bf16(__uint_as_float(xv[8 * c + 0]), __uint_as_float(xv[8 * c + 1]));
-                        v.y = pack_bf16(__uint_as_float(xv[8 * c + 2]), __uint_as_float(xv[8 * c + 3]));
-                        v.z = pack_bf16(__uint_as_float(xv[8 * c + 4]), __uint_as_float(xv[8 * c + 5]));
-                        v.w = pack_bf16(__uint_as_float(xv[8 * c + 6]), __uint_as_float(xv[8 * c + 7]));
-                        reinterpret_cast<uint4*>(p.dv + off)[c] = v;
-                        v.x = pack_bf16(__uint_as_float(xk[8 * c + 0]) * p.scale, __uint_as_float(xk[8 * c + 1]) * p.scale);
-                        v.y = pack_bf16(__uint_as_float(xk[8 * c + 2]) * p.scale, __uint_as_float(xk[8 * c + 3]) * p.scale);
-                        v.z = pack_bf16(__uint_as_float(xk[8 * c + 4]) * p.scale, __uint_as_float(xk[8 * c + 5]) * p.scale);
-                        v.w = pack_bf16(__uint_as_float(xk[8 * c + 6]) * p.scale, __uint_as_float(xk[8 * c + 7]) * p.scale);
-                        reinterpret_cast<uint4*>(p.dk + off)[c] = v;
+                        v.x = pack_bf16(__uint_as_float(xo[8 * c + 0]), __uint_as_float(xo[8 * c + 1]));
+                        v.y = pack_bf16(__uint_as_float(xo[8 * c + 2]), __uint_as_float(xo[8 * c + 3]));
+                        v.z = pack_bf16(__uint_as_float(xo[8 * c + 4]), __uint_as_float(xo[8 * c + 5]));
+                        v.w = pack_bf16(__uint_as_float(xo[8 * c + 6]), __uint_as_float(xo[8 * c + 7]));
+                        reinterpret_cast<uint4*>(p.dv + off + 32 * h)[c] = v;
                     }
                 }
-            } else {
-                ok = false;
+                tmem_ld32_sync(tmem + lane_base + kDK + w * (D / 2) + 32 * h, xo);
+                if (key < p.Nk && out_ok) {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        uint4 v;
+                        v.x = pack_bf16(__uint_as_float(xo[8 * c + 0]) * p.scale, __uint_as_float(xo[8 * c + 1]) * p.scale);
+                        v.y = pack_bf16(__uint_as_float(xo[8 * c + 2]) * p.scale, __uint_as_float(xo[8 * c + 3]) * p.scale);
+                        v.z = pack_bf16(__uint_as_float(xo[8 * c + 4]) * p.scale, __uint_as_float(xo[8 * c + 5]) * p.scale);
+                        v.w = pack_bf16(__uint_as_float(xo[8 * c + 6]) * p.scale, __uint_as_float(xo[8 * c + 7]) * p.scale);
+                        reinterpret_cast<uint4*>(p.dk + off + 32 * h)[c] = v;
+                    }
+                }
             }
-            ++ua;
         }
     }
 
@@ -864,13 +784,9 @@ attn_status_t launch_bwd_impl(const void* q, const void* k, const void* v, const
     const long long dot_rows_per_block = (long long)(kDotThreads / (D / 8)) * kDotRows;
     const long long dot_blocks = (rows + dot_rows_per_block - 1) / dot_rows_per_block;
     const long long dq_blocks = (long long)B * Hq * ((Nq + kT - 1) / kT);
-    const long long dkv_units = (long long)B * Hkv * ((Nk + kT - 1) / kT);
-    if (dot_blocks > 0x7fffffffLL || dq_blocks > 0x7fffffffLL || dkv_units > 0x7fffffffLL)
+    const long long dkv_blocks = (long long)B * Hkv * ((Nk + kT - 1) / kT);
+    if (dot_blocks > 0x7fffffffLL || dq_blocks > 0x7fffffffLL || dkv_blocks > 0x7fffffffLL)
         return ATTN_ERR_UNSUPPORTED;
-    prm.num_kv_units = (int)dkv_units;
-    const int sms = attn_host::device_sm_count();
-    if (sms <= 0) return ATTN_ERR_CUDA;
-    const long long dkv_blocks = dkv_units < sms ? dkv_units : sms;  // persistent
     bwd_dot_kernel<D><<<(unsigned)dot_blocks, kDotThreads, 0, stream>>>(static_cast<const __nv_bfloat16*>(o),
                                                                prm.do_, dvec, B, Nq, Hq);
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
