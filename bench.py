@@ -85,8 +85,8 @@ NOMINAL_HBM_GBS = 8000.0  # the ~8 TB/s HBM3e figure the decode target is quoted
 NCU_TRAFFIC = {
     "long_sequence": {"bytes_per_launch": 350.80e6 + 101.38e6, "src": "fwd_tc.cu",
                       "src_hash": "f289683a689bd204"},
-    "decode_b16_8k": {"bytes_per_launch": 537.04e6 + 3.35e6, "src": "decode.cu",
-                      "src_hash": "b1a4a625e04ba019"},
+    "decode_b16_8k": {"bytes_per_launch": 537.03e6 + 3.31e6, "src": "decode.cu",
+                      "src_hash": "6895569f4a77a618"},
 }
 
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
