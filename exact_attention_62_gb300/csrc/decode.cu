@@ -673,9 +673,11 @@ namespace attn_host {
 // split_model_best below.
 // Contiguous cache: fitted on GB300 to the measured best segment counts of
 // B = 1 x 2K-64K, B = 4 x 4K and 16K, B = 8 x 8K, B = 16 x 8K and B = 32 x 2K
-// keys (Hq = 32, Hkv = 8, d = 128); a CTA streams ~80-110 GB/s while few
-// compete, so batches of several sequences need few segments or none.
-constexpr SplitModel kDenseSplitModel = {8.0e10, 5.5e12, 0.5e-6, 4.0e-6};
+// keys (Hq = 32, Hkv = 8, d = 128), timed with L2 holding only clean lines;
+// a CTA streams ~80-110 GB/s while few compete and the grid as a whole
+// ~7-7.7 TB/s once the ring is full, so one long sequence wants ~12 segments
+// and batches of several sequences few or none.
+constexpr SplitModel kDenseSplitModel = {8.0e10, 7.5e12, 0.5e-6, 4.0e-6};
 
 // Modelled time (seconds) of S segments when every segment has `units` CTAs
 // and `slots` CTAs fit on the GPU at once: waves of CTAs, each streaming its

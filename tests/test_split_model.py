@@ -71,12 +71,16 @@ def test_model_terms(L):
     assert L.attn_decode_model_best(1, 0, 8192, 128, 60e9, 6e12, 0.0, 0.0, 0) == -1
 
 
-@pytest.mark.parametrize("B,Nk,want", [(1, 65536, 9), (4, 16384, 3), (8, 8192, 1), (16, 8192, 1),
+@pytest.mark.parametrize("B,Nk,want", [(1, 2048, 12), (1, 8192, 12), (1, 16384, 12), (1, 65536, 12),
+                                       (4, 4096, 3), (4, 16384, 3), (8, 8192, 2), (16, 8192, 1),
                                        (32, 2048, 1)])
 def test_gb300_fit_picks_the_measured_counts(L, B, Nk, want):
-    """The contiguous-cache constants (80 GB/s per CTA, 5.5 TB/s, 0.5 us per
+    """The contiguous-cache constants (80 GB/s per CTA, 7.5 TB/s, 0.5 us per
     wave, 4 us merge) on 152 SMs, one CTA per SM, Hq = 32, Hkv = 8 (four
-    query heads per CTA): the counts that measured best or within 2% of it
-    on GB300 (B = 1 x 64K: 9; B = 4 x 16K: 3; one segment from B = 8 x 8K up)."""
+    query heads per CTA): counts that measured best or within 2% of it on
+    GB300 with L2 flushed clean (µs, 22 calls each: B = 1 x 64K 45.9 at 12,
+    45.7 at 16, 47.5 at 9; B = 1 x 8K 14.6 at 12, 15.0 at 9; B = 1 x 2K
+    10.6 at 12, 10.4 at 9; B = 4 x 16K 46.0 at 3, 45.9 at 4, 57.5 at 5;
+    B = 8 x 8K 46.0 at 2, 45.7 at 1; B = 16 x 8K 79.5 at 1, 83.3 at 2)."""
     units = B * 8
-    assert L.attn_decode_model_best(units, 152, Nk, 128, 8.0e10, 5.5e12, 0.5e-6, 4.0e-6, 0) == want
+    assert L.attn_decode_model_best(units, 152, Nk, 128, 8.0e10, 7.5e12, 0.5e-6, 4.0e-6, 0) == want
