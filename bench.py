@@ -487,7 +487,7 @@ def run_ours(args):
         e_pre, e_dec = [], []
         # the forward through attn_fwd_host: chunks copied in, computed and
         # copied back on three streams, the transfers overlapping the computation
-        # (the default chunking: eight row chunks for one sequence)
+        # (the default chunking: sixteen row chunks for one sequence)
         up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
         for s in range(max(3, min(K, 10)) + 1):
             flush_l2()

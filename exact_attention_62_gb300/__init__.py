@@ -258,8 +258,9 @@ def attn_fwd(q, k, v, causal: bool = False, scale: float | None = None, o=None, 
 def attn_fwd_host(q, k, v, causal: bool = False, scale: float | None = None, o=None, lse=None,
                   device_buffers=None, chunks: int = 0, stream=None, h2d_stream=None, d2h_stream=None):
     """attn_fwd on CPU tensors (page-locked for asynchronous copies): the batch
-    is copied in, computed and copied back in chunks on three streams so the
-    transfers overlap the computation.  Returns (o, lse) CPU tensors (pinned
+    is copied in, computed and copied back in chunks (the chunks' forwards on
+    `stream` and a second compute stream by turns) so the transfers overlap
+    the computation.  Returns (o, lse) CPU tensors (pinned
     when allocated here); they hold the results once `stream` (default: the
     current stream) has completed.  device_buffers = (q_d, k_d, v_d, o_d,
     lse_d) reuses device memory across calls; h2d_stream / d2h_stream default

@@ -2,10 +2,11 @@
 // with the computation (the C entry point attn_fwd_host).
 //
 // The batch is cut into chunks of whole sequences.  Chunk c's inputs go
-// host -> device on the h2d stream, its forward runs on the compute stream
-// once they have arrived, and its outputs go device -> host on the d2h
-// stream once the forward is done; so the copy of chunk c + 1 and the read
-// back of chunk c - 1 proceed while chunk c computes.  Sequences are
+// host -> device on the h2d stream, its forward runs once they have arrived
+// (even chunks on the caller's compute stream, odd ones on a second compute
+// stream), and its outputs go device -> host on the d2h stream once the
+// forward is done; so the copy of chunk c + 1 and the read back of chunk
+// c - 1 proceed while chunk c computes.  Sequences are
 // independent in the forward, so every output element is the one a single
 // attn_fwd call over the whole batch writes, bit for bit.
 //
@@ -62,6 +63,29 @@ struct EventPool {
 };
 thread_local EventPool t_events;
 
+// The second compute stream: consecutive chunks' forwards run on the caller's
+// stream and on this one by turns, so the next chunk's CTAs take the SMs
+// that the current chunk's last wave of work units leaves idle (eight row
+// chunks of one 16K-key sequence: 1.67 ms back to back on one stream, 1.56
+// on two; sixteen: 1.82 and 1.52).  Created once per host thread and
+// device, like the events; its work is ordered by events only.
+struct SideStream {
+    cudaStream_t s = nullptr;
+    int device = -1;
+    bool get(int dev) {
+        if (s != nullptr && device == dev) return true;
+        if (s != nullptr) cudaStreamDestroy(s);
+        s = nullptr;
+        if (cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking) != cudaSuccess) {
+            s = nullptr;
+            return false;
+        }
+        device = dev;
+        return true;
+    }
+};
+thread_local SideStream t_side;
+
 bool misaligned16(const void* p) { return (reinterpret_cast<unsigned long long>(p) & 15ull) != 0; }
 
 }  // namespace
@@ -90,18 +114,35 @@ extern "C" attn_status_t attn_fwd_host(const void* q_h, const void* k_h, const v
     // One bf16 sequence: chunks of query rows (see the top of this file).
     const bool by_rows = B == 1 && dtype == ATTN_BF16 && Nk > 0 && (!causal || Nq <= Nk);
     const int row_units = (Nq + kRowUnit - 1) / kRowUnit;
-    // Default: 8 row chunks for one sequence (B = 1, N = 16384 causal: 2.10 ms
-    // end to end against 2.23 with 4 and 2.43 with 2 on GB300), else min(B, 4).
-    int n = chunks == 0 ? (by_rows ? 8 : (B < 4 ? B : 4)) : chunks;
+    // Default: 16 row chunks for one sequence (B = 1, N = 16384 causal on
+    // GB300, end to end: 1.93 ms against 2.04 with 8, 2.07 with 20, 2.19 with
+    // 32 and 2.22 with 4), else min(B, 4).
+    int n = chunks == 0 ? (by_rows ? 16 : (B < 4 ? B : 4)) : chunks;
     if (n > kMaxChunks) return ATTN_ERR_UNSUPPORTED;
     if (n > (by_rows ? row_units : B)) n = by_rows ? row_units : B;
 
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || !t_events.get(dev)) return ATTN_ERR_CUDA;
+    if (n > 1 && !t_side.get(dev)) return ATTN_ERR_CUDA;
     cudaEvent_t* ev = t_events.ev;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaStream_t up = h2d_stream ? static_cast<cudaStream_t>(h2d_stream) : st;
     cudaStream_t down = d2h_stream ? static_cast<cudaStream_t>(d2h_stream) : st;
+    // compute stream of chunk c
+    auto cstream = [&](int c) { return (c & 1) ? t_side.s : st; };
+    // chunk c's forward starts once its inputs are in (ev_in recorded on up)
+    auto wait_inputs = [&](int c) -> bool {
+        cudaStream_t cs = cstream(c);
+        if (up == cs) return true;
+        return cudaEventRecord(ev[2 * c], up) == cudaSuccess && cudaStreamWaitEvent(cs, ev[2 * c], 0) == cudaSuccess;
+    };
+    // chunk c's read-back starts once its forward is done
+    auto release_outputs = [&](int c) -> bool {
+        cudaStream_t cs = cstream(c);
+        if (down == cs) return true;
+        return cudaEventRecord(ev[2 * c + 1], cs) == cudaSuccess &&
+               cudaStreamWaitEvent(down, ev[2 * c + 1], 0) == cudaSuccess;
+    };
 
     const size_t esz = dtype == ATTN_BF16 ? 2 : 4;
     const size_t q_seq = (size_t)Nq * Hq * d * esz;    // bytes of one sequence's q (and o)
@@ -123,6 +164,7 @@ extern "C" attn_status_t attn_fwd_host(const void* q_h, const void* k_h, const v
     if (cudaEventRecord(ev_start, st) != cudaSuccess) return ATTN_ERR_CUDA;
     if (up != st && cudaStreamWaitEvent(up, ev_start, 0) != cudaSuccess) return ATTN_ERR_CUDA;
     if (down != st && cudaStreamWaitEvent(down, ev_start, 0) != cudaSuccess) return ATTN_ERR_CUDA;
+    if (n > 1 && cudaStreamWaitEvent(t_side.s, ev_start, 0) != cudaSuccess) return ATTN_ERR_CUDA;
 
     if (by_rows) {
         const size_t q_row = (size_t)Hq * d * esz;    // bytes of one query row (all heads)
@@ -142,20 +184,13 @@ extern "C" attn_status_t attn_fwd_host(const void* q_h, const void* k_h, const v
                     return ATTN_ERR_CUDA;
                 k_done = k_end;
             }
-            cudaEvent_t ev_in = ev[2 * c], ev_out = ev[2 * c + 1];
-            if (up != st) {
-                if (cudaEventRecord(ev_in, up) != cudaSuccess || cudaStreamWaitEvent(st, ev_in, 0) != cudaSuccess)
-                    return ATTN_ERR_CUDA;
-            }
+            if (!wait_inputs(c)) return ATTN_ERR_CUDA;
             const attn_status_t s = attn_host::launch_fwd_tc(qd + r0 * q_row, kd, vd, od + r0 * q_row,
                                                              reinterpret_cast<float*>(ld) + r0, 1, Hq, Hkv,
-                                                             r1 - r0, (int)k_end, d, causal, scale, st,
-                                                             nullptr, Nq);
+                                                             r1 - r0, (int)k_end, d, causal, scale,
+                                                             cstream(c), nullptr, Nq);
             if (s != ATTN_OK) return s;
-            if (down != st) {
-                if (cudaEventRecord(ev_out, st) != cudaSuccess || cudaStreamWaitEvent(down, ev_out, 0) != cudaSuccess)
-                    return ATTN_ERR_CUDA;
-            }
+            if (!release_outputs(c)) return ATTN_ERR_CUDA;
             if (cudaMemcpyAsync(oh + r0 * q_row, od + r0 * q_row, (size_t)(r1 - r0) * q_row,
                                 cudaMemcpyDeviceToHost, down) != cudaSuccess ||
                 cudaMemcpy2DAsync(lh + (size_t)r0 * sizeof(float), (size_t)Nq * sizeof(float),
@@ -178,20 +213,13 @@ extern "C" attn_status_t attn_fwd_host(const void* q_h, const void* k_h, const v
                     cudaSuccess)
                 return ATTN_ERR_CUDA;
         }
-        cudaEvent_t ev_in = ev[2 * c], ev_out = ev[2 * c + 1];
-        if (up != st) {
-            if (cudaEventRecord(ev_in, up) != cudaSuccess || cudaStreamWaitEvent(st, ev_in, 0) != cudaSuccess)
-                return ATTN_ERR_CUDA;
-        }
+        if (!wait_inputs(c)) return ATTN_ERR_CUDA;
         const attn_status_t s = attn_fwd(qd + b0 * q_seq, Nk > 0 ? kd + b0 * kv_seq : nullptr,
                                          Nk > 0 ? vd + b0 * kv_seq : nullptr, od + b0 * q_seq,
                                          reinterpret_cast<float*>(ld + b0 * l_seq), nb, Hq, Hkv, Nq, Nk, d,
-                                         causal, scale, dtype, st);
+                                         causal, scale, dtype, cstream(c));
         if (s != ATTN_OK) return s;
-        if (down != st) {
-            if (cudaEventRecord(ev_out, st) != cudaSuccess || cudaStreamWaitEvent(down, ev_out, 0) != cudaSuccess)
-                return ATTN_ERR_CUDA;
-        }
+        if (!release_outputs(c)) return ATTN_ERR_CUDA;
         if (cudaMemcpyAsync(oh + b0 * q_seq, od + b0 * q_seq, nb * q_seq, cudaMemcpyDeviceToHost, down) !=
                 cudaSuccess ||
             cudaMemcpyAsync(lh + b0 * l_seq, ld + b0 * l_seq, nb * l_seq, cudaMemcpyDeviceToHost, down) !=

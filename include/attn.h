@@ -91,7 +91,7 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o,
  *   q_d, k_d, v_d, o_d, lse_d  device buffers of the same full sizes,
  *            caller-owned, aligned as for attn_fwd.
  *   chunks   the number of chunks n, 1..16; 0 = min(B, 4) for a batch and
- *            8 for one sequence.  With B > 1 (or fp32 inputs, or a causal
+ *            16 for one sequence.  With B > 1 (or fp32 inputs, or a causal
  *            Nq > Nk) chunk c holds sequences [B c / n, B (c + 1) / n),
  *            n <= B.  With one bf16 sequence chunk c holds the query rows
  *            [256 floor(U c / n), 256 floor(U (c + 1) / n)) (U = ceil(Nq /
@@ -101,15 +101,18 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o,
  *            row + (Nk - Nq) with the causal mask.
  *   stream   the compute stream; h2d_stream and d2h_stream carry the two
  *            copy directions (NULL: the compute stream, i.e. no overlap).
- * Chunk c is copied host -> device on h2d_stream, computed on `stream` once
- * it has arrived, and copied back on d2h_stream once computed, so chunk c + 1
- * moves in while chunk c computes.  The side
+ * Chunk c is copied host -> device on h2d_stream, computed once it has
+ * arrived, and copied back on d2h_stream once computed, so chunk c + 1 moves
+ * in while chunk c computes.  Even chunks compute on `stream`, odd chunks on
+ * a second compute stream of the library's, so that one chunk's forward can
+ * start on the SMs the previous one's last wave leaves idle.  The other
  * streams first wait for the work already queued on `stream`, and `stream`
  * finally waits for the last read back: once `stream` has completed, o_h and
  * lse_h hold the results, equal bit for bit to one attn_fwd call over the
  * whole batch.  Errors as attn_fwd, checked before anything is queued (a
  * CUDA failure later returns ATTN_ERR_CUDA with part of the work queued).
- * The library keeps a few CUDA events per host thread for this call.
+ * The library keeps a few CUDA events and one non-blocking stream per host
+ * thread and device for this call.
  */
 attn_status_t attn_fwd_host(const void* q_h, const void* k_h, const void* v_h,
                             void* o_h, float* lse_h, void* q_d, void* k_d,
