@@ -57,8 +57,11 @@ def test_concurrent_streams_and_threads_match_serial(attn):
     jobs = _jobs(attn)
     serial = {}
     for name, fn in jobs:
-        serial[name] = [t.clone() for t in fn()]
-    torch.cuda.synchronize()
+        outs = fn()
+        # attn_fwd_host returns CPU tensors that its read-back copies fill
+        # asynchronously: the results exist once the device is done
+        torch.cuda.synchronize()
+        serial[name] = [t.clone() for t in outs]
     assert attn.attn_check_device_status() == 0
 
     results, errors = {}, []
