@@ -197,6 +197,22 @@ def _stream(stream, device=None):
     return ctypes.c_void_p(s.cuda_stream)
 
 
+def _used_on(stream, *tensors):
+    """The call's kernels use these device tensors on `stream`.  When that is
+    not the current stream (the one torch's caching allocator associates
+    with tensors allocated here), record the use, so that memory freed by
+    the caller, or by this module on return, is not handed out again before
+    the stream's work is done."""
+    if stream is None:
+        return
+    import torch
+    if stream == torch.cuda.current_stream(stream.device):
+        return
+    for t in tensors:
+        if t is not None and t.is_cuda:
+            t.record_stream(stream)
+
+
 def _need_cuda_contig(name, t, device=None):
     if not t.is_cuda:
         raise ValueError("%s must be a CUDA tensor" % name)
@@ -252,6 +268,7 @@ def attn_fwd(q, k, v, causal: bool = False, scale: float | None = None, o=None, 
         st = lib().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Nq, Nk, d,
                             int(bool(causal)), float(scale), _dtype_code(q), _stream(stream, dev))
     _check("attn_fwd", st)
+    _used_on(stream, q, k, v, o, lse)
     return o, lse
 
 
@@ -306,6 +323,7 @@ def attn_fwd_host(q, k, v, causal: bool = False, scale: float | None = None, o=N
                                  int(bool(causal)), float(scale), _dtype_code(q), int(chunks),
                                  _stream(stream, dev), _stream(h2d_stream, dev), _stream(d2h_stream, dev))
     _check("attn_fwd_host", st)
+    _used_on(stream, *device_buffers)
     return o, lse
 
 
@@ -360,6 +378,7 @@ def attn_decode_splitkv(q, k_cache, v_cache, scale: float | None = None, num_spl
                                        B, Hq, Hkv, Nk, d, float(scale), int(num_splits),
                                        _ptr(workspace), wsize, _dtype_code(q), _stream(stream, dev))
     _check("attn_decode_splitkv", st)
+    _used_on(stream, q, k_cache, v_cache, workspace, o, lse)
     return o, lse
 
 
@@ -398,6 +417,7 @@ def attn_decode_splitkv_static(q, k_cache, v_cache, scale: float | None = None,
                                               _ptr(lse), B, Hq, Hkv, Nk, d, float(scale),
                                               int(num_splits), _dtype_code(q), _stream(stream, dev))
     _check("attn_decode_splitkv_static", st)
+    _used_on(stream, q, k_cache, v_cache, o, lse)
     return o, lse
 
 
@@ -424,6 +444,7 @@ def attn_merge_lse(o_parts, lse_parts, out_dtype=None, o=None, lse=None, stream=
         st = lib().attn_merge_lse(_ptr(o_parts), _ptr(lse_parts), P, rows, d, _ptr(o), _ptr(lse),
                                   _dtype_code(o), _stream(stream, dev))
     _check("attn_merge_lse", st)
+    _used_on(stream, o_parts, lse_parts, o, lse)
     return o, lse
 
 
@@ -504,6 +525,7 @@ def attn_decode_paged(q, k_pages, v_pages, block_table, seq_lens, max_seq_len: i
                                      int(num_splits), _ptr(workspace), wsize, _dtype_code(q),
                                      _stream(stream, dev))
     _check("attn_decode_paged", st)
+    _used_on(stream, q, k_pages, v_pages, block_table, seq_lens, workspace, o, lse)
     return o, lse
 
 
@@ -548,6 +570,7 @@ def attn_bwd(q, k, v, o, lse, dout, causal: bool, scale: float | None = None, dq
                             _ptr(dk), _ptr(dv), B, Hq, Hkv, Nq, Nk, d, int(bool(causal)),
                             float(scale), _ptr(workspace), wsize, _dtype_code(q), _stream(stream, dev))
     _check("attn_bwd", st)
+    _used_on(stream, q, k, v, o, lse, dout, dq, dk, dv, workspace)
     return dq, dk, dv
 
 
@@ -569,6 +592,7 @@ def attn_quantize_fp8(x, codes=None, scales=None, stream=None):
     with torch.cuda.device(dev):
         st = lib().attn_quantize_fp8(_ptr(x), _ptr(codes), _ptr(scales), B, N, H, d, _stream(stream, dev))
     _check("attn_quantize_fp8", st)
+    _used_on(stream, x, codes, scales)
     return codes, scales
 
 
@@ -595,6 +619,7 @@ def attn_quantize_fp8_rotated(x, signs, codes=None, scales=None, stream=None):
         st = lib().attn_quantize_fp8_rotated(_ptr(x), _ptr(signs), _ptr(codes), _ptr(scales), B, N, H, d,
                                              _stream(stream, dev))
     _check("attn_quantize_fp8_rotated", st)
+    _used_on(stream, x, signs, codes, scales)
     return codes, scales
 
 
@@ -625,6 +650,7 @@ def attn_fwd_fp8(q8, k8, v, q_scales, k_scales, causal: bool, scale: float | Non
                                 _ptr(lse), B, Hq, Hkv, Nq, Nk, d, int(bool(causal)), float(scale),
                                 _stream(stream, dev))
     _check("attn_fwd_fp8", st)
+    _used_on(stream, q8, k8, v, q_scales, k_scales, o, lse)
     return o, lse
 
 
@@ -653,6 +679,7 @@ def attn_quantize_fp8_v(v, vt8=None, scales=None, stream=None):
     with torch.cuda.device(dev):
         st = lib().attn_quantize_fp8_v(_ptr(v), _ptr(vt8), _ptr(scales), B, N, H, d, _stream(stream, dev))
     _check("attn_quantize_fp8_v", st)
+    _used_on(stream, v, vt8, scales)
     return vt8, scales
 
 
@@ -685,6 +712,7 @@ def attn_fwd_fp8_pv(q8, k8, vt8, q_scales, k_scales, v_scales, causal: bool, sca
                                    _ptr(v_scales), _ptr(o), _ptr(lse), B, Hq, Hkv, Nq, Nk, d,
                                    int(bool(causal)), float(scale), _stream(stream, dev))
     _check("attn_fwd_fp8_pv", st)
+    _used_on(stream, q8, k8, vt8, q_scales, k_scales, v_scales, o, lse)
     return o, lse
 
 
@@ -714,6 +742,7 @@ def attn_fwd_test(q, k, v, causal: bool, scale: float, options: AttnTestOptions,
                                  d, int(bool(causal)), float(scale), ctypes.byref(options),
                                  _stream(stream, dev))
     _check("attn_fwd_test", st)
+    _used_on(stream, q, k, v, o, lse)
     return o, lse
 
 
@@ -745,4 +774,5 @@ def attn_decode_test(q, k_cache, v_cache, scale: float, num_splits: int, options
                                     Hkv, Nk, d, float(scale), int(num_splits), _ptr(workspace), wsize,
                                     ctypes.byref(options), _stream(stream, dev))
     _check("attn_decode_test", st)
+    _used_on(stream, q, k_cache, v_cache, workspace, o, lse)
     return o, lse

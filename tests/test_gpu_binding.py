@@ -151,3 +151,32 @@ def test_fp8_pv_buffers(attn):
     o, lse = attn.attn_fwd_fp8_pv(q8, k8, vt8, qs, ks, vs, True)
     torch.cuda.synchronize()
     assert torch.isfinite(lse).all() and attn.attn_check_device_status() == 0
+
+
+def test_buffers_used_on_another_stream_are_recorded(attn):
+    """A call on a stream other than the current one records its device
+    tensors on that stream: a workspace the caller frees right after the
+    call is not handed out again by torch's caching allocator while the
+    stream (held back by a sleep queued on it) has not yet run the kernels
+    that use it.  Without the record the same block comes straight back."""
+    B, Hq, Hkv, Nk, d = 1, 8, 2, 4096, 128
+    q, k, v = _bf((B, 1, Hq, d), 4), _bf((B, Nk, Hkv, d), 5), _bf((B, Nk, Hkv, d), 6)
+    S = 8
+    nbytes = attn.attn_decode_workspace_bytes(B, Hq, Hkv, Nk, d, S)
+    ref_o, ref_l = attn.attn_decode_splitkv(q, k, v, 0.088, S)
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        torch.cuda._sleep(50_000_000)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=DEV)
+    ptr = ws.data_ptr()
+    o, lse = attn.attn_decode_splitkv(q, k, v, 0.088, S, workspace=ws, stream=side)
+    del ws
+    again = torch.empty(nbytes, dtype=torch.uint8, device=DEV)
+    assert again.data_ptr() != ptr
+    again.fill_(0xFF)                     # NaN patterns, had the block been reused
+    side.synchronize()
+    assert torch.equal(o, ref_o) and torch.equal(lse, ref_l)
+    torch.cuda.synchronize()
+    assert attn.attn_check_device_status() == 0

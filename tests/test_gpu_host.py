@@ -96,3 +96,23 @@ def test_fwd_host_orders_after_queued_work(attn):
     torch.cuda.synchronize()
     ro, rl = _device_reference(attn, q, k, v, True, 1.0 / math.sqrt(d))
     assert torch.equal(o, ro) and torch.equal(lse, rl)
+
+
+@pytest.mark.parametrize("slow", ["h2d", "d2h"])
+def test_fwd_host_done_when_its_stream_is(attn, slow):
+    """The results are in the host buffers once the caller's compute stream
+    has completed, with nothing else synchronised: the chunks' forwards on
+    the library's second compute stream and the read-back copies are all
+    ordered before that stream's end.  One copy stream is held back by a
+    kernel queued on it before the call, so the pipeline finishes late."""
+    Hq, Hkv, N, d = 8, 2, 2048, 128
+    scale = 1.0 / math.sqrt(d)
+    q, k, v = (t.pin_memory() for t in make_qkv(1, Hq, Hkv, N, N, d, 46))
+    st, up, down = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    ro, rl = _device_reference(attn, q, k, v, True, scale)
+    with torch.cuda.stream(up if slow == "h2d" else down):
+        torch.cuda._sleep(20_000_000)
+    o, lse = attn.attn_fwd_host(q, k, v, True, scale, chunks=8, stream=st, h2d_stream=up, d2h_stream=down)
+    st.synchronize()
+    assert torch.equal(o, ro) and torch.equal(lse, rl)
+    torch.cuda.synchronize()
