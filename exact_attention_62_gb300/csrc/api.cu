@@ -84,6 +84,21 @@ bool encode_vt_map(CUtensorMap* map, const void* base, int B, int H, int d, long
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool encode_page_heads_map(CUtensorMap* map, const void* pages, int num_pages, int page_size, int H, int d) {
+    EncodeTiledFn fn = encode_fn();
+    if (fn == nullptr) return false;
+    // The pool is [pages][page_size][H][d]; the map lists its dimensions as
+    // (d, key, head, page), so a box of a whole page lands in shared memory
+    // head by head, each head's keys in consecutive 128-byte rows.
+    cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)page_size, (cuuint64_t)H, (cuuint64_t)num_pages};
+    cuuint64_t strides[3] = {(cuuint64_t)H * d * 2, (cuuint64_t)d * 2, (cuuint64_t)page_size * H * d * 2};
+    cuuint32_t box[4] = {64u, (cuuint32_t)page_size, (cuuint32_t)H, 1u};
+    cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(pages), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int device_sm_count() {
     static PerDevice<int> cache;
     int dev = -1;

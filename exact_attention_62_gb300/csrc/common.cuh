@@ -61,6 +61,10 @@ inline long long fp8_v_ld(int N) { return ((long long)N + 15) / 16 * 16; }
 // (keys innermost), with a box of (box_keys keys, all d rows, 1 head, 1
 // batch) and 128-byte swizzle: a K-major operand tile of d rows.
 bool encode_vt_map(CUtensorMap* map, const void* base, int B, int H, int d, long long ld, int box_keys);
+// Paged K or V pool [pages][page_size][H][d] (bf16) as whole-page boxes of
+// all H heads: 64 columns x page_size keys x H heads, 128-byte swizzle, rows
+// ordered head by head.
+bool encode_page_heads_map(CUtensorMap* map, const void* pages, int num_pages, int page_size, int H, int d);
 
 // Number of SMs of the current device (cached per device); 0 on failure.
 int device_sm_count();

@@ -29,7 +29,10 @@
 //    (the same (m, l, acc) merge).  With a single segment the kernel writes
 //    O (bf16) and LSE directly and no merge kernel runs; otherwise the merge
 //    kernel is launched as a programmatic dependent (one pass over the
-//    partials for up to 4 segments per thread, two passes beyond).
+//    partials for up to 16 segments per thread, two passes beyond).
+//  * Paged caches with pages of 16 keys and 8 KV heads take a second kernel,
+//    decode_heads_kernel, in which one CTA reads whole pages for all KV
+//    heads (its own comment below says why).
 #include <algorithm>
 #include <cmath>
 #include <mutex>
@@ -432,6 +435,290 @@ __global__ void __launch_bounds__(kDecThreads)
     }
 }
 
+// ------------------------------------------------------------- pages of 16 keys
+// A paged cache with pages of 16 keys holds, in each page, the rows of all KV
+// heads side by side (16 keys x Hkv heads x D).  decode_split_kernel, one CTA
+// per KV head, reads such a page as 16 rows of D bf16 spread Hkv * D * 2
+// bytes apart: one small TMA box per page, head and panel.  A read-only probe
+// of that pattern on GB300 (64K keys, pages in random order) streamed 3960
+// GB/s with 96 CTAs, against 6320 GB/s when each CTA loaded whole pages of
+// all 8 heads.  So for Hkv = 8 this kernel takes a segment of pages for all
+// KV heads in one CTA.  A page arrives as one box per K/V panel (16 KB at d =
+// 128); consumer warp w works on KV head w's 16 keys of the page with the
+// same two warp-MMA products as decode_split_kernel (S^T = K Q^T with the
+// G <= 8 query heads of the KV head as columns, then O^T += V^T P^T).  The
+// tensor maps list the pool's dimensions as (d, key, head, page), so a
+// head's 16 keys are consecutive 128-byte rows of the stage and the 128-byte
+// swizzle keeps every ldmatrix conflict-free.  Each warp owns its head's
+// online-softmax state, so there is no cross-warp merge: every warp writes its
+// head's partial (or, with one segment, its final O and LSE) itself.
+constexpr int kHeadsWarps = 8;  // KV heads per CTA, one consumer warp each
+constexpr int kHeadsThreads = 32 * (1 + kHeadsWarps);
+constexpr int kSmallPage = 16;  // keys per page on this path
+// CTAs (segments x sequences) the automatic segment count aims at: about
+// 27/32 of the SMs.  On GB300 (152 SMs) 128 CTAs measured best at every batch
+// tried with pages of 16 keys (B = 1 x 16K and 64K keys, 4 x 16K, 8 x 8K,
+// 16 x 8K): one wave, and at B = 1 still few enough partials per row for the
+// one-pass merge.
+inline int heads_target_ctas(int sms) { return sms * 27 / 32; }
+
+template <int D>
+struct HeadsLayout {
+    static constexpr int kPanels = D / 64;
+    static constexpr int kPanelBytes = kSmallPage * kHeadsWarps * 128;  // 16 keys x 8 heads x 128 B
+    static constexpr int kStageBytes = 2 * kPanels * kPanelBytes;       // K panels, then V panels
+    static constexpr int kStages = D == 128 ? 3 : 6;                    // 192 KB in flight
+    static constexpr int kOffBar = kStages * kStageBytes;               // full[kStages], empty[kStages]
+    static constexpr int kOffMisc = kOffBar + 2 * kStages * 8;
+    static constexpr int kSmemBytes = kOffMisc + 16 + 1024;
+    static_assert(kSmemBytes <= 232448, "shared memory budget");
+    static_assert(kPanelBytes % 1024 == 0, "swizzle atoms start on 1024-byte boundaries");
+};
+
+template <int D>
+__global__ void __launch_bounds__(kHeadsThreads)
+    decode_heads_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                        const DecParams p) {
+    using L = HeadsLayout<D>;
+    constexpr int STAGES = L::kStages;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t sbase = (raw + 1023u) & ~1023u;
+    uint8_t* sgen = smem_raw + (sbase - raw);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    auto full_bar = [&](int st) -> uint32_t { return sbase + L::kOffBar + 8u * st; };
+    auto empty_bar = [&](int st) -> uint32_t { return sbase + L::kOffBar + 8u * (STAGES + st); };
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(sgen + L::kOffMisc);
+
+    const int seg = blockIdx.x;
+    const int b = blockIdx.z;
+    int len = 0;  // this sequence's keys, clamped to [0, Nk] (Nk: the caller's maximum)
+    if (in_bounds(b, 1, p.B, &g_dec_status)) len = min(max(p.seq_lens[b], 0), p.Nk);
+    const long long R = (long long)p.B * p.Hq;
+    const long long o_extent = R * D - p.o_slack;
+    const long long parts_rows = (long long)p.splits * R;
+    const int j0 = seg * p.seg_len;  // seg_len is a multiple of the page size
+    const int j1 = min(j0 + p.seg_len, len);
+    const int npages = j1 > j0 ? (j1 - j0 + kSmallPage - 1) / kSmallPage : 0;
+
+    if (npages == 0) {  // empty segment: o_s = 0, lse_s = -inf for every query head
+        for (int e = threadIdx.x; e < p.Hq * D; e += blockDim.x) {
+            const long long row = (long long)b * p.Hq + e / D;
+            if (p.splits == 1) {  // a sequence with no keys at all
+                if (in_bounds(row * D + (e % D), 1, o_extent, &g_dec_status))
+                    p.o[row * D + (e % D)] = __float2bfloat16_rn(0.f);
+                if (e % D == 0 && in_bounds(row, 1, R, &g_dec_status)) p.lse[row] = -INFINITY;
+            } else {
+                const long long po = ((long long)seg * R + row) * D + (e % D);
+                if (in_bounds(po, 1, parts_rows * D, &g_dec_status)) p.o_parts[po] = 0.f;
+                if (e % D == 0 && in_bounds((long long)seg * R + row, 1, parts_rows, &g_dec_status))
+                    p.lse_parts[(long long)seg * R + row] = -INFINITY;
+            }
+        }
+        return;
+    }
+
+    if (threadIdx.x == 0) {
+        for (int st = 0; st < STAGES; ++st) {
+            mbar_init(full_bar(st), 1);
+            mbar_init(empty_bar(st), kHeadsWarps);  // every consumer warp reads every page
+        }
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    if (warp == 0) {
+        // ================================================= TMA producer
+        // The whole warp runs the loop: the lanes fetch the block-table
+        // entries of 32 pages at a time, lane 0 issues the loads.
+        if (lane == 0) {
+            prefetch_tmap(&tmK);
+            prefetch_tmap(&tmV);
+        }
+        const long long tab0 = (long long)b * p.max_pages + j0 / kSmallPage;
+        int page_of_lane = 0;
+        for (int t = 0; t < npages; ++t) {
+            if ((t & 31) == 0) {
+                const int i = t + lane;
+                page_of_lane = (i < npages && in_bounds(tab0 + i, 1, (long long)p.B * p.max_pages, &g_dec_status))
+                                   ? p.table[tab0 + i]
+                                   : 0;
+            }
+            const int page = __shfl_sync(0xffffffffu, page_of_lane, t & 31);
+            const int st = t % STAGES;
+            if (!mbar_wait_warp(empty_bar(st), ((t / STAGES) & 1) ^ 1, abort_flag, &g_dec_status, p.wait_limit))
+                break;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(full_bar(st), L::kStageBytes);
+                const uint32_t dst = sbase + st * L::kStageBytes;
+#pragma unroll
+                for (int pp = 0; pp < L::kPanels; ++pp) {
+                    tma_load_4d(dst + pp * L::kPanelBytes, &tmK, full_bar(st), 64 * pp, 0, 0, page);
+                    tma_load_4d(dst + (L::kPanels + pp) * L::kPanelBytes, &tmV, full_bar(st), 64 * pp, 0, 0, page);
+                }
+            }
+            __syncwarp();
+        }
+        return;  // the producer takes no part in the consumers' work
+    }
+
+    // ===================================================== consumers
+    const int w = warp - 1;     // KV head of this warp (Hkv = kHeadsWarps)
+    const int G = p.G;          // its query heads, 1..8: the MMA columns
+    const int hq0 = w * G;
+    const int g8 = lane >> 2;   // fragment row group
+    const int t4 = lane & 3;    // fragment column pair
+    const int mi = lane >> 3;   // ldmatrix: which 8x8 matrix this lane addresses
+    const int rr = lane & 7;    // ldmatrix: which row of it
+
+    // Q^T of the head's query heads as the B operand of S^T = K Q^T
+    uint32_t qb[D / 16][2];
+    {
+        const long long qoff = ((long long)b * p.Hq + hq0 + (g8 < G ? g8 : 0)) * D;
+        const bool qv = g8 < G && in_bounds(qoff, D, R * D, &g_dec_status);
+        const __nv_bfloat16* qrow = p.q + qoff;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+            qb[kk][0] = qv ? ld_b32(qrow + kk * 16 + 2 * t4) : 0u;
+            qb[kk][1] = qv ? ld_b32(qrow + kk * 16 + 8 + 2 * t4) : 0u;
+        }
+    }
+    float acc[D / 16][4];
+#pragma unroll
+    for (int mb = 0; mb < D / 16; ++mb) acc[mb][0] = acc[mb][1] = acc[mb][2] = acc[mb][3] = 0.f;
+    float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.f, l_b = 0.f;  // columns 2 t4 and 2 t4 + 1
+    const float sl = p.scale_log2;
+    const int krow = w * kSmallPage + rr + 8 * (mi & 1);   // K row (of the stage) this lane addresses
+    const int vrow = w * kSmallPage + rr + 8 * (mi >> 1);  // V row this lane addresses
+
+    for (int t = 0; t < npages; ++t) {
+        const int st = t % STAGES;
+        if (!mbar_wait(full_bar(st), (t / STAGES) & 1, abort_flag, &g_dec_status, p.wait_limit)) break;
+        const uint32_t kb = sbase + st * L::kStageBytes;
+        const uint32_t vb = kb + L::kPanels * L::kPanelBytes;
+        const int key0 = j0 + t * kSmallPage;
+        // Keys of the last page past the sequence: their pool slots hold
+        // whatever is there (P is 0 for them, but 0 * NaN is not), so the
+        // warp zeroes its head's V rows there (K needs nothing: masked
+        // scores are replaced, not multiplied).
+        const bool zeroed = key0 + kSmallPage > j1;
+        if (zeroed) {
+            for (int e = lane; e < kSmallPage * (D / 8); e += 32) {
+                const int r = e / (D / 8), ch = e % (D / 8);
+                const int row = w * kSmallPage + r;
+                if (key0 + r >= j1)
+                    st_shared_v4(vb + (ch >> 3) * L::kPanelBytes + row * 128 + (((ch & 7) ^ (row & 7)) << 4),
+                                 0u, 0u, 0u, 0u);
+            }
+            __syncwarp();
+        }
+
+        // S^T (16 keys x 8 query columns) = K (16 x D) Q^T (D x 8); even and
+        // odd k-steps accumulate separately to halve the dependent MMA chain.
+        float ce[4] = {0.f, 0.f, 0.f, 0.f}, co[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+            const int ch = 2 * kk + (mi >> 1);
+            const uint32_t addr = kb + (ch >> 3) * L::kPanelBytes + krow * 128 + (((ch & 7) ^ (krow & 7)) << 4);
+            uint32_t a[4];
+            ldsm_x4(addr, a);
+            if (kk & 1)
+                mma_16816(co, a, qb[kk][0], qb[kk][1]);
+            else
+                mma_16816(ce, a, qb[kk][0], qb[kk][1]);
+        }
+        const float c[4] = {ce[0] + co[0], ce[1] + co[1], ce[2] + co[2], ce[3] + co[3]};
+        const int key = key0 + g8;  // keys of this lane: rows g8 and g8 + 8 of the page
+        const bool in0 = key < j1, in1 = key + 8 < j1;
+        const float x0 = in0 ? c[0] * sl : -INFINITY;  // (key,   col 2t4)
+        const float x1 = in0 ? c[1] * sl : -INFINITY;  // (key,   col 2t4+1)
+        const float x2 = in1 ? c[2] * sl : -INFINITY;  // (key+8, col 2t4)
+        const float x3 = in1 ? c[3] * sl : -INFINITY;  // (key+8, col 2t4+1)
+        float mxa = fmaxf(x0, x2), mxb = fmaxf(x1, x3);
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+            mxa = fmaxf(mxa, __shfl_xor_sync(0xffffffffu, mxa, off));
+            mxb = fmaxf(mxb, __shfl_xor_sync(0xffffffffu, mxb, off));
+        }
+        const float mna = fmaxf(m_a, mxa), mnb = fmaxf(m_b, mxb);
+        const float mua = mna == -INFINITY ? 0.f : mna;
+        const float mub = mnb == -INFINITY ? 0.f : mnb;
+        const float aa = ex2(m_a - mua), ab = ex2(m_b - mub);
+        const float p0 = ex2(x0 - mua), p2 = ex2(x2 - mua);
+        const float p1 = ex2(x1 - mub), p3 = ex2(x3 - mub);
+        l_a = fmaf(l_a, aa, p0 + p2);
+        l_b = fmaf(l_b, ab, p1 + p3);
+        m_a = mna;
+        m_b = mnb;
+#pragma unroll
+        for (int mb = 0; mb < D / 16; ++mb) {
+            acc[mb][0] *= aa;
+            acc[mb][1] *= ab;
+            acc[mb][2] *= aa;
+            acc[mb][3] *= ab;
+        }
+        // P^T as the B operand (keys x query columns), then
+        // O^T (D x 8) += V^T (D x 16 keys) P^T (16 keys x 8)
+        const uint32_t b01 = movmatrix_trans(pack_bf16(p0, p1));
+        const uint32_t b23 = movmatrix_trans(pack_bf16(p2, p3));
+#pragma unroll
+        for (int mb = 0; mb < D / 16; ++mb) {
+            const int ch = 2 * mb + (mi & 1);
+            const uint32_t addr = vb + (ch >> 3) * L::kPanelBytes + vrow * 128 + (((ch & 7) ^ (vrow & 7)) << 4);
+            uint32_t a[4];
+            ldsm_x4_trans(addr, a);
+            mma_16816(acc[mb], a, b01, b23);
+        }
+        if (zeroed) fence_proxy_async_smem();  // the zeroing stores before the stage's next TMA write
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty_bar(st));
+    }
+
+    // The merge kernel (launched as a programmatic dependent) may start now;
+    // it waits for this grid's completion before reading any partial.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // l over the warp's 16 key rows; m is already the same in those lanes
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+        l_a += __shfl_xor_sync(0xffffffffu, l_a, off);
+        l_b += __shfl_xor_sync(0xffffffffu, l_b, off);
+    }
+    // This head's result for query columns 2 t4 and 2 t4 + 1: O = acc / l
+    // (acc[mb][c] holds d = 16 mb + g8, acc[mb][2 + c] d + 8), LSE = m + ln l.
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+        const int qc = 2 * t4 + c;
+        if (qc >= G) continue;
+        const float l = c ? l_b : l_a, m = c ? m_b : m_a;
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        const float lsev = l > 0.f ? (m + lg2(l)) * kLn2 : -INFINITY;
+        const long long row = (long long)b * p.Hq + hq0 + qc;
+#pragma unroll
+        for (int mb = 0; mb < D / 16; ++mb) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int dd = mb * 16 + g8 + 8 * h;
+                const float v = acc[mb][2 * h + c] * inv;
+                if (p.splits == 1) {
+                    if (in_bounds(row * D + dd, 1, o_extent, &g_dec_status)) p.o[row * D + dd] = __float2bfloat16_rn(v);
+                } else {
+                    const long long po = ((long long)seg * R + row) * D + dd;
+                    if (in_bounds(po, 1, parts_rows * D, &g_dec_status)) p.o_parts[po] = v;
+                }
+            }
+        }
+        if (g8 == 0) {
+            if (p.splits == 1) {
+                if (in_bounds(row, 1, R, &g_dec_status)) p.lse[row] = lsev;
+            } else if (in_bounds((long long)seg * R + row, 1, parts_rows, &g_dec_status)) {
+                p.lse_parts[(long long)seg * R + row] = lsev;
+            }
+        }
+    }
+}
+
 // lse = M + log sum_s exp(lse_s - M), o = sum_s exp(lse_s - lse) o_s, one CTA
 // per row.  The merge sits between two HBM-bound launches and moves a few
 // hundred KB, so its cost is round trips, not bytes: every load of a pass is
@@ -534,14 +821,15 @@ __global__ void __launch_bounds__(kMergeThreads)
     if (tid == 0 && lse != nullptr && in_bounds(row, 1, rows, &g_dec_status)) lse[row] = Lr;
 }
 
-// The same merge in one pass for few segments (at most kShortSeg per
-// thread): every thread issues the loads of its segments' LSE and partial
+// The same merge in one pass for few segments (at most NSEG per thread:
+// kShortSeg, or kShortSegWide for up to 128 segments at d = 128): every thread issues the loads of its segments' LSE and partial
 // outputs at once, so the merge costs one round trip to L2 instead of two;
 // o = sum_s e^{lse_s - M} o_s / sum_s e^{lse_s - M} and lse = M + ln of that
 // sum (M = max_s lse_s), the same value as merge_lse_kernel up to rounding.
-constexpr int kShortSeg = 4;
+constexpr int kShortSeg = 4;   // segments per thread of the one-pass merge (P <= 32 at d = 128)
+constexpr int kShortSegWide = 16;  // the same for P <= 128 at d = 128 (many-segment paged decodes)
 
-template <bool OUT_BF16>
+template <bool OUT_BF16, int NSEG>
 __global__ void __launch_bounds__(kMergeThreads)
     merge_lse_short_kernel(const float* __restrict__ o_parts, const float* __restrict__ lse_parts, int P,
                            long long rows, int d, void* __restrict__ o, float* __restrict__ lse,
@@ -554,11 +842,11 @@ __global__ void __launch_bounds__(kMergeThreads)
     const int C = d >> 2;              // 4-column groups, 1..128
     const int SL = kMergeThreads / C;  // segment lanes, >= 2
     const int c4 = tid % C, sl = tid / C;
-    float ls[kShortSeg];
-    float4 x[kShortSeg];
+    float ls[NSEG];
+    float4 x[NSEG];
     float M = -INFINITY;
 #pragma unroll
-    for (int r = 0; r < kShortSeg; ++r) {
+    for (int r = 0; r < NSEG; ++r) {
         const int s = sl + r * SL;
         const long long lo = (long long)s * rows + row, oo = lo * d + 4 * c4;
         const bool ok = sl < SL && s < P && in_bounds(lo, 1, (long long)P * rows, &g_dec_status) &&
@@ -572,7 +860,7 @@ __global__ void __launch_bounds__(kMergeThreads)
     float lsum = 0.f;
     if (M != -INFINITY) {  // uniform across the CTA
 #pragma unroll
-        for (int r = 0; r < kShortSeg; ++r) {
+        for (int r = 0; r < NSEG; ++r) {
             if (ls[r] == -INFINITY) continue;
             const float w = expf(ls[r] - M);
             a.x = fmaf(w, x[r].x, a.x);
@@ -608,6 +896,23 @@ __global__ void __launch_bounds__(kMergeThreads)
     }
     if (tid == 0 && lse != nullptr && in_bounds(row, 1, rows, &g_dec_status))
         lse[row] = lsum > 0.f ? M + logf(lsum) : -INFINITY;
+}
+
+// decode_heads_kernel serves pages of 16 keys with 8 KV heads of at most 8
+// query heads each; every other paged cache takes decode_split_kernel.
+bool heads_path(int Hq, int Hkv, int page_size, int d) {
+    return page_size == kSmallPage && Hkv == kHeadsWarps && Hq % Hkv == 0 && Hq / Hkv <= 8 &&
+           (d == 64 || d == 128);
+}
+
+template <int D>
+attn_status_t launch_heads(const CUtensorMap& mk, const CUtensorMap& mv, const DecParams& prm,
+                           cudaStream_t stream) {
+    using L = HeadsLayout<D>;
+    if (attn_host::kernel_setup<decode_heads_kernel<D>>(L::kSmemBytes).err != cudaSuccess) return ATTN_ERR_CUDA;
+    dim3 grid(prm.splits, 1, prm.B);
+    decode_heads_kernel<D><<<grid, kHeadsThreads, L::kSmemBytes, stream>>>(mk, mv, prm);
+    return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
 int group_cols(int G) {
@@ -801,6 +1106,14 @@ int decode_paged_auto_splits(int B, int Hq, int Hkv, int max_seq_len, int d, int
     // to keep HBM busy; but a second
     // wave of such CTAs costs more than it gains (B = 16 x 8K keys: one
     // segment per sequence beats eight), so they are kept to one wave.
+    if (heads_path(Hq, Hkv, page_size, d)) {
+        // One CTA per (segment, sequence) for all KV heads, one CTA per SM,
+        // each segment whole 64-key tiles.
+        const int sms = device_sm_count();
+        if (sms <= 0) return -1;
+        const int max_s = std::max(1, (max_seq_len + kTileKeys - 1) / kTileKeys);
+        return std::max(1, std::min(max_s, heads_target_ctas(sms) / std::max(1, B)));
+    }
     const bool small = page_size < 64;
     const double cta_bw = !small ? 6.0e10 : page_size >= 32 ? 5.2e10 : 3.3e10;
     int S = auto_splits_model(B, Hq, Hkv, max_seq_len, d, SplitModel{cta_bw, 6.5e12, 1.5e-6, 3.0e-6}, small);
@@ -814,10 +1127,13 @@ attn_status_t launch_decode_paged(const void* q, const void* k_pages, const void
                                   int B, int Hq, int Hkv, int d, int num_pages, int page_size,
                                   int max_pages, int max_seq_len, float scale, int splits,
                                   void* workspace, cudaStream_t stream) {
+    const bool heads = heads_path(Hq, Hkv, page_size, d);
     const int box = page_size < kTileKeys ? page_size : kTileKeys;
     CUtensorMap mk, mv;
-    if (!encode_bshd_map(&mk, k_pages, num_pages, page_size, Hkv, d, box, 2) ||
-        !encode_bshd_map(&mv, v_pages, num_pages, page_size, Hkv, d, box, 2))
+    if (heads ? (!encode_page_heads_map(&mk, k_pages, num_pages, page_size, Hkv, d) ||
+                 !encode_page_heads_map(&mv, v_pages, num_pages, page_size, Hkv, d))
+              : (!encode_bshd_map(&mk, k_pages, num_pages, page_size, Hkv, d, box, 2) ||
+                 !encode_bshd_map(&mv, v_pages, num_pages, page_size, Hkv, d, box, 2)))
         return ATTN_ERR_CUDA;
     DecParams prm;
     prm.q = static_cast<const __nv_bfloat16*>(q);
@@ -848,7 +1164,9 @@ attn_status_t launch_decode_paged(const void* q, const void* k_pages, const void
         prm.o_parts = nullptr;
         prm.lse_parts = nullptr;
     }
-    const attn_status_t st = launch_split_any<true>(d, mk, mv, prm, stream);
+    const attn_status_t st = heads ? (d == 128 ? launch_heads<128>(mk, mv, prm, stream)
+                                               : launch_heads<64>(mk, mv, prm, stream))
+                                   : launch_split_any<true>(d, mk, mv, prm, stream);
     if (st != ATTN_OK || splits == 1) return st;
     return launch_merge(prm.o_parts, prm.lse_parts, splits, (long long)rows, d, o, lse, true, stream);
 }
@@ -872,12 +1190,18 @@ attn_status_t launch_merge(const float* o_parts, const float* lse_parts, int par
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    const bool short_merge = parts <= kShortSeg * (kMergeThreads / (d / 4));
+    const int seg_lanes = kMergeThreads / (d / 4);
     cudaError_t e;
-    if (short_merge)
-        e = out_bf16 ? cudaLaunchKernelEx(&cfg, merge_lse_short_kernel<true>, o_parts, lse_parts, parts, rows, d, o, lse, o_slack)
-                     : cudaLaunchKernelEx(&cfg, merge_lse_short_kernel<false>, o_parts, lse_parts, parts, rows, d, o,
-                                          lse, o_slack);
+    if (parts <= kShortSeg * seg_lanes)
+        e = out_bf16 ? cudaLaunchKernelEx(&cfg, merge_lse_short_kernel<true, kShortSeg>, o_parts, lse_parts, parts,
+                                          rows, d, o, lse, o_slack)
+                     : cudaLaunchKernelEx(&cfg, merge_lse_short_kernel<false, kShortSeg>, o_parts, lse_parts, parts,
+                                          rows, d, o, lse, o_slack);
+    else if (parts <= kShortSegWide * seg_lanes)
+        e = out_bf16 ? cudaLaunchKernelEx(&cfg, merge_lse_short_kernel<true, kShortSegWide>, o_parts, lse_parts,
+                                          parts, rows, d, o, lse, o_slack)
+                     : cudaLaunchKernelEx(&cfg, merge_lse_short_kernel<false, kShortSegWide>, o_parts, lse_parts,
+                                          parts, rows, d, o, lse, o_slack);
     else
         e = out_bf16 ? cudaLaunchKernelEx(&cfg, merge_lse_kernel<true>, o_parts, lse_parts, parts, rows, d, o, lse, o_slack)
                      : cudaLaunchKernelEx(&cfg, merge_lse_kernel<false>, o_parts, lse_parts, parts, rows, d, o, lse, o_slack);

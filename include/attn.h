@@ -256,7 +256,12 @@ attn_status_t attn_decode_paged(const void* q, const void* k_pages, const void* 
 
 /*
  * attn_decode_paged_num_splits -- the segment count attn_decode_paged uses
- * with num_splits = 0: attn_decode_num_splits(B, Hq, Hkv, max_seq_len, d),
+ * with num_splits = 0.  With pages of 16 keys and Hkv = 8 (at most 8 query
+ * heads per KV head) one CTA takes every KV head of a segment, and the count
+ * aims at 27/32 of the SMs in CTAs (segments x sequences: 128 on GB300), at
+ * most one segment per 64 keys of max_seq_len.  Otherwise it is the
+ * CTA-by-wave time model of attn_decode_num_splits with per-CTA rates that
+ * depend on the page size (one wave of CTAs for pages under 64 keys),
  * raised until one segment's pages fit the block-table staging area.
  * Returns -1 on invalid sizes.
  */

@@ -69,10 +69,10 @@ def test_decode_unchanged(attn, bounds_lib, B, Hq, Hkv, Nk, d, S):
     _both(attn, bounds_lib, lambda: attn.attn_decode_splitkv(q, k, v, 1.0 / math.sqrt(d), S))
 
 
-@pytest.mark.parametrize("ps,S", [(16, 0), (64, 3)])
-def test_paged_decode_unchanged(attn, bounds_lib, ps, S):
+@pytest.mark.parametrize("ps,S,Hq,Hkv", [(16, 0, 8, 2), (64, 3, 8, 2), (16, 5, 32, 8)])
+def test_paged_decode_unchanged(attn, bounds_lib, ps, S, Hq, Hkv):
     lens = [700, 1, 2049]
-    q, kp, vp, table, sl = (x.to(DEV) for x in make_paged(3, 8, 2, 128, ps, lens, seed=ps + S))
+    q, kp, vp, table, sl = (x.to(DEV) for x in make_paged(3, Hq, Hkv, 128, ps, lens, seed=ps + S))
     _both(attn, bounds_lib, lambda: attn.attn_decode_paged(q, kp, vp, table, sl, max(lens), 0.088,
                                                            num_splits=S))
 

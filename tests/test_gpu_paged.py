@@ -4,7 +4,9 @@ Block tables are random permutations of a pool with unowned pages; every
 slot no sequence owns is NaN (it must not reach the output).  Cases cover
 page sizes 16, 32, 64 and 256, lengths on both sides of page and tile
 boundaries, empty sequences (with one and with several segments), GQA
-ratios 1, 4 and 8, d = 64 and 128, and fixed and automatic segment counts."""
+ratios 1, 3, 4 and 8, d = 64 and 128, and fixed and automatic segment counts;
+with pages of 16 keys and 8 KV heads, the kernel that takes every KV head of
+a segment in one CTA."""
 import math
 
 import numpy as np
@@ -26,6 +28,12 @@ CASES = [
     (2, 8, 2, 128, 64, [0, 100], 1, None),
     (3, 8, 2, 64, 16, [63, 64, 65], 2, 400),          # segments past every sequence
     (2, 16, 2, 128, 32, [2047, 1], 7, None),
+    # pages of 16 keys with 8 KV heads: one CTA takes all KV heads of a segment
+    (4, 32, 8, 128, 16, [1, 15, 16, 17], 0, None),
+    (3, 24, 8, 64, 16, [0, 33, 700], 3, None),         # 3 query heads per KV head, an empty sequence
+    (2, 64, 8, 128, 16, [1000, 2048], 1, None),        # 8 per KV head; one segment writes O itself
+    (2, 8, 8, 128, 16, [63, 65], 4, 400),              # 1 per KV head; segments past every sequence
+    (1, 32, 8, 128, 16, [5000], 0, None),              # the automatic count: one wave of CTAs
 ]
 
 
