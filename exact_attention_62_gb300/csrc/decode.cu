@@ -30,7 +30,7 @@
 //    O (bf16) and LSE directly and no merge kernel runs; otherwise the merge
 //    kernel is launched as a programmatic dependent (one pass over the
 //    partials for up to 16 segments per thread, two passes beyond).
-//  * Paged caches with pages of 16 keys and 8 KV heads take a second kernel,
+//  * Paged caches with pages of 16 keys and 2, 4 or 8 KV heads take a second kernel,
 //    decode_heads_kernel, in which one CTA reads whole pages for all KV
 //    heads (its own comment below says why).
 #include <algorithm>
@@ -442,17 +442,19 @@ __global__ void __launch_bounds__(kDecThreads)
 // bytes apart: one small TMA box per page, head and panel.  A read-only probe
 // of that pattern on GB300 (64K keys, pages in random order) streamed 3960
 // GB/s with 96 CTAs, against 6320 GB/s when each CTA loaded whole pages of
-// all 8 heads.  So for Hkv = 8 this kernel takes a segment of pages for all
-// KV heads in one CTA.  A page arrives as one box per K/V panel (16 KB at d =
-// 128); consumer warp w works on KV head w's 16 keys of the page with the
-// same two warp-MMA products as decode_split_kernel (S^T = K Q^T with the
-// G <= 8 query heads of the KV head as columns, then O^T += V^T P^T).  The
-// tensor maps list the pool's dimensions as (d, key, head, page), so a
-// head's 16 keys are consecutive 128-byte rows of the stage and the 128-byte
-// swizzle keeps every ldmatrix conflict-free.  Each warp owns its head's
-// online-softmax state, so there is no cross-warp merge: every warp writes its
-// head's partial (or, with one segment, its final O and LSE) itself.
-constexpr int kHeadsWarps = 8;  // KV heads per CTA, one consumer warp each
+// all 8 heads.  So for Hkv = 2, 4 or 8 this kernel takes a segment of pages
+// for all KV heads in one CTA.  A page arrives as one box per K/V panel
+// (16 keys x Hkv heads x 64 columns), and a stage holds 8 / Hkv pages; each
+// of the eight consumer warps takes one (KV head, page) pair of the stage
+// and works on that head's 16 keys with the same two warp-MMA products as
+// decode_split_kernel (S^T = K Q^T with the G <= 8 query heads of the KV
+// head as columns, then O^T += V^T P^T).  The tensor maps list the pool's
+// dimensions as (d, key, head, page), so a head's 16 keys are consecutive
+// 128-byte rows of the page and the 128-byte swizzle keeps every ldmatrix
+// conflict-free.  At the end the warps of one head (8 / Hkv of them) merge
+// their online-softmax states through shared memory, and one warp per head
+// writes the head's partial (or, with one segment, its O and LSE).
+constexpr int kHeadsWarps = 8;  // consumer warps: one (KV head, page slot) pair each
 constexpr int kHeadsThreads = 32 * (1 + kHeadsWarps);
 constexpr int kSmallPage = 16;  // keys per page on this path
 // CTAs (segments x sequences) the automatic segment count aims at: about
@@ -462,25 +464,33 @@ constexpr int kSmallPage = 16;  // keys per page on this path
 // one-pass merge.
 inline int heads_target_ctas(int sms) { return sms * 27 / 32; }
 
-template <int D>
+template <int D, int NH>  // NH = Hkv: 8, 4 or 2
 struct HeadsLayout {
+    static constexpr int kSlots = kHeadsWarps / NH;                // pages per stage
     static constexpr int kPanels = D / 64;
-    static constexpr int kPanelBytes = kSmallPage * kHeadsWarps * 128;  // 16 keys x 8 heads x 128 B
-    static constexpr int kStageBytes = 2 * kPanels * kPanelBytes;       // K panels, then V panels
-    static constexpr int kStages = D == 128 ? 3 : 6;                    // 192 KB in flight
-    static constexpr int kOffBar = kStages * kStageBytes;               // full[kStages], empty[kStages]
+    static constexpr int kPanelBytes = kSmallPage * NH * 128;      // a page's panel: 16 keys x NH heads x 128 B
+    static constexpr int kPageBytes = 2 * kPanels * kPanelBytes;   // K panels, then V panels
+    static constexpr int kStageBytes = kSlots * kPageBytes;        // 32 KB per 64 columns of d
+    static constexpr int kStages = D == 128 ? 3 : 6;               // 192 KB in flight
+    static constexpr int kOffBar = kStages * kStageBytes;          // full[kStages], empty[kStages]
     static constexpr int kOffMisc = kOffBar + 2 * kStages * 8;
     static constexpr int kSmemBytes = kOffMisc + 16 + 1024;
+    // the heads' cross-warp merge: [warp][lane][acc (D/16 x 4), m_a, m_b, l_a, l_b]
+    // floats, over the stage buffers once every page has been consumed
+    static constexpr int kRedFloats = D / 16 * 4 + 4;
     static_assert(kSmemBytes <= 232448, "shared memory budget");
     static_assert(kPanelBytes % 1024 == 0, "swizzle atoms start on 1024-byte boundaries");
+    static_assert(kHeadsWarps % NH == 0, "whole page slots");
+    static_assert(kHeadsWarps * 32 * kRedFloats * 4 <= kStages * kStageBytes, "merge scratch");
 };
 
-template <int D>
+template <int D, int NH>
 __global__ void __launch_bounds__(kHeadsThreads)
     decode_heads_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                         const DecParams p) {
-    using L = HeadsLayout<D>;
+    using L = HeadsLayout<D, NH>;
     constexpr int STAGES = L::kStages;
+    constexpr int SLOTS = L::kSlots;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -501,6 +511,7 @@ __global__ void __launch_bounds__(kHeadsThreads)
     const int j0 = seg * p.seg_len;  // seg_len is a multiple of the page size
     const int j1 = min(j0 + p.seg_len, len);
     const int npages = j1 > j0 ? (j1 - j0 + kSmallPage - 1) / kSmallPage : 0;
+    const int nstages = (npages + SLOTS - 1) / SLOTS;  // SLOTS pages per stage, the last maybe fewer
 
     if (npages == 0) {  // empty segment: o_s = 0, lse_s = -inf for every query head
         for (int e = threadIdx.x; e < p.Hq * D; e += blockDim.x) {
@@ -522,7 +533,7 @@ __global__ void __launch_bounds__(kHeadsThreads)
     if (threadIdx.x == 0) {
         for (int st = 0; st < STAGES; ++st) {
             mbar_init(full_bar(st), 1);
-            mbar_init(empty_bar(st), kHeadsWarps);  // every consumer warp reads every page
+            mbar_init(empty_bar(st), kHeadsWarps);  // every consumer warp releases every stage
         }
         *abort_flag = 0;
         fence_barrier_init();
@@ -532,31 +543,38 @@ __global__ void __launch_bounds__(kHeadsThreads)
     if (warp == 0) {
         // ================================================= TMA producer
         // The whole warp runs the loop: the lanes fetch the block-table
-        // entries of 32 pages at a time, lane 0 issues the loads.
+        // entries of 32 pages at a time (SLOTS divides 32, so a stage's
+        // pages never straddle two fetches), lane 0 issues the loads.
         if (lane == 0) {
             prefetch_tmap(&tmK);
             prefetch_tmap(&tmV);
         }
         const long long tab0 = (long long)b * p.max_pages + j0 / kSmallPage;
         int page_of_lane = 0;
-        for (int t = 0; t < npages; ++t) {
-            if ((t & 31) == 0) {
-                const int i = t + lane;
+        for (int t = 0; t < nstages; ++t) {
+            const int pg = t * SLOTS;  // first page of the stage
+            if ((pg & 31) == 0) {
+                const int i = pg + lane;
                 page_of_lane = (i < npages && in_bounds(tab0 + i, 1, (long long)p.B * p.max_pages, &g_dec_status))
                                    ? p.table[tab0 + i]
                                    : 0;
             }
-            const int page = __shfl_sync(0xffffffffu, page_of_lane, t & 31);
             const int st = t % STAGES;
             if (!mbar_wait_warp(empty_bar(st), ((t / STAGES) & 1) ^ 1, abort_flag, &g_dec_status, p.wait_limit))
                 break;
-            if (lane == 0) {
-                mbar_arrive_expect_tx(full_bar(st), L::kStageBytes);
-                const uint32_t dst = sbase + st * L::kStageBytes;
+            const int np = min(SLOTS, npages - pg);  // pages in this stage
+            if (lane == 0) mbar_arrive_expect_tx(full_bar(st), (uint32_t)(np * L::kPageBytes));
 #pragma unroll
-                for (int pp = 0; pp < L::kPanels; ++pp) {
-                    tma_load_4d(dst + pp * L::kPanelBytes, &tmK, full_bar(st), 64 * pp, 0, 0, page);
-                    tma_load_4d(dst + (L::kPanels + pp) * L::kPanelBytes, &tmV, full_bar(st), 64 * pp, 0, 0, page);
+            for (int sl = 0; sl < SLOTS; ++sl) {
+                const int page = __shfl_sync(0xffffffffu, page_of_lane, (pg + sl) & 31);
+                if (lane == 0 && sl < np) {
+                    const uint32_t dst = sbase + st * L::kStageBytes + sl * L::kPageBytes;
+#pragma unroll
+                    for (int pp = 0; pp < L::kPanels; ++pp) {
+                        tma_load_4d(dst + pp * L::kPanelBytes, &tmK, full_bar(st), 64 * pp, 0, 0, page);
+                        tma_load_4d(dst + (L::kPanels + pp) * L::kPanelBytes, &tmV, full_bar(st), 64 * pp, 0, 0,
+                                    page);
+                    }
                 }
             }
             __syncwarp();
@@ -565,9 +583,11 @@ __global__ void __launch_bounds__(kHeadsThreads)
     }
 
     // ===================================================== consumers
-    const int w = warp - 1;     // KV head of this warp (Hkv = kHeadsWarps)
-    const int G = p.G;          // its query heads, 1..8: the MMA columns
-    const int hq0 = w * G;
+    const int cw = warp - 1;
+    const int h = cw % NH;      // KV head of this warp
+    const int slot = cw / NH;   // which page of each stage it takes
+    const int G = p.G;          // the head's query heads, 1..8: the MMA columns
+    const int hq0 = h * G;
     const int g8 = lane >> 2;   // fragment row group
     const int t4 = lane & 3;    // fragment column pair
     const int mi = lane >> 3;   // ldmatrix: which 8x8 matrix this lane addresses
@@ -590,88 +610,91 @@ __global__ void __launch_bounds__(kHeadsThreads)
     for (int mb = 0; mb < D / 16; ++mb) acc[mb][0] = acc[mb][1] = acc[mb][2] = acc[mb][3] = 0.f;
     float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.f, l_b = 0.f;  // columns 2 t4 and 2 t4 + 1
     const float sl = p.scale_log2;
-    const int krow = w * kSmallPage + rr + 8 * (mi & 1);   // K row (of the stage) this lane addresses
-    const int vrow = w * kSmallPage + rr + 8 * (mi >> 1);  // V row this lane addresses
+    const int krow = h * kSmallPage + rr + 8 * (mi & 1);   // K row (of the page) this lane addresses
+    const int vrow = h * kSmallPage + rr + 8 * (mi >> 1);  // V row this lane addresses
 
-    for (int t = 0; t < npages; ++t) {
+    for (int t = 0; t < nstages; ++t) {
         const int st = t % STAGES;
         if (!mbar_wait(full_bar(st), (t / STAGES) & 1, abort_flag, &g_dec_status, p.wait_limit)) break;
-        const uint32_t kb = sbase + st * L::kStageBytes;
-        const uint32_t vb = kb + L::kPanels * L::kPanelBytes;
-        const int key0 = j0 + t * kSmallPage;
-        // Keys of the last page past the sequence: their pool slots hold
-        // whatever is there (P is 0 for them, but 0 * NaN is not), so the
-        // warp zeroes its head's V rows there (K needs nothing: masked
-        // scores are replaced, not multiplied).
-        const bool zeroed = key0 + kSmallPage > j1;
-        if (zeroed) {
-            for (int e = lane; e < kSmallPage * (D / 8); e += 32) {
-                const int r = e / (D / 8), ch = e % (D / 8);
-                const int row = w * kSmallPage + r;
-                if (key0 + r >= j1)
-                    st_shared_v4(vb + (ch >> 3) * L::kPanelBytes + row * 128 + (((ch & 7) ^ (row & 7)) << 4),
-                                 0u, 0u, 0u, 0u);
+        const int pi = t * SLOTS + slot;  // this warp's page of the stage (the last stage may lack it)
+        if (pi < npages) {
+            const uint32_t kb = sbase + st * L::kStageBytes + slot * L::kPageBytes;
+            const uint32_t vb = kb + L::kPanels * L::kPanelBytes;
+            const int key0 = j0 + pi * kSmallPage;
+            // Keys of the last page past the sequence: their pool slots hold
+            // whatever is there (P is 0 for them, but 0 * NaN is not), so the
+            // warp zeroes its head's V rows there (K needs nothing: masked
+            // scores are replaced, not multiplied).
+            const bool zeroed = key0 + kSmallPage > j1;
+            if (zeroed) {
+                for (int e = lane; e < kSmallPage * (D / 8); e += 32) {
+                    const int r = e / (D / 8), ch = e % (D / 8);
+                    const int row = h * kSmallPage + r;
+                    if (key0 + r >= j1)
+                        st_shared_v4(vb + (ch >> 3) * L::kPanelBytes + row * 128 + (((ch & 7) ^ (row & 7)) << 4),
+                                     0u, 0u, 0u, 0u);
+                }
+                __syncwarp();
             }
-            __syncwarp();
-        }
 
-        // S^T (16 keys x 8 query columns) = K (16 x D) Q^T (D x 8); even and
-        // odd k-steps accumulate separately to halve the dependent MMA chain.
-        float ce[4] = {0.f, 0.f, 0.f, 0.f}, co[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-            const int ch = 2 * kk + (mi >> 1);
-            const uint32_t addr = kb + (ch >> 3) * L::kPanelBytes + krow * 128 + (((ch & 7) ^ (krow & 7)) << 4);
-            uint32_t a[4];
-            ldsm_x4(addr, a);
-            if (kk & 1)
-                mma_16816(co, a, qb[kk][0], qb[kk][1]);
-            else
-                mma_16816(ce, a, qb[kk][0], qb[kk][1]);
+            // S^T (16 keys x 8 query columns) = K (16 x D) Q^T (D x 8); even and
+            // odd k-steps accumulate separately to halve the dependent MMA chain.
+            float ce[4] = {0.f, 0.f, 0.f, 0.f}, co[4] = {0.f, 0.f, 0.f, 0.f};
+    #pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const int ch = 2 * kk + (mi >> 1);
+                const uint32_t addr = kb + (ch >> 3) * L::kPanelBytes + krow * 128 + (((ch & 7) ^ (krow & 7)) << 4);
+                uint32_t a[4];
+                ldsm_x4(addr, a);
+                if (kk & 1)
+                    mma_16816(co, a, qb[kk][0], qb[kk][1]);
+                else
+                    mma_16816(ce, a, qb[kk][0], qb[kk][1]);
+            }
+            const float c[4] = {ce[0] + co[0], ce[1] + co[1], ce[2] + co[2], ce[3] + co[3]};
+            const int key = key0 + g8;  // keys of this lane: rows g8 and g8 + 8 of the page
+            const bool in0 = key < j1, in1 = key + 8 < j1;
+            const float x0 = in0 ? c[0] * sl : -INFINITY;  // (key,   col 2t4)
+            const float x1 = in0 ? c[1] * sl : -INFINITY;  // (key,   col 2t4+1)
+            const float x2 = in1 ? c[2] * sl : -INFINITY;  // (key+8, col 2t4)
+            const float x3 = in1 ? c[3] * sl : -INFINITY;  // (key+8, col 2t4+1)
+            float mxa = fmaxf(x0, x2), mxb = fmaxf(x1, x3);
+    #pragma unroll
+            for (int off = 4; off < 32; off <<= 1) {
+                mxa = fmaxf(mxa, __shfl_xor_sync(0xffffffffu, mxa, off));
+                mxb = fmaxf(mxb, __shfl_xor_sync(0xffffffffu, mxb, off));
+            }
+            const float mna = fmaxf(m_a, mxa), mnb = fmaxf(m_b, mxb);
+            const float mua = mna == -INFINITY ? 0.f : mna;
+            const float mub = mnb == -INFINITY ? 0.f : mnb;
+            const float aa = ex2(m_a - mua), ab = ex2(m_b - mub);
+            const float p0 = ex2(x0 - mua), p2 = ex2(x2 - mua);
+            const float p1 = ex2(x1 - mub), p3 = ex2(x3 - mub);
+            l_a = fmaf(l_a, aa, p0 + p2);
+            l_b = fmaf(l_b, ab, p1 + p3);
+            m_a = mna;
+            m_b = mnb;
+    #pragma unroll
+            for (int mb = 0; mb < D / 16; ++mb) {
+                acc[mb][0] *= aa;
+                acc[mb][1] *= ab;
+                acc[mb][2] *= aa;
+                acc[mb][3] *= ab;
+            }
+            // P^T as the B operand (keys x query columns), then
+            // O^T (D x 8) += V^T (D x 16 keys) P^T (16 keys x 8)
+            const uint32_t b01 = movmatrix_trans(pack_bf16(p0, p1));
+            const uint32_t b23 = movmatrix_trans(pack_bf16(p2, p3));
+    #pragma unroll
+            for (int mb = 0; mb < D / 16; ++mb) {
+                const int ch = 2 * mb + (mi & 1);
+                const uint32_t addr = vb + (ch >> 3) * L::kPanelBytes + vrow * 128 + (((ch & 7) ^ (vrow & 7)) << 4);
+                uint32_t a[4];
+                ldsm_x4_trans(addr, a);
+                mma_16816(acc[mb], a, b01, b23);
+            }
+            if (zeroed) fence_proxy_async_smem();  // the zeroing stores before the stage's next TMA write
         }
-        const float c[4] = {ce[0] + co[0], ce[1] + co[1], ce[2] + co[2], ce[3] + co[3]};
-        const int key = key0 + g8;  // keys of this lane: rows g8 and g8 + 8 of the page
-        const bool in0 = key < j1, in1 = key + 8 < j1;
-        const float x0 = in0 ? c[0] * sl : -INFINITY;  // (key,   col 2t4)
-        const float x1 = in0 ? c[1] * sl : -INFINITY;  // (key,   col 2t4+1)
-        const float x2 = in1 ? c[2] * sl : -INFINITY;  // (key+8, col 2t4)
-        const float x3 = in1 ? c[3] * sl : -INFINITY;  // (key+8, col 2t4+1)
-        float mxa = fmaxf(x0, x2), mxb = fmaxf(x1, x3);
-#pragma unroll
-        for (int off = 4; off < 32; off <<= 1) {
-            mxa = fmaxf(mxa, __shfl_xor_sync(0xffffffffu, mxa, off));
-            mxb = fmaxf(mxb, __shfl_xor_sync(0xffffffffu, mxb, off));
-        }
-        const float mna = fmaxf(m_a, mxa), mnb = fmaxf(m_b, mxb);
-        const float mua = mna == -INFINITY ? 0.f : mna;
-        const float mub = mnb == -INFINITY ? 0.f : mnb;
-        const float aa = ex2(m_a - mua), ab = ex2(m_b - mub);
-        const float p0 = ex2(x0 - mua), p2 = ex2(x2 - mua);
-        const float p1 = ex2(x1 - mub), p3 = ex2(x3 - mub);
-        l_a = fmaf(l_a, aa, p0 + p2);
-        l_b = fmaf(l_b, ab, p1 + p3);
-        m_a = mna;
-        m_b = mnb;
-#pragma unroll
-        for (int mb = 0; mb < D / 16; ++mb) {
-            acc[mb][0] *= aa;
-            acc[mb][1] *= ab;
-            acc[mb][2] *= aa;
-            acc[mb][3] *= ab;
-        }
-        // P^T as the B operand (keys x query columns), then
-        // O^T (D x 8) += V^T (D x 16 keys) P^T (16 keys x 8)
-        const uint32_t b01 = movmatrix_trans(pack_bf16(p0, p1));
-        const uint32_t b23 = movmatrix_trans(pack_bf16(p2, p3));
-#pragma unroll
-        for (int mb = 0; mb < D / 16; ++mb) {
-            const int ch = 2 * mb + (mi & 1);
-            const uint32_t addr = vb + (ch >> 3) * L::kPanelBytes + vrow * 128 + (((ch & 7) ^ (vrow & 7)) << 4);
-            uint32_t a[4];
-            ldsm_x4_trans(addr, a);
-            mma_16816(acc[mb], a, b01, b23);
-        }
-        if (zeroed) fence_proxy_async_smem();  // the zeroing stores before the stage's next TMA write
         __syncwarp();
         if (lane == 0) mbar_arrive(empty_bar(st));
     }
@@ -684,6 +707,51 @@ __global__ void __launch_bounds__(kHeadsThreads)
     for (int off = 4; off < 32; off <<= 1) {
         l_a += __shfl_xor_sync(0xffffffffu, l_a, off);
         l_b += __shfl_xor_sync(0xffffffffu, l_b, off);
+    }
+    if constexpr (SLOTS > 1) {
+        // The SLOTS warps of a head merge their (m, l, acc) through shared
+        // memory (every page has been consumed, so the stage buffers are
+        // free); the slot-0 warp of each head takes the others' states
+        // lane by lane, fragment position by fragment position.
+        named_bar_sync(1, 32 * kHeadsWarps);
+        float* red = reinterpret_cast<float*>(sgen);
+        {
+            float* mine = red + ((size_t)cw * 32 + lane) * L::kRedFloats;
+#pragma unroll
+            for (int mb = 0; mb < D / 16; ++mb) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) mine[mb * 4 + i] = acc[mb][i];
+            }
+            mine[D / 16 * 4 + 0] = m_a;
+            mine[D / 16 * 4 + 1] = m_b;
+            mine[D / 16 * 4 + 2] = l_a;
+            mine[D / 16 * 4 + 3] = l_b;
+        }
+        named_bar_sync(1, 32 * kHeadsWarps);
+        if (slot != 0) return;
+#pragma unroll
+        for (int sl = 1; sl < SLOTS; ++sl) {
+            const float* o = red + ((size_t)(h + sl * NH) * 32 + lane) * L::kRedFloats;
+            const float om_a = o[D / 16 * 4 + 0], om_b = o[D / 16 * 4 + 1];
+            const float ol_a = o[D / 16 * 4 + 2], ol_b = o[D / 16 * 4 + 3];
+            const float Ma = fmaxf(m_a, om_a), Mb = fmaxf(m_b, om_b);
+            // a warp that saw no key has m = -inf and weight 0
+            const float wa = m_a == -INFINITY ? 0.f : ex2(m_a - Ma);
+            const float xa = om_a == -INFINITY ? 0.f : ex2(om_a - Ma);
+            const float wb = m_b == -INFINITY ? 0.f : ex2(m_b - Mb);
+            const float xb = om_b == -INFINITY ? 0.f : ex2(om_b - Mb);
+            l_a = fmaf(l_a, wa, ol_a * xa);
+            l_b = fmaf(l_b, wb, ol_b * xb);
+#pragma unroll
+            for (int mb = 0; mb < D / 16; ++mb) {
+                acc[mb][0] = fmaf(acc[mb][0], wa, o[mb * 4 + 0] * xa);
+                acc[mb][1] = fmaf(acc[mb][1], wb, o[mb * 4 + 1] * xb);
+                acc[mb][2] = fmaf(acc[mb][2], wa, o[mb * 4 + 2] * xa);
+                acc[mb][3] = fmaf(acc[mb][3], wb, o[mb * 4 + 3] * xb);
+            }
+            m_a = Ma;
+            m_b = Mb;
+        }
     }
     // This head's result for query columns 2 t4 and 2 t4 + 1: O = acc / l
     // (acc[mb][c] holds d = 16 mb + g8, acc[mb][2 + c] d + 8), LSE = m + ln l.
@@ -898,21 +966,30 @@ __global__ void __launch_bounds__(kMergeThreads)
         lse[row] = lsum > 0.f ? M + logf(lsum) : -INFINITY;
 }
 
-// decode_heads_kernel serves pages of 16 keys with 8 KV heads of at most 8
-// query heads each; every other paged cache takes decode_split_kernel.
+// decode_heads_kernel serves pages of 16 keys with 2, 4 or 8 KV heads of at
+// most 8 query heads each; every other paged cache takes decode_split_kernel.
 bool heads_path(int Hq, int Hkv, int page_size, int d) {
-    return page_size == kSmallPage && Hkv == kHeadsWarps && Hq % Hkv == 0 && Hq / Hkv <= 8 &&
-           (d == 64 || d == 128);
+    return page_size == kSmallPage && (Hkv == 8 || Hkv == 4 || Hkv == 2) && Hq % Hkv == 0 &&
+           Hq / Hkv <= 8 && (d == 64 || d == 128);
+}
+
+template <int D, int NH>
+attn_status_t launch_heads_nh(const CUtensorMap& mk, const CUtensorMap& mv, const DecParams& prm,
+                              cudaStream_t stream) {
+    using L = HeadsLayout<D, NH>;
+    if (attn_host::kernel_setup<decode_heads_kernel<D, NH>>(L::kSmemBytes).err != cudaSuccess)
+        return ATTN_ERR_CUDA;
+    dim3 grid(prm.splits, 1, prm.B);
+    decode_heads_kernel<D, NH><<<grid, kHeadsThreads, L::kSmemBytes, stream>>>(mk, mv, prm);
+    return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
 template <int D>
 attn_status_t launch_heads(const CUtensorMap& mk, const CUtensorMap& mv, const DecParams& prm,
                            cudaStream_t stream) {
-    using L = HeadsLayout<D>;
-    if (attn_host::kernel_setup<decode_heads_kernel<D>>(L::kSmemBytes).err != cudaSuccess) return ATTN_ERR_CUDA;
-    dim3 grid(prm.splits, 1, prm.B);
-    decode_heads_kernel<D><<<grid, kHeadsThreads, L::kSmemBytes, stream>>>(mk, mv, prm);
-    return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+    return prm.Hkv == 8   ? launch_heads_nh<D, 8>(mk, mv, prm, stream)
+           : prm.Hkv == 4 ? launch_heads_nh<D, 4>(mk, mv, prm, stream)
+                          : launch_heads_nh<D, 2>(mk, mv, prm, stream);
 }
 
 int group_cols(int G) {

@@ -256,8 +256,8 @@ attn_status_t attn_decode_paged(const void* q, const void* k_pages, const void* 
 
 /*
  * attn_decode_paged_num_splits -- the segment count attn_decode_paged uses
- * with num_splits = 0.  With pages of 16 keys and Hkv = 8 (at most 8 query
- * heads per KV head) one CTA takes every KV head of a segment, and the count
+ * with num_splits = 0.  With pages of 16 keys and Hkv = 2, 4 or 8 (at most 8
+ * query heads per KV head) one CTA takes every KV head of a segment, and the count
  * aims at 27/32 of the SMs in CTAs (segments x sequences: 128 on GB300), at
  * most one segment per 64 keys of max_seq_len.  Otherwise it is the
  * CTA-by-wave time model of attn_decode_num_splits with per-CTA rates that

@@ -5,8 +5,8 @@ slot no sequence owns is NaN (it must not reach the output).  Cases cover
 page sizes 16, 32, 64 and 256, lengths on both sides of page and tile
 boundaries, empty sequences (with one and with several segments), GQA
 ratios 1, 3, 4 and 8, d = 64 and 128, and fixed and automatic segment counts;
-with pages of 16 keys and 8 KV heads, the kernel that takes every KV head of
-a segment in one CTA."""
+with pages of 16 keys and 2, 4 or 8 KV heads, the kernel that takes every KV
+head of a segment in one CTA."""
 import math
 
 import numpy as np
@@ -34,6 +34,11 @@ CASES = [
     (2, 64, 8, 128, 16, [1000, 2048], 1, None),        # 8 per KV head; one segment writes O itself
     (2, 8, 8, 128, 16, [63, 65], 4, 400),              # 1 per KV head; segments past every sequence
     (1, 32, 8, 128, 16, [5000], 0, None),              # the automatic count: one wave of CTAs
+    # ... with 4 and 2 KV heads: 2 or 4 pages per stage, the warps of a head merged
+    (3, 16, 4, 128, 16, [1, 40, 1000], 0, None),
+    (2, 32, 4, 64, 16, [0, 700], 3, None),
+    (2, 16, 2, 128, 16, [2048, 33], 1, None),          # one segment: the merged warp writes O
+    (2, 8, 2, 128, 16, [63, 65], 5, 400),              # stages with fewer pages than slots
 ]
 
 
