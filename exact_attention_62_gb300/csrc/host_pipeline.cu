@@ -5,8 +5,9 @@
 // host -> device on the h2d stream, its forward runs once they have arrived
 // (even chunks on the caller's compute stream, odd ones on a second compute
 // stream), and its outputs go device -> host on the d2h stream once the
-// forward is done; so the copy of chunk c + 1 and the read back of chunk
-// c - 1 proceed while chunk c computes.  Sequences are
+// forward is done and every chunk's inputs are in; so the copy of chunk
+// c + 1 proceeds while chunk c computes, and the read-backs run while the
+// last chunks compute.  Sequences are
 // independent in the forward, so every output element is the one a single
 // attn_fwd call over the whole batch writes, bit for bit.
 //
@@ -31,7 +32,7 @@ namespace {
 
 constexpr int kMaxChunks = 16;
 constexpr int kRowUnit = 256;  // query rows of one work unit of the forward kernel
-constexpr int kEvents = 2 * kMaxChunks + 2;
+constexpr int kEvents = 2 * kMaxChunks + 3;
 
 // Events the pipeline records between its streams: created once per host
 // thread and device, reused by every call (a recorded event may be recorded
@@ -115,8 +116,8 @@ extern "C" attn_status_t attn_fwd_host(const void* q_h, const void* k_h, const v
     const bool by_rows = B == 1 && dtype == ATTN_BF16 && Nk > 0 && (!causal || Nq <= Nk);
     const int row_units = (Nq + kRowUnit - 1) / kRowUnit;
     // Default: 16 row chunks for one sequence (B = 1, N = 16384 causal on
-    // GB300, end to end: 1.93 ms against 2.04 with 8, 2.07 with 20, 2.19 with
-    // 32 and 2.22 with 4), else min(B, 4).
+    // GB300, end to end: 1.84 ms against 1.98 with 8 and 2.29 with 12), else
+    // min(B, 4).
     int n = chunks == 0 ? (by_rows ? 16 : (B < 4 ? B : 4)) : chunks;
     if (n > kMaxChunks) return ATTN_ERR_UNSUPPORTED;
     if (n > (by_rows ? row_units : B)) n = by_rows ? row_units : B;
@@ -130,11 +131,24 @@ extern "C" attn_status_t attn_fwd_host(const void* q_h, const void* k_h, const v
     cudaStream_t down = d2h_stream ? static_cast<cudaStream_t>(d2h_stream) : st;
     // compute stream of chunk c
     auto cstream = [&](int c) { return (c & 1) ? t_side.s : st; };
-    // chunk c's forward starts once its inputs are in (ev_in recorded on up)
+    // chunk c's inputs are in (ev_in, recorded on up after its copies); its
+    // forward waits for that
+    auto inputs_sent = [&](int c) -> bool {
+        return up == cstream(c) || cudaEventRecord(ev[2 * c], up) == cudaSuccess;
+    };
     auto wait_inputs = [&](int c) -> bool {
         cudaStream_t cs = cstream(c);
-        if (up == cs) return true;
-        return cudaEventRecord(ev[2 * c], up) == cudaSuccess && cudaStreamWaitEvent(cs, ev[2 * c], 0) == cudaSuccess;
+        return up == cs || cudaStreamWaitEvent(cs, ev[2 * c], 0) == cudaSuccess;
+    };
+    // The read-backs start once every input copy is done: the two copy
+    // directions share the host link (measured: 0.97 ms in, 0.71 ms out, 1.12
+    // ms both at once), and the forwards wait for the inputs, so the inputs go
+    // first (one 16K-key sequence in 16 row chunks: 1.84 ms end to end, 1.93
+    // with the read-backs interleaved).
+    cudaEvent_t ev_all_in = ev[2 * kMaxChunks + 2];
+    auto hold_outputs = [&]() -> bool {
+        if (down == st || down == up) return true;
+        return cudaEventRecord(ev_all_in, up) == cudaSuccess && cudaStreamWaitEvent(down, ev_all_in, 0) == cudaSuccess;
     };
     // chunk c's read-back starts once its forward is done
     auto release_outputs = [&](int c) -> bool {
@@ -170,9 +184,13 @@ extern "C" attn_status_t attn_fwd_host(const void* q_h, const void* k_h, const v
         const size_t q_row = (size_t)Hq * d * esz;    // bytes of one query row (all heads)
         const size_t kv_row = (size_t)Hkv * d * esz;  // bytes of one key row
         long long k_done = 0;                         // keys already sent
-        for (int c = 0; c < n; ++c) {
-            const int r0 = (int)((long long)row_units * c / n) * kRowUnit;
-            const int r1 = c + 1 == n ? Nq : (int)((long long)row_units * (c + 1) / n) * kRowUnit;
+        auto rows_of = [&](int c, int* r0, int* r1) {
+            *r0 = (int)((long long)row_units * c / n) * kRowUnit;
+            *r1 = c + 1 == n ? Nq : (int)((long long)row_units * (c + 1) / n) * kRowUnit;
+        };
+        for (int c = 0; c < n; ++c) {  // every chunk's inputs
+            int r0, r1;
+            rows_of(c, &r0, &r1);
             const long long k_end = causal ? (long long)r1 + (Nk - Nq) : Nk;
             if (cudaMemcpyAsync(qd + r0 * q_row, qh + r0 * q_row, (size_t)(r1 - r0) * q_row,
                                 cudaMemcpyHostToDevice, up) != cudaSuccess)
@@ -184,6 +202,13 @@ extern "C" attn_status_t attn_fwd_host(const void* q_h, const void* k_h, const v
                     return ATTN_ERR_CUDA;
                 k_done = k_end;
             }
+            if (!inputs_sent(c)) return ATTN_ERR_CUDA;
+        }
+        if (!hold_outputs()) return ATTN_ERR_CUDA;
+        for (int c = 0; c < n; ++c) {  // the forwards and the read-backs
+            int r0, r1;
+            rows_of(c, &r0, &r1);
+            const long long k_end = causal ? (long long)r1 + (Nk - Nq) : Nk;
             if (!wait_inputs(c)) return ATTN_ERR_CUDA;
             const attn_status_t s = attn_host::launch_fwd_tc(qd + r0 * q_row, kd, vd, od + r0 * q_row,
                                                              reinterpret_cast<float*>(ld) + r0, 1, Hq, Hkv,
@@ -200,31 +225,45 @@ extern "C" attn_status_t attn_fwd_host(const void* q_h, const void* k_h, const v
                 return ATTN_ERR_CUDA;
         }
     }
-    for (int c = 0; c < n && !by_rows; ++c) {
-        const int b0 = (int)((long long)B * c / n), b1 = (int)((long long)B * (c + 1) / n);
-        const int nb = b1 - b0;
-        if (cudaMemcpyAsync(qd + b0 * q_seq, qh + b0 * q_seq, nb * q_seq, cudaMemcpyHostToDevice, up) !=
-            cudaSuccess)
-            return ATTN_ERR_CUDA;
-        if (Nk > 0) {
-            if (cudaMemcpyAsync(kd + b0 * kv_seq, kh + b0 * kv_seq, nb * kv_seq, cudaMemcpyHostToDevice, up) !=
+    if (!by_rows) {
+        auto seqs_of = [&](int c, int* b0, int* b1) {
+            *b0 = (int)((long long)B * c / n);
+            *b1 = (int)((long long)B * (c + 1) / n);
+        };
+        for (int c = 0; c < n; ++c) {  // every chunk's inputs
+            int b0, b1;
+            seqs_of(c, &b0, &b1);
+            const int nb = b1 - b0;
+            if (cudaMemcpyAsync(qd + b0 * q_seq, qh + b0 * q_seq, nb * q_seq, cudaMemcpyHostToDevice, up) !=
+                cudaSuccess)
+                return ATTN_ERR_CUDA;
+            if (Nk > 0) {
+                if (cudaMemcpyAsync(kd + b0 * kv_seq, kh + b0 * kv_seq, nb * kv_seq, cudaMemcpyHostToDevice,
+                                    up) != cudaSuccess ||
+                    cudaMemcpyAsync(vd + b0 * kv_seq, vh + b0 * kv_seq, nb * kv_seq, cudaMemcpyHostToDevice,
+                                    up) != cudaSuccess)
+                    return ATTN_ERR_CUDA;
+            }
+            if (!inputs_sent(c)) return ATTN_ERR_CUDA;
+        }
+        if (!hold_outputs()) return ATTN_ERR_CUDA;
+        for (int c = 0; c < n; ++c) {  // the forwards and the read-backs
+            int b0, b1;
+            seqs_of(c, &b0, &b1);
+            const int nb = b1 - b0;
+            if (!wait_inputs(c)) return ATTN_ERR_CUDA;
+            const attn_status_t s = attn_fwd(qd + b0 * q_seq, Nk > 0 ? kd + b0 * kv_seq : nullptr,
+                                             Nk > 0 ? vd + b0 * kv_seq : nullptr, od + b0 * q_seq,
+                                             reinterpret_cast<float*>(ld + b0 * l_seq), nb, Hq, Hkv, Nq, Nk, d,
+                                             causal, scale, dtype, cstream(c));
+            if (s != ATTN_OK) return s;
+            if (!release_outputs(c)) return ATTN_ERR_CUDA;
+            if (cudaMemcpyAsync(oh + b0 * q_seq, od + b0 * q_seq, nb * q_seq, cudaMemcpyDeviceToHost, down) !=
                     cudaSuccess ||
-                cudaMemcpyAsync(vd + b0 * kv_seq, vh + b0 * kv_seq, nb * kv_seq, cudaMemcpyHostToDevice, up) !=
+                cudaMemcpyAsync(lh + b0 * l_seq, ld + b0 * l_seq, nb * l_seq, cudaMemcpyDeviceToHost, down) !=
                     cudaSuccess)
                 return ATTN_ERR_CUDA;
         }
-        if (!wait_inputs(c)) return ATTN_ERR_CUDA;
-        const attn_status_t s = attn_fwd(qd + b0 * q_seq, Nk > 0 ? kd + b0 * kv_seq : nullptr,
-                                         Nk > 0 ? vd + b0 * kv_seq : nullptr, od + b0 * q_seq,
-                                         reinterpret_cast<float*>(ld + b0 * l_seq), nb, Hq, Hkv, Nq, Nk, d,
-                                         causal, scale, dtype, cstream(c));
-        if (s != ATTN_OK) return s;
-        if (!release_outputs(c)) return ATTN_ERR_CUDA;
-        if (cudaMemcpyAsync(oh + b0 * q_seq, od + b0 * q_seq, nb * q_seq, cudaMemcpyDeviceToHost, down) !=
-                cudaSuccess ||
-            cudaMemcpyAsync(lh + b0 * l_seq, ld + b0 * l_seq, nb * l_seq, cudaMemcpyDeviceToHost, down) !=
-                cudaSuccess)
-            return ATTN_ERR_CUDA;
     }
     // the compute stream completes after the last read back
     if (down != st) {

@@ -102,8 +102,9 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o,
  *   stream   the compute stream; h2d_stream and d2h_stream carry the two
  *            copy directions (NULL: the compute stream, i.e. no overlap).
  * Chunk c is copied host -> device on h2d_stream, computed once it has
- * arrived, and copied back on d2h_stream once computed, so chunk c + 1 moves
- * in while chunk c computes.  Even chunks compute on `stream`, odd chunks on
+ * arrived, and copied back on d2h_stream once computed and once every chunk
+ * has been copied in (the two directions share the host link), so chunk
+ * c + 1 moves in while chunk c computes.  Even chunks compute on `stream`, odd chunks on
  * a second compute stream of the library's, so that one chunk's forward can
  * start on the SMs the previous one's last wave leaves idle.  The other
  * streams first wait for the work already queued on `stream`, and `stream`
