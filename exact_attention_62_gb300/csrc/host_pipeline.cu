@@ -140,16 +140,6 @@ extern "C" attn_status_t attn_fwd_host(const void* q_h, const void* k_h, const v
         cudaStream_t cs = cstream(c);
         return up == cs || cudaStreamWaitEvent(cs, ev[2 * c], 0) == cudaSuccess;
     };
-    // The read-backs start once every input copy is done: the two copy
-    // directions share the host link (measured: 0.97 ms in, 0.71 ms out, 1.12
-    // ms both at once), and the forwards wait for the inputs, so the inputs go
-    // first (one 16K-key sequence in 16 row chunks: 1.84 ms end to end, 1.93
-    // with the read-backs interleaved).
-    cudaEvent_t ev_all_in = ev[2 * kMaxChunks + 2];
-    auto hold_outputs = [&]() -> bool {
-        if (down == st || down == up) return true;
-        return cudaEventRecord(ev_all_in, up) == cudaSuccess && cudaStreamWaitEvent(down, ev_all_in, 0) == cudaSuccess;
-    };
     // chunk c's read-back starts once its forward is done
     auto release_outputs = [&](int c) -> bool {
         cudaStream_t cs = cstream(c);
@@ -172,6 +162,25 @@ extern "C" attn_status_t attn_fwd_host(const void* q_h, const void* k_h, const v
     char* vd = static_cast<char*>(v_d);
     char* od = static_cast<char*>(o_d);
     char* ld = reinterpret_cast<char*>(lse_d);
+
+    // The read-backs start once every input copy is done: the two copy
+    // directions share the host link (measured: 0.97 ms in, 0.71 ms out, 1.12
+    // ms both at once), and the forwards wait for the inputs, so the inputs go
+    // first (one 16K-key sequence in 16 row chunks: 1.84 ms end to end, 1.93
+    // with the read-backs interleaved).
+    // That pays only when the forwards outlast the read-backs: holding them
+    // behind the inputs of a short computation (B = 4 x 4K keys: 0.2 ms of
+    // forward for 134 MB of outputs) would serialise the two copies.  So
+    // the read-backs are held when the forward's estimated time (at 1.3
+    // PFLOP/s) exceeds that of the read-backs (at 190 GB/s).
+    cudaEvent_t ev_all_in = ev[2 * kMaxChunks + 2];
+    const double flops = 4.0 * B * Hq * (double)Nq * Nk * d * (causal ? 0.5 : 1.0);
+    const double out_bytes = (double)B * (q_seq + l_seq);
+    const bool hold = flops / 1.3e15 > out_bytes / 1.9e11;
+    auto hold_outputs = [&]() -> bool {
+        if (!hold || down == st || down == up) return true;
+        return cudaEventRecord(ev_all_in, up) == cudaSuccess && cudaStreamWaitEvent(down, ev_all_in, 0) == cudaSuccess;
+    };
 
     // the side streams start after the work already queued on the compute stream
     cudaEvent_t ev_start = ev[2 * kMaxChunks], ev_done = ev[2 * kMaxChunks + 1];
