@@ -1176,25 +1176,29 @@ bool paged_splits_fit(int max_seq_len, int page_size, int splits) {
 }
 
 int decode_paged_auto_splits(int B, int Hq, int Hkv, int max_seq_len, int d, int page_size) {
-    // Pages of 64 or more keys stream like the contiguous cache.  Smaller
-    // pages split every tile into 64 / page_size boxes at random places, and
-    // one CTA sustains less (rates fitted to 64K and 16K keys, d = 128: ~33
-    // GB/s with 16-key pages, ~52 with 32-key pages), so more CTAs are needed
-    // to keep HBM busy; but a second
-    // wave of such CTAs costs more than it gains (B = 16 x 8K keys: one
-    // segment per sequence beats eight), so they are kept to one wave.
+    int S;
     if (heads_path(Hq, Hkv, page_size, d)) {
         // One CTA per (segment, sequence) for all KV heads, one CTA per SM,
         // each segment whole 64-key tiles.
         const int sms = device_sm_count();
         if (sms <= 0) return -1;
         const int max_s = std::max(1, (max_seq_len + kTileKeys - 1) / kTileKeys);
-        return std::max(1, std::min(max_s, heads_target_ctas(sms) / std::max(1, B)));
+        S = std::max(1, std::min(max_s, heads_target_ctas(sms) / std::max(1, B)));
+    } else {
+        // Pages of 64 or more keys stream like the contiguous cache.  Smaller
+        // pages split every tile into 64 / page_size boxes at random places,
+        // and one CTA sustains less (rates fitted to 64K and 16K keys, d =
+        // 128: ~33 GB/s with 16-key pages, ~52 with 32-key pages), so more
+        // CTAs are needed to keep HBM busy; but a second wave of such CTAs
+        // costs more than it gains (B = 16 x 8K keys: one segment per
+        // sequence beats eight), so they are kept to one wave.
+        const bool small = page_size < 64;
+        const double cta_bw = !small ? 6.0e10 : page_size >= 32 ? 5.2e10 : 3.3e10;
+        S = auto_splits_model(B, Hq, Hkv, max_seq_len, d, SplitModel{cta_bw, 6.5e12, 1.5e-6, 3.0e-6}, small);
+        if (S < 1) return S;
     }
-    const bool small = page_size < 64;
-    const double cta_bw = !small ? 6.0e10 : page_size >= 32 ? 5.2e10 : 3.3e10;
-    int S = auto_splits_model(B, Hq, Hkv, max_seq_len, d, SplitModel{cta_bw, 6.5e12, 1.5e-6, 3.0e-6}, small);
-    if (S < 1) return S;
+    // every count attn_decode_paged accepts keeps one segment's pages within
+    // the block-table staging area
     while (!paged_splits_fit(max_seq_len, page_size, S) && S < max_seq_len) ++S;
     return S;
 }

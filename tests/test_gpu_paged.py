@@ -102,3 +102,16 @@ def test_paged_equals_contiguous_decode(attn):
         else:
             assert (o1.float() - o2.float()).abs().max().item() <= 1e-2
             assert (l1 - l2).abs().max().item() <= 1e-4
+
+
+@pytest.mark.parametrize("Hkv,ps", [(8, 16), (4, 16), (2, 64)])
+def test_auto_count_keeps_segments_within_the_table(attn, Hkv, ps):
+    """For very long sequences the automatic segment count is raised until
+    one segment's pages fit the 4096-entry block-table staging area, which
+    attn_decode_paged requires of every count (both kernels)."""
+    for max_len in (1 << 20, 1 << 26, (1 << 27) + 5):
+        S = attn.attn_decode_paged_num_splits(1, 4 * Hkv, Hkv, 128, ps, max_len)
+        assert S >= 1
+        seg = -(-max_len // S)
+        seg = -(-seg // 64) * 64
+        assert seg // ps + 2 <= 4096, (Hkv, ps, max_len, S)
