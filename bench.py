@@ -86,8 +86,8 @@ NOMINAL_HBM_GBS = 8000.0  # the ~8 TB/s HBM3e figure the decode target is quoted
 NCU_TRAFFIC = {
     "long_sequence": {"bytes_per_launch": 350.80e6 + 101.38e6, "src": "fwd_tc.cu",
                       "src_hash": "f289683a689bd204"},
-    "decode_b16_8k": {"bytes_per_launch": 537.03e6 + 3.09e6, "src": "decode.cu",
-                      "src_hash": "96f16f3686915c9a"},
+    "decode_b16_8k": {"bytes_per_launch": 537.03e6 + 2.67e6, "src": "decode.cu",
+                      "src_hash": "38855097fe3c6171"},
 }
 
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}

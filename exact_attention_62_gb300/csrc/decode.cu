@@ -890,12 +890,12 @@ __global__ void __launch_bounds__(kMergeThreads)
 }
 
 // The same merge in one pass for few segments (at most NSEG per thread:
-// kShortSeg, or kShortSegWide for up to 128 segments at d = 128): every thread issues the loads of its segments' LSE and partial
+// kShortSeg, or kShortSegWide for up to 152 segments at d = 128): every thread issues the loads of its segments' LSE and partial
 // outputs at once, so the merge costs one round trip to L2 instead of two;
 // o = sum_s e^{lse_s - M} o_s / sum_s e^{lse_s - M} and lse = M + ln of that
 // sum (M = max_s lse_s), the same value as merge_lse_kernel up to rounding.
 constexpr int kShortSeg = 4;   // segments per thread of the one-pass merge (P <= 32 at d = 128)
-constexpr int kShortSegWide = 16;  // the same for P <= 128 at d = 128 (many-segment paged decodes)
+constexpr int kShortSegWide = 19;  // the same for P <= 152 at d = 128 (many-segment paged decodes)
 
 template <bool OUT_BF16, int NSEG>
 __global__ void __launch_bounds__(kMergeThreads)

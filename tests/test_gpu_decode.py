@@ -98,9 +98,12 @@ def test_decode_empty_cache(attn):
                                           (2500, 3, 128, torch.float32), (1025, 4, 64, torch.bfloat16),
                                           # 4-column groups that do not divide the thread count
                                           (9, 6, 12, torch.float32), (33, 5, 20, torch.bfloat16),
-                                          # the one-pass merge with 16 segments per thread
+                                          # the one-pass merge with 19 segments per thread, up to its
+                                          # limit (152 parts at d = 128, 304 at d = 64), and one past it
                                           (33, 40, 128, torch.bfloat16), (128, 7, 128, torch.float32),
-                                          (200, 9, 64, torch.float32), (129, 3, 128, torch.bfloat16)])
+                                          (200, 9, 64, torch.float32), (129, 3, 128, torch.bfloat16),
+                                          (152, 5, 128, torch.bfloat16), (153, 5, 128, torch.float32),
+                                          (304, 3, 64, torch.bfloat16), (305, 3, 64, torch.float32)])
 def test_merge_lse(attn, oracle_mod, P, rows, d, out):
     """attn_merge_lse against the oracle's log-sum-exp merge, with some empty
     parts and some rows whose parts are all empty."""
