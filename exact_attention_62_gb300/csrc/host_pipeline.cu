@@ -34,58 +34,47 @@ constexpr int kMaxChunks = 16;
 constexpr int kRowUnit = 256;  // query rows of one work unit of the forward kernel
 constexpr int kEvents = 2 * kMaxChunks + 3;
 
-// Events the pipeline records between its streams: created once per host
-// thread and device, reused by every call (a recorded event may be recorded
-// again once the waits on it have been enqueued).
+// Events the pipeline records between its streams: created on first use per
+// host thread and device, then reused by every call (a recorded event may be
+// recorded again once the waits on it have been enqueued).
 struct EventPool {
     cudaEvent_t ev[kEvents];
-    int device = -1;
     bool ready = false;
-    void release() {
-        if (!ready) return;
-        for (int i = 0; i < kEvents; ++i) cudaEventDestroy(ev[i]);
-        ready = false;
-    }
-    bool get(int dev) {
-        if (ready && device == dev) return true;
-        release();
+    bool get() {
+        if (ready) return true;
         for (int i = 0; i < kEvents; ++i) {
             if (cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming) != cudaSuccess) {
                 for (int k = 0; k < i; ++k) cudaEventDestroy(ev[k]);
                 return false;
             }
         }
-        device = dev;
         ready = true;
         return true;
     }
     // (no destructor: the events live until the process ends, so nothing
     // calls into the CUDA runtime during its own teardown)
 };
-thread_local EventPool t_events;
 
 // The second compute stream: consecutive chunks' forwards run on the caller's
 // stream and on this one by turns, so the next chunk's CTAs take the SMs
 // that the current chunk's last wave of work units leaves idle (eight row
 // chunks of one 16K-key sequence: 1.67 ms back to back on one stream, 1.56
-// on two; sixteen: 1.82 and 1.52).  Created once per host thread and
+// on two; sixteen: 1.82 and 1.52).  Created on first use per host thread and
 // device, like the events; its work is ordered by events only.
 struct SideStream {
     cudaStream_t s = nullptr;
-    int device = -1;
-    bool get(int dev) {
-        if (s != nullptr && device == dev) return true;
-        if (s != nullptr) cudaStreamDestroy(s);
-        s = nullptr;
-        if (cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking) != cudaSuccess) {
-            s = nullptr;
-            return false;
-        }
-        device = dev;
-        return true;
+    bool get() {
+        return s != nullptr || cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking) == cudaSuccess ||
+               (s = nullptr, false);
     }
 };
-thread_local SideStream t_side;
+
+// Per device, so that a thread that drives several GPUs keeps one set each.
+struct DeviceResources {
+    EventPool events;
+    SideStream side;
+};
+thread_local DeviceResources t_res[attn_host::kMaxDevices];
 
 bool misaligned16(const void* p) { return (reinterpret_cast<unsigned long long>(p) & 15ull) != 0; }
 
@@ -123,14 +112,18 @@ extern "C" attn_status_t attn_fwd_host(const void* q_h, const void* k_h, const v
     if (n > (by_rows ? row_units : B)) n = by_rows ? row_units : B;
 
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || !t_events.get(dev)) return ATTN_ERR_CUDA;
-    if (n > 1 && !t_side.get(dev)) return ATTN_ERR_CUDA;
-    cudaEvent_t* ev = t_events.ev;
+    if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
+    if (dev < 0 || dev >= attn_host::kMaxDevices) return ATTN_ERR_UNSUPPORTED;
+    DeviceResources& res = t_res[dev];
+    if (!res.events.get()) return ATTN_ERR_CUDA;
+    if (n > 1 && !res.side.get()) return ATTN_ERR_CUDA;
+    cudaEvent_t* ev = res.events.ev;
+    cudaStream_t side = n > 1 ? res.side.s : nullptr;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaStream_t up = h2d_stream ? static_cast<cudaStream_t>(h2d_stream) : st;
     cudaStream_t down = d2h_stream ? static_cast<cudaStream_t>(d2h_stream) : st;
     // compute stream of chunk c
-    auto cstream = [&](int c) { return (c & 1) ? t_side.s : st; };
+    auto cstream = [&](int c) { return (c & 1) ? side : st; };
     // chunk c's inputs are in (ev_in, recorded on up after its copies); its
     // forward waits for that
     auto inputs_sent = [&](int c) -> bool {
@@ -187,7 +180,7 @@ extern "C" attn_status_t attn_fwd_host(const void* q_h, const void* k_h, const v
     if (cudaEventRecord(ev_start, st) != cudaSuccess) return ATTN_ERR_CUDA;
     if (up != st && cudaStreamWaitEvent(up, ev_start, 0) != cudaSuccess) return ATTN_ERR_CUDA;
     if (down != st && cudaStreamWaitEvent(down, ev_start, 0) != cudaSuccess) return ATTN_ERR_CUDA;
-    if (n > 1 && cudaStreamWaitEvent(t_side.s, ev_start, 0) != cudaSuccess) return ATTN_ERR_CUDA;
+    if (n > 1 && cudaStreamWaitEvent(side, ev_start, 0) != cudaSuccess) return ATTN_ERR_CUDA;
 
     if (by_rows) {
         const size_t q_row = (size_t)Hq * d * esz;    // bytes of one query row (all heads)

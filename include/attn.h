@@ -113,7 +113,8 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o,
  * whole batch.  Errors as attn_fwd, checked before anything is queued (a
  * CUDA failure later returns ATTN_ERR_CUDA with part of the work queued).
  * The library keeps a few CUDA events and one non-blocking stream per host
- * thread and device for this call.
+ * thread and device for this call (devices 0..63; a higher device number
+ * returns ATTN_ERR_UNSUPPORTED).
  */
 attn_status_t attn_fwd_host(const void* q_h, const void* k_h, const void* v_h,
                             void* o_h, float* lse_h, void* q_d, void* k_d,
