@@ -1,4 +1,6 @@
-"""Every entry point can be captured into a CUDA graph and replayed.
+"""Every entry point can be captured into a CUDA graph and replayed
+(attn_fwd_host included: its copy streams and second compute stream join
+the capture through its events).
 
 A launch path that synchronises, allocates or reads back from the device
 would break stream capture; one that baked input values into the launch
@@ -204,3 +206,35 @@ def test_fp8_pv_graph(attn):
     torch.cuda.synchronize()
     assert torch.equal(vt8, evt) and torch.equal(vs, evs)
     assert torch.equal(o, eo) and torch.equal(lse, el)
+
+
+@pytest.mark.parametrize("B,Nq,Nk,causal,chunks", [(1, 1000, 1000, True, 4),   # chunks of query rows
+                                                   (3, 300, 500, False, 3)])    # chunks of sequences
+def test_host_pipeline_graph(attn, B, Nq, Nk, causal, chunks):
+    """attn_fwd_host in a graph: its copies, events and second compute stream
+    join the capture; a replay reads the page-locked inputs' new contents and
+    writes the results into the same host outputs."""
+    Hq, Hkv, d = 4, 2, 128
+    scale = 1.0 / math.sqrt(d)
+    q, k, v = make_qkv(B, Hq, Hkv, Nq, Nk, d, 41)
+    qh, kh, vh = q.pin_memory(), k.pin_memory(), v.pin_memory()
+    oh = torch.empty(q.shape, dtype=q.dtype).pin_memory()
+    lh = torch.empty((B, Hq, Nq), dtype=torch.float32).pin_memory()
+    bufs = (torch.empty(q.shape, dtype=q.dtype, device=DEV), torch.empty(k.shape, dtype=k.dtype, device=DEV),
+            torch.empty(v.shape, dtype=v.dtype, device=DEV), torch.empty(q.shape, dtype=q.dtype, device=DEV),
+            torch.empty((B, Hq, Nq), dtype=torch.float32, device=DEV))
+    up, down = torch.cuda.Stream(), torch.cuda.Stream()
+    g = _capture(lambda: attn.attn_fwd_host(qh, kh, vh, causal, scale, o=oh, lse=lh, device_buffers=bufs,
+                                            chunks=chunks, h2d_stream=up, d2h_stream=down))
+    q2, k2, v2 = make_qkv(B, Hq, Hkv, Nq, Nk, d, 42)
+    qh.copy_(q2)
+    kh.copy_(k2)
+    vh.copy_(v2)
+    oh.zero_()
+    lh.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert attn.attn_check_device_status() == 0
+    eo, el = attn.attn_fwd(q2.to(DEV), k2.to(DEV), v2.to(DEV), causal, scale)
+    torch.cuda.synchronize()
+    assert torch.equal(oh, eo.cpu()) and torch.equal(lh, el.cpu())
