@@ -7,9 +7,11 @@ which one mistake at a time is planted -- a dropped scale, the wrong causal
 alignment or an off-by-one mask, the wrong GQA head, a missing
 normalisation, the log-sum-exp without its max or in base 2, V read one key
 off, the score matrix transposed, masked scores filled with 0 instead of
--inf -- and, for the log-sum-exp merge (section 3.2 in lse form), merges
-with the max in place of the log-sum-exp, unweighted or unnormalised sums,
-or a part left out.  Every planted mistake must fail at least one pin, and
+-inf -- for the log-sum-exp merge (section 3.2 in lse form), merges with
+the max in place of the log-sum-exp, unweighted or unnormalised sums, or a
+part left out -- and for decode over a block table (section 9), a slot past
+the length read, an empty sequence attended, the pages taken in reverse
+order or positions laid out slot-major.  Every planted mistake must fail at least one pin, and
 the same restatement without a mistake must pass them all, so the pins are
 neither vacuous nor too strict for a correct oracle."""
 import math
@@ -35,6 +37,11 @@ FWD_PINS = [
 MERGE_PINS = [
     pins.test_merge_lse_closed_forms,
     pins.test_decode_splits_merge_to_direct,
+]
+PAGED_PINS = [
+    pins.test_paged_decode_zero_query_is_mean_of_named_rows,
+    pins.test_paged_decode_dominant_key_selects_its_row,
+    pins.test_paged_decode_ignores_slots_past_the_length,
 ]
 
 
@@ -146,6 +153,42 @@ def _merge(o_parts, lse_parts, slip=None):
     return o, lse
 
 
+def _paged(oracle_mod, q, kp, vp, table, lens, scale, slip=None):
+    """Decode over a block table (Lecture 11, section 9) as the plain
+    gather-then-attend, with an optional planted mistake: position j of
+    sequence b is slot j % page_size of page table[b, j // page_size]."""
+    q = np.asarray(q, np.float32)
+    kp, vp = np.asarray(kp, np.float32), np.asarray(vp, np.float32)
+    B, _, Hq, d = q.shape
+    ps, Hkv = kp.shape[1], kp.shape[2]
+    o = np.zeros((B, 1, Hq, d))
+    lse = np.full((B, Hq), -np.inf)
+    for b in range(B):
+        L = int(lens[b])
+        if slip == "one_past_the_length":  # (while the table has a slot for it)
+            L = min(L + 1, table.shape[1] * ps)
+        if L <= 0 and slip != "empty_attends":
+            continue
+        npg = (L + ps - 1) // ps
+        pages = list(table[b, :npg])
+        if slip == "pages_reversed":
+            pages = pages[::-1]
+        if slip == "slot_major":  # position j -> page j % npg, slot j // npg
+            pos = [(pages[j % npg], j // npg) for j in range(L)]
+        else:
+            pos = [(pages[j // ps], j % ps) for j in range(L)]
+        kb = np.array([kp[pg, r] for pg, r in pos], np.float32).reshape(1, L, Hkv, d)
+        vb = np.array([vp[pg, r] for pg, r in pos], np.float32).reshape(1, L, Hkv, d)
+        if L == 0:  # the slip: attend over nothing (0/0)
+            o[b] = np.nan
+            lse[b] = np.nan
+            continue
+        ob, lb = oracle_mod.attn_fwd(q[b:b + 1], kb, vb, False, scale)
+        o[b] = ob[0]
+        lse[b] = lb[0, :, 0]
+    return o, lse
+
+
 def _stand_in(oracle_mod, **overrides):
     """The oracle module with some functions replaced."""
     ns = {n: getattr(oracle_mod, n) for n in dir(oracle_mod) if not n.startswith("_")}
@@ -156,6 +199,7 @@ def _stand_in(oracle_mod, **overrides):
 FWD_SLIPS = ["scale", "top_left", "off_by_one", "gqa", "no_norm", "lse_no_max", "lse_log2", "v_shift",
              "transpose", "fill_zero"]
 MERGE_SLIPS = ["max_for_lse", "unweighted", "unnormalised", "drop_last"]
+PAGED_SLIPS = ["one_past_the_length", "empty_attends", "pages_reversed", "slot_major"]
 
 
 def test_restatement_without_a_slip_passes_every_pin(oracle_mod):
@@ -163,6 +207,8 @@ def test_restatement_without_a_slip_passes_every_pin(oracle_mod):
     assert _failed_pins(fwd, FWD_PINS) == []
     mrg = _stand_in(oracle_mod, merge_lse=lambda o, l: _merge(o, l))
     assert _failed_pins(mrg, MERGE_PINS) == []
+    pgd = _stand_in(oracle_mod, decode_paged=lambda *a: _paged(oracle_mod, *a))
+    assert _failed_pins(pgd, PAGED_PINS) == []
 
 
 @pytest.mark.parametrize("slip", FWD_SLIPS)
@@ -175,3 +221,9 @@ def test_planted_forward_slip_fails_a_pin(oracle_mod, slip):
 def test_planted_merge_slip_fails_a_pin(oracle_mod, slip):
     mrg = _stand_in(oracle_mod, merge_lse=lambda o, l: _merge(o, l, slip))
     assert _failed_pins(mrg, MERGE_PINS), "no pin rejects the merge with slip %r" % slip
+
+
+@pytest.mark.parametrize("slip", PAGED_SLIPS)
+def test_planted_paged_slip_fails_a_pin(oracle_mod, slip):
+    pgd = _stand_in(oracle_mod, decode_paged=lambda *a: _paged(oracle_mod, *a, slip=slip))
+    assert _failed_pins(pgd, PAGED_PINS), "no pin rejects the paged decode with slip %r" % slip
