@@ -11,7 +11,9 @@ off, the score matrix transposed, masked scores filled with 0 instead of
 the max in place of the log-sum-exp, unweighted or unnormalised sums, or a
 part left out -- and for decode over a block table (section 9), a slot past
 the length read, an empty sequence attended, the pages taken in reverse
-order or positions laid out slot-major.  Every planted mistake must fail at least one pin, and
+order or positions laid out slot-major; for the backward (section 5.1), dS
+without the D term, dV from dS, dQ without the scale, dK from P, or a KV
+head that gets the gradient of only one of its query heads.  Every planted mistake must fail at least one pin, and
 the same restatement without a mistake must pass them all, so the pins are
 neither vacuous nor too strict for a correct oracle."""
 import math
@@ -42,6 +44,10 @@ PAGED_PINS = [
     pins.test_paged_decode_zero_query_is_mean_of_named_rows,
     pins.test_paged_decode_dominant_key_selects_its_row,
     pins.test_paged_decode_ignores_slots_past_the_length,
+]
+BWD_PINS = [
+    pins.test_backward_matches_finite_differences,
+    pins.test_backward_gqa_sums_over_the_group,
 ]
 
 
@@ -189,6 +195,40 @@ def _paged(oracle_mod, q, kp, vp, table, lens, scale, slip=None):
     return o, lse
 
 
+def _bwd(q, k, v, do, causal, scale, slip=None):
+    """The gradients of Lecture 11, section 5.1 in float64 with an optional
+    planted mistake: P = softmax(scale S), dV = P^T dO, dP = dO V^T,
+    D = rowsum(dO o O), dS = P o (dP - D), dQ = scale dS K, dK = scale dS^T Q,
+    each KV head summing over its query heads."""
+    q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
+    B, Nq, Hq, d = q.shape
+    Nk, Hkv = k.shape[1], k.shape[2]
+    G = Hq // Hkv
+    dq, dk, dv = np.zeros(q.shape), np.zeros(k.shape), np.zeros(v.shape)
+    allowed = (np.arange(Nk)[None, :] <= np.arange(Nq)[:, None] + (Nk - Nq)) if causal else \
+        np.ones((Nq, Nk), bool)
+    for b in range(B):
+        for h in range(Hq):
+            g = h // G
+            if slip == "one_head_per_group" and h % G != 0:
+                continue
+            s = np.where(allowed, scale * (q[b, :, h] @ k[b, :, g].T), -np.inf)
+            m = s.max(axis=1, keepdims=True)
+            m = np.where(np.isfinite(m), m, 0.0)
+            e = np.exp(s - m)
+            ell = e.sum(axis=1, keepdims=True)
+            P = np.where(ell > 0, e / np.where(ell > 0, ell, 1.0), 0.0)
+            O = P @ v[b, :, g]
+            dO = do[b, :, h]
+            dP = dO @ v[b, :, g].T
+            Dv = (dO * O).sum(axis=1, keepdims=True)
+            dS = P * dP if slip == "no_D" else P * (dP - Dv)
+            dv[b, :, g] += (dS if slip == "dv_from_ds" else P).T @ dO
+            dq[b, :, h] = (1.0 if slip == "dq_unscaled" else scale) * dS @ k[b, :, g]
+            dk[b, :, g] += scale * (P if slip == "dk_from_p" else dS).T @ q[b, :, h]
+    return dq, dk, dv
+
+
 def _stand_in(oracle_mod, **overrides):
     """The oracle module with some functions replaced."""
     ns = {n: getattr(oracle_mod, n) for n in dir(oracle_mod) if not n.startswith("_")}
@@ -200,6 +240,7 @@ FWD_SLIPS = ["scale", "top_left", "off_by_one", "gqa", "no_norm", "lse_no_max", 
              "transpose", "fill_zero"]
 MERGE_SLIPS = ["max_for_lse", "unweighted", "unnormalised", "drop_last"]
 PAGED_SLIPS = ["one_past_the_length", "empty_attends", "pages_reversed", "slot_major"]
+BWD_SLIPS = ["no_D", "dv_from_ds", "dq_unscaled", "dk_from_p", "one_head_per_group"]
 
 
 def test_restatement_without_a_slip_passes_every_pin(oracle_mod):
@@ -209,6 +250,8 @@ def test_restatement_without_a_slip_passes_every_pin(oracle_mod):
     assert _failed_pins(mrg, MERGE_PINS) == []
     pgd = _stand_in(oracle_mod, decode_paged=lambda *a: _paged(oracle_mod, *a))
     assert _failed_pins(pgd, PAGED_PINS) == []
+    bwd = _stand_in(oracle_mod, attn_bwd=lambda *a: _bwd(*a))
+    assert _failed_pins(bwd, BWD_PINS) == []
 
 
 @pytest.mark.parametrize("slip", FWD_SLIPS)
@@ -227,3 +270,9 @@ def test_planted_merge_slip_fails_a_pin(oracle_mod, slip):
 def test_planted_paged_slip_fails_a_pin(oracle_mod, slip):
     pgd = _stand_in(oracle_mod, decode_paged=lambda *a: _paged(oracle_mod, *a, slip=slip))
     assert _failed_pins(pgd, PAGED_PINS), "no pin rejects the paged decode with slip %r" % slip
+
+
+@pytest.mark.parametrize("slip", BWD_SLIPS)
+def test_planted_backward_slip_fails_a_pin(oracle_mod, slip):
+    bwd = _stand_in(oracle_mod, attn_bwd=lambda *a: _bwd(*a, slip=slip))
+    assert _failed_pins(bwd, BWD_PINS), "no pin rejects the backward with slip %r" % slip
